@@ -1,0 +1,309 @@
+"""IceCache CPU oracle (test infrastructure only).
+
+The plain C restatement of the method lives in ``oracle.c``; this module
+compiles it with gcc into ``liboracle.so`` next to it and wraps each step for
+numpy arrays.  Every floating-point step runs in IEEE double on inputs that
+are exact in double (bf16 or fp32 values widened).
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline /
+reference leg of ``bench.py`` may import this package.  The product library
+(``semantic_paged_kv_gb300``) never imports it and shares no code with it.
+
+Steps and their sources (page title, section):
+  lift, promote, assign, pack, insert -- IceCache popular-science article
+      (aitangshan.cn/news/751385) section 三; papernotes.org "IceCache:
+      Memory-Efficient KV-cache Management for Long-Sequence LLMs",
+      关键设计 2.
+  select + GQA union -- papernotes 关键设计 3; article section 六.
+  gather -- papernotes 关键设计 4; article section 四.
+  attention -- papernotes 关键设计 1 (the a_ij formula).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+OK, ERR_ARG, ERR_NOMEM, ERR_CAPACITY = 0, 1, 3, 4
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (plain gcc, no target-specific flags)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        build()
+        lib = ctypes.CDLL(_LIB)
+        P = ctypes.c_void_p
+        i32, i64, u64, u32, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_double
+        lib.orc_splitmix64_mix.argtypes = [u64]
+        lib.orc_splitmix64_mix.restype = u64
+        lib.orc_splitmix64_nth.argtypes = [u64, u64]
+        lib.orc_splitmix64_nth.restype = u64
+        lib.orc_promote_draw.argtypes = [u64, i32, i32, i32, i64, i32]
+        lib.orc_promote_draw.restype = u32
+        lib.orc_lift.argtypes = [P, i64, i32, P, P, P]
+        lib.orc_promote.argtypes = [u64, i32, i32, i32, i64, u64, P, P]
+        lib.orc_assign.argtypes = [P, P, i64, i32, P, i32, P]
+        lib.orc_pack.argtypes = [P, i64, i32, i32, i32, P, P, P, P, P, P]
+        lib.orc_scatter.argtypes = [P, P, i64, i32, i32, i32, P, P, P]
+        lib.orc_select.argtypes = [P, i32, i32, P, i32, P, i32, i32, P, P, P]
+        lib.orc_gather.argtypes = [P, P, P, i32, i32, i32, P, i32, P, P, P]
+        lib.orc_attention.argtypes = [P, i32, i32, P, P, P, i32, i32, f64, P]
+        lib.orc_insert.argtypes = [u64, i32, i32, i32, u64, i32, i32, f64, P, P, i64,
+                                   i32, P, P, P, P,
+                                   i32, P, P, P, P, P, P,
+                                   i64, P, P, P]
+        for name in ("orc_lift", "orc_promote", "orc_assign", "orc_pack", "orc_scatter",
+                     "orc_select", "orc_gather", "orc_attention", "orc_insert"):
+            getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise RuntimeError(f"oracle {what} failed with code {rc}")
+
+
+# ---------------------------------------------------------------- hash ----
+def splitmix64_mix(z: int) -> int:
+    return int(_load().orc_splitmix64_mix(z & 0xFFFFFFFFFFFFFFFF))
+
+
+def splitmix64_nth(s0: int, n: int) -> int:
+    return int(_load().orc_splitmix64_nth(s0 & 0xFFFFFFFFFFFFFFFF, n & 0xFFFFFFFFFFFFFFFF))
+
+
+def promote_draw(seed: int, layer: int, seq: int, head: int, token: int, level: int = 1) -> int:
+    return int(_load().orc_promote_draw(seed, layer, seq, head, token, level))
+
+
+def promote_threshold(p: float) -> int:
+    """floor(p * 2^32) for p in [0, 1] (2^32 means always promoted)."""
+    return int(np.floor(p * 4294967296.0))
+
+
+# ---------------------------------------------------------- build steps ----
+def lift(K) -> tuple[np.ndarray, float, np.ndarray]:
+    K = _f64(K)
+    N, d = K.shape
+    n = np.empty(N, np.float64)
+    e = np.empty(N, np.float64)
+    M2 = ctypes.c_double(0.0)
+    _check(_load().orc_lift(_p(K), N, d, _p(n), ctypes.byref(M2), _p(e)), "lift")
+    return n, float(M2.value), e
+
+
+def promote(seed: int, layer: int, seq: int, head: int, N: int, thresh: int) -> np.ndarray:
+    out = np.empty(max(N, 1), np.int32)
+    np_ = ctypes.c_int32(0)
+    _check(_load().orc_promote(seed, layer, seq, head, N, thresh, _p(out), ctypes.byref(np_)), "promote")
+    return out[: np_.value].copy()
+
+
+def assign(K, e, parent_tok) -> np.ndarray:
+    K = _f64(K)
+    e = _f64(e)
+    pt = _i32(parent_tok)
+    N, d = K.shape
+    out = np.empty(max(N, 1), np.int32)
+    _check(_load().orc_assign(_p(K), _p(e), N, d, _p(pt), len(pt), _p(out)), "assign")
+    return out[:N].copy()
+
+
+def page_capacity(N: int, Np: int, S: int) -> int:
+    """Upper bound on pages: sum_m ceil(c_m / S) <= (N + (S-1) Np) / S."""
+    return (N + (S - 1) * Np + S - 1) // S
+
+
+def pack(token_parent, Np: int, S: int, page_cap: int | None = None) -> dict:
+    tp = _i32(token_parent)
+    N = len(tp)
+    cap = page_capacity(N, Np, S) if page_cap is None else page_cap
+    c1 = max(cap, 1)
+    page_parent = np.full(c1, -1, np.int32)
+    page_len = np.zeros(c1, np.int32)
+    page_tokens = np.full(c1 * S, -1, np.int32)
+    token_page = np.full(max(N, 1), -1, np.int32)
+    token_slot = np.full(max(N, 1), -1, np.int32)
+    P = ctypes.c_int32(0)
+    _check(_load().orc_pack(_p(tp), N, Np, S, cap, ctypes.byref(P), _p(page_parent), _p(page_len),
+                            _p(page_tokens), _p(token_page), _p(token_slot)), "pack")
+    P = P.value
+    return dict(n_pages=P, page_parent=page_parent[:P].copy(), page_len=page_len[:P].copy(),
+                page_tokens=page_tokens[: P * S].reshape(P, S).copy(),
+                token_page=token_page[:N].copy(), token_slot=token_slot[:N].copy())
+
+
+def scatter(K, V, page_tokens: np.ndarray, S: int) -> tuple[np.ndarray, np.ndarray]:
+    K = _f64(K)
+    V = _f64(V)
+    N, d = K.shape
+    pt = _i32(page_tokens).reshape(-1)
+    P = pt.size // S
+    pk = np.zeros((max(P, 1), S, d), np.float64)
+    pv = np.zeros((max(P, 1), S, d), np.float64)
+    _check(_load().orc_scatter(_p(K), _p(V), N, d, S, P, _p(pt), _p(pk), _p(pv)), "scatter")
+    return pk[:P].copy(), pv[:P].copy()
+
+
+# ---------------------------------------------------------- decode steps ----
+def select(q, parent_keys, page_parent, k_pages: int) -> tuple[np.ndarray, np.ndarray]:
+    """Returns (head_pages [g, k_pages] with -1 pad, union [count] ascending)."""
+    q = _f64(q)
+    pk = _f64(parent_keys)
+    pp = _i32(page_parent)
+    g, d = q.shape
+    Np = pk.shape[0] if pk.size else 0
+    P = len(pp)
+    head = np.full(max(g * k_pages, 1), -1, np.int32)
+    sel = np.full(max(g * k_pages, 1), -1, np.int32)
+    cnt = ctypes.c_int32(0)
+    _check(_load().orc_select(_p(q), g, d, _p(pk if pk.size else np.zeros(1)), Np, _p(pp if P else np.zeros(1, np.int32)),
+                              P, k_pages, _p(head), _p(sel), ctypes.byref(cnt)), "select")
+    return head[: g * k_pages].reshape(g, k_pages).copy(), sel[: cnt.value].copy()
+
+
+def gather(pool_k, pool_v, page_len, sel_pages) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+    pk = _f64(pool_k)
+    pv = _f64(pool_v)
+    P, S, d = pk.shape
+    sel = _i32(sel_pages)
+    U = len(sel)
+    kb = np.zeros((max(U, 1), S, d), np.float64)
+    vb = np.zeros((max(U, 1), S, d), np.float64)
+    bl = np.zeros(max(U, 1), np.int32)
+    _check(_load().orc_gather(_p(pk), _p(pv), _p(_i32(page_len)), P, S, d, _p(sel), U, _p(kb), _p(vb), _p(bl)),
+           "gather")
+    return kb[:U].copy(), vb[:U].copy(), bl[:U].copy()
+
+
+def attention(q, kbuf, vbuf, buf_len, scale: float | None = None) -> np.ndarray:
+    q = _f64(q)
+    g, d = q.shape
+    kb = _f64(kbuf)
+    vb = _f64(vbuf)
+    U = kb.shape[0]
+    S = kb.shape[1] if kb.ndim == 3 else 1
+    bl = _i32(buf_len)
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    out = np.zeros((g, d), np.float64)
+    _check(_load().orc_attention(_p(q), g, d, _p(kb if U else np.zeros(1)), _p(vb if U else np.zeros(1)),
+                                 _p(bl if U else np.zeros(1, np.int32)), U, S, float(scale), _p(out)), "attention")
+    return out
+
+
+# ------------------------------------------------------- whole-unit drivers ----
+def build_unit(K, V, *, seed: int, layer: int, seq: int, head: int, thresh: int, S: int = 16) -> dict:
+    """All build steps (a1-a5) for one (seq, layer, KV head) unit."""
+    K = _f64(K)
+    V = _f64(V)
+    N = K.shape[0]
+    n, M2, e = lift(K)
+    parent_tok = promote(seed, layer, seq, head, N, thresh)
+    token_parent = assign(K, e, parent_tok)
+    pk = pack(token_parent, len(parent_tok), S)
+    pool_k, pool_v = scatter(K, V, pk["page_tokens"], S)
+    return dict(n=n, M2=M2, e=e, parent_tok=parent_tok, parent_keys=K[parent_tok] if N else K[:0],
+                parent_e=e[parent_tok] if N else e[:0], token_parent=token_parent,
+                pool_k=pool_k, pool_v=pool_v, S=S, **pk)
+
+
+def decode_unit(idx: dict, q, budget_tokens: int, scale: float | None = None) -> dict:
+    """Decode steps a6-a10 for one unit and its g query heads."""
+    S = idx["S"]
+    k_pages = -(-budget_tokens // S)
+    head_pages, sel = select(q, idx["parent_keys"], idx["page_parent"], k_pages)
+    kb, vb, bl = gather(idx["pool_k"], idx["pool_v"], idx["page_len"], sel)
+    out = attention(q, kb, vb, bl, scale)
+    return dict(head_pages=head_pages, sel_pages=sel, kbuf=kb, vbuf=vb, buf_len=bl, out=out)
+
+
+class UnitIndex:
+    """Mutable per-unit index for the incremental insert (capacities fixed)."""
+
+    def __init__(self, idx: dict, d: int, np_cap: int, page_cap: int, n_cap: int):
+        S = idx["S"]
+        self.S, self.d, self.M2 = S, d, float(idx["M2"])
+        Np, P, N = len(idx["parent_tok"]), idx["n_pages"], len(idx["token_parent"])
+        self.n_parents = ctypes.c_int32(Np)
+        self.n_pages = ctypes.c_int32(P)
+        self.parent_tok = np.full(np_cap, -1, np.int32); self.parent_tok[:Np] = idx["parent_tok"]
+        self.parent_keys = np.zeros((np_cap, d)); self.parent_keys[:Np] = idx["parent_keys"]
+        self.parent_e = np.zeros(np_cap); self.parent_e[:Np] = idx["parent_e"]
+        self.page_parent = np.full(page_cap, -1, np.int32); self.page_parent[:P] = idx["page_parent"]
+        self.page_len = np.zeros(page_cap, np.int32); self.page_len[:P] = idx["page_len"]
+        self.page_tokens = np.full((page_cap, S), -1, np.int32); self.page_tokens[:P] = idx["page_tokens"]
+        self.pool_k = np.zeros((page_cap, S, d)); self.pool_k[:P] = idx["pool_k"]
+        self.pool_v = np.zeros((page_cap, S, d)); self.pool_v[:P] = idx["pool_v"]
+        self.token_parent = np.full(n_cap, -1, np.int32); self.token_parent[:N] = idx["token_parent"]
+        self.token_page = np.full(n_cap, -1, np.int32); self.token_page[:N] = idx["token_page"]
+        self.token_slot = np.full(n_cap, -1, np.int32); self.token_slot[:N] = idx["token_slot"]
+        self.np_cap, self.page_cap, self.n_cap = np_cap, page_cap, n_cap
+
+    def insert(self, k_new, v_new, pos: int, *, seed: int, layer: int, seq: int, head: int, thresh: int):
+        k = _f64(k_new)
+        v = _f64(v_new)
+        rc = _load().orc_insert(seed, layer, seq, head, thresh, self.d, self.S, self.M2, _p(k), _p(v), pos,
+                                self.np_cap, ctypes.byref(self.n_parents), _p(self.parent_tok),
+                                _p(self.parent_keys), _p(self.parent_e),
+                                self.page_cap, ctypes.byref(self.n_pages), _p(self.page_parent),
+                                _p(self.page_len), _p(self.page_tokens), _p(self.pool_k), _p(self.pool_v),
+                                self.n_cap, _p(self.token_parent), _p(self.token_page), _p(self.token_slot))
+        _check(rc, "insert")
+
+    def as_dict(self) -> dict:
+        Np, P = self.n_parents.value, self.n_pages.value
+        return dict(S=self.S, M2=self.M2, parent_tok=self.parent_tok[:Np], parent_keys=self.parent_keys[:Np],
+                    parent_e=self.parent_e[:Np], n_pages=P, page_parent=self.page_parent[:P],
+                    page_len=self.page_len[:P], page_tokens=self.page_tokens[:P], pool_k=self.pool_k[:P],
+                    pool_v=self.pool_v[:P], token_parent=self.token_parent, token_page=self.token_page,
+                    token_slot=self.token_slot)
+
+
+def run_units(fn, items, threads: int | None = None):
+    """Run fn(item) over independent units on a thread pool.
+
+    The C calls release the GIL, so units run in parallel on host cores.
+    Returns the results in item order and the thread count used.
+    """
+    items = list(items)
+    threads = max(1, min(threads or os.cpu_count() or 1, len(items) or 1))
+    _load()
+    if threads == 1:
+        return [fn(x) for x in items], 1
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        return list(ex.map(fn, items)), threads

@@ -1,0 +1,365 @@
+"""Pins for the CPU oracle against facts fixed outside it.
+
+Each test checks the oracle against something it cannot agree with by
+construction: the published splitmix64 outputs, hand-derived worked examples
+(tests/golden), closed forms of the key lift, textbook special cases (one
+parent gives sequential paging, p = 1 gives exact top-k inner-product search,
+full budget gives dense softmax attention, computed by torch's SDPA), brute
+force over subsets on tiny inputs, and statistical properties of the random
+promotion.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+# ------------------------------------------------------------ promotion draw
+def test_splitmix64_published_vectors():
+    g = _load("splitmix64_vectors.json")
+    s0 = g["streams"][0]
+    for n, h in enumerate(s0["outputs_hex"], start=1):
+        assert oracle.splitmix64_nth(s0["seed"], n) == int(h, 16)
+    s1 = g["streams"][1]
+    for n, v in enumerate(s1["outputs_dec"], start=1):
+        assert oracle.splitmix64_nth(s1["seed"], n) == int(v)
+
+
+def test_promote_draw_is_the_stated_stream_composition():
+    for seed, layer, seq, head, tok, lvl in [(0, 0, 0, 0, 0, 1), (7, 3, 2, 5, 12345, 1), (2**40 + 3, 31, 15, 63, 99999, 2)]:
+        key = oracle.splitmix64_nth(seed, layer + 1)
+        ctr = tok | (lvl << 32) | (head << 40) | (seq << 52)
+        assert oracle.promote_draw(seed, layer, seq, head, tok, lvl) == oracle.splitmix64_nth(key, ctr + 1) >> 32
+
+
+@pytest.mark.parametrize("p", [1 / 16, 1 / 4, 1 / 2])
+def test_promotion_count_is_binomial(p):
+    N = 20000
+    th = oracle.promote_threshold(p)
+    for head in range(3):
+        n = len(oracle.promote(11, 2, 0, head, N, th))
+        mu, sd = N * p, math.sqrt(N * p * (1 - p))
+        assert abs(n - mu) < 5 * sd
+
+
+def test_promotion_depends_on_every_key_field_and_is_deterministic():
+    th = oracle.promote_threshold(1 / 16)
+    base = oracle.promote(5, 1, 2, 3, 4096, th)
+    assert np.array_equal(base, oracle.promote(5, 1, 2, 3, 4096, th))
+    for args in [(6, 1, 2, 3), (5, 2, 2, 3), (5, 1, 3, 3), (5, 1, 2, 4)]:
+        other = oracle.promote(*args, 4096, th)
+        assert not np.array_equal(base, other)
+    assert np.all(np.diff(base) > 0)  # ascending token order
+
+
+def test_promotion_extremes():
+    assert np.array_equal(oracle.promote(0, 0, 0, 0, 100, oracle.promote_threshold(1.0)), np.arange(100))
+    only = oracle.promote(0, 0, 0, 0, 100, 0)
+    draws = [oracle.promote_draw(0, 0, 0, 0, j, 1) for j in range(100)]
+    assert list(only) == [int(np.argmin(draws))]
+    assert len(oracle.promote(0, 0, 0, 0, 0, 0)) == 0
+
+
+# ---------------------------------------------------------------- the lift
+def test_handworked_lift_assign_pack_select():
+    g = _load("handworked_d2.json")
+    K = np.array(g["keys"], float)
+    n, M2, e = oracle.lift(K)
+    assert np.allclose(n, g["lift"]["norm2"], rtol=0, atol=0)
+    assert M2 == g["lift"]["M2"]
+    assert np.allclose(e, g["lift"]["e"], rtol=1e-15, atol=0)
+    tp = oracle.assign(K, e, g["parent_tok"])
+    assert tp.tolist() == g["token_parent"]
+    pk = oracle.pack(tp, len(g["parent_tok"]), g["page_size"])
+    for key in ("page_parent", "page_len", "page_tokens", "token_page", "token_slot"):
+        assert np.asarray(pk[key]).tolist() == g["pages"][key], key
+    pkeys = K[g["parent_tok"]]
+    for case in g["select"]:
+        head, union = oracle.select(np.array(case["q"], float), pkeys, pk["page_parent"], case["k_pages"])
+        assert head.tolist() == case["head_pages"]
+        assert union.tolist() == case["union"]
+
+
+def test_lift_closed_form_all_lifted_norms_equal_M():
+    w = workloads.WORKLOADS["tiny"]
+    K, _ = workloads.unit_kv(w, 0, 0, 0, 512)
+    n, M2, e = oracle.lift(K)
+    Kd = K.astype(np.float64)
+    lifted = np.concatenate([Kd, e[:, None]], axis=1)
+    assert np.allclose(np.linalg.norm(lifted, axis=1), math.sqrt(M2), rtol=1e-14)
+    assert e.min() == 0.0 and np.isclose(M2, (Kd * Kd).sum(1).max(), rtol=1e-15)
+
+
+def _mixture_unit(seed, N, d, centres=8, spread=0.3, lognormal=0.0):
+    r = np.random.default_rng(seed)
+    C = r.standard_normal((centres, d))
+    K = C[r.integers(0, centres, N)] + spread * r.standard_normal((N, d))
+    if lognormal:
+        K *= np.exp(lognormal * r.standard_normal((N, 1)))
+    return workloads.round_bf16(K.astype(np.float32)).astype(np.float64)
+
+
+@pytest.mark.parametrize("d,p,lognormal", [(4, 1 / 4, 0.0), (8, 1 / 16, 0.5), (128, 1 / 16, 0.0), (128, 1 / 4, 0.5)])
+def test_assign_equals_max_lifted_inner_product(d, p, lognormal):
+    """argmin of the lifted distance (oracle) == argmax of the lifted inner
+    product computed by a matrix product (|k'| = |p'| = M makes them equal)."""
+    K = _mixture_unit(int(d * 1000 + p * 64), 384, d, lognormal=lognormal)
+    n, M2, e = oracle.lift(K)
+    pt = oracle.promote(3, 0, 0, d, len(K), oracle.promote_threshold(p))
+    tp = oracle.assign(K, e, pt)
+    lifted = np.concatenate([K, e[:, None]], 1)
+    ip = lifted @ lifted[pt].T
+    expect = np.argmax(ip, axis=1)
+    expect[pt] = np.arange(len(pt))
+    # accept only exact agreement or a near-tie of the inner product
+    best = ip[np.arange(len(K)), expect]
+    got = ip[np.arange(len(K)), tp]
+    assert np.all((tp == expect) | (best - got <= 1e-9 * M2))
+    assert (tp == expect).mean() > 0.99
+
+
+def test_assign_nearest_promoted_point_brute_force():
+    K = _mixture_unit(77, 64, 4)
+    n, M2, e = oracle.lift(K)
+    pt = oracle.promote(1, 0, 0, 0, len(K), oracle.promote_threshold(1 / 4))
+    tp = oracle.assign(K, e, pt)
+    for j in range(len(K)):
+        if j in set(pt.tolist()):
+            assert pt[tp[j]] == j
+            continue
+        dists = [np.linalg.norm(np.append(K[j], e[j]) - np.append(K[t], e[t])) for t in pt]
+        assert tp[j] == int(np.argmin(dists))
+
+
+# -------------------------------------------------------------- packing
+def _check_pack_invariants(tp, Np, S, pk):
+    N = len(tp)
+    P = pk["n_pages"]
+    seen = np.zeros(N, int)
+    counts = np.bincount(tp, minlength=Np)
+    for p in range(P):
+        L = pk["page_len"][p]
+        assert 1 <= L <= S
+        toks = pk["page_tokens"][p]
+        assert np.all(toks[L:] == -1) and np.all(toks[:L] >= 0)
+        assert np.all(tp[toks[:L]] == pk["page_parent"][p])  # one parent per page
+        assert np.all(np.diff(toks[:L]) > 0)
+        seen[toks[:L]] += 1
+        for s, j in enumerate(toks[:L]):
+            assert pk["token_page"][j] == p and pk["token_slot"][j] == s
+    assert np.all(seen == 1)  # every token in exactly one page
+    pages_per_parent = np.bincount(pk["page_parent"], minlength=Np)
+    assert np.array_equal(pages_per_parent, -(-counts // S))
+    assert P <= Np + -(-N // S)
+    assert np.all(np.diff(pk["page_parent"]) >= 0)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_pack_invariants_random(seed):
+    r = np.random.default_rng(seed)
+    N, Np, S = int(r.integers(1, 3000)), int(r.integers(1, 200)), 16
+    tp = r.integers(0, Np, N).astype(np.int32)
+    tp[:Np] = np.arange(Np)  # every parent owns its own token at least
+    pk = oracle.pack(tp, Np, S)
+    _check_pack_invariants(tp, Np, S, pk)
+
+
+def test_pack_single_parent_is_sequential_paging():
+    """With exactly one parent the pages are the classic sequential paging:
+    page i holds tokens 16i .. 16i+15 (papernotes 关键设计 1 / article section 二)."""
+    N, S = 1000, 16
+    pk = oracle.pack(np.zeros(N, np.int32), 1, S)
+    assert pk["n_pages"] == -(-N // S)
+    for p in range(pk["n_pages"]):
+        toks = pk["page_tokens"][p]
+        want = np.arange(p * S, min((p + 1) * S, N))
+        assert np.array_equal(toks[: len(want)], want)
+    assert np.array_equal(pk["token_page"], np.arange(N) // S)
+
+
+def test_pack_capacity_error():
+    with pytest.raises(RuntimeError):
+        oracle.pack(np.zeros(40, np.int32), 1, 16, page_cap=2)
+
+
+# ------------------------------------------------------------- selection
+def test_select_p1_is_exact_topk_mips():
+    """p = 1: every token is its own parent with a one-token page, so page
+    selection is exact top-k maximum inner product search (torch.topk)."""
+    w = workloads.WORKLOADS["tiny"]
+    K, V = workloads.unit_kv(w, 0, 0, 0, 300)
+    q = workloads.unit_queries(w, 0, 0, 0)
+    idx = oracle.build_unit(K, V, seed=0, layer=0, seq=0, head=0, thresh=oracle.promote_threshold(1.0))
+    assert idx["n_pages"] == len(K) and np.all(idx["page_len"] == 1)
+    assert np.array_equal(idx["page_tokens"][:, 0], np.arange(len(K)))
+    k = 10
+    head, union = oracle.select(q, idx["parent_keys"], idx["page_parent"], k)
+    scores = torch.tensor(q, dtype=torch.float64) @ torch.tensor(K, dtype=torch.float64).T
+    top = torch.topk(scores, k, dim=1).indices.numpy()
+    for h in range(q.shape[0]):
+        assert set(head[h].tolist()) == set(top[h].tolist())
+    assert union.tolist() == sorted(set(top.reshape(-1).tolist()))
+
+
+def test_select_brute_force_subsets():
+    """On tiny inputs, the chosen set is the unique k-subset whose every
+    member precedes every non-member in the (-score, page id) order."""
+    r = np.random.default_rng(5)
+    for trial in range(20):
+        Np, d = int(r.integers(1, 6)), 3
+        tp = r.integers(0, Np, 30).astype(np.int32)
+        tp[:Np] = np.arange(Np)
+        pk = oracle.pack(tp, Np, 4)
+        keys = np.round(r.standard_normal((Np, d)), 1)  # coarse values: ties happen
+        q = np.round(r.standard_normal((1, d)), 1)
+        P = pk["n_pages"]
+        s = keys @ q[0]
+        k = int(r.integers(1, P + 1))
+        head, union = oracle.select(q, keys, pk["page_parent"], k)
+        ok = []
+        for T in itertools.combinations(range(P), k):
+            Tset = set(T)
+            good = all((-s[pk["page_parent"][a]], a) < (-s[pk["page_parent"][b]], b)
+                       for a in Tset for b in range(P) if b not in Tset)
+            if good:
+                ok.append(Tset)
+        assert len(ok) == 1
+        assert set(head[0].tolist()) == ok[0] and union.tolist() == sorted(ok[0])
+
+
+def test_select_union_g1_identity_and_k_ge_P():
+    w = workloads.WORKLOADS["tiny"]
+    K, V = workloads.unit_kv(w, 0, 0, 0, 500)
+    idx = oracle.build_unit(K, V, seed=0, layer=0, seq=0, head=0, thresh=oracle.promote_threshold(1 / 16))
+    q = workloads.unit_queries(w, 0, 0, 0)
+    head, union = oracle.select(q[:1], idx["parent_keys"], idx["page_parent"], 4)
+    assert union.tolist() == sorted(head[0].tolist())
+    head, union = oracle.select(q, idx["parent_keys"], idx["page_parent"], idx["n_pages"] + 5)
+    assert union.tolist() == list(range(idx["n_pages"]))
+
+
+# ------------------------------------------------------------- attention
+def test_attention_handworked():
+    g = _load("attention_d2.json")
+    a = math.sqrt(2.0) * math.log(2.0)
+    kb = np.array([[[0, 0], [a, 0]], [[-a, 0], [50, 0]]], float)
+    vb = np.array(g["values"], float)
+    out = oracle.attention(np.array(g["q"], float), kb, vb, g["buf_len"])
+    assert np.allclose(out, g["out"], rtol=0, atol=1e-13)
+
+
+def test_full_budget_equals_dense_sdpa():
+    """Full budget selects every page, and the masked sparse attention over
+    the gathered pages equals dense softmax attention over all N tokens
+    (torch.nn.functional.scaled_dot_product_attention, float64)."""
+    w = workloads.WORKLOADS["tiny"].scaled(n_tokens=700)
+    K, V = workloads.unit_kv(w, 0, 0, 0)
+    q = workloads.unit_queries(w, 0, 0, 0)
+    idx = oracle.build_unit(K, V, seed=0, layer=0, seq=0, head=0, thresh=oracle.promote_threshold(1 / 16))
+    res = oracle.decode_unit(idx, q, budget_tokens=16 * idx["n_pages"])
+    assert res["sel_pages"].tolist() == list(range(idx["n_pages"]))
+    t = lambda x: torch.tensor(x, dtype=torch.float64)
+    dense = torch.nn.functional.scaled_dot_product_attention(t(q)[None, :, None, :], t(K)[None, None].expand(1, q.shape[0], -1, -1),
+                                                             t(V)[None, None].expand(1, q.shape[0], -1, -1))
+    assert np.allclose(res["out"], dense[0, :, 0].numpy(), rtol=0, atol=1e-12)
+
+
+def test_attention_subset_equals_sdpa_on_selected_tokens():
+    w = workloads.WORKLOADS["tiny"].scaled(n_tokens=900)
+    K, V = workloads.unit_kv(w, 0, 0, 0)
+    q = workloads.unit_queries(w, 0, 0, 0)
+    idx = oracle.build_unit(K, V, seed=0, layer=0, seq=0, head=0, thresh=oracle.promote_threshold(1 / 16))
+    res = oracle.decode_unit(idx, q, budget_tokens=64)
+    toks = idx["page_tokens"][res["sel_pages"]].reshape(-1)
+    toks = toks[toks >= 0]
+    t = lambda x: torch.tensor(x, dtype=torch.float64)
+    Ks, Vs = t(K[toks]), t(V[toks])
+    dense = torch.nn.functional.scaled_dot_product_attention(t(q)[None, :, None, :], Ks[None, None].expand(1, q.shape[0], -1, -1),
+                                                             Vs[None, None].expand(1, q.shape[0], -1, -1))
+    assert np.allclose(res["out"], dense[0, :, 0].numpy(), rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- insert
+def _unit_invariants(ui):
+    d = ui.as_dict()
+    P, S = d["n_pages"], d["S"]
+    N = int((ui.token_parent >= 0).sum())
+    for p in range(P):
+        L = d["page_len"][p]
+        assert 1 <= L <= S
+        toks = d["page_tokens"][p][:L]
+        assert np.all(ui.token_parent[toks] == d["page_parent"][p])
+        assert np.all(ui.token_page[toks] == p) and np.array_equal(ui.token_slot[toks], np.arange(L))
+    assert d["page_len"].sum() == N
+
+
+def test_insert_p1_creates_one_token_pages():
+    w = workloads.WORKLOADS["tiny"]
+    K, V = workloads.unit_kv(w, 0, 0, 0, 64)
+    th = oracle.promote_threshold(1.0)
+    idx = oracle.build_unit(K, V, seed=0, layer=0, seq=0, head=0, thresh=th)
+    ui = oracle.UnitIndex(idx, 128, np_cap=80, page_cap=80, n_cap=80)
+    Kn, Vn = workloads.unit_new_tokens(w, 0, 0, 0, 8)
+    for s in range(8):
+        ui.insert(Kn[s], Vn[s], 64 + s, seed=0, layer=0, seq=0, head=0, thresh=th)
+        assert ui.n_parents.value == 65 + s and ui.n_pages.value == 65 + s
+        assert ui.page_len[64 + s] == 1 and ui.page_tokens[64 + s, 0] == 64 + s
+    _unit_invariants(ui)
+
+
+def test_insert_attaches_to_nearest_parent_and_splits_at_17():
+    """Keys equal to parent 0's key attach to parent 0 (distance 0); once its
+    last page holds 16 tokens the 17th opens a new page."""
+    d, S = 4, 16
+    K = np.array([[1.0, 0, 0, 0], [0, 1.0, 0, 0]])
+    V = np.zeros_like(K)
+    idx = {"S": S, "M2": 1.0, "parent_tok": np.array([0, 1]), "parent_keys": K, "parent_e": np.zeros(2),
+           "n_pages": 2, "page_parent": np.array([0, 1]), "page_len": np.array([1, 1]),
+           "page_tokens": np.array([[0] + [-1] * 15, [1] + [-1] * 15]), "pool_k": np.zeros((2, S, d)),
+           "pool_v": np.zeros((2, S, d)), "token_parent": np.array([0, 1]), "token_page": np.array([0, 1]),
+           "token_slot": np.array([0, 0])}
+    ui = oracle.UnitIndex(idx, d, np_cap=4, page_cap=8, n_cap=64)
+    pos = 2
+    for _ in range(40):
+        ui.insert(K[0], np.ones(d), pos, seed=0, layer=0, seq=0, head=0, thresh=0)  # thresh 0: never promoted
+        pos += 1
+    assert ui.n_pages.value == 4  # page 0 filled to 16, then pages 2 and 3
+    assert ui.page_len[:4].tolist() == [16, 1, 16, 9]
+    assert ui.page_parent[:4].tolist() == [0, 1, 0, 0]
+    _unit_invariants(ui)
+
+
+def test_insert_stream_keeps_invariants_and_matches_rebuild_when_nothing_promotes():
+    """With promotion switched off for the new tokens, inserting tokens one by
+    one attaches each to its nearest parent exactly as a build over all the
+    tokens with the same parents and the same M would (the page layout then
+    differs only in page numbering, so compare the parent of every token)."""
+    w = workloads.WORKLOADS["tiny"]
+    K, V = workloads.unit_kv(w, 0, 0, 0, 400)
+    th = oracle.promote_threshold(1 / 16)
+    idx = oracle.build_unit(K, V, seed=0, layer=0, seq=0, head=0, thresh=th)
+    Kn, Vn = workloads.unit_new_tokens(w, 0, 0, 0, 50)
+    Kn = Kn * 0.5  # keep |k| < M so that the extra coordinate never clamps
+    ui = oracle.UnitIndex(idx, 128, np_cap=100, page_cap=200, n_cap=450)
+    for s in range(50):
+        ui.insert(Kn[s], Vn[s], 400 + s, seed=0, layer=0, seq=0, head=0, thresh=0)
+    _unit_invariants(ui)
+    Kall = np.concatenate([K, Kn]).astype(np.float64)
+    n = (Kall ** 2).sum(1)
+    e = np.sqrt(np.maximum(idx["M2"] - n, 0))
+    tp = oracle.assign(Kall, e, idx["parent_tok"])
+    assert np.array_equal(ui.token_parent[:450], tp)
