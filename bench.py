@@ -1,0 +1,366 @@
+#!/usr/bin/env python
+"""Benchmark of the IceCache hot path on GB300.
+
+One step = the whole hot path over one layer's batch: index build (lift and
+promotion, nearest-parent assignment, page packing and pool scatter) and one
+decode step (selection + GQA union, gather, masked sparse attention) at the
+workload's largest budget.  value = keys indexed and decoded per second over
+all ranks.  Each rank processes its own batch (weak scaling, no collective on
+the data path; torch.distributed only carries the barrier and the max of the
+timings).
+
+Usage: python bench.py [--gpus N --steps K --warmup W --impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "decode-step µs & HBM GB/s (select+gather+sparse attn); index-build keys/s"
+L2_BYTES = 129 * 2 ** 20
+KERNELS_PER_STEP = 8  # lift_count, promote_write, assign, pack_count, pack_scan, pack_rank_scatter, select, attn
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama31_8b_16k")
+    ap.add_argument("--budget", type=int, default=None)
+    ap.add_argument("--sets", type=int, default=4, help="input sets rotated between steps (L2 stays cold)")
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-units", type=int, default=None, help="units in the CPU-baseline sample")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, src="fallback")
+
+
+def rank_info():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+# ------------------------------------------------------------- clocks ------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+        if self.gpu_id is not None:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons, n = [], None, set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            n += 1
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": n}
+
+
+def gpu_id_for(dev) -> str | None:
+    import torch
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        if dev < len(ids):
+            return ids[dev]
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        return str(dev)
+
+
+# ------------------------------------------------------- CPU oracle leg ---
+def oracle_sample(w: workloads.Workload, budget: int, units: int, rank_seed: int = 0):
+    """Time the oracle (as it stands) on `units` units of the workload: build
+    (a1-a5) and one decode step (a6-a10), one unit per host thread."""
+    import oracle
+    th = oracle.promote_threshold(w.promote_p)
+    items = [(u // w.n_kv_heads, u % w.n_kv_heads) for u in range(units)]
+    data = {it: (workloads.unit_kv(w, 0, *it), workloads.unit_queries(w, 0, *it)) for it in items}
+
+    def one(it):
+        (K, V), q = data[it]
+        idx = oracle.build_unit(K, V, seed=w.seed, layer=0, seq=it[0], head=it[1], thresh=th, S=w.page_size)
+        oracle.decode_unit(idx, q, budget)
+
+    oracle.build()
+    t0 = time.perf_counter()
+    _, threads = oracle.run_units(one, items, threads=min(units, os.cpu_count() or 1))
+    dt = time.perf_counter() - t0
+    return dt, threads
+
+
+def run_reference(args):
+    rank, _, world = rank_info()
+    if rank != 0:
+        return  # the oracle arm runs on rank 0 only
+    w = workloads.WORKLOADS[args.workload]
+    budget = args.budget or max(w.budgets)
+    units = args.cpu_units or min(w.units, os.cpu_count() or 1)
+    times, threads = [], 1
+    for i in range(args.warmup + args.steps):
+        dt, threads = oracle_sample(w, budget, units)
+        if i >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = units * w.n_tokens * len(times) / total
+    sample = f"{units} of {w.units} units (KV heads) per step, full N={w.n_tokens}, budget {budget}"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "keys/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, budget, args.gpus, args.sets),
+        "cpu_baseline": {"value": value, "unit": "keys/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "keys/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def config_of(w, budget, gpus, sets):
+    return {"workload": w.name, "batch_per_gpu": w.batch, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
+            "n_tokens": w.n_tokens, "head_dim": w.head_dim, "page_size": w.page_size, "promote_p": w.promote_p,
+            "levels": 2, "budget_tokens": budget, "layers_per_step": 1, "parallelism": f"dp{gpus}",
+            "l2": f"inputs rotated over {sets} sets between steps (each set larger than half of L2; "
+                  f"{sets} sets > 4x L2 combined)"}
+
+
+# ------------------------------------------------------------- our arm ----
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import semantic_paged_kv_gb300 as ice
+
+    rank, local, world = rank_info()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    base = workloads.WORKLOADS[args.workload]
+    w = base.scaled(seed=base.seed + 1000 * rank)  # each rank owns its own batch
+    budget = args.budget or max(w.budgets)
+    cfg = ice.Config(batch=w.batch, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, n_tokens=w.n_tokens,
+                     dtype=ice.ICE_BF16 if w.dtype == "bf16" else ice.ICE_FP32, promote_p=w.promote_p, seed=w.seed)
+    dt = cfg.torch_dtype
+    sets = []
+    for s in range(args.sets):
+        K, V = workloads.batch_kv(w, layer=s)
+        Q = workloads.batch_queries(w, layer=s)
+        c = ice.Config(**{**cfg.__dict__, "layer": s})
+        p = c.params()
+        st = dict(cfg=c, params=p, Kh=torch.from_numpy(K).to(dt).pin_memory(), Vh=torch.from_numpy(V).to(dt).pin_memory(),
+                  Qh=torch.from_numpy(Q).to(dt).pin_memory())
+        st["K"], st["V"], st["Q"] = st["Kh"].cuda(), st["Vh"].cuda(), st["Qh"].cuda()
+        st["idx"] = ice.Index(c)
+        st["ws"] = ice.workspace(ice.ice_build_workspace_bytes(p))
+        st["buf"] = ice.DecodeBuffers(c, budget)
+        st["Oh"] = torch.empty_like(st["buf"].O, device="cpu").pin_memory()
+        sets.append(st)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    scale = 1.0 / math.sqrt(w.head_dim)
+    set_bytes = sum(x.numel() * x.element_size() for x in (sets[0]["K"], sets[0]["V"], sets[0]["idx"].pool_k,
+                                                           sets[0]["idx"].pool_v))
+
+    def step(st, evs=None):
+        p, idx, buf = st["params"], st["idx"], st["buf"]
+        if evs: evs[0].record()
+        ice.ice_build_lift_promote(p, st["K"], idx, st["ws"], err)
+        if evs: evs[1].record()
+        ice.ice_build_assign(p, st["K"], idx, st["ws"], err)
+        if evs: evs[2].record()
+        ice.ice_build_pack(p, st["K"], st["V"], idx, st["ws"], err)
+        if evs: evs[3].record()
+        ice.ice_decode_step(p, idx, st["Q"], budget, buf.sel_pages, buf.sel_count, buf.kbuf, buf.vbuf, buf.buf_len,
+                            scale, buf.O, buf.ws, err)
+        if evs: evs[4].record()
+
+    for i in range(max(args.warmup, 3)):
+        step(sets[i % len(sets)])
+    torch.cuda.synchronize()
+    status = ice.ice_check(err)
+    if status != ice.ICE_OK:
+        raise SystemExit(f"device reported status {status}: {ice.ice_status_string(status)}")
+
+    # ---- timed region: exactly `steps` steps
+    E = lambda: torch.cuda.Event(enable_timing=True)
+    evs = [[E() for _ in range(5)] for _ in range(args.steps)]
+    sampler = ClockSampler(gpu_id_for(local))
+    barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.15)
+    t0, t1 = E(), E()
+    t0.record()
+    for i in range(args.steps):
+        step(sets[i % len(sets)], evs[i])
+    t1.record()
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([elapsed_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    stage = np.array([[e[k].elapsed_time(e[k + 1]) for k in range(4)] for e in evs])  # ms
+    lift_ms, assign_ms, pack_ms, decode_ms = stage.mean(0)
+
+    # ---- algorithmic work of a step (averaged over the sets)
+    d, S, U, N = w.head_dim, w.page_size, cfg.units, w.n_tokens
+    esz = 2 if w.dtype == "bf16" else 4
+    np_tot = np.mean([int(s["idx"].n_parents.sum()) for s in sets])
+    pages_tot = np.mean([int(s["idx"].n_pages.sum()) for s in sets])
+    sel_tot = np.mean([int(s["buf"].sel_count.sum()) for s in sets])
+    flops_assign = 2.0 * N * np_tot * d
+    qo_bytes = cfg.batch * cfg.n_q_heads * d * (esz + 4)
+    decode_min_bytes = np_tot * d * esz + sel_tot * S * d * esz * 2 + qo_bytes
+    decode_pipe_bytes = decode_min_bytes + sel_tot * S * d * esz * 2  # + the contiguous-buffer write
+    pack_bytes = 2 * U * N * d * esz + 2 * pages_tot * S * d * esz
+    lift_bytes = U * N * d * esz + np_tot * d * esz
+    pk = peaks()
+    cands = {
+        "assign": (assign_ms, "tensor", flops_assign / (assign_ms * 1e-3) / 1e12, pk["bf16"], "TFLOP/s", flops_assign),
+        "pack": (pack_ms, "hbm", pack_bytes / (pack_ms * 1e-3) / 1e9, pk["hbm"], "GB/s", pack_bytes),
+        "lift_promote": (lift_ms, "hbm", lift_bytes / (lift_ms * 1e-3) / 1e9, pk["hbm"], "GB/s", lift_bytes),
+        "decode": (decode_ms, "hbm", decode_min_bytes / (decode_ms * 1e-3) / 1e9, pk["hbm"], "GB/s", decode_min_bytes),
+    }
+    if w.dtype != "bf16":
+        cands["assign"] = (assign_ms, "alu", flops_assign / (assign_ms * 1e-3) / 1e12, 37.0 * 2, "TFLOP/s",
+                           flops_assign)
+    dom = max(cands, key=lambda k: cands[k][0])
+    ms_, bound, ach, peak, unit, work = cands[dom]
+    keys_step = U * N
+    value = world * keys_step * args.steps / (elapsed_ms * 1e-3)
+
+    # ---- end to end through the public API with host buffers
+    e2e_steps = args.e2e_steps or min(args.steps, 100)
+    h2d = sum(sets[0][k].numel() * sets[0][k].element_size() for k in ("Kh", "Vh", "Qh"))
+    d2h = sets[0]["Oh"].numel() * 4
+    barrier()
+    torch.cuda.synchronize()
+    a, b_ = E(), E()
+    a.record()
+    for i in range(e2e_steps):
+        st = sets[i % len(sets)]
+        st["K"].copy_(st["Kh"], non_blocking=True)
+        st["V"].copy_(st["Vh"], non_blocking=True)
+        st["Q"].copy_(st["Qh"], non_blocking=True)
+        step(st)
+        st["Oh"].copy_(st["buf"].O, non_blocking=True)
+    b_.record()
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(b_)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_value = world * keys_step * e2e_steps / (e2e_ms * 1e-3)
+    status = ice.ice_check(err)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        units = args.cpu_units or min(U, os.cpu_count() or 1)
+        cdt, threads = oracle_sample(w, budget, units)
+        cpu = {"value": units * N / cdt, "unit": "keys/s", "cores": threads, "kind": "oracle",
+               "sample": f"{units} of {U} units (KV heads) of this workload, full N={N}: index build + one decode "
+                         f"step at budget {budget}, one unit per host thread ({cdt:.1f} s)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "keys/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": config_of(w, budget, world, args.sets),
+            "phases": {
+                "decode_step_us": 1000 * decode_ms,
+                "decode_hbm_gbs_min_bytes": decode_min_bytes / (decode_ms * 1e-3) / 1e9,
+                "decode_hbm_gbs_pipeline_bytes": decode_pipe_bytes / (decode_ms * 1e-3) / 1e9,
+                "index_build_keys_per_s": keys_step / ((lift_ms + assign_ms + pack_ms) * 1e-3),
+                "build_us": {"lift_promote": 1000 * lift_ms, "assign": 1000 * assign_ms, "pack": 1000 * pack_ms},
+                "assign_tflops": flops_assign / (assign_ms * 1e-3) / 1e12,
+                "parents_per_step": np_tot, "pages_per_step": pages_tot, "selected_pages_per_step": sel_tot,
+                "set_bytes": set_bytes,
+            },
+            "roofline": {"kernel": dom, "bound": bound, "achieved": ach, "peak": peak, "unit": unit,
+                         "frac": ach / peak, "peak_source": pk["src"] + (" burst" if bound == "tensor" else ""),
+                         "work_per_launch": work, "traffic": None},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "keys/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": e2e_steps},
+            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "clocks": clocks,
+            "device_status": ice.ice_status_string(status),
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

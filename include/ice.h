@@ -1,0 +1,271 @@
+/*
+ * ice.h -- C ABI of the IceCache hot path for one GB300 (sm_103a).
+ *
+ * IceCache keeps a long KV cache in pages whose tokens are grouped by key
+ * similarity instead of position, and at decode time loads only the pages a
+ * query needs.  Sources, by page and section:
+ *   [A] "IceCache: Memory-Efficient KV-cache Management for Long-Sequence
+ *       LLMs" (papernotes.org ICLR 2026 notes), 方法详解 / 整体框架 and
+ *       关键设计 1-4.
+ *   [B] IceCache popular-science article (aitangshan.cn/news/751385),
+ *       sections 二, 三, 四 and 六.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every function returns an ice_status (ICE_OK = 0).  On a non-zero
+ *    return nothing was launched unless the code is ICE_ERR_CUDA, and
+ *    ice_last_error() (thread-local) describes the failure.
+ *  - Every array argument is a raw pointer owned by the caller: DEVICE memory
+ *    unless the argument says "host".  Arrays are dense row-major with the
+ *    shapes written next to them.  The library never allocates, frees or
+ *    keeps a pointer after the call returns (the host page pool is the one
+ *    library-owned object, see ice_host_pool_create).
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and is asynchronous: no entry point synchronises unless it says
+ *    so.  Scratch memory comes from the caller's workspace `ws` of `ws_bytes`
+ *    bytes (256-byte aligned), sized by the matching *_workspace_bytes query.
+ *  - A "unit" is one (sequence b, KV head h) pair of one layer; units are
+ *    numbered u = b * n_kv_heads + h and are fully independent.
+ *  - Conditions only the device can see (a capacity that turns out too
+ *    small) are written to the caller's device word `err_dev` (int32, set to
+ *    0 by the caller before first use) as an ice_status; the kernels then
+ *    clamp every write to the capacities, so memory outside the arrays is
+ *    never touched.  ice_check() reads and clears that word.
+ *  - Floating point: keys/values/queries are bf16 or fp32 (ice_params.dtype);
+ *    every score and every softmax is accumulated in fp32; outputs O are
+ *    fp32.
+ */
+#ifndef ICE_H_
+#define ICE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t ice_status;
+#define ICE_OK 0
+#define ICE_ERR_INVALID_ARG 1
+#define ICE_ERR_CUDA 2
+#define ICE_ERR_OOM 3
+#define ICE_ERR_CAPACITY 4
+#define ICE_ERR_TIMEOUT 5
+#define ICE_ERR_UNSUPPORTED 6
+
+#define ICE_BF16 0
+#define ICE_FP32 1
+
+/* Shapes and knobs of one layer's index.  All fields are plain values. */
+typedef struct ice_params {
+    int32_t batch;          /* B: sequences */
+    int32_t n_q_heads;      /* Hq */
+    int32_t n_kv_heads;     /* Hkv; Hq must be a multiple (g = Hq / Hkv) */
+    int32_t head_dim;       /* d; 128 is the supported value */
+    int32_t n_tokens;       /* N: tokens per unit given to ice_build_index */
+    int32_t page_size;      /* S; 16 is the supported value ([B] section 二) */
+    int32_t dtype;          /* ICE_BF16 or ICE_FP32 for K, V, Q and the pool */
+    int32_t n_levels;       /* index levels; 2 is the supported value */
+    uint64_t promote_thresh;/* floor(p * 2^32), 0 .. 2^32: promotion probability p */
+    uint64_t seed;          /* promotion seed */
+    int32_t layer;          /* layer id (enters the promotion draw) */
+    int32_t np_cap;         /* parent capacity per unit */
+    int32_t page_cap;       /* page capacity per unit */
+    int32_t n_cap;          /* token capacity per unit (>= n_tokens; room for inserts) */
+} ice_params;
+
+/*
+ * Device arrays of one layer's index, all caller-owned.  U = B * Hkv units.
+ * Sizes: Np = np_cap, Pc = page_cap, Nc = n_cap, S = page_size, d = head_dim.
+ *
+ *  per unit      n_parents[U], n_pages[U], n_indexed[U] (tokens indexed so
+ *                far: N after the build, +1 per insert) int32;
+ *                m2[U] double: M^2, the squared largest key norm of the build.
+ *  parent level  parent_tok[U,Np] int32 (token of parent m, ascending);
+ *                parent_keys[U,Np,d] (dtype, the parent tokens' keys);
+ *                parent_e[U,Np] float: lifted extra coordinate
+ *                  sqrt(max(0, M^2 - |p|^2));
+ *                parent_corr[U,Np] float: (M^2 - max(M^2, |p|^2)) / 2, zero
+ *                  for every parent chosen at build time;
+ *                parent_first_page[U,Np], parent_last_page[U,Np],
+ *                parent_n_pages[U,Np] int32.
+ *  pages         page_parent[U,Pc], page_len[U,Pc] (1..S),
+ *                page_next[U,Pc] (next page of the same parent, -1 at the
+ *                end), page_tokens[U,Pc,S] (token of each slot, -1 pad) int32.
+ *  tokens        token_parent[U,Nc], token_page[U,Nc], token_slot[U,Nc] int32.
+ *  pool          pool_k[U,Pc,S,d], pool_v[U,Pc,S,d] (dtype): each page's K and
+ *                V rows in slot order, pad slots zero ([A] 整体框架: one
+ *                node = one physical page).
+ * Only the first n_parents / n_pages / n_indexed entries of a unit are
+ * defined after a call.
+ */
+typedef struct ice_index {
+    int32_t *n_parents;
+    int32_t *n_pages;
+    int32_t *n_indexed;
+    double *m2;
+    int32_t *parent_tok;
+    void *parent_keys;
+    float *parent_e;
+    float *parent_corr;
+    int32_t *parent_first_page;
+    int32_t *parent_last_page;
+    int32_t *parent_n_pages;
+    int32_t *page_parent;
+    int32_t *page_len;
+    int32_t *page_next;
+    int32_t *page_tokens;
+    int32_t *token_parent;
+    int32_t *token_page;
+    int32_t *token_slot;
+    void *pool_k;
+    void *pool_v;
+} ice_index;
+
+/* ---------------------------------------------------------------- misc -- */
+const char *ice_status_string(ice_status s);
+/* Message for the last failing call on this host thread ("" if none). */
+const char *ice_last_error(void);
+/* Library version string. */
+const char *ice_version(void);
+/* Synchronises `stream`, reads the device error word, clears it and returns
+ * its value (ICE_OK when no device-side condition was raised). */
+ice_status ice_check(int32_t *err_dev, void *stream);
+/* Largest page count a unit of N tokens with Np parents can need:
+ * sum_m ceil(c_m / S) <= (N + (S - 1) * Np) / S, rounded down (the sum is an
+ * integer). */
+int32_t ice_page_bound(int32_t n_tokens, int32_t n_parents, int32_t page_size);
+
+/* ------------------------------------------------------ index build ----- */
+/* Workspace bytes needed by ice_build_index and its three stages. */
+ice_status ice_build_workspace_bytes(const ice_params *p, size_t *bytes);
+
+/*
+ * Builds every unit's index from K, V [B, Hkv, N, d] (dtype):
+ * ice_build_lift_promote, then ice_build_assign, then ice_build_pack, on one
+ * stream.  The three stages are also exported so that they can be timed or
+ * overlapped separately; they must run in this order with the same
+ * arguments and workspace.
+ */
+ice_status ice_build_index(const ice_params *p, const void *K, const void *V, const ice_index *idx,
+                           void *ws, size_t ws_bytes, int32_t *err_dev, void *stream);
+
+/*
+ * Stage a1 + a2: the key lift and the random promotion.
+ * Lift ([B] sections 三 and 六; [A] 关键设计 2): with n_j = |k_j|^2 and
+ * M^2 = max_j n_j, every key becomes k'_j = [k_j, sqrt(M^2 - n_j)], so all
+ * lifted keys have norm M and nearest-neighbour search in lifted space is
+ * maximum inner-product search.  n_j and M^2 are computed exactly enough
+ * that the fp32 extra coordinate is the correctly rounded value.
+ * Promotion ([B] section 三): every token is at level 0; token j is promoted
+ * to level 1 iff draw(j) < promote_thresh, where draw is the top 32 bits of
+ * a splitmix64 output (Steele, Lea & Flood 2014) at counter
+ * (token | 1 << 32 | h << 40 | b << 52) + 1 in the stream keyed by output
+ * (layer + 1) of the stream seeded by `seed`.  If no token of a unit is
+ * promoted, its token with the smallest draw is (lowest token on equal
+ * draws).  Parents m = 0..Np-1 are the promoted tokens in ascending order.
+ * Writes m2, n_parents, parent_tok, parent_keys, parent_e, parent_corr (0),
+ * token_parent (m for a promoted token, -1 otherwise), n_indexed = N.
+ * Requires B, Hkv < 4096.  ICE_ERR_CAPACITY in err_dev if Np > np_cap.
+ */
+ice_status ice_build_lift_promote(const ice_params *p, const void *K, const ice_index *idx, void *ws,
+                                  size_t ws_bytes, int32_t *err_dev, void *stream);
+
+/*
+ * Stage a3: nearest parent ([B] section 三: every token takes as parent the
+ * most similar point one level up; [A] 关键设计 2).
+ *   parent(j) = argmin_m |k'_j - p'_m|^2 = argmax_m (k_j . p_m + e_j e_m)
+ * with the dot product of the stored keys accumulated in fp32 (bf16: the
+ * sm_103a tensor cores, fp32: CUDA cores) and exact fp32 ties going to the
+ * lowest m.  A promoted token keeps itself as parent.  Writes token_parent.
+ */
+ice_status ice_build_assign(const ice_params *p, const void *K, const ice_index *idx, void *ws,
+                            size_t ws_bytes, int32_t *err_dev, void *stream);
+
+/*
+ * Stage a3 on CUDA cores (fp32 FMA) for either dtype.  Same contract and
+ * results as ice_build_assign up to fp32 rounding order; ice_build_assign
+ * uses it for ICE_FP32, and for ICE_BF16 it serves as an independent
+ * cross-check of the tensor-core kernel.
+ */
+ice_status ice_build_assign_simt(const ice_params *p, const void *K, const ice_index *idx, void *ws,
+                                 size_t ws_bytes, int32_t *err_dev, void *stream);
+
+/*
+ * Stage a4 + a5: pages ([B] section 三: the tokens under one parent share a
+ * physical page; [A] 关键设计 2: a node larger than a page splits off a new
+ * page; [B] section 二: S = 16).  For parents in ascending m, the parent's
+ * tokens in ascending token order are cut into consecutive chunks of S, and
+ * pages are numbered in that order.  Writes n_pages, page_parent, page_len,
+ * page_next, page_tokens, token_page, token_slot, parent_first_page,
+ * parent_last_page, parent_n_pages, and copies K/V rows into pool_k/pool_v
+ * (pad slots zero).  ICE_ERR_CAPACITY in err_dev if the pages exceed
+ * page_cap.
+ */
+ice_status ice_build_pack(const ice_params *p, const void *K, const void *V, const ice_index *idx,
+                          void *ws, size_t ws_bytes, int32_t *err_dev, void *stream);
+
+/* ------------------------------------------------------- decode step ---- */
+/* Workspace bytes for ice_select_pages / ice_sparse_attn_decode /
+ * ice_decode_step at this budget and output capacity max_sel. */
+ice_status ice_decode_workspace_bytes(const ice_params *p, int32_t budget_tokens, int32_t max_sel,
+                                      size_t *bytes);
+
+/*
+ * Steps a6-a8: page selection and the GQA union ([A] 关键设计 3: each query
+ * head chooses its own top-k pages; the query heads of one GQA group share
+ * the union of their choices; [B] section 六).
+ * Q [B, Hq, d] (dtype); query head hq belongs to KV head hq / g.
+ * The lifted query q' = [q, 0] gives |q' - p'|^2 = |q|^2 + M^2 - 2 q.p, so a
+ * page scores s = q . (its parent's key), accumulated in fp32.  Each query
+ * head takes the first k = ceil(budget_tokens / S) pages in the order
+ * (-s, page id); sel_pages[u, 0..sel_count[u]) is the ascending union of the
+ * g lists, sel_pages [U, max_sel] int32 (rest -1), sel_count [U] int32.
+ * max_sel must be >= min(g * k, page_cap).
+ */
+ice_status ice_select_pages(const ice_params *p, const ice_index *idx, const void *Q, int32_t budget_tokens,
+                            int32_t *sel_pages, int32_t *sel_count, int32_t max_sel, void *ws,
+                            size_t ws_bytes, int32_t *err_dev, void *stream);
+
+/*
+ * Step a9: bulk gather ([A] 关键设计 4; [B] section 四): the selected,
+ * non-contiguous pages are copied into one contiguous buffer.
+ * kbuf, vbuf [U, max_sel, S, d] (dtype): slot u holds page sel_pages[u];
+ * buf_len [U, max_sel] int32 its length (0 beyond sel_count).
+ */
+ice_status ice_gather_pages(const ice_params *p, const ice_index *idx, const int32_t *sel_pages,
+                            const int32_t *sel_count, int32_t max_sel, void *kbuf, void *vbuf,
+                            int32_t *buf_len, void *stream);
+
+/*
+ * Step a10: masked sparse attention ([A] 关键设计 1):
+ *   a_ij = s_ij exp(q_i.k_j * scale) / sum_j' s_ij' exp(q_i.k_j' * scale),
+ *   o_i  = sum_j a_ij v_j,
+ * with s_ij = 1 on the first buf_len[u] slots of each of the sel_count
+ * gathered pages of the query head's group and 0 elsewhere; scale is
+ * 1/sqrt(d) in the formula (pass it explicitly).  Split over the pages with
+ * a log-sum-exp merge; fp32 throughout.  O [B, Hq, d] float; a unit with no
+ * selected page gives O = 0.
+ */
+ice_status ice_sparse_attn_decode(const ice_params *p, const void *Q, const void *kbuf, const void *vbuf,
+                                  const int32_t *buf_len, const int32_t *sel_count, int32_t max_sel,
+                                  float scale, float *O, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * The whole decode step a6-a10 in two launches: ice_select_pages, then one
+ * kernel that reads each selected page once from the pool, writes it to
+ * kbuf/vbuf/buf_len (the contiguous buffer of step a9) and computes the
+ * attention of step a10 from the same copy.  Same outputs as the three
+ * separate calls.
+ */
+ice_status ice_decode_step(const ice_params *p, const ice_index *idx, const void *Q, int32_t budget_tokens,
+                           int32_t *sel_pages, int32_t *sel_count, int32_t max_sel, void *kbuf, void *vbuf,
+                           int32_t *buf_len, float scale, float *O, void *ws, size_t ws_bytes,
+                           int32_t *err_dev, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ICE_H_ */

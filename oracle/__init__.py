@@ -145,7 +145,7 @@ def assign(K, e, parent_tok) -> np.ndarray:
 
 def page_capacity(N: int, Np: int, S: int) -> int:
     """Upper bound on pages: sum_m ceil(c_m / S) <= (N + (S-1) Np) / S."""
-    return (N + (S - 1) * Np + S - 1) // S
+    return (N + (S - 1) * Np) // S
 
 
 def pack(token_parent, Np: int, S: int, page_cap: int | None = None) -> dict:

@@ -1,0 +1,319 @@
+"""Python binding of the IceCache GB300 library (libice.so, C ABI in include/ice.h).
+
+Argument marshalling only: every function below has the name of the C entry
+point it calls, turns torch tensors into raw device pointers and the current
+torch CUDA stream into a cudaStream_t, and raises IceError on a non-zero
+status.  Every step of the hot path runs in the library's CUDA kernels; there
+is no CPU or PyTorch fallback, and importing this package fails loudly when
+libice.so has not been built (``python semantic_paged_kv_gb300/build.py``).
+
+PyTorch serves only as the allocator of device memory and as the source of
+streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import math
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libice.so")
+
+ICE_OK, ICE_ERR_INVALID_ARG, ICE_ERR_CUDA, ICE_ERR_OOM, ICE_ERR_CAPACITY, ICE_ERR_TIMEOUT, ICE_ERR_UNSUPPORTED = range(7)
+ICE_BF16, ICE_FP32 = 0, 1
+HEAD_DIM, PAGE_SIZE = 128, 16
+
+
+class IceError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"[{status}] {msg}")
+        self.status = status
+
+
+class IceParams(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("n_tokens", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("n_levels", ctypes.c_int32), ("promote_thresh", ctypes.c_uint64),
+                ("seed", ctypes.c_uint64), ("layer", ctypes.c_int32), ("np_cap", ctypes.c_int32),
+                ("page_cap", ctypes.c_int32), ("n_cap", ctypes.c_int32)]
+
+
+INDEX_FIELDS = ["n_parents", "n_pages", "n_indexed", "m2", "parent_tok", "parent_keys", "parent_e", "parent_corr",
+                "parent_first_page", "parent_last_page", "parent_n_pages", "page_parent", "page_len", "page_next",
+                "page_tokens", "token_parent", "token_page", "token_slot", "pool_k", "pool_v"]
+
+
+class IceIndex(ctypes.Structure):
+    _fields_ = [(f, ctypes.c_void_p) for f in INDEX_FIELDS]
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libice.so from this package directory (never from elsewhere)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build the IceCache CUDA library first "
+                          "(python semantic_paged_kv_gb300/build.py or __graft_entry__.build())")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, i32, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+    pp, pi = ctypes.POINTER(IceParams), ctypes.POINTER(IceIndex)
+    sigs = {
+        "ice_status_string": ([i32], ctypes.c_char_p),
+        "ice_last_error": ([], ctypes.c_char_p),
+        "ice_version": ([], ctypes.c_char_p),
+        "ice_check": ([P, P], i32),
+        "ice_page_bound": ([i32, i32, i32], i32),
+        "ice_build_workspace_bytes": ([pp, ctypes.POINTER(sz)], i32),
+        "ice_build_index": ([pp, P, P, pi, P, sz, P, P], i32),
+        "ice_build_lift_promote": ([pp, P, pi, P, sz, P, P], i32),
+        "ice_build_assign": ([pp, P, pi, P, sz, P, P], i32),
+        "ice_build_assign_simt": ([pp, P, pi, P, sz, P, P], i32),
+        "ice_build_pack": ([pp, P, P, pi, P, sz, P, P], i32),
+        "ice_decode_workspace_bytes": ([pp, i32, i32, ctypes.POINTER(sz)], i32),
+        "ice_select_pages": ([pp, pi, P, i32, P, P, i32, P, sz, P, P], i32),
+        "ice_gather_pages": ([pp, pi, P, P, i32, P, P, P, P], i32),
+        "ice_sparse_attn_decode": ([pp, P, P, P, P, P, i32, f32, P, P, sz, P], i32),
+        "ice_decode_step": ([pp, pi, P, i32, P, P, i32, P, P, P, f32, P, P, sz, P, P], i32),
+    }
+    for name, (args, res) in sigs.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def exported_symbols() -> list[str]:
+    return ["ice_status_string", "ice_last_error", "ice_version", "ice_check", "ice_page_bound",
+            "ice_build_workspace_bytes", "ice_build_index", "ice_build_lift_promote", "ice_build_assign",
+            "ice_build_assign_simt", "ice_build_pack", "ice_decode_workspace_bytes", "ice_select_pages",
+            "ice_gather_pages", "ice_sparse_attn_decode", "ice_decode_step"]
+
+
+# ----------------------------------------------------------- marshalling --
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, torch.Tensor):
+        return x.data_ptr()
+    return int(x)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(status: int):
+    if status != ICE_OK:
+        lib = load()
+        raise IceError(status, lib.ice_last_error().decode())
+
+
+def promote_threshold(p: float) -> int:
+    return int(math.floor(p * 4294967296.0))
+
+
+@dataclasses.dataclass
+class Config:
+    """Shapes of one layer's index (mirrors ice_params)."""
+    batch: int
+    n_q_heads: int
+    n_kv_heads: int
+    n_tokens: int
+    dtype: int = ICE_BF16
+    promote_p: float = 1.0 / 16.0
+    seed: int = 0
+    layer: int = 0
+    np_cap: int | None = None
+    page_cap: int | None = None
+    n_cap: int | None = None
+    head_dim: int = HEAD_DIM
+    page_size: int = PAGE_SIZE
+    n_levels: int = 2
+
+    def __post_init__(self):
+        N, p = self.n_tokens, self.promote_p
+        if self.n_cap is None:
+            self.n_cap = max(N, 1)
+        if self.np_cap is None:
+            # expected promoted count plus 8 standard deviations (a device-side
+            # capacity error reports the rare case that needs more)
+            mu = self.n_cap * p
+            self.np_cap = max(1, min(self.n_cap, int(mu + 8 * math.sqrt(mu * (1 - p) + 1) + 16)))
+        if self.page_cap is None:
+            self.page_cap = max(1, ice_page_bound(self.n_cap, self.np_cap, self.page_size))
+
+    @property
+    def group(self) -> int:
+        return self.n_q_heads // self.n_kv_heads
+
+    @property
+    def units(self) -> int:
+        return self.batch * self.n_kv_heads
+
+    @property
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == ICE_BF16 else torch.float32
+
+    def params(self) -> IceParams:
+        return IceParams(self.batch, self.n_q_heads, self.n_kv_heads, self.head_dim, self.n_tokens, self.page_size,
+                         self.dtype, self.n_levels, promote_threshold(self.promote_p), self.seed, self.layer,
+                         self.np_cap, self.page_cap, self.n_cap)
+
+
+class Index:
+    """Device arrays of one layer's index, allocated with torch (caller-owned
+    memory in the C ABI's terms)."""
+
+    def __init__(self, cfg: Config, device="cuda", pool_device=None):
+        U, Np, Pc, Nc, S, d = cfg.units, cfg.np_cap, cfg.page_cap, cfg.n_cap, cfg.page_size, cfg.head_dim
+        i32, dt = torch.int32, cfg.torch_dtype
+        z = lambda shape, t: torch.zeros(shape, dtype=t, device=device)
+        self.cfg = cfg
+        self.n_parents, self.n_pages, self.n_indexed = z(U, i32), z(U, i32), z(U, i32)
+        self.m2 = z(U, torch.float64)
+        self.parent_tok = z((U, Np), i32)
+        self.parent_keys = z((U, Np, d), dt)
+        self.parent_e = z((U, Np), torch.float32)
+        self.parent_corr = z((U, Np), torch.float32)
+        self.parent_first_page, self.parent_last_page, self.parent_n_pages = z((U, Np), i32), z((U, Np), i32), z((U, Np), i32)
+        self.page_parent, self.page_len, self.page_next = z((U, Pc), i32), z((U, Pc), i32), z((U, Pc), i32)
+        self.page_tokens = z((U, Pc, S), i32)
+        self.token_parent, self.token_page, self.token_slot = z((U, Nc), i32), z((U, Nc), i32), z((U, Nc), i32)
+        pd = device if pool_device is None else pool_device
+        self.pool_k = torch.zeros((U, Pc, S, d), dtype=dt, device=pd)
+        self.pool_v = torch.zeros((U, Pc, S, d), dtype=dt, device=pd)
+        self._struct = IceIndex(*[getattr(self, f).data_ptr() for f in INDEX_FIELDS])
+
+    @property
+    def struct(self) -> IceIndex:
+        return self._struct
+
+
+# ------------------------------------------------------- entry points -----
+def ice_version() -> str:
+    return load().ice_version().decode()
+
+
+def ice_status_string(s: int) -> str:
+    return load().ice_status_string(s).decode()
+
+
+def ice_page_bound(n_tokens: int, n_parents: int, page_size: int = PAGE_SIZE) -> int:
+    return int(load().ice_page_bound(n_tokens, n_parents, page_size))
+
+
+def ice_check(err_dev, stream=None) -> int:
+    """Synchronise, read and clear the device error word; returns its status."""
+    return int(load().ice_check(_ptr(err_dev), _stream(stream)))
+
+
+def ice_build_workspace_bytes(params: IceParams) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().ice_build_workspace_bytes(ctypes.byref(params), ctypes.byref(n)))
+    return n.value
+
+
+def ice_decode_workspace_bytes(params: IceParams, budget_tokens: int, max_sel: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().ice_decode_workspace_bytes(ctypes.byref(params), budget_tokens, max_sel, ctypes.byref(n)))
+    return n.value
+
+
+def _build_call(name, params, K, V, index, ws, err, stream):
+    fn = getattr(load(), name)
+    ix = index.struct if isinstance(index, Index) else index
+    args = [ctypes.byref(params), _ptr(K)]
+    if V is not None:
+        args.append(_ptr(V))
+    args += [ctypes.byref(ix), _ptr(ws), ws.numel() * ws.element_size() if isinstance(ws, torch.Tensor) else 0,
+             _ptr(err), _stream(stream)]
+    _check(fn(*args))
+
+
+def ice_build_index(params, K, V, index, ws, err, stream=None):
+    _build_call("ice_build_index", params, K, V, index, ws, err, stream)
+
+
+def ice_build_lift_promote(params, K, index, ws, err, stream=None):
+    _build_call("ice_build_lift_promote", params, K, None, index, ws, err, stream)
+
+
+def ice_build_assign(params, K, index, ws, err, stream=None):
+    _build_call("ice_build_assign", params, K, None, index, ws, err, stream)
+
+
+def ice_build_assign_simt(params, K, index, ws, err, stream=None):
+    _build_call("ice_build_assign_simt", params, K, None, index, ws, err, stream)
+
+
+def ice_build_pack(params, K, V, index, ws, err, stream=None):
+    _build_call("ice_build_pack", params, K, V, index, ws, err, stream)
+
+
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size() if isinstance(t, torch.Tensor) else 0
+
+
+def ice_select_pages(params, index, Q, budget_tokens, sel_pages, sel_count, ws, err, stream=None):
+    ix = index.struct if isinstance(index, Index) else index
+    _check(load().ice_select_pages(ctypes.byref(params), ctypes.byref(ix), _ptr(Q), budget_tokens, _ptr(sel_pages),
+                                   _ptr(sel_count), sel_pages.shape[-1], _ptr(ws), _nbytes(ws), _ptr(err),
+                                   _stream(stream)))
+
+
+def ice_gather_pages(params, index, sel_pages, sel_count, kbuf, vbuf, buf_len, stream=None):
+    ix = index.struct if isinstance(index, Index) else index
+    _check(load().ice_gather_pages(ctypes.byref(params), ctypes.byref(ix), _ptr(sel_pages), _ptr(sel_count),
+                                   sel_pages.shape[-1], _ptr(kbuf), _ptr(vbuf), _ptr(buf_len), _stream(stream)))
+
+
+def ice_sparse_attn_decode(params, Q, kbuf, vbuf, buf_len, sel_count, scale, O, ws, stream=None):
+    _check(load().ice_sparse_attn_decode(ctypes.byref(params), _ptr(Q), _ptr(kbuf), _ptr(vbuf), _ptr(buf_len),
+                                         _ptr(sel_count), buf_len.shape[-1], float(scale), _ptr(O), _ptr(ws),
+                                         _nbytes(ws), _stream(stream)))
+
+
+def ice_decode_step(params, index, Q, budget_tokens, sel_pages, sel_count, kbuf, vbuf, buf_len, scale, O, ws, err,
+                    stream=None):
+    ix = index.struct if isinstance(index, Index) else index
+    _check(load().ice_decode_step(ctypes.byref(params), ctypes.byref(ix), _ptr(Q), budget_tokens, _ptr(sel_pages),
+                                  _ptr(sel_count), sel_pages.shape[-1], _ptr(kbuf), _ptr(vbuf), _ptr(buf_len),
+                                  float(scale), _ptr(O), _ptr(ws), _nbytes(ws), _ptr(err), _stream(stream)))
+
+
+# ----------------------------------------------------- buffer helpers -----
+def workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """A 256-byte aligned device workspace (torch's allocator aligns to 512)."""
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def max_selected(cfg: Config, budget_tokens: int) -> int:
+    k = -(-budget_tokens // cfg.page_size)
+    return max(1, min(cfg.group * k, cfg.page_cap))
+
+
+class DecodeBuffers:
+    """Outputs of one decode step for a config and budget."""
+
+    def __init__(self, cfg: Config, budget_tokens: int, device="cuda"):
+        U, S, d = cfg.units, cfg.page_size, cfg.head_dim
+        self.max_sel = max_selected(cfg, budget_tokens)
+        self.sel_pages = torch.full((U, self.max_sel), -1, dtype=torch.int32, device=device)
+        self.sel_count = torch.zeros(U, dtype=torch.int32, device=device)
+        self.kbuf = torch.zeros((U, self.max_sel, S, d), dtype=cfg.torch_dtype, device=device)
+        self.vbuf = torch.zeros((U, self.max_sel, S, d), dtype=cfg.torch_dtype, device=device)
+        self.buf_len = torch.zeros((U, self.max_sel), dtype=torch.int32, device=device)
+        self.O = torch.zeros((cfg.batch, cfg.n_q_heads, d), dtype=torch.float32, device=device)
+        self.ws = workspace(ice_decode_workspace_bytes(cfg.params(), budget_tokens, self.max_sel), device)

@@ -1,0 +1,97 @@
+// Internal helpers shared by the sm_103a kernels of the IceCache library.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ice.h"
+
+namespace ice {
+
+constexpr int kHeadDim = 128;  // d
+constexpr int kPage = 16;      // S
+
+// ---------------------------------------------------------------- errors --
+// First device-side condition wins; later ones are dropped.
+__device__ __forceinline__ void set_err(int32_t *err, int32_t code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+// ------------------------------------------------------------ element I/O --
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static constexpr int kPerVec = 4;  // elements per 16-byte vector
+    __device__ __forceinline__ static void unpack(const uint4 &v, float *f) {
+        f[0] = __uint_as_float(v.x);
+        f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z);
+        f[3] = __uint_as_float(v.w);
+    }
+    __device__ __forceinline__ static float load(const float *p) { return *p; }
+};
+template <> struct Elem<__nv_bfloat16> {
+    static constexpr int kPerVec = 8;
+    __device__ __forceinline__ static void unpack(const uint4 &v, float *f) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    }
+    __device__ __forceinline__ static float load(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+};
+
+// Bytes of one d-element row.
+template <typename T> constexpr int row_bytes() { return kHeadDim * (int)sizeof(T); }
+// 16-byte vectors per row.
+template <typename T> constexpr int row_vecs() { return row_bytes<T>() / 16; }
+
+// ------------------------------------------------------------ splitmix64 --
+// splitmix64 (Steele, Lea & Flood 2014): state advances by the golden-ratio
+// increment; an output is the state run through the 64-bit finaliser.
+__host__ __device__ __forceinline__ uint64_t sm64_finalise(uint64_t z) {
+    z ^= z >> 30;
+    z *= 0xBF58476D1CE4E5B9ull;
+    z ^= z >> 27;
+    z *= 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+__host__ __device__ __forceinline__ uint64_t sm64_output(uint64_t state0, uint64_t n) {
+    return sm64_finalise(state0 + n * 0x9E3779B97F4A7C15ull);
+}
+// Stream key of one layer: output (layer + 1) of the stream seeded by seed.
+__host__ __device__ __forceinline__ uint64_t promote_key(uint64_t seed, int32_t layer) {
+    return sm64_output(seed, (uint64_t)(int64_t)layer + 1ull);
+}
+// Level-`level` promotion draw of `token` in unit (seq, head).
+__device__ __forceinline__ uint32_t promote_draw(uint64_t key, int32_t seq, int32_t head, uint32_t token,
+                                                 uint32_t level) {
+    const uint64_t ctr = (uint64_t)token | ((uint64_t)level << 32) | ((uint64_t)(uint32_t)head << 40) |
+                         ((uint64_t)(uint32_t)seq << 52);
+    return (uint32_t)(sm64_output(key, ctr + 1ull) >> 32);
+}
+
+// ------------------------------------------------- double-float summation --
+// Error-free transformation of a + b (Knuth's two-sum).
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+    s = a + b;
+    const float bb = s - a;
+    e = (a - (s - bb)) + (b - bb);
+}
+
+// ------------------------------------------------------------ warp utils --
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// (score, index) order used by every argmax / top-k here: larger score first,
+// lower index on equal scores.
+__device__ __forceinline__ bool better(float sa, int ia, float sb, int ib) {
+    return sa > sb || (sa == sb && ia < ib);
+}
+
+}  // namespace ice

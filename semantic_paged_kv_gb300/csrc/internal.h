@@ -1,0 +1,70 @@
+// Internal launch interface between the C ABI layer (abi.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "ice.h"
+
+namespace ice {
+
+// Tokens per tile of the lift/promotion kernels and of the page-packing kernels.
+constexpr int kLiftTile = 2048;
+constexpr int kPackTile = 2048;
+// Parents per CTA of the selection scan.
+constexpr int kSelChunk = 256;
+// Selected pages per CTA of the split attention.
+constexpr int kAttnPagesPerSplit = 4;
+// Largest parent count whose per-tile histogram fits in shared memory.
+constexpr int kPackSmemBins = 12288;
+
+inline int units_of(const ice_params &p) { return p.batch * p.n_kv_heads; }
+inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+// ------------------------------------------------ workspace layouts -------
+struct BuildWs {
+    double *norm2;        // [U, N]  |k_j|^2 (double)
+    int32_t *pcount;      // [U, Tp] promoted tokens per lift tile
+    unsigned long long *minpack;  // [U] min over tokens of draw << 32 | token
+    int32_t *pack_cnt;    // [U, Tk, np_cap] per-tile parent counts -> offsets
+    int32_t *pack_total;  // [U, np_cap] tokens per parent
+    size_t bytes;
+};
+BuildWs build_ws_layout(const ice_params &p, void *base);
+
+struct DecodeWs {
+    int32_t *sel_ticket;   // [U]
+    int32_t *attn_ticket;  // [U]
+    float *cand_score;     // [U, n_chunks, g, k]
+    int32_t *cand_id;      // [U, n_chunks, g, k]
+    float *part_ml;        // [U, n_splits, g, 2]  running max, running sum
+    float *part_o;         // [U, n_splits, g, d]
+    int n_chunks, k_pages, n_splits;
+    size_t bytes;
+};
+DecodeWs decode_ws_layout(const ice_params &p, int budget_tokens, int max_sel, void *base);
+
+// --------------------------------------------------------- launchers ------
+// Each returns cudaGetLastError() after enqueueing its kernels.
+cudaError_t launch_lift_promote(const ice_params &p, const void *K, const ice_index &idx, const BuildWs &ws,
+                                int32_t *err, cudaStream_t s);
+cudaError_t launch_assign_simt(const ice_params &p, const void *K, const ice_index &idx, const BuildWs &ws,
+                               int32_t *err, cudaStream_t s);
+cudaError_t launch_assign_tc(const ice_params &p, const void *K, const ice_index &idx, const BuildWs &ws,
+                             int32_t *err, cudaStream_t s);
+cudaError_t launch_pack(const ice_params &p, const void *K, const void *V, const ice_index &idx,
+                        const BuildWs &ws, int32_t *err, cudaStream_t s);
+cudaError_t launch_select(const ice_params &p, const ice_index &idx, const void *Q, const DecodeWs &ws,
+                          int32_t *sel_pages, int32_t *sel_count, int max_sel, int32_t *err, cudaStream_t s);
+cudaError_t launch_gather(const ice_params &p, const ice_index &idx, const int32_t *sel_pages,
+                          const int32_t *sel_count, int max_sel, void *kbuf, void *vbuf, int32_t *buf_len,
+                          cudaStream_t s);
+// pool == nullptr: attention over kbuf/vbuf/buf_len (step a10 alone).
+// pool != nullptr: each CTA first copies its selected pages from the pool to
+// kbuf/vbuf/buf_len (step a9) and attends over that copy (fused a9 + a10).
+cudaError_t launch_attention(const ice_params &p, const ice_index *pool, const int32_t *sel_pages,
+                             const void *Q, void *kbuf, void *vbuf, int32_t *buf_len, const int32_t *sel_count,
+                             int max_sel, float scale, float *O, const DecodeWs &ws, cudaStream_t s);
+
+}  // namespace ice

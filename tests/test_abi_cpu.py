@@ -1,0 +1,79 @@
+"""CPU-side checks of the C ABI library: it builds for sm_103a, loads without
+a GPU, exports every function include/ice.h declares, and its host-only
+entry points behave; the product package and the oracle share no code."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import semantic_paged_kv_gb300 as ice
+from semantic_paged_kv_gb300 import build as icebuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    icebuild.build()
+    return ice.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "ice.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(ice_[a-z0-9_]+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_function_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(ice.exported_symbols()) == names
+
+
+def test_host_only_entry_points(lib):
+    assert "sm_103a" in ice.ice_version()
+    assert ice.ice_status_string(ice.ICE_ERR_CAPACITY) == "capacity exceeded"
+    assert ice.ice_page_bound(1000, 1, 16) == 63
+    assert ice.ice_page_bound(1000, 100, 16) == (1000 + 15 * 100) // 16
+    cfg = ice.Config(batch=2, n_q_heads=8, n_kv_heads=2, n_tokens=5000)
+    assert ice.ice_build_workspace_bytes(cfg.params()) > 2 * 2 * 5000 * 8
+    assert ice.ice_decode_workspace_bytes(cfg.params(), 256, 64) > 0
+
+
+@pytest.mark.parametrize("field,value,status", [("head_dim", 64, ice.ICE_ERR_UNSUPPORTED),
+                                                 ("page_size", 8, ice.ICE_ERR_UNSUPPORTED),
+                                                 ("n_levels", 3, ice.ICE_ERR_UNSUPPORTED),
+                                                 ("n_kv_heads", 3, ice.ICE_ERR_INVALID_ARG),
+                                                 ("dtype", 7, ice.ICE_ERR_INVALID_ARG),
+                                                 ("promote_thresh", 2 ** 32 + 1, ice.ICE_ERR_INVALID_ARG),
+                                                 ("n_cap", 10, ice.ICE_ERR_INVALID_ARG)])
+def test_invalid_params_rejected_on_host(lib, field, value, status):
+    p = ice.Config(batch=1, n_q_heads=8, n_kv_heads=2, n_tokens=100).params()
+    setattr(p, field, value)
+    with pytest.raises(ice.IceError) as ei:
+        ice.ice_build_workspace_bytes(p)
+    assert ei.value.status == status
+    assert lib.ice_last_error().decode()
+
+
+def test_struct_layouts_match_header():
+    assert ctypes.sizeof(ice.IceParams) == 64
+    assert ctypes.sizeof(ice.IceIndex) == 20 * 8
+
+
+def test_product_never_touches_the_oracle():
+    pkg = os.path.join(ROOT, "semantic_paged_kv_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                txt = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert not re.search(r"\bimport\s+oracle\b|\bfrom\s+oracle\b|oracle\.c|liboracle|orc_", txt), f
+    for f in os.listdir(os.path.join(ROOT, "oracle")):
+        if f.endswith((".py", ".c", ".h")):
+            txt = open(os.path.join(ROOT, "oracle", f), encoding="utf-8").read()
+            assert not re.search(r"\bimport\s+semantic_paged_kv_gb300|\bfrom\s+semantic_paged_kv_gb300|"
+                                 r"#\s*include\s*[<\"].*(ice\.h|\.cuh)", txt), f

@@ -1,0 +1,166 @@
+"""GPU parity of every step of the hot path against the CPU oracle, called
+through the C ABI (libice.so) on seeded workloads shaped like the pages'
+models: small enough for the oracle to finish in seconds, large enough to
+span several tiles and a ragged tail, plus the edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import semantic_paged_kv_gb300 as ice
+import workloads
+from parity_util import GpuRun, check_build_unit, check_decode_unit, to_dev
+
+pytestmark = pytest.mark.gpu
+
+W = workloads.WORKLOADS
+
+
+def _all_units(run, budgets, fused=True, sample=None):
+    for u in range(run.cfg.units):
+        check_build_unit(run, u, sample_tokens=sample)
+    for bgt in budgets:
+        Q, buf, st = run.decode(bgt, fused=fused)
+        assert st == ice.ICE_OK
+        for u in range(run.cfg.units):
+            check_decode_unit(run, u, Q, bgt, buf)
+
+
+def test_tiny_fp32_full():
+    """The tiny fp32 workload (1 KV head, 4 query heads, N = 2048) end to end."""
+    run = GpuRun(W["tiny"])
+    assert run.status == ice.ICE_OK
+    _all_units(run, [64, 128], fused=True)
+    _all_units(run, [64], fused=False)
+
+
+@pytest.mark.parametrize("assign", ["auto", "simt"])
+def test_llama_shaped_bf16_ragged(assign):
+    """Llama-3.1-8B head layout (g = 4), bf16, a ragged N spanning several
+    2048-token tiles and 128-row tiles, two sequences, needle planted."""
+    w = W["llama31_8b_16k"].scaled(n_tokens=5003, batch=2, n_q_heads=8, n_kv_heads=2)
+    run = GpuRun(w, assign=assign)
+    assert run.status == ice.ICE_OK
+    _all_units(run, [64, 128, 256])
+
+
+def test_many_parent_tiles_ring_wrap():
+    """Np ~ 750 parents: three 256-parent MMA tiles per CTA, so the shared-memory
+    ring and the two TMEM accumulators are reused; assignment checked on a
+    seeded sample of tokens, everything else on all tokens."""
+    w = W["llama31_8b_16k"].scaled(n_tokens=12003, n_q_heads=4, n_kv_heads=1)
+    run = GpuRun(w)
+    assert run.status == ice.ICE_OK
+    _all_units(run, [256], sample=3000)
+
+
+def test_llama_full_size_sampled():
+    """The full Llama-3.1-8B-shaped layer (32 query / 8 KV heads, N = 16384,
+    needle) in the launch configuration the benchmark times: promotion, pages,
+    pool and decode checked in full, the assignment on 1500 sampled tokens per
+    unit."""
+    run = GpuRun(W["llama31_8b_16k"])
+    assert run.status == ice.ICE_OK
+    _all_units(run, [64, 128, 256], sample=1500)
+
+
+def test_fused_decode_equals_separate_calls():
+    w = W["llama31_8b_16k"].scaled(n_tokens=3000, n_q_heads=8, n_kv_heads=2)
+    run = GpuRun(w)
+    Q1, a, _ = run.decode(128, fused=True)
+    Q2, b, _ = run.decode(128, fused=False)
+    for x, y in [(a.sel_pages, b.sel_pages), (a.sel_count, b.sel_count), (a.kbuf, b.kbuf), (a.vbuf, b.vbuf),
+                 (a.buf_len, b.buf_len), (a.O, b.O)]:
+        assert torch.equal(x, y)
+
+
+def test_qwen_shaped_g8_mha_longchat_shaped_g1():
+    for w in (W["qwen3_32b_100k"].scaled(n_tokens=4100, batch=2, n_q_heads=16, n_kv_heads=2, centres=512),
+              W["longchat_7b_100k"].scaled(n_tokens=4100, batch=1, n_q_heads=3, n_kv_heads=3, centres=512)):
+        run = GpuRun(w)
+        assert run.status == ice.ICE_OK
+        _all_units(run, [64, 256])
+
+
+def test_promote_all_is_exact_topk_mips():
+    """p = 1: one-token pages, so selection is exact top-k inner product search."""
+    w = W["tiny"].scaled(n_tokens=700, promote_p=1.0)
+    run = GpuRun(w)
+    assert run.status == ice.ICE_OK
+    assert int(run.h["n_pages"][0]) == 700
+    _all_units(run, [16 * 5, 16 * 40])
+    Q, buf, _ = run.decode(16 * 9)
+    s = torch.tensor(Q[0], dtype=torch.float64) @ torch.tensor(run.K[0, 0], dtype=torch.float64).T
+    top = torch.topk(s, 9, dim=1).indices
+    got = set(buf.sel_pages[0, : int(buf.sel_count[0])].cpu().tolist())
+    toks = set(run.h["page_tokens"][0, sorted(got), 0].tolist())
+    assert toks == set(top.reshape(-1).tolist())
+
+
+def test_promote_none_is_sequential_paging():
+    """p = 0: one parent (the smallest draw), so pages are sequential 16-token pages."""
+    w = W["tiny"].scaled(n_tokens=1000, promote_p=0.0)
+    run = GpuRun(w)
+    assert int(run.h["n_parents"][0]) == 1
+    assert np.array_equal(run.h["token_page"][0, :1000], np.arange(1000) // 16)
+    _all_units(run, [64])
+
+
+def test_full_budget_is_dense_attention():
+    w = W["llama31_8b_16k"].scaled(n_tokens=2500, n_q_heads=8, n_kv_heads=2)
+    run = GpuRun(w)
+    P = int(run.h["n_pages"].max())
+    Q, buf, _ = run.decode(16 * P)
+    for u in range(run.cfg.units):
+        assert int(buf.sel_count[u]) == int(run.h["n_pages"][u])
+    q = torch.tensor(Q, dtype=torch.float64).reshape(1, 2, 4, 128)
+    K = torch.tensor(run.K[0], dtype=torch.float64)[:, None].expand(2, 4, -1, -1)
+    V = torch.tensor(run.V[0], dtype=torch.float64)[:, None].expand(2, 4, -1, -1)
+    dense = torch.nn.functional.scaled_dot_product_attention(q[0][:, :, None], K, V)[:, :, 0].reshape(8, 128)
+    assert torch.max(torch.abs(buf.O[0].double().cpu() - dense)) < 2e-3
+
+
+@pytest.mark.parametrize("n", [0, 1, 17, 2049])
+def test_small_and_empty_units(n):
+    w = W["tiny"].scaled(n_tokens=n)
+    run = GpuRun(w, n_cap=max(n, 1))
+    assert run.status == ice.ICE_OK
+    _all_units(run, [64])
+
+
+def test_needle_page_selected_at_every_budget():
+    """Behavioural check from the passkey claim: the planted needle key's page
+    is selected for its query head at budgets 64/128/256."""
+    w = W["llama31_8b_16k"].scaled(n_tokens=6000, n_q_heads=8, n_kv_heads=2)
+    run = GpuRun(w)
+    for bgt in (64, 128, 256):
+        Q, buf, _ = run.decode(bgt)
+        for u in range(run.cfg.units):
+            pos = workloads.needle_position(w, 0, 0, u, 6000)
+            page = int(run.h["token_page"][u, pos])
+            got = buf.sel_pages[u, : int(buf.sel_count[u])].cpu().tolist()
+            assert page in got
+
+
+def test_capacity_error_is_reported_not_overrun():
+    w = W["tiny"].scaled(n_tokens=3000)
+    run = GpuRun(w, np_cap=20, page_cap=200)
+    assert run.status == ice.ICE_ERR_CAPACITY
+    assert int(run.h["n_parents"][0]) == 20
+
+
+def test_invalid_arguments_rejected():
+    cfg = ice.Config(batch=1, n_q_heads=4, n_kv_heads=1, n_tokens=64)
+    p = cfg.params()
+    p.head_dim = 64
+    with pytest.raises(ice.IceError) as ei:
+        ice.ice_build_workspace_bytes(p)
+    assert ei.value.status == ice.ICE_ERR_UNSUPPORTED
+    p = cfg.params()
+    idx = ice.Index(cfg)
+    K = torch.zeros((1, 1, 64, 128), dtype=torch.bfloat16, device="cuda")
+    small = ice.workspace(256)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    with pytest.raises(ice.IceError) as ei:
+        ice.ice_build_index(p, K, K, idx, small, err)
+    assert ei.value.status == ice.ICE_ERR_INVALID_ARG
