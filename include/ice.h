@@ -253,6 +253,36 @@ ice_status ice_sparse_attn_decode(const ice_params *p, const void *Q, const void
                                   float scale, float *O, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * Allocation-free variant of ice_sparse_attn_decode.  The paper has no
+ * counterpart: this entry point exists for callers that cannot call
+ * cudaMalloc, such as a plugin inside a serving runtime that owns every byte
+ * of device memory through its own pool and forbids raw allocations, or a
+ * decode loop that cannot afford the implicit device-wide synchronisation of
+ * an allocation.  It takes no workspace: its scratch (one ticket word per
+ * unit and the per-split partial results) lives in a device array of
+ * ICE_NOALLOC_SCRATCH_BYTES bytes that the library defines statically, which
+ * every GPU that loads the library holds until the process exits.
+ *  - Same arguments (minus the workspace), layouts and results as
+ *    ice_sparse_attn_decode.  The caller still owns Q, kbuf, vbuf, buf_len,
+ *    sel_count and O.
+ *  - A shape whose scratch exceeds ICE_NOALLOC_SCRATCH_BYTES is rejected
+ *    with ICE_ERR_CAPACITY before anything is launched (about
+ *    U * ceil(max_sel / 4) * g * 520 bytes are needed).
+ *  - The first call on a device looks up the array's device address with
+ *    that device current (cudaGetSymbolAddress) and caches it; make that
+ *    first call before any stream capture.
+ *  - It calls no cudaMalloc, cudaFree or allocating library routine.
+ *  - Every call on a device shares the one array, which keeps the last
+ *    call's contents; the ticket words are cleared on the stream at the start
+ *    of each call.  Calls whose executions overlap on the GPU (different
+ *    streams, or different host threads) race on the array: order them.
+ */
+#define ICE_NOALLOC_SCRATCH_BYTES (8u << 20)
+ice_status ice_sparse_attn_decode_noalloc(const ice_params *p, const void *Q, const void *kbuf, const void *vbuf,
+                                          const int32_t *buf_len, const int32_t *sel_count, int32_t max_sel,
+                                          float scale, float *O, void *stream);
+
+/*
  * The whole decode step a6-a10 in two launches: ice_select_pages, then one
  * kernel that reads each selected page once from the pool, writes it to
  * kbuf/vbuf/buf_len (the contiguous buffer of step a9) and computes the

@@ -81,6 +81,7 @@ def load() -> ctypes.CDLL:
         "ice_gather_pages": ([pp, pi, P, P, i32, P, P, P, P], i32),
         "ice_sparse_attn_decode": ([pp, P, P, P, P, P, i32, f32, P, P, sz, P], i32),
         "ice_decode_step": ([pp, pi, P, i32, P, P, i32, P, P, P, f32, P, P, sz, P, P], i32),
+        "ice_sparse_attn_decode_noalloc": ([pp, P, P, P, P, P, i32, f32, P, P], i32),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -94,7 +95,7 @@ def exported_symbols() -> list[str]:
     return ["ice_status_string", "ice_last_error", "ice_version", "ice_check", "ice_page_bound",
             "ice_build_workspace_bytes", "ice_build_index", "ice_build_lift_promote", "ice_build_assign",
             "ice_build_assign_simt", "ice_build_pack", "ice_decode_workspace_bytes", "ice_select_pages",
-            "ice_gather_pages", "ice_sparse_attn_decode", "ice_decode_step"]
+            "ice_gather_pages", "ice_sparse_attn_decode", "ice_sparse_attn_decode_noalloc", "ice_decode_step"]
 
 
 # ----------------------------------------------------------- marshalling --
@@ -283,6 +284,14 @@ def ice_sparse_attn_decode(params, Q, kbuf, vbuf, buf_len, sel_count, scale, O, 
     _check(load().ice_sparse_attn_decode(ctypes.byref(params), _ptr(Q), _ptr(kbuf), _ptr(vbuf), _ptr(buf_len),
                                          _ptr(sel_count), buf_len.shape[-1], float(scale), _ptr(O), _ptr(ws),
                                          _nbytes(ws), _stream(stream)))
+
+
+def ice_sparse_attn_decode_noalloc(params, Q, kbuf, vbuf, buf_len, sel_count, scale, O, stream=None):
+    """ice_sparse_attn_decode without a workspace: scratch in the library's
+    static device array (see ice.h for its limit and sharing rules)."""
+    _check(load().ice_sparse_attn_decode_noalloc(ctypes.byref(params), _ptr(Q), _ptr(kbuf), _ptr(vbuf), _ptr(buf_len),
+                                                 _ptr(sel_count), buf_len.shape[-1], float(scale), _ptr(O),
+                                                 _stream(stream)))
 
 
 def ice_decode_step(params, index, Q, budget_tokens, sel_pages, sel_count, kbuf, vbuf, buf_len, scale, O, ws, err,

@@ -328,6 +328,24 @@ ice_status ice_sparse_attn_decode(const ice_params *p, const void *Q, const void
                        "ice_sparse_attn_decode");
 }
 
+ice_status ice_sparse_attn_decode_noalloc(const ice_params *p, const void *Q, const void *kbuf, const void *vbuf,
+                                          const int32_t *buf_len, const int32_t *sel_count, int32_t max_sel,
+                                          float scale, float *O, void *stream) {
+    ice_status st = check_params(p);
+    if (st) return st;
+    if (max_sel < 1) return fail(ICE_ERR_INVALID_ARG, "max_sel must be >= 1");
+    if (!Q || !kbuf || !vbuf || !buf_len || !sel_count || !O)
+        return fail(ICE_ERR_INVALID_ARG, "attention needs non-NULL Q, kbuf, vbuf, buf_len, sel_count and O");
+    if (!aligned16(kbuf) || !aligned16(vbuf)) return fail(ICE_ERR_INVALID_ARG, "kbuf and vbuf must be 16-byte aligned");
+    const size_t need = attention_noalloc_bytes(*p, max_sel);
+    if (need > ICE_NOALLOC_SCRATCH_BYTES)
+        return fail(ICE_ERR_CAPACITY, "this shape needs %zu bytes of scratch; the allocation-free entry point has %u",
+                    need, (unsigned)ICE_NOALLOC_SCRATCH_BYTES);
+    return cuda_status(launch_attention_noalloc(*p, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O,
+                                                static_cast<cudaStream_t>(stream)),
+                       "ice_sparse_attn_decode_noalloc");
+}
+
 ice_status ice_decode_step(const ice_params *p, const ice_index *idx, const void *Q, int32_t budget_tokens,
                            int32_t *sel_pages, int32_t *sel_count, int32_t max_sel, void *kbuf, void *vbuf,
                            int32_t *buf_len, float scale, float *O, void *ws, size_t ws_bytes, int32_t *err_dev,

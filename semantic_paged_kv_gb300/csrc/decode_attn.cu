@@ -266,3 +266,59 @@ cudaError_t launch_attention(const ice_params &p, const ice_index *pool, const i
 }
 
 }  // namespace ice
+
+// ---------------------------------------------------------------------------
+// Allocation-free attention: the same split-KV kernel, with its scratch (one
+// ticket word per unit and the per-split partials) in a fixed device array
+// that the library owns, so the caller passes no workspace.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace ice {
+namespace {
+
+// Every GPU that loads the library holds this array until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[ICE_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the array on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up
+// once per device with that device current and cached.
+cudaError_t noalloc_scratch(void **out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+size_t attention_noalloc_bytes(const ice_params &p, int max_sel) {
+    return decode_ws_layout(p, 0, max_sel, nullptr).bytes;
+}
+
+cudaError_t launch_attention_noalloc(const ice_params &p, const void *Q, const void *kbuf, const void *vbuf,
+                                     const int32_t *buf_len, const int32_t *sel_count, int max_sel, float scale,
+                                     float *O, cudaStream_t s) {
+    void *base = nullptr;
+    cudaError_t e = noalloc_scratch(&base);
+    if (e != cudaSuccess) return e;
+    const DecodeWs ws = decode_ws_layout(p, 0, max_sel, base);
+    if (ws.bytes > ICE_NOALLOC_SCRATCH_BYTES) return cudaErrorInvalidValue;
+    return launch_attention(p, nullptr, nullptr, Q, const_cast<void *>(kbuf), const_cast<void *>(vbuf),
+                            const_cast<int32_t *>(buf_len), sel_count, max_sel, scale, O, ws, s);
+}
+
+}  // namespace ice

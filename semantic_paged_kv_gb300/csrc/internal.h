@@ -67,4 +67,10 @@ cudaError_t launch_attention(const ice_params &p, const ice_index *pool, const i
                              const void *Q, void *kbuf, void *vbuf, int32_t *buf_len, const int32_t *sel_count,
                              int max_sel, float scale, float *O, const DecodeWs &ws, cudaStream_t s);
 
+// Allocation-free attention: scratch in the library's static device array.
+size_t attention_noalloc_bytes(const ice_params &p, int max_sel);
+cudaError_t launch_attention_noalloc(const ice_params &p, const void *Q, const void *kbuf, const void *vbuf,
+                                     const int32_t *buf_len, const int32_t *sel_count, int max_sel, float scale,
+                                     float *O, cudaStream_t s);
+
 }  // namespace ice
