@@ -208,7 +208,11 @@ ice_status ice_build_pack(const ice_params *p, const void *K, const void *V, con
 
 /* ------------------------------------------------------- decode step ---- */
 /* Workspace bytes for ice_select_pages / ice_sparse_attn_decode /
- * ice_decode_step at this budget and output capacity max_sel. */
+ * ice_decode_step at this budget and output capacity max_sel.  A decode
+ * workspace must be zero-filled once before its first use: it holds one
+ * completion counter per unit and kernel, and every call that completes
+ * leaves those counters at zero again, so no call has to clear them.  Calls
+ * that share a workspace must not overlap on the GPU. */
 ice_status ice_decode_workspace_bytes(const ice_params *p, int32_t budget_tokens, int32_t max_sel,
                                       size_t *bytes);
 

@@ -304,8 +304,9 @@ def ice_decode_step(params, index, Q, budget_tokens, sel_pages, sel_count, kbuf,
 
 # ----------------------------------------------------- buffer helpers -----
 def workspace(nbytes: int, device="cuda") -> torch.Tensor:
-    """A 256-byte aligned device workspace (torch's allocator aligns to 512)."""
-    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+    """A zero-filled, 256-byte aligned device workspace (torch's allocator
+    aligns to 512); decode workspaces must start zeroed (see ice.h)."""
+    return torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
 
 
 def max_selected(cfg: Config, budget_tokens: int) -> int:

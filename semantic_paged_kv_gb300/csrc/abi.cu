@@ -98,7 +98,8 @@ BuildWs build_ws_layout(const ice_params &p, void *base) {
     };
     w.norm2 = reinterpret_cast<double *>(take(sizeof(double) * U * N));
     w.pcount = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * U * tp));
-    w.minpack = reinterpret_cast<unsigned long long *>(take(sizeof(unsigned long long) * U));
+    w.tile_max = reinterpret_cast<double *>(take(sizeof(double) * U * tp));
+    w.tile_min = reinterpret_cast<unsigned long long *>(take(sizeof(unsigned long long) * U * tp));
     w.pack_cnt = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * U * tk * (size_t)p.np_cap));
     w.pack_total = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * U * (size_t)p.np_cap));
     w.bytes = off;
@@ -122,8 +123,9 @@ DecodeWs decode_ws_layout(const ice_params &p, int budget_tokens, int max_sel, v
     };
     w.sel_ticket = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * U));
     w.attn_ticket = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * U));
-    w.cand_score = reinterpret_cast<float *>(take(sizeof(float) * U * w.n_chunks * g * (kc ? kc : 1)));
-    w.cand_id = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * U * w.n_chunks * g * (kc ? kc : 1)));
+    w.cand_key = reinterpret_cast<unsigned long long *>(
+        take(sizeof(unsigned long long) * U * w.n_chunks * g * (kc ? kc : 1)));
+    w.cand_span = reinterpret_cast<int4 *>(take(sizeof(int4) * U * w.n_chunks * kSelChunk));
     w.part_ml = reinterpret_cast<float *>(take(sizeof(float) * U * w.n_splits * g * 2));
     w.part_o = reinterpret_cast<float *>(take(sizeof(float) * U * w.n_splits * g * kHeadDim));
     w.bytes = off;

@@ -9,19 +9,27 @@
 // a dense contraction of the keys with the parent keys followed by a row
 // argmax.  bf16 products are exact in fp32; the sum is accumulated in fp32.
 //
-// One CTA per (128-token tile, unit), 6 warps, one CTA per SM:
-//   warp 0      TMA producer: the 128x128 key tile once, then the unit's
-//               parent keys in 256-row tiles through a 2-stage ring
-//               (128-byte swizzled, two 64-column halves per tile);
+// Persistent kernel, one CTA per SM (10 warps), looping over work items =
+// (unit, 128-token tile) in unit-major order, so that the CTAs working at
+// the same time share one unit's parent table in L2:
+//   warp 0      TMA producer: per item the 128x128 key tile into one of two
+//               key buffers, then the unit's parent keys in 256-row tiles
+//               through a 2-stage ring (128-byte swizzle, two 64-column
+//               halves per tile);
 //   warp 1      allocates 512 TMEM columns and issues tcgen05.mma
 //               (M=128, N=256, K=16, bf16 -> fp32) into one of two TMEM
-//               accumulators, committing to the ring's empty barrier and to
-//               the accumulator's full barrier;
-//   warps 2..5  epilogue: TMEM row = token, 32 columns per tcgen05.ld; score
-//               = acc + e_j e_m, running argmax with the lowest index on
-//               exact ties; releases the accumulator to the MMA warp.
-// Every mbarrier wait gives up after ~2 s (globaltimer), records
-// ICE_ERR_TIMEOUT, drains what it issued and frees TMEM before returning.
+//               accumulators, committing to the ring's empty barrier, the
+//               accumulator's full barrier and, after an item's last tile,
+//               the key buffer's empty barrier;
+//   warps 2..9  epilogue: warp w reads TMEM lane quarter w % 4 and column
+//               half (w - 2) / 4; 64 columns per tcgen05 wait; score =
+//               acc + e_j e_m, running argmax with the lowest index on exact
+//               ties; the two halves of a row combine through shared memory
+//               at the end of the item.  The parent coordinates e_m of the
+//               next tile are prefetched into registers.
+// Every mbarrier wait gives up after ~2 s (globaltimer) and records
+// ICE_ERR_TIMEOUT; roles drain what they issued and TMEM is freed before
+// the CTA returns.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -33,7 +41,9 @@ namespace {
 constexpr int BM = 128;      // tokens per CTA (TMEM lanes)
 constexpr int BN = 256;      // parents per MMA tile (TMEM columns per accumulator)
 constexpr int NSTAGE = 2;    // parent-tile ring depth
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kThreads = 64 + kEpiThreads;
 constexpr uint32_t A_HALF = BM * 128;     // 128 rows x 128 bytes (64 bf16 columns)
 constexpr uint32_t A_BYTES = 2 * A_HALF;  // d = 128 -> two halves
 constexpr uint32_t B_HALF = BN * 128;
@@ -45,10 +55,13 @@ constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >
                            ((uint32_t)(BM >> 4) << 24);
 
 struct Bars {
-    unsigned long long full[NSTAGE], empty[NSTAGE], a_full, tfull[2], tempty[2];
+    unsigned long long full[NSTAGE], empty[NSTAGE], a_full[2], a_empty[2], tfull[2], tempty[2];
+    float comb_s[BM];
+    int comb_i[BM];
     uint32_t tmem_base;
 };
-constexpr size_t kSmemBytes = 1024 /*align slack*/ + A_BYTES + NSTAGE * B_STAGE + 2 * BN * sizeof(float) + sizeof(Bars);
+constexpr size_t kSmemBytes =
+    1024 /*align slack*/ + 2 * A_BYTES + NSTAGE * B_STAGE + 2 * BN * sizeof(float) + sizeof(Bars);
 
 __device__ __forceinline__ uint32_t su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -113,8 +126,8 @@ __device__ __forceinline__ void umma_commit(unsigned long long *bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 32 consecutive fp32 TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+// 32 consecutive fp32 TMEM columns of this thread's lane (no wait).
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, float *v) {
     uint32_t r[32];
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -125,38 +138,49 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Work item -> (unit, first token) and the unit's parent-tile count.
+struct Item {
+    int u, m0, Np, T;
+};
+__device__ __forceinline__ Item item_of(int item, int mt_per_unit, const int32_t *n_parents, int np_cap) {
+    Item it;
+    it.u = item / mt_per_unit;
+    it.m0 = (item % mt_per_unit) * BM;
+    it.Np = min(n_parents[it.u], np_cap);
+    it.T = (it.Np + BN - 1) / BN;
+    return it;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     k_assign_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmP, int N, int np_cap,
-                int n_cap, const int32_t *__restrict__ n_parents, const double *__restrict__ m2,
-                const double *__restrict__ norm2, const float *__restrict__ parent_e,
-                int32_t *__restrict__ token_parent, int32_t *__restrict__ err) {
+                int n_cap, int n_items, int mt_per_unit, const int32_t *__restrict__ n_parents,
+                const double *__restrict__ m2, const double *__restrict__ norm2,
+                const float *__restrict__ parent_e, int32_t *__restrict__ token_parent, int32_t *__restrict__ err) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    unsigned char *sA = smem;
-    unsigned char *sB = smem + A_BYTES;
+    unsigned char *sA = smem;  // two key buffers
+    unsigned char *sB = smem + 2 * A_BYTES;
     float *sE = reinterpret_cast<float *>(sB + NSTAGE * B_STAGE);
     Bars *bars = reinterpret_cast<Bars *>(sE + 2 * BN);
 
-    const int u = blockIdx.y;
-    const int m0 = blockIdx.x * BM;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int Np = min(n_parents[u], np_cap);
-    const int T = (Np + BN - 1) / BN;
+    const int G = gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
             mbar_init(&bars->full[s], 1);
             mbar_init(&bars->empty[s], 1);
         }
-        mbar_init(&bars->a_full, 1);
         for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars->a_full[b], 1);
+            mbar_init(&bars->a_empty[b], 1);
             mbar_init(&bars->tfull[b], 1);
-            mbar_init(&bars->tempty[b], 4 * 32);
+            mbar_init(&bars->tempty[b], kEpiThreads);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -174,112 +198,172 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer
-        if (lane == 0 && T > 0) {
-            const int row0 = u * N + m0;
-            mbar_expect_tx(&bars->a_full, A_BYTES);
-            tma_load_2d(sA, &tmK, &bars->a_full, 0, row0);
-            tma_load_2d(sA + A_HALF, &tmK, &bars->a_full, 64, row0);
-            int issued = 0;
-            for (int t = 0; t < T; ++t) {
-                const int s = t % NSTAGE;
-                const uint32_t ph = (t / NSTAGE) & 1;
-                if (!mbar_wait(&bars->empty[s], ph ^ 1)) {
+        if (lane == 0) {
+            int gt = 0, it = 0;
+            int last_a = -1;
+            for (int item = blockIdx.x; ok && item < n_items; item += G, ++it) {
+                const Item I = item_of(item, mt_per_unit, n_parents, np_cap);
+                const int ab = it & 1;
+                if (!mbar_wait(&bars->a_empty[ab], ((it >> 1) & 1) ^ 1)) {
                     ok = false;
                     break;
                 }
-                unsigned char *dst = sB + s * B_STAGE;
-                const int y = u * np_cap + t * BN;
-                mbar_expect_tx(&bars->full[s], B_STAGE);
-                tma_load_2d(dst, &tmP, &bars->full[s], 0, y);
-                tma_load_2d(dst + B_HALF, &tmP, &bars->full[s], 64, y);
-                issued = t + 1;
+                unsigned char *a = sA + ab * A_BYTES;
+                mbar_expect_tx(&bars->a_full[ab], A_BYTES);
+                tma_load_2d(a, &tmK, &bars->a_full[ab], 0, I.u * N + I.m0);
+                tma_load_2d(a + A_HALF, &tmK, &bars->a_full[ab], 64, I.u * N + I.m0);
+                last_a = it;
+                for (int t = 0; t < I.T; ++t, ++gt) {
+                    const int s = gt % NSTAGE;
+                    if (!mbar_wait(&bars->empty[s], ((gt / NSTAGE) & 1) ^ 1)) {
+                        ok = false;
+                        break;
+                    }
+                    unsigned char *dst = sB + s * B_STAGE;
+                    const int y = I.u * np_cap + t * BN;
+                    mbar_expect_tx(&bars->full[s], B_STAGE);
+                    tma_load_2d(dst, &tmP, &bars->full[s], 0, y);
+                    tma_load_2d(dst + B_HALF, &tmP, &bars->full[s], 64, y);
+                }
             }
             // drain: every issued copy has landed before the CTA may exit
-            for (int t = (issued > NSTAGE ? issued - NSTAGE : 0); t < issued; ++t)
-                mbar_wait(&bars->full[t % NSTAGE], (t / NSTAGE) & 1);
-            mbar_wait(&bars->a_full, 0);
+            for (int g2 = (gt > NSTAGE ? gt - NSTAGE : 0); g2 < gt; ++g2)
+                mbar_wait(&bars->full[g2 % NSTAGE], (g2 / NSTAGE) & 1);
+            for (int a2 = (last_a > 0 ? last_a - 1 : 0); a2 <= last_a; ++a2)
+                mbar_wait(&bars->a_full[a2 & 1], (a2 >> 1) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
-        if (lane == 0 && T > 0) {
-            int issued = 0;
-            if (!mbar_wait(&bars->a_full, 0)) ok = false;
-            const uint32_t a0 = su32(sA);
-            for (int t = 0; ok && t < T; ++t) {
-                const int s = t % NSTAGE, b = t & 1;
-                const uint32_t ph = (t / NSTAGE) & 1, bph = (t >> 1) & 1;
-                if (!mbar_wait(&bars->tempty[b], bph ^ 1) || !mbar_wait(&bars->full[s], ph)) {
+        if (lane == 0) {
+            int gt = 0, it = 0;
+            for (int item = blockIdx.x; ok && item < n_items; item += G, ++it) {
+                const Item I = item_of(item, mt_per_unit, n_parents, np_cap);
+                const int ab = it & 1;
+                if (!mbar_wait(&bars->a_full[ab], (it >> 1) & 1)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                const uint32_t b0 = su32(sB + s * B_STAGE);
+                const uint32_t a0 = su32(sA + ab * A_BYTES);
+                for (int t = 0; t < I.T; ++t, ++gt) {
+                    const int s = gt % NSTAGE, b = gt & 1;
+                    if (!mbar_wait(&bars->tempty[b], ((gt >> 1) & 1) ^ 1) ||
+                        !mbar_wait(&bars->full[s], (gt / NSTAGE) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t b0 = su32(sB + s * B_STAGE);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t off = (k & 3) * 32;  // 16 bf16 columns inside the swizzle atom
-                    const uint64_t da = sw128_desc(a0 + (k >> 2) * A_HALF + off);
-                    const uint64_t db = sw128_desc(b0 + (k >> 2) * B_HALF + off);
-                    umma_bf16(tmem + b * BN, da, db, k > 0 ? 1u : 0u);
+                    for (int k = 0; k < 8; ++k) {
+                        const uint32_t off = (k & 3) * 32;  // 16 bf16 columns inside the swizzle atom
+                        const uint64_t da = sw128_desc(a0 + (k >> 2) * A_HALF + off);
+                        const uint64_t db = sw128_desc(b0 + (k >> 2) * B_HALF + off);
+                        umma_bf16(tmem + b * BN, da, db, k > 0 ? 1u : 0u);
+                    }
+                    umma_commit(&bars->empty[s]);
+                    umma_commit(&bars->tfull[b]);
                 }
-                umma_commit(&bars->empty[s]);
-                umma_commit(&bars->tfull[b]);
-                issued = t + 1;
+                if (!ok) break;
+                umma_commit(&bars->a_empty[ab]);  // the key buffer is free once these MMAs finish
             }
             // drain: the last accumulator is complete before TMEM is freed
-            if (issued > 0) mbar_wait(&bars->tfull[(issued - 1) & 1], ((issued - 1) >> 1) & 1);
+            if (gt > 0) mbar_wait(&bars->tfull[(gt - 1) & 1], ((gt - 1) >> 1) & 1);
         }
     } else {
         // -------------------------------------------------------- epilogue
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int ew = warp - 2;          // 0..7
+        const int q = warp & 3;           // TMEM lane quarter this warp may access
+        const int hf = ew >> 2;           // column half of each 256-column tile
         const int row = q * 32 + lane;
-        const long long j = (long long)m0 + row;
-        float ej = 0.f;
-        if (j < N) {
-            const double r = m2[u] - norm2[(size_t)u * N + j];
-            ej = (float)sqrt(r > 0.0 ? r : 0.0);
-        }
-        float best = -INFINITY;
-        int bidx = 0x7fffffff;
-        const int et = threadIdx.x - 64;  // 0..127 among the epilogue threads
-        for (int t = 0; t < T; ++t) {
-            const int b = t & 1;
-            const uint32_t bph = (t >> 1) & 1;
-            float *se = sE + b * BN;
-            for (int c = et; c < BN; c += 128) {
-                const int m = t * BN + c;
-                se[c] = m < Np ? parent_e[(size_t)u * np_cap + m] : 0.f;
+        const int et = threadIdx.x - 64;  // 0..255
+        int gt = 0;
+        // prefetch cursor (one tile ahead) for the parent coordinates e_m
+        int p_item = blockIdx.x, p_t = 0;
+        Item P = p_item < n_items ? item_of(p_item, mt_per_unit, n_parents, np_cap) : Item{0, 0, 0, 0};
+        float e_next = 0.f;
+        if (p_item < n_items && et < P.Np) e_next = __ldg(parent_e + (size_t)P.u * np_cap + et);
+        for (int item = blockIdx.x; item < n_items; item += G) {
+            const Item I = item_of(item, mt_per_unit, n_parents, np_cap);
+            const long long j = (long long)I.m0 + row;
+            float ej = 0.f;
+            if (j < N) {
+                const double r = m2[I.u] - norm2[(size_t)I.u * N + j];
+                ej = (float)sqrt(r > 0.0 ? r : 0.0);
             }
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            // a failed wait stops this warp's work but not its barrier turns,
-            // so the other epilogue warps never wait for it
-            if (ok) ok = mbar_wait(&bars->tfull[b], bph);
-            ok = __all_sync(0xffffffffu, ok);
-            tc_fence_after();
-            const int valid = ok ? min(BN, Np - t * BN) : 0;
-            for (int c0 = 0; c0 < valid; c0 += 32) {
-                float v[32];
-                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + c0), v);
-                float cmax = -INFINITY;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    v[i] = (c0 + i < valid) ? fmaf(ej, se[c0 + i], v[i]) : -INFINITY;
-                    cmax = fmaxf(cmax, v[i]);
+            float best = -INFINITY;
+            int bidx = 0x7fffffff;
+            for (int t = 0; t < I.T; ++t, ++gt) {
+                const int b = gt & 1;
+                float *se = sE + b * BN;
+                se[et] = e_next;
+                // advance the prefetch cursor and load the next tile's e_m
+                if (++p_t >= P.T) {
+                    p_t = 0;
+                    p_item += G;
+                    if (p_item < n_items) P = item_of(p_item, mt_per_unit, n_parents, np_cap);
                 }
-                if (cmax > best) {
-                    int first = 0;
+                e_next = 0.f;
+                if (p_item < n_items && p_t * BN + et < P.Np)
+                    e_next = __ldg(parent_e + (size_t)P.u * np_cap + p_t * BN + et);
+                asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");
+                // a failed wait stops this warp's work but not its barrier turns
+                if (ok) ok = mbar_wait(&bars->tfull[b], (gt >> 1) & 1);
+                ok = __all_sync(0xffffffffu, ok);
+                tc_fence_after();
+                const int c_lo = t * BN + hf * (BN / 2);
+                const int valid = ok ? max(0, min(BN / 2, I.Np - c_lo)) : 0;
+                const float *seh = se + hf * (BN / 2);
+                for (int c0 = 0; c0 < valid; c0 += 64) {
+                    float v[64];
+                    const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + hf * (BN / 2) + c0);
+                    tmem_ld32_nowait(ta, v);
+                    tmem_ld32_nowait(ta + 32, v + 32);
+                    tmem_wait_ld();
+                    float cmax = -INFINITY;
+                    if (valid - c0 >= 64) {
 #pragma unroll
-                    for (int i = 31; i >= 0; --i)
-                        if (v[i] == cmax) first = i;
-                    best = cmax;
-                    bidx = t * BN + c0 + first;
+                        for (int i = 0; i < 64; ++i) {
+                            v[i] = fmaf(ej, seh[c0 + i], v[i]);
+                            cmax = fmaxf(cmax, v[i]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) {
+                            v[i] = (c0 + i < valid) ? fmaf(ej, seh[c0 + i], v[i]) : -INFINITY;
+                            cmax = fmaxf(cmax, v[i]);
+                        }
+                    }
+                    if (cmax > best) {
+                        int first = 0;
+#pragma unroll
+                        for (int i = 63; i >= 0; --i)
+                            if (v[i] == cmax) first = i;
+                        best = cmax;
+                        bidx = c_lo + c0 + first;
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&bars->tempty[b]);
+            }
+            // combine the two column halves of each row
+            if (hf == 1) {
+                bars->comb_s[row] = best;
+                bars->comb_i[row] = bidx;
+            }
+            asm volatile("bar.sync 2, %0;" ::"r"(kEpiThreads) : "memory");
+            if (hf == 0) {
+                const float os = bars->comb_s[row];
+                const int oi = bars->comb_i[row];
+                if (better(os, oi, best, bidx)) {
+                    best = os;
+                    bidx = oi;
+                }
+                if (ok && j < N && I.Np > 0) {
+                    int32_t *tp = token_parent + (size_t)I.u * n_cap + j;
+                    if (*tp < 0) *tp = bidx;  // promoted tokens keep themselves
                 }
             }
-            tc_fence_before();
-            mbar_arrive(&bars->tempty[b]);
-        }
-        if (ok && j < N && Np > 0) {
-            int32_t *tp = token_parent + (size_t)u * n_cap + j;
-            if (*tp < 0) *tp = bidx;  // promoted tokens keep themselves
+            asm volatile("bar.sync 2, %0;" ::"r"(kEpiThreads) : "memory");
         }
     }
     if (!ok) set_err(err, ICE_ERR_TIMEOUT);
@@ -338,9 +422,18 @@ cudaError_t launch_assign_tc(const ice_params &p, const void *K, const ice_index
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    dim3 grid(ceil_div(p.n_tokens, BM), U);
-    k_assign_tc<<<grid, kThreads, kSmemBytes, s>>>(tmK, tmP, p.n_tokens, p.np_cap, p.n_cap, idx.n_parents, idx.m2,
-                                                   ws.norm2, idx.parent_e, idx.token_parent, err);
+    static int n_sm = 0;
+    if (!n_sm) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+        if (n_sm <= 0) n_sm = 1;
+    }
+    const int mt = ceil_div(p.n_tokens, BM);
+    const int items = mt * U;
+    const int grid = items < n_sm ? items : n_sm;
+    k_assign_tc<<<grid, kThreads, kSmemBytes, s>>>(tmK, tmP, p.n_tokens, p.np_cap, p.n_cap, items, mt, idx.n_parents,
+                                                   idx.m2, ws.norm2, idx.parent_e, idx.token_parent, err);
     return cudaGetLastError();
 }
 

@@ -8,13 +8,17 @@
 // Management for Long-Sequence LLMs", 关键设计 2: points are promoted at
 // random and each lower point picks its nearest parent one level up.
 //
-// Two kernels per layer:
-//   k_lift_count    grid (tiles, units): |k_j|^2 for every token (double-float
-//                   accumulation, exact enough that sqrt(M^2 - |k|^2) rounds
-//                   correctly to fp32), M^2 = max via a 64-bit atomicMax on
-//                   the non-negative double's bits, and per tile the number
-//                   of promoted tokens plus the unit's smallest draw.
-//   k_promote_write grid (tiles, units): order-preserving compaction of the
+// Two kernels per layer, both over 256-token tiles (one token per thread):
+//   k_lift_count    |k_j|^2 for every token with double-float accumulation
+//                   (exact enough that sqrt(M^2 - |k|^2) rounds correctly to
+//                   fp32): four lanes per token, each loading its 64-byte
+//                   quarter of the row for all 8 of its tokens before any
+//                   arithmetic (many loads in flight).  Per tile: the largest
+//                   |k|^2, the number of promoted tokens and the smallest
+//                   (draw, token), written to the workspace (no atomics, no
+//                   memset).
+//   k_promote_write reduces the unit's tile values (M^2, promoted count,
+//                   smallest draw), then order-preserving compaction of the
 //                   promoted tokens into the parent table (block scan plus
 //                   the counts of the tiles before), parent keys, lifted
 //                   extra coordinate of each parent, token_parent seeds.
@@ -24,32 +28,43 @@
 namespace ice {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kTokPerThread = kLiftTile / kThreads;  // 8
+constexpr int kThreads = kLiftTile;  // one token per thread
+constexpr int kWarps = kThreads / 32;
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) k_lift_count(const T *__restrict__ K, int N, int n_kv_heads,
-                                                         uint64_t thresh, uint64_t key, double *__restrict__ m2,
+                                                         uint64_t thresh, uint64_t key,
                                                          double *__restrict__ norm2, int32_t *__restrict__ pcount,
-                                                         unsigned long long *__restrict__ minpack, int n_tiles) {
+                                                         double *__restrict__ tile_max,
+                                                         unsigned long long *__restrict__ tile_min, int n_tiles) {
     const int u = blockIdx.y, tile = blockIdx.x;
     const int seq = u / n_kv_heads, head = u % n_kv_heads;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long t0 = (long long)tile * kLiftTile;
     const T *Ku = K + (size_t)u * N * kHeadDim;
 
-    // ---- squared norms: LPT lanes per token, one 16-byte vector per lane
-    constexpr int LPT = row_vecs<T>();  // 16 (bf16) or 32 (fp32)
-    constexpr int TPS = 32 / LPT;       // tokens per warp step
+    // ---- squared norms: the warp's 32 tokens, 4 lanes per token, 8 tokens per step
+    constexpr int RV = row_vecs<T>();  // 16-byte vectors per row
+    constexpr int VPL = RV / 4;        // vectors per lane per token
+    constexpr int STEPS = 4;           // 4 steps x 8 tokens = the warp's 32 tokens
+    const long long wt0 = t0 + warp * 32;
+    uint4 buf[STEPS][VPL];
+#pragma unroll
+    for (int s = 0; s < STEPS; ++s) {
+        const long long j = wt0 + s * 8 + lane / 4;
+        const uint4 *row = reinterpret_cast<const uint4 *>(Ku + (size_t)(j < N ? j : 0) * kHeadDim);
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) buf[s][v] = (j < N) ? __ldg(row + (lane % 4) + 4 * v) : make_uint4(0, 0, 0, 0);
+    }
     double wmax = 0.0;
-    const int per_warp = kLiftTile / (kThreads / 32);
-    for (int s = 0; s < per_warp; s += TPS) {
-        const long long j = t0 + (long long)warp * per_warp + s + lane / LPT;
+    double mine = 0.0;  // lane s*8 + token of step s keeps its own token's norm
+#pragma unroll
+    for (int s = 0; s < STEPS; ++s) {
         float hi = 0.f, lo = 0.f;
-        if (j < N) {
-            const uint4 v = reinterpret_cast<const uint4 *>(Ku + (size_t)j * kHeadDim)[lane % LPT];
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
             float f[Elem<T>::kPerVec];
-            Elem<T>::unpack(v, f);
+            Elem<T>::unpack(buf[s][v], f);
 #pragma unroll
             for (int i = 0; i < Elem<T>::kPerVec; ++i) {
                 const float t = f[i] * f[i];
@@ -61,7 +76,7 @@ __global__ void __launch_bounds__(kThreads) k_lift_count(const T *__restrict__ K
             }
         }
 #pragma unroll
-        for (int off = LPT / 2; off >= 1; off >>= 1) {
+        for (int off = 2; off >= 1; off >>= 1) {
             const float ohi = __shfl_xor_sync(0xffffffffu, hi, off);
             const float olo = __shfl_xor_sync(0xffffffffu, lo, off);
             float sum, err;
@@ -69,22 +84,23 @@ __global__ void __launch_bounds__(kThreads) k_lift_count(const T *__restrict__ K
             hi = sum;
             lo += olo + err;
         }
-        if (j < N && lane % LPT == 0) {
-            const double n = (double)hi + (double)lo;
-            norm2[(size_t)u * N + j] = n;
-            wmax = fmax(wmax, n);
-        }
+        const double n = (double)hi + (double)lo;
+        // token (s*8 + lane/4) of the warp: hand it to lane s*8 + lane/4
+        const double got = __shfl_sync(0xffffffffu, n, ((lane - s * 8) & 7) * 4);
+        if (lane / 8 == s) mine = got;
     }
-    // ---- promotion draws: kTokPerThread consecutive tokens per thread
+    const long long j = wt0 + lane;
+    if (j < N) {
+        norm2[(size_t)u * N + j] = mine;
+        wmax = mine;
+    }
+    // ---- promotion draw of this thread's token
     int cnt = 0;
     unsigned long long best = ~0ull;
-    for (int i = 0; i < kTokPerThread; ++i) {
-        const long long j = t0 + threadIdx.x * kTokPerThread + i;
-        if (j >= N) break;
+    if (j < N) {
         const uint32_t d = promote_draw(key, seq, head, (uint32_t)j, 1u);
-        cnt += ((uint64_t)d < thresh);
-        const unsigned long long pk = ((unsigned long long)d << 32) | (unsigned long long)j;
-        best = pk < best ? pk : best;
+        cnt = ((uint64_t)d < thresh);
+        best = ((unsigned long long)d << 32) | (unsigned long long)j;
     }
     // ---- block reductions
 #pragma unroll
@@ -94,9 +110,9 @@ __global__ void __launch_bounds__(kThreads) k_lift_count(const T *__restrict__ K
         const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
         best = o < best ? o : best;
     }
-    __shared__ double s_max[kThreads / 32];
-    __shared__ int s_cnt[kThreads / 32];
-    __shared__ unsigned long long s_best[kThreads / 32];
+    __shared__ double s_max[kWarps];
+    __shared__ int s_cnt[kWarps];
+    __shared__ unsigned long long s_best[kWarps];
     if (lane == 0) {
         s_max[warp] = wmax;
         s_cnt[warp] = cnt;
@@ -107,14 +123,13 @@ __global__ void __launch_bounds__(kThreads) k_lift_count(const T *__restrict__ K
         double mx = 0.0;
         int c = 0;
         unsigned long long b = ~0ull;
-        for (int w = 0; w < kThreads / 32; ++w) {
+        for (int w = 0; w < kWarps; ++w) {
             mx = fmax(mx, s_max[w]);
             c += s_cnt[w];
             b = s_best[w] < b ? s_best[w] : b;
         }
-        // non-negative doubles order like their bit patterns
-        atomicMax(reinterpret_cast<unsigned long long *>(m2 + u), (unsigned long long)__double_as_longlong(mx));
-        atomicMin(minpack + u, b);
+        tile_max[(size_t)u * n_tiles + tile] = mx;
+        tile_min[(size_t)u * n_tiles + tile] = b;
         pcount[(size_t)u * n_tiles + tile] = c;
     }
 }
@@ -122,8 +137,9 @@ __global__ void __launch_bounds__(kThreads) k_lift_count(const T *__restrict__ K
 template <typename T>
 __global__ void __launch_bounds__(kThreads) k_promote_write(
     const T *__restrict__ K, int N, int n_kv_heads, uint64_t thresh, uint64_t key, int np_cap, int n_cap,
-    const double *__restrict__ m2, const double *__restrict__ norm2, const int32_t *__restrict__ pcount,
-    const unsigned long long *__restrict__ minpack, int n_tiles, int32_t *__restrict__ n_parents,
+    double *__restrict__ m2, const double *__restrict__ norm2, const int32_t *__restrict__ pcount,
+    const double *__restrict__ tile_max, const unsigned long long *__restrict__ tile_min, int n_tiles,
+    int32_t *__restrict__ n_parents,
     int32_t *__restrict__ n_indexed, int32_t *__restrict__ parent_tok, T *__restrict__ parent_keys,
     float *__restrict__ parent_e, float *__restrict__ parent_corr, int32_t *__restrict__ token_parent,
     int32_t *__restrict__ err) {
@@ -132,94 +148,96 @@ __global__ void __launch_bounds__(kThreads) k_promote_write(
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long t0 = (long long)tile * kLiftTile;
 
-    __shared__ int s_base, s_total;
-    __shared__ int s_warp[kThreads / 32];
+    __shared__ int s_part[kWarps][2];
+    __shared__ double s_pmax[kWarps];
+    __shared__ unsigned long long s_pmin[kWarps];
+    __shared__ int s_warp[kWarps];
     __shared__ int s_list_tok[kLiftTile];
     __shared__ int s_list_m[kLiftTile];
-    __shared__ int s_nlist;
-    if (warp == 0) {
-        int before = 0, all = 0;
-        for (int t = lane; t < n_tiles; t += 32) {
-            const int c = pcount[(size_t)u * n_tiles + t];
-            all += c;
-            before += (t < tile) ? c : 0;
-        }
+    // the unit's tile values: counts before this tile and in all, M^2, smallest draw
+    int before = 0, all = 0;
+    double mx = 0.0;
+    unsigned long long mn = ~0ull;
+    for (int t = threadIdx.x; t < n_tiles; t += kThreads) {
+        const size_t o = (size_t)u * n_tiles + t;
+        const int c = pcount[o];
+        all += c;
+        before += (t < tile) ? c : 0;
+        mx = fmax(mx, tile_max[o]);
+        mn = tile_min[o] < mn ? tile_min[o] : mn;
+    }
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) {
-            before += __shfl_xor_sync(0xffffffffu, before, off);
-            all += __shfl_xor_sync(0xffffffffu, all, off);
-        }
-        if (lane == 0) {
-            s_base = before;
-            s_total = all;
-            s_nlist = 0;
-        }
+    for (int off = 16; off >= 1; off >>= 1) {
+        before += __shfl_xor_sync(0xffffffffu, before, off);
+        all += __shfl_xor_sync(0xffffffffu, all, off);
+        mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, mn, off);
+        mn = o < mn ? o : mn;
+    }
+    if (lane == 0) {
+        s_part[warp][0] = before;
+        s_part[warp][1] = all;
+        s_pmax[warp] = mx;
+        s_pmin[warp] = mn;
     }
     __syncthreads();
+    int s_base = 0, s_total = 0;
+    double M2 = 0.0;
+    unsigned long long minpack = ~0ull;
+    for (int w = 0; w < kWarps; ++w) {
+        s_base += s_part[w][0];
+        s_total += s_part[w][1];
+        M2 = fmax(M2, s_pmax[w]);
+        minpack = s_pmin[w] < minpack ? s_pmin[w] : minpack;
+    }
     // No token promoted: the smallest draw (lowest token on ties) is.
     const bool fallback = (s_total == 0 && N > 0);
-    const long long jmin = fallback ? (long long)(minpack[u] & 0xFFFFFFFFull) : -1;
+    const long long jmin = fallback ? (long long)(minpack & 0xFFFFFFFFull) : -1;
     const int total = fallback ? 1 : s_total;
     const int base = fallback ? 0 : s_base;
     if (tile == 0 && threadIdx.x == 0) {
         if (total > np_cap) set_err(err, ICE_ERR_CAPACITY);
         n_parents[u] = total < np_cap ? total : np_cap;
         n_indexed[u] = N;
+        m2[u] = M2;
     }
 
-    // flags of this thread's tokens, in token order
-    unsigned flags = 0;
-    for (int i = 0; i < kTokPerThread; ++i) {
-        const long long j = t0 + threadIdx.x * kTokPerThread + i;
-        if (j >= N) break;
-        const bool f = fallback ? (j == jmin)
-                                : ((uint64_t)promote_draw(key, seq, head, (uint32_t)j, 1u) < thresh);
-        flags |= (unsigned)f << i;
-    }
-    const int c = __popc(flags);
-    int incl = c;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
-    }
-    if (lane == 31) s_warp[warp] = incl;
+    const long long j = t0 + threadIdx.x;
+    const bool f = (j < N) && (fallback ? (j == jmin)
+                                        : ((uint64_t)promote_draw(key, seq, head, (uint32_t)j, 1u) < thresh));
+    const unsigned bal = __ballot_sync(0xffffffffu, f);
+    if (lane == 0) s_warp[warp] = __popc(bal);
     __syncthreads();
     int woff = 0;
     for (int w = 0; w < warp; ++w) woff += s_warp[w];
-    int m = base + woff + incl - c;
-
-    const double M2 = m2[u];
-    const size_t ubase_n = (size_t)u * n_cap;
-    const size_t ubase_p = (size_t)u * np_cap;
-    for (int i = 0; i < kTokPerThread; ++i) {
-        const long long j = t0 + threadIdx.x * kTokPerThread + i;
-        if (j >= N) break;
+    const int local = woff + __popc(bal & lanemask_lt());
+    const int m = base + local;
+    if (j < N) {
         int32_t tp = -1;
-        if ((flags >> i) & 1u) {
-            if (m < np_cap) {
-                tp = m;
-                parent_tok[ubase_p + m] = (int32_t)j;
-                const double r = M2 - norm2[(size_t)u * N + j];
-                parent_e[ubase_p + m] = (float)sqrt(r > 0.0 ? r : 0.0);
-                parent_corr[ubase_p + m] = 0.f;
-                const int slot = atomicAdd(&s_nlist, 1);
-                s_list_tok[slot] = (int)j;
-                s_list_m[slot] = m;
-            }
-            ++m;
+        if (f && m < np_cap) {
+            tp = m;
+            const size_t up = (size_t)u * np_cap;
+            parent_tok[up + m] = (int32_t)j;
+            const double r = M2 - norm2[(size_t)u * N + j];
+            parent_e[up + m] = (float)sqrt(r > 0.0 ? r : 0.0);
+            parent_corr[up + m] = 0.f;
         }
-        token_parent[ubase_n + j] = tp;
+        token_parent[(size_t)u * n_cap + j] = tp;
+        if (f) {
+            s_list_tok[local] = (int)j;
+            s_list_m[local] = m;
+        }
     }
     __syncthreads();
+    int nl = 0;
+    for (int w = 0; w < kWarps; ++w) nl += s_warp[w];
     // copy the promoted keys into the parent table, one 16-byte vector per thread
     constexpr int RV = row_vecs<T>();
-    const int nl = s_nlist;
     const uint4 *src = reinterpret_cast<const uint4 *>(K + (size_t)u * N * kHeadDim);
-    uint4 *dst = reinterpret_cast<uint4 *>(parent_keys + ubase_p * kHeadDim);
+    uint4 *dst = reinterpret_cast<uint4 *>(parent_keys + (size_t)u * np_cap * kHeadDim);
     for (int x = threadIdx.x; x < nl * RV; x += kThreads) {
         const int r = x / RV, v = x % RV;
-        dst[(size_t)s_list_m[r] * RV + v] = src[(size_t)s_list_tok[r] * RV + v];
+        if (s_list_m[r] < np_cap) dst[(size_t)s_list_m[r] * RV + v] = src[(size_t)s_list_tok[r] * RV + v];
     }
 }
 
@@ -229,15 +247,13 @@ cudaError_t launch_lift_promote_t(const ice_params &p, const void *K, const ice_
     const int U = units_of(p);
     const int N = p.n_tokens;
     const int tiles = ceil_div(N, kLiftTile);
-    cudaMemsetAsync(idx.m2, 0, sizeof(double) * U, s);
-    cudaMemsetAsync(ws.minpack, 0xFF, sizeof(unsigned long long) * U, s);
     const uint64_t key = promote_key(p.seed, p.layer);
     dim3 grid(tiles, U);
     k_lift_count<T><<<grid, kThreads, 0, s>>>(static_cast<const T *>(K), N, p.n_kv_heads, p.promote_thresh, key,
-                                              idx.m2, ws.norm2, ws.pcount, ws.minpack, tiles);
+                                              ws.norm2, ws.pcount, ws.tile_max, ws.tile_min, tiles);
     k_promote_write<T><<<grid, kThreads, 0, s>>>(
         static_cast<const T *>(K), N, p.n_kv_heads, p.promote_thresh, key, p.np_cap, p.n_cap, idx.m2, ws.norm2,
-        ws.pcount, ws.minpack, tiles, idx.n_parents, idx.n_indexed, idx.parent_tok,
+        ws.pcount, ws.tile_max, ws.tile_min, tiles, idx.n_parents, idx.n_indexed, idx.parent_tok,
         static_cast<T *>(idx.parent_keys), idx.parent_e, idx.parent_corr, idx.token_parent, err);
     return cudaGetLastError();
 }

@@ -10,20 +10,23 @@
 //
 // Layout rule: parents in ascending m; a parent's tokens in ascending token
 // order; consecutive chunks of S tokens per page; pages numbered in that
-// order.  This is a stable counting sort of the tokens by parent, done
-// without library sorts in three kernels:
-//   k_pack_count  grid (tiles, units): per 2048-token tile, tokens per parent
-//                 (shared-memory histogram, or global atomics when the parent
-//                 count is too large for shared memory).
+// order.  This is a stable counting sort of the tokens by parent, written
+// without library sorts, in four kernels:
+//   k_pack_count  grid (2048-token tiles, units): tokens per parent in the
+//                 tile (shared-memory histogram, or global atomics when the
+//                 parent count is too large for shared memory).
 //   k_pack_scan   grid (units): per parent, exclusive scan of its tile counts
-//                 (column scan) -> tile offsets and total c_m; exclusive scan
-//                 of ceil(c_m / S) over m -> first page; page tables.
-//   k_pack_rank_scatter grid (tiles, units): the stable rank of every token
-//                 inside its parent = tile offset + rank inside the tile.
-//                 Inside a tile, warps take turns (in token order), each
-//                 ranking its 32 tokens with __match_any_sync and bumping
-//                 per-parent counters; then the CTA copies the K/V rows to
-//                 (page, slot) with 16-byte vectors and zeroes pad slots.
+//                 (column scan, loads batched) -> tile offsets and total c_m;
+//                 exclusive scan of ceil(c_m / S) over m -> first page; page
+//                 tables.
+//   k_pack_rank   grid (tiles, units): stable rank of every token inside its
+//                 parent = tile offset + rank inside the tile.  Inside a tile,
+//                 warps take turns in token order, each ranking its 32 tokens
+//                 with __match_any_sync and bumping per-parent counters; the
+//                 token tables and page_tokens get (page, slot).
+//   k_pack_copy   grid (pages / 8, units): one warp per page gathers the K
+//                 and V rows of the page's tokens (all 16-byte loads issued
+//                 before the stores) into the pool and zeroes pad slots.
 #include "common.cuh"
 #include "internal.h"
 
@@ -32,6 +35,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kScanThreads = 1024;
+constexpr int kTokPerThread = kPackTile / kThreads;  // 8
 
 __global__ void __launch_bounds__(kThreads) k_pack_count(const int32_t *__restrict__ token_parent, int N, int n_cap,
                                                          int np_cap, const int32_t *__restrict__ n_parents,
@@ -42,20 +46,23 @@ __global__ void __launch_bounds__(kThreads) k_pack_count(const int32_t *__restri
     const int Np = min(n_parents[u], np_cap);
     int32_t *row = pack_cnt + ((size_t)u * n_tiles + tile) * np_cap;
     int *hist = smem_path ? s_hist : row;
-    if (smem_path) {
-        for (int m = threadIdx.x; m < Np; m += kThreads) s_hist[m] = 0;
-        __syncthreads();
-    }
     const long long t0 = (long long)tile * kPackTile;
-    for (int i = threadIdx.x; i < kPackTile; i += kThreads) {
-        const long long j = t0 + i;
-        if (j >= N) break;
-        const int m = token_parent[(size_t)u * n_cap + j];
-        if (m >= 0 && m < Np) atomicAdd(&hist[m], 1);
+    int m[kTokPerThread];
+#pragma unroll
+    for (int i = 0; i < kTokPerThread; ++i) {
+        const long long j = t0 + i * kThreads + threadIdx.x;
+        m[i] = j < N ? token_parent[(size_t)u * n_cap + j] : -1;
     }
     if (smem_path) {
+        for (int x = threadIdx.x; x < Np; x += kThreads) s_hist[x] = 0;
         __syncthreads();
-        for (int m = threadIdx.x; m < Np; m += kThreads) row[m] = s_hist[m];
+    }
+#pragma unroll
+    for (int i = 0; i < kTokPerThread; ++i)
+        if (m[i] >= 0 && m[i] < Np) atomicAdd(&hist[m[i]], 1);
+    if (smem_path) {
+        __syncthreads();
+        for (int x = threadIdx.x; x < Np; x += kThreads) row[x] = s_hist[x];
     }
 }
 
@@ -72,6 +79,7 @@ __global__ void __launch_bounds__(kScanThreads) k_pack_scan(int np_cap, int page
                                                             int32_t *__restrict__ page_next,
                                                             int32_t *__restrict__ page_tokens,
                                                             int32_t *__restrict__ err) {
+    constexpr int kBatch = 16;  // column entries loaded before they are scanned
     __shared__ int s_warp[kScanThreads / 32];
     __shared__ long long s_carry;
     const int u = blockIdx.x;
@@ -85,10 +93,15 @@ __global__ void __launch_bounds__(kScanThreads) k_pack_scan(int np_cap, int page
         int c = 0;
         if (m < Np) {
             int32_t *col = pack_cnt + (size_t)u * n_tiles * np_cap + m;
-            for (int t = 0; t < n_tiles; ++t) {
-                const int v = col[(size_t)t * np_cap];
-                col[(size_t)t * np_cap] = c;
-                c += v;
+            for (int t0 = 0; t0 < n_tiles; t0 += kBatch) {
+                int v[kBatch];
+#pragma unroll
+                for (int i = 0; i < kBatch; ++i) v[i] = (t0 + i < n_tiles) ? col[(size_t)(t0 + i) * np_cap] : 0;
+#pragma unroll
+                for (int i = 0; i < kBatch; ++i) {
+                    if (t0 + i < n_tiles) col[(size_t)(t0 + i) * np_cap] = c;
+                    c += v[i];
+                }
             }
         }
         const int pages = (c + kPage - 1) / kPage;
@@ -128,92 +141,98 @@ __global__ void __launch_bounds__(kScanThreads) k_pack_scan(int np_cap, int page
     }
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kThreads) k_pack_rank_scatter(
-    const T *__restrict__ K, const T *__restrict__ V, int N, int n_cap, int np_cap, int page_cap, int n_tiles,
-    int smem_path, const int32_t *__restrict__ n_parents, const int32_t *__restrict__ token_parent,
-    int32_t *__restrict__ pack_cnt, const int32_t *__restrict__ pack_total,
-    const int32_t *__restrict__ parent_first_page, int32_t *__restrict__ page_tokens,
-    int32_t *__restrict__ token_page, int32_t *__restrict__ token_slot, T *__restrict__ pool_k,
-    T *__restrict__ pool_v) {
+__global__ void __launch_bounds__(kThreads) k_pack_rank(int N, int n_cap, int np_cap, int page_cap, int n_tiles,
+                                                        int smem_path, const int32_t *__restrict__ n_parents,
+                                                        const int32_t *__restrict__ token_parent,
+                                                        int32_t *__restrict__ pack_cnt,
+                                                        const int32_t *__restrict__ parent_first_page,
+                                                        int32_t *__restrict__ page_tokens,
+                                                        int32_t *__restrict__ token_page,
+                                                        int32_t *__restrict__ token_slot) {
     extern __shared__ int s_ctr_dyn[];
-    __shared__ int s_dst[kThreads];   // page * S + slot, or -1
-    __shared__ int s_pad[kThreads];   // first pad slot after this token, or S
     const int u = blockIdx.y, tile = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Np = min(n_parents[u], np_cap);
     int32_t *row = pack_cnt + ((size_t)u * n_tiles + tile) * np_cap;
     int *ctr = smem_path ? s_ctr_dyn : row;
+    const size_t un = (size_t)u * n_cap, up = (size_t)u * np_cap, ug = (size_t)u * page_cap;
+    const long long t0 = (long long)tile * kPackTile;
+    int m[kTokPerThread], first[kTokPerThread];
+#pragma unroll
+    for (int i = 0; i < kTokPerThread; ++i) {
+        const long long j = t0 + i * kThreads + threadIdx.x;
+        m[i] = j < N ? token_parent[un + j] : -1;
+    }
+#pragma unroll
+    for (int i = 0; i < kTokPerThread; ++i) first[i] = (m[i] >= 0 && m[i] < Np) ? parent_first_page[up + m[i]] : 0;
     if (smem_path) {
-        for (int m = threadIdx.x; m < Np; m += kThreads) s_ctr_dyn[m] = row[m];
+        for (int x = threadIdx.x; x < Np; x += kThreads) s_ctr_dyn[x] = row[x];
     }
     __syncthreads();
-    const size_t un = (size_t)u * n_cap, up = (size_t)u * np_cap, ug = (size_t)u * page_cap;
-    const T *Ku = K + (size_t)u * N * kHeadDim;
-    const T *Vu = V + (size_t)u * N * kHeadDim;
-    constexpr int RV = row_vecs<T>();
-    const long long t0 = (long long)tile * kPackTile;
-    for (int r0 = 0; r0 < kPackTile; r0 += kThreads) {
-        if (t0 + r0 >= N) break;
-        const long long j = t0 + r0 + threadIdx.x;
-        const int m = (j < N) ? token_parent[un + j] : -1;
-        const bool valid = (m >= 0 && m < Np);
+#pragma unroll
+    for (int i = 0; i < kTokPerThread; ++i) {
+        const long long j = t0 + i * kThreads + threadIdx.x;
+        const bool valid = m[i] >= 0 && m[i] < Np;
         int rank = 0;
         for (int w = 0; w < kThreads / 32; ++w) {
             if (warp == w) {
-                const int key = valid ? m : -1 - lane;  // invalid lanes stay alone
+                const int key = valid ? m[i] : -1 - lane;  // invalid lanes stay alone
                 const unsigned peers = __match_any_sync(0xffffffffu, key);
                 const int leader = __ffs(peers) - 1;
                 int base = 0;
                 if (valid && lane == leader) {
-                    base = ctr[m];
-                    ctr[m] = base + __popc(peers);
+                    base = ctr[m[i]];
+                    ctr[m[i]] = base + __popc(peers);
                 }
                 base = __shfl_sync(0xffffffffu, base, leader);
                 rank = base + __popc(peers & lanemask_lt());
             }
             __syncthreads();
         }
-        int dst = -1, pad = kPage;
         if (valid) {
-            const long long pg = (long long)parent_first_page[up + m] + rank / kPage;
+            const long long pg = (long long)first[i] + rank / kPage;
             const int slot = rank % kPage;
             if (pg < page_cap) {
-                dst = (int)(pg * kPage + slot);
-                page_tokens[ug * kPage + dst] = (int32_t)j;
+                page_tokens[(ug + pg) * kPage + slot] = (int32_t)j;
                 token_page[un + j] = (int32_t)pg;
                 token_slot[un + j] = slot;
-                if (rank == pack_total[up + m] - 1) pad = slot + 1;
             }
         }
-        s_dst[threadIdx.x] = dst;
-        s_pad[threadIdx.x] = pad;
-        __syncthreads();
-        // K/V rows -> pool, 16-byte vectors
-        const uint4 *k4 = reinterpret_cast<const uint4 *>(Ku);
-        const uint4 *v4 = reinterpret_cast<const uint4 *>(Vu);
-        uint4 *pk4 = reinterpret_cast<uint4 *>(pool_k + ug * kPage * kHeadDim);
-        uint4 *pv4 = reinterpret_cast<uint4 *>(pool_v + ug * kPage * kHeadDim);
-        for (int x = threadIdx.x; x < kThreads * RV; x += kThreads) {
-            const int r = x / RV, v = x % RV;
-            const int d = s_dst[r];
-            if (d < 0) continue;
-            const size_t src = (size_t)(t0 + r0 + r) * RV + v;
-            pk4[(size_t)d * RV + v] = k4[src];
-            pv4[(size_t)d * RV + v] = v4[src];
-        }
-        // zero the pad slots after each parent's last token
-        for (int r = warp; r < kThreads; r += kThreads / 32) {
-            const int pad0 = s_pad[r];
-            if (pad0 >= kPage) continue;
-            const int d0 = s_dst[r] - (s_dst[r] % kPage);
-            for (int x = lane; x < (kPage - pad0) * RV; x += 32) {
-                const size_t o = (size_t)(d0 + pad0 + x / RV) * RV + x % RV;
-                pk4[o] = make_uint4(0, 0, 0, 0);
-                pv4[o] = make_uint4(0, 0, 0, 0);
-            }
-        }
-        __syncthreads();
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) k_pack_copy(const T *__restrict__ K, const T *__restrict__ V, int N,
+                                                        int page_cap, const int32_t *__restrict__ n_pages,
+                                                        const int32_t *__restrict__ page_len,
+                                                        const int32_t *__restrict__ page_tokens,
+                                                        T *__restrict__ pool_k, T *__restrict__ pool_v) {
+    constexpr int RV = row_vecs<T>();         // 16-byte vectors per row
+    constexpr int PER_LANE = kPage * RV / 32;  // vectors per lane per page (8 bf16, 16 fp32)
+    const int u = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int pg = blockIdx.x * (kThreads / 32) + warp;
+    if (pg >= min(n_pages[u], page_cap)) return;
+    const size_t gp = (size_t)u * page_cap + pg;
+    const int len = page_len[gp];
+    const int tok = lane < kPage ? page_tokens[gp * kPage + lane] : -1;
+    const uint4 *k4 = reinterpret_cast<const uint4 *>(K + (size_t)u * N * kHeadDim);
+    const uint4 *v4 = reinterpret_cast<const uint4 *>(V + (size_t)u * N * kHeadDim);
+    uint4 kv[PER_LANE], vv[PER_LANE];
+#pragma unroll
+    for (int i = 0; i < PER_LANE; ++i) {
+        const int x = lane + 32 * i, slot = x / RV, vec = x % RV;
+        const int j = __shfl_sync(0xffffffffu, tok, slot);
+        const bool ok = slot < len && j >= 0 && j < N;
+        kv[i] = ok ? __ldg(k4 + (size_t)j * RV + vec) : make_uint4(0, 0, 0, 0);
+        vv[i] = ok ? __ldg(v4 + (size_t)j * RV + vec) : make_uint4(0, 0, 0, 0);
+    }
+    uint4 *pk = reinterpret_cast<uint4 *>(pool_k) + gp * kPage * RV;
+    uint4 *pv = reinterpret_cast<uint4 *>(pool_v) + gp * kPage * RV;
+#pragma unroll
+    for (int i = 0; i < PER_LANE; ++i) {
+        pk[lane + 32 * i] = kv[i];
+        pv[lane + 32 * i] = vv[i];
     }
 }
 
@@ -226,7 +245,7 @@ cudaError_t launch_t(const ice_params &p, const void *K, const void *V, const ic
     const size_t smem = smem_path ? sizeof(int) * (size_t)p.np_cap : 0;
     if (smem > 48 * 1024) {
         cudaFuncSetAttribute(k_pack_count, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        cudaFuncSetAttribute(k_pack_rank_scatter<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(k_pack_rank, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     }
     if (!smem_path) cudaMemsetAsync(ws.pack_cnt, 0, sizeof(int32_t) * (size_t)U * tiles * p.np_cap, s);
     dim3 grid(tiles, U);
@@ -236,11 +255,13 @@ cudaError_t launch_t(const ice_params &p, const void *K, const void *V, const ic
                                            idx.n_pages, idx.parent_first_page, idx.parent_last_page,
                                            idx.parent_n_pages, idx.page_parent, idx.page_len, idx.page_next,
                                            idx.page_tokens, err);
-    k_pack_rank_scatter<T><<<grid, kThreads, smem, s>>>(
-        static_cast<const T *>(K), static_cast<const T *>(V), p.n_tokens, p.n_cap, p.np_cap, p.page_cap, tiles,
-        smem_path, idx.n_parents, idx.token_parent, ws.pack_cnt, ws.pack_total, idx.parent_first_page,
-        idx.page_tokens, idx.token_page, idx.token_slot, static_cast<T *>(idx.pool_k),
-        static_cast<T *>(idx.pool_v));
+    k_pack_rank<<<grid, kThreads, smem, s>>>(p.n_tokens, p.n_cap, p.np_cap, p.page_cap, tiles, smem_path,
+                                             idx.n_parents, idx.token_parent, ws.pack_cnt, idx.parent_first_page,
+                                             idx.page_tokens, idx.token_page, idx.token_slot);
+    dim3 cgrid(ceil_div(p.page_cap, kThreads / 32), U);
+    k_pack_copy<T><<<cgrid, kThreads, 0, s>>>(static_cast<const T *>(K), static_cast<const T *>(V), p.n_tokens,
+                                              p.page_cap, idx.n_pages, idx.page_len, idx.page_tokens,
+                                              static_cast<T *>(idx.pool_k), static_cast<T *>(idx.pool_v));
     return cudaGetLastError();
 }
 

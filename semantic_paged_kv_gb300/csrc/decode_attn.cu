@@ -12,9 +12,12 @@
 //              V (16 x d) with 16-byte vectors and writes its length.
 // k_attn<F>    grid (splits, units), split-KV flash decode: a CTA owns up to
 //              kAttnPagesPerSplit consecutive selected pages of a unit and all
-//              g query heads of its GQA group.  Per page: K and V are staged
-//              in shared memory as fp32, thread (head, slot) computes one
-//              logit, thread 0..g-1 fold the page into that head's running
+//              g query heads of its GQA group.  All of the split's page loads
+//              are issued at once (16-byte vectors into registers), then
+//              staged in shared memory in the storage dtype.  Per page: the
+//              logits are split over the head dimension (16 lanes x 8
+//              elements, two slots per lane group, shuffle reduction), a
+//              16-lane group per head folds the page into that head's running
 //              max / sum (online softmax), and thread t accumulates output
 //              dimension t.  Partials (max, sum, o) go to the workspace; the
 //              unit's last CTA (atomic ticket, no waiting) merges them with
@@ -30,7 +33,6 @@ namespace {
 
 constexpr int kThreads = 128;  // == kHeadDim: thread t owns output dimension t
 constexpr int kMaxG = 16;
-constexpr int kKStride = kHeadDim + 4;  // fp32 row stride of the staged K page
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) k_gather(const T *__restrict__ pool_k, const T *__restrict__ pool_v,
@@ -68,117 +70,167 @@ __global__ void __launch_bounds__(kThreads) k_attn(
     int32_t *__restrict__ buf_len, const int32_t *__restrict__ sel_count, int max_sel, float scale,
     int n_splits, float *__restrict__ part_ml, float *__restrict__ part_o, int32_t *__restrict__ ticket,
     float *__restrict__ O) {
+    constexpr int PPS = kAttnPagesPerSplit;
+    constexpr int RV = row_vecs<T>();        // 16-byte vectors per row
+    constexpr int PVEC = kPage * RV;         // 16-byte vectors per page
+    constexpr int VPT = PVEC / kThreads;     // vectors per thread per page and tensor
+    constexpr int CV = 8 / Elem<T>::kPerVec; // vectors per 8-element chunk (1 bf16, 2 fp32)
+    extern __shared__ __align__(16) uint4 s_kv[];  // [PPS][K, V][PVEC], reused by the merge
     __shared__ __align__(16) float s_q[kMaxG][kHeadDim];
-    __shared__ __align__(16) float s_k[kPage][kKStride];
-    __shared__ __align__(16) float s_v[kPage][kHeadDim];
     __shared__ float s_p[kMaxG][kPage];
-    __shared__ float s_alpha[kMaxG];
-    __shared__ float s_m[kMaxG], s_l[kMaxG];
+    __shared__ float s_alpha[kMaxG], s_m[kMaxG], s_l[kMaxG];
+    __shared__ int s_len[PPS];
     __shared__ int s_last;
     const int u = blockIdx.y, split = blockIdx.x;
     const int b = u / n_kv_heads, h = u % n_kv_heads;
-    const int t = threadIdx.x;
+    const int t = threadIdx.x, lane = t & 31;
     const T *Qu = Q + ((size_t)b * n_q_heads + (size_t)h * g) * kHeadDim;
     for (int x = t; x < g * kHeadDim; x += kThreads) s_q[x / kHeadDim][x % kHeadDim] = Elem<T>::load(Qu + x);
     if (t < g) {
         s_m[t] = -INFINITY;
         s_l[t] = 0.f;
     }
+    const int n = sel_count[u];
+    const int x0 = split * PPS;
+    const int np = max(0, min(PPS, n - x0));
+
+    // ---- stage the split's pages: all loads in flight at once
+    uint4 rk[PPS][VPT], rv[PPS][VPT];
+#pragma unroll
+    for (int i = 0; i < PPS; ++i) {
+        if (i < np) {
+            const size_t slot = (size_t)u * max_sel + x0 + i;
+            const uint4 *sk, *sv;
+            if (kFused) {
+                const size_t src = ((size_t)u * page_cap + sel_pages[slot]) * PVEC;
+                sk = reinterpret_cast<const uint4 *>(pool_k) + src;
+                sv = reinterpret_cast<const uint4 *>(pool_v) + src;
+            } else {
+                sk = reinterpret_cast<const uint4 *>(kbuf) + slot * PVEC;
+                sv = reinterpret_cast<const uint4 *>(vbuf) + slot * PVEC;
+            }
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                rk[i][v] = sk[t + v * kThreads];
+                rv[i][v] = sv[t + v * kThreads];
+            }
+        }
+    }
+    if (t < np) {
+        const size_t slot = (size_t)u * max_sel + x0 + t;
+        if (kFused) {
+            const int len = page_len[(size_t)u * page_cap + sel_pages[slot]];
+            s_len[t] = len;
+            buf_len[slot] = len;
+        } else {
+            s_len[t] = buf_len[slot];
+        }
+    }
+    if (kFused) {  // slots of this split past the selection hold no page
+        for (int x = max(x0, n) + t; x < min(x0 + PPS, max_sel); x += kThreads) buf_len[(size_t)u * max_sel + x] = 0;
+    }
+#pragma unroll
+    for (int i = 0; i < PPS; ++i) {
+        if (i < np) {
+            const size_t slot = (size_t)u * max_sel + x0 + i;
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                s_kv[(2 * i) * PVEC + t + v * kThreads] = rk[i][v];
+                s_kv[(2 * i + 1) * PVEC + t + v * kThreads] = rv[i][v];
+                if (kFused) {
+                    reinterpret_cast<uint4 *>(kbuf)[slot * PVEC + t + v * kThreads] = rk[i][v];
+                    reinterpret_cast<uint4 *>(vbuf)[slot * PVEC + t + v * kThreads] = rv[i][v];
+                }
+            }
+        }
+    }
+    __syncthreads();
+
     float o[kMaxG];
 #pragma unroll
     for (int hh = 0; hh < kMaxG; ++hh) o[hh] = 0.f;
-
-    const int n = sel_count[u];
-    const int x0 = split * kAttnPagesPerSplit;
-    const int x1 = min(n, x0 + kAttnPagesPerSplit);
-    constexpr int RV = row_vecs<T>();
-    constexpr int PVEC = kPage * RV;
-    constexpr int EPV = Elem<T>::kPerVec;
-    for (int x = x0; x < x1; ++x) {
-        const size_t slot = (size_t)u * max_sel + x;
-        const uint4 *sk, *sv;
-        int len;
-        if (kFused) {
-            const int pg = sel_pages[slot];
-            const size_t src = ((size_t)u * page_cap + pg) * PVEC;
-            sk = reinterpret_cast<const uint4 *>(pool_k) + src;
-            sv = reinterpret_cast<const uint4 *>(pool_v) + src;
-            len = page_len[(size_t)u * page_cap + pg];
-        } else {
-            sk = reinterpret_cast<const uint4 *>(kbuf) + slot * PVEC;
-            sv = reinterpret_cast<const uint4 *>(vbuf) + slot * PVEC;
-            len = buf_len[slot];
+    const int c = t & 15;      // 8-element chunk of the head dimension
+    const int sg = t >> 4;     // slots 2 sg and 2 sg + 1
+    for (int i = 0; i < np; ++i) {
+        const uint4 *Kp = s_kv + (2 * i) * PVEC;
+        const T *Vp = reinterpret_cast<const T *>(s_kv + (2 * i + 1) * PVEC);
+        const int len = s_len[i];
+        // logits: split-K over 16 lanes, 8 elements each, 2 slots per lane group
+        float kf[2][8];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+#pragma unroll
+            for (int w = 0; w < CV; ++w) Elem<T>::unpack(Kp[(2 * sg + r) * RV + c * CV + w], &kf[r][w * Elem<T>::kPerVec]);
         }
-        __syncthreads();  // previous page fully consumed
-        for (int i = t; i < PVEC; i += kThreads) {
-            const uint4 kv = sk[i], vv = sv[i];
-            if (kFused) {
-                reinterpret_cast<uint4 *>(kbuf)[slot * PVEC + i] = kv;
-                reinterpret_cast<uint4 *>(vbuf)[slot * PVEC + i] = vv;
+        for (int hh = 0; hh < g; ++hh) {
+            const float4 q0 = reinterpret_cast<const float4 *>(&s_q[hh][8 * c])[0];
+            const float4 q1 = reinterpret_cast<const float4 *>(&s_q[hh][8 * c])[1];
+            float a[2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                float x = q0.x * kf[r][0];
+                x = fmaf(q0.y, kf[r][1], x);
+                x = fmaf(q0.z, kf[r][2], x);
+                x = fmaf(q0.w, kf[r][3], x);
+                x = fmaf(q1.x, kf[r][4], x);
+                x = fmaf(q1.y, kf[r][5], x);
+                x = fmaf(q1.z, kf[r][6], x);
+                x = fmaf(q1.w, kf[r][7], x);
+                a[r] = x;
             }
-            const int r = i / RV, c = (i % RV) * EPV;
-            float f[EPV];
-            Elem<T>::unpack(kv, f);
 #pragma unroll
-            for (int e = 0; e < EPV; ++e) s_k[r][c + e] = f[e];
-            Elem<T>::unpack(vv, f);
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) s_v[r][c + e] = f[e];
+            for (int off = 8; off >= 1; off >>= 1) {
+                a[0] += __shfl_xor_sync(0xffffffffu, a[0], off);
+                a[1] += __shfl_xor_sync(0xffffffffu, a[1], off);
+            }
+            if (c == 0) {
+                s_p[hh][2 * sg] = a[0];
+                s_p[hh][2 * sg + 1] = a[1];
+            }
         }
-        if (kFused && t == 0) buf_len[slot] = len;
         __syncthreads();
-        // logits: thread (head, slot)
-        for (int hs = t; hs < g * kPage; hs += kThreads) {
+        // online softmax: lane group of 16 per head
+        for (int hs0 = 0; hs0 < g * kPage; hs0 += kThreads) {
+            const int hs = hs0 + t;
             const int hh = hs / kPage, sl = hs % kPage;
-            float acc = 0.f;
-            const float4 *kr = reinterpret_cast<const float4 *>(&s_k[sl][0]);
-            const float4 *qr = reinterpret_cast<const float4 *>(&s_q[hh][0]);
-#pragma unroll 8
-            for (int i = 0; i < kHeadDim / 4; ++i) {
-                const float4 a = kr[i], qq = qr[i];
-                acc = fmaf(qq.x, a.x, acc);
-                acc = fmaf(qq.y, a.y, acc);
-                acc = fmaf(qq.z, a.z, acc);
-                acc = fmaf(qq.w, a.w, acc);
-            }
-            s_p[hh][sl] = sl < len ? acc * scale : -INFINITY;
-        }
-        __syncthreads();
-        // online softmax bookkeeping, one thread per head
-        if (t < g) {
-            float pmax = -INFINITY;
-            for (int sl = 0; sl < kPage; ++sl) pmax = fmaxf(pmax, s_p[t][sl]);
-            const float m_old = s_m[t];
+            const bool on = hh < g;
+            const float lg = (on && sl < len) ? s_p[hh][sl] * scale : -INFINITY;
+            float pmax = lg;
+#pragma unroll
+            for (int off = 8; off >= 1; off >>= 1) pmax = fmaxf(pmax, __shfl_xor_sync(0xffffffffu, pmax, off));
+            const float m_old = on ? s_m[hh] : -INFINITY;
             const float m_new = fmaxf(m_old, pmax);
-            const float alpha = (m_old == -INFINITY) ? 0.f : expf(m_old - m_new);
-            float sum = 0.f;
-            for (int sl = 0; sl < kPage; ++sl) {
-                const float lg = s_p[t][sl];
-                const float pr = (lg == -INFINITY) ? 0.f : expf(lg - m_new);
-                s_p[t][sl] = pr;
-                sum += pr;
+            const float pr = (lg == -INFINITY) ? 0.f : expf(lg - m_new);
+            float psum = pr;
+#pragma unroll
+            for (int off = 8; off >= 1; off >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, off);
+            if (on) s_p[hh][sl] = pr;
+            __syncwarp();
+            if (on && sl == 0) {
+                const float alpha = (m_old == -INFINITY) ? 0.f : expf(m_old - m_new);
+                s_alpha[hh] = alpha;
+                s_l[hh] = s_l[hh] * alpha + psum;
+                s_m[hh] = m_new;
             }
-            s_alpha[t] = alpha;
-            s_l[t] = s_l[t] * alpha + sum;
-            s_m[t] = m_new;
         }
         __syncthreads();
+        // o[h][t] += sum_s p[h][s] v[s][t]
+        float vt[kPage];
+#pragma unroll
+        for (int sl = 0; sl < kPage; ++sl) vt[sl] = Elem<T>::load(Vp + sl * kHeadDim + t);
 #pragma unroll
         for (int hh = 0; hh < kMaxG; ++hh) {
             if (hh < g) {
                 float acc = o[hh] * s_alpha[hh];
 #pragma unroll
-                for (int sl = 0; sl < kPage; ++sl) acc = fmaf(s_p[hh][sl], s_v[sl][t], acc);
+                for (int sl = 0; sl < kPage; ++sl) acc = fmaf(s_p[hh][sl], vt[sl], acc);
                 o[hh] = acc;
             }
         }
+        __syncthreads();
     }
-    if (kFused) {  // slots of this split past the selection hold no page
-        for (int x = max(x0, n) + t; x < min(x0 + kAttnPagesPerSplit, max_sel); x += kThreads)
-            buf_len[(size_t)u * max_sel + x] = 0;
-    }
-    __syncthreads();
-    // partials of this split
+    (void)lane;
+    // ---- partials of this split
     const size_t pbase = ((size_t)u * n_splits + split) * g;
     if (t < g) {
         part_ml[(pbase + t) * 2 + 0] = s_m[t];
@@ -193,24 +245,44 @@ __global__ void __launch_bounds__(kThreads) k_attn(
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    // merge the unit's splits (log-sum-exp)
-    for (int hh = 0; hh < g; ++hh) {
+    // ---- the unit's last CTA merges the splits (log-sum-exp)
+    float *s_w = reinterpret_cast<float *>(s_kv);  // [n_splits * g] weights, then [g] totals
+    const int ns_g = n_splits * g;
+    const float *ml = part_ml + (size_t)u * ns_g * 2;
+    for (int x = t; x < ns_g; x += kThreads) s_w[x] = __ldcg(ml + 2 * x);
+    __syncthreads();
+    if (t < g) {
         float M = -INFINITY;
-        for (int sp = 0; sp < n_splits; ++sp)
-            M = fmaxf(M, __ldcg(part_ml + ((((size_t)u * n_splits + sp) * g + hh) * 2)));
-        float Lsum = 0.f, acc = 0.f;
-        if (M != -INFINITY) {
-            for (int sp = 0; sp < n_splits; ++sp) {
-                const size_t pb = ((size_t)u * n_splits + sp) * g + hh;
-                const float ms = __ldcg(part_ml + pb * 2);
-                if (ms == -INFINITY) continue;
-                const float w = expf(ms - M);
-                Lsum = fmaf(__ldcg(part_ml + pb * 2 + 1), w, Lsum);
-                acc = fmaf(__ldcg(part_o + pb * kHeadDim + t), w, acc);
-            }
-        }
-        O[((size_t)b * n_q_heads + (size_t)h * g + hh) * kHeadDim + t] = Lsum > 0.f ? acc / Lsum : 0.f;
+        for (int sp = 0; sp < n_splits; ++sp) M = fmaxf(M, s_w[sp * g + t]);
+        s_m[t] = M;
     }
+    __syncthreads();
+    for (int x = t; x < ns_g; x += kThreads) {
+        const float ms = s_w[x], M = s_m[x % g];
+        s_w[x] = (ms == -INFINITY) ? 0.f : expf(ms - M);
+    }
+    __syncthreads();
+    if (t < g) {
+        float L = 0.f;
+        for (int sp = 0; sp < n_splits; ++sp) L = fmaf(__ldcg(ml + 2 * (sp * g + t) + 1), s_w[sp * g + t], L);
+        s_l[t] = L;
+    }
+    __syncthreads();
+    const float *po = part_o + (size_t)u * ns_g * kHeadDim;
+    float acc[kMaxG];
+#pragma unroll
+    for (int hh = 0; hh < kMaxG; ++hh) acc[hh] = 0.f;
+    for (int sp = 0; sp < n_splits; ++sp) {
+#pragma unroll
+        for (int hh = 0; hh < kMaxG; ++hh)
+            if (hh < g) acc[hh] = fmaf(__ldcg(po + ((size_t)sp * g + hh) * kHeadDim + t), s_w[sp * g + hh], acc[hh]);
+    }
+#pragma unroll
+    for (int hh = 0; hh < kMaxG; ++hh)
+        if (hh < g) {
+            const float L = s_l[hh];
+            O[((size_t)b * n_q_heads + (size_t)h * g + hh) * kHeadDim + t] = L > 0.f ? acc[hh] / L : 0.f;
+        }
     if (t == 0) ticket[u] = 0;
 }
 
@@ -230,18 +302,25 @@ cudaError_t attn_t(const ice_params &p, const ice_index *pool, const int32_t *se
                    const DecodeWs &ws, cudaStream_t s) {
     const int U = units_of(p);
     const int g = p.n_q_heads / p.n_kv_heads;
-    cudaMemsetAsync(ws.attn_ticket, 0, sizeof(int32_t) * U, s);
-    dim3 grid(ws.n_splits, U);
+    dim3 grid(ws.n_splits, U);  // the tickets are zero between calls
     const T *pk = pool ? static_cast<const T *>(pool->pool_k) : nullptr;
     const T *pv = pool ? static_cast<const T *>(pool->pool_v) : nullptr;
     const int32_t *pl = pool ? pool->page_len : nullptr;
+    const size_t stage = sizeof(uint4) * 2 * kAttnPagesPerSplit * kPage * row_vecs<T>();
+    const size_t merge = sizeof(float) * (size_t)ws.n_splits * g;
+    const size_t smem = stage > merge ? stage : merge;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(pool ? (const void *)k_attn<T, true> : (const void *)k_attn<T, false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
     if (pool)
-        k_attn<T, true><<<grid, kThreads, 0, s>>>(static_cast<const T *>(Q), g, p.n_q_heads, p.n_kv_heads, pk, pv,
+        k_attn<T, true><<<grid, kThreads, smem, s>>>(static_cast<const T *>(Q), g, p.n_q_heads, p.n_kv_heads, pk, pv,
                                                   pl, p.page_cap, sel_pages, static_cast<T *>(kbuf),
                                                   static_cast<T *>(vbuf), buf_len, sel_count, max_sel, scale,
                                                   ws.n_splits, ws.part_ml, ws.part_o, ws.attn_ticket, O);
     else
-        k_attn<T, false><<<grid, kThreads, 0, s>>>(static_cast<const T *>(Q), g, p.n_q_heads, p.n_kv_heads, pk, pv,
+        k_attn<T, false><<<grid, kThreads, smem, s>>>(static_cast<const T *>(Q), g, p.n_q_heads, p.n_kv_heads, pk, pv,
                                                    pl, p.page_cap, sel_pages, static_cast<T *>(kbuf),
                                                    static_cast<T *>(vbuf), buf_len, sel_count, max_sel, scale,
                                                    ws.n_splits, ws.part_ml, ws.part_o, ws.attn_ticket, O);
@@ -317,6 +396,8 @@ cudaError_t launch_attention_noalloc(const ice_params &p, const void *Q, const v
     if (e != cudaSuccess) return e;
     const DecodeWs ws = decode_ws_layout(p, 0, max_sel, base);
     if (ws.bytes > ICE_NOALLOC_SCRATCH_BYTES) return cudaErrorInvalidValue;
+    e = cudaMemsetAsync(ws.attn_ticket, 0, sizeof(int32_t) * units_of(p), s);
+    if (e != cudaSuccess) return e;
     return launch_attention(p, nullptr, nullptr, Q, const_cast<void *>(kbuf), const_cast<void *>(vbuf),
                             const_cast<int32_t *>(buf_len), sel_count, max_sel, scale, O, ws, s);
 }

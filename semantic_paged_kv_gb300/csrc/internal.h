@@ -10,7 +10,7 @@
 namespace ice {
 
 // Tokens per tile of the lift/promotion kernels and of the page-packing kernels.
-constexpr int kLiftTile = 2048;
+constexpr int kLiftTile = 256;
 constexpr int kPackTile = 2048;
 // Parents per CTA of the selection scan.
 constexpr int kSelChunk = 256;
@@ -26,7 +26,8 @@ inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 struct BuildWs {
     double *norm2;        // [U, N]  |k_j|^2 (double)
     int32_t *pcount;      // [U, Tp] promoted tokens per lift tile
-    unsigned long long *minpack;  // [U] min over tokens of draw << 32 | token
+    double *tile_max;     // [U, Tp] largest |k|^2 of each lift tile
+    unsigned long long *tile_min;  // [U, Tp] smallest draw << 32 | token of each lift tile
     int32_t *pack_cnt;    // [U, Tk, np_cap] per-tile parent counts -> offsets
     int32_t *pack_total;  // [U, np_cap] tokens per parent
     size_t bytes;
@@ -34,10 +35,10 @@ struct BuildWs {
 BuildWs build_ws_layout(const ice_params &p, void *base);
 
 struct DecodeWs {
-    int32_t *sel_ticket;   // [U]
-    int32_t *attn_ticket;  // [U]
-    float *cand_score;     // [U, n_chunks, g, k]
-    int32_t *cand_id;      // [U, n_chunks, g, k]
+    int32_t *sel_ticket;   // [U]  zero between calls
+    int32_t *attn_ticket;  // [U]  zero between calls
+    unsigned long long *cand_key;  // [U, n_chunks, g, kc] sorted (-score, m) keys
+    int4 *cand_span;       // [U, n_chunks, 256] (first page, pages, contiguous, m)
     float *part_ml;        // [U, n_splits, g, 2]  running max, running sum
     float *part_o;         // [U, n_splits, g, d]
     int n_chunks, k_pages, n_splits;
