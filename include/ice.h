@@ -206,6 +206,31 @@ ice_status ice_build_assign_simt(const ice_params *p, const void *K, const ice_i
 ice_status ice_build_pack(const ice_params *p, const void *K, const void *V, const ice_index *idx,
                           void *ws, size_t ws_bytes, int32_t *err_dev, void *stream);
 
+/* -------------------------------------------------- incremental insert -- */
+/* Workspace bytes for ice_insert_tokens (zero-filled once before first use,
+ * like a decode workspace). */
+ice_status ice_insert_workspace_bytes(const ice_params *p, size_t *bytes);
+
+/*
+ * Step a11: appends one new token to every unit's index without a rebuild
+ * ([B] section 三: a new token goes through the same random promotion and is
+ * attached to the most similar parent one level up; [A] 关键设计 2: a node
+ * that outgrows its page opens a new page).  k_new, v_new [B, Hkv, d]
+ * (dtype).  The token's position is the unit's n_indexed (then n_indexed
+ * grows by one); it is lifted with the build-time M^2 (extra coordinate
+ * sqrt(max(0, M^2 - |k|^2))).  If its level-1 draw (the promotion rule of
+ * ice_build_lift_promote at that position) is below promote_thresh, it
+ * becomes a new parent with a page of its own.  Otherwise its parent is the
+ * nearest one in lifted space (exact fp32 ties to the lowest m), and it
+ * takes the next slot of that parent's last page, or a new page linked
+ * after it (page_next) when that page already holds S tokens.  Existing
+ * tokens never move.  Updates every index array and the pool.
+ * ICE_ERR_CAPACITY in err_dev (and that unit left unchanged) if n_cap,
+ * np_cap or page_cap would be exceeded.
+ */
+ice_status ice_insert_tokens(const ice_params *p, const ice_index *idx, const void *k_new, const void *v_new,
+                             void *ws, size_t ws_bytes, int32_t *err_dev, void *stream);
+
 /* ------------------------------------------------------- decode step ---- */
 /* Workspace bytes for ice_select_pages / ice_sparse_attn_decode /
  * ice_decode_step at this budget and output capacity max_sel.  A decode
@@ -297,6 +322,50 @@ ice_status ice_decode_step(const ice_params *p, const ice_index *idx, const void
                            int32_t *sel_pages, int32_t *sel_count, int32_t max_sel, void *kbuf, void *vbuf,
                            int32_t *buf_len, float scale, float *O, void *ws, size_t ws_bytes,
                            int32_t *err_dev, void *stream);
+
+/* ----------------------------------------------------- host page pool --- */
+/*
+ * Step a12: the page pool in pinned host memory, with the selected pages of
+ * a decode step moved to the device in one bulk transfer ([A] 关键设计 4:
+ * the non-contiguous selected pages are gathered into one contiguous host
+ * buffer and moved in a single transfer instead of many small ones; [B]
+ * section 四).  This is the one object the library allocates and owns.
+ */
+typedef struct ice_host_pool ice_host_pool;
+
+/* Allocates two pinned, device-mapped pools of pool_bytes each (K and V,
+ * laid out like ice_index.pool_k / pool_v: [U, page_cap, S, d]), a pinned
+ * staging buffer of staging_bytes (see ice_host_pool_staging_bytes) and
+ * n_threads host worker threads.  ICE_ERR_OOM if pinned memory runs out. */
+ice_status ice_host_pool_create(size_t pool_bytes, size_t staging_bytes, int32_t n_threads, ice_host_pool **out);
+/* Waits for the last staged transfer, joins the workers, frees everything. */
+ice_status ice_host_pool_destroy(ice_host_pool *hp);
+/* Device-visible and host pointers of the two pools (any may be NULL).  Put
+ * the device pointers into ice_index.pool_k / pool_v to build into the host
+ * pool and to let ice_decode_step / ice_gather_pages read pages straight
+ * from host memory over the CPU-GPU link, with no host copy. */
+ice_status ice_host_pool_pointers(const ice_host_pool *hp, void **pool_k_dev, void **pool_v_dev, void **pool_k_host,
+                                  void **pool_v_host);
+/* Staging bytes of one layer's transfer: kbuf | vbuf | buf_len for
+ * [U, max_sel] slots (2 * U * max_sel * S * d * elem + 4 * U * max_sel). */
+size_t ice_host_pool_staging_bytes(const ice_params *p, int32_t max_sel);
+/*
+ * Staged gather: host threads copy the selected pages of every unit from the
+ * host pool into the staging buffer (slot u * max_sel + x holds page
+ * sel_pages_host[u * max_sel + x] for x < sel_count_host[u]; buf_len 0
+ * beyond), then ONE cudaMemcpyAsync on `stream` moves the whole staging
+ * buffer to dst_dev, laid out as kbuf [U, max_sel, S, d] | vbuf (same) |
+ * buf_len [U, max_sel] int32 — ready for ice_sparse_attn_decode.
+ * sel_pages_host / sel_count_host are HOST copies of ice_select_pages'
+ * outputs (the caller copies them back and synchronises); page_len_host is
+ * a HOST copy of ice_index.page_len [U, page_cap].  Returns once the copy is
+ * enqueued; the next call first waits for this transfer to have read the
+ * staging buffer.  ICE_ERR_CAPACITY if the staging buffer or dst_bytes is
+ * too small, ICE_ERR_INVALID_ARG on a page id outside [0, page_cap).
+ */
+ice_status ice_host_pool_gather_h2d(ice_host_pool *hp, const ice_params *p, const int32_t *sel_pages_host,
+                                    const int32_t *sel_count_host, const int32_t *page_len_host, int32_t max_sel,
+                                    void *dst_dev, size_t dst_bytes, void *stream);
 
 #ifdef __cplusplus
 }

@@ -82,6 +82,13 @@ def load() -> ctypes.CDLL:
         "ice_sparse_attn_decode": ([pp, P, P, P, P, P, i32, f32, P, P, sz, P], i32),
         "ice_decode_step": ([pp, pi, P, i32, P, P, i32, P, P, P, f32, P, P, sz, P, P], i32),
         "ice_sparse_attn_decode_noalloc": ([pp, P, P, P, P, P, i32, f32, P, P], i32),
+        "ice_insert_workspace_bytes": ([pp, ctypes.POINTER(sz)], i32),
+        "ice_insert_tokens": ([pp, pi, P, P, P, sz, P, P], i32),
+        "ice_host_pool_create": ([sz, sz, i32, ctypes.POINTER(P)], i32),
+        "ice_host_pool_destroy": ([P], i32),
+        "ice_host_pool_pointers": ([P, ctypes.POINTER(P), ctypes.POINTER(P), ctypes.POINTER(P), ctypes.POINTER(P)], i32),
+        "ice_host_pool_staging_bytes": ([pp, i32], sz),
+        "ice_host_pool_gather_h2d": ([P, pp, P, P, P, i32, P, sz, P], i32),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -95,7 +102,9 @@ def exported_symbols() -> list[str]:
     return ["ice_status_string", "ice_last_error", "ice_version", "ice_check", "ice_page_bound",
             "ice_build_workspace_bytes", "ice_build_index", "ice_build_lift_promote", "ice_build_assign",
             "ice_build_assign_simt", "ice_build_pack", "ice_decode_workspace_bytes", "ice_select_pages",
-            "ice_gather_pages", "ice_sparse_attn_decode", "ice_sparse_attn_decode_noalloc", "ice_decode_step"]
+            "ice_gather_pages", "ice_sparse_attn_decode", "ice_sparse_attn_decode_noalloc", "ice_decode_step",
+            "ice_insert_workspace_bytes", "ice_insert_tokens", "ice_host_pool_create", "ice_host_pool_destroy",
+            "ice_host_pool_pointers", "ice_host_pool_staging_bytes", "ice_host_pool_gather_h2d"]
 
 
 # ----------------------------------------------------------- marshalling --
@@ -177,7 +186,7 @@ class Index:
     """Device arrays of one layer's index, allocated with torch (caller-owned
     memory in the C ABI's terms)."""
 
-    def __init__(self, cfg: Config, device="cuda", pool_device=None):
+    def __init__(self, cfg: Config, device="cuda", host_pool=None):
         U, Np, Pc, Nc, S, d = cfg.units, cfg.np_cap, cfg.page_cap, cfg.n_cap, cfg.page_size, cfg.head_dim
         i32, dt = torch.int32, cfg.torch_dtype
         z = lambda shape, t: torch.zeros(shape, dtype=t, device=device)
@@ -192,10 +201,15 @@ class Index:
         self.page_parent, self.page_len, self.page_next = z((U, Pc), i32), z((U, Pc), i32), z((U, Pc), i32)
         self.page_tokens = z((U, Pc, S), i32)
         self.token_parent, self.token_page, self.token_slot = z((U, Nc), i32), z((U, Nc), i32), z((U, Nc), i32)
-        pd = device if pool_device is None else pool_device
-        self.pool_k = torch.zeros((U, Pc, S, d), dtype=dt, device=pd)
-        self.pool_v = torch.zeros((U, Pc, S, d), dtype=dt, device=pd)
-        self._struct = IceIndex(*[getattr(self, f).data_ptr() for f in INDEX_FIELDS])
+        if host_pool is not None:  # pages live in the pinned host pool (device-mapped pointers)
+            self.host_pool = host_pool
+            self.pool_k = self.pool_v = None
+            ptrs = {"pool_k": host_pool.k_dev, "pool_v": host_pool.v_dev}
+        else:
+            self.pool_k = torch.zeros((U, Pc, S, d), dtype=dt, device=device)
+            self.pool_v = torch.zeros((U, Pc, S, d), dtype=dt, device=device)
+            ptrs = {}
+        self._struct = IceIndex(*[ptrs[f] if f in ptrs else getattr(self, f).data_ptr() for f in INDEX_FIELDS])
 
     @property
     def struct(self) -> IceIndex:
@@ -261,6 +275,68 @@ def ice_build_assign_simt(params, K, index, ws, err, stream=None):
 
 def ice_build_pack(params, K, V, index, ws, err, stream=None):
     _build_call("ice_build_pack", params, K, V, index, ws, err, stream)
+
+
+def ice_insert_workspace_bytes(params: IceParams) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().ice_insert_workspace_bytes(ctypes.byref(params), ctypes.byref(n)))
+    return n.value
+
+
+def ice_insert_tokens(params, index, k_new, v_new, ws, err, stream=None):
+    ix = index.struct if isinstance(index, Index) else index
+    _check(load().ice_insert_tokens(ctypes.byref(params), ctypes.byref(ix), _ptr(k_new), _ptr(v_new), _ptr(ws),
+                                    _nbytes(ws), _ptr(err), _stream(stream)))
+
+
+class HostPool:
+    """The library-owned pinned host page pool (ice_host_pool_*)."""
+
+    def __init__(self, cfg: "Config", max_sel: int, n_threads: int = 8):
+        esz = 2 if cfg.dtype == ICE_BF16 else 4
+        self.cfg = cfg
+        self.pool_bytes = cfg.units * cfg.page_cap * cfg.page_size * cfg.head_dim * esz
+        self.staging_bytes = int(load().ice_host_pool_staging_bytes(ctypes.byref(cfg.params()), max_sel))
+        h = ctypes.c_void_p()
+        _check_plain(load().ice_host_pool_create(self.pool_bytes, self.staging_bytes, n_threads, ctypes.byref(h)))
+        self.handle = h
+        kd, vd, kh, vh = (ctypes.c_void_p() for _ in range(4))
+        _check_plain(load().ice_host_pool_pointers(h, ctypes.byref(kd), ctypes.byref(vd), ctypes.byref(kh),
+                                                   ctypes.byref(vh)))
+        self.k_dev, self.v_dev, self.k_host, self.v_host = kd.value, vd.value, kh.value, vh.value
+
+    def host_array(self, which: str):
+        """numpy view of a host pool [U, page_cap, S, d] (storage dtype bits)."""
+        import numpy as np
+        cfg = self.cfg
+        n = self.pool_bytes // (2 if cfg.dtype == ICE_BF16 else 4)
+        ct = ctypes.c_uint16 if cfg.dtype == ICE_BF16 else ctypes.c_float
+        ptr = ctypes.cast(self.k_host if which == "k" else self.v_host, ctypes.POINTER(ct))
+        return np.ctypeslib.as_array(ptr, shape=(n,)).reshape(cfg.units, cfg.page_cap, cfg.page_size, cfg.head_dim)
+
+    def close(self):
+        if self.handle is not None:
+            load().ice_host_pool_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _check_plain(status: int):
+    if status != ICE_OK:
+        raise IceError(status, ice_status_string(status))
+
+
+def ice_host_pool_gather_h2d(pool: HostPool, params, sel_pages_host, sel_count_host, page_len_host, max_sel, dst,
+                             stream=None):
+    """sel_pages_host etc. are host (CPU) tensors; dst a device uint8 tensor."""
+    _check_plain(load().ice_host_pool_gather_h2d(pool.handle, ctypes.byref(params), _ptr(sel_pages_host),
+                                                 _ptr(sel_count_host), _ptr(page_len_host), max_sel, _ptr(dst),
+                                                 _nbytes(dst), _stream(stream)))
 
 
 def _nbytes(t) -> int:

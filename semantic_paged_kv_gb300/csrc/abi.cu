@@ -132,6 +132,24 @@ DecodeWs decode_ws_layout(const ice_params &p, int budget_tokens, int max_sel, v
     return w;
 }
 
+InsertWs insert_ws_layout(const ice_params &p, void *base) {
+    InsertWs w{};
+    const size_t U = (size_t)units_of(p);
+    w.n_chunks = ceil_div(p.np_cap, kSelChunk);
+    char *b = static_cast<char *>(base);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        char *r = b ? b + off : nullptr;
+        off += align256(bytes);
+        return r;
+    };
+    w.ticket = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * U));
+    w.best_s = reinterpret_cast<float *>(take(sizeof(float) * U * w.n_chunks));
+    w.best_m = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * U * w.n_chunks));
+    w.bytes = off;
+    return w;
+}
+
 }  // namespace ice
 
 using namespace ice;
@@ -249,6 +267,28 @@ ice_status ice_build_index(const ice_params *p, const void *K, const void *V, co
     if (st) return st;
     if ((st = ice_build_assign(p, K, idx, ws, ws_bytes, err_dev, stream))) return st;
     return ice_build_pack(p, K, V, idx, ws, ws_bytes, err_dev, stream);
+}
+
+// ------------------------------------------------------------- insert ----
+ice_status ice_insert_workspace_bytes(const ice_params *p, size_t *bytes) {
+    ice_status st = check_params(p);
+    if (st) return st;
+    if (!bytes) return fail(ICE_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = insert_ws_layout(*p, nullptr).bytes;
+    return ICE_OK;
+}
+
+ice_status ice_insert_tokens(const ice_params *p, const ice_index *idx, const void *k_new, const void *v_new,
+                             void *ws, size_t ws_bytes, int32_t *err_dev, void *stream) {
+    ice_status st = check_params(p);
+    if (st) return st;
+    if ((st = check_index(idx))) return st;
+    if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))
+        return fail(ICE_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned device pointers");
+    const InsertWs w = insert_ws_layout(*p, ws);
+    if ((st = check_ws(ws, ws_bytes, w.bytes))) return st;
+    return cuda_status(launch_insert(*p, *idx, k_new, v_new, w, err_dev, static_cast<cudaStream_t>(stream)),
+                       "ice_insert_tokens");
 }
 
 // ------------------------------------------------------------- decode ----

@@ -46,6 +46,17 @@ struct DecodeWs {
 };
 DecodeWs decode_ws_layout(const ice_params &p, int budget_tokens, int max_sel, void *base);
 
+struct InsertWs {
+    int32_t *ticket;  // [U]  zero between calls
+    float *best_s;    // [U, n_chunks]
+    int32_t *best_m;  // [U, n_chunks]
+    int n_chunks;
+    size_t bytes;
+};
+InsertWs insert_ws_layout(const ice_params &p, void *base);
+cudaError_t launch_insert(const ice_params &p, const ice_index &idx, const void *k_new, const void *v_new,
+                          const InsertWs &ws, int32_t *err, cudaStream_t s);
+
 // --------------------------------------------------------- launchers ------
 // Each returns cudaGetLastError() after enqueueing its kernels.
 cudaError_t launch_lift_promote(const ice_params &p, const void *K, const ice_index &idx, const BuildWs &ws,
