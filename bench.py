@@ -31,7 +31,32 @@ import workloads  # noqa: E402
 
 METRIC = "decode-step µs & HBM GB/s (select+gather+sparse attn); index-build keys/s"
 L2_BYTES = 129 * 2 ** 20
-KERNELS_PER_STEP = 8  # lift_count, promote_write, assign, pack_count, pack_scan, pack_rank_scatter, select, attn
+# kernels of one step: lift_count, promote_write, assign, pack_count, pack_scan,
+# pack_rank, pack_copy, select, attn
+KERNELS_PER_STEP = 9
+# CUDA-core fp32 peak from unit counts and clock: 152 SMs x 128 FMA/clk x 2 x 2.07 GHz
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+# DRAM bytes per launch of a kernel from one ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum) on the named workload, with the SHA-256 of the kernel's
+# source file at capture time; reported only while the source is unchanged.
+TRAFFIC = {
+    # profiles/assign_tc_llama31_8b_16k.md
+    "assign": {"workload": "llama31_8b_16k", "source": "build_assign_tc.cu", "bytes": 37356544,
+               "sha256": "b2d85a41b10c9196c9d978dd266d456bb602ee0c09fcba19b2e216728be006da"},
+}
+
+
+def measured_traffic(kernel: str, workload: str):
+    import hashlib
+    t = TRAFFIC.get(kernel)
+    if not t or t["workload"] != workload:
+        return None
+    src = os.path.join(ROOT, "semantic_paged_kv_gb300", "csrc", t["source"])
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    return t["bytes"] if sha == t["sha256"] else None
 
 
 def parse():
@@ -178,6 +203,30 @@ def config_of(w, budget, gpus, sets):
                   f"{sets} sets > 4x L2 combined)"}
 
 
+# ------------------------------------------------- multi-rank host logic ---
+def rank_workload(name: str, rank: int) -> workloads.Workload:
+    """Each rank owns its own batch of the workload: same shapes, its own
+    seed, so the ranks' units are disjoint and need no exchange."""
+    base = workloads.WORKLOADS[name]
+    return base.scaled(seed=base.seed + 1000 * rank)
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest of a host scalar over all ranks (the only collective)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, per_unit: int, steps: int, world: int, max_ms: float) -> float:
+    """Work of all ranks over the slowest rank's time (weak scaling)."""
+    return world * units_per_rank * per_unit * steps / (max_ms * 1e-3)
+
+
 # ------------------------------------------------------------- our arm ----
 def run_ours(args):
     import torch
@@ -194,12 +243,13 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
 
-    base = workloads.WORKLOADS[args.workload]
-    w = base.scaled(seed=base.seed + 1000 * rank)  # each rank owns its own batch
+    w = rank_workload(args.workload, rank)
     budget = args.budget or max(w.budgets)
     cfg = ice.Config(batch=w.batch, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, n_tokens=w.n_tokens,
                      dtype=ice.ICE_BF16 if w.dtype == "bf16" else ice.ICE_FP32, promote_p=w.promote_p, seed=w.seed)
     dt = cfg.torch_dtype
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    scale = 1.0 / math.sqrt(w.head_dim)
     sets = []
     for s in range(args.sets):
         K, V = workloads.batch_kv(w, layer=s)
@@ -214,30 +264,50 @@ def run_ours(args):
         st["buf"] = ice.DecodeBuffers(c, budget)
         st["Oh"] = torch.empty_like(st["buf"].O, device="cpu").pin_memory()
         sets.append(st)
-    err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    scale = 1.0 / math.sqrt(w.head_dim)
     set_bytes = sum(x.numel() * x.element_size() for x in (sets[0]["K"], sets[0]["V"], sets[0]["idx"].pool_k,
                                                            sets[0]["idx"].pool_v))
 
-    def step(st, evs=None):
+    # the four stages of a step, each a call into the C ABI
+    def stages(st):
         p, idx, buf = st["params"], st["idx"], st["buf"]
-        if evs: evs[0].record()
-        ice.ice_build_lift_promote(p, st["K"], idx, st["ws"], err)
-        if evs: evs[1].record()
-        ice.ice_build_assign(p, st["K"], idx, st["ws"], err)
-        if evs: evs[2].record()
-        ice.ice_build_pack(p, st["K"], st["V"], idx, st["ws"], err)
-        if evs: evs[3].record()
-        ice.ice_decode_step(p, idx, st["Q"], budget, buf.sel_pages, buf.sel_count, buf.kbuf, buf.vbuf, buf.buf_len,
-                            scale, buf.O, buf.ws, err)
-        if evs: evs[4].record()
+        return [
+            lambda: ice.ice_build_lift_promote(p, st["K"], idx, st["ws"], err),
+            lambda: ice.ice_build_assign(p, st["K"], idx, st["ws"], err),
+            lambda: ice.ice_build_pack(p, st["K"], st["V"], idx, st["ws"], err),
+            lambda: ice.ice_decode_step(p, idx, st["Q"], budget, buf.sel_pages, buf.sel_count, buf.kbuf, buf.vbuf,
+                                        buf.buf_len, scale, buf.O, buf.ws, err),
+        ]
 
     for i in range(max(args.warmup, 3)):
-        step(sets[i % len(sets)])
+        for f in stages(sets[i % len(sets)]):
+            f()
     torch.cuda.synchronize()
     status = ice.ice_check(err)
     if status != ice.ICE_OK:
         raise SystemExit(f"device reported status {status}: {ice.ice_status_string(status)}")
+    # capture each stage of each input set in a CUDA graph (launch overhead off the host)
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    for st in sets:
+        st["graphs"] = []
+        for f in stages(st):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                f()
+            st["graphs"].append(g)
+    torch.cuda.current_stream().wait_stream(cap)
+    torch.cuda.synchronize()
+
+    def step(st, evs=None):
+        for k, g in enumerate(st["graphs"]):
+            if evs:
+                evs[k].record()
+            g.replay()
+        if evs:
+            evs[4].record()
+
+    for i in range(2 * len(sets)):  # warm the graphs
+        step(sets[i % len(sets)])
 
     # ---- timed region: exactly `steps` steps
     E = lambda: torch.cuda.Event(enable_timing=True)
@@ -255,11 +325,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     barrier()
     clocks = sampler.stop()
-    elapsed_ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world, "cuda")
     stage = np.array([[e[k].elapsed_time(e[k + 1]) for k in range(4)] for e in evs])  # ms
     lift_ms, assign_ms, pack_ms, decode_ms = stage.mean(0)
 
@@ -283,14 +349,13 @@ def run_ours(args):
         "decode": (decode_ms, "hbm", decode_min_bytes / (decode_ms * 1e-3) / 1e9, pk["hbm"], "GB/s", decode_min_bytes),
     }
     if w.dtype != "bf16":
-        cands["assign"] = (assign_ms, "alu", flops_assign / (assign_ms * 1e-3) / 1e12, 37.0 * 2, "TFLOP/s",
+        cands["assign"] = (assign_ms, "alu", flops_assign / (assign_ms * 1e-3) / 1e12, FP32_ALU_TFLOPS, "TFLOP/s",
                            flops_assign)
     dom = max(cands, key=lambda k: cands[k][0])
     ms_, bound, ach, peak, unit, work = cands[dom]
-    keys_step = U * N
-    value = world * keys_step * args.steps / (elapsed_ms * 1e-3)
+    value = whole_job_rate(U, N, args.steps, world, elapsed_ms)
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end with host buffers: H2D of the inputs, the step, D2H of O
     e2e_steps = args.e2e_steps or min(args.steps, 100)
     h2d = sum(sets[0][k].numel() * sets[0][k].element_size() for k in ("Kh", "Vh", "Qh"))
     d2h = sets[0]["Oh"].numel() * 4
@@ -307,12 +372,8 @@ def run_ours(args):
         st["Oh"].copy_(st["buf"].O, non_blocking=True)
     b_.record()
     torch.cuda.synchronize()
-    e2e_ms = a.elapsed_time(b_)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e_value = world * keys_step * e2e_steps / (e2e_ms * 1e-3)
+    e2e_ms = max_over_ranks(a.elapsed_time(b_), world, "cuda")
+    e2e_value = whole_job_rate(U, N, e2e_steps, world, e2e_ms)
     status = ice.ice_check(err)
 
     cpu = None
@@ -324,6 +385,7 @@ def run_ours(args):
                          f"step at budget {budget}, one unit per host thread ({cdt:.1f} s)"}
 
     if rank == 0:
+        tr = measured_traffic(dom, w.name)
         line = {
             "metric": METRIC, "value": value, "unit": "keys/s", "n_gpus": world, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
@@ -333,15 +395,15 @@ def run_ours(args):
                 "decode_step_us": 1000 * decode_ms,
                 "decode_hbm_gbs_min_bytes": decode_min_bytes / (decode_ms * 1e-3) / 1e9,
                 "decode_hbm_gbs_pipeline_bytes": decode_pipe_bytes / (decode_ms * 1e-3) / 1e9,
-                "index_build_keys_per_s": keys_step / ((lift_ms + assign_ms + pack_ms) * 1e-3),
+                "index_build_keys_per_s": U * N / ((lift_ms + assign_ms + pack_ms) * 1e-3),
                 "build_us": {"lift_promote": 1000 * lift_ms, "assign": 1000 * assign_ms, "pack": 1000 * pack_ms},
                 "assign_tflops": flops_assign / (assign_ms * 1e-3) / 1e12,
                 "parents_per_step": np_tot, "pages_per_step": pages_tot, "selected_pages_per_step": sel_tot,
-                "set_bytes": set_bytes,
+                "set_bytes": set_bytes, "stages_as": "CUDA graphs, one per stage, events between them",
             },
             "roofline": {"kernel": dom, "bound": bound, "achieved": ach, "peak": peak, "unit": unit,
                          "frac": ach / peak, "peak_source": pk["src"] + (" burst" if bound == "tensor" else ""),
-                         "work_per_launch": work, "traffic": None},
+                         "work_per_launch": work, "traffic": tr},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "keys/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps},
