@@ -399,6 +399,10 @@ ice_status ice_decode_step(const ice_params *p, const ice_index *idx, const void
     if (!kbuf || !vbuf || !buf_len || !O) return fail(ICE_ERR_INVALID_ARG, "decode needs non-NULL kbuf, vbuf, buf_len and O");
     if (!aligned16(kbuf) || !aligned16(vbuf)) return fail(ICE_ERR_INVALID_ARG, "kbuf and vbuf must be 16-byte aligned");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (decode_cluster_supported(*p, w.k_pages, max_sel))
+        return cuda_status(launch_decode_cluster(*p, *idx, Q, w.k_pages, sel_pages, sel_count, max_sel, kbuf, vbuf,
+                                                 buf_len, scale, O, err_dev, s),
+                           "ice_decode_step");
     if ((st = cuda_status(launch_select(*p, *idx, Q, w, sel_pages, sel_count, max_sel, err_dev, s), "ice_decode_step select")))
         return st;
     return cuda_status(launch_attention(*p, idx, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, w, s),

@@ -79,6 +79,15 @@ cudaError_t launch_attention(const ice_params &p, const ice_index *pool, const i
                              const void *Q, void *kbuf, void *vbuf, int32_t *buf_len, const int32_t *sel_count,
                              int max_sel, float scale, float *O, const DecodeWs &ws, cudaStream_t s);
 
+// The whole decode step of a unit in one thread-block cluster (DSMEM
+// exchanges, hardware cluster barriers); supported when the unit's parent
+// slice and candidate lists fit its shared memory.
+constexpr int kDecodeCluster = 8;
+bool decode_cluster_supported(const ice_params &p, int k_pages, int max_sel);
+cudaError_t launch_decode_cluster(const ice_params &p, const ice_index &idx, const void *Q, int k_pages,
+                                  int32_t *sel_pages, int32_t *sel_count, int max_sel, void *kbuf, void *vbuf,
+                                  int32_t *buf_len, float scale, float *O, int32_t *err, cudaStream_t s);
+
 // Allocation-free attention: scratch in the library's static device array.
 size_t attention_noalloc_bytes(const ice_params &p, int max_sel);
 cudaError_t launch_attention_noalloc(const ice_params &p, const void *Q, const void *kbuf, const void *vbuf,

@@ -75,6 +75,7 @@ def test_host_pool_direct_and_staged_match_hbm_pool():
         O = torch.zeros_like(ref.O)
         ws = ice.workspace(ice.ice_decode_workspace_bytes(cfg.params(), budget, max_sel))
         ice.ice_sparse_attn_decode(cfg.params(), Qd, kbuf, vbuf, blen, ref.sel_count, 1.0 / np.sqrt(128), O, ws)
-        assert torch.equal(O, ref.O)
+        # a different split of the pages before the log-sum-exp merge than the fused step
+        assert torch.max(torch.abs(O - ref.O)).item() <= 1e-5
     finally:
         hp.close()

@@ -70,8 +70,10 @@ def test_fused_decode_equals_separate_calls():
     Q1, a, _ = run.decode(128, fused=True)
     Q2, b, _ = run.decode(128, fused=False)
     for x, y in [(a.sel_pages, b.sel_pages), (a.sel_count, b.sel_count), (a.kbuf, b.kbuf), (a.vbuf, b.vbuf),
-                 (a.buf_len, b.buf_len), (a.O, b.O)]:
+                 (a.buf_len, b.buf_len)]:
         assert torch.equal(x, y)
+    # the two paths split the pages differently before the log-sum-exp merge
+    assert torch.max(torch.abs(a.O - b.O)).item() <= 1e-5
 
 
 def test_qwen_shaped_g8_mha_longchat_shaped_g1():
