@@ -54,8 +54,14 @@ __global__ void __launch_bounds__(kThreads) k_lift_count(const T *__restrict__ K
         const long long j = wt0 + s * 8 + lane / 4;
         const uint4 *row = reinterpret_cast<const uint4 *>(Ku + (size_t)(j < N ? j : 0) * kHeadDim);
 #pragma unroll
-        for (int v = 0; v < VPL; ++v) buf[s][v] = (j < N) ? __ldg(row + (lane % 4) + 4 * v) : make_uint4(0, 0, 0, 0);
+        for (int v = 0; v < VPL; ++v) buf[s][v] = (j < N) ? ld_stream16(row + (lane % 4) + 4 * v) : make_uint4(0, 0, 0, 0);
     }
+    // every load above is issued before any of the arithmetic below
+#pragma unroll
+    for (int s = 0; s < STEPS; ++s)
+#pragma unroll
+        for (int v = 0; v < VPL; ++v)
+            asm volatile("" : "+r"(buf[s][v].x), "+r"(buf[s][v].y), "+r"(buf[s][v].z), "+r"(buf[s][v].w));
     double wmax = 0.0;
     double mine = 0.0;  // lane s*8 + token of step s keeps its own token's norm
 #pragma unroll

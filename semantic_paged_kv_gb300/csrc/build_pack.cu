@@ -201,6 +201,94 @@ __global__ void __launch_bounds__(kThreads) k_pack_rank(int N, int n_cap, int np
     }
 }
 
+// k_pack_rank when a warp-private counter per parent fits in shared memory:
+// warp w owns tokens [w*256, w*256 + 256) of the tile.  (1) each warp counts
+// its segment per parent (match_any groups, the group leader adds; the
+// counters are the warp's own, so no atomics); (2) per parent, an exclusive
+// scan over the 8 warps turns the counts into warp bases; (3) each warp ranks
+// its segment in token order from its bases.  Three block barriers per tile
+// instead of one per warp turn.
+constexpr int kSegWarps = kThreads / 32;
+constexpr int kSeg = kPackTile / kSegWarps;  // 256 tokens per warp
+
+__global__ void __launch_bounds__(kThreads) k_pack_rank_seg(int N, int n_cap, int np_cap, int page_cap, int n_tiles,
+                                                            const int32_t *__restrict__ n_parents,
+                                                            const int32_t *__restrict__ token_parent,
+                                                            const int32_t *__restrict__ pack_cnt,
+                                                            const int32_t *__restrict__ parent_first_page,
+                                                            int32_t *__restrict__ page_tokens,
+                                                            int32_t *__restrict__ token_page,
+                                                            int32_t *__restrict__ token_slot) {
+    extern __shared__ __align__(16) unsigned char s_raw[];
+    const int u = blockIdx.y, tile = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int Np = min(n_parents[u], np_cap);
+    int32_t *s_off = reinterpret_cast<int32_t *>(s_raw);                       // [Np] tile offsets
+    unsigned short *s_ctr = reinterpret_cast<unsigned short *>(s_off + np_cap);  // [8][Np]
+    const size_t un = (size_t)u * n_cap, up = (size_t)u * np_cap, ug = (size_t)u * page_cap;
+    const int32_t *row = pack_cnt + ((size_t)u * n_tiles + tile) * np_cap;
+    const long long j0 = (long long)tile * kPackTile + (long long)warp * kSeg;
+    int m[kSeg / 32];
+#pragma unroll
+    for (int i = 0; i < kSeg / 32; ++i) {
+        const long long j = j0 + i * 32 + lane;
+        const int v = j < N ? token_parent[un + j] : -1;
+        m[i] = (v >= 0 && v < Np) ? v : -1;
+    }
+    for (int x = threadIdx.x; x < Np; x += kThreads) s_off[x] = row[x];
+    for (int x = threadIdx.x; x < kSegWarps * Np; x += kThreads) s_ctr[x] = 0;
+    __syncthreads();
+    unsigned short *mine = s_ctr + (size_t)warp * Np;
+    // (1) counts of this warp's segment
+#pragma unroll
+    for (int i = 0; i < kSeg / 32; ++i) {
+        const int key = m[i] >= 0 ? m[i] : -1 - lane;
+        const unsigned peers = __match_any_sync(0xffffffffu, key);
+        if (m[i] >= 0 && lane == __ffs(peers) - 1) mine[m[i]] += (unsigned short)__popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    // (2) per parent: exclusive scan of the warp counts (within-tile bases)
+    for (int x = threadIdx.x; x < Np; x += kThreads) {
+        unsigned short run = 0;
+#pragma unroll
+        for (int w = 0; w < kSegWarps; ++w) {
+            const unsigned short c = s_ctr[(size_t)w * Np + x];
+            s_ctr[(size_t)w * Np + x] = run;
+            run = (unsigned short)(run + c);
+        }
+    }
+    __syncthreads();
+    // (3) ranks of this warp's segment, in token order
+#pragma unroll
+    for (int i = 0; i < kSeg / 32; ++i) {
+        const int mm = m[i];
+        const int key = mm >= 0 ? mm : -1 - lane;
+        const unsigned peers = __match_any_sync(0xffffffffu, key);
+        const int leader = __ffs(peers) - 1;
+        int base = 0;
+        if (mm >= 0 && lane == leader) {
+            base = mine[mm];
+            mine[mm] = (unsigned short)(base + __popc(peers));
+        }
+        base = __shfl_sync(0xffffffffu, base, leader);
+        __syncwarp();
+        if (mm >= 0) {
+            const long long j = j0 + i * 32 + lane;
+            const int rank = s_off[mm] + base + __popc(peers & lanemask_lt());
+            const long long pg = (long long)parent_first_page[up + mm] + rank / kPage;
+            const int slot = rank % kPage;
+            if (pg < page_cap) {
+                page_tokens[(ug + pg) * kPage + slot] = (int32_t)j;
+                token_page[un + j] = (int32_t)pg;
+                token_slot[un + j] = slot;
+            }
+        }
+    }
+}
+
+size_t rank_seg_smem(int np_cap) { return (size_t)np_cap * (sizeof(int32_t) + kSegWarps * sizeof(unsigned short)); }
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads) k_pack_copy(const T *__restrict__ K, const T *__restrict__ V, int N,
                                                         int page_cap, const int32_t *__restrict__ n_pages,
@@ -255,9 +343,20 @@ cudaError_t launch_t(const ice_params &p, const void *K, const void *V, const ic
                                            idx.n_pages, idx.parent_first_page, idx.parent_last_page,
                                            idx.parent_n_pages, idx.page_parent, idx.page_len, idx.page_next,
                                            idx.page_tokens, err);
-    k_pack_rank<<<grid, kThreads, smem, s>>>(p.n_tokens, p.n_cap, p.np_cap, p.page_cap, tiles, smem_path,
-                                             idx.n_parents, idx.token_parent, ws.pack_cnt, idx.parent_first_page,
-                                             idx.page_tokens, idx.token_page, idx.token_slot);
+    const size_t seg_smem = rank_seg_smem(p.np_cap);
+    if (smem_path && seg_smem <= 200 * 1024) {
+        if (seg_smem > 48 * 1024)
+            cudaFuncSetAttribute(k_pack_rank_seg, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)seg_smem);
+        k_pack_rank_seg<<<grid, kThreads, seg_smem, s>>>(p.n_tokens, p.n_cap, p.np_cap, p.page_cap, tiles,
+                                                         idx.n_parents, idx.token_parent, ws.pack_cnt,
+                                                         idx.parent_first_page, idx.page_tokens, idx.token_page,
+                                                         idx.token_slot);
+    } else {
+        k_pack_rank<<<grid, kThreads, smem, s>>>(p.n_tokens, p.n_cap, p.np_cap, p.page_cap, tiles, smem_path,
+                                                 idx.n_parents, idx.token_parent, ws.pack_cnt,
+                                                 idx.parent_first_page, idx.page_tokens, idx.token_page,
+                                                 idx.token_slot);
+    }
     dim3 cgrid(ceil_div(p.page_cap, kThreads / 32), U);
     k_pack_copy<T><<<cgrid, kThreads, 0, s>>>(static_cast<const T *>(K), static_cast<const T *>(V), p.n_tokens,
                                               p.page_cap, idx.n_pages, idx.page_len, idx.page_tokens,

@@ -48,6 +48,17 @@ template <typename T> constexpr int row_bytes() { return kHeadDim * (int)sizeof(
 // 16-byte vectors per row.
 template <typename T> constexpr int row_vecs() { return row_bytes<T>() / 16; }
 
+// 16-byte read-only load issued in program order (volatile asm is not
+// reordered with other volatile asm), so a batch of them is in flight before
+// the arithmetic that consumes them; no L1 allocation (data read once).
+__device__ __forceinline__ uint4 ld_stream16(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
 // ------------------------------------------------------------ splitmix64 --
 // splitmix64 (Steele, Lea & Flood 2014): state advances by the golden-ratio
 // increment; an output is the state run through the 64-bit finaliser.
