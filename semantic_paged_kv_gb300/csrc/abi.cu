@@ -100,6 +100,8 @@ BuildWs build_ws_layout(const ice_params &p, void *base) {
     w.pcount = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * U * tp));
     w.tile_max = reinterpret_cast<double *>(take(sizeof(double) * U * tp));
     w.tile_min = reinterpret_cast<unsigned long long *>(take(sizeof(unsigned long long) * U * tp));
+    w.a_extra = reinterpret_cast<uint4 *>(take(32 * U * N));
+    w.b_extra = reinterpret_cast<uint4 *>(take(32 * U * (size_t)p.np_cap));
     w.pack_cnt = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * U * tk * (size_t)p.np_cap));
     w.pack_total = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * U * (size_t)p.np_cap));
     w.bytes = off;

@@ -7,26 +7,32 @@
 // nearest parent one level up.  With every lifted key of norm M,
 //   argmin_m |k'_j - p'_m|^2 = argmax_m (k_j . p_m + e_j e_m),
 // a dense contraction of the keys with the parent keys followed by a row
-// argmax.  bf16 products are exact in fp32; the sum is accumulated in fp32.
+// argmax.  The whole score is one contraction here: each key row carries 16
+// extra bf16 columns [e1, e1, e2, e1, e2, e3, 0...] and each parent row
+// [f1, f2, f1, f3, f2, f1, 0...] (e = e1 + e2 + e3, f likewise, split into
+// bf16 parts by the promotion kernel), whose products give e_j e_m to about
+// 2^-23 relative; all bf16 products are exact in fp32 and the sum is
+// accumulated in fp32.
 //
 // Persistent kernel, one CTA per SM (10 warps), looping over work items =
 // (unit, 128-token tile) in unit-major order, so that the CTAs working at
 // the same time share one unit's parent table in L2:
-//   warp 0      TMA producer: per item the 128x128 key tile into one of two
-//               key buffers, then the unit's parent keys in 256-row tiles
-//               through a 2-stage ring (128-byte swizzle, two 64-column
-//               halves per tile);
+//   warp 0      TMA producer: per item the 128x128 key tile (128-byte
+//               swizzle, two 64-column halves) and its 128x16 extra tile
+//               (32-byte swizzle) into one of two key buffers, then the
+//               unit's parent keys and parent extras in 256-row tiles
+//               through a 2-stage ring;
 //   warp 1      allocates 512 TMEM columns and issues tcgen05.mma
-//               (M=128, N=256, K=16, bf16 -> fp32) into one of two TMEM
-//               accumulators, committing to the ring's empty barrier, the
-//               accumulator's full barrier and, after an item's last tile,
-//               the key buffer's empty barrier;
+//               (M=128, N=256, K=16, bf16 -> fp32; 8 K-steps of keys plus
+//               one of extras) into one of two TMEM accumulators, committing
+//               to the ring's empty barrier, the accumulator's full barrier
+//               and, after an item's last tile, the key buffer's empty
+//               barrier;
 //   warps 2..9  epilogue: warp w reads TMEM lane quarter w % 4 and column
-//               half (w - 2) / 4; 64 columns per tcgen05 wait; score =
-//               acc + e_j e_m, running argmax with the lowest index on exact
-//               ties; the two halves of a row combine through shared memory
-//               at the end of the item.  The parent coordinates e_m of the
-//               next tile are prefetched into registers.
+//               half (w - 2) / 4, 64 columns per tcgen05 wait, and keeps a
+//               running argmax with the lowest index on exact ties; the two
+//               halves of a row combine through shared memory at the end of
+//               the item.  The next item's promoted flags are prefetched.
 // Every mbarrier wait gives up after ~2 s (globaltimer) and records
 // ICE_ERR_TIMEOUT; roles drain what they issued and TMEM is freed before
 // the CTA returns.
@@ -44,10 +50,13 @@ constexpr int NSTAGE = 2;    // parent-tile ring depth
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kThreads = 64 + kEpiThreads;
-constexpr uint32_t A_HALF = BM * 128;     // 128 rows x 128 bytes (64 bf16 columns)
-constexpr uint32_t A_BYTES = 2 * A_HALF;  // d = 128 -> two halves
+constexpr int kExtra = 16;                  // extra K columns (bf16)
+constexpr uint32_t A_HALF = BM * 128;       // 128 rows x 128 bytes (64 bf16 columns)
+constexpr uint32_t A_BYTES = 2 * A_HALF;    // d = 128 -> two halves
+constexpr uint32_t A2_BYTES = BM * kExtra * 2;
 constexpr uint32_t B_HALF = BN * 128;
 constexpr uint32_t B_STAGE = 2 * B_HALF;
+constexpr uint32_t B2_STAGE = BN * kExtra * 2;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr unsigned long long kWaitNs = 2000000000ull;
 // kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major, N, M.
@@ -60,8 +69,8 @@ struct Bars {
     int comb_i[BM];
     uint32_t tmem_base;
 };
-constexpr size_t kSmemBytes =
-    1024 /*align slack*/ + 2 * A_BYTES + NSTAGE * B_STAGE + 2 * BN * sizeof(float) + sizeof(Bars);
+constexpr size_t kSmemBytes = 1024 /*align slack*/ + 2 * A_BYTES + NSTAGE * B_STAGE + 2 * A2_BYTES +
+                              NSTAGE * B2_STAGE + sizeof(Bars);
 
 __device__ __forceinline__ uint32_t su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -105,11 +114,16 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
         "l"(reinterpret_cast<uint64_t>(map)), "r"(su32(bar)), "r"(x), "r"(y)
         : "memory");
 }
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
-// 1024 bytes apart (stride byte offset), descriptor version 1.
+// Shared-memory matrix descriptors, K-major, descriptor version 1:
+// 128-byte swizzle (8-row groups 1024 bytes apart) for the 64-column halves,
+// 32-byte swizzle (8-row groups 256 bytes apart) for the 16-column extras.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+__device__ __forceinline__ uint64_t sw32_desc(uint32_t saddr) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(256 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)6 << 61);
 }
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
     asm volatile(
@@ -157,16 +171,17 @@ __device__ __forceinline__ Item item_of(int item, int mt_per_unit, const int32_t
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    k_assign_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmP, int N, int np_cap,
+    k_assign_tc(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmP,
+                const __grid_constant__ CUtensorMap tmK2, const __grid_constant__ CUtensorMap tmP2, int N, int np_cap,
                 int n_cap, int n_items, int mt_per_unit, const int32_t *__restrict__ n_parents,
-                const double *__restrict__ m2, const double *__restrict__ norm2,
-                const float *__restrict__ parent_e, int32_t *__restrict__ token_parent, int32_t *__restrict__ err) {
+                int32_t *__restrict__ token_parent, int32_t *__restrict__ err) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    unsigned char *sA = smem;  // two key buffers
-    unsigned char *sB = smem + 2 * A_BYTES;
-    float *sE = reinterpret_cast<float *>(sB + NSTAGE * B_STAGE);
-    Bars *bars = reinterpret_cast<Bars *>(sE + 2 * BN);
+    unsigned char *sA = smem;                         // two key buffers
+    unsigned char *sB = sA + 2 * A_BYTES;             // parent ring
+    unsigned char *sA2 = sB + NSTAGE * B_STAGE;       // two key-extra buffers
+    unsigned char *sB2 = sA2 + 2 * A2_BYTES;          // parent-extra ring
+    Bars *bars = reinterpret_cast<Bars *>(sB2 + NSTAGE * B2_STAGE);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x;
@@ -209,9 +224,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 unsigned char *a = sA + ab * A_BYTES;
-                mbar_expect_tx(&bars->a_full[ab], A_BYTES);
-                tma_load_2d(a, &tmK, &bars->a_full[ab], 0, I.u * N + I.m0);
-                tma_load_2d(a + A_HALF, &tmK, &bars->a_full[ab], 64, I.u * N + I.m0);
+                const int row0 = I.u * N + I.m0;
+                mbar_expect_tx(&bars->a_full[ab], A_BYTES + A2_BYTES);
+                tma_load_2d(a, &tmK, &bars->a_full[ab], 0, row0);
+                tma_load_2d(a + A_HALF, &tmK, &bars->a_full[ab], 64, row0);
+                tma_load_2d(sA2 + ab * A2_BYTES, &tmK2, &bars->a_full[ab], 0, row0);
                 last_a = it;
                 for (int t = 0; t < I.T; ++t, ++gt) {
                     const int s = gt % NSTAGE;
@@ -221,9 +238,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     unsigned char *dst = sB + s * B_STAGE;
                     const int y = I.u * np_cap + t * BN;
-                    mbar_expect_tx(&bars->full[s], B_STAGE);
+                    mbar_expect_tx(&bars->full[s], B_STAGE + B2_STAGE);
                     tma_load_2d(dst, &tmP, &bars->full[s], 0, y);
                     tma_load_2d(dst + B_HALF, &tmP, &bars->full[s], 64, y);
+                    tma_load_2d(sB2 + s * B2_STAGE, &tmP2, &bars->full[s], 0, y);
                 }
             }
             // drain: every issued copy has landed before the CTA may exit
@@ -244,6 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const uint32_t a0 = su32(sA + ab * A_BYTES);
+                const uint32_t a2 = su32(sA2 + ab * A2_BYTES);
                 for (int t = 0; t < I.T; ++t, ++gt) {
                     const int s = gt % NSTAGE, b = gt & 1;
                     if (!mbar_wait(&bars->tempty[b], ((gt >> 1) & 1) ^ 1) ||
@@ -260,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t db = sw128_desc(b0 + (k >> 2) * B_HALF + off);
                         umma_bf16(tmem + b * BN, da, db, k > 0 ? 1u : 0u);
                     }
+                    umma_bf16(tmem + b * BN, sw32_desc(a2), sw32_desc(su32(sB2 + s * B2_STAGE)), 1u);
                     umma_commit(&bars->empty[s]);
                     umma_commit(&bars->tfull[b]);
                 }
@@ -271,48 +291,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // -------------------------------------------------------- epilogue
-        const int ew = warp - 2;          // 0..7
-        const int q = warp & 3;           // TMEM lane quarter this warp may access
-        const int hf = ew >> 2;           // column half of each 256-column tile
+        const int ew = warp - 2;  // 0..7
+        const int q = warp & 3;   // TMEM lane quarter this warp may access
+        const int hf = ew >> 2;   // column half of each 256-column tile
         const int row = q * 32 + lane;
-        const int et = threadIdx.x - 64;  // 0..255
         int gt = 0;
-        // prefetch cursor (one tile ahead) for the parent coordinates e_m
-        int p_item = blockIdx.x, p_t = 0;
-        Item P = p_item < n_items ? item_of(p_item, mt_per_unit, n_parents, np_cap) : Item{0, 0, 0, 0};
-        float e_next = 0.f;
-        if (p_item < n_items && et < P.Np) e_next = __ldg(parent_e + (size_t)P.u * np_cap + et);
+        Item I = blockIdx.x < n_items ? item_of(blockIdx.x, mt_per_unit, n_parents, np_cap) : Item{0, 0, 0, 0};
+        int r_tp = -1;  // token_parent seed of this row (>= 0: promoted, keeps itself)
+        if (blockIdx.x < n_items && (long long)I.m0 + row < N) r_tp = token_parent[(size_t)I.u * n_cap + I.m0 + row];
         for (int item = blockIdx.x; item < n_items; item += G) {
-            const Item I = item_of(item, mt_per_unit, n_parents, np_cap);
             const long long j = (long long)I.m0 + row;
-            float ej = 0.f;
-            if (j < N) {
-                const double r = m2[I.u] - norm2[(size_t)I.u * N + j];
-                ej = (float)sqrt(r > 0.0 ? r : 0.0);
-            }
+            const bool promoted = r_tp >= 0;
+            // the next item's row data, loaded while this item runs
+            const int nitem = item + G;
+            const Item In = nitem < n_items ? item_of(nitem, mt_per_unit, n_parents, np_cap) : Item{0, 0, 0, 0};
+            if (nitem < n_items && (long long)In.m0 + row < N) r_tp = token_parent[(size_t)In.u * n_cap + In.m0 + row];
             float best = -INFINITY;
             int bidx = 0x7fffffff;
             for (int t = 0; t < I.T; ++t, ++gt) {
                 const int b = gt & 1;
-                float *se = sE + b * BN;
-                se[et] = e_next;
-                // advance the prefetch cursor and load the next tile's e_m
-                if (++p_t >= P.T) {
-                    p_t = 0;
-                    p_item += G;
-                    if (p_item < n_items) P = item_of(p_item, mt_per_unit, n_parents, np_cap);
-                }
-                e_next = 0.f;
-                if (p_item < n_items && p_t * BN + et < P.Np)
-                    e_next = __ldg(parent_e + (size_t)P.u * np_cap + p_t * BN + et);
-                asm volatile("bar.sync 1, %0;" ::"r"(kEpiThreads) : "memory");
-                // a failed wait stops this warp's work but not its barrier turns
+                // a failed wait stops this warp's work
                 if (ok) ok = mbar_wait(&bars->tfull[b], (gt >> 1) & 1);
                 ok = __all_sync(0xffffffffu, ok);
                 tc_fence_after();
                 const int c_lo = t * BN + hf * (BN / 2);
                 const int valid = ok ? max(0, min(BN / 2, I.Np - c_lo)) : 0;
-                const float *seh = se + hf * (BN / 2);
                 for (int c0 = 0; c0 < valid; c0 += 64) {
                     float v[64];
                     const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + hf * (BN / 2) + c0);
@@ -322,18 +325,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float cmax = -INFINITY;
                     if (valid - c0 >= 64) {
 #pragma unroll
-                        for (int i = 0; i < 64; ++i) {
-                            v[i] = fmaf(ej, seh[c0 + i], v[i]);
-                            cmax = fmaxf(cmax, v[i]);
-                        }
+                        for (int i = 0; i < 64; i += 4)
+                            cmax = fmaxf(cmax, fmaxf(fmaxf(v[i], v[i + 1]), fmaxf(v[i + 2], v[i + 3])));
                     } else {
 #pragma unroll
                         for (int i = 0; i < 64; ++i) {
-                            v[i] = (c0 + i < valid) ? fmaf(ej, seh[c0 + i], v[i]) : -INFINITY;
+                            v[i] = (c0 + i < valid) ? v[i] : -INFINITY;
                             cmax = fmaxf(cmax, v[i]);
                         }
                     }
-                    if (cmax > best) {
+                    if (cmax > best) {  // columns ascend, so only a strictly larger score moves the argmax
                         int first = 0;
 #pragma unroll
                         for (int i = 63; i >= 0; --i)
@@ -358,12 +359,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     best = os;
                     bidx = oi;
                 }
-                if (ok && j < N && I.Np > 0) {
-                    int32_t *tp = token_parent + (size_t)I.u * n_cap + j;
-                    if (*tp < 0) *tp = bidx;  // promoted tokens keep themselves
-                }
+                // promoted tokens keep themselves as parent
+                if (ok && j < N && I.Np > 0 && !promoted) token_parent[(size_t)I.u * n_cap + j] = bidx;
             }
             asm volatile("bar.sync 2, %0;" ::"r"(kEpiThreads) : "memory");
+            I = In;
         }
     }
     if (!ok) set_err(err, ICE_ERR_TIMEOUT);
@@ -393,16 +393,17 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2-D bf16 map over rows of 128 elements (256 bytes), box {64, box_rows}, 128-byte swizzle.
-bool make_map(CUtensorMap *m, const void *base, unsigned long long rows, unsigned box_rows) {
+// 2-D bf16 map over rows of `cols` elements, box {box_cols, box_rows}.
+bool make_map(CUtensorMap *m, const void *base, unsigned long long rows, unsigned cols, unsigned box_cols,
+              unsigned box_rows, CUtensorMapSwizzle sw) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
-    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -412,9 +413,12 @@ cudaError_t launch_assign_tc(const ice_params &p, const void *K, const ice_index
                              int32_t *err, cudaStream_t s) {
     if (p.dtype != ICE_BF16) return launch_assign_simt(p, K, idx, ws, err, s);
     const int U = units_of(p);
-    CUtensorMap tmK, tmP;
-    if (!make_map(&tmK, K, (unsigned long long)U * p.n_tokens, BM) ||
-        !make_map(&tmP, idx.parent_keys, (unsigned long long)U * p.np_cap, BN))
+    CUtensorMap tmK, tmP, tmK2, tmP2;
+    const unsigned long long kr = (unsigned long long)U * p.n_tokens, pr = (unsigned long long)U * p.np_cap;
+    if (!make_map(&tmK, K, kr, kHeadDim, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&tmP, idx.parent_keys, pr, kHeadDim, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&tmK2, ws.a_extra, kr, kExtra, kExtra, BM, CU_TENSOR_MAP_SWIZZLE_32B) ||
+        !make_map(&tmP2, ws.b_extra, pr, kExtra, kExtra, BN, CU_TENSOR_MAP_SWIZZLE_32B))
         return cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {
@@ -432,8 +436,8 @@ cudaError_t launch_assign_tc(const ice_params &p, const void *K, const ice_index
     const int mt = ceil_div(p.n_tokens, BM);
     const int items = mt * U;
     const int grid = items < n_sm ? items : n_sm;
-    k_assign_tc<<<grid, kThreads, kSmemBytes, s>>>(tmK, tmP, p.n_tokens, p.np_cap, p.n_cap, items, mt, idx.n_parents,
-                                                   idx.m2, ws.norm2, idx.parent_e, idx.token_parent, err);
+    k_assign_tc<<<grid, kThreads, kSmemBytes, s>>>(tmK, tmP, tmK2, tmP2, p.n_tokens, p.np_cap, p.n_cap, items, mt,
+                                                   idx.n_parents, idx.token_parent, err);
     return cudaGetLastError();
 }
 

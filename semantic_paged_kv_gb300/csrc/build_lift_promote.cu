@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(kThreads) k_promote_write(
     int32_t *__restrict__ n_parents,
     int32_t *__restrict__ n_indexed, int32_t *__restrict__ parent_tok, T *__restrict__ parent_keys,
     float *__restrict__ parent_e, float *__restrict__ parent_corr, int32_t *__restrict__ token_parent,
-    int32_t *__restrict__ err) {
+    uint4 *__restrict__ a_extra, uint4 *__restrict__ b_extra, int32_t *__restrict__ err) {
     const int u = blockIdx.y, tile = blockIdx.x;
     const int seq = u / n_kv_heads, head = u % n_kv_heads;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -220,13 +220,35 @@ __global__ void __launch_bounds__(kThreads) k_promote_write(
     const int m = base + local;
     if (j < N) {
         int32_t tp = -1;
+        const double r = M2 - norm2[(size_t)u * N + j];
+        const double e = sqrt(r > 0.0 ? r : 0.0);
+        // e as three bf16 parts e1 + e2 + e3 (24 significant bits): the extra
+        // K columns of the tensor-core contraction, [e1, e1, e2, e1, e2, e3]
+        // for the token and [e1, e2, e1, e3, e2, e1] for a parent, whose dot
+        // product holds every term e_a f_b with a + b <= 4.
+        __nv_bfloat16 e1 = __double2bfloat16(e);
+        const double r1 = e - (double)__bfloat162float(e1);
+        __nv_bfloat16 e2 = __double2bfloat16(r1);
+        __nv_bfloat16 e3 = __double2bfloat16(r1 - (double)__bfloat162float(e2));
+        const __nv_bfloat16 z = __float2bfloat16(0.f);
+        if (a_extra) {
+            const __nv_bfloat16 row[16] = {e1, e1, e2, e1, e2, e3, z, z, z, z, z, z, z, z, z, z};
+            const uint4 *w = reinterpret_cast<const uint4 *>(row);
+            a_extra[((size_t)u * N + j) * 2 + 0] = w[0];
+            a_extra[((size_t)u * N + j) * 2 + 1] = w[1];
+        }
         if (f && m < np_cap) {
             tp = m;
             const size_t up = (size_t)u * np_cap;
             parent_tok[up + m] = (int32_t)j;
-            const double r = M2 - norm2[(size_t)u * N + j];
-            parent_e[up + m] = (float)sqrt(r > 0.0 ? r : 0.0);
+            parent_e[up + m] = (float)e;
             parent_corr[up + m] = 0.f;
+            if (b_extra) {
+                const __nv_bfloat16 prow[16] = {e1, e2, e1, e3, e2, e1, z, z, z, z, z, z, z, z, z, z};
+                const uint4 *w = reinterpret_cast<const uint4 *>(prow);
+                b_extra[(up + m) * 2 + 0] = w[0];
+                b_extra[(up + m) * 2 + 1] = w[1];
+            }
         }
         token_parent[(size_t)u * n_cap + j] = tp;
         if (f) {
@@ -260,7 +282,8 @@ cudaError_t launch_lift_promote_t(const ice_params &p, const void *K, const ice_
     k_promote_write<T><<<grid, kThreads, 0, s>>>(
         static_cast<const T *>(K), N, p.n_kv_heads, p.promote_thresh, key, p.np_cap, p.n_cap, idx.m2, ws.norm2,
         ws.pcount, ws.tile_max, ws.tile_min, tiles, idx.n_parents, idx.n_indexed, idx.parent_tok,
-        static_cast<T *>(idx.parent_keys), idx.parent_e, idx.parent_corr, idx.token_parent, err);
+        static_cast<T *>(idx.parent_keys), idx.parent_e, idx.parent_corr, idx.token_parent,
+        p.dtype == ICE_BF16 ? ws.a_extra : nullptr, p.dtype == ICE_BF16 ? ws.b_extra : nullptr, err);
     return cudaGetLastError();
 }
 

@@ -28,6 +28,8 @@ struct BuildWs {
     int32_t *pcount;      // [U, Tp] promoted tokens per lift tile
     double *tile_max;     // [U, Tp] largest |k|^2 of each lift tile
     unsigned long long *tile_min;  // [U, Tp] smallest draw << 32 | token of each lift tile
+    uint4 *a_extra;       // [U, N, 16] bf16: split lifted coordinate of each token (tensor-core K tail)
+    uint4 *b_extra;       // [U, np_cap, 16] bf16: the same for each parent
     int32_t *pack_cnt;    // [U, Tk, np_cap] per-tile parent counts -> offsets
     int32_t *pack_total;  // [U, np_cap] tokens per parent
     size_t bytes;
