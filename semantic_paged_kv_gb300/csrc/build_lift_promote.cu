@@ -32,7 +32,7 @@ constexpr int kThreads = kLiftTile;  // one token per thread
 constexpr int kWarps = kThreads / 32;
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads) k_lift_count(const T *__restrict__ K, int N, int n_kv_heads,
+__global__ void __launch_bounds__(kThreads, 3) k_lift_count(const T *__restrict__ K, int N, int n_kv_heads,
                                                          uint64_t thresh, uint64_t key,
                                                          double *__restrict__ norm2, int32_t *__restrict__ pcount,
                                                          double *__restrict__ tile_max,
@@ -62,8 +62,7 @@ __global__ void __launch_bounds__(kThreads) k_lift_count(const T *__restrict__ K
 #pragma unroll
         for (int v = 0; v < VPL; ++v)
             asm volatile("" : "+r"(buf[s][v].x), "+r"(buf[s][v].y), "+r"(buf[s][v].z), "+r"(buf[s][v].w));
-    double wmax = 0.0;
-    double mine = 0.0;  // lane s*8 + token of step s keeps its own token's norm
+    float mine_hi = 0.f, mine_lo = 0.f;  // lane s*8 + t keeps token s*8 + t's norm
 #pragma unroll
     for (int s = 0; s < STEPS; ++s) {
         float hi = 0.f, lo = 0.f;
@@ -90,15 +89,20 @@ __global__ void __launch_bounds__(kThreads) k_lift_count(const T *__restrict__ K
             hi = sum;
             lo += olo + err;
         }
-        const double n = (double)hi + (double)lo;
         // token (s*8 + lane/4) of the warp: hand it to lane s*8 + lane/4
-        const double got = __shfl_sync(0xffffffffu, n, ((lane - s * 8) & 7) * 4);
-        if (lane / 8 == s) mine = got;
+        const float ghi = __shfl_sync(0xffffffffu, hi, ((lane - s * 8) & 7) * 4);
+        const float glo = __shfl_sync(0xffffffffu, lo, ((lane - s * 8) & 7) * 4);
+        if (lane / 8 == s) {
+            mine_hi = ghi;
+            mine_lo = glo;
+        }
     }
     const long long j = wt0 + lane;
+    double wmax = 0.0;  // one conversion per token: the fp64 units are few
     if (j < N) {
-        norm2[(size_t)u * N + j] = mine;
-        wmax = mine;
+        const double n = (double)mine_hi + (double)mine_lo;
+        norm2[(size_t)u * N + j] = n;
+        wmax = n;
     }
     // ---- promotion draw of this thread's token
     int cnt = 0;
@@ -220,16 +224,20 @@ __global__ void __launch_bounds__(kThreads) k_promote_write(
     const int m = base + local;
     if (j < N) {
         int32_t tp = -1;
+        // M^2 - |k|^2 is exact in fp64 to ~2^-52 M^2; rounded to fp32, its
+        // square root is within 1.5 ulp of the exact e (fp32 sqrt: the fp64
+        // units are few on this part)
         const double r = M2 - norm2[(size_t)u * N + j];
-        const double e = sqrt(r > 0.0 ? r : 0.0);
-        // e as three bf16 parts e1 + e2 + e3 (24 significant bits): the extra
-        // K columns of the tensor-core contraction, [e1, e1, e2, e1, e2, e3]
-        // for the token and [e1, e2, e1, e3, e2, e1] for a parent, whose dot
-        // product holds every term e_a f_b with a + b <= 4.
-        __nv_bfloat16 e1 = __double2bfloat16(e);
-        const double r1 = e - (double)__bfloat162float(e1);
-        __nv_bfloat16 e2 = __double2bfloat16(r1);
-        __nv_bfloat16 e3 = __double2bfloat16(r1 - (double)__bfloat162float(e2));
+        const float e = sqrtf(r > 0.0 ? (float)r : 0.f);
+        // e as three bf16 parts e1 + e2 + e3 (24 significant bits, each
+        // remainder exact in fp32): the extra K columns of the tensor-core
+        // contraction, [e1, e1, e2, e1, e2, e3] for the token and
+        // [e1, e2, e1, e3, e2, e1] for a parent, whose dot product holds every
+        // term e_a f_b with a + b <= 4.
+        const __nv_bfloat16 e1 = __float2bfloat16_rn(e);
+        const float r1 = e - __bfloat162float(e1);
+        const __nv_bfloat16 e2 = __float2bfloat16_rn(r1);
+        const __nv_bfloat16 e3 = __float2bfloat16_rn(r1 - __bfloat162float(e2));
         const __nv_bfloat16 z = __float2bfloat16(0.f);
         if (a_extra) {
             const __nv_bfloat16 row[16] = {e1, e1, e2, e1, e2, e3, z, z, z, z, z, z, z, z, z, z};
@@ -241,7 +249,7 @@ __global__ void __launch_bounds__(kThreads) k_promote_write(
             tp = m;
             const size_t up = (size_t)u * np_cap;
             parent_tok[up + m] = (int32_t)j;
-            parent_e[up + m] = (float)e;
+            parent_e[up + m] = e;
             parent_corr[up + m] = 0.f;
             if (b_extra) {
                 const __nv_bfloat16 prow[16] = {e1, e2, e1, e3, e2, e1, z, z, z, z, z, z, z, z, z, z};

@@ -27,6 +27,8 @@
 //   k_pack_copy   grid (pages / 8, units): one warp per page gathers the K
 //                 and V rows of the page's tokens (all 16-byte loads issued
 //                 before the stores) into the pool and zeroes pad slots.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -287,6 +289,203 @@ __global__ void __launch_bounds__(kThreads) k_pack_rank_seg(int N, int n_cap, in
     }
 }
 
+// Steps a4 for one unit in one thread-block cluster of kPackCluster CTAs
+// (replaces count, scan and rank when the per-warp counters fit in shared
+// memory).  CTA r owns tokens [r*Tc, (r+1)*Tc) and parents
+// [r*Sc, (r+1)*Sc); warp w of a CTA owns a contiguous run of Tw tokens.
+//   A  each warp counts its run per parent (warp-private u16 counters, no
+//      atomics); per parent, an exclusive scan over the warps gives warp
+//      bases and the CTA's count;                          -- cluster barrier
+//   B  per owned parent: c_m = sum of the CTAs' counts (distributed shared
+//      memory reads), pages ceil(c_m / S), exclusive scan of pages over the
+//      slice; the slice's page total goes to every CTA;     -- cluster barrier
+//   C  per owned parent: first page, parent tables, and into every CTA the
+//      position base S * first + (tokens of m in the CTAs before it) and the
+//      end position S * first + c_m;                        -- cluster barrier
+//   D  each warp ranks its run in token order from its bases: position
+//      pos -> page pos / S, slot pos % S; the token at a page's slot 0
+//      writes the page's parent, length and successor, the parent's last
+//      token marks the page's empty slots.
+// Positions are global slot indices, so a parent's rank order is token order
+// (stable counting sort).
+constexpr int kPackCluster = 8;
+constexpr int kPCThreads = 256;
+constexpr int kPCWarps = kPCThreads / 32;
+constexpr size_t kPackClusterSmem = 225 * 1024;  // dynamic shared memory of one cluster CTA, at most
+
+struct PackClusterShape {
+    int tc, tw, sc;  // tokens per CTA, tokens per warp, parents per CTA slice
+    size_t smem;
+};
+PackClusterShape pack_cluster_shape(int N, int np_cap) {
+    PackClusterShape sh;
+    sh.tc = ceil_div(N, kPackCluster);
+    sh.tw = ceil_div(sh.tc, kPCWarps);
+    sh.sc = ceil_div(np_cap, kPackCluster);
+    // s_tok[tc] int32, s_ctr[W][np_cap] u16 (rounded to 4 bytes), s_B, s_E [np_cap], s_F [sc]
+    const size_t ctr = ((size_t)kPCWarps * np_cap * 2 + 3) & ~(size_t)3;
+    sh.smem = 4 * (size_t)sh.tc + ctr + 8 * (size_t)np_cap + 4 * (size_t)sh.sc;
+    return sh;
+}
+
+__global__ void __cluster_dims__(kPackCluster, 1, 1) __launch_bounds__(kPCThreads)
+    k_pack_cluster(int N, int n_cap, int np_cap, int page_cap, int tc, int tw, int sc,
+                   const int32_t *__restrict__ n_parents, const int32_t *__restrict__ token_parent,
+                   int32_t *__restrict__ pack_total, int32_t *__restrict__ n_pages,
+                   int32_t *__restrict__ parent_first_page, int32_t *__restrict__ parent_last_page,
+                   int32_t *__restrict__ parent_n_pages, int32_t *__restrict__ page_parent,
+                   int32_t *__restrict__ page_len, int32_t *__restrict__ page_next,
+                   int32_t *__restrict__ page_tokens, int32_t *__restrict__ token_page,
+                   int32_t *__restrict__ token_slot, int32_t *__restrict__ err) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    extern __shared__ __align__(16) unsigned char s_raw[];
+    __shared__ int s_slice[kPackCluster];
+    __shared__ int s_wsum[kPCWarps];
+    __shared__ int s_carry;
+    const int r = (int)cluster.block_rank();
+    const int u = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int Np = min(n_parents[u], np_cap);
+    int32_t *s_tok = reinterpret_cast<int32_t *>(s_raw);
+    unsigned short *s_ctr = reinterpret_cast<unsigned short *>(s_tok + tc);
+    int32_t *s_B = reinterpret_cast<int32_t *>(s_raw + 4 * (size_t)tc +
+                                               (((size_t)kPCWarps * np_cap * 2 + 3) & ~(size_t)3));
+    int32_t *s_E = s_B + np_cap;
+    int32_t *s_F = s_E + np_cap;
+    const size_t un = (size_t)u * n_cap, up = (size_t)u * np_cap, ug = (size_t)u * page_cap;
+    const long long tok0 = (long long)r * tc;
+
+    // ---- A: load the CTA's token parents, clear the counters, count
+    for (int i = threadIdx.x; i < tc; i += kPCThreads) {
+        const long long j = tok0 + i;
+        const int v = j < N ? token_parent[un + j] : -1;
+        s_tok[i] = (v >= 0 && v < Np) ? v : -1;
+    }
+    for (int x = threadIdx.x; x < kPCWarps * Np; x += kPCThreads) s_ctr[x] = 0;
+    __syncthreads();
+    unsigned short *mine = s_ctr + (size_t)warp * Np;
+    const int w0 = warp * tw;
+    for (int i0 = 0; i0 < tw; i0 += 32) {
+        const int i = w0 + i0 + lane;
+        const int m = (i0 + lane < tw && i < tc) ? s_tok[i] : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, m >= 0 ? m : -1 - lane);
+        if (m >= 0 && lane == __ffs(peers) - 1) mine[m] += (unsigned short)__popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    for (int x = threadIdx.x; x < Np; x += kPCThreads) {
+        int run = 0;
+#pragma unroll
+        for (int w = 0; w < kPCWarps; ++w) {
+            const int c = s_ctr[(size_t)w * Np + x];
+            s_ctr[(size_t)w * Np + x] = (unsigned short)run;
+            run += c;
+        }
+        s_B[x] = run;  // this CTA's tokens of parent x
+    }
+    cluster.sync();
+
+    // ---- B: totals and page scan over this CTA's parent slice
+    const int lo = min(r * sc, Np), hi = min(lo + sc, Np);
+    if (threadIdx.x == 0) s_carry = 0;
+    __syncthreads();
+    for (int x0 = lo; x0 < hi; x0 += kPCThreads) {
+        const int x = x0 + threadIdx.x;
+        int c = 0;
+        if (x < hi) {
+            int v[kPackCluster];
+#pragma unroll
+            for (int q = 0; q < kPackCluster; ++q) v[q] = cluster.map_shared_rank(s_B, q)[x];
+#pragma unroll
+            for (int q = 0; q < kPackCluster; ++q) c += v[q];
+            s_E[x] = c;  // c_m, kept here until C
+        }
+        const int pages = (c + kPage - 1) / kPage;
+        int incl = pages;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        if (lane == 31) s_wsum[warp] = incl;
+        __syncthreads();
+        int woff = 0;
+        for (int w = 0; w < warp; ++w) woff += s_wsum[w];
+        if (x < hi) s_F[x - lo] = s_carry + woff + incl - pages;
+        __syncthreads();
+        if (threadIdx.x == kPCThreads - 1) s_carry += woff + incl;
+        __syncthreads();
+    }
+    if (threadIdx.x < kPackCluster) cluster.map_shared_rank(s_slice, threadIdx.x)[r] = s_carry;
+    cluster.sync();
+
+    // ---- C: first pages, parent tables, position bases in every CTA
+    int base = 0, total = 0;
+#pragma unroll
+    for (int q = 0; q < kPackCluster; ++q) {
+        base += q < r ? s_slice[q] : 0;
+        total += s_slice[q];
+    }
+    for (int x = lo + threadIdx.x; x < hi; x += kPCThreads) {
+        const int c = s_E[x];
+        const int pages = (c + kPage - 1) / kPage;
+        const int first = base + s_F[x - lo];
+        pack_total[up + x] = c;
+        parent_first_page[up + x] = first;
+        parent_n_pages[up + x] = pages;
+        parent_last_page[up + x] = first + pages - 1;
+        int v[kPackCluster];
+#pragma unroll
+        for (int q = 0; q < kPackCluster; ++q) v[q] = cluster.map_shared_rank(s_B, q)[x];
+        int run = first * kPage;
+#pragma unroll
+        for (int q = 0; q < kPackCluster; ++q) {
+            cluster.map_shared_rank(s_B, q)[x] = run;
+            cluster.map_shared_rank(s_E, q)[x] = first * kPage + c;
+            run += v[q];
+        }
+    }
+    if (r == 0 && threadIdx.x == 0) {
+        if (total > page_cap) set_err(err, ICE_ERR_CAPACITY);
+        n_pages[u] = total < page_cap ? total : page_cap;
+    }
+    cluster.sync();  // no distributed shared memory access after this point
+
+    // ---- D: stable ranks of this warp's run
+    for (int i0 = 0; i0 < tw; i0 += 32) {
+        const int i = w0 + i0 + lane;
+        const int m = (i0 + lane < tw && i < tc) ? s_tok[i] : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, m >= 0 ? m : -1 - lane);
+        const int leader = __ffs(peers) - 1;
+        int b = 0;
+        if (m >= 0 && lane == leader) {
+            b = mine[m];
+            mine[m] = (unsigned short)(b + __popc(peers));
+        }
+        b = __shfl_sync(0xffffffffu, b, leader);
+        __syncwarp();
+        if (m >= 0) {
+            const long long j = tok0 + i;
+            const int pos = s_B[m] + b + __popc(peers & lanemask_lt());
+            const int end = s_E[m];
+            const int pg = pos / kPage, slot = pos % kPage;
+            if (pg < page_cap) {
+                page_tokens[(ug + pg) * kPage + slot] = (int32_t)j;
+                token_page[un + j] = pg;
+                token_slot[un + j] = slot;
+                if (slot == 0) {
+                    page_parent[ug + pg] = m;
+                    page_len[ug + pg] = min(kPage, end - pos);
+                    page_next[ug + pg] = (pos + kPage < end && pg + 1 < page_cap) ? pg + 1 : -1;
+                }
+                if (pos == end - 1)
+                    for (int sl = slot + 1; sl < kPage; ++sl) page_tokens[(ug + pg) * kPage + sl] = -1;
+            }
+        }
+    }
+}
+
 size_t rank_seg_smem(int np_cap) { return (size_t)np_cap * (sizeof(int32_t) + kSegWarps * sizeof(unsigned short)); }
 
 template <typename T>
@@ -324,9 +523,35 @@ __global__ void __launch_bounds__(kThreads) k_pack_copy(const T *__restrict__ K,
     }
 }
 
+void launch_rank_tiles(const ice_params &p, const ice_index &idx, const BuildWs &ws, int32_t *err, cudaStream_t s);
+
 template <typename T>
 cudaError_t launch_t(const ice_params &p, const void *K, const void *V, const ice_index &idx, const BuildWs &ws,
                      int32_t *err, cudaStream_t s) {
+    const int U = units_of(p);
+    const PackClusterShape pcs = pack_cluster_shape(p.n_tokens, p.np_cap);
+    if (pcs.smem <= kPackClusterSmem && pcs.tw <= 65535) {
+        if (pcs.smem > 48 * 1024) {
+            cudaError_t e =
+                cudaFuncSetAttribute(k_pack_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pcs.smem);
+            if (e != cudaSuccess) return e;
+        }
+        k_pack_cluster<<<dim3(kPackCluster, U), kPCThreads, pcs.smem, s>>>(
+            p.n_tokens, p.n_cap, p.np_cap, p.page_cap, pcs.tc, pcs.tw, pcs.sc, idx.n_parents, idx.token_parent,
+            ws.pack_total, idx.n_pages, idx.parent_first_page, idx.parent_last_page, idx.parent_n_pages,
+            idx.page_parent, idx.page_len, idx.page_next, idx.page_tokens, idx.token_page, idx.token_slot, err);
+    } else {
+        launch_rank_tiles(p, idx, ws, err, s);
+    }
+    dim3 cgrid(ceil_div(p.page_cap, kThreads / 32), U);
+    k_pack_copy<T><<<cgrid, kThreads, 0, s>>>(static_cast<const T *>(K), static_cast<const T *>(V), p.n_tokens,
+                                              p.page_cap, idx.n_pages, idx.page_len, idx.page_tokens,
+                                              static_cast<T *>(idx.pool_k), static_cast<T *>(idx.pool_v));
+    return cudaGetLastError();
+}
+
+// count, scan and rank as separate kernels over 2048-token tiles
+void launch_rank_tiles(const ice_params &p, const ice_index &idx, const BuildWs &ws, int32_t *err, cudaStream_t s) {
     const int U = units_of(p);
     const int tiles = ceil_div(p.n_tokens, kPackTile);
     const int smem_path = p.np_cap <= kPackSmemBins;
@@ -357,11 +582,6 @@ cudaError_t launch_t(const ice_params &p, const void *K, const void *V, const ic
                                                  idx.parent_first_page, idx.page_tokens, idx.token_page,
                                                  idx.token_slot);
     }
-    dim3 cgrid(ceil_div(p.page_cap, kThreads / 32), U);
-    k_pack_copy<T><<<cgrid, kThreads, 0, s>>>(static_cast<const T *>(K), static_cast<const T *>(V), p.n_tokens,
-                                              p.page_cap, idx.n_pages, idx.page_len, idx.page_tokens,
-                                              static_cast<T *>(idx.pool_k), static_cast<T *>(idx.pool_v));
-    return cudaGetLastError();
 }
 
 }  // namespace

@@ -135,7 +135,19 @@ def check_build_unit(run: GpuRun, u: int, sample_tokens: int | None = None):
         o = lifted_d2(K, e, j, pt[tp_ora[j]])
         assert a - o <= 2 * TIE_REL * M2, (u, j, tp_gpu[j], tp_ora[j], a, o)
     assert len(mism) <= max(2, len(js) // 2000), (u, len(mism))
-    # pages: the oracle packs the GPU's assignment; must match bit-exactly
+    check_pack_unit(run, u)
+
+
+def check_pack_unit(run: GpuRun, u: int):
+    """Pages, page tables and pool of unit u: the oracle packs the GPU's own
+    assignment, and every table must match bit-exactly."""
+    b, h = run.unit(u)
+    cfg, H = run.cfg, run.h
+    K = run.K[b, h].astype(np.float64)
+    V = run.V[b, h].astype(np.float64)
+    N = cfg.n_tokens
+    Np = int(H["n_parents"][u])
+    tp_gpu = H["token_parent"][u, :N]
     pk = oracle.pack(tp_gpu, Np, cfg.page_size)
     P = pk["n_pages"]
     assert int(H["n_pages"][u]) == P

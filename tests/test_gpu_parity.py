@@ -9,7 +9,7 @@ import torch
 import oracle
 import semantic_paged_kv_gb300 as ice
 import workloads
-from parity_util import GpuRun, check_build_unit, check_decode_unit, to_dev
+from parity_util import GpuRun, check_build_unit, check_decode_unit, check_pack_unit, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -97,6 +97,21 @@ def test_promote_all_is_exact_topk_mips():
     got = set(buf.sel_pages[0, : int(buf.sel_count[0])].cpu().tolist())
     toks = set(run.h["page_tokens"][0, sorted(got), 0].tolist())
     assert toks == set(top.reshape(-1).tolist())
+
+
+def test_pack_with_many_parents_uses_tile_kernels():
+    """p = 0.95 on N = 10000: ~9500 parents, too many for the per-unit
+    cluster packer's shared memory, so pages are built by the tile kernels
+    (count, scan, rank); checked bit-exactly against the oracle's packing of
+    the GPU's assignment, then decoded."""
+    w = W["llama31_8b_16k"].scaled(n_tokens=10000, n_q_heads=4, n_kv_heads=1, promote_p=0.95)
+    run = GpuRun(w)
+    assert run.status == ice.ICE_OK
+    assert run.cfg.np_cap * 24 > 225 * 1024
+    check_pack_unit(run, 0)
+    Q, buf, st = run.decode(256)
+    assert st == ice.ICE_OK
+    check_decode_unit(run, 0, Q, 256, buf)
 
 
 def test_promote_none_is_sequential_paging():
