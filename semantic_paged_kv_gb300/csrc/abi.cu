@@ -81,6 +81,13 @@ ice_status check_ws(void *ws, size_t ws_bytes, size_t need) {
 
 int k_pages_of(int budget_tokens) { return (budget_tokens + kPage - 1) / kPage; }
 
+int sm_count() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+}
+
 }  // namespace
 
 BuildWs build_ws_layout(const ice_params &p, void *base) {
@@ -108,7 +115,7 @@ BuildWs build_ws_layout(const ice_params &p, void *base) {
     return w;
 }
 
-DecodeWs decode_ws_layout(const ice_params &p, int budget_tokens, int max_sel, void *base) {
+DecodeWs decode_ws_layout(const ice_params &p, int budget_tokens, int max_sel, void *base, bool with_select) {
     DecodeWs w{};
     const size_t U = (size_t)units_of(p);
     const size_t g = (size_t)(p.n_q_heads / p.n_kv_heads);
@@ -130,6 +137,7 @@ DecodeWs decode_ws_layout(const ice_params &p, int budget_tokens, int max_sel, v
     w.cand_span = reinterpret_cast<int4 *>(take(sizeof(int4) * U * w.n_chunks * kSelChunk));
     w.part_ml = reinterpret_cast<float *>(take(sizeof(float) * U * w.n_splits * g * 2));
     w.part_o = reinterpret_cast<float *>(take(sizeof(float) * U * w.n_splits * g * kHeadDim));
+    w.scores = with_select ? reinterpret_cast<float *>(take(sizeof(float) * U * select_tc_scores(p))) : nullptr;
     w.bytes = off;
     return w;
 }
@@ -401,7 +409,9 @@ ice_status ice_decode_step(const ice_params *p, const ice_index *idx, const void
     if (!kbuf || !vbuf || !buf_len || !O) return fail(ICE_ERR_INVALID_ARG, "decode needs non-NULL kbuf, vbuf, buf_len and O");
     if (!aligned16(kbuf) || !aligned16(vbuf)) return fail(ICE_ERR_INVALID_ARG, "kbuf and vbuf must be 16-byte aligned");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (decode_cluster_supported(*p, w.k_pages, max_sel))
+    // one cluster per unit pays off while all clusters fit in one wave; with
+    // more units the select / attention kernels keep every SM streaming
+    if (units_of(*p) * kDecodeCluster <= sm_count() && decode_cluster_supported(*p, w.k_pages, max_sel))
         return cuda_status(launch_decode_cluster(*p, *idx, Q, w.k_pages, sel_pages, sel_count, max_sel, kbuf, vbuf,
                                                  buf_len, scale, O, err_dev, s),
                            "ice_decode_step");

@@ -40,9 +40,12 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc_common.cuh"
 
 namespace ice {
 namespace {
+
+using namespace tc;
 
 constexpr int BM = 128;      // tokens per CTA (TMEM lanes)
 constexpr int BN = 256;      // parents per MMA tile (TMEM columns per accumulator)
@@ -58,10 +61,8 @@ constexpr uint32_t B_HALF = BN * 128;
 constexpr uint32_t B_STAGE = 2 * B_HALF;
 constexpr uint32_t B2_STAGE = BN * kExtra * 2;
 constexpr uint32_t TMEM_COLS = 2 * BN;
-constexpr unsigned long long kWaitNs = 2000000000ull;
 // kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major, N, M.
-constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                           ((uint32_t)(BM >> 4) << 24);
+constexpr uint32_t IDESC = idesc_bf16(BM, BN);
 
 struct Bars {
     unsigned long long full[NSTAGE], empty[NSTAGE], a_full[2], a_empty[2], tfull[2], tempty[2];
@@ -71,91 +72,6 @@ struct Bars {
 };
 constexpr size_t kSmemBytes = 1024 /*align slack*/ + 2 * A_BYTES + NSTAGE * B_STAGE + 2 * A2_BYTES +
                               NSTAGE * B2_STAGE + sizeof(Bars);
-
-__device__ __forceinline__ uint32_t su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ unsigned long long now_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-__device__ __forceinline__ void mbar_init(unsigned long long *b, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(unsigned long long *b, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(unsigned long long *b) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
-}
-__device__ __forceinline__ bool mbar_test(unsigned long long *b, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(su32(b)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Bounded wait for the phase of the given parity; false after kWaitNs.
-__device__ __forceinline__ bool mbar_wait(unsigned long long *b, uint32_t parity) {
-    if (mbar_test(b, parity)) return true;
-    const unsigned long long t0 = now_ns();
-    while (!mbar_test(b, parity))
-        if (now_ns() - t0 > kWaitNs) return false;
-    return true;
-}
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, unsigned long long *bar, int x, int y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
-            su32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(su32(bar)), "r"(x), "r"(y)
-        : "memory");
-}
-// Shared-memory matrix descriptors, K-major, descriptor version 1:
-// 128-byte swizzle (8-row groups 1024 bytes apart) for the 64-column halves,
-// 32-byte swizzle (8-row groups 256 bytes apart) for the 16-column extras.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-__device__ __forceinline__ uint64_t sw32_desc(uint32_t saddr) {
-    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(256 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)6 << 61);
-}
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(IDESC), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ void umma_commit(unsigned long long *bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
-                 : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// 32 consecutive fp32 TMEM columns of this thread's lane (no wait).
-__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, float *v) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Work item -> (unit, first token) and the unit's parent-tile count.
 struct Item {
@@ -197,17 +113,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->tfull[b], 1);
             mbar_init(&bars->tempty[b], kEpiThreads);
         }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_init_fence();
     }
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&bars->tmem_base)),
-                     "r"(TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    tc_fence_before();
+    if (warp == 1) tmem_alloc(&bars->tmem_base, TMEM_COLS);
+    fence_before();
     __syncthreads();
-    tc_fence_after();
+    fence_after();
     const uint32_t tmem = bars->tmem_base;
     bool ok = true;
 
@@ -270,16 +181,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
+                    fence_after();
                     const uint32_t b0 = su32(sB + s * B_STAGE);
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
                         const uint32_t off = (k & 3) * 32;  // 16 bf16 columns inside the swizzle atom
                         const uint64_t da = sw128_desc(a0 + (k >> 2) * A_HALF + off);
                         const uint64_t db = sw128_desc(b0 + (k >> 2) * B_HALF + off);
-                        umma_bf16(tmem + b * BN, da, db, k > 0 ? 1u : 0u);
+                        umma_bf16<IDESC>(tmem + b * BN, da, db, k > 0 ? 1u : 0u);
                     }
-                    umma_bf16(tmem + b * BN, sw32_desc(a2), sw32_desc(su32(sB2 + s * B2_STAGE)), 1u);
+                    umma_bf16<IDESC>(tmem + b * BN, sw32_desc(a2), sw32_desc(su32(sB2 + s * B2_STAGE)), 1u);
                     umma_commit(&bars->empty[s]);
                     umma_commit(&bars->tfull[b]);
                 }
@@ -313,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // a failed wait stops this warp's work
                 if (ok) ok = mbar_wait(&bars->tfull[b], (gt >> 1) & 1);
                 ok = __all_sync(0xffffffffu, ok);
-                tc_fence_after();
+                fence_after();
                 const int c_lo = t * BN + hf * (BN / 2);
                 const int valid = ok ? max(0, min(BN / 2, I.Np - c_lo)) : 0;
                 for (int c0 = 0; c0 < valid; c0 += 64) {
@@ -343,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         bidx = c_lo + c0 + first;
                     }
                 }
-                tc_fence_before();
+                fence_before();
                 mbar_arrive(&bars->tempty[b]);
             }
             // combine the two column halves of each row
@@ -367,44 +278,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     if (!ok) set_err(err, ICE_ERR_TIMEOUT);
-    tc_fence_before();
+    fence_before();
     __syncthreads();
     if (warp == 1) {
-        tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+        fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
     }
-}
-
-// ------------------------------------------------------------------ host --
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            p = nullptr;
-        return reinterpret_cast<EncodeTiledFn>(p);
-    }();
-    return fn;
-}
-
-// 2-D bf16 map over rows of `cols` elements, box {box_cols, box_rows}.
-bool make_map(CUtensorMap *m, const void *base, unsigned long long rows, unsigned cols, unsigned box_cols,
-              unsigned box_rows, CUtensorMapSwizzle sw) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    const cuuint32_t box[2] = {box_cols, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -415,10 +294,10 @@ cudaError_t launch_assign_tc(const ice_params &p, const void *K, const ice_index
     const int U = units_of(p);
     CUtensorMap tmK, tmP, tmK2, tmP2;
     const unsigned long long kr = (unsigned long long)U * p.n_tokens, pr = (unsigned long long)U * p.np_cap;
-    if (!make_map(&tmK, K, kr, kHeadDim, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&tmP, idx.parent_keys, pr, kHeadDim, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&tmK2, ws.a_extra, kr, kExtra, kExtra, BM, CU_TENSOR_MAP_SWIZZLE_32B) ||
-        !make_map(&tmP2, ws.b_extra, pr, kExtra, kExtra, BN, CU_TENSOR_MAP_SWIZZLE_32B))
+    if (!make_map_bf16(&tmK, K, kr, kHeadDim, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_bf16(&tmP, idx.parent_keys, pr, kHeadDim, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_bf16(&tmK2, ws.a_extra, kr, kExtra, kExtra, BM, CU_TENSOR_MAP_SWIZZLE_32B) ||
+        !make_map_bf16(&tmP2, ws.b_extra, pr, kExtra, kExtra, BN, CU_TENSOR_MAP_SWIZZLE_32B))
         return cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {

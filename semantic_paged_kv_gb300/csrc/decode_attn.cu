@@ -385,7 +385,7 @@ cudaError_t noalloc_scratch(void **out) {
 }  // namespace
 
 size_t attention_noalloc_bytes(const ice_params &p, int max_sel) {
-    return decode_ws_layout(p, 0, max_sel, nullptr).bytes;
+    return decode_ws_layout(p, 0, max_sel, nullptr, false).bytes;
 }
 
 cudaError_t launch_attention_noalloc(const ice_params &p, const void *Q, const void *kbuf, const void *vbuf,
@@ -394,7 +394,7 @@ cudaError_t launch_attention_noalloc(const ice_params &p, const void *Q, const v
     void *base = nullptr;
     cudaError_t e = noalloc_scratch(&base);
     if (e != cudaSuccess) return e;
-    const DecodeWs ws = decode_ws_layout(p, 0, max_sel, base);
+    const DecodeWs ws = decode_ws_layout(p, 0, max_sel, base, false);
     if (ws.bytes > ICE_NOALLOC_SCRATCH_BYTES) return cudaErrorInvalidValue;
     e = cudaMemsetAsync(ws.attn_ticket, 0, sizeof(int32_t) * units_of(p), s);
     if (e != cudaSuccess) return e;

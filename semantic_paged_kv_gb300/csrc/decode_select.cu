@@ -46,11 +46,6 @@ __device__ __forceinline__ unsigned long long sort_key(float s, int id) {
     return ((unsigned long long)b << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)id);
 }
 __device__ __forceinline__ int key_id(unsigned long long k) { return (int)(0xFFFFFFFFu - (uint32_t)k); }
-__device__ __forceinline__ float key_score(unsigned long long k) {
-    uint32_t b = (uint32_t)(k >> 32);
-    b = (b & 0x80000000u) ? (b & 0x7FFFFFFFu) : ~b;
-    return __uint_as_float(b);
-}
 
 // Sorts rows[r][0..n) descending for r < nrows (n a power of two) with every
 // thread of the block; ends with a barrier.
@@ -318,6 +313,10 @@ size_t select_smem_bytes(const ice_params &p, int k_pages, int n_chunks) {
 
 cudaError_t launch_select(const ice_params &p, const ice_index &idx, const void *Q, const DecodeWs &ws,
                           int32_t *sel_pages, int32_t *sel_count, int max_sel, int32_t *err, cudaStream_t s) {
+    if (select_tc_supported(p, ws.k_pages)) {
+        const cudaError_t e = launch_select_tc(p, idx, Q, ws, sel_pages, sel_count, max_sel, err, s);
+        if (e != cudaErrorNotSupported) return e;
+    }
     if (p.dtype == ICE_BF16) return launch_t<__nv_bfloat16>(p, idx, Q, ws, sel_pages, sel_count, max_sel, err, s);
     return launch_t<float>(p, idx, Q, ws, sel_pages, sel_count, max_sel, err, s);
 }

@@ -43,10 +43,12 @@ struct DecodeWs {
     int4 *cand_span;       // [U, n_chunks, 256] (first page, pages, contiguous, m)
     float *part_ml;        // [U, n_splits, g, 2]  running max, running sum
     float *part_o;         // [U, n_splits, g, d]
+    float *scores;         // [U, g, np_cap] parent scores of the tensor-core selection
     int n_chunks, k_pages, n_splits;
     size_t bytes;
 };
-DecodeWs decode_ws_layout(const ice_params &p, int budget_tokens, int max_sel, void *base);
+// with_select = false: the attention part only (no selection scratch).
+DecodeWs decode_ws_layout(const ice_params &p, int budget_tokens, int max_sel, void *base, bool with_select = true);
 
 struct InsertWs {
     int32_t *ticket;  // [U]  zero between calls
@@ -71,6 +73,11 @@ cudaError_t launch_pack(const ice_params &p, const void *K, const void *V, const
                         const BuildWs &ws, int32_t *err, cudaStream_t s);
 cudaError_t launch_select(const ice_params &p, const ice_index &idx, const void *Q, const DecodeWs &ws,
                           int32_t *sel_pages, int32_t *sel_count, int max_sel, int32_t *err, cudaStream_t s);
+// Selection with tensor-core scoring (bf16, g <= 16, k <= 64 pages per head).
+bool select_tc_supported(const ice_params &p, int k_pages);
+size_t select_tc_scores(const ice_params &p);
+cudaError_t launch_select_tc(const ice_params &p, const ice_index &idx, const void *Q, const DecodeWs &ws,
+                             int32_t *sel_pages, int32_t *sel_count, int max_sel, int32_t *err, cudaStream_t s);
 cudaError_t launch_gather(const ice_params &p, const ice_index &idx, const int32_t *sel_pages,
                           const int32_t *sel_count, int max_sel, void *kbuf, void *vbuf, int32_t *buf_len,
                           cudaStream_t s);

@@ -205,11 +205,13 @@ def check_decode_unit(run: GpuRun, u: int, Q: np.ndarray, budget: int, buf):
         assert required <= gs and gs <= allowed, (u, sorted(gs ^ set(union.tolist())))
     assert np.all(np.diff(got) > 0)
     # gather: exact copies of the selected pages
-    pk_, pv_ = run.pool(u)
+    gi = torch.as_tensor(got, dtype=torch.long, device=buf.kbuf.device)
+    pk_sel = run.idx.pool_k[u].index_select(0, gi).float().cpu().numpy()
+    pv_sel = run.idx.pool_v[u].index_select(0, gi).float().cpu().numpy()
     kb = buf.kbuf[u, :cnt].float().cpu().numpy()
     vb = buf.vbuf[u, :cnt].float().cpu().numpy()
     bl = buf.buf_len[u].cpu().numpy()
-    assert np.array_equal(kb, pk_[got]) and np.array_equal(vb, pv_[got])
+    assert np.array_equal(kb, pk_sel) and np.array_equal(vb, pv_sel)
     assert np.array_equal(bl[:cnt], H["page_len"][u, got]) and np.all(bl[cnt:] == 0)
     # attention over the GPU's selection
     out = oracle.attention(q, kb, vb, bl[:cnt], 1.0 / np.sqrt(cfg.head_dim))

@@ -26,6 +26,14 @@ def _all_units(run, budgets, fused=True, sample=None):
             check_decode_unit(run, u, Q, bgt, buf)
 
 
+def _all_units_decode(run, budgets, fused=True):
+    for bgt in budgets:
+        Q, buf, st = run.decode(bgt, fused=fused)
+        assert st == ice.ICE_OK
+        for u in range(run.cfg.units):
+            check_decode_unit(run, u, Q, bgt, buf)
+
+
 def test_tiny_fp32_full():
     """The tiny fp32 workload (1 KV head, 4 query heads, N = 2048) end to end."""
     run = GpuRun(W["tiny"])
@@ -82,6 +90,37 @@ def test_qwen_shaped_g8_mha_longchat_shaped_g1():
         run = GpuRun(w)
         assert run.status == ice.ICE_OK
         _all_units(run, [64, 256])
+
+
+def test_many_units_take_select_and_attention_kernels():
+    """More units than one wave of per-unit clusters: ice_decode_step runs the
+    tensor-core selection and the split attention (Qwen3-shaped g = 8 and
+    LongChat-shaped g = 1 groups), every unit checked."""
+    for w in (W["qwen3_32b_100k"].scaled(n_tokens=3000, batch=3, centres=256),
+              W["longchat_7b_100k"].scaled(n_tokens=2500, batch=1, n_q_heads=24, n_kv_heads=24, centres=256)):
+        run = GpuRun(w)
+        assert run.status == ice.ICE_OK
+        assert run.cfg.units * 8 > torch.cuda.get_device_properties(0).multi_processor_count
+        for u in (0, run.cfg.units - 1):
+            check_build_unit(run, u)
+        _all_units_decode(run, [64, 256], fused=True)
+        _all_units_decode(run, [128], fused=False)
+
+
+def test_longchat_100k_full_size_sampled():
+    """The LongChat-7B-shaped layer at its full size (32 KV heads, N = 100000,
+    log-normal norms) in the launch configuration the benchmark times: the
+    selection runs as several segments per unit.  Build checked on two units
+    (assignment on 800 sampled tokens), decode on four."""
+    run = GpuRun(W["longchat_7b_100k"])
+    assert run.status == ice.ICE_OK
+    for u in (3, 30):
+        check_build_unit(run, u, sample_tokens=800)
+    for bgt in (64, 256):
+        Q, buf, st = run.decode(bgt)
+        assert st == ice.ICE_OK
+        for u in (0, 3, 17, 30):
+            check_decode_unit(run, u, Q, bgt, buf)
 
 
 def test_promote_all_is_exact_topk_mips():
