@@ -417,8 +417,9 @@ ice_status ice_decode_step(const ice_params *p, const ice_index *idx, const void
                            "ice_decode_step");
     if ((st = cuda_status(launch_select(*p, *idx, Q, w, sel_pages, sel_count, max_sel, err_dev, s), "ice_decode_step select")))
         return st;
-    return cuda_status(launch_attention(*p, idx, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, w, s),
-                       "ice_decode_step attention");
+    return cuda_status(
+        launch_attention(*p, idx, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, w, s, err_dev),
+        "ice_decode_step attention");
 }
 
 }  // extern "C"

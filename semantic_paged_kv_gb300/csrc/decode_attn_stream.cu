@@ -1,0 +1,340 @@
+// Decode steps a9 (bulk gather of the selected pages) and a10 (masked sparse
+// attention over them) for bf16 pools with at most 8 query heads per KV head.
+//
+// papernotes.org "IceCache: Memory-Efficient KV-cache Management for
+// Long-Sequence LLMs", 关键设计 4: the selected pages are not contiguous, so
+// they are collected into one contiguous buffer and moved in one transfer;
+// 关键设计 1: a_ij = s_ij exp(q_i.k_j/sqrt(d)) / sum_j' s_ij' exp(q_i.k_j'/sqrt(d)).
+// IceCache popular-science article (aitangshan.cn/news/751385), section 四:
+// bulk loading gathers everything needed into one staging area first.
+//
+// k_attn_stream<F, GT>: grid (splits of 8 selected pages, units), 8 warps.
+// Thread 0 starts one 1-D bulk copy per page for K and for V (4 KB each) into
+// shared memory; warp w owns page w of the split:
+//   * with F (fused gather) it writes the page back to kbuf / vbuf with 1-D
+//     bulk stores straight from shared memory, and the page's length to
+//     buf_len; without F the pages come from kbuf / vbuf;
+//   * logits: 16 lanes per key, 8 dimensions per lane, the lane's q slices of
+//     the group's GT heads in registers; the 16 partial sums of each head are
+//     folded by recursive halving (each step a lane keeps half of its heads);
+//   * softmax over the page's 16 slots per head (masked past the page length);
+//   * P V: lane owns output dimensions 4 lane .. 4 lane + 3 of every head.
+// The 8 warps' (max, sum, o) merge in shared memory into one partial per
+// split (log-sum-exp rule); the unit's last CTA (atomic ticket, nobody waits)
+// merges the splits and writes O.
+#include "common.cuh"
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace ice {
+namespace {
+
+using namespace tc;
+
+constexpr int SP = 8;  // pages per CTA, one per warp
+constexpr int kThreads = 32 * SP;
+constexpr int kPageElems = kPage * kHeadDim;        // 2048
+constexpr uint32_t kPageBytes = kPageElems * 2;     // bf16: 4 KB
+
+struct Smem {
+    __nv_bfloat16 kv[SP][2][kPageElems];  // 64 KB; reused by the merges
+    float p[SP][kPage][8];                 // per warp: logits, then probabilities [slot][head]
+    float ml[SP][8][2];                    // per warp and head: max, sum
+    float wgt[SP][8];                      // merge weights
+    unsigned long long full[SP];
+    int last;
+};
+
+__device__ __forceinline__ void unpack8(const uint4 &v, float *f) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+template <bool kFused, int GT>
+__global__ void __launch_bounds__(kThreads, 2) k_attn_stream(
+    const __nv_bfloat16 *__restrict__ Q, int g, int n_q_heads, int n_kv_heads,
+    const __nv_bfloat16 *__restrict__ pool_k, const __nv_bfloat16 *__restrict__ pool_v,
+    const int32_t *__restrict__ page_len, int page_cap, const int32_t *__restrict__ sel_pages,
+    __nv_bfloat16 *__restrict__ kbuf, __nv_bfloat16 *__restrict__ vbuf, int32_t *__restrict__ buf_len,
+    const int32_t *__restrict__ sel_count, int max_sel, float scale, int n_splits, float *__restrict__ part_ml,
+    float *__restrict__ part_o, int32_t *__restrict__ ticket, float *__restrict__ O, int32_t *__restrict__ err) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    Smem &S = *reinterpret_cast<Smem *>(smem_raw);
+    const int u = blockIdx.y, split = blockIdx.x;
+    const int b = u / n_kv_heads, h = u % n_kv_heads;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n = min(sel_count[u], max_sel);
+    const int x0 = split * SP;
+    const int np = max(0, min(SP, n - x0));
+    const size_t sbase = (size_t)u * max_sel + x0;  // slot of this split's first page
+
+    if (tid == 0) {
+        for (int i = 0; i < SP; ++i) mbar_init(&S.full[i], 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    if (tid == 0) {
+        for (int i = 0; i < np; ++i) {
+            const __nv_bfloat16 *sk, *sv;
+            if (kFused) {
+                const size_t pg = (size_t)u * page_cap + sel_pages[sbase + i];
+                sk = pool_k + pg * kPageElems;
+                sv = pool_v + pg * kPageElems;
+            } else {
+                sk = kbuf + (sbase + i) * kPageElems;
+                sv = vbuf + (sbase + i) * kPageElems;
+            }
+            mbar_expect_tx(&S.full[i], 2 * kPageBytes);
+            bulk_load(S.kv[i][0], sk, kPageBytes, &S.full[i]);
+            bulk_load(S.kv[i][1], sv, kPageBytes, &S.full[i]);
+        }
+    }
+    if (kFused)  // slots of this split past the selection hold no page
+        for (int x = max(x0, n) + tid; x < min(x0 + SP, max_sel); x += kThreads) buf_len[(size_t)u * max_sel + x] = 0;
+
+    // q slices: head hh, dimensions 8 c .. 8 c + 7 with c = lane % 16
+    const int c = lane & 15, half = lane >> 4;
+    float q[GT][8];
+    {
+        const __nv_bfloat16 *Qu = Q + ((size_t)b * n_q_heads + (size_t)h * g) * kHeadDim;
+#pragma unroll
+        for (int hh = 0; hh < GT; ++hh) {
+            if (hh < g) {
+                unpack8(*reinterpret_cast<const uint4 *>(Qu + (size_t)hh * kHeadDim + 8 * c), q[hh]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) q[hh][i] = 0.f;
+            }
+        }
+    }
+    float o[GT][4];
+#pragma unroll
+    for (int hh = 0; hh < GT; ++hh)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[hh][i] = 0.f;
+    bool ok = true;
+    bool stored = false;
+    if (warp < np) {
+        const int w = warp;
+        const size_t slot = sbase + w;
+        int len;
+        if (kFused) {
+            len = page_len[(size_t)u * page_cap + sel_pages[slot]];
+            if (lane == 0) buf_len[slot] = len;
+        } else {
+            len = buf_len[slot];
+        }
+        ok = mbar_wait(&S.full[w], 0);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok && kFused && lane == 0) {  // the contiguous buffer, straight from shared memory
+            fence_proxy_async();
+            bulk_store(kbuf + slot * kPageElems, S.kv[w][0], kPageBytes);
+            bulk_store(vbuf + slot * kPageElems, S.kv[w][1], kPageBytes);
+            bulk_commit();
+            stored = true;
+        }
+        if (ok) {
+            const __nv_bfloat16 *Kp = S.kv[w][0];
+            const __nv_bfloat16 *Vp = S.kv[w][1];
+            // ---- logits: keys 2 kp + half, 16 lanes each
+#pragma unroll 2
+            for (int kp = 0; kp < kPage / 2; ++kp) {
+                const int j = 2 * kp + half;
+                float x[8];
+                unpack8(*reinterpret_cast<const uint4 *>(Kp + j * kHeadDim + 8 * c), x);
+                float a[GT];
+#pragma unroll
+                for (int hh = 0; hh < GT; ++hh) {
+                    float s = q[hh][0] * x[0];
+#pragma unroll
+                    for (int i = 1; i < 8; ++i) s = fmaf(q[hh][i], x[i], s);
+                    a[hh] = s;
+                }
+                // fold the 16 lanes of this key: halving over heads, then the rest
+                int head = 0, off = 8;
+#pragma unroll
+                for (int nn = GT; nn > 1; nn >>= 1, off >>= 1) {
+                    const bool up = (lane & off) != 0;
+#pragma unroll
+                    for (int i = 0; i < nn / 2; ++i) {
+                        const float send = up ? a[i] : a[i + nn / 2];
+                        const float keep = up ? a[i + nn / 2] : a[i];
+                        a[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                    }
+                    head += up ? nn / 2 : 0;
+                }
+                float v = a[0];
+                for (; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                if ((lane & (16 / GT - 1)) == 0 && head < g) S.p[w][j][head] = v;
+            }
+            __syncwarp();
+            // ---- softmax over the page's slots, 16 lanes per head
+#pragma unroll
+            for (int e = 0; e < (GT * kPage + 31) / 32; ++e) {
+                const int item = e * 32 + lane;
+                const int hh = item / kPage, sl = item % kPage;
+                const bool on = hh < g && item < GT * kPage;
+                const float lg = (on && sl < len) ? S.p[w][sl][hh] * scale : -INFINITY;
+                float mx = lg;
+#pragma unroll
+                for (int of = 8; of >= 1; of >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, of));
+                const float pr = lg == -INFINITY ? 0.f : expf(lg - mx);
+                float sm = pr;
+#pragma unroll
+                for (int of = 8; of >= 1; of >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, of);
+                if (on) S.p[w][sl][hh] = pr;
+                if (on && sl == 0) {
+                    S.ml[w][hh][0] = mx;
+                    S.ml[w][hh][1] = sm;
+                }
+            }
+            __syncwarp();
+            // ---- o[hh][d] = sum_s p[s][hh] v[s][d], d = 4 lane .. 4 lane + 3
+#pragma unroll 4
+            for (int sl = 0; sl < kPage; ++sl) {
+                const uint2 raw = *reinterpret_cast<const uint2 *>(Vp + sl * kHeadDim + 4 * lane);
+                const float v0 = __uint_as_float(raw.x << 16), v1 = __uint_as_float(raw.x & 0xFFFF0000u);
+                const float v2 = __uint_as_float(raw.y << 16), v3 = __uint_as_float(raw.y & 0xFFFF0000u);
+                const float *pp = S.p[w][sl];
+#pragma unroll
+                for (int hh = 0; hh < GT; ++hh) {
+                    const float pv = pp[hh];
+                    o[hh][0] = fmaf(pv, v0, o[hh][0]);
+                    o[hh][1] = fmaf(pv, v1, o[hh][1]);
+                    o[hh][2] = fmaf(pv, v2, o[hh][2]);
+                    o[hh][3] = fmaf(pv, v3, o[hh][3]);
+                }
+            }
+        }
+    }
+    if (!ok) set_err(err, ICE_ERR_TIMEOUT);
+    // warps without a page contribute nothing
+    if (warp >= np || !ok) {
+        if (lane < 8) {
+            S.ml[warp][lane][0] = -INFINITY;
+            S.ml[warp][lane][1] = 0.f;
+        }
+    }
+    if (stored) bulk_wait_read_all();  // the page buffers are reused below
+    __syncthreads();
+
+    // ---- merge the 8 warps into this split's partial (kv area reused)
+    float *s_o = reinterpret_cast<float *>(&S.kv[0][0][0]);  // [SP][GT][128]
+#pragma unroll
+    for (int hh = 0; hh < GT; ++hh)
+        *reinterpret_cast<float4 *>(s_o + ((size_t)warp * GT + hh) * kHeadDim + 4 * lane) =
+            make_float4(o[hh][0], o[hh][1], o[hh][2], o[hh][3]);
+    if (tid < GT) {
+        float M = -INFINITY;
+        for (int w = 0; w < SP; ++w) M = fmaxf(M, S.ml[w][tid][0]);
+        float L = 0.f;
+        for (int w = 0; w < SP; ++w) {
+            const float m = S.ml[w][tid][0];
+            const float wt = m == -INFINITY ? 0.f : expf(m - M);
+            S.wgt[w][tid] = wt;
+            L = fmaf(S.ml[w][tid][1], wt, L);
+        }
+        if (tid < g) {
+            const size_t pb = ((size_t)u * n_splits + split) * g + tid;
+            part_ml[pb * 2 + 0] = M;
+            part_ml[pb * 2 + 1] = L;
+        }
+    }
+    __syncthreads();
+    for (int x = tid; x < g * kHeadDim; x += kThreads) {
+        const int hh = x / kHeadDim, d = x % kHeadDim;
+        float acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < SP; ++w) acc = fmaf(s_o[((size_t)w * GT + hh) * kHeadDim + d], S.wgt[w][hh], acc);
+        part_o[(((size_t)u * n_splits + split) * g + hh) * kHeadDim + d] = acc;
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) S.last = (atomicAdd(ticket + u, 1) == n_splits - 1);
+    __syncthreads();
+    if (!S.last) return;
+    __threadfence();
+
+    // ---- the unit's last CTA merges the splits (log-sum-exp) and writes O
+    float *s_w = s_o;  // [n_splits][g] weights, then [g] totals
+    const int nsg = n_splits * g;
+    const float *ml = part_ml + (size_t)u * nsg * 2;
+    if (tid < g) {
+        float M = -INFINITY;
+        for (int sp = 0; sp < n_splits; ++sp) M = fmaxf(M, __ldcg(ml + 2 * (sp * g + tid)));
+        float L = 0.f;
+        for (int sp = 0; sp < n_splits; ++sp) {
+            const float m = __ldcg(ml + 2 * (sp * g + tid));
+            const float wt = m == -INFINITY ? 0.f : expf(m - M);
+            s_w[sp * g + tid] = wt;
+            L = fmaf(__ldcg(ml + 2 * (sp * g + tid) + 1), wt, L);
+        }
+        s_w[nsg + tid] = L;
+    }
+    __syncthreads();
+    const float *po = part_o + (size_t)u * nsg * kHeadDim;
+    for (int x = tid; x < g * kHeadDim; x += kThreads) {
+        const int hh = x / kHeadDim, d = x % kHeadDim;
+        float acc = 0.f;
+        for (int sp = 0; sp < n_splits; ++sp)
+            acc = fmaf(__ldcg(po + ((size_t)sp * g + hh) * kHeadDim + d), s_w[sp * g + hh], acc);
+        const float L = s_w[nsg + hh];
+        O[((size_t)b * n_q_heads + (size_t)h * g + hh) * kHeadDim + d] = L > 0.f ? acc / L : 0.f;
+    }
+    if (tid == 0) ticket[u] = 0;
+}
+
+template <bool F, int GT>
+cudaError_t launch_gt(const ice_params &p, const ice_index *pool, const int32_t *sel_pages, const void *Q,
+                      void *kbuf, void *vbuf, int32_t *buf_len, const int32_t *sel_count, int max_sel, float scale,
+                      float *O, const DecodeWs &ws, int32_t *err, cudaStream_t s) {
+    const int U = units_of(p);
+    const int g = p.n_q_heads / p.n_kv_heads;
+    const int n_splits = ceil_div(max_sel, SP);
+    const size_t need = sizeof(Smem) > sizeof(float) * (size_t)(n_splits * g + g) ? sizeof(Smem)
+                                                                                   : sizeof(float) * (n_splits * g + g);
+    if (need > 200 * 1024) return cudaErrorNotSupported;
+    cudaError_t e = cudaFuncSetAttribute(k_attn_stream<F, GT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)need);
+    if (e != cudaSuccess) return e;
+    const __nv_bfloat16 *pk = pool ? static_cast<const __nv_bfloat16 *>(pool->pool_k) : nullptr;
+    const __nv_bfloat16 *pv = pool ? static_cast<const __nv_bfloat16 *>(pool->pool_v) : nullptr;
+    const int32_t *pl = pool ? pool->page_len : nullptr;
+    k_attn_stream<F, GT><<<dim3(n_splits, U), kThreads, need, s>>>(
+        static_cast<const __nv_bfloat16 *>(Q), g, p.n_q_heads, p.n_kv_heads, pk, pv, pl, p.page_cap, sel_pages,
+        static_cast<__nv_bfloat16 *>(kbuf), static_cast<__nv_bfloat16 *>(vbuf), buf_len, sel_count, max_sel, scale,
+        n_splits, ws.part_ml, ws.part_o, ws.attn_ticket, O, err);
+    return cudaGetLastError();
+}
+
+template <bool F>
+cudaError_t launch_f(const ice_params &p, const ice_index *pool, const int32_t *sel_pages, const void *Q, void *kbuf,
+                     void *vbuf, int32_t *buf_len, const int32_t *sel_count, int max_sel, float scale, float *O,
+                     const DecodeWs &ws, int32_t *err, cudaStream_t s) {
+    const int g = p.n_q_heads / p.n_kv_heads;
+    if (g <= 1) return launch_gt<F, 1>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s);
+    if (g <= 2) return launch_gt<F, 2>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s);
+    if (g <= 4) return launch_gt<F, 4>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s);
+    return launch_gt<F, 8>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s);
+}
+
+}  // namespace
+
+bool attention_stream_supported(const ice_params &p) {
+    const int g = p.n_q_heads / p.n_kv_heads;
+    return p.dtype == ICE_BF16 && g >= 1 && g <= 8;
+}
+
+cudaError_t launch_attention_stream(const ice_params &p, const ice_index *pool, const int32_t *sel_pages,
+                                    const void *Q, void *kbuf, void *vbuf, int32_t *buf_len,
+                                    const int32_t *sel_count, int max_sel, float scale, float *O, const DecodeWs &ws,
+                                    int32_t *err, cudaStream_t s) {
+    if (pool)
+        return launch_f<true>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s);
+    return launch_f<false>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s);
+}
+
+}  // namespace ice

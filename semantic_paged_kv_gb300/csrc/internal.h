@@ -86,7 +86,14 @@ cudaError_t launch_gather(const ice_params &p, const ice_index &idx, const int32
 // kbuf/vbuf/buf_len (step a9) and attends over that copy (fused a9 + a10).
 cudaError_t launch_attention(const ice_params &p, const ice_index *pool, const int32_t *sel_pages,
                              const void *Q, void *kbuf, void *vbuf, int32_t *buf_len, const int32_t *sel_count,
-                             int max_sel, float scale, float *O, const DecodeWs &ws, cudaStream_t s);
+                             int max_sel, float scale, float *O, const DecodeWs &ws, cudaStream_t s,
+                             int32_t *err = nullptr);
+// The same with bulk-copied pages, one page per warp (bf16, g <= 8).
+bool attention_stream_supported(const ice_params &p);
+cudaError_t launch_attention_stream(const ice_params &p, const ice_index *pool, const int32_t *sel_pages,
+                                    const void *Q, void *kbuf, void *vbuf, int32_t *buf_len,
+                                    const int32_t *sel_count, int max_sel, float scale, float *O, const DecodeWs &ws,
+                                    int32_t *err, cudaStream_t s);
 
 // The whole decode step of a unit in one thread-block cluster (DSMEM
 // exchanges, hardware cluster barriers); supported when the unit's parent
