@@ -38,24 +38,37 @@ constexpr uint32_t kPageBytes = kPageElems * 2;     // bf16: 4 KB
 
 struct Smem {
     __nv_bfloat16 kv[SP][2][kPageElems];  // 64 KB; reused by the merges
-    float p[SP][kPage][8];                 // per warp: logits, then probabilities [slot][head]
+    float p[SP][kPage][8];                 // per warp: logits [slot][head]
+    unsigned long long pp[SP][kPage][8];   // per warp: probabilities, each duplicated into an fp32 pair
     float ml[SP][8][2];                    // per warp and head: max, sum
     float wgt[SP][8];                      // merge weights
     unsigned long long full[SP];
     int last;
 };
 
-__device__ __forceinline__ void unpack8(const uint4 &v, float *f) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
+// Packed fp32 pairs (fma.rn.f32x2: two IEEE fp32 FMAs per instruction).
+__device__ __forceinline__ unsigned long long pk2(float x, float y) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+    return r;
+}
+__device__ __forceinline__ float2 upk2(unsigned long long r) {
+    float2 f;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(r));
+    return f;
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+// bf16 pair in one 32-bit word -> fp32 pair
+__device__ __forceinline__ unsigned long long bf2_pair(uint32_t w) {
+    return pk2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
 template <bool kFused, int GT>
-__global__ void __launch_bounds__(kThreads, 2) k_attn_stream(
+__global__ void __launch_bounds__(kThreads, GT >= 8 ? 2 : 3) k_attn_stream(
     const __nv_bfloat16 *__restrict__ Q, int g, int n_q_heads, int n_kv_heads,
     const __nv_bfloat16 *__restrict__ pool_k, const __nv_bfloat16 *__restrict__ pool_v,
     const int32_t *__restrict__ page_len, int page_cap, const int32_t *__restrict__ sel_pages,
@@ -98,24 +111,22 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_stream(
 
     // q slices: head hh, dimensions 8 c .. 8 c + 7 with c = lane % 16
     const int c = lane & 15, half = lane >> 4;
-    float q[GT][8];
+    unsigned long long q[GT][4];  // fp32 pairs of dims 8c + 2i, 8c + 2i + 1
     {
         const __nv_bfloat16 *Qu = Q + ((size_t)b * n_q_heads + (size_t)h * g) * kHeadDim;
 #pragma unroll
         for (int hh = 0; hh < GT; ++hh) {
-            if (hh < g) {
-                unpack8(*reinterpret_cast<const uint4 *>(Qu + (size_t)hh * kHeadDim + 8 * c), q[hh]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) q[hh][i] = 0.f;
-            }
+            uint4 raw = make_uint4(0, 0, 0, 0);
+            if (hh < g) raw = *reinterpret_cast<const uint4 *>(Qu + (size_t)hh * kHeadDim + 8 * c);
+            q[hh][0] = bf2_pair(raw.x);
+            q[hh][1] = bf2_pair(raw.y);
+            q[hh][2] = bf2_pair(raw.z);
+            q[hh][3] = bf2_pair(raw.w);
         }
     }
-    float o[GT][4];
+    unsigned long long o[GT][2];  // fp32 pairs of dims 4 lane + {0, 1}, {2, 3}
 #pragma unroll
-    for (int hh = 0; hh < GT; ++hh)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) o[hh][i] = 0.f;
+    for (int hh = 0; hh < GT; ++hh) o[hh][0] = o[hh][1] = 0ull;
     bool ok = true;
     bool stored = false;
     if (warp < np) {
@@ -144,15 +155,18 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_stream(
 #pragma unroll 2
             for (int kp = 0; kp < kPage / 2; ++kp) {
                 const int j = 2 * kp + half;
-                float x[8];
-                unpack8(*reinterpret_cast<const uint4 *>(Kp + j * kHeadDim + 8 * c), x);
+                const uint4 raw = *reinterpret_cast<const uint4 *>(Kp + j * kHeadDim + 8 * c);
+                const unsigned long long x0 = bf2_pair(raw.x), x1 = bf2_pair(raw.y), x2 = bf2_pair(raw.z),
+                                         x3 = bf2_pair(raw.w);
                 float a[GT];
 #pragma unroll
                 for (int hh = 0; hh < GT; ++hh) {
-                    float s = q[hh][0] * x[0];
-#pragma unroll
-                    for (int i = 1; i < 8; ++i) s = fmaf(q[hh][i], x[i], s);
-                    a[hh] = s;
+                    unsigned long long sp = fma2(q[hh][0], x0, 0ull);
+                    sp = fma2(q[hh][1], x1, sp);
+                    sp = fma2(q[hh][2], x2, sp);
+                    sp = fma2(q[hh][3], x3, sp);
+                    const float2 f = upk2(sp);
+                    a[hh] = f.x + f.y;
                 }
                 // fold the 16 lanes of this key: halving over heads, then the rest
                 int head = 0, off = 8;
@@ -186,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_stream(
                 float sm = pr;
 #pragma unroll
                 for (int of = 8; of >= 1; of >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, of);
-                if (on) S.p[w][sl][hh] = pr;
+                if (on) S.pp[w][sl][hh] = pk2(pr, pr);
                 if (on && sl == 0) {
                     S.ml[w][hh][0] = mx;
                     S.ml[w][hh][1] = sm;
@@ -197,16 +211,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_stream(
 #pragma unroll 4
             for (int sl = 0; sl < kPage; ++sl) {
                 const uint2 raw = *reinterpret_cast<const uint2 *>(Vp + sl * kHeadDim + 4 * lane);
-                const float v0 = __uint_as_float(raw.x << 16), v1 = __uint_as_float(raw.x & 0xFFFF0000u);
-                const float v2 = __uint_as_float(raw.y << 16), v3 = __uint_as_float(raw.y & 0xFFFF0000u);
-                const float *pp = S.p[w][sl];
+                const unsigned long long v01 = bf2_pair(raw.x), v23 = bf2_pair(raw.y);
+                const unsigned long long *pp = S.pp[w][sl];
 #pragma unroll
                 for (int hh = 0; hh < GT; ++hh) {
-                    const float pv = pp[hh];
-                    o[hh][0] = fmaf(pv, v0, o[hh][0]);
-                    o[hh][1] = fmaf(pv, v1, o[hh][1]);
-                    o[hh][2] = fmaf(pv, v2, o[hh][2]);
-                    o[hh][3] = fmaf(pv, v3, o[hh][3]);
+                    const unsigned long long pv = pp[hh];
+                    o[hh][0] = fma2(pv, v01, o[hh][0]);
+                    o[hh][1] = fma2(pv, v23, o[hh][1]);
                 }
             }
         }
@@ -225,9 +236,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_stream(
     // ---- merge the 8 warps into this split's partial (kv area reused)
     float *s_o = reinterpret_cast<float *>(&S.kv[0][0][0]);  // [SP][GT][128]
 #pragma unroll
-    for (int hh = 0; hh < GT; ++hh)
+    for (int hh = 0; hh < GT; ++hh) {
+        const float2 a = upk2(o[hh][0]), bq = upk2(o[hh][1]);
         *reinterpret_cast<float4 *>(s_o + ((size_t)warp * GT + hh) * kHeadDim + 4 * lane) =
-            make_float4(o[hh][0], o[hh][1], o[hh][2], o[hh][3]);
+            make_float4(a.x, a.y, bq.x, bq.y);
+    }
     if (tid < GT) {
         float M = -INFINITY;
         for (int w = 0; w < SP; ++w) M = fmaxf(M, S.ml[w][tid][0]);
