@@ -14,7 +14,7 @@
 // 2^-23 relative; all bf16 products are exact in fp32 and the sum is
 // accumulated in fp32.
 //
-// Persistent kernel, one CTA per SM (10 warps), looping over work items =
+// Persistent kernel, one CTA per SM (18 warps), looping over work items =
 // (unit, 128-token tile) in unit-major order, so that the CTAs working at
 // the same time share one unit's parent table in L2:
 //   warp 0      TMA producer: per item the 128x128 key tile (128-byte
@@ -28,11 +28,12 @@
 //               to the ring's empty barrier, the accumulator's full barrier
 //               and, after an item's last tile, the key buffer's empty
 //               barrier;
-//   warps 2..9  epilogue: warp w reads TMEM lane quarter w % 4 and column
-//               half (w - 2) / 4, 64 columns per tcgen05 wait, and keeps a
-//               running argmax with the lowest index on exact ties; the two
-//               halves of a row combine through shared memory at the end of
-//               the item.  The next item's promoted flags are prefetched.
+//   warps 2..17 epilogue: warp w reads TMEM lane quarter w % 4 and the 64
+//               columns (w - 2) / 4 of each tile in one tcgen05 wait, frees
+//               the accumulator at once and then keeps a running argmax with
+//               the lowest index on exact ties; the four column quarters of a
+//               row combine through shared memory at the end of the item.
+//               The next item's promoted flags are prefetched.
 // Every mbarrier wait gives up after ~2 s (globaltimer) and records
 // ICE_ERR_TIMEOUT; roles drain what they issued and TMEM is freed before
 // the CTA returns.
@@ -50,7 +51,8 @@ using namespace tc;
 constexpr int BM = 128;      // tokens per CTA (TMEM lanes)
 constexpr int BN = 256;      // parents per MMA tile (TMEM columns per accumulator)
 constexpr int NSTAGE = 2;    // parent-tile ring depth
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;  // 4 per TMEM lane quarter, 64 columns of each tile apiece
+constexpr int kEpiCols = BN / (kEpiWarps / 4);
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kExtra = 16;                  // extra K columns (bf16)
@@ -66,8 +68,8 @@ constexpr uint32_t IDESC = idesc_bf16(BM, BN);
 
 struct Bars {
     unsigned long long full[NSTAGE], empty[NSTAGE], a_full[2], a_empty[2], tfull[2], tempty[2];
-    float comb_s[BM];
-    int comb_i[BM];
+    float comb_s[kEpiWarps / 4 - 1][BM];  // column quarters 1..3 of each row
+    int comb_i[kEpiWarps / 4 - 1][BM];
     uint32_t tmem_base;
 };
 constexpr size_t kSmemBytes = 1024 /*align slack*/ + 2 * A_BYTES + NSTAGE * B_STAGE + 2 * A2_BYTES +
@@ -202,9 +204,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // -------------------------------------------------------- epilogue
-        const int ew = warp - 2;  // 0..7
+        const int ew = warp - 2;  // 0..15
         const int q = warp & 3;   // TMEM lane quarter this warp may access
-        const int hf = ew >> 2;   // column half of each 256-column tile
+        const int hf = ew >> 2;   // column quarter of each 256-column tile
         const int row = q * 32 + lane;
         int gt = 0;
         Item I = blockIdx.x < n_items ? item_of(blockIdx.x, mt_per_unit, n_parents, np_cap) : Item{0, 0, 0, 0};
@@ -225,50 +227,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok) ok = mbar_wait(&bars->tfull[b], (gt >> 1) & 1);
                 ok = __all_sync(0xffffffffu, ok);
                 fence_after();
-                const int c_lo = t * BN + hf * (BN / 2);
-                const int valid = ok ? max(0, min(BN / 2, I.Np - c_lo)) : 0;
-                for (int c0 = 0; c0 < valid; c0 += 64) {
-                    float v[64];
-                    const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + hf * (BN / 2) + c0);
-                    tmem_ld32_nowait(ta, v);
-                    tmem_ld32_nowait(ta + 32, v + 32);
-                    tmem_wait_ld();
-                    float cmax = -INFINITY;
-                    if (valid - c0 >= 64) {
+                const int c_lo = t * BN + hf * kEpiCols;
+                const int valid = ok ? max(0, min(kEpiCols, I.Np - c_lo)) : 0;
+                float v[kEpiCols];
+                if (valid > 0) {
+                    const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + hf * kEpiCols);
 #pragma unroll
-                        for (int i = 0; i < 64; i += 4)
+                    for (int c = 0; c < kEpiCols; c += 32) tmem_ld32_nowait(ta + c, v + c);
+                    tmem_wait_ld();
+                }
+                // the accumulator is free as soon as its values are in registers
+                fence_before();
+                mbar_arrive(&bars->tempty[b]);
+                if (valid > 0) {
+                    float cmax = -INFINITY;
+                    if (valid >= kEpiCols) {
+#pragma unroll
+                        for (int i = 0; i < kEpiCols; i += 4)
                             cmax = fmaxf(cmax, fmaxf(fmaxf(v[i], v[i + 1]), fmaxf(v[i + 2], v[i + 3])));
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 64; ++i) {
-                            v[i] = (c0 + i < valid) ? v[i] : -INFINITY;
+                        for (int i = 0; i < kEpiCols; ++i) {
+                            v[i] = i < valid ? v[i] : -INFINITY;
                             cmax = fmaxf(cmax, v[i]);
                         }
                     }
                     if (cmax > best) {  // columns ascend, so only a strictly larger score moves the argmax
                         int first = 0;
 #pragma unroll
-                        for (int i = 63; i >= 0; --i)
+                        for (int i = kEpiCols - 1; i >= 0; --i)
                             if (v[i] == cmax) first = i;
                         best = cmax;
-                        bidx = c_lo + c0 + first;
+                        bidx = c_lo + first;
                     }
                 }
-                fence_before();
-                mbar_arrive(&bars->tempty[b]);
             }
-            // combine the two column halves of each row
-            if (hf == 1) {
-                bars->comb_s[row] = best;
-                bars->comb_i[row] = bidx;
+            // combine the column quarters of each row
+            if (hf > 0) {
+                bars->comb_s[hf - 1][row] = best;
+                bars->comb_i[hf - 1][row] = bidx;
             }
             asm volatile("bar.sync 2, %0;" ::"r"(kEpiThreads) : "memory");
             if (hf == 0) {
-                const float os = bars->comb_s[row];
-                const int oi = bars->comb_i[row];
-                if (better(os, oi, best, bidx)) {
-                    best = os;
-                    bidx = oi;
+#pragma unroll
+                for (int k = 0; k < kEpiWarps / 4 - 1; ++k) {
+                    const float os = bars->comb_s[k][row];
+                    const int oi = bars->comb_i[k][row];
+                    if (better(os, oi, best, bidx)) {
+                        best = os;
+                        bidx = oi;
+                    }
                 }
                 // promoted tokens keep themselves as parent
                 if (ok && j < N && I.Np > 0 && !promoted) token_parent[(size_t)I.u * n_cap + j] = bidx;
