@@ -411,6 +411,11 @@ ice_status ice_decode_step(const ice_params *p, const ice_index *idx, const void
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // one cluster per unit pays off while all clusters fit in one wave; with
     // more units the select / attention kernels keep every SM streaming
+    if (units_of(*p) * kDecodeCluster <= sm_count() && aligned16(Q) &&
+        decode_cluster2_supported(*p, w.k_pages, max_sel))
+        return cuda_status(launch_decode_cluster2(*p, *idx, Q, w.k_pages, sel_pages, sel_count, max_sel, kbuf, vbuf,
+                                                  buf_len, scale, O, err_dev, s),
+                           "ice_decode_step");
     if (units_of(*p) * kDecodeCluster <= sm_count() && decode_cluster_supported(*p, w.k_pages, max_sel))
         return cuda_status(launch_decode_cluster(*p, *idx, Q, w.k_pages, sel_pages, sel_count, max_sel, kbuf, vbuf,
                                                  buf_len, scale, O, err_dev, s),

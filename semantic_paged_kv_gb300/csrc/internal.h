@@ -104,6 +104,13 @@ cudaError_t launch_decode_cluster(const ice_params &p, const ice_index &idx, con
                                   int32_t *sel_pages, int32_t *sel_count, int max_sel, void *kbuf, void *vbuf,
                                   int32_t *buf_len, float scale, float *O, int32_t *err, cudaStream_t s);
 
+// The same for bf16 tables with g <= 8 and k <= 32 pages per head: bulk-copied
+// pages, bisection top-k, packed fp32-pair arithmetic.
+bool decode_cluster2_supported(const ice_params &p, int k_pages, int max_sel);
+cudaError_t launch_decode_cluster2(const ice_params &p, const ice_index &idx, const void *Q, int k_pages,
+                                   int32_t *sel_pages, int32_t *sel_count, int max_sel, void *kbuf, void *vbuf,
+                                   int32_t *buf_len, float scale, float *O, int32_t *err, cudaStream_t s);
+
 // Allocation-free attention: scratch in the library's static device array.
 size_t attention_noalloc_bytes(const ice_params &p, int max_sel);
 cudaError_t launch_attention_noalloc(const ice_params &p, const void *Q, const void *kbuf, const void *vbuf,
