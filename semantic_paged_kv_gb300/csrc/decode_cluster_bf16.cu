@@ -216,7 +216,7 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT) k_decode_cluste
         s_span[loc] = sp;
     }
     {
-        constexpr int U4 = 4;  // parent rows per lane in flight
+        constexpr int U4 = 8;  // parent rows per lane in flight
         for (int base = 0; base < chunk; base += kW * 2 * U4) {
             uint4 raw[U4];
 #pragma unroll
@@ -271,14 +271,24 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT) k_decode_cluste
         uint32_t tbits = 0u;  // order-preserving form of T
         if (nvalid >= kc) {
             uint32_t res = 0u;
-            for (int bit = 31; bit >= 0; --bit) {
-                const uint32_t cnd = res | (1u << bit);
-                int cnt = 0;
-                for (int x0 = 0; x0 < nvalid; x0 += 32) {
-                    const int x = x0 + lane;
-                    cnt += __popc(__ballot_sync(0xffffffffu, x < nvalid && ord_f32(sc[x]) >= cnd));
+            if (nvalid <= 8 * 32) {  // the lane's values in registers, counts summed by one reduction per bit
+                uint32_t vo[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) vo[e] = e * 32 + lane < nvalid ? ord_f32(sc[e * 32 + lane]) : 0u;
+                for (int bit = 31; bit >= 0; --bit) {
+                    const uint32_t cnd = res | (1u << bit);
+                    unsigned cnt = 0;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) cnt += vo[e] >= cnd;
+                    if ((int)__reduce_add_sync(0xffffffffu, cnt) >= kc) res = cnd;
                 }
-                if (cnt >= kc) res = cnd;
+            } else {
+                for (int bit = 31; bit >= 0; --bit) {
+                    const uint32_t cnd = res | (1u << bit);
+                    unsigned cnt = 0;
+                    for (int x = lane; x < nvalid; x += 32) cnt += ord_f32(sc[x]) >= cnd;
+                    if ((int)__reduce_add_sync(0xffffffffu, cnt) >= kc) res = cnd;
+                }
             }
             tbits = res;
         }

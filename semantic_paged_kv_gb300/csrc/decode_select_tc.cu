@@ -395,9 +395,11 @@ __global__ void __launch_bounds__(32 * BQ) k_select_topk(
                 uint32_t r = 0u;
                 for (int bit = 31; bit >= 0; --bit) {
                     const uint32_t c = r | (1u << bit);
-                    int n = c <= prev ? kc : 0;  // the earlier stretches already hold kc keys >= prev
+                    unsigned cnt = 0;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) n += __popc(__ballot_sync(0xffffffffu, v[e] >= c));
+                    for (int e = 0; e < 8; ++e) cnt += v[e] >= c;
+                    // the earlier stretches already hold kc keys >= prev
+                    const int n = (int)__reduce_add_sync(0xffffffffu, cnt) + (c <= prev ? kc : 0);
                     if (n >= kc) r = c;
                 }
                 res = r;
