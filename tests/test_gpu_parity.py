@@ -107,6 +107,20 @@ def test_many_units_take_select_and_attention_kernels():
         _all_units_decode(run, [128], fused=False)
 
 
+def test_one_attention_cta_per_unit():
+    """More units than SMs with a 128-page selection: the streaming attention
+    runs one CTA per unit and writes O directly (fused and separate calls)."""
+    w = W["qwen3_32b_100k"].scaled(n_tokens=2200, batch=20, centres=128)
+    run = GpuRun(w)
+    assert run.status == ice.ICE_OK
+    assert run.cfg.units >= torch.cuda.get_device_properties(0).multi_processor_count
+    for fused in (True, False):
+        Q, buf, st = run.decode(256, fused=fused)
+        assert st == ice.ICE_OK
+        for u in (0, 77, run.cfg.units - 1):
+            check_decode_unit(run, u, Q, 256, buf)
+
+
 def test_longchat_100k_full_size_sampled():
     """The LongChat-7B-shaped layer at its full size (32 KV heads, N = 100000,
     log-normal norms) in the launch configuration the benchmark times: the
