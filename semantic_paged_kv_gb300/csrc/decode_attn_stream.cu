@@ -384,13 +384,24 @@ __global__ void __launch_bounds__(kUT, 1) k_attn_unit(
     }
     __syncthreads();
 
-    // page k of this warp: share index warp + k * kUW, in slot k & 1
-    const int nk = np > warp ? (np - warp + kUW - 1) / kUW : 0;
-    auto issue = [&](int k) {
+    // page k of this warp: share index warp + k * kUW, in slot k & 1; lane k
+    // holds its page id and length (one round trip for all of them)
+    const int nk = np > warp ? (np - warp + kUW - 1) / kUW : 0;  // <= 32 (checked on the host)
+    int my_pid = 0, my_len = 0;
+    if (lane < nk) {
+        const size_t sl = ubase + xs + warp + lane * kUW;
+        if (kFused) {
+            my_pid = sel_pages[sl];
+            my_len = page_len[(size_t)u * page_cap + my_pid];
+        } else {
+            my_len = buf_len[sl];
+        }
+    }
+    auto issue = [&](int k, int pid) {
         const int x = xs + warp + k * kUW;
         const __nv_bfloat16 *sk, *sv;
         if (kFused) {
-            const size_t pg = (size_t)u * page_cap + sel_pages[ubase + x];
+            const size_t pg = (size_t)u * page_cap + pid;
             sk = pool_k + pg * kPageElems;
             sv = pool_v + pg * kPageElems;
         } else {
@@ -401,9 +412,12 @@ __global__ void __launch_bounds__(kUT, 1) k_attn_unit(
         bulk_load(S.kv[warp][k & 1][0], sk, kPageBytes, &S.full[warp][k & 1]);
         bulk_load(S.kv[warp][k & 1][1], sv, kPageBytes, &S.full[warp][k & 1]);
     };
-    if (lane == 0) {
-        if (nk > 0) issue(0);
-        if (nk > 1) issue(1);
+    {
+        const int p0 = __shfl_sync(0xffffffffu, my_pid, 0), p1 = __shfl_sync(0xffffffffu, my_pid, 1);
+        if (lane == 0) {
+            if (nk > 0) issue(0, p0);
+            if (nk > 1) issue(1, p1);
+        }
     }
 
     const int c = lane & 15, half = lane >> 4;
@@ -427,13 +441,9 @@ __global__ void __launch_bounds__(kUT, 1) k_attn_unit(
     for (int k = 0; k < nk; ++k) {
         const int x = xs + warp + k * kUW;
         const size_t slot = ubase + x;
-        int len;
-        if (kFused) {
-            len = page_len[(size_t)u * page_cap + sel_pages[slot]];
-            if (lane == 0) buf_len[slot] = len;
-        } else {
-            len = buf_len[slot];
-        }
+        const int len = __shfl_sync(0xffffffffu, my_len, k);
+        const int pid_next = __shfl_sync(0xffffffffu, my_pid, (k + 2) & 31);
+        if (kFused && lane == 0) buf_len[slot] = len;
         if (ok) ok = mbar_wait(&S.full[warp][k & 1], (k >> 1) & 1);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -531,7 +541,7 @@ __global__ void __launch_bounds__(kUT, 1) k_attn_unit(
         // refill this slot with page k + 2 once its stores have read it
         if (lane == 0 && k + 2 < nk) {
             if (kFused) bulk_wait_read_all();
-            issue(k + 2);
+            issue(k + 2, pid_next);
         }
         __syncwarp();
     }
@@ -654,7 +664,8 @@ cudaError_t launch_f(const ice_params &p, const ice_index *pool, const int32_t *
         int splits = n_sm / U;
         const int most = (max_sel + kUW - 1) / kUW;
         splits = splits < 1 ? 1 : (splits > most ? most : splits);
-        if (splits <= ws.n_splits) {
+        const int per_warp = (ceil_div(max_sel, splits) + kUW - 1) / kUW;  // pages a warp takes
+        if (splits <= ws.n_splits && per_warp <= 32) {
             cudaError_t e = cudaErrorNotSupported;
             if (g <= 1) e = launch_unit<F, 1>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s, splits);
             else if (g <= 2) e = launch_unit<F, 2>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s, splits);
