@@ -1,0 +1,428 @@
+// Decode steps a9 (bulk gather of the selected pages) and a10 (masked sparse
+// attention over them) for bf16 pools with up to 16 query heads per KV head,
+// the two contractions of each page on warp-level tensor-core MMAs.
+//
+// papernotes.org "IceCache: Memory-Efficient KV-cache Management for
+// Long-Sequence LLMs", 关键设计 4: the selected pages are collected into one
+// contiguous buffer; 关键设计 1: a_ij = s_ij exp(q_i.k_j/sqrt(d)) /
+// sum_j' s_ij' exp(q_i.k_j'/sqrt(d)) over the selected pages only.
+//
+// k_attn_mma<F, HR>: grid (S, units), 12 warps; CTA s takes its share of the
+// unit's union, warp w the share's pages w, w + 12, ... in order, double-
+// buffered in the warp's two shared-memory slots by 2-D TMA loads with a
+// 128-byte swizzle (so the 8-row fragment loads below are conflict-free).
+// Per page, with the g <= 16 query rows of the group as the M = 16 rows:
+//   S = Q K^T     mma.sync m16n8k16 (bf16 in, fp32 accumulate): A = q in
+//                 registers (loaded once), B = K rows by ldmatrix; 2 key
+//                 tiles x 8 dimension steps;
+//   online softmax on the accumulator fragments: a quad of lanes holds a
+//                 row's 16 keys (two shuffles per reduction), masked past
+//                 the page length;
+//   O += P V      P as the A fragment straight from S's accumulators, split
+//                 into bf16 hi + lo parts (two MMAs, ~2^-16 relative error
+//                 instead of bf16's 2^-9); B = V rows by ldmatrix.trans;
+//                 16 dimension tiles.
+// With F the page goes back to kbuf / vbuf by 2-D TMA stores from shared
+// memory (the slot is reloaded only after its stores have read it) and its
+// length to buf_len.  The warps merge in shared memory; with S = 1 the CTA
+// writes O, otherwise its partial joins the others through the unit's ticket
+// (log-sum-exp, the last CTA writes O).  HR = 2 when g > 8 (rows 8..15 hold
+// query heads too).
+#include <cuda.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace ice {
+namespace {
+
+using namespace tc;
+
+constexpr int kMW = 12;  // warps per CTA
+constexpr int kMT = kMW * 32;
+constexpr uint32_t kHalfBytes = kPage * 128;       // 16 rows x 64 bf16 columns (one swizzled box)
+constexpr uint32_t kTileBytes = 2 * kHalfBytes;    // K or V of one page: 4 KB
+constexpr uint32_t kSlotBytes = 2 * kTileBytes;    // K and V
+
+struct SmemM {
+    unsigned char kv[kMW][2][kSlotBytes];  // per warp two slots: 192 KB, reused by the merge
+    float ml[kMW][16][2];                  // per warp and query row: running max, sum
+    float wgt[kMW][16];
+    float cml[16][2];
+    unsigned long long full[kMW][2];
+    int last;
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+// D += A B, m16n8k16, bf16 in, fp32 accumulate.
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// bf16 pair (round to nearest) and the pair of remainders, as packed words.
+__device__ __forceinline__ void split_pair(float x, float y, uint32_t &hi, uint32_t &lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x - hf.x, y - hf.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+// Shared-memory address of 16-byte chunk `cc` (0..15 across the two 64-column
+// halves) of row `row` in a 128-byte-swizzled 16-row tile.
+__device__ __forceinline__ uint32_t sw_addr(uint32_t tile, int row, int cc) {
+    return tile + (uint32_t)((cc >> 3) * kHalfBytes + row * 128 + (((cc & 7) ^ (row & 7)) << 4));
+}
+
+template <bool kFused, int HR>
+__global__ void __launch_bounds__(kMT, 1) k_attn_mma(
+    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+    const __grid_constant__ CUtensorMap tm_kb, const __grid_constant__ CUtensorMap tm_vb,
+    const __nv_bfloat16 *__restrict__ Q, int g, int n_q_heads, int n_kv_heads, const int32_t *__restrict__ page_len,
+    int page_cap, const int32_t *__restrict__ sel_pages, int32_t *__restrict__ buf_len,
+    const int32_t *__restrict__ sel_count, int max_sel, float scale, int n_splits, float *__restrict__ part_ml,
+    float *__restrict__ part_o, int32_t *__restrict__ ticket, float *__restrict__ O, int32_t *__restrict__ err) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    // the swizzled page tiles want 1024-byte alignment
+    SmemM &S = *reinterpret_cast<SmemM *>(smem_raw + ((1024u - (su32(smem_raw) & 1023u)) & 1023u));
+    const int u = blockIdx.y, split = blockIdx.x;
+    const int b = u / n_kv_heads, h = u % n_kv_heads;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int qr = lane >> 2, qc = lane & 3;  // fragment row (query row) and column pair
+    const int n = min(sel_count[u], max_sel);
+    const int ps = (max_sel + n_splits - 1) / n_splits;
+    const int xs = split * ps;
+    const int xe = min(n, xs + ps);
+    const int np = max(0, xe - xs);
+    const size_t ubase = (size_t)u * max_sel;
+
+    if (tid < 2 * kMW) mbar_init(&S.full[tid >> 1][tid & 1], 1);
+    if (tid == 0) mbar_init_fence();
+    if (kFused)
+        for (int x = max(xs, n) + tid; x < min(xs + ps, max_sel); x += kMT) buf_len[ubase + x] = 0;
+    if (lane < 16) {
+        S.ml[warp][lane][0] = -INFINITY;
+        S.ml[warp][lane][1] = 0.f;
+    }
+    __syncthreads();
+
+    // this warp's pages: lane k holds page k's id and length
+    const int nk = np > warp ? (np - warp + kMW - 1) / kMW : 0;  // <= 32 (checked on the host)
+    int my_pid = 0, my_len = 0;
+    if (lane < nk) {
+        const size_t sl = ubase + xs + warp + lane * kMW;
+        if (kFused) {
+            my_pid = sel_pages[sl];
+            my_len = page_len[(size_t)u * page_cap + my_pid];
+        } else {
+            my_len = buf_len[sl];
+        }
+    }
+    auto issue = [&](int k, int pid) {
+        const int x = xs + warp + k * kMW;
+        const int row = kFused ? (u * page_cap + pid) * kPage : (int)((ubase + x) * kPage);
+        unsigned char *slot = S.kv[warp][k & 1];
+        unsigned long long *bar = &S.full[warp][k & 1];
+        mbar_expect_tx(bar, kSlotBytes);
+        tma_load_2d(slot, &tm_k, bar, 0, row);
+        tma_load_2d(slot + kHalfBytes, &tm_k, bar, 64, row);
+        tma_load_2d(slot + kTileBytes, &tm_v, bar, 0, row);
+        tma_load_2d(slot + kTileBytes + kHalfBytes, &tm_v, bar, 64, row);
+    };
+    {
+        const int p0 = __shfl_sync(0xffffffffu, my_pid, 0), p1 = __shfl_sync(0xffffffffu, my_pid, 1);
+        if (lane == 0) {
+            if (nk > 0) issue(0, p0);
+            if (nk > 1) issue(1, p1);
+        }
+    }
+
+    // A fragments of Q (rows = query rows of the group), 8 steps of 16 dims
+    uint32_t qa[8][4];
+    {
+        const __nv_bfloat16 *Qu = Q + ((size_t)b * n_q_heads + (size_t)h * g) * kHeadDim;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const int c0 = ks * 16 + 2 * qc;
+            qa[ks][0] = qr < g ? *reinterpret_cast<const uint32_t *>(Qu + (size_t)qr * kHeadDim + c0) : 0u;
+            qa[ks][1] = (HR > 1 && qr + 8 < g) ? *reinterpret_cast<const uint32_t *>(Qu + (size_t)(qr + 8) * kHeadDim + c0) : 0u;
+            qa[ks][2] = qr < g ? *reinterpret_cast<const uint32_t *>(Qu + (size_t)qr * kHeadDim + c0 + 8) : 0u;
+            qa[ks][3] = (HR > 1 && qr + 8 < g) ? *reinterpret_cast<const uint32_t *>(Qu + (size_t)(qr + 8) * kHeadDim + c0 + 8) : 0u;
+        }
+    }
+    float o[16][4];
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+    bool ok = true;
+    for (int k = 0; k < nk; ++k) {
+        const int x = xs + warp + k * kMW;
+        const size_t slot = ubase + x;
+        const int len = __shfl_sync(0xffffffffu, my_len, k);
+        const int pid_next = __shfl_sync(0xffffffffu, my_pid, (k + 2) & 31);
+        if (kFused && lane == 0) buf_len[slot] = len;
+        if (ok) ok = mbar_wait(&S.full[warp][k & 1], (k >> 1) & 1);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        unsigned char *sp = S.kv[warp][k & 1];
+        if (kFused && lane == 0) {  // the contiguous buffer, straight from shared memory
+            fence_proxy_async();
+            const int row = (int)(slot * kPage);
+            tma_store_2d(&tm_kb, sp, 0, row);
+            tma_store_2d(&tm_kb, sp + kHalfBytes, 64, row);
+            tma_store_2d(&tm_vb, sp + kTileBytes, 0, row);
+            tma_store_2d(&tm_vb, sp + kTileBytes + kHalfBytes, 64, row);
+            bulk_commit();
+        }
+        const uint32_t ks_base = su32(sp), vs_base = su32(sp + kTileBytes);
+        // ---- S = Q K^T: two 8-key tiles
+        float s[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < 8; kk += 2) {
+                // matrices: keys 8nt..8nt+7 x 16-byte chunks 2kk .. 2kk + 3
+                const int mi = lane >> 3;
+                const uint32_t addr = sw_addr(ks_base, 8 * nt + (lane & 7), 2 * kk + mi);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(addr, b0, b1, b2, b3);
+                mma16816(s[nt], qa[kk], b0, b1);
+                mma16816(s[nt], qa[kk + 1], b2, b3);
+            }
+        }
+        // ---- online softmax of rows qr (and qr + 8): keys 8nt + 2qc + {0, 1}
+        float p[2][2][2];  // [row half][tile][pair]
+        float alpha[2];
+#pragma unroll
+        for (int rh = 0; rh < HR; ++rh) {
+            float v[2][2];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int key = 8 * nt + 2 * qc + e;
+                    v[nt][e] = key < len ? s[nt][2 * rh + e] * scale : -INFINITY;
+                    mx = fmaxf(mx, v[nt][e]);
+                }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float m_new = fmaxf(m_run[rh], mx);
+            alpha[rh] = m_run[rh] == -INFINITY ? 0.f : expf(m_run[rh] - m_new);
+            float sm = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    p[rh][nt][e] = v[nt][e] == -INFINITY ? 0.f : expf(v[nt][e] - m_new);
+                    sm += p[rh][nt][e];
+                }
+            sm += __shfl_xor_sync(0xffffffffu, sm, 1);
+            sm += __shfl_xor_sync(0xffffffffu, sm, 2);
+            l_run[rh] = l_run[rh] * alpha[rh] + sm;
+            m_run[rh] = m_new;
+        }
+        if (HR == 1) {
+            alpha[1] = 0.f;
+            p[1][0][0] = p[1][0][1] = p[1][1][0] = p[1][1][1] = 0.f;
+        }
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+            o[nt][0] *= alpha[0];
+            o[nt][1] *= alpha[0];
+            o[nt][2] *= alpha[1];
+            o[nt][3] *= alpha[1];
+        }
+        // ---- O += P V: A = P (rows x 16 keys) as bf16 hi + lo
+        uint32_t ahi[4], alo[4];
+        split_pair(p[0][0][0], p[0][0][1], ahi[0], alo[0]);
+        split_pair(p[1][0][0], p[1][0][1], ahi[1], alo[1]);
+        split_pair(p[0][1][0], p[0][1][1], ahi[2], alo[2]);
+        split_pair(p[1][1][0], p[1][1][1], ahi[3], alo[3]);
+#pragma unroll
+        for (int nt = 0; nt < 16; nt += 2) {
+            // matrices: (keys 0-7, chunk nt), (keys 8-15, chunk nt), (keys 0-7, nt+1), (keys 8-15, nt+1)
+            const int mi = lane >> 3;
+            const uint32_t addr = sw_addr(vs_base, (mi & 1) * 8 + (lane & 7), nt + (mi >> 1));
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(addr, b0, b1, b2, b3);
+            mma16816(o[nt], ahi, b0, b1);
+            mma16816(o[nt], alo, b0, b1);
+            mma16816(o[nt + 1], ahi, b2, b3);
+            mma16816(o[nt + 1], alo, b2, b3);
+        }
+        __syncwarp();
+        if (lane == 0 && k + 2 < nk) {  // refill this slot once its stores have read it
+            if (kFused) bulk_wait_read_all();
+            issue(k + 2, pid_next);
+        }
+        __syncwarp();
+    }
+    if (!ok) set_err(err, ICE_ERR_TIMEOUT);
+    if (kFused && lane == 0) bulk_wait_read_all();  // the slots are reused below
+    if (qc == 0) {
+        S.ml[warp][qr][0] = m_run[0];
+        S.ml[warp][qr][1] = l_run[0];
+        if (HR > 1) {
+            S.ml[warp][qr + 8][0] = m_run[1];
+            S.ml[warp][qr + 8][1] = l_run[1];
+        }
+    }
+    __syncthreads();
+
+    // ---- merge the warps (slot area reused): s_o[w][row][d]
+    float *s_o = reinterpret_cast<float *>(&S.kv[0][0][0]);
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) {
+        const int d = 8 * nt + 2 * qc;
+        *reinterpret_cast<float2 *>(s_o + ((size_t)warp * 16 + qr) * kHeadDim + d) = make_float2(o[nt][0], o[nt][1]);
+        if (HR > 1)
+            *reinterpret_cast<float2 *>(s_o + ((size_t)warp * 16 + qr + 8) * kHeadDim + d) = make_float2(o[nt][2], o[nt][3]);
+    }
+    if (tid < g) {
+        float M = -INFINITY;
+        for (int w = 0; w < kMW; ++w) M = fmaxf(M, S.ml[w][tid][0]);
+        float L = 0.f;
+        for (int w = 0; w < kMW; ++w) {
+            const float m = S.ml[w][tid][0];
+            const float wt = m == -INFINITY ? 0.f : expf(m - M);
+            S.wgt[w][tid] = wt;
+            L = fmaf(S.ml[w][tid][1], wt, L);
+        }
+        S.cml[tid][0] = M;
+        S.cml[tid][1] = L;
+        if (n_splits > 1) {
+            const size_t pb = ((size_t)u * n_splits + split) * g + tid;
+            part_ml[pb * 2 + 0] = M;
+            part_ml[pb * 2 + 1] = L;
+        }
+    }
+    __syncthreads();
+    for (int xx = tid; xx < g * kHeadDim; xx += kMT) {
+        const int hh = xx / kHeadDim, d = xx % kHeadDim;
+        float acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < kMW; ++w) acc = fmaf(s_o[((size_t)w * 16 + hh) * kHeadDim + d], S.wgt[w][hh], acc);
+        if (n_splits == 1) {
+            const float L = S.cml[hh][1];
+            O[((size_t)b * n_q_heads + (size_t)h * g + hh) * kHeadDim + d] = L > 0.f ? acc / L : 0.f;
+        } else {
+            part_o[(((size_t)u * n_splits + split) * g + hh) * kHeadDim + d] = acc;
+        }
+    }
+    if (n_splits == 1) return;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) S.last = (atomicAdd(ticket + u, 1) == n_splits - 1);
+    __syncthreads();
+    if (!S.last) return;
+    __threadfence();
+    float *s_w = s_o;  // [n_splits][g] weights, then [g] totals
+    const int nsg = n_splits * g;
+    const float *ml = part_ml + (size_t)u * nsg * 2;
+    if (tid < g) {
+        float M = -INFINITY;
+        for (int sp2 = 0; sp2 < n_splits; ++sp2) M = fmaxf(M, __ldcg(ml + 2 * (sp2 * g + tid)));
+        float L = 0.f;
+        for (int sp2 = 0; sp2 < n_splits; ++sp2) {
+            const float m = __ldcg(ml + 2 * (sp2 * g + tid));
+            const float wt = m == -INFINITY ? 0.f : expf(m - M);
+            s_w[sp2 * g + tid] = wt;
+            L = fmaf(__ldcg(ml + 2 * (sp2 * g + tid) + 1), wt, L);
+        }
+        s_w[nsg + tid] = L;
+    }
+    __syncthreads();
+    const float *po = part_o + (size_t)u * nsg * kHeadDim;
+    for (int xx = tid; xx < g * kHeadDim; xx += kMT) {
+        const int hh = xx / kHeadDim, d = xx % kHeadDim;
+        float acc = 0.f;
+        for (int sp2 = 0; sp2 < n_splits; ++sp2)
+            acc = fmaf(__ldcg(po + ((size_t)sp2 * g + hh) * kHeadDim + d), s_w[sp2 * g + hh], acc);
+        const float L = s_w[nsg + hh];
+        O[((size_t)b * n_q_heads + (size_t)h * g + hh) * kHeadDim + d] = L > 0.f ? acc / L : 0.f;
+    }
+    if (tid == 0) ticket[u] = 0;
+}
+
+template <bool F, int HR>
+cudaError_t launch_hr(const ice_params &p, const ice_index *pool, const int32_t *sel_pages, const void *Q, void *kbuf,
+                      void *vbuf, int32_t *buf_len, const int32_t *sel_count, int max_sel, float scale, float *O,
+                      const DecodeWs &ws, int32_t *err, cudaStream_t s, int n_splits) {
+    const int U = units_of(p);
+    const int g = p.n_q_heads / p.n_kv_heads;
+    CUtensorMap tk, tv, tkb, tvb;
+    const unsigned long long prow = (unsigned long long)U * p.page_cap * kPage;
+    const unsigned long long brow = (unsigned long long)U * max_sel * kPage;
+    if (brow > 0x7FFFFFFFull || prow > 0x7FFFFFFFull) return cudaErrorNotSupported;
+    if (!make_map_bf16(&tkb, kbuf, brow, kHeadDim, 64, kPage, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_bf16(&tvb, vbuf, brow, kHeadDim, 64, kPage, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorNotSupported;
+    if (F) {
+        if (!make_map_bf16(&tk, pool->pool_k, prow, kHeadDim, 64, kPage, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_map_bf16(&tv, pool->pool_v, prow, kHeadDim, 64, kPage, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorNotSupported;
+    } else {
+        tk = tkb;
+        tv = tvb;
+    }
+    const size_t merge = sizeof(float) * (size_t)(n_splits * g + g);
+    const size_t need = (sizeof(SmemM) > merge ? sizeof(SmemM) : merge) + 1024;  // + alignment slack
+    if (need > 227 * 1024) return cudaErrorNotSupported;
+    cudaError_t e = cudaFuncSetAttribute(k_attn_mma<F, HR>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)need);
+    if (e != cudaSuccess) return e;
+    k_attn_mma<F, HR><<<dim3(n_splits, U), kMT, need, s>>>(
+        tk, tv, tkb, tvb, static_cast<const __nv_bfloat16 *>(Q), g, p.n_q_heads, p.n_kv_heads,
+        pool ? pool->page_len : nullptr, p.page_cap, sel_pages, buf_len, sel_count, max_sel, scale, n_splits,
+        ws.part_ml, ws.part_o, ws.attn_ticket, O, err);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool attention_mma_supported(const ice_params &p) {
+    const int g = p.n_q_heads / p.n_kv_heads;
+    return p.dtype == ICE_BF16 && g >= 1 && g <= 16;
+}
+
+// One CTA per unit while the units fill the SMs, else a few per unit; each
+// warp takes at most 32 pages.  cudaErrorNotSupported: nothing launched.
+cudaError_t launch_attention_mma(const ice_params &p, const ice_index *pool, const int32_t *sel_pages, const void *Q,
+                                 void *kbuf, void *vbuf, int32_t *buf_len, const int32_t *sel_count, int max_sel,
+                                 float scale, float *O, const DecodeWs &ws, int32_t *err, cudaStream_t s) {
+    const int U = units_of(p);
+    const int g = p.n_q_heads / p.n_kv_heads;
+    static int n_sm = 0;
+    if (!n_sm) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+        if (n_sm <= 0) n_sm = 1;
+    }
+    int splits = n_sm / U;
+    const int most = (max_sel + kMW - 1) / kMW;
+    splits = splits < 1 ? 1 : (splits > most ? most : splits);
+    const int per_warp = (ceil_div(max_sel, splits) + kMW - 1) / kMW;
+    if (splits > ws.n_splits || per_warp > 32) return cudaErrorNotSupported;
+    if (pool) {
+        if (g <= 8) return launch_hr<true, 1>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s, splits);
+        return launch_hr<true, 2>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s, splits);
+    }
+    if (g <= 8) return launch_hr<false, 1>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s, splits);
+    return launch_hr<false, 2>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s, splits);
+}
+
+}  // namespace ice

@@ -88,6 +88,11 @@ cudaError_t launch_attention(const ice_params &p, const ice_index *pool, const i
                              const void *Q, void *kbuf, void *vbuf, int32_t *buf_len, const int32_t *sel_count,
                              int max_sel, float scale, float *O, const DecodeWs &ws, cudaStream_t s,
                              int32_t *err = nullptr);
+// The same with the page contractions on warp-level MMAs (bf16, g <= 16).
+bool attention_mma_supported(const ice_params &p);
+cudaError_t launch_attention_mma(const ice_params &p, const ice_index *pool, const int32_t *sel_pages, const void *Q,
+                                 void *kbuf, void *vbuf, int32_t *buf_len, const int32_t *sel_count, int max_sel,
+                                 float scale, float *O, const DecodeWs &ws, int32_t *err, cudaStream_t s);
 // The same with bulk-copied pages, one page per warp (bf16, g <= 8).
 bool attention_stream_supported(const ice_params &p);
 cudaError_t launch_attention_stream(const ice_params &p, const ice_index *pool, const int32_t *sel_pages,
