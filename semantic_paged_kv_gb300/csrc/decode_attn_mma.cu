@@ -101,21 +101,22 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
     const int b = u / n_kv_heads, h = u % n_kv_heads;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int qr = lane >> 2, qc = lane & 3;  // fragment row (query row) and column pair
+    if (tid < 2 * kMW) mbar_init(&S.full[tid >> 1][tid & 1], 1);
+    if (tid == 0) mbar_init_fence();
+    if (lane < 16) {
+        S.ml[warp][lane][0] = -INFINITY;
+        S.ml[warp][lane][1] = 0.f;
+    }
+    dep_wait();  // the selected pages (and the contiguous buffer) are complete
+
     const int n = min(sel_count[u], max_sel);
     const int ps = (max_sel + n_splits - 1) / n_splits;
     const int xs = split * ps;
     const int xe = min(n, xs + ps);
     const int np = max(0, xe - xs);
     const size_t ubase = (size_t)u * max_sel;
-
-    if (tid < 2 * kMW) mbar_init(&S.full[tid >> 1][tid & 1], 1);
-    if (tid == 0) mbar_init_fence();
     if (kFused)
         for (int x = max(xs, n) + tid; x < min(xs + ps, max_sel); x += kMT) buf_len[ubase + x] = 0;
-    if (lane < 16) {
-        S.ml[warp][lane][0] = -INFINITY;
-        S.ml[warp][lane][1] = 0.f;
-    }
     __syncthreads();
 
     // this warp's pages: lane k holds page k's id and length
@@ -384,11 +385,12 @@ cudaError_t launch_hr(const ice_params &p, const ice_index *pool, const int32_t 
     if (need > 227 * 1024) return cudaErrorNotSupported;
     cudaError_t e = cudaFuncSetAttribute(k_attn_mma<F, HR>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)need);
     if (e != cudaSuccess) return e;
-    k_attn_mma<F, HR><<<dim3(n_splits, U), kMT, need, s>>>(
-        tk, tv, tkb, tvb, static_cast<const __nv_bfloat16 *>(Q), g, p.n_q_heads, p.n_kv_heads,
-        pool ? pool->page_len : nullptr, p.page_cap, sel_pages, buf_len, sel_count, max_sel, scale, n_splits,
-        ws.part_ml, ws.part_o, ws.attn_ticket, O, err);
-    return cudaGetLastError();
+    const __nv_bfloat16 *Qb = static_cast<const __nv_bfloat16 *>(Q);
+    const int32_t *plen = pool ? pool->page_len : nullptr;
+    e = launch_dependent(k_attn_mma<F, HR>, dim3(n_splits, U), dim3(kMT), need, s, tk, tv, tkb, tvb, Qb, g,
+                         p.n_q_heads, p.n_kv_heads, plen, p.page_cap, sel_pages, buf_len, sel_count, max_sel, scale,
+                         n_splits, ws.part_ml, ws.part_o, ws.attn_ticket, O, err);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

@@ -33,11 +33,14 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "topk_common.cuh"
 
 namespace cg = cooperative_groups;
 
 namespace ice {
 namespace {
+
+using namespace topk;
 
 constexpr int kC = kDecodeCluster;  // CTAs per cluster = per unit
 constexpr int kT = 256;             // threads per CTA
@@ -45,12 +48,6 @@ constexpr int kWarps = kT / 32;
 constexpr int kMaxG = 16;
 constexpr int kPB = 8;              // pages per batch in phase 3
 
-__device__ __forceinline__ unsigned long long sort_key(float s, int id) {
-    uint32_t b = __float_as_uint(s);
-    b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-    return ((unsigned long long)b << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)id);
-}
-__device__ __forceinline__ int key_id(unsigned long long k) { return (int)(0xFFFFFFFFu - (uint32_t)k); }
 
 // The warp's best kc of keys[0..n) in descending order (0 = no key).  Keys
 // are unique, so round r takes the largest key below round r-1's.

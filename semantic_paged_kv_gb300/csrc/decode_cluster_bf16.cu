@@ -34,12 +34,14 @@
 #include "common.cuh"
 #include "internal.h"
 #include "tc_common.cuh"
+#include "topk_common.cuh"
 
 namespace ice {
 namespace {
 
 namespace cg = cooperative_groups;
 using namespace tc;
+using namespace topk;
 
 constexpr int kC = kDecodeCluster;  // CTAs per cluster = per unit
 constexpr int kT = 256;
@@ -48,19 +50,6 @@ constexpr int kPageElems = kPage * kHeadDim;
 constexpr uint32_t kPageBytes = kPageElems * 2;
 constexpr int kCand = 64;    // keys a selection warp collects
 constexpr int kMaxPPC = 16;  // pages of the union per CTA
-
-__device__ __forceinline__ unsigned long long sort_key(float s, int id) {
-    uint32_t b = __float_as_uint(s);
-    b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-    return ((unsigned long long)b << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)id);
-}
-__device__ __forceinline__ int key_id(unsigned long long k) { return (int)(0xFFFFFFFFu - (uint32_t)k); }
-__device__ __forceinline__ uint32_t ord_f32(float f) {
-    const uint32_t b = __float_as_uint(f);
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) { return a > b ? a : b; }
-__device__ __forceinline__ unsigned long long umin64(unsigned long long a, unsigned long long b) { return a < b ? a : b; }
 
 // Packed fp32 pairs (fma.rn.f32x2: two IEEE fp32 FMAs per instruction).
 __device__ __forceinline__ unsigned long long pk2(float x, float y) {
@@ -80,41 +69,6 @@ __device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigne
 }
 __device__ __forceinline__ unsigned long long bf2_pair(uint32_t w) {
     return pk2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-}
-
-// Descending bitonic sort of the warp's 64 keys: key i in lane i % 32 of v[i / 32].
-__device__ __forceinline__ void sort64_desc(unsigned long long (&v)[2]) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int size = 2; size <= 64; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            if (stride == 32) {
-                const unsigned long long a = v[0], b = v[1];
-                v[0] = umax64(a, b);
-                v[1] = umin64(a, b);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const unsigned long long o = __shfl_xor_sync(0xffffffffu, v[e], stride);
-                    const bool desc = ((e * 32 + lane) & size) == 0;
-                    const bool lower = (lane & stride) == 0;
-                    v[e] = (lower == desc) ? umax64(v[e], o) : umin64(v[e], o);
-                }
-            }
-        }
-    }
-}
-// The best 32 of two descending lists (one key per lane), descending.
-__device__ __forceinline__ unsigned long long merge32(unsigned long long a, unsigned long long b) {
-    const int lane = threadIdx.x & 31;
-    a = umax64(a, __shfl_sync(0xffffffffu, b, 31 - lane));
-#pragma unroll
-    for (int stride = 16; stride > 0; stride >>= 1) {
-        const unsigned long long o = __shfl_xor_sync(0xffffffffu, a, stride);
-        a = (lane & stride) == 0 ? umax64(a, o) : umin64(a, o);
-    }
-    return a;
 }
 
 // Shared-memory layout (byte offsets, 128-byte aligned pieces).

@@ -31,21 +31,17 @@
 // parent's earlier pages through the page_next chain.
 #include "common.cuh"
 #include "internal.h"
+#include "topk_common.cuh"
 
 namespace ice {
 namespace {
+
+using namespace topk;
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kHeadTile = 8;  // query heads scored per pass over a parent row
 
-// 64-bit key whose descending order is (score descending, id ascending).
-__device__ __forceinline__ unsigned long long sort_key(float s, int id) {
-    uint32_t b = __float_as_uint(s);
-    b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-    return ((unsigned long long)b << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)id);
-}
-__device__ __forceinline__ int key_id(unsigned long long k) { return (int)(0xFFFFFFFFu - (uint32_t)k); }
 
 // Sorts rows[r][0..n) descending for r < nrows (n a power of two) with every
 // thread of the block; ends with a barrier.

@@ -25,16 +25,18 @@
 //   warps 2-5  lane = parent: 16 fp32 scores from TMEM; the unit's g are
 //              written to the score table [unit][head][parent] (coalesced)
 //              and the maximum of each 32-parent group to [unit][head][group].
-//   The kernel streams the parent table once; its extra traffic is the
-//   score table (g x 4 bytes per 256-byte parent row).
+//   The kernel streams the parent table once; its extra traffic is the score
+//   table (g x 4 bytes per 256-byte parent row).
 // k_select_topk: one CTA per unit, one warp per query head.  The kc-th
 //   largest group maximum T0 is a lower bound of the kc-th best score (kc
 //   groups reach it), so the best kc keys (score, -m) all lie in the groups
-//   whose maximum is >= T0 (about kc of them): the warp sorts the group
-//   maxima (bitonic network), reads only those groups' scores, keeps the keys
-//   with score >= T0 and sorts them into the ordered best kc.  The ordered
-//   parents give pages until k per head, ORed into the union bitmask; the
-//   block writes the ascending page list.
+//   whose maximum is >= T0 (about kc of them): T0 by bisection on the group
+//   maxima, then only those groups' scores are read, the keys >= T0 sorted
+//   into the ordered best kc (their page spans load during the sort), whose
+//   pages (k per head) are ORed into the union bitmask; the block writes the
+//   ascending page list.  The kernel is a short chain of dependent loads; it
+//   runs after the streaming kernel so that the chain sees an idle memory
+//   system (inside the streaming kernel each load waited ~2.5 us).
 // Every mbarrier wait gives up after ~2 s and records ICE_ERR_TIMEOUT; the
 // roles drain what they issued and TMEM is freed before the CTA returns.
 #include <cuda.h>
@@ -42,11 +44,13 @@
 #include "common.cuh"
 #include "internal.h"
 #include "tc_common.cuh"
+#include "topk_common.cuh"
 
 namespace ice {
 namespace {
 
 using namespace tc;
+using namespace topk;
 
 constexpr int BM = 128;    // parents per tile (TMEM lanes)
 constexpr int BQ = 16;     // query rows per MMA (N)
@@ -69,23 +73,6 @@ struct Bars {
     uint32_t tmem_base;
 };
 constexpr size_t kSmemBytes = 1024 + (size_t)NS * A_BYTES + 2 * Q_BYTES + sizeof(Bars);
-
-// Order-preserving map of a float onto uint32 and back.
-__device__ __forceinline__ uint32_t ord_f32(float f) {
-    const uint32_t b = __float_as_uint(f);
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-__device__ __forceinline__ float unord_f32(uint32_t o) {
-    return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
-}
-// 64-bit key whose descending order is (score descending, id ascending).
-__device__ __forceinline__ unsigned long long sort_key(float s, int id) {
-    uint32_t b = __float_as_uint(s);
-    b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-    return ((unsigned long long)b << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)id);
-}
-__device__ __forceinline__ int key_id(unsigned long long k) { return (int)(0xFFFFFFFFu - (uint32_t)k); }
-__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) { return a > b ? a : b; }
 
 // Descending bitonic sort of the warp's 32 E values (E a power of two):
 // value i in lane i % 32 of register i / 32.  Strides below 32 pair lanes
@@ -141,6 +128,8 @@ __device__ __forceinline__ Seg seg_at(long long it, long long end, int T, int np
     return s;
 }
 
+__device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
 // Per lane: a[0..GT) values of GT heads; returns the maximum over the warp
 // of head *head (set here): recursive halving, each step a lane keeps half of
 // its heads and takes its partner's maxima for them (GT - 1 + 5 - log2 GT
@@ -164,6 +153,277 @@ __device__ __forceinline__ float warp_max_heads(float (&a)[GT], int &head) {
     float v = a[0];
     for (; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
+}
+
+// The ordered best kc (<= 32) keys of all Np scores of one head, exactly, by
+// kc rounds of a warp-wide maximum below the previous round's (slow; used
+// only when very many scores tie with the group-maximum bound).
+__device__ unsigned long long best_slow(const float *__restrict__ sh, int Np, int kc) {
+    const int lane = threadIdx.x & 31;
+    unsigned long long last = ~0ull, mine = 0ull;
+    for (int r = 0; r < kc; ++r) {
+        unsigned long long best = 0ull;
+        for (int m = lane; m < Np; m += 32) {
+            const unsigned long long k = sort_key(sh[m], m);
+            if (k < last && k > best) best = k;
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) best = umax64(best, __shfl_xor_sync(0xffffffffu, best, off));
+        if (lane == r) mine = best;
+        last = best;
+    }
+    return mine;
+}
+
+// What the selection of a unit reads and writes.
+struct SelArgs {
+    int g, np_cap, page_cap, k_pages, kc, max_sel;
+    const int32_t *n_parents, *n_pages;
+    const float *scores, *gmax;
+    const int32_t *parent_first_page, *parent_last_page, *parent_n_pages, *page_next;
+    int32_t *sel_pages, *sel_count, *err;
+};
+
+// The kc-th largest of the warp's values (8 per lane, order-preserving
+// integer form, 0 = none), found bit by bit from the top: the largest c with
+// at least kc values >= c.  Stops early once exactly kc values reach the
+// prefix: the answer is then their minimum.
+__device__ __forceinline__ uint32_t kth_largest_ord(const uint32_t (&v)[8], int kc) {
+    uint32_t r = 0u;
+    for (int bit = 31; bit >= 0; --bit) {
+        const uint32_t c = r | (1u << bit);
+        unsigned cnt = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) cnt += v[e] >= c;
+        const int n = (int)__reduce_add_sync(0xffffffffu, cnt);
+        if (n >= kc) {
+            r = c;
+            if (n == kc) {
+                uint32_t mn = 0xFFFFFFFFu;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) mn = v[e] >= c ? min(mn, v[e]) : mn;
+                return __reduce_min_sync(0xffffffffu, mn);
+            }
+        }
+    }
+    return r;
+}
+
+// Selection of unit u by the select group (NSW warps, thread tid of the
+// group): warp hh < g takes query head hh, finds its ordered best kc parents
+// and ORs their pages (k per head) into the union bitmask; then the group
+// writes the ascending page list.  Synchronises the group on barrier 2.
+// Parent ids stay below 2^24 (checked by the launcher), so the low key bits
+// can carry a candidate's slot while the order is unchanged.
+template <int NSW>
+__device__ void select_unit(const SelArgs &A, int u, int tid, unsigned *s_mask, unsigned long long *s_cand,
+                            int *s_wsum) {
+    constexpr int nt = 32 * NSW;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int g = A.g, np_cap = A.np_cap, kc = A.kc, k_pages = A.k_pages, max_sel = A.max_sel;
+    const int Np = min(A.n_parents[u], np_cap);
+    const size_t up = (size_t)u * np_cap, ug = (size_t)u * A.page_cap;
+    const int P = min(A.n_pages[u], A.page_cap);
+    const int words = (P + 31) / 32;
+    const int ngc = (np_cap + kGroup - 1) / kGroup, ng = (Np + kGroup - 1) / kGroup;
+    for (int x = tid; x < words; x += nt) s_mask[x] = 0u;
+    named_bar(2, nt);
+    if (k_pages >= P) {
+        for (int x = tid; x < words; x += nt) {
+            const int rem = P - x * 32;
+            s_mask[x] = rem >= 32 ? 0xffffffffu : ((1u << rem) - 1u);
+        }
+    } else if (warp < g) {
+        const int hh = warp;
+        const float *sh = A.scores + ((size_t)u * g + hh) * np_cap;
+        const float *gh = A.gmax + ((size_t)u * g + hh) * ngc;
+        unsigned long long *cand = s_cand + (size_t)hh * kCand;
+        int *glist = reinterpret_cast<int *>(cand + kCand - 64);  // qualifying groups (tail of the buffer)
+        // T0: the kc-th largest group maximum (a lower bound of the kc-th best
+        // score: kc groups reach it)
+        uint32_t v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int x = e * 32 + lane;
+            v[e] = x < ng ? ord_f32(__ldcg(gh + x)) : 0u;
+        }
+        float t0 = -INFINITY;
+        if (ng >= kc) {
+            if (ng <= 8 * 32) {
+                t0 = unord_f32(kth_largest_ord(v, kc));
+            } else {  // more groups: stretches of 256 with a running bound
+                uint32_t res = 0u;
+                for (int x0 = 0; x0 < ng; x0 += 8 * 32) {
+                    uint32_t w[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int x = x0 + e * 32 + lane;
+                        w[e] = x < ng ? ord_f32(__ldcg(gh + x)) : 0u;
+                    }
+                    const uint32_t prev = res;
+                    uint32_t r = 0u;
+                    for (int bit = 31; bit >= 0; --bit) {
+                        const uint32_t c = r | (1u << bit);
+                        unsigned cnt = 0;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) cnt += w[e] >= c;
+                        // the earlier stretches already hold kc keys >= prev
+                        const int n = (int)__reduce_add_sync(0xffffffffu, cnt) + (c <= prev ? kc : 0);
+                        if (n >= kc) r = c;
+                    }
+                    res = r;
+                }
+                t0 = unord_f32(res);
+            }
+        }
+        // keys with score >= T0, read only from groups whose maximum reaches it
+        int cnt = 0;
+        for (int x0 = 0; x0 < ng; x0 += 8 * 32) {
+            float gm[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int x = x0 + i * 32 + lane;
+                if (x0 == 0)
+                    gm[i] = x < ng ? unord_f32(v[i]) : -INFINITY;
+                else
+                    gm[i] = x < ng ? __ldcg(gh + x) : -INFINITY;
+            }
+            // the qualifying groups of this stretch, in order
+            int ngl = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const unsigned b = __ballot_sync(0xffffffffu, gm[i] >= t0);
+                if (((b >> lane) & 1u) && ngl + __popc(b & lanemask_lt()) < 128)
+                    glist[ngl + __popc(b & lanemask_lt())] = x0 + i * 32 + lane;
+                ngl += __popc(b);
+            }
+            __syncwarp();
+            if (ngl > 128) {  // very many ties with T0: exact slow path below
+                cnt = kCand + 1;
+                break;
+            }
+            for (int j0 = 0; j0 < ngl; j0 += 16) {  // 16 groups' loads in flight at once
+                float sv[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int m = j0 + i < ngl ? glist[j0 + i] * kGroup + lane : Np;
+                    sv[i] = m < Np ? __ldcg(sh + m) : -INFINITY;
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int m = j0 + i < ngl ? glist[j0 + i] * kGroup + lane : Np;
+                    const bool pass = m < Np && sv[i] >= t0;
+                    const unsigned bal = __ballot_sync(0xffffffffu, pass);
+                    const int at = cnt + __popc(bal & lanemask_lt());
+                    if (pass && at < kCand - 64) cand[at] = sort_key(sv[i], m);
+                    cnt += __popc(bal);
+                }
+            }
+            __syncwarp();
+        }
+        __syncwarp();
+        // lane r < kc: the r-th best parent and its pages
+        int pm = -1, fp = 0, pc = 0, contig = 1;
+        if (cnt <= 64) {
+            // the candidates' page spans load while the keys sort; a key's low
+            // byte holds its slot in the list
+            unsigned long long w[2];
+            int4 sp[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int i = e * 32 + lane;
+                const unsigned long long k = i < cnt ? cand[i] : 0ull;
+                sp[e] = make_int4(0, 0, 0, 0);
+                if (k != 0ull) {
+                    const int m = key_id(k);
+                    sp[e] = make_int4(A.parent_first_page[up + m], A.parent_n_pages[up + m],
+                                      A.parent_last_page[up + m], m);
+                }
+                w[e] = k == 0ull ? 0ull : ((k & 0xFFFFFFFF00000000ull) | ((k & 0xFFFFFFull) << 8) | (unsigned)i);
+            }
+            sort64_desc(w);
+            __syncwarp();
+            int4 *s_span = reinterpret_cast<int4 *>(cand);  // the list is in registers now
+            s_span[lane] = sp[0];
+            s_span[32 + lane] = sp[1];
+            __syncwarp();
+            if (lane < kc && w[0] != 0ull) {
+                const int4 s = s_span[(int)(w[0] & 0xFFu)];
+                pm = s.w;
+                fp = s.x;
+                pc = s.y;
+                contig = s.z - s.x + 1 == s.y;
+            }
+        } else {
+            unsigned long long best;
+            if (cnt <= kCand - 64) {
+                unsigned long long w[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) w[e] = e * 32 + lane < cnt ? cand[e * 32 + lane] : 0ull;
+                warp_sort_desc<unsigned long long, 8>(w);
+                best = w[0];
+            } else {
+                best = best_slow(sh, Np, kc);
+            }
+            if (lane < kc && best != 0ull) {
+                pm = key_id(best);
+                fp = A.parent_first_page[up + pm];
+                pc = A.parent_n_pages[up + pm];
+                contig = A.parent_last_page[up + pm] - fp + 1 == pc;
+            }
+        }
+        // take pages of the ordered parents until k pages
+        if (pm < 0) pc = 0;
+        int incl = pc;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        const int tk = max(0, min(pc, k_pages - (incl - pc)));
+        int pg = fp;
+        for (int i = 0; i < tk; ++i) {
+            const int qq = contig ? fp + i : pg;
+            if (qq < 0 || qq >= P) break;
+            atomicOr(&s_mask[qq >> 5], 1u << (qq & 31));
+            if (!contig) pg = A.page_next[ug + qq];
+        }
+    }
+    named_bar(2, nt);
+    // ascending list of the union's pages: thread tid owns words
+    // [tid * wpt, (tid + 1) * wpt); one block-wide scan of the counts
+    const int wpt = (words + nt - 1) / nt;
+    const int wb = tid * wpt, we = min(words, wb + wpt);
+    int c = 0;
+    for (int x = wb; x < we; ++x) c += __popc(s_mask[x]);
+    int incl = c;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    named_bar(2, nt);
+    int pos = incl - c, total = 0;
+#pragma unroll
+    for (int w = 0; w < NSW; ++w) {
+        const int sw = s_wsum[w];
+        pos += w < warp ? sw : 0;
+        total += sw;
+    }
+    for (int x = wb; x < we && pos < max_sel; ++x) {
+        unsigned bb = s_mask[x];
+        while (bb && pos < max_sel) {
+            const int bit = __ffs(bb) - 1;
+            bb &= bb - 1;
+            A.sel_pages[(size_t)u * max_sel + pos++] = x * 32 + bit;
+        }
+    }
+    for (int x = total + tid; x < max_sel; x += nt) A.sel_pages[(size_t)u * max_sel + x] = -1;
+    if (tid == 0) {
+        if (total > max_sel) set_err(A.err, ICE_ERR_CAPACITY);
+        A.sel_count[u] = min(total, max_sel);
+    }
 }
 
 template <int GT>
@@ -202,6 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_after();
     const uint32_t tmem = bars->tmem_base;
     bool ok = true;
+    dep_trigger();  // the selection grid may be scheduled now; it waits for this one
 
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer
@@ -326,215 +587,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// The ordered best kc (<= 32) keys of all Np scores of one head, exactly, by
-// kc rounds of a warp-wide maximum below the previous round's (slow; used
-// only when very many scores tie with the group-maximum bound).
-__device__ unsigned long long best_slow(const float *__restrict__ sh, int Np, int kc) {
-    const int lane = threadIdx.x & 31;
-    unsigned long long last = ~0ull, mine = 0ull;
-    for (int r = 0; r < kc; ++r) {
-        unsigned long long best = 0ull;
-        for (int m = lane; m < Np; m += 32) {
-            const unsigned long long k = sort_key(sh[m], m);
-            if (k < last && k > best) best = k;
-        }
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) best = umax64(best, __shfl_xor_sync(0xffffffffu, best, off));
-        if (lane == r) mine = best;
-        last = best;
-    }
-    return mine;
-}
-
-// One CTA per unit, warp hh per query head (hh < g): the ordered best kc
-// parents, their pages into the union bitmask, then the ascending list.
-__global__ void __launch_bounds__(32 * BQ) k_select_topk(
-    int g, int np_cap, int page_cap, int k_pages, int kc, const int32_t *__restrict__ n_parents,
-    const int32_t *__restrict__ n_pages, const float *__restrict__ scores, const float *__restrict__ gmax,
-    const int32_t *__restrict__ parent_first_page, const int32_t *__restrict__ parent_last_page,
-    const int32_t *__restrict__ parent_n_pages, const int32_t *__restrict__ page_next,
-    int32_t *__restrict__ sel_pages, int32_t *__restrict__ sel_count, int max_sel, int32_t *__restrict__ err) {
-    extern __shared__ unsigned s_mask[];
-    __shared__ unsigned long long s_cand[BQ][kCand];
-    __shared__ int s_wsum[BQ];
-    __shared__ int s_carry;
-    const int u = blockIdx.x;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nt = blockDim.x;
-    const int Np = min(n_parents[u], np_cap);
-    const size_t up = (size_t)u * np_cap, ug = (size_t)u * page_cap;
-    const int P = min(n_pages[u], page_cap);
-    const int words = (P + 31) / 32;
-    const int ngc = (np_cap + kGroup - 1) / kGroup, ng = (Np + kGroup - 1) / kGroup;
-    for (int x = tid; x < words; x += nt) s_mask[x] = 0u;
-    __syncthreads();
-    if (k_pages >= P) {
-        for (int x = tid; x < words; x += nt) {
-            const int rem = P - x * 32;
-            s_mask[x] = rem >= 32 ? 0xffffffffu : ((1u << rem) - 1u);
-        }
-    } else if (warp < g) {
-        const int hh = warp;
-        const float *sh = scores + ((size_t)u * g + hh) * np_cap;
-        const float *gh = gmax + ((size_t)u * g + hh) * ngc;
-        // T0: the kc-th largest group maximum, found bit by bit (MSB first) on
-        // the order-preserving integer form: the largest c with at least kc
-        // maxima >= c
-        float t0 = -INFINITY;
-        if (ng >= kc) {
-            uint32_t res = 0u;
-            for (int x0 = 0; x0 < ng; x0 += 8 * 32) {  // ng <= 256 in one pass; more: running bound
-                uint32_t v[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int x = x0 + e * 32 + lane;
-                    v[e] = x < ng ? ord_f32(__ldcg(gh + x)) : 0u;
-                }
-                // keep the bound of earlier stretches: count those >= c as present
-                const uint32_t prev = res;
-                uint32_t r = 0u;
-                for (int bit = 31; bit >= 0; --bit) {
-                    const uint32_t c = r | (1u << bit);
-                    unsigned cnt = 0;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) cnt += v[e] >= c;
-                    // the earlier stretches already hold kc keys >= prev
-                    const int n = (int)__reduce_add_sync(0xffffffffu, cnt) + (c <= prev ? kc : 0);
-                    if (n >= kc) r = c;
-                }
-                res = r;
-            }
-            t0 = unord_f32(res);
-        }
-        // keys with score >= T0, read only from groups whose maximum reaches it
-        unsigned long long *cand = s_cand[hh];
-        int *glist = reinterpret_cast<int *>(cand + kCand - 64);  // qualifying groups (tail of the buffer)
-        int cnt = 0;
-        for (int x0 = 0; x0 < ng; x0 += 8 * 32) {
-            float gm[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int x = x0 + i * 32 + lane;
-                gm[i] = x < ng ? __ldcg(gh + x) : -INFINITY;
-            }
-            // the qualifying groups of this stretch, in order, 8 groups' loads in flight at once
-            int ngl = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const unsigned b = __ballot_sync(0xffffffffu, gm[i] >= t0);
-                if (((b >> lane) & 1u) && ngl + __popc(b & lanemask_lt()) < 128)
-                    glist[ngl + __popc(b & lanemask_lt())] = x0 + i * 32 + lane;
-                ngl += __popc(b);
-            }
-            __syncwarp();
-            if (ngl > 128) {  // very many ties with T0: exact slow path below
-                cnt = kCand + 1;
-                break;
-            }
-            for (int j0 = 0; j0 < ngl; j0 += 8) {
-                float sv[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int m = j0 + i < ngl ? glist[j0 + i] * kGroup + lane : Np;
-                    sv[i] = m < Np ? __ldcg(sh + m) : -INFINITY;
-                }
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int m = j0 + i < ngl ? glist[j0 + i] * kGroup + lane : Np;
-                    const bool pass = m < Np && sv[i] >= t0;
-                    const unsigned bal = __ballot_sync(0xffffffffu, pass);
-                    const int at = cnt + __popc(bal & lanemask_lt());
-                    if (pass && at < kCand - 64) cand[at] = sort_key(sv[i], m);
-                    cnt += __popc(bal);
-                }
-            }
-            __syncwarp();
-        }
-        __syncwarp();
-        unsigned long long best;
-        if (cnt <= 64) {
-            unsigned long long w[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) w[e] = e * 32 + lane < cnt ? cand[e * 32 + lane] : 0ull;
-            warp_sort_desc<unsigned long long, 2>(w);
-            best = w[0];
-        } else if (cnt <= kCand - 64) {
-            unsigned long long w[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) w[e] = e * 32 + lane < cnt ? cand[e * 32 + lane] : 0ull;
-            warp_sort_desc<unsigned long long, 8>(w);
-            best = w[0];
-        } else {
-            best = best_slow(sh, Np, kc);
-        }
-        // take pages of the ordered parents until k pages
-        const unsigned long long k = lane < kc ? best : 0ull;
-        int pc = 0, fp = 0, contig = 1;
-        if (k != 0ull) {
-            const int pm = key_id(k);
-            fp = parent_first_page[up + pm];
-            pc = parent_n_pages[up + pm];
-            contig = parent_last_page[up + pm] - fp + 1 == pc;
-        }
-        int incl = pc;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int o = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += o;
-        }
-        const int tk = max(0, min(pc, k_pages - (incl - pc)));
-        int pg = fp;
-        for (int i = 0; i < tk; ++i) {
-            const int qq = contig ? fp + i : pg;
-            if (qq < 0 || qq >= P) break;
-            atomicOr(&s_mask[qq >> 5], 1u << (qq & 31));
-            if (!contig) pg = page_next[ug + qq];
-        }
-    }
-    __syncthreads();
-    // ascending list of the union's pages
-    if (tid == 0) s_carry = 0;
-    __syncthreads();
-    for (int w0 = 0; w0 < words; w0 += nt) {
-        const int x = w0 + tid;
-        const unsigned bits = x < words ? s_mask[x] : 0u;
-        const int c = __popc(bits);
-        int incl = c;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int o = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += o;
-        }
-        if (lane == 31) s_wsum[warp] = incl;
-        __syncthreads();
-        int pos = s_carry;
-        for (int w = 0; w < warp; ++w) pos += s_wsum[w];
-        pos += incl - c;
-        unsigned bb = bits;
-        while (bb) {
-            const int bit = __ffs(bb) - 1;
-            bb &= bb - 1;
-            if (pos < max_sel) sel_pages[(size_t)u * max_sel + pos] = x * 32 + bit;
-            ++pos;
-        }
-        __syncthreads();
-        if (tid == nt - 1) s_carry = pos;
-        __syncthreads();
-    }
-    const int total = s_carry;
-    for (int x = total + tid; x < max_sel; x += nt) sel_pages[(size_t)u * max_sel + x] = -1;
-    if (tid == 0) {
-        if (total > max_sel) set_err(err, ICE_ERR_CAPACITY);
-        sel_count[u] = min(total, max_sel);
-    }
+// One CTA per unit, NSW warps (warp hh < g takes query head hh).
+template <int NSW>
+__global__ void __launch_bounds__(32 * NSW) k_select_topk(const SelArgs A) {
+    extern __shared__ unsigned long long s_cand[];  // [NSW][kCand], then the union bitmask
+    __shared__ int s_wsum[NSW];
+    dep_trigger();  // the attention grid may be scheduled now; it waits for this one
+    dep_wait();     // the score table is complete
+    select_unit<NSW>(A, blockIdx.x, threadIdx.x, reinterpret_cast<unsigned *>(s_cand + NSW * kCand), s_cand, s_wsum);
 }
 
 }  // namespace
 
+static int gt_of(int g) { return g <= 1 ? 1 : g <= 2 ? 2 : g <= 4 ? 4 : g <= 8 ? 8 : 16; }
+// Warps of the selection CTA: one per query head, at least 4 (the page-list
+// scan wants >= 128 threads).
+static int nsw_of(int g) { return gt_of(g) < 4 ? 4 : gt_of(g); }
+// Shared memory of the selection CTA: candidate keys, then the union bitmask.
+static size_t topk_smem(int g, int page_cap) {
+    return (size_t)nsw_of(g) * kCand * 8 + sizeof(unsigned) * (size_t)((page_cap + 31) / 32);
+}
+
 bool select_tc_supported(const ice_params &p, int k_pages) {
     const int g = p.n_q_heads / p.n_kv_heads;
-    return p.dtype == ICE_BF16 && g >= 1 && g <= BQ && k_pages >= 1 && k_pages <= kMaxKc &&
-           sizeof(unsigned) * (size_t)((p.page_cap + 31) / 32) <= 160 * 1024;
+    return p.dtype == ICE_BF16 && g >= 1 && g <= BQ && k_pages >= 1 && k_pages <= kMaxKc && p.np_cap < (1 << 24) &&
+           topk_smem(g, p.page_cap) <= 227 * 1024;
 }
 
 // Score-table floats per unit: the scores, then the group maxima.
@@ -555,7 +632,7 @@ cudaError_t launch_select_tc(const ice_params &p, const ice_index &idx, const vo
         !make_map_bf16(&tmQ, Q, (unsigned long long)p.batch * p.n_q_heads, kHeadDim, 64, BQ,
                        CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorNotSupported;
-    const int gt = g <= 1 ? 1 : g <= 2 ? 2 : g <= 4 ? 4 : g <= 8 ? 8 : 16;
+    const int gt = gt_of(g);
     auto kern = gt == 1 ? k_score_tc<1> : gt == 2 ? k_score_tc<2> : gt == 4 ? k_score_tc<4> : gt == 8 ? k_score_tc<8>
                                                                                              : k_score_tc<16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
@@ -573,16 +650,34 @@ cudaError_t launch_select_tc(const ice_params &p, const ice_index &idx, const vo
     kern<<<grid, kThreads, kSmemBytes, s>>>(tmP, tmQ, U, g, p.n_q_heads, p.n_kv_heads, p.np_cap, T,
                                                   idx.n_parents, ws.scores, gmax, err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const size_t mask = sizeof(unsigned) * (size_t)((p.page_cap + 31) / 32);
-    if (mask > 48 * 1024) {
-        e = cudaFuncSetAttribute(k_select_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mask);
+
+    SelArgs A;
+    A.g = g;
+    A.np_cap = p.np_cap;
+    A.page_cap = p.page_cap;
+    A.k_pages = ws.k_pages;
+    A.kc = ws.k_pages;
+    A.max_sel = max_sel;
+    A.n_parents = idx.n_parents;
+    A.n_pages = idx.n_pages;
+    A.scores = ws.scores;
+    A.gmax = gmax;
+    A.parent_first_page = idx.parent_first_page;
+    A.parent_last_page = idx.parent_last_page;
+    A.parent_n_pages = idx.parent_n_pages;
+    A.page_next = idx.page_next;
+    A.sel_pages = sel_pages;
+    A.sel_count = sel_count;
+    A.err = err;
+    const int nsw = nsw_of(g);
+    auto topk = nsw == 4 ? k_select_topk<4> : nsw == 8 ? k_select_topk<8> : k_select_topk<16>;
+    const size_t smem = topk_smem(g, p.page_cap);
+    if (smem > 48 * 1024) {
+        e = cudaFuncSetAttribute(topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    const int threads = 32 * (g < 4 ? 4 : g);
-    k_select_topk<<<U, threads, mask, s>>>(g, p.np_cap, p.page_cap, ws.k_pages, ws.k_pages, idx.n_parents,
-                                           idx.n_pages, ws.scores, gmax, idx.parent_first_page, idx.parent_last_page,
-                                           idx.parent_n_pages, idx.page_next, sel_pages, sel_count, max_sel, err);
-    return cudaGetLastError();
+    e = launch_dependent(topk, dim3(U), dim3(32 * nsw), smem, s, A);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace ice
