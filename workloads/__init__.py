@@ -159,3 +159,49 @@ def batch_queries(w: Workload, layer: int = 0, step: int = 0) -> np.ndarray:
         for h in range(w.n_kv_heads):
             Q[b, h * g:(h + 1) * g] = unit_queries(w, layer, b, h, step)
     return Q
+
+
+# ------------------------------------------------------------------------------
+# Device-side draws of the same mixtures, for timing at full size (100k-token
+# contexts, batch 16), where drawing on the host takes tens of seconds.  Same
+# recipe as unit_kv / unit_queries (per-unit N(0, I) centres, spread noise,
+# log-normal norms when set, N(0, I) values), drawn from torch's generator on
+# the device instead of PCG64, so the values differ from the host draws; only
+# timing runs use them (parity runs use the host arrays above).
+def _torch_gen(w: Workload, layer: int, stream: int, device):
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(((w.seed * 1_000_003 + layer) * 1_000_003 + stream) & 0x7FFFFFFFFFFFFFFF)
+    return g
+
+
+def batch_kv_device(w: Workload, layer: int = 0, device="cuda"):
+    """K, V [B, Hkv, N, d] in the workload's storage dtype, drawn on `device`."""
+    import torch
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    B, H, N, d = w.batch, w.n_kv_heads, w.n_tokens, w.head_dim
+    g = _torch_gen(w, layer, 0, device)
+    C = torch.randn((B * H, w.centres, d), generator=g, device=device)
+    K = torch.empty((B * H, N, d), dtype=dt, device=device)
+    V = torch.empty((B * H, N, d), dtype=dt, device=device)
+    for u in range(B * H):  # one unit at a time keeps the fp32 temporaries small
+        lab = torch.randint(0, w.centres, (N,), generator=g, device=device)
+        k = C[u][lab] + w.spread * torch.randn((N, d), generator=g, device=device)
+        if w.lognormal_sigma > 0:
+            k *= torch.exp(w.lognormal_sigma * torch.randn((N, 1), generator=g, device=device))
+        K[u] = k.to(dt)
+        V[u] = torch.randn((N, d), generator=g, device=device).to(dt)
+    return K.view(B, H, N, d), V.view(B, H, N, d), C
+
+
+def batch_queries_device(w: Workload, centres, layer: int = 0, device="cuda"):
+    """Q [B, Hq, d]: query head h*g + i is a centre of KV head h's mixture
+    plus spread noise (centres as returned by batch_kv_device)."""
+    import torch
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    B, H, gq, d = w.batch, w.n_kv_heads, w.group, w.head_dim
+    g = _torch_gen(w, layer, 1, device)
+    lab = torch.randint(0, w.centres, (B * H, gq), generator=g, device=device)
+    q = torch.gather(centres, 1, lab[..., None].expand(-1, -1, d)) + \
+        w.spread * torch.randn((B * H, gq, d), generator=g, device=device)
+    return q.reshape(B, H * gq, d).to(dt)
