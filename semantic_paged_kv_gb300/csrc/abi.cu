@@ -420,6 +420,19 @@ ice_status ice_decode_step(const ice_params *p, const ice_index *idx, const void
         return cuda_status(launch_decode_cluster(*p, *idx, Q, w.k_pages, sel_pages, sel_count, max_sel, kbuf, vbuf,
                                                  buf_len, scale, O, err_dev, s),
                            "ice_decode_step");
+    // more units: the score table on the tensor cores, then attention CTAs that
+    // select their unit's pages themselves
+    if (select_tc_supported(*p, w.k_pages) && attention_mma_select_supported(*p, max_sel)) {
+        cudaError_t e = launch_score_tc(*p, *idx, Q, w, err_dev, s);
+        if (e == cudaSuccess) {
+            const SelArgs A = select_args(*p, *idx, w, sel_pages, sel_count, max_sel, err_dev);
+            e = launch_attention_mma_select(*p, *idx, A, Q, kbuf, vbuf, buf_len, max_sel, scale, O, w, err_dev, s);
+            if (e == cudaErrorNotSupported && (e = launch_topk(*p, A, s)) == cudaSuccess)  // scores are there
+                e = launch_attention(*p, idx, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, w, s,
+                                     err_dev);
+        }
+        if (e != cudaErrorNotSupported) return cuda_status(e, "ice_decode_step");
+    }
     if ((st = cuda_status(launch_select(*p, *idx, Q, w, sel_pages, sel_count, max_sel, err_dev, s), "ice_decode_step select")))
         return st;
     return cuda_status(

@@ -32,6 +32,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "select_unit.cuh"
 #include "tc_common.cuh"
 
 namespace ice {
@@ -51,6 +52,7 @@ struct SmemM {
     float wgt[kMW][16];
     float cml[16][2];
     unsigned long long full[kMW][2];
+    int wsum[kMW];
     int last;
 };
 
@@ -86,14 +88,15 @@ __device__ __forceinline__ uint32_t sw_addr(uint32_t tile, int row, int cc) {
     return tile + (uint32_t)((cc >> 3) * kHalfBytes + row * 128 + (((cc & 7) ^ (row & 7)) << 4));
 }
 
-template <bool kFused, int HR>
+template <bool kFused, int HR, bool kSel>
 __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
     const __grid_constant__ CUtensorMap tm_kb, const __grid_constant__ CUtensorMap tm_vb,
     const __nv_bfloat16 *__restrict__ Q, int g, int n_q_heads, int n_kv_heads, const int32_t *__restrict__ page_len,
     int page_cap, const int32_t *__restrict__ sel_pages, int32_t *__restrict__ buf_len,
     const int32_t *__restrict__ sel_count, int max_sel, float scale, int n_splits, float *__restrict__ part_ml,
-    float *__restrict__ part_o, int32_t *__restrict__ ticket, float *__restrict__ O, int32_t *__restrict__ err) {
+    float *__restrict__ part_o, int32_t *__restrict__ ticket, float *__restrict__ O, int32_t *__restrict__ err,
+    const SelArgs SA) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     // the swizzled page tiles want 1024-byte alignment
     SmemM &S = *reinterpret_cast<SmemM *>(smem_raw + ((1024u - (su32(smem_raw) & 1023u)) & 1023u));
@@ -107,9 +110,21 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
         S.ml[warp][lane][0] = -INFINITY;
         S.ml[warp][lane][1] = 0.f;
     }
-    dep_wait();  // the selected pages (and the contiguous buffer) are complete
+    dep_wait();  // the selected pages, or the score table (kSel), are complete
 
-    const int n = min(sel_count[u], max_sel);
+    // kSel: the CTA selects its unit's pages itself, in the slot area; split 0
+    // also writes them out (sel_pages, sel_count)
+    int n;
+    const int *s_list = nullptr;
+    if (kSel) {
+        unsigned long long *s_cand = reinterpret_cast<unsigned long long *>(&S.kv[0][0][0]);
+        unsigned *s_mask = reinterpret_cast<unsigned *>(s_cand + kMW * sel::kCand);
+        int *lst = reinterpret_cast<int *>(s_mask + (page_cap + 31) / 32);
+        n = sel::select_unit<kMW>(SA, u, tid, s_mask, s_cand, S.wsum, lst, split == 0);
+        s_list = lst;
+    } else {
+        n = min(sel_count[u], max_sel);
+    }
     const int ps = (max_sel + n_splits - 1) / n_splits;
     const int xs = split * ps;
     const int xe = min(n, xs + ps);
@@ -125,7 +140,7 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
     if (lane < nk) {
         const size_t sl = ubase + xs + warp + lane * kMW;
         if (kFused) {
-            my_pid = sel_pages[sl];
+            my_pid = kSel ? s_list[xs + warp + lane * kMW] : sel_pages[sl];
             my_len = page_len[(size_t)u * page_cap + my_pid];
         } else {
             my_len = buf_len[sl];
@@ -142,6 +157,7 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
         tma_load_2d(slot + kTileBytes, &tm_v, bar, 0, row);
         tma_load_2d(slot + kTileBytes + kHalfBytes, &tm_v, bar, 64, row);
     };
+    if (kSel) __syncthreads();  // every warp has its page ids before the slots fill
     {
         const int p0 = __shfl_sync(0xffffffffu, my_pid, 0), p1 = __shfl_sync(0xffffffffu, my_pid, 1);
         if (lane == 0) {
@@ -359,10 +375,21 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
     if (tid == 0) ticket[u] = 0;
 }
 
-template <bool F, int HR>
+int sm_count_cached() {
+    static int n_sm = 0;
+    if (!n_sm) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+        if (n_sm <= 0) n_sm = 1;
+    }
+    return n_sm;
+}
+
+template <bool F, int HR, bool kSel>
 cudaError_t launch_hr(const ice_params &p, const ice_index *pool, const int32_t *sel_pages, const void *Q, void *kbuf,
                       void *vbuf, int32_t *buf_len, const int32_t *sel_count, int max_sel, float scale, float *O,
-                      const DecodeWs &ws, int32_t *err, cudaStream_t s, int n_splits) {
+                      const DecodeWs &ws, int32_t *err, cudaStream_t s, int n_splits, const SelArgs &SA) {
     const int U = units_of(p);
     const int g = p.n_q_heads / p.n_kv_heads;
     CUtensorMap tk, tv, tkb, tvb;
@@ -383,17 +410,42 @@ cudaError_t launch_hr(const ice_params &p, const ice_index *pool, const int32_t 
     const size_t merge = sizeof(float) * (size_t)(n_splits * g + g);
     const size_t need = (sizeof(SmemM) > merge ? sizeof(SmemM) : merge) + 1024;  // + alignment slack
     if (need > 227 * 1024) return cudaErrorNotSupported;
-    cudaError_t e = cudaFuncSetAttribute(k_attn_mma<F, HR>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)need);
+    cudaError_t e = cudaFuncSetAttribute(k_attn_mma<F, HR, kSel>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)need);
     if (e != cudaSuccess) return e;
     const __nv_bfloat16 *Qb = static_cast<const __nv_bfloat16 *>(Q);
     const int32_t *plen = pool ? pool->page_len : nullptr;
-    e = launch_dependent(k_attn_mma<F, HR>, dim3(n_splits, U), dim3(kMT), need, s, tk, tv, tkb, tvb, Qb, g,
+    e = launch_dependent(k_attn_mma<F, HR, kSel>, dim3(n_splits, U), dim3(kMT), need, s, tk, tv, tkb, tvb, Qb, g,
                          p.n_q_heads, p.n_kv_heads, plen, p.page_cap, sel_pages, buf_len, sel_count, max_sel, scale,
-                         n_splits, ws.part_ml, ws.part_o, ws.attn_ticket, O, err);
+                         n_splits, ws.part_ml, ws.part_o, ws.attn_ticket, O, err, SA);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
+
+// The selection runs in the attention CTAs: one warp per query head (g <= 12),
+// candidate keys, union bitmask and page list in the 192 KB slot area.
+bool attention_mma_select_supported(const ice_params &p, int max_sel) {
+    const int g = p.n_q_heads / p.n_kv_heads;
+    const size_t need = (size_t)kMW * sel::kCand * 8 + 4 * (size_t)((p.page_cap + 31) / 32) + 4 * (size_t)max_sel;
+    return attention_mma_supported(p) && g <= kMW && need <= sizeof(SmemM::kv);
+}
+
+cudaError_t launch_attention_mma_select(const ice_params &p, const ice_index &idx, const SelArgs &A, const void *Q,
+                                        void *kbuf, void *vbuf, int32_t *buf_len, int max_sel, float scale, float *O,
+                                        const DecodeWs &ws, int32_t *err, cudaStream_t s) {
+    const int U = units_of(p);
+    const int g = p.n_q_heads / p.n_kv_heads;
+    int splits = sm_count_cached() / U;
+    const int most = (max_sel + kMW - 1) / kMW;
+    splits = splits < 1 ? 1 : (splits > most ? most : splits);
+    const int per_warp = (ceil_div(max_sel, splits) + kMW - 1) / kMW;
+    if (splits > ws.n_splits || per_warp > 32 || ((uintptr_t)Q & 3u) != 0) return cudaErrorNotSupported;
+    if (g <= 8)
+        return launch_hr<true, 1, true>(p, &idx, A.sel_pages, Q, kbuf, vbuf, buf_len, A.sel_count, max_sel, scale, O,
+                                        ws, err, s, splits, A);
+    return launch_hr<true, 2, true>(p, &idx, A.sel_pages, Q, kbuf, vbuf, buf_len, A.sel_count, max_sel, scale, O, ws,
+                                    err, s, splits, A);
+}
 
 bool attention_mma_supported(const ice_params &p) {
     const int g = p.n_q_heads / p.n_kv_heads;
@@ -407,24 +459,17 @@ cudaError_t launch_attention_mma(const ice_params &p, const ice_index *pool, con
                                  float scale, float *O, const DecodeWs &ws, int32_t *err, cudaStream_t s) {
     const int U = units_of(p);
     const int g = p.n_q_heads / p.n_kv_heads;
-    static int n_sm = 0;
-    if (!n_sm) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-        if (n_sm <= 0) n_sm = 1;
-    }
-    int splits = n_sm / U;
+    int splits = sm_count_cached() / U;
     const int most = (max_sel + kMW - 1) / kMW;
     splits = splits < 1 ? 1 : (splits > most ? most : splits);
     const int per_warp = (ceil_div(max_sel, splits) + kMW - 1) / kMW;
     if (splits > ws.n_splits || per_warp > 32) return cudaErrorNotSupported;
     if (pool) {
-        if (g <= 8) return launch_hr<true, 1>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s, splits);
-        return launch_hr<true, 2>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s, splits);
+        if (g <= 8) return launch_hr<true, 1, false>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s, splits, SelArgs{});
+        return launch_hr<true, 2, false>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s, splits, SelArgs{});
     }
-    if (g <= 8) return launch_hr<false, 1>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s, splits);
-    return launch_hr<false, 2>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s, splits);
+    if (g <= 8) return launch_hr<false, 1, false>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s, splits, SelArgs{});
+    return launch_hr<false, 2, false>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s, splits, SelArgs{});
 }
 
 }  // namespace ice

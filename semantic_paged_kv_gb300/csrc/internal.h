@@ -47,6 +47,16 @@ struct DecodeWs {
     int n_chunks, k_pages, n_splits;
     size_t bytes;
 };
+// What the page selection of a unit reads and writes (score table, group
+// maxima, page spans; the ascending page list per unit).
+struct SelArgs {
+    int g, np_cap, page_cap, k_pages, kc, max_sel;
+    const int32_t *n_parents, *n_pages;
+    const float *scores, *gmax;
+    const int32_t *parent_first_page, *parent_last_page, *parent_n_pages, *page_next;
+    int32_t *sel_pages, *sel_count, *err;
+};
+
 // with_select = false: the attention part only (no selection scratch).
 DecodeWs decode_ws_layout(const ice_params &p, int budget_tokens, int max_sel, void *base, bool with_select = true);
 
@@ -78,6 +88,12 @@ bool select_tc_supported(const ice_params &p, int k_pages);
 size_t select_tc_scores(const ice_params &p);
 cudaError_t launch_select_tc(const ice_params &p, const ice_index &idx, const void *Q, const DecodeWs &ws,
                              int32_t *sel_pages, int32_t *sel_count, int max_sel, int32_t *err, cudaStream_t s);
+SelArgs select_args(const ice_params &p, const ice_index &idx, const DecodeWs &ws, int32_t *sel_pages,
+                    int32_t *sel_count, int max_sel, int32_t *err);
+cudaError_t launch_score_tc(const ice_params &p, const ice_index &idx, const void *Q, const DecodeWs &ws,
+                            int32_t *err, cudaStream_t s);
+cudaError_t launch_topk(const ice_params &p, const SelArgs &A, cudaStream_t s);
+
 cudaError_t launch_gather(const ice_params &p, const ice_index &idx, const int32_t *sel_pages,
                           const int32_t *sel_count, int max_sel, void *kbuf, void *vbuf, int32_t *buf_len,
                           cudaStream_t s);
@@ -90,6 +106,10 @@ cudaError_t launch_attention(const ice_params &p, const ice_index *pool, const i
                              int32_t *err = nullptr);
 // The same with the page contractions on warp-level MMAs (bf16, g <= 16).
 bool attention_mma_supported(const ice_params &p);
+bool attention_mma_select_supported(const ice_params &p, int max_sel);
+cudaError_t launch_attention_mma_select(const ice_params &p, const ice_index &idx, const SelArgs &A, const void *Q,
+                                        void *kbuf, void *vbuf, int32_t *buf_len, int max_sel, float scale, float *O,
+                                        const DecodeWs &ws, int32_t *err, cudaStream_t s);
 cudaError_t launch_attention_mma(const ice_params &p, const ice_index *pool, const int32_t *sel_pages, const void *Q,
                                  void *kbuf, void *vbuf, int32_t *buf_len, const int32_t *sel_count, int max_sel,
                                  float scale, float *O, const DecodeWs &ws, int32_t *err, cudaStream_t s);
