@@ -93,6 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap tmK2, const __grid_constant__ CUtensorMap tmP2, int N, int np_cap,
                 int n_cap, int n_items, int mt_per_unit, const int32_t *__restrict__ n_parents,
                 int32_t *__restrict__ token_parent, int32_t *__restrict__ err) {
+    dep_wait();  // the previous kernel of the stream is complete (launched as its dependent)
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     unsigned char *sA = smem;                         // two key buffers
@@ -323,8 +324,12 @@ cudaError_t launch_assign_tc(const ice_params &p, const void *K, const ice_index
     const int mt = ceil_div(p.n_tokens, BM);
     const int items = mt * U;
     const int grid = items < n_sm ? items : n_sm;
-    k_assign_tc<<<grid, kThreads, kSmemBytes, s>>>(tmK, tmP, tmK2, tmP2, p.n_tokens, p.np_cap, p.n_cap, items, mt,
-                                                   idx.n_parents, idx.token_parent, err);
+    {
+        const cudaError_t e_ = launch_dependent(k_assign_tc, dim3(grid), dim3(kThreads), kSmemBytes, s, tmK, tmP,
+                                                tmK2, tmP2, p.n_tokens, p.np_cap, p.n_cap, items, mt, idx.n_parents,
+                                                idx.token_parent, err);
+        if (e_ != cudaSuccess) return e_;
+    }
     return cudaGetLastError();
 }
 

@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_lift_count(const T *__restrict_
                                                          double *__restrict__ norm2, int32_t *__restrict__ pcount,
                                                          double *__restrict__ tile_max,
                                                          unsigned long long *__restrict__ tile_min, int n_tiles) {
+    dep_wait();  // the previous kernel of the stream is complete (launched as its dependent)
     const int u = blockIdx.y, tile = blockIdx.x;
     const int seq = u / n_kv_heads, head = u % n_kv_heads;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -66,18 +67,40 @@ __global__ void __launch_bounds__(kThreads, 3) k_lift_count(const T *__restrict_
 #pragma unroll
     for (int s = 0; s < STEPS; ++s) {
         float hi = 0.f, lo = 0.f;
+        if constexpr (sizeof(T) == 2) {
+            // bf16: every square is exact in fp32; two double-float sums (even
+            // and odd elements) on packed pairs, joined at the end
+            unsigned long long hi2 = 0ull, lo2 = 0ull;
 #pragma unroll
-        for (int v = 0; v < VPL; ++v) {
-            float f[Elem<T>::kPerVec];
-            Elem<T>::unpack(buf[s][v], f);
+            for (int v = 0; v < VPL; ++v) {
+                const uint32_t w[4] = {buf[s][v].x, buf[s][v].y, buf[s][v].z, buf[s][v].w};
 #pragma unroll
-            for (int i = 0; i < Elem<T>::kPerVec; ++i) {
-                const float t = f[i] * f[i];
-                const float te = fmaf(f[i], f[i], -t);  // 0 for bf16 inputs
-                float sum, err;
-                two_sum(hi, t, sum, err);
-                hi = sum;
-                lo += err + te;
+                for (int i = 0; i < 4; ++i) {
+                    const unsigned long long f2 = bf2_pair(w[i]);
+                    unsigned long long s2, e2;
+                    two_sum2(hi2, mul2(f2, f2), s2, e2);
+                    hi2 = s2;
+                    lo2 = add2(lo2, e2);
+                }
+            }
+            const float2 h = upk2(hi2), l = upk2(lo2);
+            float err;
+            two_sum(h.x, h.y, hi, err);
+            lo = (l.x + l.y) + err;
+        } else {
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) {
+                float f[Elem<T>::kPerVec];
+                Elem<T>::unpack(buf[s][v], f);
+#pragma unroll
+                for (int i = 0; i < Elem<T>::kPerVec; ++i) {
+                    const float t = f[i] * f[i];
+                    const float te = fmaf(f[i], f[i], -t);  // the square's rounding error
+                    float sum, err;
+                    two_sum(hi, t, sum, err);
+                    hi = sum;
+                    lo += err + te;
+                }
             }
         }
 #pragma unroll
@@ -153,6 +176,7 @@ __global__ void __launch_bounds__(kThreads) k_promote_write(
     int32_t *__restrict__ n_indexed, int32_t *__restrict__ parent_tok, T *__restrict__ parent_keys,
     float *__restrict__ parent_e, float *__restrict__ parent_corr, int32_t *__restrict__ token_parent,
     uint4 *__restrict__ a_extra, uint4 *__restrict__ b_extra, int32_t *__restrict__ err) {
+    dep_wait();  // the previous kernel of the stream is complete (launched as its dependent)
     const int u = blockIdx.y, tile = blockIdx.x;
     const int seq = u / n_kv_heads, head = u % n_kv_heads;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -164,6 +188,11 @@ __global__ void __launch_bounds__(kThreads) k_promote_write(
     __shared__ int s_warp[kWarps];
     __shared__ int s_list_tok[kLiftTile];
     __shared__ int s_list_m[kLiftTile];
+    // this thread's token: its squared norm and promotion draw do not depend
+    // on the unit's totals, so their loads overlap the reduction below
+    const long long j = t0 + threadIdx.x;
+    const double n2 = j < N ? norm2[(size_t)u * N + j] : 0.0;
+    const bool drawn = j < N && (uint64_t)promote_draw(key, seq, head, (uint32_t)j, 1u) < thresh;
     // the unit's tile values: counts before this tile and in all, M^2, smallest draw
     int before = 0, all = 0;
     double mx = 0.0;
@@ -212,9 +241,7 @@ __global__ void __launch_bounds__(kThreads) k_promote_write(
         m2[u] = M2;
     }
 
-    const long long j = t0 + threadIdx.x;
-    const bool f = (j < N) && (fallback ? (j == jmin)
-                                        : ((uint64_t)promote_draw(key, seq, head, (uint32_t)j, 1u) < thresh));
+    const bool f = (j < N) && (fallback ? (j == jmin) : drawn);
     const unsigned bal = __ballot_sync(0xffffffffu, f);
     if (lane == 0) s_warp[warp] = __popc(bal);
     __syncthreads();
@@ -227,7 +254,7 @@ __global__ void __launch_bounds__(kThreads) k_promote_write(
         // M^2 - |k|^2 is exact in fp64 to ~2^-52 M^2; rounded to fp32, its
         // square root is within 1.5 ulp of the exact e (fp32 sqrt: the fp64
         // units are few on this part)
-        const double r = M2 - norm2[(size_t)u * N + j];
+        const double r = M2 - n2;
         const float e = sqrtf(r > 0.0 ? (float)r : 0.f);
         // e as three bf16 parts e1 + e2 + e3 (24 significant bits, each
         // remainder exact in fp32): the extra K columns of the tensor-core
@@ -285,13 +312,22 @@ cudaError_t launch_lift_promote_t(const ice_params &p, const void *K, const ice_
     const int tiles = ceil_div(N, kLiftTile);
     const uint64_t key = promote_key(p.seed, p.layer);
     dim3 grid(tiles, U);
-    k_lift_count<T><<<grid, kThreads, 0, s>>>(static_cast<const T *>(K), N, p.n_kv_heads, p.promote_thresh, key,
-                                              ws.norm2, ws.pcount, ws.tile_max, ws.tile_min, tiles);
-    k_promote_write<T><<<grid, kThreads, 0, s>>>(
-        static_cast<const T *>(K), N, p.n_kv_heads, p.promote_thresh, key, p.np_cap, p.n_cap, idx.m2, ws.norm2,
-        ws.pcount, ws.tile_max, ws.tile_min, tiles, idx.n_parents, idx.n_indexed, idx.parent_tok,
-        static_cast<T *>(idx.parent_keys), idx.parent_e, idx.parent_corr, idx.token_parent,
-        p.dtype == ICE_BF16 ? ws.a_extra : nullptr, p.dtype == ICE_BF16 ? ws.b_extra : nullptr, err);
+    {
+        const cudaError_t e_ = launch_dependent(k_lift_count<T>, dim3(grid), dim3(kThreads), 0, s,
+                                                static_cast<const T *>(K), N, p.n_kv_heads, p.promote_thresh, key,
+                                                ws.norm2, ws.pcount, ws.tile_max, ws.tile_min, tiles);
+        if (e_ != cudaSuccess) return e_;
+    }
+    {
+        const cudaError_t e_ = launch_dependent(k_promote_write<T>, dim3(grid), dim3(kThreads), 0, s,
+                                                static_cast<const T *>(K), N, p.n_kv_heads, p.promote_thresh, key,
+                                                p.np_cap, p.n_cap, idx.m2, ws.norm2, ws.pcount, ws.tile_max,
+                                                ws.tile_min, tiles, idx.n_parents, idx.n_indexed, idx.parent_tok,
+                                                static_cast<T *>(idx.parent_keys), idx.parent_e, idx.parent_corr,
+                                                idx.token_parent, p.dtype == ICE_BF16 ? ws.a_extra : nullptr,
+                                                p.dtype == ICE_BF16 ? ws.b_extra : nullptr, err);
+        if (e_ != cudaSuccess) return e_;
+    }
     return cudaGetLastError();
 }
 

@@ -337,6 +337,7 @@ __global__ void __cluster_dims__(kPackCluster, 1, 1) __launch_bounds__(kPCThread
                    int32_t *__restrict__ page_len, int32_t *__restrict__ page_next,
                    int32_t *__restrict__ page_tokens, int32_t *__restrict__ token_page,
                    int32_t *__restrict__ token_slot, int32_t *__restrict__ err) {
+    dep_wait();  // the previous kernel of the stream is complete (launched as its dependent)
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
     extern __shared__ __align__(16) unsigned char s_raw[];
@@ -494,6 +495,7 @@ __global__ void __launch_bounds__(kThreads) k_pack_copy(const T *__restrict__ K,
                                                         const int32_t *__restrict__ page_len,
                                                         const int32_t *__restrict__ page_tokens,
                                                         T *__restrict__ pool_k, T *__restrict__ pool_v) {
+    dep_wait();  // the previous kernel of the stream is complete (launched as its dependent)
     constexpr int RV = row_vecs<T>();         // 16-byte vectors per row
     constexpr int PER_LANE = kPage * RV / 32;  // vectors per lane per page (8 bf16, 16 fp32)
     const int u = blockIdx.y;
@@ -536,17 +538,26 @@ cudaError_t launch_t(const ice_params &p, const void *K, const void *V, const ic
                 cudaFuncSetAttribute(k_pack_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pcs.smem);
             if (e != cudaSuccess) return e;
         }
-        k_pack_cluster<<<dim3(kPackCluster, U), kPCThreads, pcs.smem, s>>>(
-            p.n_tokens, p.n_cap, p.np_cap, p.page_cap, pcs.tc, pcs.tw, pcs.sc, idx.n_parents, idx.token_parent,
-            ws.pack_total, idx.n_pages, idx.parent_first_page, idx.parent_last_page, idx.parent_n_pages,
-            idx.page_parent, idx.page_len, idx.page_next, idx.page_tokens, idx.token_page, idx.token_slot, err);
+        {
+            const cudaError_t e_ = launch_dependent(k_pack_cluster, dim3(kPackCluster, U), dim3(kPCThreads), pcs.smem,
+                                                    s, p.n_tokens, p.n_cap, p.np_cap, p.page_cap, pcs.tc, pcs.tw,
+                                                    pcs.sc, idx.n_parents, idx.token_parent, ws.pack_total,
+                                                    idx.n_pages, idx.parent_first_page, idx.parent_last_page,
+                                                    idx.parent_n_pages, idx.page_parent, idx.page_len, idx.page_next,
+                                                    idx.page_tokens, idx.token_page, idx.token_slot, err);
+            if (e_ != cudaSuccess) return e_;
+        }
     } else {
         launch_rank_tiles(p, idx, ws, err, s);
     }
     dim3 cgrid(ceil_div(p.page_cap, kThreads / 32), U);
-    k_pack_copy<T><<<cgrid, kThreads, 0, s>>>(static_cast<const T *>(K), static_cast<const T *>(V), p.n_tokens,
-                                              p.page_cap, idx.n_pages, idx.page_len, idx.page_tokens,
-                                              static_cast<T *>(idx.pool_k), static_cast<T *>(idx.pool_v));
+    {
+        const cudaError_t e_ = launch_dependent(k_pack_copy<T>, dim3(cgrid), dim3(kThreads), 0, s,
+                                                static_cast<const T *>(K), static_cast<const T *>(V), p.n_tokens,
+                                                p.page_cap, idx.n_pages, idx.page_len, idx.page_tokens,
+                                                static_cast<T *>(idx.pool_k), static_cast<T *>(idx.pool_v));
+        if (e_ != cudaSuccess) return e_;
+    }
     return cudaGetLastError();
 }
 

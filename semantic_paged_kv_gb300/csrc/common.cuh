@@ -84,12 +84,57 @@ __device__ __forceinline__ uint32_t promote_draw(uint64_t key, int32_t seq, int3
     return (uint32_t)(sm64_output(key, ctr + 1ull) >> 32);
 }
 
+// ----------------------------------------------------- packed fp32 pairs --
+// Two IEEE fp32 values in one 64-bit register; add / sub / mul / fma.rn.f32x2
+// each do two correctly rounded fp32 operations in one instruction.
+__device__ __forceinline__ unsigned long long pk2(float x, float y) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+    return r;
+}
+__device__ __forceinline__ float2 upk2(unsigned long long r) {
+    float2 f;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(r));
+    return f;
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long sub2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// bf16 pair in one 32-bit word -> fp32 pair
+__device__ __forceinline__ unsigned long long bf2_pair(uint32_t w) {
+    return pk2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
 // ------------------------------------------------- double-float summation --
 // Error-free transformation of a + b (Knuth's two-sum).
 __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
     s = a + b;
     const float bb = s - a;
     e = (a - (s - bb)) + (b - bb);
+}
+// The same on two independent pairs at once.
+__device__ __forceinline__ void two_sum2(unsigned long long a, unsigned long long b, unsigned long long &s,
+                                         unsigned long long &e) {
+    s = add2(a, b);
+    const unsigned long long bb = sub2(s, a);
+    e = add2(sub2(a, sub2(s, bb)), sub2(b, bb));
 }
 
 // ------------------------------------------------------------ warp utils --
@@ -106,13 +151,14 @@ __device__ __forceinline__ bool better(float sa, int ia, float sb, int ib) {
 }
 
 // ------------------------------------------- programmatic dependent launch --
-// A kernel launched with launch_dependent() may become resident while the
-// previous kernel of the stream still runs; it calls dep_wait() before it
-// reads anything that kernel writes (returns once that grid has completed
-// and its writes are visible; a no-op for a plain launch).  dep_trigger()
-// lets the next such kernel be scheduled before this one ends.
+// A kernel launched with launch_dependent() is scheduled as the CTAs of the
+// previous kernel of the stream exit, without waiting for the whole launch to
+// retire; it calls dep_wait() before it touches global memory (returns once
+// that grid has completed and its writes are visible; a no-op for a plain
+// launch).  No kernel here signals its dependents early: measured on the
+// build + decode step, dependents scheduled at the start of their predecessor
+// sat on the SMs it was still using and cost ~20 us per step.
 __device__ __forceinline__ void dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void dep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,

@@ -50,26 +50,6 @@ struct Smem {
     int last;
 };
 
-// Packed fp32 pairs (fma.rn.f32x2: two IEEE fp32 FMAs per instruction).
-__device__ __forceinline__ unsigned long long pk2(float x, float y) {
-    unsigned long long r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
-    return r;
-}
-__device__ __forceinline__ float2 upk2(unsigned long long r) {
-    float2 f;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(r));
-    return f;
-}
-__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c) {
-    unsigned long long d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-// bf16 pair in one 32-bit word -> fp32 pair
-__device__ __forceinline__ unsigned long long bf2_pair(uint32_t w) {
-    return pk2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-}
 
 template <bool kFused, int GT, int HS>
 __global__ void __launch_bounds__(kThreads, (GT / HS) >= 8 ? 2 : 3) k_attn_stream(

@@ -51,25 +51,6 @@ constexpr uint32_t kPageBytes = kPageElems * 2;
 constexpr int kCand = 64;    // keys a selection warp collects
 constexpr int kMaxPPC = 16;  // pages of the union per CTA
 
-// Packed fp32 pairs (fma.rn.f32x2: two IEEE fp32 FMAs per instruction).
-__device__ __forceinline__ unsigned long long pk2(float x, float y) {
-    unsigned long long r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
-    return r;
-}
-__device__ __forceinline__ float2 upk2(unsigned long long r) {
-    float2 f;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(r));
-    return f;
-}
-__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c) {
-    unsigned long long d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ unsigned long long bf2_pair(uint32_t w) {
-    return pk2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-}
 
 // Shared-memory layout (byte offsets, 128-byte aligned pieces).
 struct Lay {
@@ -109,6 +90,7 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT) k_decode_cluste
     const __nv_bfloat16 *__restrict__ pool_k, const __nv_bfloat16 *__restrict__ pool_v, int32_t *__restrict__ sel_pages,
     int32_t *__restrict__ sel_count, int max_sel, __nv_bfloat16 *__restrict__ kbuf, __nv_bfloat16 *__restrict__ vbuf,
     int32_t *__restrict__ buf_len, float scale, float *__restrict__ O, int32_t *__restrict__ err) {
+    dep_wait();  // the previous kernel of the stream is complete (launched as its dependent)
     cg::cluster_group cluster = cg::this_cluster();
     const int r = (int)cluster.block_rank();
     const int u = blockIdx.y;
@@ -587,13 +569,19 @@ cudaError_t launch_gt(const ice_params &p, const ice_index &idx, const void *Q, 
         if (e != cudaSuccess) return e;
     }
     const int g = p.n_q_heads / p.n_kv_heads;
-    k_decode_cluster2<GT><<<dim3(kC, units_of(p)), kT, sh.smem, s>>>(
-        static_cast<const __nv_bfloat16 *>(Q), g, p.n_q_heads, p.n_kv_heads, p.np_cap, p.page_cap, k_pages, sh.chunk,
-        sh.ppc, idx.n_parents, idx.n_pages, static_cast<const __nv_bfloat16 *>(idx.parent_keys), idx.parent_first_page,
-        idx.parent_last_page, idx.parent_n_pages, idx.page_next, idx.page_len,
-        static_cast<const __nv_bfloat16 *>(idx.pool_k), static_cast<const __nv_bfloat16 *>(idx.pool_v), sel_pages,
-        sel_count, max_sel, static_cast<__nv_bfloat16 *>(kbuf), static_cast<__nv_bfloat16 *>(vbuf), buf_len, scale, O,
-        err);
+    {
+        const cudaError_t e_ = launch_dependent(k_decode_cluster2<GT>, dim3(kC, units_of(p)), dim3(kT), sh.smem, s,
+                                                static_cast<const __nv_bfloat16 *>(Q), g, p.n_q_heads, p.n_kv_heads,
+                                                p.np_cap, p.page_cap, k_pages, sh.chunk, sh.ppc, idx.n_parents,
+                                                idx.n_pages, static_cast<const __nv_bfloat16 *>(idx.parent_keys),
+                                                idx.parent_first_page, idx.parent_last_page, idx.parent_n_pages,
+                                                idx.page_next, idx.page_len,
+                                                static_cast<const __nv_bfloat16 *>(idx.pool_k),
+                                                static_cast<const __nv_bfloat16 *>(idx.pool_v), sel_pages, sel_count,
+                                                max_sel, static_cast<__nv_bfloat16 *>(kbuf),
+                                                static_cast<__nv_bfloat16 *>(vbuf), buf_len, scale, O, err);
+        if (e_ != cudaSuccess) return e_;
+    }
     return cudaGetLastError();
 }
 

@@ -119,6 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     k_score_tc(const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmQ, int U, int g,
                int n_q_heads, int n_kv_heads, int np_cap, int T, const int32_t *__restrict__ n_parents,
                float *__restrict__ scores, float *__restrict__ gmax, int32_t *__restrict__ err) {
+    dep_wait();  // the previous kernel of the stream is complete (launched as its dependent)
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem =
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -150,7 +151,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_after();
     const uint32_t tmem = bars->tmem_base;
     bool ok = true;
-    dep_trigger();  // the selection grid may be scheduled now; it waits for this one
 
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer
@@ -280,8 +280,7 @@ template <int NSW>
 __global__ void __launch_bounds__(32 * NSW) k_select_topk(const SelArgs A) {
     extern __shared__ unsigned long long s_cand[];  // [NSW][kCand], then the union bitmask
     __shared__ int s_wsum[NSW];
-    dep_trigger();  // the attention grid may be scheduled now; it waits for this one
-    dep_wait();     // the score table is complete
+    dep_wait();  // the score table is complete
     select_unit<NSW>(A, blockIdx.x, threadIdx.x, reinterpret_cast<unsigned *>(s_cand + NSW * kCand), s_cand, s_wsum);
 }
 
@@ -359,8 +358,12 @@ cudaError_t launch_score_tc(const ice_params &p, const ice_index &idx, const voi
     const long long items = (long long)U * T;
     const int grid = items < n_sm ? (int)items : n_sm;
     float *gmax = ws.scores + (size_t)U * g * p.np_cap;
-    kern<<<grid, kThreads, kSmemBytes, s>>>(tmP, tmQ, U, g, p.n_q_heads, p.n_kv_heads, p.np_cap, T,
-                                                  idx.n_parents, ws.scores, gmax, err);
+    {
+        const cudaError_t e_ = launch_dependent(kern, dim3(grid), dim3(kThreads), kSmemBytes, s, tmP, tmQ, U, g,
+                                                p.n_q_heads, p.n_kv_heads, p.np_cap, T, idx.n_parents, ws.scores,
+                                                gmax, err);
+        if (e_ != cudaSuccess) return e_;
+    }
     return cudaGetLastError();
 }
 
