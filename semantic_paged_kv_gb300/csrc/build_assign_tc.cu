@@ -72,6 +72,15 @@ struct Bars {
     int comb_i[kEpiWarps / 4 - 1][BM];
     uint32_t tmem_base;
 };
+static_assert(kEpiCols == 64, "the epilogue's maximum tree is written for 64 columns");
+
+// max(a, b, c) in one instruction (no NaN reaches it: scores are finite or -inf).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 constexpr size_t kSmemBytes = 1024 /*align slack*/ + 2 * A_BYTES + NSTAGE * B_STAGE + 2 * A2_BYTES +
                               NSTAGE * B2_STAGE + sizeof(Bars);
 
@@ -243,9 +252,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (valid > 0) {
                     float cmax = -INFINITY;
                     if (valid >= kEpiCols) {
+                        // three-input maxima: 64 -> 22 -> 8 -> 3 -> 1
+                        float m1[22], m2[8];
 #pragma unroll
-                        for (int i = 0; i < kEpiCols; i += 4)
-                            cmax = fmaxf(cmax, fmaxf(fmaxf(v[i], v[i + 1]), fmaxf(v[i + 2], v[i + 3])));
+                        for (int i = 0; i < 21; ++i) m1[i] = fmax3(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+                        m1[21] = v[63];
+#pragma unroll
+                        for (int i = 0; i < 7; ++i) m2[i] = fmax3(m1[3 * i], m1[3 * i + 1], m1[3 * i + 2]);
+                        m2[7] = m1[21];
+                        cmax = fmax3(fmax3(m2[0], m2[1], m2[2]), fmax3(m2[3], m2[4], m2[5]), fmaxf(m2[6], m2[7]));
                     } else {
 #pragma unroll
                         for (int i = 0; i < kEpiCols; ++i) {
