@@ -67,8 +67,8 @@ FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 # source file at capture time; reported only while the source is unchanged.
 TRAFFIC = {
     # profiles/assign_tc_llama31_8b_16k.md
-    "assign": {"workload": "llama31_8b_16k", "source": "build_assign_tc.cu", "bytes": 40956160,
-               "sha256": "09e28c41332ceff8c275fa306ce55cd30151dd08335fdfea5b0e847ffa63d801"},
+    "assign": {"workload": "llama31_8b_16k", "source": "build_assign_tc.cu", "bytes": 40955904,
+               "sha256": "6bfded2608bcb66426c2df4f483ad31a169341ad9c03a4acd0191b59939134f5"},
 }
 
 
@@ -99,6 +99,12 @@ def parse():
     ap.add_argument("--cpu-units", type=int, default=None, help="units in the CPU-baseline sample")
     ap.add_argument("--no-at-scale", action="store_true",
                     help="skip the full-size decode and assignment timings (100k-token contexts)")
+    ap.add_argument("--at-scale-only", action="store_true",
+                    help="run only the full-size timings and print them as one JSON line (profiling runs)")
+    ap.add_argument("--at-scale-parts", default="qwen_decode,longchat_assign,longchat_decode",
+                    help="comma list of qwen_decode, longchat_assign, longchat_decode")
+    ap.add_argument("--at-scale-batch", type=int, default=None, help="sequences of the Qwen3-shaped batch (16)")
+    ap.add_argument("--at-scale-reps", type=int, default=30)
     return ap.parse_args()
 
 
@@ -256,7 +262,7 @@ def whole_job_rate(units_per_rank: int, per_unit: int, steps: int, world: int, m
 
 
 # ------------------------------------------------------------- our arm ----
-def at_scale(pk, reps: int = 30):
+def at_scale(pk, reps: int = 30, parts=("qwen_decode", "longchat_assign", "longchat_decode"), qwen_batch=None):
     """Full-size timings of the two parts the roofline targets are quoted on:
     the decode step (select + gather + sparse attention) of the Qwen3-32B-
     shaped batch (16 sequences x 8 KV heads, 100k tokens, budget 256) and of
@@ -327,27 +333,36 @@ def at_scale(pk, reps: int = 30):
            "timing": f"median of {reps} CUDA-graph replays, L2 flushed before each, CUDA events",
            "peak_source": pk["src"]}
     # Qwen3-32B shape: decode step
-    w = workloads.WORKLOADS["qwen3_32b_100k"]
-    cfg, p, K, V, Q, idx, ws, err = build(w)
-    del K, V, ws
-    out["decode_qwen3_32b_100k_b16"] = decode(cfg, p, Q, idx, err, max(w.budgets))
-    out["decode_qwen3_32b_100k_b16"]["status"] = ice.ice_status_string(ice.ice_check(err))
-    del cfg, p, Q, idx, err
-    torch.cuda.empty_cache()
+    if "qwen_decode" in parts:
+        w = workloads.WORKLOADS["qwen3_32b_100k"]
+        if qwen_batch:
+            w = w.scaled(batch=qwen_batch)
+        cfg, p, K, V, Q, idx, ws, err = build(w)
+        del K, V, ws
+        key = f"decode_qwen3_32b_100k_b{w.batch}"
+        out[key] = decode(cfg, p, Q, idx, err, max(w.budgets))
+        out[key]["status"] = ice.ice_status_string(ice.ice_check(err))
+        del cfg, p, Q, idx, err
+        torch.cuda.empty_cache()
     # LongChat-7B shape: the assignment contraction at 100k tokens, then decode
-    w = workloads.WORKLOADS["longchat_7b_100k"]
-    cfg, p, K, V, Q, idx, ws, err = build(w)
-    ms = timed(lambda: ice.ice_build_assign(p, K, idx, ws, err))
-    np_tot = int(idx.n_parents.sum())
-    flops = 2.0 * w.n_tokens * np_tot * 128
-    tf = flops / (ms * 1e-3) / 1e12
-    out["assign_longchat_7b_100k"] = {"us": 1000 * ms, "units": cfg.units, "tokens_per_unit": w.n_tokens,
-                                      "parents": np_tot, "flops": flops, "tflops": tf, "peak_tflops": pk["bf16"],
-                                      "frac": tf / pk["bf16"], "peak": "bf16 dense, measured burst"}
-    del K, V, ws
-    out["decode_longchat_7b_100k_b1"] = decode(cfg, p, Q, idx, err, max(w.budgets))
-    out["status"] = ice.ice_status_string(ice.ice_check(err))
-    del cfg, p, Q, idx, err, flush
+    if "longchat_assign" in parts or "longchat_decode" in parts:
+        w = workloads.WORKLOADS["longchat_7b_100k"]
+        cfg, p, K, V, Q, idx, ws, err = build(w)
+        if "longchat_assign" in parts:
+            ms = timed(lambda: ice.ice_build_assign(p, K, idx, ws, err))
+            np_tot = int(idx.n_parents.sum())
+            flops = 2.0 * w.n_tokens * np_tot * 128
+            tf = flops / (ms * 1e-3) / 1e12
+            out["assign_longchat_7b_100k"] = {"us": 1000 * ms, "units": cfg.units, "tokens_per_unit": w.n_tokens,
+                                              "parents": np_tot, "flops": flops, "tflops": tf,
+                                              "peak_tflops": pk["bf16"], "frac": tf / pk["bf16"],
+                                              "peak": "bf16 dense, measured burst"}
+        del K, V, ws
+        if "longchat_decode" in parts:
+            out["decode_longchat_7b_100k_b1"] = decode(cfg, p, Q, idx, err, max(w.budgets))
+        out["status"] = ice.ice_status_string(ice.ice_check(err))
+        del cfg, p, Q, idx, err
+    del flush
     torch.cuda.empty_cache()
     return out
 
@@ -536,7 +551,7 @@ def run_ours(args):
     scale_res = None
     if rank == 0 and not args.no_at_scale:
         try:
-            scale_res = at_scale(pk)
+            scale_res = at_scale(pk, args.at_scale_reps, args.at_scale_parts.split(","), args.at_scale_batch)
         except Exception as e:  # reported, the main line stands
             scale_res = {"error": f"{type(e).__name__}: {e}"}
     barrier()
@@ -581,6 +596,12 @@ def run_ours(args):
 
 def main():
     args = parse()
+    if args.at_scale_only:
+        import torch
+        torch.cuda.set_device(rank_info()[1])
+        print(json.dumps({"at_scale": at_scale(peaks(), args.at_scale_reps, args.at_scale_parts.split(","),
+                                                args.at_scale_batch)}))
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
