@@ -31,45 +31,37 @@ namespace {
 constexpr int kThreads = kLiftTile;  // one token per thread
 constexpr int kWarps = kThreads / 32;
 
+// Loads of the 32 rows [wt0, wt0 + 32) of a warp (rows >= N read as zero):
+// in step s, lane 4t + q holds the 16-byte vectors q, q + 4, ... of row
+// wt0 + 8s + t.
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 3) k_lift_count(const T *__restrict__ K, int N, int n_kv_heads,
-                                                         uint64_t thresh, uint64_t key,
-                                                         double *__restrict__ norm2, int32_t *__restrict__ pcount,
-                                                         double *__restrict__ tile_max,
-                                                         unsigned long long *__restrict__ tile_min, int n_tiles) {
-    dep_wait();  // the previous kernel of the stream is complete (launched as its dependent)
-    const int u = blockIdx.y, tile = blockIdx.x;
-    const int seq = u / n_kv_heads, head = u % n_kv_heads;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long t0 = (long long)tile * kLiftTile;
-    const T *Ku = K + (size_t)u * N * kHeadDim;
-
-    // ---- squared norms: the warp's 32 tokens, 4 lanes per token, 8 tokens per step
-    constexpr int RV = row_vecs<T>();  // 16-byte vectors per row
-    constexpr int VPL = RV / 4;        // vectors per lane per token
-    constexpr int STEPS = 4;           // 4 steps x 8 tokens = the warp's 32 tokens
-    const long long wt0 = t0 + warp * 32;
-    uint4 buf[STEPS][VPL];
+__device__ __forceinline__ void load_rows32(const T *__restrict__ Ku, int N, long long wt0, int lane,
+                                            uint4 (&buf)[4][row_vecs<T>() / 4]) {
+    constexpr int VPL = row_vecs<T>() / 4;
 #pragma unroll
-    for (int s = 0; s < STEPS; ++s) {
+    for (int s = 0; s < 4; ++s) {
         const long long j = wt0 + s * 8 + lane / 4;
         const uint4 *row = reinterpret_cast<const uint4 *>(Ku + (size_t)(j < N ? j : 0) * kHeadDim);
 #pragma unroll
-        for (int v = 0; v < VPL; ++v) buf[s][v] = (j < N) ? ld_stream16(row + (lane % 4) + 4 * v) : make_uint4(0, 0, 0, 0);
-    }
-    // every load above is issued before any of the arithmetic below
-#pragma unroll
-    for (int s = 0; s < STEPS; ++s)
-#pragma unroll
         for (int v = 0; v < VPL; ++v)
-            asm volatile("" : "+r"(buf[s][v].x), "+r"(buf[s][v].y), "+r"(buf[s][v].z), "+r"(buf[s][v].w));
-    float mine_hi = 0.f, mine_lo = 0.f;  // lane s*8 + t keeps token s*8 + t's norm
+            buf[s][v] = (j < N) ? ld_stream16(row + (lane % 4) + 4 * v) : make_uint4(0, 0, 0, 0);
+    }
+}
+
+// |k|^2 of row wt0 + lane as an unevaluated double-float sum (hi + lo) from
+// load_rows32's registers.  bf16: every square is exact in fp32, and the even
+// and odd elements run as two double-float sums on packed pairs joined at the
+// end; fp32: each square's rounding error is carried too.
+template <typename T>
+__device__ __forceinline__ void norms32(const uint4 (&buf)[4][row_vecs<T>() / 4], int lane, float &mine_hi,
+                                        float &mine_lo) {
+    constexpr int VPL = row_vecs<T>() / 4;
+    mine_hi = 0.f;
+    mine_lo = 0.f;
 #pragma unroll
-    for (int s = 0; s < STEPS; ++s) {
+    for (int s = 0; s < 4; ++s) {
         float hi = 0.f, lo = 0.f;
         if constexpr (sizeof(T) == 2) {
-            // bf16: every square is exact in fp32; two double-float sums (even
-            // and odd elements) on packed pairs, joined at the end
             unsigned long long hi2 = 0ull, lo2 = 0ull;
 #pragma unroll
             for (int v = 0; v < VPL; ++v) {
@@ -120,6 +112,51 @@ __global__ void __launch_bounds__(kThreads, 3) k_lift_count(const T *__restrict_
             mine_lo = glo;
         }
     }
+}
+
+// e = e1 + e2 + e3 in bf16 parts (each remainder exact in fp32): the extra K
+// columns of the tensor-core contraction, [e1, e1, e2, e1, e2, e3] for a
+// token and [e1, e2, e1, e3, e2, e1] for a parent, whose dot product holds
+// every term e_a f_b with a + b <= 4.
+__device__ __forceinline__ void write_lifted(float e, uint4 *tok_row, uint4 *par_row) {
+    const __nv_bfloat16 e1 = __float2bfloat16_rn(e);
+    const float r1 = e - __bfloat162float(e1);
+    const __nv_bfloat16 e2 = __float2bfloat16_rn(r1);
+    const __nv_bfloat16 e3 = __float2bfloat16_rn(r1 - __bfloat162float(e2));
+    const __nv_bfloat16 z = __float2bfloat16(0.f);
+    if (tok_row) {
+        const __nv_bfloat16 row[16] = {e1, e1, e2, e1, e2, e3, z, z, z, z, z, z, z, z, z, z};
+        const uint4 *w = reinterpret_cast<const uint4 *>(row);
+        tok_row[0] = w[0];
+        tok_row[1] = w[1];
+    }
+    if (par_row) {
+        const __nv_bfloat16 prow[16] = {e1, e2, e1, e3, e2, e1, z, z, z, z, z, z, z, z, z, z};
+        const uint4 *w = reinterpret_cast<const uint4 *>(prow);
+        par_row[0] = w[0];
+        par_row[1] = w[1];
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 3) k_lift_count(const T *__restrict__ K, int N, int n_kv_heads,
+                                                         uint64_t thresh, uint64_t key,
+                                                         double *__restrict__ norm2, int32_t *__restrict__ pcount,
+                                                         double *__restrict__ tile_max,
+                                                         unsigned long long *__restrict__ tile_min, int n_tiles) {
+    dep_wait();  // the previous kernel of the stream is complete (launched as its dependent)
+    const int u = blockIdx.y, tile = blockIdx.x;
+    const int seq = u / n_kv_heads, head = u % n_kv_heads;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long t0 = (long long)tile * kLiftTile;
+    const T *Ku = K + (size_t)u * N * kHeadDim;
+
+    // ---- squared norms: the warp's 32 tokens, 4 lanes per token, 8 tokens per step
+    const long long wt0 = t0 + warp * 32;
+    uint4 buf[4][row_vecs<T>() / 4];
+    load_rows32<T>(Ku, N, wt0, lane, buf);
+    float mine_hi, mine_lo;  // lane s*8 + t keeps token s*8 + t's norm
+    norms32<T>(buf, lane, mine_hi, mine_lo);
     const long long j = wt0 + lane;
     double wmax = 0.0;  // one conversion per token: the fp64 units are few
     if (j < N) {
@@ -256,34 +293,15 @@ __global__ void __launch_bounds__(kThreads) k_promote_write(
         // units are few on this part)
         const double r = M2 - n2;
         const float e = sqrtf(r > 0.0 ? (float)r : 0.f);
-        // e as three bf16 parts e1 + e2 + e3 (24 significant bits, each
-        // remainder exact in fp32): the extra K columns of the tensor-core
-        // contraction, [e1, e1, e2, e1, e2, e3] for the token and
-        // [e1, e2, e1, e3, e2, e1] for a parent, whose dot product holds every
-        // term e_a f_b with a + b <= 4.
-        const __nv_bfloat16 e1 = __float2bfloat16_rn(e);
-        const float r1 = e - __bfloat162float(e1);
-        const __nv_bfloat16 e2 = __float2bfloat16_rn(r1);
-        const __nv_bfloat16 e3 = __float2bfloat16_rn(r1 - __bfloat162float(e2));
-        const __nv_bfloat16 z = __float2bfloat16(0.f);
-        if (a_extra) {
-            const __nv_bfloat16 row[16] = {e1, e1, e2, e1, e2, e3, z, z, z, z, z, z, z, z, z, z};
-            const uint4 *w = reinterpret_cast<const uint4 *>(row);
-            a_extra[((size_t)u * N + j) * 2 + 0] = w[0];
-            a_extra[((size_t)u * N + j) * 2 + 1] = w[1];
-        }
-        if (f && m < np_cap) {
+        const bool par = f && m < np_cap;
+        const size_t up = (size_t)u * np_cap;
+        write_lifted(e, a_extra ? a_extra + ((size_t)u * N + j) * 2 : nullptr,
+                     (par && b_extra) ? b_extra + (up + m) * 2 : nullptr);
+        if (par) {
             tp = m;
-            const size_t up = (size_t)u * np_cap;
             parent_tok[up + m] = (int32_t)j;
             parent_e[up + m] = e;
             parent_corr[up + m] = 0.f;
-            if (b_extra) {
-                const __nv_bfloat16 prow[16] = {e1, e2, e1, e3, e2, e1, z, z, z, z, z, z, z, z, z, z};
-                const uint4 *w = reinterpret_cast<const uint4 *>(prow);
-                b_extra[(up + m) * 2 + 0] = w[0];
-                b_extra[(up + m) * 2 + 1] = w[1];
-            }
         }
         token_parent[(size_t)u * n_cap + j] = tp;
         if (f) {

@@ -50,6 +50,7 @@ constexpr int kPageElems = kPage * kHeadDim;
 constexpr uint32_t kPageBytes = kPageElems * 2;
 constexpr int kCand = 64;    // keys a selection warp collects
 constexpr int kMaxPPC = 16;  // pages of the union per CTA
+constexpr int kSpanPT = 2;   // parent spans per thread loaded with the parent rows
 
 
 // Shared-memory layout (byte offsets, 128-byte aligned pieces).
@@ -81,7 +82,7 @@ __host__ __device__ inline Lay layout(int gt, int chunk, int page_cap, int max_s
 }
 
 template <int GT>
-__global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT) k_decode_cluster2(
+__global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT, 1) k_decode_cluster2(
     const __nv_bfloat16 *__restrict__ Q, int g, int n_q_heads, int n_kv_heads, int np_cap, int page_cap, int k_pages,
     int chunk, int ppc_cap, const int32_t *__restrict__ n_parents, const int32_t *__restrict__ n_pages,
     const __nv_bfloat16 *__restrict__ parent_keys, const int32_t *__restrict__ parent_first_page,
@@ -115,7 +116,6 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT) k_decode_cluste
     float *s_po = reinterpret_cast<float *>(smem + L.po);
     unsigned long long *s_bar = reinterpret_cast<unsigned long long *>(smem + L.bars);
     __shared__ int s_wsum[kW];
-    __shared__ int s_carry;
 
     const size_t up = (size_t)u * np_cap, ug = (size_t)u * page_cap;
     const int Np = min(n_parents[u], np_cap);
@@ -126,30 +126,28 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT) k_decode_cluste
         mbar_init_fence();
     }
 
-    // q slices: head hh, dims 8c .. 8c + 7 as fp32 pairs
-    unsigned long long q[GT][4];
+    // q slices: head hh, dims 8c .. 8c + 7 (converted to fp32 pairs once the
+    // first parent rows are on their way)
+    uint4 qraw[GT];
     {
         const __nv_bfloat16 *Qu = Q + ((size_t)b * n_q_heads + (size_t)h * g) * kHeadDim;
 #pragma unroll
-        for (int hh = 0; hh < GT; ++hh) {
-            uint4 raw = make_uint4(0, 0, 0, 0);
-            if (hh < g) raw = *reinterpret_cast<const uint4 *>(Qu + (size_t)hh * kHeadDim + 8 * c);
-            q[hh][0] = bf2_pair(raw.x);
-            q[hh][1] = bf2_pair(raw.y);
-            q[hh][2] = bf2_pair(raw.z);
-            q[hh][3] = bf2_pair(raw.w);
-        }
+        for (int hh = 0; hh < GT; ++hh)
+            qraw[hh] = hh < g ? *reinterpret_cast<const uint4 *>(Qu + (size_t)hh * kHeadDim + 8 * c)
+                              : make_uint4(0, 0, 0, 0);
     }
+    unsigned long long q[GT][4];
 
     // ------------------------------------------------------------ phase 1
-    for (int loc = tid; loc < chunk; loc += kT) {
-        const int m = m0 + loc;
-        int4 sp = make_int4(0, 0, 0, 0);
-        if (m < Np) {
-            const int fp = parent_first_page[up + m], np = parent_n_pages[up + m], lp = parent_last_page[up + m];
-            sp = make_int4(fp, np, lp - fp + 1 == np ? 1 : 0, m);
-        }
-        s_span[loc] = sp;
+    // the slice's page spans (read by the leader after the first cluster
+    // barrier): their loads go out with the parent rows below
+    int4 sp_mine[kSpanPT];
+#pragma unroll
+    for (int i = 0; i < kSpanPT; ++i) {
+        const int loc = tid + i * kT, m = m0 + loc;
+        sp_mine[i] = make_int4(0, 0, 0, 0);
+        if (loc < chunk && m < Np)
+            sp_mine[i] = make_int4(parent_first_page[up + m], parent_n_pages[up + m], parent_last_page[up + m], m);
     }
     {
         constexpr int U4 = 8;  // parent rows per lane in flight
@@ -162,6 +160,15 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT) k_decode_cluste
                 raw[i] = (loc < chunk && m < Np)
                              ? *reinterpret_cast<const uint4 *>(parent_keys + (up + m) * kHeadDim + 8 * c)
                              : make_uint4(0, 0, 0, 0);
+            }
+            if (base == 0) {
+#pragma unroll
+                for (int hh = 0; hh < GT; ++hh) {
+                    q[hh][0] = bf2_pair(qraw[hh].x);
+                    q[hh][1] = bf2_pair(qraw[hh].y);
+                    q[hh][2] = bf2_pair(qraw[hh].z);
+                    q[hh][3] = bf2_pair(qraw[hh].w);
+                }
             }
 #pragma unroll
             for (int i = 0; i < U4; ++i) {
@@ -198,6 +205,22 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT) k_decode_cluste
             }
         }
     }
+#pragma unroll
+    for (int i = 0; i < kSpanPT; ++i) {
+        const int loc = tid + i * kT;
+        int4 sp = sp_mine[i];
+        sp.z = sp.z - sp.x + 1 == sp.y ? 1 : 0;  // contiguous page run
+        if (loc < chunk) s_span[loc] = sp;
+    }
+    for (int loc = tid + kSpanPT * kT; loc < chunk; loc += kT) {  // slices beyond the register batch
+        const int m = m0 + loc;
+        int4 sp = make_int4(0, 0, 0, 0);
+        if (m < Np) {
+            const int fp = parent_first_page[up + m], np = parent_n_pages[up + m], lp = parent_last_page[up + m];
+            sp = make_int4(fp, np, lp - fp + 1 == np ? 1 : 0, m);
+        }
+        s_span[loc] = sp;
+    }
     __syncthreads();
     // per head: the slice's best kc keys, sorted (lane = rank), into s_top
     if (warp < g) {
@@ -211,13 +234,7 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT) k_decode_cluste
                 uint32_t vo[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) vo[e] = e * 32 + lane < nvalid ? ord_f32(sc[e * 32 + lane]) : 0u;
-                for (int bit = 31; bit >= 0; --bit) {
-                    const uint32_t cnd = res | (1u << bit);
-                    unsigned cnt = 0;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) cnt += vo[e] >= cnd;
-                    if ((int)__reduce_add_sync(0xffffffffu, cnt) >= kc) res = cnd;
-                }
+                res = kth_largest_ord(vo, kc);
             } else {
                 for (int bit = 31; bit >= 0; --bit) {
                     const uint32_t cnd = res | (1u << bit);
@@ -262,14 +279,14 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT) k_decode_cluste
         }
         s_top[hh * 32 + lane] = lane < kc ? best : 0ull;
     }
+    const int P = min(n_pages[u], page_cap);
+    const int words = (P + 31) / 32;
+    if (r == 0)
+        for (int x = tid; x < words; x += kT) s_mask[x] = 0u;
     cluster.sync();
 
     // ------------------------------------------------------------ phase 2
     if (r == 0) {
-        const int P = min(n_pages[u], page_cap);
-        const int words = (P + 31) / 32;
-        for (int x = tid; x < words; x += kT) s_mask[x] = 0u;
-        __syncthreads();
         if (k_pages >= P) {
             for (int x = tid; x < words; x += kT) {
                 const int rem = P - x * 32;
@@ -310,38 +327,36 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT) k_decode_cluste
             }
         }
         __syncthreads();
-        if (tid == 0) s_carry = 0;
-        __syncthreads();
-        for (int w0 = 0; w0 < words; w0 += kT) {
-            const int x = w0 + tid;
-            const unsigned bits = x < words ? s_mask[x] : 0u;
-            const int cc = __popc(bits);
-            int incl = cc;
+        // ascending list of the union's pages: thread tid owns words
+        // [tid * wpt, (tid + 1) * wpt); one block-wide scan of the counts
+        const int wpt = (words + kT - 1) / kT;
+        const int wb = tid * wpt, we = min(words, wb + wpt);
+        int cc = 0;
+        for (int x = wb; x < we; ++x) cc += __popc(s_mask[x]);
+        int incl = cc;
 #pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int o = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += o;
-            }
-            if (lane == 31) s_wsum[warp] = incl;
-            __syncthreads();
-            int pos = s_carry;
-            for (int w = 0; w < warp; ++w) pos += s_wsum[w];
-            pos += incl - cc;
-            unsigned bb = bits;
-            while (bb) {
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        if (lane == 31) s_wsum[warp] = incl;
+        __syncthreads();
+        int pos = incl - cc, total = 0;
+#pragma unroll
+        for (int w = 0; w < kW; ++w) {
+            pos += w < warp ? s_wsum[w] : 0;
+            total += s_wsum[w];
+        }
+        for (int x = wb; x < we && pos < max_sel; ++x) {
+            unsigned bb = s_mask[x];
+            while (bb && pos < max_sel) {
                 const int bit = __ffs(bb) - 1;
                 bb &= bb - 1;
-                if (pos < max_sel) {
-                    s_uni[1 + pos] = x * 32 + bit;
-                    sel_pages[(size_t)u * max_sel + pos] = x * 32 + bit;
-                }
+                s_uni[1 + pos] = x * 32 + bit;
+                sel_pages[(size_t)u * max_sel + pos] = x * 32 + bit;
                 ++pos;
             }
-            __syncthreads();
-            if (tid == kT - 1) s_carry = pos;
-            __syncthreads();
         }
-        const int total = s_carry;
         for (int x = total + tid; x < max_sel; x += kT) sel_pages[(size_t)u * max_sel + x] = -1;
         if (tid == 0) {
             if (total > max_sel) set_err(err, ICE_ERR_CAPACITY);

@@ -89,31 +89,6 @@ static __device__ unsigned long long best_slow(const float *__restrict__ sh, int
     return mine;
 }
 
-// The kc-th largest of the warp's values (8 per lane, order-preserving
-// integer form, 0 = none), found bit by bit from the top: the largest c with
-// at least kc values >= c.  Stops early once exactly kc values reach the
-// prefix: the answer is then their minimum.
-__device__ __forceinline__ uint32_t kth_largest_ord(const uint32_t (&v)[8], int kc) {
-    uint32_t r = 0u;
-    for (int bit = 31; bit >= 0; --bit) {
-        const uint32_t c = r | (1u << bit);
-        unsigned cnt = 0;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) cnt += v[e] >= c;
-        const int n = (int)__reduce_add_sync(0xffffffffu, cnt);
-        if (n >= kc) {
-            r = c;
-            if (n == kc) {
-                uint32_t mn = 0xFFFFFFFFu;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) mn = v[e] >= c ? min(mn, v[e]) : mn;
-                return __reduce_min_sync(0xffffffffu, mn);
-            }
-        }
-    }
-    return r;
-}
-
 // Selection of unit u by the select group (NSW warps, thread tid of the
 // group): warp hh < g takes query head hh, finds its ordered best kc parents
 // and ORs their pages (k per head) into the union bitmask; then the group
