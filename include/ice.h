@@ -317,6 +317,11 @@ ice_status ice_sparse_attn_decode_noalloc(const ice_params *p, const void *Q, co
  * kbuf/vbuf/buf_len (the contiguous buffer of step a9) and computes the
  * attention of step a10 from the same copy.  Same outputs as the three
  * separate calls.
+ * kbuf, vbuf and buf_len may all be NULL: the selected pages are then
+ * gathered into on-chip shared memory only and attended from there, with no
+ * contiguous copy in device memory (the pool is still read once); sel_pages,
+ * sel_count and O are the same as with the buffer.  Mixing NULL and non-NULL
+ * among the three is ICE_ERR_INVALID_ARG.
  */
 ice_status ice_decode_step(const ice_params *p, const ice_index *idx, const void *Q, int32_t budget_tokens,
                            int32_t *sel_pages, int32_t *sel_count, int32_t max_sel, void *kbuf, void *vbuf,

@@ -406,7 +406,10 @@ ice_status ice_decode_step(const ice_params *p, const ice_index *idx, const void
     ice_status st = decode_common(p, budget_tokens, max_sel, ws, ws_bytes, &w);
     if (st) return st;
     if ((st = select_checks(p, idx, Q, budget_tokens, sel_pages, sel_count, max_sel, w))) return st;
-    if (!kbuf || !vbuf || !buf_len || !O) return fail(ICE_ERR_INVALID_ARG, "decode needs non-NULL kbuf, vbuf, buf_len and O");
+    if (!O) return fail(ICE_ERR_INVALID_ARG, "decode needs a non-NULL O");
+    const bool no_buffer = !kbuf && !vbuf && !buf_len;  // pages gathered on chip only
+    if (!no_buffer && (!kbuf || !vbuf || !buf_len))
+        return fail(ICE_ERR_INVALID_ARG, "kbuf, vbuf and buf_len must be all non-NULL or all NULL");
     if (!aligned16(kbuf) || !aligned16(vbuf)) return fail(ICE_ERR_INVALID_ARG, "kbuf and vbuf must be 16-byte aligned");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // one cluster per unit pays off while all clusters fit in one wave; with

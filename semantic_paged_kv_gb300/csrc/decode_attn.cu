@@ -121,12 +121,12 @@ __global__ void __launch_bounds__(kThreads) k_attn(
         if (kFused) {
             const int len = page_len[(size_t)u * page_cap + sel_pages[slot]];
             s_len[t] = len;
-            buf_len[slot] = len;
+            if (buf_len) buf_len[slot] = len;
         } else {
             s_len[t] = buf_len[slot];
         }
     }
-    if (kFused) {  // slots of this split past the selection hold no page
+    if (kFused && buf_len) {  // slots of this split past the selection hold no page
         for (int x = max(x0, n) + t; x < min(x0 + PPS, max_sel); x += kThreads) buf_len[(size_t)u * max_sel + x] = 0;
     }
 #pragma unroll
@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kThreads) k_attn(
             for (int v = 0; v < VPT; ++v) {
                 s_kv[(2 * i) * PVEC + t + v * kThreads] = rk[i][v];
                 s_kv[(2 * i + 1) * PVEC + t + v * kThreads] = rv[i][v];
-                if (kFused) {
+                if (kFused && buf_len) {  // no buf_len: no contiguous copy
                     reinterpret_cast<uint4 *>(kbuf)[slot * PVEC + t + v * kThreads] = rk[i][v];
                     reinterpret_cast<uint4 *>(vbuf)[slot * PVEC + t + v * kThreads] = rv[i][v];
                 }

@@ -24,7 +24,8 @@
 //                 16 dimension tiles.
 // With F the page goes back to kbuf / vbuf by 2-D TMA stores from shared
 // memory (the slot is reloaded only after its stores have read it) and its
-// length to buf_len.  The warps merge in shared memory; with S = 1 the CTA
+// length to buf_len, unless buf_len is null: then the pages are gathered into
+// shared memory only and no contiguous copy is written.  The warps merge in shared memory; with S = 1 the CTA
 // writes O, otherwise its partial joins the others through the unit's ticket
 // (log-sum-exp, the last CTA writes O).  HR = 2 when g > 8 (rows 8..15 hold
 // query heads too).
@@ -130,7 +131,8 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
     const int xe = min(n, xs + ps);
     const int np = max(0, xe - xs);
     const size_t ubase = (size_t)u * max_sel;
-    if (kFused)
+    const bool store = kFused && buf_len != nullptr;  // write the contiguous buffer
+    if (store)
         for (int x = max(xs, n) + tid; x < min(xs + ps, max_sel); x += kMT) buf_len[ubase + x] = 0;
     __syncthreads();
 
@@ -189,12 +191,12 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
         const size_t slot = ubase + x;
         const int len = __shfl_sync(0xffffffffu, my_len, k);
         const int pid_next = __shfl_sync(0xffffffffu, my_pid, (k + 2) & 31);
-        if (kFused && lane == 0) buf_len[slot] = len;
+        if (store && lane == 0) buf_len[slot] = len;
         if (ok) ok = mbar_wait(&S.full[warp][k & 1], (k >> 1) & 1);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         unsigned char *sp = S.kv[warp][k & 1];
-        if (kFused && lane == 0) {  // the contiguous buffer, straight from shared memory
+        if (store && lane == 0) {  // the contiguous buffer, straight from shared memory
             fence_proxy_async();
             const int row = (int)(slot * kPage);
             tma_store_2d(&tm_kb, sp, 0, row);
@@ -283,13 +285,13 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
         }
         __syncwarp();
         if (lane == 0 && k + 2 < nk) {  // refill this slot once its stores have read it
-            if (kFused) bulk_wait_read_all();
+            if (store) bulk_wait_read_all();
             issue(k + 2, pid_next);
         }
         __syncwarp();
     }
     if (!ok) set_err(err, ICE_ERR_TIMEOUT);
-    if (kFused && lane == 0) bulk_wait_read_all();  // the slots are reused below
+    if (store && lane == 0) bulk_wait_read_all();  // the slots are reused below
     if (qc == 0) {
         S.ml[warp][qr][0] = m_run[0];
         S.ml[warp][qr][1] = l_run[0];
@@ -396,13 +398,16 @@ cudaError_t launch_hr(const ice_params &p, const ice_index *pool, const int32_t 
     const unsigned long long prow = (unsigned long long)U * p.page_cap * kPage;
     const unsigned long long brow = (unsigned long long)U * max_sel * kPage;
     if (brow > 0x7FFFFFFFull || prow > 0x7FFFFFFFull) return cudaErrorNotSupported;
-    if (!make_map_bf16(&tkb, kbuf, brow, kHeadDim, 64, kPage, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map_bf16(&tvb, vbuf, brow, kHeadDim, 64, kPage, CU_TENSOR_MAP_SWIZZLE_128B))
+    const bool store = buf_len != nullptr;  // fused without buf_len: no contiguous copy
+    if (store && (!make_map_bf16(&tkb, kbuf, brow, kHeadDim, 64, kPage, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                  !make_map_bf16(&tvb, vbuf, brow, kHeadDim, 64, kPage, CU_TENSOR_MAP_SWIZZLE_128B)))
         return cudaErrorNotSupported;
+    if (!F && !store) return cudaErrorInvalidValue;
     if (F) {
         if (!make_map_bf16(&tk, pool->pool_k, prow, kHeadDim, 64, kPage, CU_TENSOR_MAP_SWIZZLE_128B) ||
             !make_map_bf16(&tv, pool->pool_v, prow, kHeadDim, 64, kPage, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorNotSupported;
+        if (!store) tkb = tvb = tk;  // unused
     } else {
         tk = tkb;
         tv = tvb;

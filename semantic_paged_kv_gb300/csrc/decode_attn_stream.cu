@@ -93,7 +93,8 @@ __global__ void __launch_bounds__(kThreads, (GT / HS) >= 8 ? 2 : 3) k_attn_strea
             bulk_load(S.kv[i][1], sv, kPageBytes, &S.full[i]);
         }
     }
-    if (kFused)  // slots of this split past the selection hold no page
+    const bool store = kFused && buf_len != nullptr;  // no buf_len: no contiguous copy
+    if (store)  // slots of this split past the selection hold no page
         for (int x = max(x0, n) + tid; x < min(x0 + SPP, max_sel); x += kThreads) buf_len[(size_t)u * max_sel + x] = 0;
 
     // q slices: heads hbase .. hbase + GH - 1, dimensions 8 c .. 8 c + 7 with c = lane % 16
@@ -121,13 +122,13 @@ __global__ void __launch_bounds__(kThreads, (GT / HS) >= 8 ? 2 : 3) k_attn_strea
         int len;
         if (kFused) {
             len = page_len[(size_t)u * page_cap + sel_pages[slot]];
-            if (lane == 0 && hbase == 0) buf_len[slot] = len;
+            if (store && lane == 0 && hbase == 0) buf_len[slot] = len;
         } else {
             len = buf_len[slot];
         }
         ok = mbar_wait(&S.full[pw], 0);
         ok = __all_sync(0xffffffffu, ok);
-        if (ok && kFused && lane == 0 && hbase == 0) {  // the contiguous buffer, straight from shared memory
+        if (ok && store && lane == 0 && hbase == 0) {  // the contiguous buffer, straight from shared memory
             fence_proxy_async();
             bulk_store(kbuf + slot * kPageElems, S.kv[pw][0], kPageBytes);
             bulk_store(vbuf + slot * kPageElems, S.kv[pw][1], kPageBytes);
@@ -356,7 +357,8 @@ __global__ void __launch_bounds__(kUT, 1) k_attn_unit(
 
     if (tid < 2 * kUW) mbar_init(&S.full[tid >> 1][tid & 1], 1);
     if (tid == 0) mbar_init_fence();
-    if (kFused)  // slots of this share past the selection hold no page
+    const bool store = kFused && buf_len != nullptr;  // no buf_len: no contiguous copy
+    if (store)  // slots of this share past the selection hold no page
         for (int x = max(xs, n) + tid; x < min(xs + ps, max_sel); x += kUT) buf_len[ubase + x] = 0;
     if (lane < 8) {
         S.ml[warp][lane][0] = -INFINITY;
@@ -423,13 +425,13 @@ __global__ void __launch_bounds__(kUT, 1) k_attn_unit(
         const size_t slot = ubase + x;
         const int len = __shfl_sync(0xffffffffu, my_len, k);
         const int pid_next = __shfl_sync(0xffffffffu, my_pid, (k + 2) & 31);
-        if (kFused && lane == 0) buf_len[slot] = len;
+        if (store && lane == 0) buf_len[slot] = len;
         if (ok) ok = mbar_wait(&S.full[warp][k & 1], (k >> 1) & 1);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         const __nv_bfloat16 *Kp = S.kv[warp][k & 1][0];
         const __nv_bfloat16 *Vp = S.kv[warp][k & 1][1];
-        if (kFused && lane == 0) {  // the contiguous buffer, straight from shared memory
+        if (store && lane == 0) {  // the contiguous buffer, straight from shared memory
             fence_proxy_async();
             bulk_store(kbuf + slot * kPageElems, Kp, kPageBytes);
             bulk_store(vbuf + slot * kPageElems, Vp, kPageBytes);
@@ -520,13 +522,13 @@ __global__ void __launch_bounds__(kUT, 1) k_attn_unit(
         __syncwarp();
         // refill this slot with page k + 2 once its stores have read it
         if (lane == 0 && k + 2 < nk) {
-            if (kFused) bulk_wait_read_all();
+            if (store) bulk_wait_read_all();
             issue(k + 2, pid_next);
         }
         __syncwarp();
     }
     if (!ok) set_err(err, ICE_ERR_TIMEOUT);
-    if (kFused && lane == 0) bulk_wait_read_all();  // the slots are reused below
+    if (store && lane == 0) bulk_wait_read_all();  // the slots are reused below
     __syncthreads();
 
     // ---- merge the warps (slot area reused)

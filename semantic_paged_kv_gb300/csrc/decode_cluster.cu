@@ -293,10 +293,12 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT) k_decode_cluste
     const int n = uni[0];
     const int ppc = (n + kC - 1) / kC;
     const int x0 = min(n, r * ppc), x1 = min(n, x0 + ppc);
-    for (int x = min(max_sel, r * ppc) + t; x < min(max_sel, (r + 1) * ppc); x += kT)
-        if (x >= n) buf_len[(size_t)u * max_sel + x] = 0;
-    if (r == kC - 1)  // slots no CTA's share reaches
-        for (int x = kC * ppc + t; x < max_sel; x += kT) buf_len[(size_t)u * max_sel + x] = 0;
+    if (buf_len) {  // no buf_len: no contiguous copy
+        for (int x = min(max_sel, r * ppc) + t; x < min(max_sel, (r + 1) * ppc); x += kT)
+            if (x >= n) buf_len[(size_t)u * max_sel + x] = 0;
+        if (r == kC - 1)  // slots no CTA's share reaches
+            for (int x = kC * ppc + t; x < max_sel; x += kT) buf_len[(size_t)u * max_sel + x] = 0;
+    }
     if (t < g) {
         s_pm[t] = -INFINITY;
         s_pl[t] = 0.f;
@@ -326,7 +328,7 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT) k_decode_cluste
         if (t < np) {
             const int len = page_len[ug + uni[1 + xb + t]];
             s_len[t] = len;
-            buf_len[(size_t)u * max_sel + xb + t] = len;
+            if (buf_len) buf_len[(size_t)u * max_sel + xb + t] = len;
         }
         __syncthreads();  // the previous batch is consumed
 #pragma unroll
@@ -338,8 +340,10 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT) k_decode_cluste
                     const int e = t + v * kT;
                     s_stage[(2 * i) * PVEC + e] = rk[i][v];
                     s_stage[(2 * i + 1) * PVEC + e] = rv[i][v];
-                    reinterpret_cast<uint4 *>(kbuf)[slot * PVEC + e] = rk[i][v];
-                    reinterpret_cast<uint4 *>(vbuf)[slot * PVEC + e] = rv[i][v];
+                    if (buf_len) {
+                        reinterpret_cast<uint4 *>(kbuf)[slot * PVEC + e] = rk[i][v];
+                        reinterpret_cast<uint4 *>(vbuf)[slot * PVEC + e] = rv[i][v];
+                    }
                 }
             }
         }

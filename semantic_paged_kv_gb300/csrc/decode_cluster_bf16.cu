@@ -374,7 +374,8 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT, 1) k_decode_clu
     const int np = x1 - x0;  // <= ppc_cap (checked on the host from max_sel)
     {
         const int ps = (max_sel + kC - 1) / kC;  // slots past the selection: each CTA a static share
-        for (int x = max(n, r * ps) + tid; x < min(max_sel, (r + 1) * ps); x += kT) buf_len[(size_t)u * max_sel + x] = 0;
+        if (buf_len)  // no buf_len: no contiguous copy
+            for (int x = max(n, r * ps) + tid; x < min(max_sel, (r + 1) * ps); x += kT) buf_len[(size_t)u * max_sel + x] = 0;
     }
     if (tid == 0) {
         for (int i = 0; i < np; ++i) {
@@ -399,13 +400,13 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT, 1) k_decode_clu
         const size_t slot = (size_t)u * max_sel + x;
         const int pgid = uni[1 + x];
         const int len = page_len[ug + pgid];
-        if (lane == 0) buf_len[slot] = len;
+        if (buf_len && lane == 0) buf_len[slot] = len;
         if (ok) ok = mbar_wait(&s_bar[i], 0);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         const __nv_bfloat16 *Kp = s_kv + (size_t)i * 2 * kPageElems;
         const __nv_bfloat16 *Vp = Kp + kPageElems;
-        if (lane == 0) {  // the contiguous buffer, straight from shared memory
+        if (buf_len && lane == 0) {  // the contiguous buffer, straight from shared memory
             fence_proxy_async();
             bulk_store(kbuf + slot * kPageElems, Kp, kPageBytes);
             bulk_store(vbuf + slot * kPageElems, Vp, kPageBytes);

@@ -67,14 +67,17 @@ class GpuRun:
     def unit(self, u):
         return u // self.cfg.n_kv_heads, u % self.cfg.n_kv_heads
 
-    def decode(self, budget: int, fused: bool = True, step: int = 0):
+    def decode(self, budget: int, fused: bool = True, step: int = 0, contiguous: bool = True):
+        """contiguous=False: ice_decode_step without kbuf/vbuf/buf_len (pages
+        gathered on chip only)."""
         Q = workloads.batch_queries(self.w, self.layer, step)
         Qd = to_dev(Q, self.cfg.torch_dtype)
         buf = ice.DecodeBuffers(self.cfg, budget)
         scale = 1.0 / np.sqrt(self.cfg.head_dim)
         if fused:
-            ice.ice_decode_step(self.params, self.idx, Qd, budget, buf.sel_pages, buf.sel_count, buf.kbuf, buf.vbuf,
-                                buf.buf_len, scale, buf.O, buf.ws, self.err)
+            kb, vb, bl = (buf.kbuf, buf.vbuf, buf.buf_len) if contiguous else (None, None, None)
+            ice.ice_decode_step(self.params, self.idx, Qd, budget, buf.sel_pages, buf.sel_count, kb, vb, bl, scale,
+                                buf.O, buf.ws, self.err)
         else:
             ice.ice_select_pages(self.params, self.idx, Qd, budget, buf.sel_pages, buf.sel_count, buf.ws, self.err)
             ice.ice_gather_pages(self.params, self.idx, buf.sel_pages, buf.sel_count, buf.kbuf, buf.vbuf, buf.buf_len)

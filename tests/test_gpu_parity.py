@@ -84,6 +84,30 @@ def test_fused_decode_equals_separate_calls():
     assert torch.max(torch.abs(a.O - b.O)).item() <= 1e-5
 
 
+@pytest.mark.parametrize("shape", ["tiny_fp32", "llama_cluster", "qwen_many_units", "longchat_many_units"])
+def test_decode_without_contiguous_buffer(shape):
+    """ice_decode_step with kbuf = vbuf = buf_len = NULL gathers the pages on
+    chip only: same page lists and bit-identical O as with the buffer, on
+    each kernel path (fp32 and bf16 per-unit clusters, tensor-core selection
+    with the streaming attention for many units)."""
+    w = {"tiny_fp32": W["tiny"],
+         "llama_cluster": W["llama31_8b_16k"].scaled(n_tokens=3000, n_q_heads=8, n_kv_heads=2),
+         "qwen_many_units": W["qwen3_32b_100k"].scaled(n_tokens=3000, batch=3, centres=256),
+         "longchat_many_units": W["longchat_7b_100k"].scaled(n_tokens=2500, batch=1, n_q_heads=24, n_kv_heads=24,
+                                                             centres=256)}[shape]
+    run = GpuRun(w)
+    assert run.status == ice.ICE_OK
+    for bgt in (64, 256):
+        Q, a, st_a = run.decode(bgt, contiguous=True)
+        _, b, st_b = run.decode(bgt, contiguous=False)
+        assert st_a == ice.ICE_OK and st_b == ice.ICE_OK
+        assert torch.equal(a.sel_count, b.sel_count)
+        assert torch.equal(a.sel_pages, b.sel_pages)
+        assert torch.equal(a.O, b.O)
+        assert torch.all(b.buf_len == 0)  # untouched
+        check_decode_unit(run, run.cfg.units - 1, Q, bgt, a)
+
+
 def test_qwen_shaped_g8_mha_longchat_shaped_g1():
     for w in (W["qwen3_32b_100k"].scaled(n_tokens=4100, batch=2, n_q_heads=16, n_kv_heads=2, centres=512),
               W["longchat_7b_100k"].scaled(n_tokens=4100, batch=1, n_q_heads=3, n_kv_heads=3, centres=512)):
@@ -233,4 +257,11 @@ def test_invalid_arguments_rejected():
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     with pytest.raises(ice.IceError) as ei:
         ice.ice_build_index(p, K, K, idx, small, err)
+    assert ei.value.status == ice.ICE_ERR_INVALID_ARG
+    # the decode step's contiguous buffer: all three pointers or none
+    buf = ice.DecodeBuffers(cfg, 64)
+    Q = torch.zeros((1, 4, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ice.IceError) as ei:
+        ice.ice_decode_step(p, idx, Q, 64, buf.sel_pages, buf.sel_count, None, buf.vbuf, buf.buf_len, 0.1, buf.O,
+                            buf.ws, err)
     assert ei.value.status == ice.ICE_ERR_INVALID_ARG
