@@ -242,6 +242,29 @@ def build_unit(K, V, *, seed: int, layer: int, seq: int, head: int, thresh: int,
                 pool_k=pool_k, pool_v=pool_v, S=S, **pk)
 
 
+def build_unit_reuse(K, V, prev: dict, S: int = 16) -> dict:
+    """Build of one unit on another layer's node structure (the inter-layer
+    index reuse of the article's section 五, "IceCache (reuse)"; its mechanism
+    is not described, so this is the stated rule): the promoted tokens and
+    the token -> parent assignment are prev's; the lift (M^2, e) comes from
+    this layer's keys (step a1), the pages from packing prev's assignment
+    (step a4), the pool from this layer's K and V (step a5).  prev must index
+    the same N tokens."""
+    K = _f64(K)
+    V = _f64(V)
+    N = K.shape[0]
+    parent_tok = np.asarray(prev["parent_tok"], np.int32)
+    token_parent = np.asarray(prev["token_parent"][:N], np.int32)
+    if len(token_parent) != N or (len(parent_tok) and (parent_tok.min() < 0 or parent_tok.max() >= N)):
+        raise ValueError("prev does not index the same N tokens")
+    n, M2, e = lift(K)
+    pk = pack(token_parent, len(parent_tok), S)
+    pool_k, pool_v = scatter(K, V, pk["page_tokens"], S)
+    return dict(n=n, M2=M2, e=e, parent_tok=parent_tok, parent_keys=K[parent_tok] if N else K[:0],
+                parent_e=e[parent_tok] if N else e[:0], token_parent=token_parent,
+                pool_k=pool_k, pool_v=pool_v, S=S, **pk)
+
+
 def decode_unit(idx: dict, q, budget_tokens: int, scale: float | None = None) -> dict:
     """Decode steps a6-a10 for one unit and its g query heads."""
     S = idx["S"]

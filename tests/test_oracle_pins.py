@@ -363,3 +363,59 @@ def test_insert_stream_keeps_invariants_and_matches_rebuild_when_nothing_promote
     e = np.sqrt(np.maximum(idx["M2"] - n, 0))
     tp = oracle.assign(Kall, e, idx["parent_tok"])
     assert np.array_equal(ui.token_parent[:450], tp)
+
+
+# ------------------------------------------------------- inter-layer reuse
+def _reuse_pair(n_tokens=1500, centres=24):
+    w = workloads.WORKLOADS["llama31_8b_16k"].scaled(n_tokens=n_tokens, centres=centres, dtype="fp32")
+    th = oracle.promote_threshold(w.promote_p)
+    K0, V0 = workloads.unit_kv(w, 0, 0, 1)
+    K1, V1 = workloads.unit_kv(w, 1, 0, 1)
+    prev = oracle.build_unit(K0, V0, seed=w.seed, layer=0, seq=0, head=1, thresh=th)
+    return w, th, (K0, V0), (K1, V1), prev
+
+
+def test_reuse_of_own_index_is_the_full_build():
+    """Reusing a unit's own node structure on its own keys reproduces the full
+    build (lift, promotion, nearest-parent assignment, pack, scatter)."""
+    w, th, (K0, V0), _, prev = _reuse_pair()
+    r = oracle.build_unit_reuse(K0, V0, prev)
+    for f in ("parent_tok", "token_parent", "page_parent", "page_len", "page_tokens", "token_page", "token_slot",
+              "parent_keys", "parent_e", "pool_k", "pool_v", "e"):
+        assert np.array_equal(np.asarray(r[f]), np.asarray(prev[f])), f
+    assert r["M2"] == prev["M2"] and r["n_pages"] == prev["n_pages"]
+
+
+def test_reuse_on_another_layer_keeps_pages_and_takes_this_layers_keys():
+    w, th, _, (K1, V1), prev = _reuse_pair()
+    r = oracle.build_unit_reuse(K1, V1, prev)
+    for f in ("parent_tok", "token_parent", "page_parent", "page_len", "page_tokens", "token_page", "token_slot"):
+        assert np.array_equal(np.asarray(r[f]), np.asarray(prev[f])), f
+    K = K1.astype(np.float64)
+    n2 = np.einsum("ij,ij->i", K, K)
+    assert abs(r["M2"] - n2.max()) <= 1e-14 * n2.max()  # summation order only
+    assert np.array_equal(r["parent_keys"], K[prev["parent_tok"]])
+    # closed form of the lift: every lifted parent has norm M
+    pe = np.asarray(r["parent_e"])
+    assert np.allclose(n2[prev["parent_tok"]] + pe ** 2, r["M2"], rtol=1e-12, atol=1e-9)
+    # the pool holds this layer's rows in the kept pages, zero pads
+    for p in range(r["n_pages"]):
+        for s in range(16):
+            t = r["page_tokens"][p][s]
+            want = K1[t] if t >= 0 else np.zeros(K1.shape[1])
+            assert np.array_equal(r["pool_k"][p][s], want)
+    _check_pack_invariants(r["token_parent"], len(r["parent_tok"]), 16, r)
+
+
+def test_reuse_full_budget_is_dense_attention_of_this_layer():
+    """With every page selected, decode over the reused index is dense softmax
+    attention over all N tokens of the new layer (torch SDPA, float64)."""
+    w, th, _, (K1, V1), prev = _reuse_pair(n_tokens=700)
+    r = oracle.build_unit_reuse(K1, V1, prev)
+    q = workloads.unit_queries(w, 1, 0, 1)
+    dec = oracle.decode_unit(r, q, budget_tokens=16 * r["n_pages"])
+    qt = torch.from_numpy(q.astype(np.float64))[None, :, None, :]
+    kt = torch.from_numpy(K1.astype(np.float64))[None, None].expand(1, q.shape[0], -1, -1)
+    vt = torch.from_numpy(V1.astype(np.float64))[None, None].expand(1, q.shape[0], -1, -1)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt)[0, :, 0].numpy()
+    assert np.max(np.abs(dec["out"] - ref)) < 1e-12
