@@ -445,6 +445,7 @@ def run_ours(args):
         st["idx"] = ice.Index(c)
         st["ws"] = ice.workspace(ice.ice_build_workspace_bytes(p))
         st["buf"] = ice.DecodeBuffers(c, budget)
+        st["idx_reuse"] = ice.Index(c)  # this layer built on the previous set's node structure
         st["Oh"] = torch.empty_like(st["buf"].O, device="cpu").pin_memory()
         sets.append(st)
     set_bytes = sum(x.numel() * x.element_size() for x in (sets[0]["K"], sets[0]["V"], sets[0]["idx"].pool_k,
@@ -488,6 +489,14 @@ def run_ours(args):
         with torch.cuda.graph(st["step_graph"], stream=cap):
             for f in stages(st):
                 f()
+    # the inter-layer reuse build of each set on the previous set's index
+    for i, st in enumerate(sets):
+        prev = sets[(i - 1) % len(sets)]["idx"]
+        st["reuse"] = (lambda st=st, prev=prev: ice.ice_build_index_reuse(st["params"], st["K"], st["V"], prev,
+                                                                          st["idx_reuse"], st["ws"], err))
+        st["reuse_graph"] = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(st["reuse_graph"], stream=cap):
+            st["reuse"]()
     torch.cuda.current_stream().wait_stream(cap)
     torch.cuda.synchronize()
 
@@ -504,6 +513,8 @@ def run_ours(args):
     for i in range(2 * len(sets)):  # warm the graphs
         step(sets[i % len(sets)])
         step(sets[i % len(sets)], [E() for _ in range(5)])
+    for st in sets:  # every set's index is built now
+        st["reuse_graph"].replay()
 
     # ---- timed region: exactly `steps` steps, each one whole-step graph
     evs = [[E() for _ in range(5)] for _ in range(args.steps)]
@@ -528,6 +539,14 @@ def run_ours(args):
     elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world, "cuda")
     stage = np.array([[e[k].elapsed_time(e[k + 1]) for k in range(4)] for e in evs])  # ms
     lift_ms, assign_ms, pack_ms, decode_ms = stage.mean(0)
+    # the reuse build, timed the same way (sets rotated, one graph per build)
+    rev = [(E(), E()) for _ in range(args.steps)]
+    for i in range(args.steps):
+        rev[i][0].record()
+        sets[i % len(sets)]["reuse_graph"].replay()
+        rev[i][1].record()
+    torch.cuda.synchronize()
+    reuse_ms = float(np.mean([a.elapsed_time(b) for a, b in rev]))
 
     # ---- algorithmic work of a step (averaged over the sets)
     d, S, U, N = w.head_dim, w.page_size, cfg.units, w.n_tokens
@@ -614,6 +633,10 @@ def run_ours(args):
                 "index_build_keys_per_s": U * N / ((lift_ms + assign_ms + pack_ms) * 1e-3),
                 "build_us": {"lift_promote": 1000 * lift_ms, "assign": 1000 * assign_ms, "pack": 1000 * pack_ms},
                 "assign_tflops": flops_assign / (assign_ms * 1e-3) / 1e12,
+                "build_reuse_us": 1000 * reuse_ms,
+                "index_build_reuse_keys_per_s": U * N / (reuse_ms * 1e-3),
+                "build_reuse_as": "ice_build_index_reuse of each input set on the previous set's index (inter-layer "
+                                  "reuse: lift, parent keys, table copies, pool; no assignment, no ranking)",
                 "parents_per_step": np_tot, "pages_per_step": pages_tot, "selected_pages_per_step": sel_tot,
                 "set_bytes": set_bytes,
                 "stages_as": "a second timed pass of the same steps: one CUDA graph per stage, events between them "

@@ -206,6 +206,28 @@ ice_status ice_build_assign_simt(const ice_params *p, const void *K, const ice_i
 ice_status ice_build_pack(const ice_params *p, const void *K, const void *V, const ice_index *idx,
                           void *ws, size_t ws_bytes, int32_t *err_dev, void *stream);
 
+/*
+ * Index build of a layer on another layer's node structure ([B] section 五:
+ * "IceCache (reuse)", an inter-layer index reuse that shortens the build; the
+ * article does not describe its mechanism).  Rule used here: the promoted
+ * tokens, the token -> parent assignment and hence the pages of `prev` are
+ * kept; this layer's K gives M^2 (step a1), the parent keys that the
+ * selection scores against and their lifted coordinate; this layer's K and V
+ * fill the pool (step a5).  The nearest-parent contraction (a3) and the
+ * ranking into pages (a4) are skipped.  Results equal those of ice_build_index
+ * on this layer's K, V with parent_tok and token_parent taken from prev.
+ *  - prev: an index of the same shapes and capacities built over the same N
+ *    tokens (ice_build_index or this call; no inserts since).  A unit of prev
+ *    whose n_indexed is not N, or whose parent token is outside [0, N), sets
+ *    ICE_ERR_INVALID_ARG in err_dev.
+ *  - idx may be prev itself (its tables stay and keys, lift values and pool
+ *    are overwritten) or share any page or token table array with prev: a
+ *    shared array is not copied.  Otherwise prev is only read.
+ *  - Workspace: ice_build_workspace_bytes.
+ */
+ice_status ice_build_index_reuse(const ice_params *p, const void *K, const void *V, const ice_index *prev,
+                                 const ice_index *idx, void *ws, size_t ws_bytes, int32_t *err_dev, void *stream);
+
 /* -------------------------------------------------- incremental insert -- */
 /* Workspace bytes for ice_insert_tokens (zero-filled once before first use,
  * like a decode workspace). */

@@ -76,6 +76,7 @@ def load() -> ctypes.CDLL:
         "ice_build_assign": ([pp, P, pi, P, sz, P, P], i32),
         "ice_build_assign_simt": ([pp, P, pi, P, sz, P, P], i32),
         "ice_build_pack": ([pp, P, P, pi, P, sz, P, P], i32),
+        "ice_build_index_reuse": ([pp, P, P, pi, pi, P, sz, P, P], i32),
         "ice_decode_workspace_bytes": ([pp, i32, i32, ctypes.POINTER(sz)], i32),
         "ice_select_pages": ([pp, pi, P, i32, P, P, i32, P, sz, P, P], i32),
         "ice_gather_pages": ([pp, pi, P, P, i32, P, P, P, P], i32),
@@ -101,7 +102,8 @@ def load() -> ctypes.CDLL:
 def exported_symbols() -> list[str]:
     return ["ice_status_string", "ice_last_error", "ice_version", "ice_check", "ice_page_bound",
             "ice_build_workspace_bytes", "ice_build_index", "ice_build_lift_promote", "ice_build_assign",
-            "ice_build_assign_simt", "ice_build_pack", "ice_decode_workspace_bytes", "ice_select_pages",
+            "ice_build_assign_simt", "ice_build_pack", "ice_build_index_reuse", "ice_decode_workspace_bytes",
+            "ice_select_pages",
             "ice_gather_pages", "ice_sparse_attn_decode", "ice_sparse_attn_decode_noalloc", "ice_decode_step",
             "ice_insert_workspace_bytes", "ice_insert_tokens", "ice_host_pool_create", "ice_host_pool_destroy",
             "ice_host_pool_pointers", "ice_host_pool_staging_bytes", "ice_host_pool_gather_h2d"]
@@ -275,6 +277,15 @@ def ice_build_assign_simt(params, K, index, ws, err, stream=None):
 
 def ice_build_pack(params, K, V, index, ws, err, stream=None):
     _build_call("ice_build_pack", params, K, V, index, ws, err, stream)
+
+
+def ice_build_index_reuse(params, K, V, prev, index, ws, err, stream=None):
+    """Build `index` for this layer's K, V on `prev`'s parents, assignment and
+    pages (the inter-layer index reuse)."""
+    px = prev.struct if isinstance(prev, Index) else prev
+    ix = index.struct if isinstance(index, Index) else index
+    _check(load().ice_build_index_reuse(ctypes.byref(params), _ptr(K), _ptr(V), ctypes.byref(px), ctypes.byref(ix),
+                                        _ptr(ws), _nbytes(ws), _ptr(err), _stream(stream)))
 
 
 def ice_insert_workspace_bytes(params: IceParams) -> int:

@@ -279,6 +279,18 @@ ice_status ice_build_index(const ice_params *p, const void *K, const void *V, co
     return ice_build_pack(p, K, V, idx, ws, ws_bytes, err_dev, stream);
 }
 
+ice_status ice_build_index_reuse(const ice_params *p, const void *K, const void *V, const ice_index *prev,
+                                 const ice_index *idx, void *ws, size_t ws_bytes, int32_t *err_dev, void *stream) {
+    BuildWs w;
+    ice_status st = build_common(p, K, idx, ws, ws_bytes, &w);
+    if (st) return st;
+    if ((st = check_index(prev))) return st;
+    if (p->n_tokens > 0 && (!V || !aligned16(V))) return fail(ICE_ERR_INVALID_ARG, "V must be a 16-byte aligned device pointer");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p->n_tokens == 0) return build_empty(p, idx, s);
+    return cuda_status(launch_build_reuse(*p, K, V, *prev, *idx, w, err_dev, s), "ice_build_index_reuse");
+}
+
 // ------------------------------------------------------------- insert ----
 ice_status ice_insert_workspace_bytes(const ice_params *p, size_t *bytes) {
     ice_status st = check_params(p);

@@ -349,7 +349,22 @@ cudaError_t launch_lift_promote_t(const ice_params &p, const void *K, const ice_
     return cudaGetLastError();
 }
 
+template <typename T>
+cudaError_t launch_lift_norms_t(const ice_params &p, const void *K, const BuildWs &ws, cudaStream_t s) {
+    const int tiles = ceil_div(p.n_tokens, kLiftTile);
+    const cudaError_t e = launch_dependent(k_lift_count<T>, dim3(tiles, units_of(p)), dim3(kThreads), 0, s,
+                                           static_cast<const T *>(K), p.n_tokens, p.n_kv_heads, p.promote_thresh,
+                                           promote_key(p.seed, p.layer), ws.norm2, ws.pcount, ws.tile_max,
+                                           ws.tile_min, tiles);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_lift_norms(const ice_params &p, const void *K, const BuildWs &ws, cudaStream_t s) {
+    if (p.dtype == ICE_BF16) return launch_lift_norms_t<__nv_bfloat16>(p, K, ws, s);
+    return launch_lift_norms_t<float>(p, K, ws, s);
+}
 
 cudaError_t launch_lift_promote(const ice_params &p, const void *K, const ice_index &idx, const BuildWs &ws,
                                 int32_t *err, cudaStream_t s) {

@@ -595,7 +595,23 @@ void launch_rank_tiles(const ice_params &p, const ice_index &idx, const BuildWs 
     }
 }
 
+template <typename T>
+cudaError_t launch_copy_t(const ice_params &p, const void *K, const void *V, const ice_index &idx, cudaStream_t s) {
+    const cudaError_t e = launch_dependent(k_pack_copy<T>, dim3(ceil_div(p.page_cap, kThreads / 32), units_of(p)),
+                                           dim3(kThreads), 0, s, static_cast<const T *>(K),
+                                           static_cast<const T *>(V), p.n_tokens, p.page_cap, idx.n_pages,
+                                           idx.page_len, idx.page_tokens, static_cast<T *>(idx.pool_k),
+                                           static_cast<T *>(idx.pool_v));
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_pack_copy(const ice_params &p, const void *K, const void *V, const ice_index &idx,
+                             cudaStream_t s) {
+    if (p.dtype == ICE_BF16) return launch_copy_t<__nv_bfloat16>(p, K, V, idx, s);
+    return launch_copy_t<float>(p, K, V, idx, s);
+}
 
 cudaError_t launch_pack(const ice_params &p, const void *K, const void *V, const ice_index &idx,
                         const BuildWs &ws, int32_t *err, cudaStream_t s) {

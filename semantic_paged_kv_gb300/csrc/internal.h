@@ -81,6 +81,15 @@ cudaError_t launch_assign_tc(const ice_params &p, const void *K, const ice_index
                              int32_t *err, cudaStream_t s);
 cudaError_t launch_pack(const ice_params &p, const void *K, const void *V, const ice_index &idx,
                         const BuildWs &ws, int32_t *err, cudaStream_t s);
+// Pieces of the build used by the reuse build: the squared norms and per-tile
+// maxima of k_lift_count, and the pool scatter k_pack_copy over idx's pages.
+cudaError_t launch_lift_norms(const ice_params &p, const void *K, const BuildWs &ws, cudaStream_t s);
+cudaError_t launch_pack_copy(const ice_params &p, const void *K, const void *V, const ice_index &idx,
+                             cudaStream_t s);
+// Build of a layer on another layer's node structure (parents, assignment,
+// pages): lift of this layer's keys, parent keys, table copies, pool.
+cudaError_t launch_build_reuse(const ice_params &p, const void *K, const void *V, const ice_index &prev,
+                               const ice_index &idx, const BuildWs &ws, int32_t *err, cudaStream_t s);
 cudaError_t launch_select(const ice_params &p, const ice_index &idx, const void *Q, const DecodeWs &ws,
                           int32_t *sel_pages, int32_t *sel_count, int max_sel, int32_t *err, cudaStream_t s);
 // Selection with tensor-core scoring (bf16, g <= 16, k <= 64 pages per head).

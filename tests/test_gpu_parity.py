@@ -265,3 +265,66 @@ def test_invalid_arguments_rejected():
         ice.ice_decode_step(p, idx, Q, 64, buf.sel_pages, buf.sel_count, None, buf.vbuf, buf.buf_len, 0.1, buf.O,
                             buf.ws, err)
     assert ei.value.status == ice.ICE_ERR_INVALID_ARG
+
+
+def _reused_run(run0: GpuRun, layer: int = 1, in_place: bool = False) -> GpuRun:
+    """Layer `layer` built by ice_build_index_reuse on run0's index."""
+    r = object.__new__(GpuRun)
+    r.w, r.layer = run0.w, layer
+    r.cfg = ice.Config(**{**run0.cfg.__dict__, "layer": layer})
+    r.K, r.V = workloads.batch_kv(r.w, layer)
+    dt = r.cfg.torch_dtype
+    r.Kd, r.Vd = to_dev(r.K, dt), to_dev(r.V, dt)
+    r.idx = run0.idx if in_place else ice.Index(r.cfg)
+    r.params = r.cfg.params()
+    r.ws = ice.workspace(ice.ice_build_workspace_bytes(r.params))
+    r.err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ice.ice_build_index_reuse(r.params, r.Kd, r.Vd, run0.idx, r.idx, r.ws, r.err)
+    r.status = ice.ice_check(r.err)
+    r.h = {f: getattr(r.idx, f).float().cpu().numpy() if f == "parent_keys" else getattr(r.idx, f).cpu().numpy()
+           for f in ice.INDEX_FIELDS if f not in ("pool_k", "pool_v")}
+    return r
+
+
+@pytest.mark.parametrize("shape", ["llama_bf16", "tiny_fp32", "in_place"])
+def test_reuse_build_matches_oracle(shape):
+    """ice_build_index_reuse: the next layer on this layer's parents,
+    assignment and pages, against oracle.build_unit_reuse on the oracle's own
+    build of this layer (units whose GPU assignment met an fp32 near-tie are
+    skipped, as the reuse would then start from a different structure), then
+    the decode step over the reused index."""
+    w = W["tiny"] if shape == "tiny_fp32" else W["llama31_8b_16k"].scaled(n_tokens=4003, batch=2, n_q_heads=8,
+                                                                          n_kv_heads=2)
+    run0 = GpuRun(w)
+    assert run0.status == ice.ICE_OK
+    h0 = {k: v.copy() for k, v in run0.h.items()}
+    run1 = _reused_run(run0, in_place=shape == "in_place")
+    assert run1.status == ice.ICE_OK
+    th = oracle.promote_threshold(w.promote_p)
+    N, checked = w.n_tokens, 0
+    for u in range(run1.cfg.units):
+        b, h = run1.unit(u)
+        prev = oracle.build_unit(run0.K[b, h], run0.V[b, h], seed=w.seed, layer=0, seq=b, head=h, thresh=th)
+        if not np.array_equal(h0["token_parent"][u, :N], prev["token_parent"]):
+            continue
+        ref = oracle.build_unit_reuse(run1.K[b, h], run1.V[b, h], prev)
+        H, Np, P = run1.h, len(ref["parent_tok"]), int(ref["n_pages"])
+        assert int(H["n_parents"][u]) == Np and int(H["n_pages"][u]) == P and int(H["n_indexed"][u]) == N
+        assert np.array_equal(H["parent_tok"][u, :Np], ref["parent_tok"])
+        assert np.array_equal(H["token_parent"][u, :N], ref["token_parent"])
+        for f in ("page_parent", "page_len", "page_tokens"):
+            assert np.array_equal(H[f][u, :P], ref[f]), f
+        assert np.array_equal(H["token_page"][u, :N], ref["token_page"])
+        assert np.array_equal(H["token_slot"][u, :N], ref["token_slot"])
+        assert abs(H["m2"][u] - ref["M2"]) <= 1e-12 * ref["M2"]
+        assert np.allclose(H["parent_e"][u, :Np], ref["parent_e"], rtol=2e-7, atol=2e-7 * np.sqrt(ref["M2"]))
+        assert np.array_equal(H["parent_keys"][u, :Np], ref["parent_keys"].astype(np.float32))
+        pk, pv = run1.pool(u)
+        assert np.array_equal(pk, ref["pool_k"].astype(np.float32)) and np.array_equal(pv, ref["pool_v"].astype(np.float32))
+        checked += 1
+    assert checked >= run1.cfg.units - 1
+    for bgt in (64, 256):
+        Q, buf, st = run1.decode(bgt)
+        assert st == ice.ICE_OK
+        for u in range(run1.cfg.units):
+            check_decode_unit(run1, u, Q, bgt, buf)
