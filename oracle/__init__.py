@@ -242,6 +242,88 @@ def build_unit(K, V, *, seed: int, layer: int, seq: int, head: int, thresh: int,
                 pool_k=pool_k, pool_v=pool_v, S=S, **pk)
 
 
+# ------------------------------------------- sink and recent-window pages ----
+def positional_split(N: int, n_sink: int, n_window: int) -> tuple[int, int]:
+    """(sink_end, window_start) of a build over N tokens.  The article's
+    section 六 splits the tokens into the first few anchor (sink) tokens, the
+    window of the newest tokens, and everything in between; the sink and
+    window stay resident and only the middle goes into the index.  Sink =
+    [0, sink_end), window = [window_start, N), middle = [sink_end,
+    window_start); a window reaching into the sink is cut at the sink."""
+    se = min(max(n_sink, 0), N)
+    return se, max(se, N - max(n_window, 0))
+
+
+def positional_pages(N: int, n_sink: int, n_window: int, S: int = 16) -> int:
+    se, ws = positional_split(N, n_sink, n_window)
+    return -(-se // S) + -(-(N - ws) // S)
+
+
+def promote_range(seed: int, layer: int, seq: int, head: int, lo: int, hi: int, thresh: int) -> np.ndarray:
+    """Promotion restricted to the tokens [lo, hi) (article section 三's random
+    promotion, over the indexed tokens only): token j is promoted iff its
+    draw is below thresh; if none is, the token of smallest draw (lowest j
+    on ties) is.  Token ids stay absolute."""
+    d = np.array([promote_draw(seed, layer, seq, head, j) for j in range(lo, hi)], np.int64)
+    if hi <= lo:
+        return np.zeros(0, np.int32)
+    out = np.nonzero(d < thresh)[0]
+    if len(out) == 0:
+        out = np.array([int(np.argmin(d))])
+    return (out + lo).astype(np.int32)
+
+
+def build_unit_positional(K, V, *, seed: int, layer: int, seq: int, head: int, thresh: int, S: int = 16,
+                          n_sink: int = 0, n_window: int = 0) -> dict:
+    """Build of one unit whose first n_sink and last n_window tokens are kept
+    as positional pages (article section 六: the anchor and window pages stay
+    on the GPU, only the middle tokens are managed by the index).  The middle
+    tokens go through the steps of build_unit (lift with M over the middle,
+    promotion among the middle, nearest parent, pack); the sink tokens then
+    fill pages P_sem .. in chunks of S in token order, and the window tokens
+    the pages after them.  Positional pages have no parent (-1) and their
+    tokens token_parent -2."""
+    K = _f64(K)
+    V = _f64(V)
+    N = K.shape[0]
+    se, ws = positional_split(N, n_sink, n_window)
+    Km = K[se:ws]
+    n_m, M2, e_m = lift(Km) if ws > se else (np.zeros(0), 0.0, np.zeros(0))
+    parent_tok = promote_range(seed, layer, seq, head, se, ws, thresh)
+    Np = len(parent_tok)
+    tp_mid = assign(Km, e_m, parent_tok - se) if Np else np.zeros(0, np.int32)
+    pk = pack(tp_mid, Np, S) if ws > se else dict(n_pages=0, page_parent=np.zeros(0, np.int32),
+                                                   page_len=np.zeros(0, np.int32),
+                                                   page_tokens=np.zeros((0, S), np.int32),
+                                                   token_page=np.zeros(0, np.int32), token_slot=np.zeros(0, np.int32))
+    P_sem = pk["n_pages"]
+    sem_tokens = np.where(pk["page_tokens"] >= 0, pk["page_tokens"] + se, -1)
+    ranges = [(a, min(a + S, se)) for a in range(0, se, S)] + [(a, min(a + S, N)) for a in range(ws, N, S)]
+    pos_tokens = np.full((len(ranges), S), -1, np.int32)
+    for i, (a, b) in enumerate(ranges):
+        pos_tokens[i, : b - a] = np.arange(a, b)
+    page_tokens = np.concatenate([sem_tokens.astype(np.int32), pos_tokens]).astype(np.int32)
+    P = P_sem + len(ranges)
+    page_parent = np.concatenate([pk["page_parent"], np.full(len(ranges), -1, np.int32)]).astype(np.int32)
+    page_len = np.concatenate([pk["page_len"], np.array([b - a for a, b in ranges], np.int32)]).astype(np.int32)
+    token_parent = np.full(N, -2, np.int32)
+    token_parent[se:ws] = tp_mid
+    token_page = np.full(N, -1, np.int32)
+    token_slot = np.full(N, -1, np.int32)
+    for p in range(P):
+        for sl in range(S):
+            t = page_tokens[p, sl]
+            if t >= 0:
+                token_page[t], token_slot[t] = p, sl
+    pool_k, pool_v = scatter(K, V, page_tokens, S)
+    e = np.full(N, np.nan)
+    e[se:ws] = e_m
+    return dict(n=n_m, M2=M2, e=e, parent_tok=parent_tok, parent_keys=K[parent_tok] if Np else K[:0],
+                parent_e=e[parent_tok] if Np else e[:0], token_parent=token_parent, pool_k=pool_k, pool_v=pool_v,
+                S=S, n_pages=P, n_pos=len(ranges), page_parent=page_parent, page_len=page_len,
+                page_tokens=page_tokens, token_page=token_page, token_slot=token_slot)
+
+
 def build_unit_reuse(K, V, prev: dict, S: int = 16) -> dict:
     """Build of one unit on another layer's node structure (the inter-layer
     index reuse of the article's section 五, "IceCache (reuse)"; its mechanism
@@ -269,7 +351,11 @@ def decode_unit(idx: dict, q, budget_tokens: int, scale: float | None = None) ->
     """Decode steps a6-a10 for one unit and its g query heads."""
     S = idx["S"]
     k_pages = -(-budget_tokens // S)
-    head_pages, sel = select(q, idx["parent_keys"], idx["page_parent"], k_pages)
+    n_pos = int(idx.get("n_pos", 0))  # positional (sink / window) pages: the last n_pos, always attended
+    P_sem = int(idx["n_pages"]) - n_pos
+    head_pages, sel = select(q, idx["parent_keys"], idx["page_parent"][:P_sem], k_pages)
+    if n_pos:
+        sel = np.concatenate([sel, np.arange(P_sem, P_sem + n_pos, dtype=np.int32)]).astype(np.int32)
     kb, vb, bl = gather(idx["pool_k"], idx["pool_v"], idx["page_len"], sel)
     out = attention(q, kb, vb, bl, scale)
     return dict(head_pages=head_pages, sel_pages=sel, kbuf=kb, vbuf=vb, buf_len=bl, out=out)

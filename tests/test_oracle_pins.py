@@ -419,3 +419,97 @@ def test_reuse_full_budget_is_dense_attention_of_this_layer():
     vt = torch.from_numpy(V1.astype(np.float64))[None, None].expand(1, q.shape[0], -1, -1)
     ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt)[0, :, 0].numpy()
     assert np.max(np.abs(dec["out"] - ref)) < 1e-12
+
+
+# ------------------------------------------------- sink and window pages
+def _pos_unit(N=900, n_sink=40, n_window=70, seed_layer=0, **kw):
+    w = workloads.WORKLOADS["llama31_8b_16k"].scaled(n_tokens=N, centres=24, dtype="fp32", **kw)
+    th = oracle.promote_threshold(w.promote_p)
+    K, V = workloads.unit_kv(w, seed_layer, 0, 0)
+    idx = oracle.build_unit_positional(K, V, seed=w.seed, layer=seed_layer, seq=0, head=0, thresh=th,
+                                       n_sink=n_sink, n_window=n_window)
+    return w, th, K, V, idx
+
+
+def test_positional_build_without_sink_or_window_is_the_plain_build():
+    w, th, K, V, idx = _pos_unit(n_sink=0, n_window=0)
+    ref = oracle.build_unit(K, V, seed=w.seed, layer=0, seq=0, head=0, thresh=th)
+    for f in ("parent_tok", "token_parent", "page_parent", "page_len", "page_tokens", "token_page", "token_slot",
+              "parent_keys", "pool_k", "pool_v"):
+        assert np.array_equal(np.asarray(idx[f]), np.asarray(ref[f])), f
+    assert idx["n_pages"] == ref["n_pages"] and idx["n_pos"] == 0 and idx["M2"] == ref["M2"]
+
+
+@pytest.mark.parametrize("n_sink,n_window", [(40, 70), (16, 0), (0, 33), (5, 1)])
+def test_positional_pages_are_sequential_and_the_middle_is_indexed(n_sink, n_window):
+    N, S = 900, 16
+    w, th, K, V, idx = _pos_unit(N=N, n_sink=n_sink, n_window=n_window)
+    se, ws = n_sink, N - n_window
+    P, n_pos = idx["n_pages"], idx["n_pos"]
+    assert n_pos == -(-n_sink // S) + -(-n_window // S)
+    P_sem = P - n_pos
+    # positional pages: textbook sequential paging of the sink, then of the window
+    want = [np.arange(a, min(a + S, se)) for a in range(0, se, S)] + [np.arange(a, min(a + S, N)) for a in range(ws, N, S)]
+    for i, toks in enumerate(want):
+        p = P_sem + i
+        assert idx["page_parent"][p] == -1 and idx["page_len"][p] == len(toks)
+        assert np.array_equal(idx["page_tokens"][p][: len(toks)], toks) and np.all(idx["page_tokens"][p][len(toks):] == -1)
+    # promotion: exactly the middle tokens the plain promotion over all N picks
+    full = oracle.promote(w.seed, 0, 0, 0, N, th)
+    mid = full[(full >= se) & (full < ws)]
+    if len(mid):
+        assert np.array_equal(idx["parent_tok"], mid)
+    # M is the middle's largest norm; every middle token's parent is its nearest promoted point
+    Km = K[se:ws].astype(np.float64)
+    assert abs(idx["M2"] - np.einsum("ij,ij->i", Km, Km).max()) <= 1e-14 * idx["M2"]
+    assert np.all(idx["token_parent"][:se] == -2) and np.all(idx["token_parent"][ws:] == -2)
+    tp = idx["token_parent"][se:ws]
+    pk = K[idx["parent_tok"]].astype(np.float64)
+    M2 = idx["M2"]
+    e_m = np.sqrt(np.maximum(0.0, M2 - np.einsum("ij,ij->i", Km, Km)))
+    e_p = np.sqrt(np.maximum(0.0, M2 - np.einsum("ij,ij->i", pk, pk)))
+    d2 = ((Km[:, None, :] - pk[None, :, :]) ** 2).sum(-1) + (e_m[:, None] - e_p[None, :]) ** 2
+    best = d2.min(1)
+    assert np.all(d2[np.arange(len(tp)), tp] <= best + 1e-9 * M2)
+    # every token in exactly one page
+    seen = np.zeros(N, int)
+    for p in range(P):
+        for sl, t in enumerate(idx["page_tokens"][p]):
+            if t >= 0:
+                seen[t] += 1
+                assert idx["token_page"][t] == p and idx["token_slot"][t] == sl
+    assert np.all(seen == 1)
+    assert np.all(idx["page_parent"][:P_sem] >= 0)
+
+
+@pytest.mark.parametrize("n_sink,n_window", [(40, 70), (900, 0), (500, 500)])
+def test_positional_full_budget_is_dense_attention(n_sink, n_window):
+    """Every page selected (or no middle at all): dense softmax attention over
+    all N tokens (torch SDPA, float64)."""
+    w, th, K, V, idx = _pos_unit(N=900, n_sink=n_sink, n_window=n_window)
+    q = workloads.unit_queries(w, 0, 0, 0)
+    dec = oracle.decode_unit(idx, q, budget_tokens=16 * max(1, idx["n_pages"]))
+    assert len(dec["sel_pages"]) == idx["n_pages"]
+    qt = torch.from_numpy(q.astype(np.float64))[None, :, None, :]
+    kt = torch.from_numpy(K.astype(np.float64))[None, None].expand(1, q.shape[0], -1, -1)
+    vt = torch.from_numpy(V.astype(np.float64))[None, None].expand(1, q.shape[0], -1, -1)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt)[0, :, 0].numpy()
+    assert np.max(np.abs(dec["out"] - ref)) < 1e-12
+
+
+def test_positional_small_budget_attends_sink_window_and_selected_pages():
+    """A small budget: the union is the selected middle pages plus every
+    sink and window page, and attention equals SDPA over exactly those tokens."""
+    w, th, K, V, idx = _pos_unit(N=900, n_sink=20, n_window=50)
+    q = workloads.unit_queries(w, 0, 0, 0)
+    dec = oracle.decode_unit(idx, q, budget_tokens=32)
+    P, n_pos = idx["n_pages"], idx["n_pos"]
+    sel = dec["sel_pages"]
+    assert np.all(np.diff(sel) > 0) and set(range(P - n_pos, P)) <= set(sel.tolist())
+    toks = np.concatenate([idx["page_tokens"][p][idx["page_tokens"][p] >= 0] for p in sel])
+    assert set(range(20)) <= set(toks.tolist()) and set(range(850, 900)) <= set(toks.tolist())
+    qt = torch.from_numpy(q.astype(np.float64))[None, :, None, :]
+    kt = torch.from_numpy(K[toks].astype(np.float64))[None, None].expand(1, q.shape[0], -1, -1)
+    vt = torch.from_numpy(V[toks].astype(np.float64))[None, None].expand(1, q.shape[0], -1, -1)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt)[0, :, 0].numpy()
+    assert np.max(np.abs(dec["out"] - ref)) < 1e-12
