@@ -73,7 +73,28 @@ typedef struct ice_params {
     int32_t np_cap;         /* parent capacity per unit */
     int32_t page_cap;       /* page capacity per unit */
     int32_t n_cap;          /* token capacity per unit (>= n_tokens; room for inserts) */
+    int32_t n_sink;         /* first n_sink tokens kept as positional pages ([B] section 六) */
+    int32_t n_window;       /* last n_window tokens of the build kept as positional pages */
 } ice_params;
+
+/*
+ * Sink and recent-window pages ([B] section 六: the anchor tokens at the start
+ * and the window of newest tokens stay resident on the GPU; only the tokens in
+ * between are managed by the index).  With n_sink or n_window > 0 a build over
+ * N tokens indexes only the middle tokens [sink_end, window_start), where
+ * sink_end = min(n_sink, N) and window_start = max(sink_end, N - n_window):
+ * M^2, the promotion and the nearest parent are taken over the middle only.
+ * After the middle's semantic pages, the sink tokens fill positional pages in
+ * token order, S per page, and then the window tokens; these pages have
+ * page_parent -1 and their tokens token_parent -2.  Every decode step attends
+ * over all positional pages (the last ice_positional_pages(...) pages of the
+ * unit) besides the budget's selected pages, so max_sel must cover both, and
+ * page_cap must hold the positional pages besides ice_page_bound of the
+ * middle.  Incremental insert is not supported with positional pages.
+ */
+/* The positional page count of a unit: ceil(sink_end / S) +
+ * ceil((N - window_start) / S) (0 when n_sink = n_window = 0). */
+int32_t ice_positional_pages(int32_t n_tokens, int32_t n_sink, int32_t n_window, int32_t page_size);
 
 /*
  * Device arrays of one layer's index, all caller-owned.  U = B * Hkv units.

@@ -38,7 +38,8 @@ class IceParams(ctypes.Structure):
                 ("head_dim", ctypes.c_int32), ("n_tokens", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("n_levels", ctypes.c_int32), ("promote_thresh", ctypes.c_uint64),
                 ("seed", ctypes.c_uint64), ("layer", ctypes.c_int32), ("np_cap", ctypes.c_int32),
-                ("page_cap", ctypes.c_int32), ("n_cap", ctypes.c_int32)]
+                ("page_cap", ctypes.c_int32), ("n_cap", ctypes.c_int32), ("n_sink", ctypes.c_int32),
+                ("n_window", ctypes.c_int32)]
 
 
 INDEX_FIELDS = ["n_parents", "n_pages", "n_indexed", "m2", "parent_tok", "parent_keys", "parent_e", "parent_corr",
@@ -70,6 +71,7 @@ def load() -> ctypes.CDLL:
         "ice_version": ([], ctypes.c_char_p),
         "ice_check": ([P, P], i32),
         "ice_page_bound": ([i32, i32, i32], i32),
+        "ice_positional_pages": ([i32, i32, i32, i32], i32),
         "ice_build_workspace_bytes": ([pp, ctypes.POINTER(sz)], i32),
         "ice_build_index": ([pp, P, P, pi, P, sz, P, P], i32),
         "ice_build_lift_promote": ([pp, P, pi, P, sz, P, P], i32),
@@ -100,7 +102,7 @@ def load() -> ctypes.CDLL:
 
 
 def exported_symbols() -> list[str]:
-    return ["ice_status_string", "ice_last_error", "ice_version", "ice_check", "ice_page_bound",
+    return ["ice_status_string", "ice_last_error", "ice_version", "ice_check", "ice_page_bound", "ice_positional_pages",
             "ice_build_workspace_bytes", "ice_build_index", "ice_build_lift_promote", "ice_build_assign",
             "ice_build_assign_simt", "ice_build_pack", "ice_build_index_reuse", "ice_decode_workspace_bytes",
             "ice_select_pages",
@@ -153,6 +155,8 @@ class Config:
     head_dim: int = HEAD_DIM
     page_size: int = PAGE_SIZE
     n_levels: int = 2
+    n_sink: int = 0    # first tokens kept as positional pages (not indexed)
+    n_window: int = 0  # last tokens of the build kept as positional pages (not indexed)
 
     def __post_init__(self):
         N, p = self.n_tokens, self.promote_p
@@ -164,7 +168,12 @@ class Config:
             mu = self.n_cap * p
             self.np_cap = max(1, min(self.n_cap, int(mu + 8 * math.sqrt(mu * (1 - p) + 1) + 16)))
         if self.page_cap is None:
-            self.page_cap = max(1, ice_page_bound(self.n_cap, self.np_cap, self.page_size))
+            self.page_cap = max(1, ice_page_bound(self.n_cap, self.np_cap, self.page_size) + self.n_pos)
+
+    @property
+    def n_pos(self) -> int:
+        """Positional (sink and window) pages of a unit."""
+        return int(load().ice_positional_pages(self.n_tokens, self.n_sink, self.n_window, self.page_size))
 
     @property
     def group(self) -> int:
@@ -181,7 +190,7 @@ class Config:
     def params(self) -> IceParams:
         return IceParams(self.batch, self.n_q_heads, self.n_kv_heads, self.head_dim, self.n_tokens, self.page_size,
                          self.dtype, self.n_levels, promote_threshold(self.promote_p), self.seed, self.layer,
-                         self.np_cap, self.page_cap, self.n_cap)
+                         self.np_cap, self.page_cap, self.n_cap, self.n_sink, self.n_window)
 
 
 class Index:
@@ -398,7 +407,7 @@ def workspace(nbytes: int, device="cuda") -> torch.Tensor:
 
 def max_selected(cfg: Config, budget_tokens: int) -> int:
     k = -(-budget_tokens // cfg.page_size)
-    return max(1, min(cfg.group * k, cfg.page_cap))
+    return max(1, min(cfg.group * k + cfg.n_pos, cfg.page_cap))
 
 
 class DecodeBuffers:

@@ -54,6 +54,7 @@ ice_status check_params(const ice_params *p) {
     if (p->np_cap < 1 || p->page_cap < 1) return fail(ICE_ERR_INVALID_ARG, "np_cap and page_cap must be >= 1");
     if ((long long)p->np_cap * p->n_kv_heads * p->batch > (1ll << 40))
         return fail(ICE_ERR_INVALID_ARG, "capacities too large");
+    if (p->n_sink < 0 || p->n_window < 0) return fail(ICE_ERR_INVALID_ARG, "n_sink and n_window must be >= 0");
     return ICE_OK;
 }
 
@@ -183,6 +184,15 @@ const char *ice_last_error(void) { return g_last_error.c_str(); }
 
 const char *ice_version(void) { return "icecache-gb300 0.1 (sm_103a)"; }
 
+int32_t ice_positional_pages(int32_t n_tokens, int32_t n_sink, int32_t n_window, int32_t page_size) {
+    if (n_tokens < 0 || n_sink < 0 || n_window < 0 || page_size != kPage) return -1;
+    ice_params p{};
+    p.n_tokens = n_tokens;
+    p.n_sink = n_sink;
+    p.n_window = n_window;
+    return pos_split(p).n_pos;
+}
+
 int32_t ice_page_bound(int32_t n_tokens, int32_t n_parents, int32_t page_size) {
     if (n_tokens < 0 || n_parents < 0 || page_size <= 0) return -1;
     // the page count is an integer, so the floor of the bound holds too
@@ -307,6 +317,8 @@ ice_status ice_insert_tokens(const ice_params *p, const ice_index *idx, const vo
     if ((st = check_index(idx))) return st;
     if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))
         return fail(ICE_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned device pointers");
+    if (p->n_sink > 0 || p->n_window > 0)
+        return fail(ICE_ERR_UNSUPPORTED, "incremental insert is not supported with sink or window pages");
     const InsertWs w = insert_ws_layout(*p, ws);
     if ((st = check_ws(ws, ws_bytes, w.bytes))) return st;
     return cuda_status(launch_insert(*p, *idx, k_new, v_new, w, err_dev, static_cast<cudaStream_t>(stream)),
@@ -339,9 +351,11 @@ static ice_status select_checks(const ice_params *p, const ice_index *idx, const
     if (st) return st;
     if (!Q || !sel_pages || !sel_count) return fail(ICE_ERR_INVALID_ARG, "Q, sel_pages and sel_count must be non-NULL");
     const long long g = p->n_q_heads / p->n_kv_heads;
-    const long long need = g * (long long)k_pages_of(budget_tokens);
+    const long long need = g * (long long)k_pages_of(budget_tokens) + pos_split(*p).n_pos;
     const long long want = need < p->page_cap ? need : p->page_cap;
-    if (max_sel < want) return fail(ICE_ERR_INVALID_ARG, "max_sel (%d) must be >= min(g * k, page_cap) = %lld", max_sel, want);
+    if (max_sel < want)
+        return fail(ICE_ERR_INVALID_ARG, "max_sel (%d) must be >= min(g * k + positional pages, page_cap) = %lld",
+                    max_sel, want);
     int dev = 0, optin = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);

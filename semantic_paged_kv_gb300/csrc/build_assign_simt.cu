@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kThreads) k_assign_simt(const T *__restrict__ 
         const long long j = r0 + warp * kRowsPerWarp + r;
         if (lane == 0 && j < N && Np > 0) {
             int32_t *tp = token_parent + (size_t)u * n_cap + j;
-            if (*tp < 0) *tp = bi;  // promoted tokens keep themselves
+            if (*tp == -1) *tp = bi;  // promoted tokens keep themselves, sink / window tokens (-2) stay out
         }
     }
 }

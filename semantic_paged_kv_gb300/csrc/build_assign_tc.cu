@@ -220,11 +220,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = q * 32 + lane;
         int gt = 0;
         Item I = blockIdx.x < n_items ? item_of(blockIdx.x, mt_per_unit, n_parents, np_cap) : Item{0, 0, 0, 0};
-        int r_tp = -1;  // token_parent seed of this row (>= 0: promoted, keeps itself)
+        int r_tp = -1;  // token_parent seed of this row (-1: to assign; >= 0 promoted, -2 sink / window: kept)
         if (blockIdx.x < n_items && (long long)I.m0 + row < N) r_tp = token_parent[(size_t)I.u * n_cap + I.m0 + row];
         for (int item = blockIdx.x; item < n_items; item += G) {
             const long long j = (long long)I.m0 + row;
-            const bool promoted = r_tp >= 0;
+            const bool keep = r_tp != -1;
             // the next item's row data, loaded while this item runs
             const int nitem = item + G;
             const Item In = nitem < n_items ? item_of(nitem, mt_per_unit, n_parents, np_cap) : Item{0, 0, 0, 0};
@@ -294,8 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         bidx = oi;
                     }
                 }
-                // promoted tokens keep themselves as parent
-                if (ok && j < N && I.Np > 0 && !promoted) token_parent[(size_t)I.u * n_cap + j] = bidx;
+                // promoted tokens keep themselves as parent, sink / window tokens stay outside the index
+                if (ok && j < N && I.Np > 0 && !keep) token_parent[(size_t)I.u * n_cap + j] = bidx;
             }
             asm volatile("bar.sync 2, %0;" ::"r"(kEpiThreads) : "memory");
             I = In;

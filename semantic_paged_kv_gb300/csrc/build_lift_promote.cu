@@ -139,8 +139,8 @@ __device__ __forceinline__ void write_lifted(float e, uint4 *tok_row, uint4 *par
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 3) k_lift_count(const T *__restrict__ K, int N, int n_kv_heads,
-                                                         uint64_t thresh, uint64_t key,
+__global__ void __launch_bounds__(kThreads, 3) k_lift_count(const T *__restrict__ K, int N, int lo, int hi,
+                                                         int n_kv_heads, uint64_t thresh, uint64_t key,
                                                          double *__restrict__ norm2, int32_t *__restrict__ pcount,
                                                          double *__restrict__ tile_max,
                                                          unsigned long long *__restrict__ tile_min, int n_tiles) {
@@ -158,16 +158,17 @@ __global__ void __launch_bounds__(kThreads, 3) k_lift_count(const T *__restrict_
     float mine_hi, mine_lo;  // lane s*8 + t keeps token s*8 + t's norm
     norms32<T>(buf, lane, mine_hi, mine_lo);
     const long long j = wt0 + lane;
+    const bool mid = j >= lo && j < hi;  // indexed tokens (not sink or window)
     double wmax = 0.0;  // one conversion per token: the fp64 units are few
     if (j < N) {
         const double n = (double)mine_hi + (double)mine_lo;
         norm2[(size_t)u * N + j] = n;
-        wmax = n;
+        wmax = mid ? n : 0.0;
     }
     // ---- promotion draw of this thread's token
     int cnt = 0;
     unsigned long long best = ~0ull;
-    if (j < N) {
+    if (mid) {
         const uint32_t d = promote_draw(key, seq, head, (uint32_t)j, 1u);
         cnt = ((uint64_t)d < thresh);
         best = ((unsigned long long)d << 32) | (unsigned long long)j;
@@ -206,7 +207,8 @@ __global__ void __launch_bounds__(kThreads, 3) k_lift_count(const T *__restrict_
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) k_promote_write(
-    const T *__restrict__ K, int N, int n_kv_heads, uint64_t thresh, uint64_t key, int np_cap, int n_cap,
+    const T *__restrict__ K, int N, int lo, int hi, int n_kv_heads, uint64_t thresh, uint64_t key, int np_cap,
+    int n_cap,
     double *__restrict__ m2, const double *__restrict__ norm2, const int32_t *__restrict__ pcount,
     const double *__restrict__ tile_max, const unsigned long long *__restrict__ tile_min, int n_tiles,
     int32_t *__restrict__ n_parents,
@@ -229,7 +231,8 @@ __global__ void __launch_bounds__(kThreads) k_promote_write(
     // on the unit's totals, so their loads overlap the reduction below
     const long long j = t0 + threadIdx.x;
     const double n2 = j < N ? norm2[(size_t)u * N + j] : 0.0;
-    const bool drawn = j < N && (uint64_t)promote_draw(key, seq, head, (uint32_t)j, 1u) < thresh;
+    const bool mid = j >= lo && j < hi;  // indexed tokens (not sink or window)
+    const bool drawn = mid && (uint64_t)promote_draw(key, seq, head, (uint32_t)j, 1u) < thresh;
     // the unit's tile values: counts before this tile and in all, M^2, smallest draw
     int before = 0, all = 0;
     double mx = 0.0;
@@ -267,7 +270,7 @@ __global__ void __launch_bounds__(kThreads) k_promote_write(
         minpack = s_pmin[w] < minpack ? s_pmin[w] : minpack;
     }
     // No token promoted: the smallest draw (lowest token on ties) is.
-    const bool fallback = (s_total == 0 && N > 0);
+    const bool fallback = (s_total == 0 && hi > lo);
     const long long jmin = fallback ? (long long)(minpack & 0xFFFFFFFFull) : -1;
     const int total = fallback ? 1 : s_total;
     const int base = fallback ? 0 : s_base;
@@ -278,7 +281,7 @@ __global__ void __launch_bounds__(kThreads) k_promote_write(
         m2[u] = M2;
     }
 
-    const bool f = (j < N) && (fallback ? (j == jmin) : drawn);
+    const bool f = mid && (fallback ? (j == jmin) : drawn);
     const unsigned bal = __ballot_sync(0xffffffffu, f);
     if (lane == 0) s_warp[warp] = __popc(bal);
     __syncthreads();
@@ -287,7 +290,7 @@ __global__ void __launch_bounds__(kThreads) k_promote_write(
     const int local = woff + __popc(bal & lanemask_lt());
     const int m = base + local;
     if (j < N) {
-        int32_t tp = -1;
+        int32_t tp = mid ? -1 : -2;  // -2: a sink or window token, packed by position
         // M^2 - |k|^2 is exact in fp64 to ~2^-52 M^2; rounded to fp32, its
         // square root is within 1.5 ulp of the exact e (fp32 sqrt: the fp64
         // units are few on this part)
@@ -329,16 +332,19 @@ cudaError_t launch_lift_promote_t(const ice_params &p, const void *K, const ice_
     const int N = p.n_tokens;
     const int tiles = ceil_div(N, kLiftTile);
     const uint64_t key = promote_key(p.seed, p.layer);
+    const PosSplit ps = pos_split(p);
     dim3 grid(tiles, U);
     {
         const cudaError_t e_ = launch_dependent(k_lift_count<T>, dim3(grid), dim3(kThreads), 0, s,
-                                                static_cast<const T *>(K), N, p.n_kv_heads, p.promote_thresh, key,
+                                                static_cast<const T *>(K), N, ps.lo, ps.hi, p.n_kv_heads,
+                                                p.promote_thresh, key,
                                                 ws.norm2, ws.pcount, ws.tile_max, ws.tile_min, tiles);
         if (e_ != cudaSuccess) return e_;
     }
     {
         const cudaError_t e_ = launch_dependent(k_promote_write<T>, dim3(grid), dim3(kThreads), 0, s,
-                                                static_cast<const T *>(K), N, p.n_kv_heads, p.promote_thresh, key,
+                                                static_cast<const T *>(K), N, ps.lo, ps.hi, p.n_kv_heads,
+                                                p.promote_thresh, key,
                                                 p.np_cap, p.n_cap, idx.m2, ws.norm2, ws.pcount, ws.tile_max,
                                                 ws.tile_min, tiles, idx.n_parents, idx.n_indexed, idx.parent_tok,
                                                 static_cast<T *>(idx.parent_keys), idx.parent_e, idx.parent_corr,
@@ -352,8 +358,10 @@ cudaError_t launch_lift_promote_t(const ice_params &p, const void *K, const ice_
 template <typename T>
 cudaError_t launch_lift_norms_t(const ice_params &p, const void *K, const BuildWs &ws, cudaStream_t s) {
     const int tiles = ceil_div(p.n_tokens, kLiftTile);
+    const PosSplit ps = pos_split(p);
     const cudaError_t e = launch_dependent(k_lift_count<T>, dim3(tiles, units_of(p)), dim3(kThreads), 0, s,
-                                           static_cast<const T *>(K), p.n_tokens, p.n_kv_heads, p.promote_thresh,
+                                           static_cast<const T *>(K), p.n_tokens, ps.lo, ps.hi, p.n_kv_heads,
+                                           p.promote_thresh,
                                            promote_key(p.seed, p.layer), ws.norm2, ws.pcount, ws.tile_max,
                                            ws.tile_min, tiles);
     return e != cudaSuccess ? e : cudaGetLastError();

@@ -525,6 +525,49 @@ __global__ void __launch_bounds__(kThreads) k_pack_copy(const T *__restrict__ K,
     }
 }
 
+// Positional pages after the unit's semantic pages: the sink tokens [0, lo)
+// in order, S per page, then the window tokens [hi, N) (IceCache popular-
+// science article, section 六: anchor and window tokens stay resident, only
+// the middle is indexed).  Page parent -1, page_next -1.
+__global__ void __launch_bounds__(kThreads) k_pack_positional(int N, int lo, int hi, int page_cap, int n_cap,
+                                                              int32_t *__restrict__ n_pages,
+                                                              int32_t *__restrict__ page_parent,
+                                                              int32_t *__restrict__ page_len,
+                                                              int32_t *__restrict__ page_next,
+                                                              int32_t *__restrict__ page_tokens,
+                                                              int32_t *__restrict__ token_page,
+                                                              int32_t *__restrict__ token_slot,
+                                                              int32_t *__restrict__ err) {
+    dep_wait();  // the semantic pages are complete
+    const int u = blockIdx.x;
+    const int ns = (lo + kPage - 1) / kPage, npos = ns + (N - hi + kPage - 1) / kPage;
+    const int P_sem = min(n_pages[u], page_cap);
+    __syncthreads();  // every thread has the semantic count before it grows
+    if (threadIdx.x == 0) {
+        if (P_sem + npos > page_cap) set_err(err, ICE_ERR_CAPACITY);
+        n_pages[u] = min(P_sem + npos, page_cap);
+    }
+    for (int x = threadIdx.x; x < npos * kPage; x += kThreads) {
+        const int i = x / kPage, sl = x % kPage;
+        const int pg = P_sem + i;
+        if (pg >= page_cap) break;
+        const int a = i < ns ? i * kPage : hi + (i - ns) * kPage;  // first token of the page
+        const int e = i < ns ? lo : N;                            // end of its range
+        const int tok = a + sl < e ? a + sl : -1;
+        const size_t gp = (size_t)u * page_cap + pg;
+        page_tokens[gp * kPage + sl] = tok;
+        if (sl == 0) {
+            page_parent[gp] = -1;
+            page_len[gp] = min(kPage, e - a);
+            page_next[gp] = -1;
+        }
+        if (tok >= 0) {
+            token_page[(size_t)u * n_cap + tok] = pg;
+            token_slot[(size_t)u * n_cap + tok] = sl;
+        }
+    }
+}
+
 void launch_rank_tiles(const ice_params &p, const ice_index &idx, const BuildWs &ws, int32_t *err, cudaStream_t s);
 
 template <typename T>
@@ -549,6 +592,14 @@ cudaError_t launch_t(const ice_params &p, const void *K, const void *V, const ic
         }
     } else {
         launch_rank_tiles(p, idx, ws, err, s);
+    }
+    const PosSplit ps = pos_split(p);
+    if (ps.n_pos > 0) {
+        const cudaError_t e_ = launch_dependent(k_pack_positional, dim3(U), dim3(kThreads), 0, s, p.n_tokens, ps.lo,
+                                                ps.hi, p.page_cap, p.n_cap, idx.n_pages, idx.page_parent,
+                                                idx.page_len, idx.page_next, idx.page_tokens, idx.token_page,
+                                                idx.token_slot, err);
+        if (e_ != cudaSuccess) return e_;
     }
     dim3 cgrid(ceil_div(p.page_cap, kThreads / 32), U);
     {

@@ -107,7 +107,7 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT) k_decode_cluste
     const int32_t *__restrict__ page_next, const int32_t *__restrict__ page_len, const T *__restrict__ pool_k,
     const T *__restrict__ pool_v, int32_t *__restrict__ sel_pages, int32_t *__restrict__ sel_count, int max_sel,
     T *__restrict__ kbuf, T *__restrict__ vbuf, int32_t *__restrict__ buf_len, float scale, float *__restrict__ O,
-    int32_t *__restrict__ err) {
+    int n_pos, int32_t *__restrict__ err) {
     cg::cluster_group cluster = cg::this_cluster();
     const int r = (int)cluster.block_rank();
     const int u = blockIdx.y;
@@ -198,9 +198,10 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT) k_decode_cluste
     // ------------------------------------------------------------ phase 2
     if (r == 0) {
         const int P = min(n_pages[u], page_cap);
+        const int Ps = max(0, P - n_pos);  // semantic pages; the positional rest is always in the union
         const int words = (P + 31) / 32;
         for (int x = t; x < words; x += kT) s_mask[x] = 0u;
-        if (k_pages >= P) {
+        if (k_pages >= Ps) {
             __syncthreads();
             for (int x = t; x < words; x += kT) {
                 const int rem = P - x * 32;
@@ -213,6 +214,7 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT) k_decode_cluste
                 s_cand[x] = cluster.map_shared_rank(s_top, i / kc)[hh * kc + i % kc];
             }
             __syncthreads();
+            for (int x = Ps + t; x < P; x += kT) atomicOr(&s_mask[x >> 5], 1u << (x & 31));
             for (int hh = warp; hh < g; hh += kWarps) {
                 warp_topk64(s_cand + (size_t)hh * nc, nc, kt, s_ord + (size_t)hh * kt);
                 int taken = 0;
@@ -238,7 +240,7 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT) k_decode_cluste
                     int pg = sp.x;
                     for (int i = 0; i < take; ++i) {
                         const int q = sp.z ? pg + i : pg;
-                        if (q < 0 || q >= P) break;
+                        if (q < 0 || q >= Ps) break;
                         atomicOr(&s_mask[q >> 5], 1u << (q & 31));
                         if (!sp.z) pg = page_next[ug + q];
                     }
@@ -511,7 +513,7 @@ cudaError_t launch_t(const ice_params &p, const ice_index &idx, const void *Q, i
         sh.chunk, idx.n_parents, idx.n_pages, static_cast<const T *>(idx.parent_keys), idx.parent_first_page,
         idx.parent_last_page, idx.parent_n_pages, idx.page_next, idx.page_len, static_cast<const T *>(idx.pool_k),
         static_cast<const T *>(idx.pool_v), sel_pages, sel_count, max_sel, static_cast<T *>(kbuf),
-        static_cast<T *>(vbuf), buf_len, scale, O, err);
+        static_cast<T *>(vbuf), buf_len, scale, O, pos_split(p).n_pos, err);
     return cudaGetLastError();
 }
 

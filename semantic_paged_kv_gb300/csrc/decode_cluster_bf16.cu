@@ -90,7 +90,7 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT, 1) k_decode_clu
     const int32_t *__restrict__ page_next, const int32_t *__restrict__ page_len,
     const __nv_bfloat16 *__restrict__ pool_k, const __nv_bfloat16 *__restrict__ pool_v, int32_t *__restrict__ sel_pages,
     int32_t *__restrict__ sel_count, int max_sel, __nv_bfloat16 *__restrict__ kbuf, __nv_bfloat16 *__restrict__ vbuf,
-    int32_t *__restrict__ buf_len, float scale, float *__restrict__ O, int32_t *__restrict__ err) {
+    int32_t *__restrict__ buf_len, float scale, float *__restrict__ O, int n_pos, int32_t *__restrict__ err) {
     dep_wait();  // the previous kernel of the stream is complete (launched as its dependent)
     cg::cluster_group cluster = cg::this_cluster();
     const int r = (int)cluster.block_rank();
@@ -280,6 +280,7 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT, 1) k_decode_clu
         s_top[hh * 32 + lane] = lane < kc ? best : 0ull;
     }
     const int P = min(n_pages[u], page_cap);
+    const int Ps = max(0, P - n_pos);  // semantic pages; the positional rest is always in the union
     const int words = (P + 31) / 32;
     if (r == 0)
         for (int x = tid; x < words; x += kT) s_mask[x] = 0u;
@@ -287,12 +288,15 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT, 1) k_decode_clu
 
     // ------------------------------------------------------------ phase 2
     if (r == 0) {
-        if (k_pages >= P) {
+        if (k_pages >= Ps) {
             for (int x = tid; x < words; x += kT) {
                 const int rem = P - x * 32;
                 s_mask[x] = rem >= 32 ? 0xffffffffu : ((1u << rem) - 1u);
             }
-        } else if (warp < g) {
+        } else {
+            for (int x = Ps + tid; x < P; x += kT) atomicOr(&s_mask[x >> 5], 1u << (x & 31));
+        }
+        if (k_pages < Ps && warp < g) {
             const int hh = warp;
             unsigned long long v[kC];
 #pragma unroll
@@ -321,7 +325,7 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT, 1) k_decode_clu
             int pg = fp;
             for (int i = 0; i < tk; ++i) {
                 const int qq = contig ? fp + i : pg;
-                if (qq < 0 || qq >= P) break;
+                if (qq < 0 || qq >= Ps) break;
                 atomicOr(&s_mask[qq >> 5], 1u << (qq & 31));
                 if (!contig) pg = page_next[ug + qq];
             }
@@ -595,7 +599,8 @@ cudaError_t launch_gt(const ice_params &p, const ice_index &idx, const void *Q, 
                                                 static_cast<const __nv_bfloat16 *>(idx.pool_k),
                                                 static_cast<const __nv_bfloat16 *>(idx.pool_v), sel_pages, sel_count,
                                                 max_sel, static_cast<__nv_bfloat16 *>(kbuf),
-                                                static_cast<__nv_bfloat16 *>(vbuf), buf_len, scale, O, err);
+                                                static_cast<__nv_bfloat16 *>(vbuf), buf_len, scale, O,
+                                                pos_split(p).n_pos, err);
         if (e_ != cudaSuccess) return e_;
     }
     return cudaGetLastError();

@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(kThreads) k_select(
     const int32_t *__restrict__ parent_last_page, const int32_t *__restrict__ parent_n_pages,
     const int32_t *__restrict__ page_next, unsigned long long *__restrict__ cand_key, int4 *__restrict__ cand_span,
     int32_t *__restrict__ ticket, int32_t *__restrict__ sel_pages, int32_t *__restrict__ sel_count, int max_sel,
-    int32_t *__restrict__ err) {
+    int n_pos, int32_t *__restrict__ err) {
     extern __shared__ __align__(16) unsigned char smem[];
     const SelectSmem L = select_smem(g, n_chunks, kc, page_cap);
     float *s_q = reinterpret_cast<float *>(smem + L.q);
@@ -185,9 +185,10 @@ __global__ void __launch_bounds__(kThreads) k_select(
     __threadfence();
 
     const int P = min(n_pages[u], page_cap);
+    const int Ps = max(0, P - n_pos);  // semantic pages; the positional rest is always in the union
     const int words = (P + 31) / 32;
     for (int x = threadIdx.x; x < words; x += kThreads) s_mask[x] = 0u;
-    if (k_pages >= P) {
+    if (k_pages >= Ps) {
         __syncthreads();
         for (int x = threadIdx.x; x < words; x += kThreads) {
             const int rem = P - x * 32;
@@ -206,6 +207,7 @@ __global__ void __launch_bounds__(kThreads) k_select(
             s_key[x] = k;
         }
         __syncthreads();
+        for (int x = Ps + threadIdx.x; x < P; x += kThreads) atomicOr(&s_mask[x >> 5], 1u << (x & 31));
         block_bitonic_desc(s_key, g, n2);
         // one warp per head: take pages of the ordered parents until k pages
         const int kt = min(k_pages, nc);
@@ -232,7 +234,7 @@ __global__ void __launch_bounds__(kThreads) k_select(
                 int pg = sp.x;
                 for (int i = 0; i < take; ++i) {
                     const int q = sp.z ? pg + i : pg;
-                    if (q < 0 || q >= P) break;
+                    if (q < 0 || q >= Ps) break;
                     atomicOr(&s_mask[q >> 5], 1u << (q & 31));
                     if (!sp.z) pg = page_next[ug + q];
                 }
@@ -295,7 +297,7 @@ cudaError_t launch_t(const ice_params &p, const ice_index &idx, const void *Q, c
         static_cast<const T *>(Q), g, p.n_q_heads, p.n_kv_heads, p.np_cap, p.page_cap, ws.k_pages, kc > 0 ? kc : 1,
         ws.n_chunks, idx.n_parents, idx.n_pages, static_cast<const T *>(idx.parent_keys), idx.parent_first_page,
         idx.parent_last_page, idx.parent_n_pages, idx.page_next, ws.cand_key, ws.cand_span, ws.sel_ticket,
-        sel_pages, sel_count, max_sel, err);
+        sel_pages, sel_count, max_sel, pos_split(p).n_pos, err);
     return cudaGetLastError();
 }
 

@@ -316,6 +316,7 @@ SelArgs select_args(const ice_params &p, const ice_index &idx, const DecodeWs &w
     A.k_pages = ws.k_pages;
     A.kc = ws.k_pages;
     A.max_sel = max_sel;
+    A.n_pos = pos_split(p).n_pos;
     A.n_parents = idx.n_parents;
     A.n_pages = idx.n_pages;
     A.scores = ws.scores;

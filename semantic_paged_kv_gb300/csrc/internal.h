@@ -22,6 +22,20 @@ constexpr int kPackSmemBins = 12288;
 inline int units_of(const ice_params &p) { return p.batch * p.n_kv_heads; }
 inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
+// Sink / window split of a build over p.n_tokens tokens: the index covers the
+// middle [lo, hi); the sink [0, lo) and the window [hi, N) fill n_pos
+// positional pages after the semantic ones.
+struct PosSplit {
+    int lo, hi, n_pos;
+};
+inline PosSplit pos_split(const ice_params &p) {
+    const int N = p.n_tokens;
+    const int lo = p.n_sink < N ? (p.n_sink > 0 ? p.n_sink : 0) : N;
+    const int w = p.n_window > 0 ? p.n_window : 0;
+    const int hi = N - w > lo ? N - w : lo;
+    return PosSplit{lo, hi, (lo + 15) / 16 + (N - hi + 15) / 16};
+}
+
 // ------------------------------------------------ workspace layouts -------
 struct BuildWs {
     double *norm2;        // [U, N]  |k_j|^2 (double)
@@ -51,6 +65,7 @@ struct DecodeWs {
 // maxima, page spans; the ascending page list per unit).
 struct SelArgs {
     int g, np_cap, page_cap, k_pages, kc, max_sel;
+    int n_pos;  // positional pages at the end of each unit's pages, always in the union
     const int32_t *n_parents, *n_pages;
     const float *scores, *gmax;
     const int32_t *parent_first_page, *parent_last_page, *parent_n_pages, *page_next;

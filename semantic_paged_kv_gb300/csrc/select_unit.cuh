@@ -106,16 +106,20 @@ __device__ int select_unit(const SelArgs &A, int u, int tid, unsigned *s_mask, u
     const int Np = min(A.n_parents[u], np_cap);
     const size_t up = (size_t)u * np_cap, ug = (size_t)u * A.page_cap;
     const int P = min(A.n_pages[u], A.page_cap);
+    const int Ps = max(0, P - A.n_pos);  // semantic pages; the rest are positional (always in the union)
     const int words = (P + 31) / 32;
     const int ngc = (np_cap + kGroup - 1) / kGroup, ng = (Np + kGroup - 1) / kGroup;
     for (int x = tid; x < words; x += nt) s_mask[x] = 0u;
     named_bar(2, nt);
-    if (k_pages >= P) {
+    if (k_pages >= Ps) {
         for (int x = tid; x < words; x += nt) {
             const int rem = P - x * 32;
             s_mask[x] = rem >= 32 ? 0xffffffffu : ((1u << rem) - 1u);
         }
-    } else if (warp < g) {
+    } else {
+        for (int x = Ps + tid; x < P; x += nt) atomicOr(&s_mask[x >> 5], 1u << (x & 31));
+    }
+    if (k_pages < Ps && warp < g) {
         const int hh = warp;
         const float *sh = A.scores + ((size_t)u * g + hh) * np_cap;
         const float *gh = A.gmax + ((size_t)u * g + hh) * ngc;
@@ -266,7 +270,7 @@ __device__ int select_unit(const SelArgs &A, int u, int tid, unsigned *s_mask, u
         int pg = fp;
         for (int i = 0; i < tk; ++i) {
             const int qq = contig ? fp + i : pg;
-            if (qq < 0 || qq >= P) break;
+            if (qq < 0 || qq >= Ps) break;
             atomicOr(&s_mask[qq >> 5], 1u << (qq & 31));
             if (!contig) pg = A.page_next[ug + qq];
         }

@@ -190,7 +190,10 @@ def check_decode_unit(run: GpuRun, u: int, Q: np.ndarray, budget: int, buf):
         assert cnt == 0
         assert np.all(buf.O[b, h * g:(h + 1) * g].cpu().numpy() == 0)
         return
-    head, union = oracle.select(q, pkeys, H["page_parent"][u, :P], k_pages)
+    n_pos = run.cfg.n_pos  # positional (sink / window) pages: the last n_pos, always in the union
+    Ps = P - n_pos
+    head, union = oracle.select(q, pkeys, H["page_parent"][u, :Ps], k_pages)
+    union = np.concatenate([union, np.arange(Ps, P, dtype=union.dtype)])
     if not np.array_equal(got, union):
         # near-tie protocol: differences only through parents tied with the boundary
         _, M2, _ = oracle.lift(run.K[b, h].astype(np.float64))
@@ -198,8 +201,8 @@ def check_decode_unit(run: GpuRun, u: int, Q: np.ndarray, budget: int, buf):
         required = set()
         for hh in range(g):
             s = pkeys @ q[hh]
-            ps = s[H["page_parent"][u, :P]]
-            kth = ps[head[hh][min(k_pages, P) - 1]]
+            ps = s[H["page_parent"][u, :Ps]]
+            kth = ps[head[hh][min(k_pages, Ps) - 1]]
             tol = TIE_REL * np.linalg.norm(q[hh]) * np.sqrt(M2)
             near = np.where(np.abs(ps - kth) <= tol)[0]
             allowed |= set(near.tolist())

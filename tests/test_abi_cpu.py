@@ -39,6 +39,11 @@ def test_host_only_entry_points(lib):
     assert ice.ice_status_string(ice.ICE_ERR_CAPACITY) == "capacity exceeded"
     assert ice.ice_page_bound(1000, 1, 16) == 63
     assert ice.ice_page_bound(1000, 100, 16) == (1000 + 15 * 100) // 16
+    # sink / window pages: ceil(sink / 16) + ceil(window / 16), the window cut at the sink
+    pp = lib.ice_positional_pages
+    assert pp(900, 40, 70, 16) == 3 + 5 and pp(900, 0, 0, 16) == 0 and pp(900, 900, 10, 16) == 57
+    assert pp(900, 500, 500, 16) == 32 + 25 and pp(10, 3, 4, 16) == 2 and pp(0, 5, 5, 16) == 0
+    assert pp(-1, 0, 0, 16) == -1 and pp(100, 0, 0, 8) == -1
     cfg = ice.Config(batch=2, n_q_heads=8, n_kv_heads=2, n_tokens=5000)
     assert ice.ice_build_workspace_bytes(cfg.params()) > 2 * 2 * 5000 * 8
     assert ice.ice_decode_workspace_bytes(cfg.params(), 256, 64) > 0
@@ -61,7 +66,7 @@ def test_invalid_params_rejected_on_host(lib, field, value, status):
 
 
 def test_struct_layouts_match_header():
-    assert ctypes.sizeof(ice.IceParams) == 64
+    assert ctypes.sizeof(ice.IceParams) == 72
     assert ctypes.sizeof(ice.IceIndex) == 20 * 8
 
 

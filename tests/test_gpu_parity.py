@@ -328,3 +328,62 @@ def test_reuse_build_matches_oracle(shape):
         assert st == ice.ICE_OK
         for u in range(run1.cfg.units):
             check_decode_unit(run1, u, Q, bgt, buf)
+
+
+@pytest.mark.parametrize("shape,n_sink,n_window", [("llama_bf16", 64, 250), ("tiny_fp32", 16, 100),
+                                                   ("llama_bf16", 3, 0), ("many_units", 32, 130),
+                                                   ("no_middle", 2000, 2000)])
+def test_sink_and_window_pages(shape, n_sink, n_window):
+    """Sink and recent-window tokens kept as positional pages outside the
+    index: the middle's index against oracle.build_unit_positional (parents
+    exact, assignment tie-aware, pages and pool exact where the assignment
+    agrees), then every decode path attends over the selected pages plus all
+    positional pages."""
+    w = {"llama_bf16": W["llama31_8b_16k"].scaled(n_tokens=4003, batch=2, n_q_heads=8, n_kv_heads=2),
+         "tiny_fp32": W["tiny"],
+         "many_units": W["qwen3_32b_100k"].scaled(n_tokens=3000, batch=3, centres=256),
+         "no_middle": W["llama31_8b_16k"].scaled(n_tokens=3000, n_q_heads=8, n_kv_heads=2)}[shape]
+    run = GpuRun(w, n_sink=n_sink, n_window=n_window)
+    assert run.status == ice.ICE_OK
+    th = oracle.promote_threshold(w.promote_p)
+    N, exact = w.n_tokens, 0
+    for u in range(run.cfg.units):
+        b, h = run.unit(u)
+        ref = oracle.build_unit_positional(run.K[b, h], run.V[b, h], seed=w.seed, layer=0, seq=b, head=h, thresh=th,
+                                           n_sink=n_sink, n_window=n_window)
+        H, Np = run.h, len(ref["parent_tok"])
+        assert int(H["n_parents"][u]) == Np and np.array_equal(H["parent_tok"][u, :Np], ref["parent_tok"])
+        assert abs(H["m2"][u] - ref["M2"]) <= 1e-12 * max(ref["M2"], 1e-30)
+        assert np.array_equal(run.idx.parent_keys[u, :Np].float().cpu().numpy(), run.K[b, h][ref["parent_tok"]])
+        tp = H["token_parent"][u, :N]
+        se, ws = oracle.positional_split(N, n_sink, n_window)
+        assert np.all(tp[:se] == -2) and np.all(tp[ws:] == -2)
+        assert np.mean(tp == ref["token_parent"]) > 0.999
+        if not np.array_equal(tp, ref["token_parent"]):
+            continue  # an fp32 near-tie moved a token: the page layout legitimately differs
+        P = int(ref["n_pages"])
+        assert int(H["n_pages"][u]) == P
+        for f in ("page_parent", "page_len", "page_tokens"):
+            assert np.array_equal(H[f][u, :P], ref[f]), f
+        assert np.array_equal(H["token_page"][u, :N], ref["token_page"])
+        assert np.array_equal(H["token_slot"][u, :N], ref["token_slot"])
+        pk, pv = run.pool(u)
+        assert np.array_equal(pk, ref["pool_k"].astype(np.float32)) and np.array_equal(pv, ref["pool_v"].astype(np.float32))
+        exact += 1
+    assert exact >= run.cfg.units - 1
+    for bgt in (64, 256):
+        for fused in (True, False):
+            Q, buf, st = run.decode(bgt, fused=fused)
+            assert st == ice.ICE_OK
+            for u in range(run.cfg.units):
+                check_decode_unit(run, u, Q, bgt, buf)
+
+
+def test_insert_rejected_with_positional_pages():
+    w = W["llama31_8b_16k"].scaled(n_tokens=1000, n_q_heads=4, n_kv_heads=1)
+    run = GpuRun(w, n_sink=16, n_window=32)
+    ws = ice.workspace(ice.ice_insert_workspace_bytes(run.params))
+    kn = torch.zeros((1, 1, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ice.IceError) as ei:
+        ice.ice_insert_tokens(run.params, run.idx, kn, kn, ws, run.err)
+    assert ei.value.status == ice.ICE_ERR_UNSUPPORTED
