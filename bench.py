@@ -68,8 +68,8 @@ FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 # source file at capture time; reported only while the source is unchanged.
 TRAFFIC = {
     # profiles/assign_tc_llama31_8b_16k.md
-    "assign": {"workload": "llama31_8b_16k", "source": "build_assign_tc.cu", "bytes": 40955904,
-               "sha256": "6bfded2608bcb66426c2df4f483ad31a169341ad9c03a4acd0191b59939134f5"},
+    "assign": {"workload": "llama31_8b_16k", "source": "build_assign_tc.cu", "bytes": 40956928,
+               "sha256": "0768da93b82fd5183f887be91f167e1f2067cf6d18cd4655f1fa685817a3c947"},
 }
 
 
@@ -584,7 +584,7 @@ def run_ours(args):
 
     # ---- end to end with host buffers: H2D of the inputs, the step, D2H of O
     e2e_steps = args.e2e_steps or min(args.steps, 100)
-    h2d = sum(sets[0][k].numel() * sets[0][k].element_size() for k in ("Kh", "Vh", "Qh"))
+    h2d_bytes = sum(sets[0][k].numel() * sets[0][k].element_size() for k in ("Kh", "Vh", "Qh"))
     d2h = sets[0]["Oh"].numel() * 4
     barrier()
     torch.cuda.synchronize()
@@ -599,8 +599,45 @@ def run_ours(args):
         st["Oh"].copy_(st["buf"].O, non_blocking=True)
     b_.record()
     torch.cuda.synchronize()
+    e2e_serial_ms = max_over_ranks(a.elapsed_time(b_), world, "cuda")
+    # the same with the next layer's host-to-device copy on a second stream
+    # while this layer is built and decoded (the on-device form of the pages'
+    # copy / index / compute pipeline): copies of step i + 1 overlap step i
+    cs, xs = torch.cuda.Stream(), torch.cuda.current_stream()
+    copied = [torch.cuda.Event() for _ in range(e2e_steps)]
+    done = [torch.cuda.Event() for _ in range(e2e_steps)]
+
+    def h2d(i):
+        st = sets[i % len(sets)]
+        with torch.cuda.stream(cs):
+            if i >= len(sets):
+                cs.wait_event(done[i - len(sets)])  # the set's buffers are free again
+            st["K"].copy_(st["Kh"], non_blocking=True)
+            st["V"].copy_(st["Vh"], non_blocking=True)
+            st["Q"].copy_(st["Qh"], non_blocking=True)
+            copied[i].record(cs)
+
+    barrier()
+    torch.cuda.synchronize()
+    a, b_ = E(), E()
+    a.record()
+    cs.wait_stream(xs)
+    h2d(0)
+    for i in range(e2e_steps):
+        if i + 1 < e2e_steps:
+            h2d(i + 1)
+        st = sets[i % len(sets)]
+        xs.wait_event(copied[i])
+        step(st)
+        st["Oh"].copy_(st["buf"].O, non_blocking=True)
+        done[i].record(xs)
+    b_.record()
+    torch.cuda.synchronize()
     e2e_ms = max_over_ranks(a.elapsed_time(b_), world, "cuda")
     e2e_value = whole_job_rate(U, N, e2e_steps, world, e2e_ms)
+    compute_ms = elapsed_ms / args.steps * e2e_steps
+    copy_ms = max(e2e_serial_ms - compute_ms, 1e-9)
+    hidden = min(1.0, max(0.0, (e2e_serial_ms - e2e_ms) / min(copy_ms, compute_ms)))
     status = ice.ice_check(err)
 
     cpu = None
@@ -648,8 +685,14 @@ def run_ours(args):
                          "work_per_launch": work, "traffic": tr},
             "at_scale": scale_res,
             "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": "keys/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "steps": e2e_steps},
+            "e2e": {"value": e2e_value, "unit": "keys/s", "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h,
+                    "steps": e2e_steps,
+                    "how": "every step: H2D of its K, V, Q from pinned host memory, the step (index build + decode, "
+                           "one CUDA graph), D2H of O; the next step's H2D runs on a second stream during this step",
+                    "serial_value": whole_job_rate(U, N, e2e_steps, world, e2e_serial_ms),
+                    "hidden_fraction": hidden,
+                    "hidden_fraction_is": "(serial - overlapped time) / min(copy time, compute time), at most 1; "
+                                          "copy time = serial time - device-only step time"},
             "gpu_launches": kernels_per_step * args.steps,
             "gpu_launches_counted_from": "captured graph kernel nodes" if all(x is not None for x in per_step)
             else "static plan",
