@@ -324,6 +324,69 @@ def build_unit_positional(K, V, *, seed: int, layer: int, seq: int, head: int, t
                 page_tokens=page_tokens, token_page=token_page, token_slot=token_slot)
 
 
+# ------------------------------------------------------------ level 2 ----
+def build_level2(idx: dict, *, seed: int, layer: int, seq: int, head: int, thresh: int) -> dict:
+    """The level above the parents (papernotes 关键设计 2: points are promoted
+    at random level by level and every point of a level takes its nearest
+    point one level up as parent; article section 三).  A parent (level-1
+    node) m is promoted to level 2 iff the draw of its token at level 2 is
+    below thresh; if none is, the one of smallest draw (lowest m on ties).
+    Level-2 nodes i = 0.. are those parents in ascending m (node2[i] = m).
+    parent2[m]: the level-2 node nearest to parent m in lifted space (the
+    parents' keys with their lifted coordinate; ties to the lowest i), a
+    level-2 node being its own.  children: the parents grouped by parent2,
+    ascending m inside a group, group i at [child_start[i], child_start[i+1])."""
+    pt = np.asarray(idx["parent_tok"], np.int64)
+    Np = len(pt)
+    if Np == 0:
+        return dict(node2=np.zeros(0, np.int32), parent2=np.zeros(0, np.int32),
+                    child_start=np.zeros(1, np.int32), children=np.zeros(0, np.int32))
+    d2 = np.array([promote_draw(seed, layer, seq, head, int(t), 2) for t in pt], np.int64)
+    node2 = np.nonzero(d2 < thresh)[0]
+    if len(node2) == 0:
+        node2 = np.array([int(np.argmin(d2))])
+    node2 = node2.astype(np.int32)
+    parent2 = assign(idx["parent_keys"], idx["parent_e"], node2)
+    order = np.argsort(parent2, kind="stable").astype(np.int32)
+    counts = np.bincount(parent2, minlength=len(node2))
+    child_start = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    return dict(node2=node2, parent2=parent2.astype(np.int32), child_start=child_start, children=order)
+
+
+def select_descent(q, idx: dict, lv2: dict, k_pages: int) -> tuple[list, np.ndarray]:
+    """Page selection by descent through level 2 (papernotes 关键设计 2: the
+    query finds the k nearest points of the top level, then continues among
+    their children; 关键设计 3: per head, union over the GQA group).  With
+    the lifted query q' = [q, 0], nearest means largest q.p.  Per head: the
+    first k = k_pages level-2 nodes in (-q.p, i) order, then their children
+    in (-q.p, m) order, whose pages (page-id order inside a parent) are taken
+    until k pages.  Returns (per-head page lists, ascending union) over the
+    semantic pages."""
+    q = _f64(q)
+    pk = _f64(idx["parent_keys"])
+    node2, ch, cs = lv2["node2"], lv2["children"], lv2["child_start"]
+    n_pos = int(idx.get("n_pos", 0))
+    P_sem = int(idx["n_pages"]) - n_pos
+    page_parent = np.asarray(idx["page_parent"][:P_sem])
+    pages_of = [[] for _ in range(len(pk))]
+    for pg, m in enumerate(page_parent):
+        pages_of[m].append(pg)
+    heads, union = [], set()
+    for qh in q:
+        s2 = pk[node2] @ qh if len(node2) else np.zeros(0)
+        top2 = sorted(range(len(node2)), key=lambda i: (-s2[i], i))[:k_pages]
+        cand = [int(m) for i in top2 for m in ch[cs[i]:cs[i + 1]]]
+        s1 = {m: float(pk[m] @ qh) for m in cand}
+        pages = []
+        for m in sorted(cand, key=lambda m: (-s1[m], m)):
+            for pg in pages_of[m]:
+                if len(pages) < k_pages:
+                    pages.append(pg)
+        heads.append(pages)
+        union |= set(pages)
+    return heads, np.array(sorted(union), np.int32)
+
+
 def build_unit_reuse(K, V, prev: dict, S: int = 16) -> dict:
     """Build of one unit on another layer's node structure (the inter-layer
     index reuse of the article's section 五, "IceCache (reuse)"; its mechanism
@@ -353,7 +416,10 @@ def decode_unit(idx: dict, q, budget_tokens: int, scale: float | None = None) ->
     k_pages = -(-budget_tokens // S)
     n_pos = int(idx.get("n_pos", 0))  # positional (sink / window) pages: the last n_pos, always attended
     P_sem = int(idx["n_pages"]) - n_pos
-    head_pages, sel = select(q, idx["parent_keys"], idx["page_parent"][:P_sem], k_pages)
+    if "level2" in idx:  # three levels: descent through level 2
+        head_pages, sel = select_descent(q, idx, idx["level2"], k_pages)
+    else:
+        head_pages, sel = select(q, idx["parent_keys"], idx["page_parent"][:P_sem], k_pages)
     if n_pos:
         sel = np.concatenate([sel, np.arange(P_sem, P_sem + n_pos, dtype=np.int32)]).astype(np.int32)
     kb, vb, bl = gather(idx["pool_k"], idx["pool_v"], idx["page_len"], sel)

@@ -513,3 +513,78 @@ def test_positional_small_budget_attends_sink_window_and_selected_pages():
     vt = torch.from_numpy(V[toks].astype(np.float64))[None, None].expand(1, q.shape[0], -1, -1)
     ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt)[0, :, 0].numpy()
     assert np.max(np.abs(dec["out"] - ref)) < 1e-12
+
+
+# ------------------------------------------------------------ three levels
+def _l3_unit(N=3000, centres=48, promote_p=1.0 / 16, seed_head=0):
+    w = workloads.WORKLOADS["llama31_8b_16k"].scaled(n_tokens=N, centres=centres, dtype="fp32",
+                                                      promote_p=promote_p)
+    th = oracle.promote_threshold(w.promote_p)
+    K, V = workloads.unit_kv(w, 0, 0, seed_head)
+    idx = oracle.build_unit(K, V, seed=w.seed, layer=0, seq=0, head=seed_head, thresh=th)
+    lv2 = oracle.build_level2(idx, seed=w.seed, layer=0, seq=0, head=seed_head, thresh=th)
+    return w, th, K, V, idx, lv2
+
+
+def test_level2_nodes_assignment_and_children():
+    w, th, K, V, idx, lv2 = _l3_unit()
+    Np, node2, p2 = len(idx["parent_tok"]), lv2["node2"], lv2["parent2"]
+    # promotion: exactly the parents whose level-2 draw is below the threshold
+    want = [m for m, t in enumerate(idx["parent_tok"]) if oracle.promote_draw(w.seed, 0, 0, 0, int(t), 2) < th]
+    assert list(node2) == want and len(want) > 0
+    mu, sd = Np * w.promote_p, math.sqrt(Np * w.promote_p * (1 - w.promote_p))
+    assert abs(len(node2) - mu) <= 5 * sd
+    # every parent's level-2 parent is its nearest level-2 node (brute force in the lifted space)
+    P = np.hstack([idx["parent_keys"], np.asarray(idx["parent_e"])[:, None]])
+    D = ((P[:, None, :] - P[node2][None, :, :]) ** 2).sum(-1)
+    assert np.all(D[np.arange(Np), p2] <= D.min(1) + 1e-12 * idx["M2"])
+    assert np.all(p2[node2] == np.arange(len(node2)))  # level-2 nodes are their own parents
+    # children: every parent in exactly one group, ascending inside it
+    cs, ch = lv2["child_start"], lv2["children"]
+    assert cs[0] == 0 and cs[-1] == Np and np.array_equal(np.sort(ch), np.arange(Np))
+    for i in range(len(node2)):
+        grp = ch[cs[i]:cs[i + 1]]
+        assert np.all(np.diff(grp) > 0) and np.all(p2[grp] == i) and node2[i] in grp
+
+
+def test_descent_expanding_every_level2_node_is_the_flat_selection():
+    """With k at least the number of level-2 nodes every parent is a
+    candidate, so the descent picks what the exact parent scan picks."""
+    w, th, K, V, idx, lv2 = _l3_unit(N=1200, centres=16)
+    q = workloads.unit_queries(w, 0, 0, 0)
+    k = len(lv2["node2"])
+    assert k <= 16 * 4
+    heads, union = oracle.select_descent(q, idx, lv2, k)
+    head_flat, union_flat = oracle.select(q, idx["parent_keys"], idx["page_parent"], k)
+    assert np.array_equal(union, union_flat)
+    for hh in range(len(q)):
+        flat = [p for p in head_flat[hh] if p >= 0]
+        assert heads[hh] == flat
+
+
+def test_descent_with_every_token_promoted_is_exact_topk_mips():
+    """p = 1: every token is a parent and a level-2 node with a one-token page;
+    the descent is the exact top-k of q.k (torch.topk)."""
+    w, th, K, V, idx, lv2 = _l3_unit(N=500, promote_p=1.0)
+    q = workloads.unit_queries(w, 0, 0, 0)
+    for k in (1, 5, 17):
+        heads, union = oracle.select_descent(q, idx, lv2, k)
+        for hh in range(len(q)):
+            s = torch.from_numpy(K.astype(np.float64) @ q[hh].astype(np.float64))
+            top = torch.topk(s, k).indices.numpy()
+            assert sorted(heads[hh]) == sorted(idx["token_page"][top].tolist())
+
+
+def test_decode_unit_three_levels_attends_over_the_descent_pages():
+    w, th, K, V, idx, lv2 = _l3_unit()
+    q = workloads.unit_queries(w, 0, 0, 0)
+    idx3 = dict(idx, level2=lv2)
+    dec = oracle.decode_unit(idx3, q, budget_tokens=128)
+    _, union = oracle.select_descent(q, idx, lv2, 8)
+    assert np.array_equal(dec["sel_pages"], union)
+    toks = np.concatenate([idx["page_tokens"][p][idx["page_tokens"][p] >= 0] for p in union])
+    qt = torch.from_numpy(q.astype(np.float64))[None, :, None, :]
+    kt = torch.from_numpy(K[toks].astype(np.float64))[None, None].expand(1, q.shape[0], -1, -1)
+    vt = torch.from_numpy(V[toks].astype(np.float64))[None, None].expand(1, q.shape[0], -1, -1)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt)[0, :, 0].numpy()
+    assert np.max(np.abs(dec["out"] - ref)) < 1e-12
