@@ -66,7 +66,7 @@ typedef struct ice_params {
     int32_t n_tokens;       /* N: tokens per unit given to ice_build_index */
     int32_t page_size;      /* S; 16 is the supported value ([B] section 二) */
     int32_t dtype;          /* ICE_BF16 or ICE_FP32 for K, V, Q and the pool */
-    int32_t n_levels;       /* index levels; 2 is the supported value */
+    int32_t n_levels;       /* index levels: 2 (tokens, parents) or 3 (+ a level above the parents) */
     uint64_t promote_thresh;/* floor(p * 2^32), 0 .. 2^32: promotion probability p */
     uint64_t seed;          /* promotion seed */
     int32_t layer;          /* layer id (enters the promotion draw) */
@@ -142,6 +142,16 @@ typedef struct ice_index {
     int32_t *token_slot;
     void *pool_k;
     void *pool_v;
+    /* Level 2 (ice_params.n_levels = 3 only; may be NULL with 2 levels):
+     * n_nodes2[U]; node2[U,Np] the parent m of level-2 node i (ascending m);
+     * parent2[U,Np] the level-2 node of parent m; child_start[U,Np+1] and
+     * children[U,Np]: the parents of level-2 node i, ascending, at
+     * children[child_start[i] .. child_start[i+1]) (all int32). */
+    int32_t *n_nodes2;
+    int32_t *node2;
+    int32_t *parent2;
+    int32_t *child_start;
+    int32_t *children;
 } ice_index;
 
 /* ---------------------------------------------------------------- misc -- */
@@ -203,6 +213,18 @@ ice_status ice_build_lift_promote(const ice_params *p, const void *K, const ice_
  */
 ice_status ice_build_assign(const ice_params *p, const void *K, const ice_index *idx, void *ws,
                             size_t ws_bytes, int32_t *err_dev, void *stream);
+/*
+ * With n_levels = 3, ice_build_assign (and so ice_build_index) also builds
+ * level 2 ([A] 关键设计 2: points are promoted level by level and every
+ * point takes its nearest point one level up as parent): parent m is
+ * promoted iff the draw of its token at level 2 (the promotion rule above
+ * with level 2 in the counter) is below promote_thresh, or, if none is, the
+ * parent of smallest such draw (lowest m on ties); node2 lists them in
+ * ascending m.  parent2[m] is the level-2 node nearest to parent m in the
+ * lifted space, argmax_i (p_m . p_i + e_m e_i) in fp32, exact ties to the
+ * lowest i (a level-2 node is its own); children groups the parents by
+ * parent2.  Needs np_cap <= 50000.
+ */
 
 /*
  * Stage a3 on CUDA cores (fp32 FMA) for either dtype.  Same contract and
@@ -295,6 +317,14 @@ ice_status ice_decode_workspace_bytes(const ice_params *p, int32_t budget_tokens
  * (-s, page id); sel_pages[u, 0..sel_count[u]) is the ascending union of the
  * g lists, sel_pages [U, max_sel] int32 (rest -1), sel_count [U] int32.
  * max_sel must be >= min(g * k, page_cap).
+ */
+/*
+ * With n_levels = 3 the selection descends ([A] 关键设计 2: the query finds
+ * the k nearest points of the top level, then searches among their
+ * children): per query head, the first k level-2 nodes in (-q.p, i) order,
+ * then their children (parents) in (-q.p, m) order, whose pages are taken in
+ * page-id order until k pages; union and positional pages as above.  Needs
+ * k <= 32.  ice_decode_step follows the same rule.
  */
 ice_status ice_select_pages(const ice_params *p, const ice_index *idx, const void *Q, int32_t budget_tokens,
                             int32_t *sel_pages, int32_t *sel_count, int32_t max_sel, void *ws,

@@ -44,7 +44,8 @@ class IceParams(ctypes.Structure):
 
 INDEX_FIELDS = ["n_parents", "n_pages", "n_indexed", "m2", "parent_tok", "parent_keys", "parent_e", "parent_corr",
                 "parent_first_page", "parent_last_page", "parent_n_pages", "page_parent", "page_len", "page_next",
-                "page_tokens", "token_parent", "token_page", "token_slot", "pool_k", "pool_v"]
+                "page_tokens", "token_parent", "token_page", "token_slot", "pool_k", "pool_v",
+                "n_nodes2", "node2", "parent2", "child_start", "children"]
 
 
 class IceIndex(ctypes.Structure):
@@ -212,6 +213,9 @@ class Index:
         self.page_parent, self.page_len, self.page_next = z((U, Pc), i32), z((U, Pc), i32), z((U, Pc), i32)
         self.page_tokens = z((U, Pc, S), i32)
         self.token_parent, self.token_page, self.token_slot = z((U, Nc), i32), z((U, Nc), i32), z((U, Nc), i32)
+        # level 2 (used when cfg.n_levels == 3)
+        self.n_nodes2, self.node2, self.parent2 = z(U, i32), z((U, Np), i32), z((U, Np), i32)
+        self.child_start, self.children = z((U, Np + 1), i32), z((U, Np), i32)
         if host_pool is not None:  # pages live in the pinned host pool (device-mapped pointers)
             self.host_pool = host_pool
             self.pool_k = self.pool_v = None

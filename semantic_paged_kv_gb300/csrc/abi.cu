@@ -48,7 +48,9 @@ ice_status check_params(const ice_params *p) {
     if (p->head_dim != kHeadDim) return fail(ICE_ERR_UNSUPPORTED, "head_dim must be %d", kHeadDim);
     if (p->page_size != kPage) return fail(ICE_ERR_UNSUPPORTED, "page_size must be %d", kPage);
     if (p->dtype != ICE_BF16 && p->dtype != ICE_FP32) return fail(ICE_ERR_INVALID_ARG, "dtype must be ICE_BF16 or ICE_FP32");
-    if (p->n_levels != 2) return fail(ICE_ERR_UNSUPPORTED, "n_levels must be 2");
+    if (p->n_levels != 2 && p->n_levels != 3) return fail(ICE_ERR_UNSUPPORTED, "n_levels must be 2 or 3");
+    if (p->n_levels == 3 && p->np_cap > kLevel2MaxParents)
+        return fail(ICE_ERR_UNSUPPORTED, "three levels need np_cap <= %d", kLevel2MaxParents);
     if (p->promote_thresh > (1ull << 32)) return fail(ICE_ERR_INVALID_ARG, "promote_thresh must be <= 2^32");
     if (p->n_tokens < 0 || p->n_cap < p->n_tokens) return fail(ICE_ERR_INVALID_ARG, "need 0 <= n_tokens <= n_cap");
     if (p->np_cap < 1 || p->page_cap < 1) return fail(ICE_ERR_INVALID_ARG, "np_cap and page_cap must be >= 1");
@@ -70,6 +72,14 @@ ice_status check_index(const ice_index *x) {
         if (!q) return fail(ICE_ERR_INVALID_ARG, "an ice_index array pointer is NULL");
     if (!aligned16(x->parent_keys) || !aligned16(x->pool_k) || !aligned16(x->pool_v))
         return fail(ICE_ERR_INVALID_ARG, "parent_keys, pool_k and pool_v must be 16-byte aligned");
+    return ICE_OK;
+}
+
+// The level-2 arrays a three-level index needs.
+ice_status check_level2(const ice_params *p, const ice_index *x) {
+    if (p->n_levels != 3) return ICE_OK;
+    if (!x->n_nodes2 || !x->node2 || !x->parent2 || !x->child_start || !x->children)
+        return fail(ICE_ERR_INVALID_ARG, "a three-level index needs n_nodes2, node2, parent2, child_start, children");
     return ICE_OK;
 }
 
@@ -225,6 +235,7 @@ static ice_status build_common(const ice_params *p, const void *K, const ice_ind
     ice_status st = check_params(p);
     if (st) return st;
     if ((st = check_index(idx))) return st;
+    if ((st = check_level2(p, idx))) return st;
     if (p->n_tokens > 0 && (!K || !aligned16(K))) return fail(ICE_ERR_INVALID_ARG, "K must be a 16-byte aligned device pointer");
     *w = build_ws_layout(*p, ws);
     return check_ws(ws, ws_bytes, w->bytes);
@@ -237,6 +248,7 @@ static ice_status build_empty(const ice_params *p, const ice_index *idx, cudaStr
     cudaMemsetAsync(idx->n_pages, 0, sizeof(int32_t) * U, s);
     cudaMemsetAsync(idx->n_indexed, 0, sizeof(int32_t) * U, s);
     cudaMemsetAsync(idx->m2, 0, sizeof(double) * U, s);
+    if (p->n_levels == 3) cudaMemsetAsync(idx->n_nodes2, 0, sizeof(int32_t) * U, s);
     return cuda_status(cudaGetLastError(), "build (empty units)");
 }
 
@@ -255,10 +267,17 @@ ice_status ice_build_assign(const ice_params *p, const void *K, const ice_index 
     BuildWs w;
     ice_status st = build_common(p, K, idx, ws, ws_bytes, &w);
     if (st) return st;
-    if (p->n_tokens == 0) return ICE_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (p->dtype == ICE_BF16) return cuda_status(launch_assign_tc(*p, K, *idx, w, err_dev, s), "ice_build_assign");
-    return cuda_status(launch_assign_simt(*p, K, *idx, w, err_dev, s), "ice_build_assign");
+    if (p->n_tokens == 0)
+        return p->n_levels == 3 ? cuda_status(cudaMemsetAsync(idx->n_nodes2, 0, sizeof(int32_t) * units_of(*p), s),
+                                              "ice_build_assign")
+                                : ICE_OK;
+    if ((st = cuda_status(p->dtype == ICE_BF16 ? launch_assign_tc(*p, K, *idx, w, err_dev, s)
+                                               : launch_assign_simt(*p, K, *idx, w, err_dev, s),
+                          "ice_build_assign")))
+        return st;
+    if (p->n_levels == 3) return cuda_status(launch_level2(*p, *idx, s), "ice_build_assign (level 2)");
+    return ICE_OK;
 }
 
 ice_status ice_build_assign_simt(const ice_params *p, const void *K, const ice_index *idx, void *ws,
@@ -294,7 +313,7 @@ ice_status ice_build_index_reuse(const ice_params *p, const void *K, const void 
     BuildWs w;
     ice_status st = build_common(p, K, idx, ws, ws_bytes, &w);
     if (st) return st;
-    if ((st = check_index(prev))) return st;
+    if ((st = check_index(prev)) || (st = check_level2(p, prev))) return st;
     if (p->n_tokens > 0 && (!V || !aligned16(V))) return fail(ICE_ERR_INVALID_ARG, "V must be a 16-byte aligned device pointer");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (p->n_tokens == 0) return build_empty(p, idx, s);
@@ -319,6 +338,7 @@ ice_status ice_insert_tokens(const ice_params *p, const ice_index *idx, const vo
         return fail(ICE_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned device pointers");
     if (p->n_sink > 0 || p->n_window > 0)
         return fail(ICE_ERR_UNSUPPORTED, "incremental insert is not supported with sink or window pages");
+    if (p->n_levels != 2) return fail(ICE_ERR_UNSUPPORTED, "incremental insert is supported with two levels");
     const InsertWs w = insert_ws_layout(*p, ws);
     if ((st = check_ws(ws, ws_bytes, w.bytes))) return st;
     return cuda_status(launch_insert(*p, *idx, k_new, v_new, w, err_dev, static_cast<cudaStream_t>(stream)),
@@ -349,7 +369,10 @@ static ice_status select_checks(const ice_params *p, const ice_index *idx, const
                                 int32_t *sel_pages, int32_t *sel_count, int32_t max_sel, const DecodeWs &w) {
     ice_status st = check_index(idx);
     if (st) return st;
+    if ((st = check_level2(p, idx))) return st;
     if (!Q || !sel_pages || !sel_count) return fail(ICE_ERR_INVALID_ARG, "Q, sel_pages and sel_count must be non-NULL");
+    if (p->n_levels == 3 && k_pages_of(budget_tokens) > 32)
+        return fail(ICE_ERR_UNSUPPORTED, "the three-level descent takes at most 32 pages per head");
     const long long g = p->n_q_heads / p->n_kv_heads;
     const long long need = g * (long long)k_pages_of(budget_tokens) + pos_split(*p).n_pos;
     const long long want = need < p->page_cap ? need : p->page_cap;
@@ -372,8 +395,11 @@ ice_status ice_select_pages(const ice_params *p, const ice_index *idx, const voi
     ice_status st = decode_common(p, budget_tokens, max_sel, ws, ws_bytes, &w);
     if (st) return st;
     if ((st = select_checks(p, idx, Q, budget_tokens, sel_pages, sel_count, max_sel, w))) return st;
-    return cuda_status(launch_select(*p, *idx, Q, w, sel_pages, sel_count, max_sel, err_dev,
-                                     static_cast<cudaStream_t>(stream)),
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p->n_levels == 3)
+        return cuda_status(launch_select3(*p, *idx, Q, w, sel_pages, sel_count, max_sel, err_dev, s),
+                           "ice_select_pages");
+    return cuda_status(launch_select(*p, *idx, Q, w, sel_pages, sel_count, max_sel, err_dev, s),
                        "ice_select_pages");
 }
 
@@ -438,6 +464,13 @@ ice_status ice_decode_step(const ice_params *p, const ice_index *idx, const void
         return fail(ICE_ERR_INVALID_ARG, "kbuf, vbuf and buf_len must be all non-NULL or all NULL");
     if (!aligned16(kbuf) || !aligned16(vbuf)) return fail(ICE_ERR_INVALID_ARG, "kbuf and vbuf must be 16-byte aligned");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p->n_levels == 3) {  // descent through level 2, then the pages streamed from the pool
+        cudaError_t e = launch_select3(*p, *idx, Q, w, sel_pages, sel_count, max_sel, err_dev, s);
+        if (e == cudaSuccess)
+            e = launch_attention(*p, idx, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, w, s,
+                                 err_dev);
+        return cuda_status(e, "ice_decode_step");
+    }
     // one cluster per unit pays off while all clusters fit in one wave; with
     // more units the select / attention kernels keep every SM streaming
     if (units_of(*p) * kDecodeCluster <= sm_count() && aligned16(Q) &&

@@ -95,11 +95,11 @@ cudaError_t launch_t(const ice_params &p, const void *K, const ice_index &prev, 
                             idx.parent_tok, static_cast<T *>(idx.parent_keys), idx.parent_e, idx.parent_corr, err);
 }
 
-// Up to 11 int32 arrays copied by one grid: CTA row y takes array y.
+// Up to 16 int32 arrays copied by one grid: CTA row y takes array y.
 struct CopyList {
-    int32_t *dst[11];
-    const int32_t *src[11];
-    long long n[11];
+    int32_t *dst[16];
+    const int32_t *src[16];
+    long long n[16];
 };
 
 __global__ void __launch_bounds__(kThreads) k_copy_tables(const CopyList L) {
@@ -135,7 +135,13 @@ cudaError_t launch_build_reuse(const ice_params &p, const void *K, const void *V
                   {idx.page_tokens, prev.page_tokens, pc * kPage},
                   {idx.token_parent, prev.token_parent, nc},
                   {idx.token_page, prev.token_page, nc},
-                  {idx.token_slot, prev.token_slot, nc}};
+                  {idx.token_slot, prev.token_slot, nc},
+                  // level 2 of a three-level index: kept with the rest of the node structure
+                  {idx.n_nodes2, prev.n_nodes2, p.n_levels == 3 ? U : 0},
+                  {idx.node2, prev.node2, p.n_levels == 3 ? np : 0},
+                  {idx.parent2, prev.parent2, p.n_levels == 3 ? np : 0},
+                  {idx.child_start, prev.child_start, p.n_levels == 3 ? np + U : 0},
+                  {idx.children, prev.children, p.n_levels == 3 ? np : 0}};
     CopyList L{};
     int na = 0;
     long long most = 0;

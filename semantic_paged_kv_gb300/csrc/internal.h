@@ -96,6 +96,12 @@ cudaError_t launch_assign_tc(const ice_params &p, const void *K, const ice_index
                              int32_t *err, cudaStream_t s);
 cudaError_t launch_pack(const ice_params &p, const void *K, const void *V, const ice_index &idx,
                         const BuildWs &ws, int32_t *err, cudaStream_t s);
+// Level 2 of a three-level index (promotion, nearest level-2 node, children).
+cudaError_t launch_level2(const ice_params &p, const ice_index &idx, cudaStream_t s);
+// Page selection by descent through level 2 (n_levels = 3).
+cudaError_t launch_select3(const ice_params &p, const ice_index &idx, const void *Q, const DecodeWs &ws,
+                           int32_t *sel_pages, int32_t *sel_count, int max_sel, int32_t *err, cudaStream_t s);
+constexpr int kLevel2MaxParents = 50000;  // parent capacity the level-2 counting sort holds in shared memory
 // Pieces of the build used by the reuse build: the squared norms and per-tile
 // maxima of k_lift_count, and the pool scatter k_pack_copy over idx's pages.
 cudaError_t launch_lift_norms(const ice_params &p, const void *K, const BuildWs &ws, cudaStream_t s);

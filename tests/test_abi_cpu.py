@@ -51,7 +51,7 @@ def test_host_only_entry_points(lib):
 
 @pytest.mark.parametrize("field,value,status", [("head_dim", 64, ice.ICE_ERR_UNSUPPORTED),
                                                  ("page_size", 8, ice.ICE_ERR_UNSUPPORTED),
-                                                 ("n_levels", 3, ice.ICE_ERR_UNSUPPORTED),
+                                                 ("n_levels", 4, ice.ICE_ERR_UNSUPPORTED),
                                                  ("n_kv_heads", 3, ice.ICE_ERR_INVALID_ARG),
                                                  ("dtype", 7, ice.ICE_ERR_INVALID_ARG),
                                                  ("promote_thresh", 2 ** 32 + 1, ice.ICE_ERR_INVALID_ARG),
@@ -67,7 +67,7 @@ def test_invalid_params_rejected_on_host(lib, field, value, status):
 
 def test_struct_layouts_match_header():
     assert ctypes.sizeof(ice.IceParams) == 72
-    assert ctypes.sizeof(ice.IceIndex) == 20 * 8
+    assert ctypes.sizeof(ice.IceIndex) == 25 * 8
 
 
 def test_product_never_touches_the_oracle():

@@ -387,3 +387,63 @@ def test_insert_rejected_with_positional_pages():
     with pytest.raises(ice.IceError) as ei:
         ice.ice_insert_tokens(run.params, run.idx, kn, kn, ws, run.err)
     assert ei.value.status == ice.ICE_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("shape,n_sink,n_window", [("llama_bf16", 0, 0), ("tiny_fp32", 0, 0), ("many_units", 0, 0),
+                                                   ("llama_bf16", 32, 96)])
+def test_three_levels_build_and_descent(shape, n_sink, n_window):
+    """n_levels = 3: level-2 promotion exact, level-2 parents tie-aware,
+    children exact, against oracle.build_level2 on the oracle's own build;
+    the descent selection equals oracle.select_descent on units whose
+    structure agrees (fp32 near-ties aside), and the attention over the
+    selected pages matches the oracle, through ice_select_pages and
+    ice_decode_step."""
+    w = {"llama_bf16": W["llama31_8b_16k"].scaled(n_tokens=6003, batch=2, n_q_heads=8, n_kv_heads=2, centres=512),
+         "tiny_fp32": W["tiny"],
+         "many_units": W["qwen3_32b_100k"].scaled(n_tokens=4000, batch=3, centres=256)}[shape]
+    run = GpuRun(w, n_levels=3, n_sink=n_sink, n_window=n_window)
+    assert run.status == ice.ICE_OK
+    th = oracle.promote_threshold(w.promote_p)
+    N, H = w.n_tokens, run.h
+    refs = {}
+    for u in range(run.cfg.units):
+        b, h = run.unit(u)
+        ref = oracle.build_unit_positional(run.K[b, h], run.V[b, h], seed=w.seed, layer=0, seq=b, head=h, thresh=th,
+                                           n_sink=n_sink, n_window=n_window)
+        lv2 = oracle.build_level2(ref, seed=w.seed, layer=0, seq=b, head=h, thresh=th)
+        Np, n2 = len(ref["parent_tok"]), len(lv2["node2"])
+        assert int(H["n_nodes2"][u]) == n2 and np.array_equal(H["node2"][u, :n2], lv2["node2"])
+        p2 = H["parent2"][u, :Np]
+        mism = np.nonzero(p2 != lv2["parent2"])[0]
+        assert len(mism) <= max(1, Np // 1000), (u, len(mism))
+        for m in mism:  # only fp32 near-ties may differ
+            P = np.hstack([ref["parent_keys"], np.asarray(ref["parent_e"])[:, None]])
+            da = ((P[m] - P[lv2["node2"][p2[m]]]) ** 2).sum()
+            do = ((P[m] - P[lv2["node2"][lv2["parent2"][m]]]) ** 2).sum()
+            assert da - do <= 2 * 1e-6 * ref["M2"], (u, m, da, do)
+        if len(mism) == 0:
+            assert np.array_equal(H["child_start"][u, :n2 + 1], lv2["child_start"])
+            assert np.array_equal(H["children"][u, :Np], lv2["children"])
+        if len(mism) == 0 and np.array_equal(H["token_parent"][u, :N], ref["token_parent"]):
+            refs[u] = dict(ref, level2=lv2)
+    assert len(refs) >= run.cfg.units - 1
+    g, scale = run.cfg.group, 1.0 / np.sqrt(128)
+    for bgt in (64, 256):
+        for fused in (True, False):
+            Q, buf, st = run.decode(bgt, fused=fused)
+            assert st == ice.ICE_OK
+            agree = 0
+            for u, ref in refs.items():
+                b, h = run.unit(u)
+                q = Q[b, h * g:(h + 1) * g]
+                cnt = int(buf.sel_count[u])
+                got = buf.sel_pages[u, :cnt].cpu().numpy()
+                assert np.all(np.diff(got) > 0) and np.all(buf.sel_pages[u, cnt:].cpu().numpy() == -1)
+                dec = oracle.decode_unit(ref, q, bgt)
+                agree += np.array_equal(got, dec["sel_pages"])
+                # attention over the GPU's own selection: the oracle's softmax over those pages
+                kb, vb, bl = oracle.gather(ref["pool_k"], ref["pool_v"], ref["page_len"], got)
+                out = oracle.attention(q, kb, vb, bl, scale)
+                gpu = buf.O[b, h * g:(h + 1) * g].cpu().numpy()
+                assert np.max(np.abs(gpu - out)) <= (2e-3 if w.dtype == "bf16" else 1e-5)
+            assert agree >= len(refs) - 1, (agree, len(refs))
