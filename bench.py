@@ -102,8 +102,8 @@ def parse():
                     help="skip the full-size decode and assignment timings (100k-token contexts)")
     ap.add_argument("--at-scale-only", action="store_true",
                     help="run only the full-size timings and print them as one JSON line (profiling runs)")
-    ap.add_argument("--at-scale-parts", default="qwen_decode,longchat_assign,longchat_decode",
-                    help="comma list of qwen_decode, longchat_assign, longchat_decode")
+    ap.add_argument("--at-scale-parts", default="qwen_decode,qwen_decode3,longchat_assign,longchat_decode",
+                    help="comma list of qwen_decode, qwen_decode3, longchat_assign, longchat_decode")
     ap.add_argument("--at-scale-batch", type=int, default=None, help="sequences of the Qwen3-shaped batch (16)")
     ap.add_argument("--at-scale-reps", type=int, default=30)
     return ap.parse_args()
@@ -287,7 +287,8 @@ def whole_job_rate(units_per_rank: int, per_unit: int, steps: int, world: int, m
 
 
 # ------------------------------------------------------------- our arm ----
-def at_scale(pk, reps: int = 30, parts=("qwen_decode", "longchat_assign", "longchat_decode"), qwen_batch=None):
+def at_scale(pk, reps: int = 30, parts=("qwen_decode", "qwen_decode3", "longchat_assign", "longchat_decode"),
+             qwen_batch=None):
     """Full-size timings of the two parts the roofline targets are quoted on:
     the decode step (select + gather + sparse attention) of the Qwen3-32B-
     shaped batch (16 sequences x 8 KV heads, 100k tokens, budget 256) and of
@@ -330,9 +331,9 @@ def at_scale(pk, reps: int = 30, parts=("qwen_decode", "longchat_assign", "longc
             ts.append(a.elapsed_time(b))
         return statistics.median(ts)  # ms
 
-    def build(w):
+    def build(w, n_levels=2):
         cfg = ice.Config(batch=w.batch, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, n_tokens=w.n_tokens,
-                         dtype=ice.ICE_BF16, promote_p=w.promote_p, seed=w.seed)
+                         dtype=ice.ICE_BF16, promote_p=w.promote_p, seed=w.seed, n_levels=n_levels)
         K, V, C = workloads.batch_kv_device(w)
         Q = workloads.batch_queries_device(w, C)
         del C
@@ -387,6 +388,32 @@ def at_scale(pk, reps: int = 30, parts=("qwen_decode", "longchat_assign", "longc
         out[key] = decode(cfg, p, Q, idx, err, max(w.budgets))
         out[key]["status"] = ice.ice_status_string(ice.ice_check(err))
         del cfg, p, Q, idx, err
+        torch.cuda.empty_cache()
+    # Qwen3-32B shape with a third index level: the descent reads the level-2
+    # table and the chosen nodes' children instead of the whole parent table
+    if "qwen_decode3" in parts:
+        w = workloads.WORKLOADS["qwen3_32b_100k"]
+        if qwen_batch:
+            w = w.scaled(batch=qwen_batch)
+        cfg, p, K, V, Q, idx, ws, err = build(w, n_levels=3)
+        del K, V, ws
+        budget = max(w.budgets)
+        buf = ice.DecodeBuffers(cfg, budget)
+        scale = 1.0 / math.sqrt(cfg.head_dim)
+        ms = timed(lambda: ice.ice_decode_step(p, idx, Q, budget, buf.sel_pages, buf.sel_count, buf.kbuf, buf.vbuf,
+                                               buf.buf_len, scale, buf.O, buf.ws, err))
+        ms_nb = timed(lambda: ice.ice_decode_step(p, idx, Q, budget, buf.sel_pages, buf.sel_count, None, None, None,
+                                                  scale, buf.O, buf.ws, err))
+        ms_sel = timed(lambda: ice.ice_select_pages(p, idx, Q, budget, buf.sel_pages, buf.sel_count, buf.ws, err))
+        n2 = int(idx.n_nodes2.sum())
+        sel_tot = int(buf.sel_count.sum())
+        out[f"decode3_qwen3_32b_100k_b{w.batch}"] = {
+            "us": 1000 * ms, "no_buffer_us": 1000 * ms_nb, "select_only_us": 1000 * ms_sel, "budget_tokens": budget,
+            "level2_nodes": n2, "parents": int(idx.n_parents.sum()), "selected_pages": sel_tot,
+            "what": "n_levels = 3: per head the best k level-2 nodes, then their children; the level-2 table "
+                    f"({n2 * 256 / 1e6:.1f} MB) replaces the parent-table scan",
+            "status": ice.ice_status_string(ice.ice_check(err))}
+        del cfg, p, Q, idx, err, buf
         torch.cuda.empty_cache()
     # LongChat-7B shape: the assignment contraction at 100k tokens, then decode
     if "longchat_assign" in parts or "longchat_decode" in parts:

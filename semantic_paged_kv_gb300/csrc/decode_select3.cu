@@ -8,12 +8,15 @@
 // largest q.p.
 //
 // k_select3: one CTA per unit, one warp per query head (at least 4 warps).
-//   1. score every level-2 node (a warp-wide dot product per node, the
-//      unit's scores in the decode workspace);
-//   2. its best k nodes in (-score, i) order: k rounds of a warp maximum
-//      below the previous round's key;
-//   3. their children, scored the same way, 32 at a time: each batch sorted
-//      (bitonic, one key per lane) and merged into the running best 32;
+//   1. every level-2 node scored against all g queries by one thread (its
+//      row loaded once, the queries in shared memory), the scores in shared
+//      memory (in the decode workspace for very large level-2 tables);
+//   2. per head its best k nodes in (-score, i) order: k rounds of a warp
+//      maximum below the previous round's key;
+//   3. their children: the ids staged in shared memory (all loads in flight),
+//      then one per lane (each lane loads its child's row), 32 at a time:
+//      each batch sorted (bitonic, one key per lane) and merged into the
+//      running best 32;
 //   4. the ordered best k parents give their pages (page-id order inside a
 //      parent) until k pages, ORed into the union bitmask;
 //   5. positional pages ORed in, then the ascending list (block scan).
@@ -26,15 +29,31 @@ namespace {
 
 using namespace topk;
 
-// q . row for a 128-dim row, lane holding q's dimensions 4 lane .. 4 lane + 3;
-// every lane gets the sum.
+constexpr int kCandPerWarp = 256;               // candidate parent ids a warp stages at a time
+constexpr int kMaxCand = 16 * kCandPerWarp;     // for up to 16 warps
+constexpr size_t kS2Smem = 16 * 1024;           // shared memory for the level-2 scores of all heads
+
+// q . row for a 128-dim key row and q in shared memory (fp32): the row is
+// loaded in two halves, each half's 16-byte loads issued before its
+// arithmetic.
 template <typename T>
-__device__ __forceinline__ float warp_dot(const float (&q)[4], const T *__restrict__ row, int lane) {
+__device__ __forceinline__ float row_dot(const T *__restrict__ row, const float *__restrict__ q) {
+    constexpr int PV = Elem<T>::kPerVec;
+    constexpr int HV = row_vecs<T>() / 2;  // vectors per half row
     float a = 0.f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) a = fmaf(q[i], Elem<T>::load(row + 4 * lane + i), a);
+    for (int half = 0; half < 2; ++half) {
+        uint4 r[HV];
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+        for (int v = 0; v < HV; ++v) r[v] = __ldg(reinterpret_cast<const uint4 *>(row) + half * HV + v);
+#pragma unroll
+        for (int v = 0; v < HV; ++v) {
+            float f[PV];
+            Elem<T>::unpack(r[v], f);
+#pragma unroll
+            for (int i = 0; i < PV; ++i) a = fmaf(f[i], q[(half * HV + v) * PV + i], a);
+        }
+    }
     return a;
 }
 
@@ -55,7 +74,7 @@ __device__ __forceinline__ unsigned long long sort32_desc(unsigned long long v) 
 }
 
 template <typename T>
-__global__ void k_select3(const T *__restrict__ Q, int g, int n_q_heads, int n_kv_heads, int np_cap, int page_cap,
+__global__ void __launch_bounds__(512) k_select3(const T *__restrict__ Q, int g, int n_q_heads, int n_kv_heads, int np_cap, int page_cap,
                           int k_pages, int n_pos, const int32_t *__restrict__ n_pages,
                           const int32_t *__restrict__ n_nodes2, const int32_t *__restrict__ node2,
                           const int32_t *__restrict__ child_start, const int32_t *__restrict__ children,
@@ -63,10 +82,14 @@ __global__ void k_select3(const T *__restrict__ Q, int g, int n_q_heads, int n_k
                           const int32_t *__restrict__ parent_last_page, const int32_t *__restrict__ parent_n_pages,
                           const int32_t *__restrict__ page_next, float *__restrict__ scores,
                           int32_t *__restrict__ sel_pages, int32_t *__restrict__ sel_count, int max_sel,
-                          int32_t *__restrict__ err) {
+                          int s2_cap, int32_t *__restrict__ err) {
     dep_wait();  // the index and Q are complete
-    extern __shared__ unsigned s_mask[];  // union bitmask over the unit's pages
+    extern __shared__ float s_q[];  // [g][128] the group's queries (fp32), then [g][s2_cap] level-2 scores
+    float *s_s2 = s_q + g * kHeadDim;
+    unsigned *s_mask = reinterpret_cast<unsigned *>(s_s2 + (size_t)g * s2_cap);  // union bitmask over the unit's pages
+    __shared__ int s_cand[kMaxCand];  // [kMaxCand] one head's candidate parents at a time (warp-private slices)
     __shared__ int s_wsum[32];
+    __shared__ int s_g0[16][32], s_gn[16][32], s_gend[16][32];  // per warp: the chosen level-2 groups
     const int u = blockIdx.x;
     const int b = u / n_kv_heads, h = u % n_kv_heads;
     const int nt = blockDim.x, nw = nt >> 5;
@@ -76,23 +99,52 @@ __global__ void k_select3(const T *__restrict__ Q, int g, int n_q_heads, int n_k
     const int Ps = max(0, P - n_pos);
     const int n2 = min(n_nodes2[u], np_cap);
     const int words = (P + 31) / 32;
+    const T *Pu = parent_keys + up * kHeadDim;
     for (int x = threadIdx.x; x < words; x += nt) s_mask[x] = 0u;
+    for (int x = threadIdx.x; x < g * kHeadDim; x += nt)
+        s_q[x] = Elem<T>::load(Q + ((size_t)b * n_q_heads + (size_t)h * g) * kHeadDim + x);
     __syncthreads();
     for (int x = Ps + threadIdx.x; x < P; x += nt) atomicOr(&s_mask[x >> 5], 1u << (x & 31));
-    const T *Pu = parent_keys + up * kHeadDim;
-    for (int hh = warp; hh < g && Ps > 0; hh += nw) {
-        float q[4];
-        const T *qrow = Q + ((size_t)b * n_q_heads + (size_t)h * g + hh) * kHeadDim;
+    // 1. level-2 scores of every head: a thread per level-2 node, its row loaded once
+    // the scores live in shared memory when the unit's level-2 table fits, else in the workspace
+    const bool in_smem = n2 <= s2_cap;
+    float *su = in_smem ? s_s2 : scores + (size_t)u * g * np_cap;
+    const int ld2 = in_smem ? s2_cap : np_cap;
+    for (int i = threadIdx.x; i < n2 && Ps > 0; i += nt) {
+        const T *row = Pu + (size_t)node2[up + i] * kHeadDim;
+        float acc[16];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) q[i] = Elem<T>::load(qrow + 4 * lane + i);
-        // 1. level-2 scores
-        float *s2 = scores + ((size_t)u * g + hh) * np_cap;
-        for (int i = 0; i < n2; ++i) {
-            const float sc = warp_dot<T>(q, Pu + (size_t)node2[up + i] * kHeadDim, lane);
-            if (lane == 0) s2[i] = sc;
+        for (int hh = 0; hh < 16; ++hh) acc[hh] = 0.f;
+        constexpr int PV = Elem<T>::kPerVec;
+        constexpr int HV = row_vecs<T>() / 2;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {  // each half row loaded once for all heads
+            uint4 r[HV];
+#pragma unroll
+            for (int v = 0; v < HV; ++v) r[v] = __ldg(reinterpret_cast<const uint4 *>(row) + half * HV + v);
+#pragma unroll
+            for (int v = 0; v < HV; ++v) {
+                float f[PV];
+                Elem<T>::unpack(r[v], f);
+#pragma unroll
+                for (int hh = 0; hh < 16; ++hh) {
+                    if (hh < g) {
+                        const float *qh = s_q + hh * kHeadDim + (half * HV + v) * PV;
+#pragma unroll
+                        for (int e = 0; e < PV; ++e) acc[hh] = fmaf(f[e], qh[e], acc[hh]);
+                    }
+                }
+            }
         }
-        __syncwarp();
-        // 2. the best kc level-2 nodes: lane r gets the r-th best key
+#pragma unroll
+        for (int hh = 0; hh < 16; ++hh)
+            if (hh < g) su[(size_t)hh * ld2 + i] = acc[hh];
+    }
+    __syncthreads();  // the block's score writes are visible to the whole block
+    for (int hh = warp; hh < g && Ps > 0; hh += nw) {
+        const float *qh = s_q + hh * kHeadDim;
+        const float *s2 = su + (size_t)hh * ld2;
+        // 2. the best kc level-2 nodes: lane r gets the r-th best (score, -i) key
         const int kc = min(k_pages, n2);
         unsigned long long last = ~0ull, top = 0ull;
         for (int r = 0; r < kc; ++r) {
@@ -106,25 +158,47 @@ __global__ void k_select3(const T *__restrict__ Q, int g, int n_q_heads, int n_k
             if (lane == r) top = best;
             last = best;
         }
-        // 3. their children, 32 at a time, merged into the running best 32
-        unsigned long long run = 0ull;  // lane r: r-th best (score, -m) key so far
-        unsigned long long batch = 0ull;
-        int nb = 0;
-        for (int r = 0; r < kc; ++r) {
-            const int i = key_id(__shfl_sync(0xffffffffu, top, r));
-            const int c0 = child_start[(size_t)u * (np_cap + 1) + i], c1 = child_start[(size_t)u * (np_cap + 1) + i + 1];
-            for (int c = c0; c < c1; ++c) {
-                const int m = children[up + c];
-                const float sc = warp_dot<T>(q, Pu + (size_t)m * kHeadDim, lane);
-                if (lane == nb) batch = sort_key(sc, m);
-                if (++nb == 32) {
-                    run = merge32(run, sort32_desc(batch));
-                    batch = 0ull;
-                    nb = 0;
-                }
-            }
+        // 3. their children: lane r < kc holds group r's range; candidates go
+        //    32 at a time, one per lane, each lane loading its child's row
+        int g0 = 0, gn = 0;
+        if (lane < kc) {
+            const int i = key_id(top);
+            g0 = child_start[(size_t)u * (np_cap + 1) + i];
+            gn = child_start[(size_t)u * (np_cap + 1) + i + 1] - g0;
         }
-        if (nb > 0) run = merge32(run, sort32_desc(lane < nb ? batch : 0ull));
+        int gend = gn;  // inclusive scan of the group sizes
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int x = __shfl_up_sync(0xffffffffu, gend, o);
+            if (lane >= o) gend += x;
+        }
+        const int C = __shfl_sync(0xffffffffu, gend, 31);
+        s_g0[warp][lane] = g0;
+        s_gn[warp][lane] = gn;
+        s_gend[warp][lane] = gend;
+        __syncwarp();
+        unsigned long long run = 0ull;  // lane r: r-th best (score, -m) parent so far
+        int *cand = s_cand + (size_t)warp * kCandPerWarp;
+        for (int c0 = 0; c0 < C; c0 += kCandPerWarp) {
+            const int cn = min(kCandPerWarp, C - c0);
+            // the slice's candidate ids, all loads in flight at once
+            for (int x = lane; x < cn; x += 32) {
+                const int c = c0 + x;
+                int grp = 0;
+                for (int j = 0; j < kc; ++j) grp += (j < 32 ? s_gend[warp][j] : 0) <= c;
+                cand[x] = children[up + s_g0[warp][grp] + (c - (s_gend[warp][grp] - s_gn[warp][grp]))];
+            }
+            __syncwarp();
+            for (int x0 = 0; x0 < cn; x0 += 32) {
+                unsigned long long key = 0ull;
+                if (x0 + lane < cn) {
+                    const int m = cand[x0 + lane];
+                    key = sort_key(row_dot<T>(Pu + (size_t)m * kHeadDim, qh), m);
+                }
+                run = merge32(run, sort32_desc(key));
+            }
+            __syncwarp();
+        }
         // 4. pages of the ordered parents until k pages
         int pm = -1, fp = 0, pc = 0, contig = 1;
         if (lane < k_pages && run != 0ull) {
@@ -187,7 +261,8 @@ cudaError_t launch_t(const ice_params &p, const ice_index &idx, const void *Q, c
                      int32_t *sel_count, int max_sel, int32_t *err, cudaStream_t s) {
     const int g = p.n_q_heads / p.n_kv_heads;
     const int nw = g < 4 ? 4 : g;
-    const size_t smem = sizeof(unsigned) * (size_t)((p.page_cap + 31) / 32);
+    const int s2_cap = (int)(kS2Smem / sizeof(float) / g);
+    const size_t smem = sizeof(float) * (size_t)g * (kHeadDim + s2_cap) + sizeof(unsigned) * (size_t)((p.page_cap + 31) / 32);
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(k_select3<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
@@ -196,7 +271,7 @@ cudaError_t launch_t(const ice_params &p, const ice_index &idx, const void *Q, c
         k_select3<T>, dim3(units_of(p)), dim3(32 * nw), smem, s, static_cast<const T *>(Q), g, p.n_q_heads,
         p.n_kv_heads, p.np_cap, p.page_cap, ws.k_pages, pos_split(p).n_pos, idx.n_pages, idx.n_nodes2, idx.node2,
         idx.child_start, idx.children, static_cast<const T *>(idx.parent_keys), idx.parent_first_page,
-        idx.parent_last_page, idx.parent_n_pages, idx.page_next, ws.scores, sel_pages, sel_count, max_sel, err);
+        idx.parent_last_page, idx.parent_n_pages, idx.page_next, ws.scores, sel_pages, sel_count, max_sel, s2_cap, err);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
