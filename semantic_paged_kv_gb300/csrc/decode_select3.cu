@@ -263,7 +263,7 @@ cudaError_t launch_t(const ice_params &p, const ice_index &idx, const void *Q, c
     const int nw = g < 4 ? 4 : g;
     const int s2_cap = (int)(kS2Smem / sizeof(float) / g);
     const size_t smem = sizeof(float) * (size_t)g * (kHeadDim + s2_cap) + sizeof(unsigned) * (size_t)((p.page_cap + 31) / 32);
-    if (smem > 48 * 1024) {
+    {  // static shared memory comes on top: always opt in to the dynamic size
         cudaError_t e = cudaFuncSetAttribute(k_select3<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
