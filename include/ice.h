@@ -291,7 +291,8 @@ ice_status ice_insert_workspace_bytes(const ice_params *p, size_t *bytes);
  * after it (page_next) when that page already holds S tokens.  Existing
  * tokens never move.  Updates every index array and the pool.
  * ICE_ERR_CAPACITY in err_dev (and that unit left unchanged) if n_cap,
- * np_cap or page_cap would be exceeded.
+ * np_cap or page_cap would be exceeded.  ICE_ERR_UNSUPPORTED (nothing
+ * launched) with n_levels = 3 or with sink / window pages.
  */
 ice_status ice_insert_tokens(const ice_params *p, const ice_index *idx, const void *k_new, const void *v_new,
                              void *ws, size_t ws_bytes, int32_t *err_dev, void *stream);
