@@ -143,8 +143,9 @@ DecodeWs decode_ws_layout(const ice_params &p, int budget_tokens, int max_sel, v
     };
     w.sel_ticket = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * U));
     w.attn_ticket = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * U));
-    w.cand_key = reinterpret_cast<unsigned long long *>(
-        take(sizeof(unsigned long long) * U * w.n_chunks * g * (kc ? kc : 1)));
+    // (also the per-head page lists [U, g, 32] int32 of the three-level descent)
+    const size_t ck = sizeof(unsigned long long) * U * w.n_chunks * g * (kc ? kc : 1);
+    w.cand_key = reinterpret_cast<unsigned long long *>(take(ck > sizeof(int32_t) * U * g * 32 ? ck : sizeof(int32_t) * U * g * 32));
     w.cand_span = reinterpret_cast<int4 *>(take(sizeof(int4) * U * w.n_chunks * kSelChunk));
     w.part_ml = reinterpret_cast<float *>(take(sizeof(float) * U * w.n_splits * g * 2));
     w.part_o = reinterpret_cast<float *>(take(sizeof(float) * U * w.n_splits * g * kHeadDim));

@@ -7,19 +7,18 @@
 // union.  With the lifted query q' = [q, 0] the nearest points are those of
 // largest q.p.
 //
-// k_select3: one CTA per unit, one warp per query head (at least 4 warps).
-//   1. every level-2 node scored against all g queries by one thread (its
-//      row loaded once, the queries in shared memory), the scores in shared
-//      memory (in the decode workspace for very large level-2 tables);
-//   2. per head its best k nodes in (-score, i) order: k rounds of a warp
+// k_select3: one CTA per (query head, unit), 4 warps:
+//   1. the head's score of every level-2 node (one thread per node row), in
+//      shared memory (in the decode workspace for very large level-2 tables);
+//   2. warp 0: the best k nodes in (-score, i) order, k rounds of a warp
 //      maximum below the previous round's key;
-//   3. their children: the ids staged in shared memory (all loads in flight),
-//      then one per lane (each lane loads its child's row), 32 at a time:
-//      each batch sorted (bitonic, one key per lane) and merged into the
-//      running best 32;
-//   4. the ordered best k parents give their pages (page-id order inside a
-//      parent) until k pages, ORed into the union bitmask;
-//   5. positional pages ORed in, then the ascending list (block scan).
+//   3. their children spread over the 4 warps, one child per lane (each lane
+//      loads its child's row), batches sorted (bitonic) and merged into each
+//      warp's running best 32; the 4 lists merged by warp 0;
+//   4. warp 0: the ordered best k parents' pages (page-id order inside a
+//      parent) until k pages, written as the head's page list;
+//   5. the unit's last CTA (atomic ticket) ORs the g lists and the
+//      positional pages into a bitmask and writes the ascending union.
 #include "common.cuh"
 #include "internal.h"
 #include "topk_common.cuh"
@@ -29,9 +28,7 @@ namespace {
 
 using namespace topk;
 
-constexpr int kCandPerWarp = 256;               // candidate parent ids a warp stages at a time
-constexpr int kMaxCand = 16 * kCandPerWarp;     // for up to 16 warps
-constexpr size_t kS2Smem = 16 * 1024;           // shared memory for the level-2 scores of all heads
+constexpr size_t kS2Smem = 16 * 1024;  // shared memory for one head's level-2 scores
 
 // q . row for a 128-dim key row and q in shared memory (fp32): the row is
 // loaded in two halves, each half's 16-byte loads issued before its
@@ -74,157 +71,144 @@ __device__ __forceinline__ unsigned long long sort32_desc(unsigned long long v) 
 }
 
 template <typename T>
-__global__ void __launch_bounds__(512) k_select3(const T *__restrict__ Q, int g, int n_q_heads, int n_kv_heads, int np_cap, int page_cap,
-                          int k_pages, int n_pos, const int32_t *__restrict__ n_pages,
-                          const int32_t *__restrict__ n_nodes2, const int32_t *__restrict__ node2,
-                          const int32_t *__restrict__ child_start, const int32_t *__restrict__ children,
-                          const T *__restrict__ parent_keys, const int32_t *__restrict__ parent_first_page,
-                          const int32_t *__restrict__ parent_last_page, const int32_t *__restrict__ parent_n_pages,
-                          const int32_t *__restrict__ page_next, float *__restrict__ scores,
-                          int32_t *__restrict__ sel_pages, int32_t *__restrict__ sel_count, int max_sel,
-                          int s2_cap, int32_t *__restrict__ err) {
+__global__ void __launch_bounds__(128) k_select3(const T *__restrict__ Q, int g, int n_q_heads, int n_kv_heads,
+                                                 int np_cap, int page_cap, int k_pages, int n_pos,
+                                                 const int32_t *__restrict__ n_pages,
+                                                 const int32_t *__restrict__ n_nodes2, const int32_t *__restrict__ node2,
+                                                 const int32_t *__restrict__ child_start,
+                                                 const int32_t *__restrict__ children,
+                                                 const T *__restrict__ parent_keys,
+                                                 const int32_t *__restrict__ parent_first_page,
+                                                 const int32_t *__restrict__ parent_last_page,
+                                                 const int32_t *__restrict__ parent_n_pages,
+                                                 const int32_t *__restrict__ page_next, float *__restrict__ scores,
+                                                 int32_t *__restrict__ head_pages, int32_t *__restrict__ ticket,
+                                                 int32_t *__restrict__ sel_pages, int32_t *__restrict__ sel_count,
+                                                 int max_sel, int s2_cap, int32_t *__restrict__ err) {
     dep_wait();  // the index and Q are complete
-    extern __shared__ float s_q[];  // [g][128] the group's queries (fp32), then [g][s2_cap] level-2 scores
-    float *s_s2 = s_q + g * kHeadDim;
-    unsigned *s_mask = reinterpret_cast<unsigned *>(s_s2 + (size_t)g * s2_cap);  // union bitmask over the unit's pages
-    __shared__ int s_cand[kMaxCand];  // [kMaxCand] one head's candidate parents at a time (warp-private slices)
-    __shared__ int s_wsum[32];
-    __shared__ int s_g0[16][32], s_gn[16][32], s_gend[16][32];  // per warp: the chosen level-2 groups
-    const int u = blockIdx.x;
+    constexpr int kW = 4, kT = 32 * kW;
+    extern __shared__ float s_s2[];  // [s2_cap] this head's level-2 scores, then the union bitmask (last CTA)
+    __shared__ float s_q[kHeadDim];
+    __shared__ unsigned long long s_best[kW][32];
+    __shared__ int s_g0[32], s_gn[32], s_gend[32], s_wsum[kW];
+    __shared__ int s_last;
+    const int hh = blockIdx.x, u = blockIdx.y;
     const int b = u / n_kv_heads, h = u % n_kv_heads;
-    const int nt = blockDim.x, nw = nt >> 5;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const size_t up = (size_t)u * np_cap, ug = (size_t)u * page_cap;
     const int P = min(n_pages[u], page_cap);
     const int Ps = max(0, P - n_pos);
     const int n2 = min(n_nodes2[u], np_cap);
-    const int words = (P + 31) / 32;
     const T *Pu = parent_keys + up * kHeadDim;
-    for (int x = threadIdx.x; x < words; x += nt) s_mask[x] = 0u;
-    for (int x = threadIdx.x; x < g * kHeadDim; x += nt)
-        s_q[x] = Elem<T>::load(Q + ((size_t)b * n_q_heads + (size_t)h * g) * kHeadDim + x);
+    int32_t *hl = head_pages + ((size_t)u * g + hh) * 32;  // this head's page list (-1 padded)
+    for (int x = threadIdx.x; x < kHeadDim; x += kT)
+        s_q[x] = Elem<T>::load(Q + ((size_t)b * n_q_heads + (size_t)h * g + hh) * kHeadDim + x);
     __syncthreads();
-    for (int x = Ps + threadIdx.x; x < P; x += nt) atomicOr(&s_mask[x >> 5], 1u << (x & 31));
-    // 1. level-2 scores of every head: a thread per level-2 node, its row loaded once
-    // the scores live in shared memory when the unit's level-2 table fits, else in the workspace
-    const bool in_smem = n2 <= s2_cap;
-    float *su = in_smem ? s_s2 : scores + (size_t)u * g * np_cap;
-    const int ld2 = in_smem ? s2_cap : np_cap;
-    for (int i = threadIdx.x; i < n2 && Ps > 0; i += nt) {
-        const T *row = Pu + (size_t)node2[up + i] * kHeadDim;
-        float acc[16];
-#pragma unroll
-        for (int hh = 0; hh < 16; ++hh) acc[hh] = 0.f;
-        constexpr int PV = Elem<T>::kPerVec;
-        constexpr int HV = row_vecs<T>() / 2;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {  // each half row loaded once for all heads
-            uint4 r[HV];
-#pragma unroll
-            for (int v = 0; v < HV; ++v) r[v] = __ldg(reinterpret_cast<const uint4 *>(row) + half * HV + v);
-#pragma unroll
-            for (int v = 0; v < HV; ++v) {
-                float f[PV];
-                Elem<T>::unpack(r[v], f);
-#pragma unroll
-                for (int hh = 0; hh < 16; ++hh) {
-                    if (hh < g) {
-                        const float *qh = s_q + hh * kHeadDim + (half * HV + v) * PV;
-#pragma unroll
-                        for (int e = 0; e < PV; ++e) acc[hh] = fmaf(f[e], qh[e], acc[hh]);
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int hh = 0; hh < 16; ++hh)
-            if (hh < g) su[(size_t)hh * ld2 + i] = acc[hh];
-    }
-    __syncthreads();  // the block's score writes are visible to the whole block
-    for (int hh = warp; hh < g && Ps > 0; hh += nw) {
-        const float *qh = s_q + hh * kHeadDim;
-        const float *s2 = su + (size_t)hh * ld2;
-        // 2. the best kc level-2 nodes: lane r gets the r-th best (score, -i) key
+    if (Ps > 0) {
+        // 1. level-2 scores
+        const bool in_smem = n2 <= s2_cap;
+        float *su = in_smem ? s_s2 : scores + ((size_t)u * g + hh) * np_cap;
+        for (int i = threadIdx.x; i < n2; i += kT) su[i] = row_dot<T>(Pu + (size_t)node2[up + i] * kHeadDim, s_q);
+        __syncthreads();
+        // 2. the best kc level-2 nodes and their child ranges
         const int kc = min(k_pages, n2);
-        unsigned long long last = ~0ull, top = 0ull;
-        for (int r = 0; r < kc; ++r) {
-            unsigned long long best = 0ull;
-            for (int i = lane; i < n2; i += 32) {
-                const unsigned long long k = sort_key(s2[i], i);
-                if (k < last && k > best) best = k;
-            }
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) best = umax64(best, __shfl_xor_sync(0xffffffffu, best, o));
-            if (lane == r) top = best;
-            last = best;
-        }
-        // 3. their children: lane r < kc holds group r's range; candidates go
-        //    32 at a time, one per lane, each lane loading its child's row
-        int g0 = 0, gn = 0;
-        if (lane < kc) {
-            const int i = key_id(top);
-            g0 = child_start[(size_t)u * (np_cap + 1) + i];
-            gn = child_start[(size_t)u * (np_cap + 1) + i + 1] - g0;
-        }
-        int gend = gn;  // inclusive scan of the group sizes
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int x = __shfl_up_sync(0xffffffffu, gend, o);
-            if (lane >= o) gend += x;
-        }
-        const int C = __shfl_sync(0xffffffffu, gend, 31);
-        s_g0[warp][lane] = g0;
-        s_gn[warp][lane] = gn;
-        s_gend[warp][lane] = gend;
-        __syncwarp();
-        unsigned long long run = 0ull;  // lane r: r-th best (score, -m) parent so far
-        int *cand = s_cand + (size_t)warp * kCandPerWarp;
-        for (int c0 = 0; c0 < C; c0 += kCandPerWarp) {
-            const int cn = min(kCandPerWarp, C - c0);
-            // the slice's candidate ids, all loads in flight at once
-            for (int x = lane; x < cn; x += 32) {
-                const int c = c0 + x;
-                int grp = 0;
-                for (int j = 0; j < kc; ++j) grp += (j < 32 ? s_gend[warp][j] : 0) <= c;
-                cand[x] = children[up + s_g0[warp][grp] + (c - (s_gend[warp][grp] - s_gn[warp][grp]))];
-            }
-            __syncwarp();
-            for (int x0 = 0; x0 < cn; x0 += 32) {
-                unsigned long long key = 0ull;
-                if (x0 + lane < cn) {
-                    const int m = cand[x0 + lane];
-                    key = sort_key(row_dot<T>(Pu + (size_t)m * kHeadDim, qh), m);
+        if (warp == 0) {
+            unsigned long long last = ~0ull, top = 0ull;
+            for (int r = 0; r < kc; ++r) {
+                unsigned long long best = 0ull;
+                for (int i = lane; i < n2; i += 32) {
+                    const unsigned long long k = sort_key(su[i], i);
+                    if (k < last && k > best) best = k;
                 }
-                run = merge32(run, sort32_desc(key));
-            }
-            __syncwarp();
-        }
-        // 4. pages of the ordered parents until k pages
-        int pm = -1, fp = 0, pc = 0, contig = 1;
-        if (lane < k_pages && run != 0ull) {
-            pm = key_id(run);
-            fp = parent_first_page[up + pm];
-            pc = parent_n_pages[up + pm];
-            contig = parent_last_page[up + pm] - fp + 1 == pc;
-        }
-        int incl = pc;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int x = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += x;
+                for (int o = 16; o >= 1; o >>= 1) best = umax64(best, __shfl_xor_sync(0xffffffffu, best, o));
+                if (lane == r) top = best;
+                last = best;
+            }
+            int g0 = 0, gn = 0;
+            if (lane < kc) {
+                const int i = key_id(top);
+                g0 = child_start[(size_t)u * (np_cap + 1) + i];
+                gn = child_start[(size_t)u * (np_cap + 1) + i + 1] - g0;
+            }
+            int gend = gn;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int x = __shfl_up_sync(0xffffffffu, gend, o);
+                if (lane >= o) gend += x;
+            }
+            s_g0[lane] = g0;
+            s_gn[lane] = gn;
+            s_gend[lane] = gend;
         }
-        const int tk = max(0, min(pc, k_pages - (incl - pc)));
-        int pg = fp;
-        for (int t = 0; t < tk; ++t) {
-            const int qq = contig ? fp + t : pg;
-            if (qq < 0 || qq >= Ps) break;
-            atomicOr(&s_mask[qq >> 5], 1u << (qq & 31));
-            if (!contig) pg = page_next[ug + qq];
+        __syncthreads();
+        // 3. the children over the 4 warps, one per lane
+        const int C = s_gend[31];
+        unsigned long long run = 0ull;
+        for (int c0 = warp * 32; c0 < C; c0 += kT) {
+            const int c = c0 + lane;
+            unsigned long long key = 0ull;
+            if (c < C) {
+                int grp = 0;  // the first group whose inclusive end exceeds c
+                while (grp < kc - 1 && s_gend[grp] <= c) ++grp;
+                const int m = children[up + s_g0[grp] + (c - (s_gend[grp] - s_gn[grp]))];
+                key = sort_key(row_dot<T>(Pu + (size_t)m * kHeadDim, s_q), m);
+            }
+            run = merge32(run, sort32_desc(key));
         }
+        s_best[warp][lane] = run;
+        __syncthreads();
+        // 4. warp 0: the best parents of the 4 lists, then their pages
+        if (warp == 0) {
+            unsigned long long r = s_best[0][lane];
+#pragma unroll
+            for (int w = 1; w < kW; ++w) r = merge32(r, s_best[w][lane]);
+            int fp = 0, pc = 0, contig = 1;
+            if (lane < k_pages && r != 0ull) {
+                const int pm = key_id(r);
+                fp = parent_first_page[up + pm];
+                pc = parent_n_pages[up + pm];
+                contig = parent_last_page[up + pm] - fp + 1 == pc;
+            }
+            int incl = pc;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int x = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += x;
+            }
+            const int tk = max(0, min(pc, k_pages - (incl - pc)));
+            hl[lane] = -1;
+            __syncwarp();
+            int pg = fp;
+            for (int t = 0; t < tk; ++t) {
+                const int qq = contig ? fp + t : pg;
+                if (qq < 0 || qq >= Ps) break;
+                hl[incl - pc + t] = qq;
+                if (!contig) pg = page_next[ug + qq];
+            }
+        }
+    } else {
+        for (int x = threadIdx.x; x < 32; x += kT) hl[x] = -1;
+    }
+    // 5. the unit's last CTA forms the union
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(ticket + u, 1) == g - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    unsigned *s_mask = reinterpret_cast<unsigned *>(s_s2);
+    const int words = (P + 31) / 32;
+    for (int x = threadIdx.x; x < words; x += kT) s_mask[x] = 0u;
+    __syncthreads();
+    for (int x = Ps + threadIdx.x; x < P; x += kT) atomicOr(&s_mask[x >> 5], 1u << (x & 31));
+    const int32_t *ul = head_pages + (size_t)u * g * 32;
+    for (int x = threadIdx.x; x < g * 32; x += kT) {
+        const int q = __ldcg(ul + x);
+        if (q >= 0 && q < Ps) atomicOr(&s_mask[q >> 5], 1u << (q & 31));
     }
     __syncthreads();
-    // 5. ascending list of the union's pages: thread t owns words [t wpt, (t + 1) wpt)
-    const int wpt = (words + nt - 1) / nt;
+    const int wpt = (words + kT - 1) / kT;
     const int wb = threadIdx.x * wpt, we = min(words, wb + wpt);
     int c = 0;
     for (int x = wb; x < we; ++x) c += __popc(s_mask[x]);
@@ -237,7 +221,7 @@ __global__ void __launch_bounds__(512) k_select3(const T *__restrict__ Q, int g,
     if (lane == 31) s_wsum[warp] = incl;
     __syncthreads();
     int pos = incl - c, total = 0;
-    for (int w = 0; w < nw; ++w) {
+    for (int w = 0; w < kW; ++w) {
         pos += w < warp ? s_wsum[w] : 0;
         total += s_wsum[w];
     }
@@ -249,10 +233,11 @@ __global__ void __launch_bounds__(512) k_select3(const T *__restrict__ Q, int g,
             sel_pages[(size_t)u * max_sel + pos++] = x * 32 + bit;
         }
     }
-    for (int x = total + threadIdx.x; x < max_sel; x += nt) sel_pages[(size_t)u * max_sel + x] = -1;
+    for (int x = total + threadIdx.x; x < max_sel; x += kT) sel_pages[(size_t)u * max_sel + x] = -1;
     if (threadIdx.x == 0) {
         if (total > max_sel) set_err(err, ICE_ERR_CAPACITY);
         sel_count[u] = min(total, max_sel);
+        ticket[u] = 0;  // every CTA of the unit has counted: ready for the next call
     }
 }
 
@@ -260,18 +245,22 @@ template <typename T>
 cudaError_t launch_t(const ice_params &p, const ice_index &idx, const void *Q, const DecodeWs &ws, int32_t *sel_pages,
                      int32_t *sel_count, int max_sel, int32_t *err, cudaStream_t s) {
     const int g = p.n_q_heads / p.n_kv_heads;
-    const int nw = g < 4 ? 4 : g;
-    const int s2_cap = (int)(kS2Smem / sizeof(float) / g);
-    const size_t smem = sizeof(float) * (size_t)g * (kHeadDim + s2_cap) + sizeof(unsigned) * (size_t)((p.page_cap + 31) / 32);
+    const int s2_cap = (int)(kS2Smem / sizeof(float));
+    const size_t mask = sizeof(unsigned) * (size_t)((p.page_cap + 31) / 32);
+    const size_t smem = sizeof(float) * (size_t)s2_cap > mask ? sizeof(float) * (size_t)s2_cap : mask;
+    if (smem > 200 * 1024) return cudaErrorNotSupported;
     {  // static shared memory comes on top: always opt in to the dynamic size
         cudaError_t e = cudaFuncSetAttribute(k_select3<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
+    // the heads' page lists ([U, g, 32] int32) live in the candidate-key area of the workspace
+    int32_t *head_pages = reinterpret_cast<int32_t *>(ws.cand_key);
     const cudaError_t e = launch_dependent(
-        k_select3<T>, dim3(units_of(p)), dim3(32 * nw), smem, s, static_cast<const T *>(Q), g, p.n_q_heads,
+        k_select3<T>, dim3(g, units_of(p)), dim3(128), smem, s, static_cast<const T *>(Q), g, p.n_q_heads,
         p.n_kv_heads, p.np_cap, p.page_cap, ws.k_pages, pos_split(p).n_pos, idx.n_pages, idx.n_nodes2, idx.node2,
         idx.child_start, idx.children, static_cast<const T *>(idx.parent_keys), idx.parent_first_page,
-        idx.parent_last_page, idx.parent_n_pages, idx.page_next, ws.scores, sel_pages, sel_count, max_sel, s2_cap, err);
+        idx.parent_last_page, idx.parent_n_pages, idx.page_next, ws.scores, head_pages, ws.sel_ticket, sel_pages,
+        sel_count, max_sel, s2_cap, err);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
