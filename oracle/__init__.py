@@ -320,7 +320,7 @@ def build_unit_positional(K, V, *, seed: int, layer: int, seq: int, head: int, t
     e[se:ws] = e_m
     return dict(n=n_m, M2=M2, e=e, parent_tok=parent_tok, parent_keys=K[parent_tok] if Np else K[:0],
                 parent_e=e[parent_tok] if Np else e[:0], token_parent=token_parent, pool_k=pool_k, pool_v=pool_v,
-                S=S, n_pages=P, n_pos=len(ranges), page_parent=page_parent, page_len=page_len,
+                S=S, n_pages=P, n_pos=len(ranges), split=(se, ws), page_parent=page_parent, page_len=page_len,
                 page_tokens=page_tokens, token_page=token_page, token_slot=token_slot)
 
 
@@ -393,7 +393,9 @@ def build_unit_reuse(K, V, prev: dict, S: int = 16) -> dict:
     is not described, so this is the stated rule): the promoted tokens and
     the token -> parent assignment are prev's; the lift (M^2, e) comes from
     this layer's keys (step a1), the pages from packing prev's assignment
-    (step a4), the pool from this layer's K and V (step a5).  prev must index
+    (step a4), the pool from this layer's K and V (step a5).  With sink /
+    window pages in prev, M is taken over the indexed middle tokens and every
+    page is kept as it is; a third level in prev is kept too.  prev must index
     the same N tokens."""
     K = _f64(K)
     V = _f64(V)
@@ -402,12 +404,22 @@ def build_unit_reuse(K, V, prev: dict, S: int = 16) -> dict:
     token_parent = np.asarray(prev["token_parent"][:N], np.int32)
     if len(token_parent) != N or (len(parent_tok) and (parent_tok.min() < 0 or parent_tok.max() >= N)):
         raise ValueError("prev does not index the same N tokens")
-    n, M2, e = lift(K)
-    pk = pack(token_parent, len(parent_tok), S)
+    extra = {k: prev[k] for k in ("level2",) if k in prev}  # a third level is node structure too: kept
+    if int(prev.get("n_pos", 0)) or "split" in prev:
+        # sink / window pages: M over the indexed (middle) tokens, every page kept as it is
+        se, ws = prev["split"]
+        n, M2, e_m = lift(K[se:ws]) if ws > se else (np.zeros(0), 0.0, np.zeros(0))
+        e = np.full(N, np.nan)
+        e[se:ws] = e_m
+        pk = {f: prev[f] for f in ("n_pages", "n_pos", "split", "page_parent", "page_len", "page_tokens",
+                                   "token_page", "token_slot")}
+    else:
+        n, M2, e = lift(K)
+        pk = pack(token_parent, len(parent_tok), S)
     pool_k, pool_v = scatter(K, V, pk["page_tokens"], S)
     return dict(n=n, M2=M2, e=e, parent_tok=parent_tok, parent_keys=K[parent_tok] if N else K[:0],
                 parent_e=e[parent_tok] if N else e[:0], token_parent=token_parent,
-                pool_k=pool_k, pool_v=pool_v, S=S, **pk)
+                pool_k=pool_k, pool_v=pool_v, S=S, **pk, **extra)
 
 
 def decode_unit(idx: dict, q, budget_tokens: int, scale: float | None = None) -> dict:

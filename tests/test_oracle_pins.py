@@ -588,3 +588,16 @@ def test_decode_unit_three_levels_attends_over_the_descent_pages():
     vt = torch.from_numpy(V[toks].astype(np.float64))[None, None].expand(1, q.shape[0], -1, -1)
     ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt)[0, :, 0].numpy()
     assert np.max(np.abs(dec["out"] - ref)) < 1e-12
+
+
+def test_reuse_of_own_positional_three_level_index_is_itself():
+    """Reusing a unit's own index with sink / window pages and a third level
+    on its own keys gives back that index (M over the middle, pages and level
+    2 kept)."""
+    w, th, K, V, idx = _pos_unit(N=1200, n_sink=40, n_window=70)
+    idx = dict(idx, level2=oracle.build_level2(idx, seed=w.seed, layer=0, seq=0, head=0, thresh=th))
+    r = oracle.build_unit_reuse(K, V, idx)
+    for f in ("parent_tok", "token_parent", "page_parent", "page_len", "page_tokens", "token_page", "token_slot",
+              "parent_keys", "parent_e", "pool_k", "pool_v"):
+        assert np.array_equal(np.asarray(r[f]), np.asarray(idx[f])), f
+    assert r["M2"] == idx["M2"] and r["n_pos"] == idx["n_pos"] and r["level2"] is idx["level2"]
