@@ -102,8 +102,10 @@ def parse():
                     help="skip the full-size decode and assignment timings (100k-token contexts)")
     ap.add_argument("--at-scale-only", action="store_true",
                     help="run only the full-size timings and print them as one JSON line (profiling runs)")
-    ap.add_argument("--at-scale-parts", default="qwen_decode,qwen_decode3,longchat_assign,longchat_decode",
-                    help="comma list of qwen_decode, qwen_decode3, longchat_assign, longchat_decode")
+    ap.add_argument("--at-scale-parts",
+                    default="qwen_decode,qwen_decode3,mistral_insert,qwen_host_pool,longchat_assign,longchat_decode",
+                    help="comma list of qwen_decode, qwen_decode3, mistral_insert, qwen_host_pool, longchat_assign, "
+                         "longchat_decode")
     ap.add_argument("--at-scale-batch", type=int, default=None, help="sequences of the Qwen3-shaped batch (16)")
     ap.add_argument("--at-scale-reps", type=int, default=30)
     return ap.parse_args()
@@ -287,8 +289,8 @@ def whole_job_rate(units_per_rank: int, per_unit: int, steps: int, world: int, m
 
 
 # ------------------------------------------------------------- our arm ----
-def at_scale(pk, reps: int = 30, parts=("qwen_decode", "qwen_decode3", "longchat_assign", "longchat_decode"),
-             qwen_batch=None):
+def at_scale(pk, reps: int = 30, parts=("qwen_decode", "qwen_decode3", "mistral_insert", "qwen_host_pool",
+                                        "longchat_assign", "longchat_decode"), qwen_batch=None):
     """Full-size timings of the two parts the roofline targets are quoted on:
     the decode step (select + gather + sparse attention) of the Qwen3-32B-
     shaped batch (16 sequences x 8 KV heads, 100k tokens, budget 256) and of
@@ -414,6 +416,125 @@ def at_scale(pk, reps: int = 30, parts=("qwen_decode", "qwen_decode3", "longchat
                     f"({n2 * 256 / 1e6:.1f} MB) replaces the parent-table scan",
             "status": ice.ice_status_string(ice.ice_check(err))}
         del cfg, p, Q, idx, err, buf
+        torch.cuda.empty_cache()
+    # Mistral-7B shape: 128 decode steps, each inserting one token per unit
+    # first (step a11), the index growing from the 36,864-token build
+    if "mistral_insert" in parts:
+        w = workloads.WORKLOADS["mistral_7b_36k"]
+        steps = 128
+        cfg = ice.Config(batch=w.batch, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, n_tokens=w.n_tokens,
+                         dtype=ice.ICE_BF16, promote_p=w.promote_p, seed=w.seed, n_cap=w.n_tokens + steps)
+        K, V, C = workloads.batch_kv_device(w)
+        Q = workloads.batch_queries_device(w, C)
+        p = cfg.params()
+        idx = ice.Index(cfg)
+        ws = ice.workspace(ice.ice_build_workspace_bytes(p))
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ice.ice_build_index(p, K, V, idx, ws, err)
+        U = cfg.units
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(w.seed * 7919 + 11)
+        lab = torch.randint(0, w.centres, (steps, U), generator=gen, device="cuda")
+        kn = (C[torch.arange(U, device="cuda")[None, :], lab]
+              + w.spread * torch.randn((steps, U, 128), generator=gen, device="cuda")).to(torch.bfloat16)
+        vn = torch.randn((steps, U, 128), generator=gen, device="cuda").to(torch.bfloat16)
+        del K, V, C, ws
+        budget = max(w.budgets)
+        buf = ice.DecodeBuffers(cfg, budget)
+        wsi = ice.workspace(ice.ice_insert_workspace_bytes(p))
+        scale = 1.0 / math.sqrt(cfg.head_dim)
+        np0 = int(idx.n_parents.sum())
+        torch.cuda.synchronize()
+        evs = [(E(), E(), E()) for _ in range(steps)]
+        for st, (a, b, c) in enumerate(evs):
+            a.record()
+            ice.ice_insert_tokens(p, idx, kn[st], vn[st], wsi, err)
+            b.record()
+            ice.ice_decode_step(p, idx, Q, budget, buf.sel_pages, buf.sel_count, buf.kbuf, buf.vbuf, buf.buf_len,
+                                scale, buf.O, buf.ws, err)
+            c.record()
+        torch.cuda.synchronize()
+        t_ins = [a.elapsed_time(b) for a, b, _ in evs]
+        t_dec = [b.elapsed_time(c) for _, b, c in evs]
+        np_avg = (np0 + int(idx.n_parents.sum())) / 2
+        ins_bytes = np_avg * 128 * 2 + U * 128 * 2 * 2 * 2  # the parent scan, the new K/V rows in and into the pool
+        ins_us = 1000 * statistics.median(t_ins)
+        out["insert_mistral_7b_36k"] = {
+            "steps": steps, "units": U, "insert_us": ins_us, "decode_step_us": 1000 * statistics.median(t_dec),
+            "insert_bytes": ins_bytes, "insert_hbm_gbs": ins_bytes / (ins_us * 1e-6) / 1e9,
+            "tokens_after": int(idx.n_indexed.sum()), "parents_after": int(idx.n_parents.sum()),
+            "pages_after": int(idx.n_pages.sum()),
+            "timing": "median over the 128 steps of eager launches, CUDA events around each call, index warm "
+                      "(no L2 flush: the decode loop reuses it)",
+            "status": ice.ice_status_string(ice.ice_check(err))}
+        del cfg, p, Q, idx, err, buf, kn, vn, wsi
+        torch.cuda.empty_cache()
+    # Qwen3-32B shape with the page pool in pinned host memory (step a12)
+    if "qwen_host_pool" in parts:
+        w = workloads.WORKLOADS["qwen3_32b_100k"]
+        if qwen_batch:
+            w = w.scaled(batch=qwen_batch)
+        cfg = ice.Config(batch=w.batch, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, n_tokens=w.n_tokens,
+                         dtype=ice.ICE_BF16, promote_p=w.promote_p, seed=w.seed)
+        budget = max(w.budgets)
+        max_sel = ice.max_selected(cfg, budget)
+        hp = ice.HostPool(cfg, max_sel, n_threads=min(16, os.cpu_count() or 1))
+        try:
+            K, V, C = workloads.batch_kv_device(w)
+            Q = workloads.batch_queries_device(w, C)
+            p = cfg.params()
+            idx = ice.Index(cfg, host_pool=hp)
+            ws = ice.workspace(ice.ice_build_workspace_bytes(p))
+            err = torch.zeros(1, dtype=torch.int32, device="cuda")
+            ice.ice_build_index(p, K, V, idx, ws, err)
+            torch.cuda.synchronize()
+            del K, V, C, ws
+            buf = ice.DecodeBuffers(cfg, budget)
+            scale = 1.0 / math.sqrt(cfg.head_dim)
+            # direct: the fused decode reads the selected pages from host memory over the CPU-GPU link
+            ms_direct = timed(lambda: ice.ice_decode_step(p, idx, Q, budget, buf.sel_pages, buf.sel_count, buf.kbuf,
+                                                          buf.vbuf, buf.buf_len, scale, buf.O, buf.ws, err))
+            sel_tot = int(buf.sel_count.sum())
+            page_bytes = sel_tot * 16 * 128 * 2 * 2
+            # staged: selection on the device, ids to the host, host threads gather the pages into pinned
+            # staging, one bulk cudaMemcpyAsync, attention over the copy
+            dst = torch.empty(hp.staging_bytes, dtype=torch.uint8, device="cuda")
+            plen_h = idx.page_len.cpu()
+            U, S, d = cfg.units, cfg.page_size, cfg.head_dim
+            nb = U * max_sel * S * d * 2
+            kbuf = dst[:nb].view(torch.bfloat16).view(U, max_sel, S, d)
+            vbuf = dst[nb:2 * nb].view(torch.bfloat16).view(U, max_sel, S, d)
+            blen = dst[2 * nb:2 * nb + U * max_sel * 4].view(torch.int32).view(U, max_sel)
+            wall = []
+            for r in range(5):
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+                ice.ice_select_pages(p, idx, Q, budget, buf.sel_pages, buf.sel_count, buf.ws, err)
+                sel_h, cnt_h = buf.sel_pages.cpu(), buf.sel_count.cpu()
+                ice.ice_host_pool_gather_h2d(hp, p, sel_h, cnt_h, plen_h, max_sel, dst)
+                ice.ice_sparse_attn_decode(p, Q, kbuf, vbuf, blen, buf.sel_count, scale, buf.O, buf.ws)
+                torch.cuda.synchronize()
+                wall.append(time.perf_counter() - t0)
+            # the bulk copy alone: the same bytes, pinned host to device, one cudaMemcpyAsync
+            src = torch.empty(hp.staging_bytes, dtype=torch.uint8).pin_memory()
+            a, b = E(), E()
+            a.record()
+            dst.copy_(src, non_blocking=True)
+            b.record()
+            torch.cuda.synchronize()
+            h2d_ms = a.elapsed_time(b)
+            out[f"host_pool_qwen3_32b_100k_b{w.batch}"] = {
+                "direct_decode_us": 1000 * ms_direct, "direct_page_bytes": page_bytes,
+                "direct_link_gbs": page_bytes / (ms_direct * 1e-3) / 1e9,
+                "staged_step_ms": 1000 * statistics.median(wall), "staging_bytes": hp.staging_bytes,
+                "bulk_h2d_ms": h2d_ms, "bulk_h2d_gbs": hp.staging_bytes / (h2d_ms * 1e-3) / 1e9,
+                "host_pool_bytes": 2 * hp.pool_bytes, "host_threads": min(16, os.cpu_count() or 1),
+                "timing": "direct: CUDA-graph replays as above; staged: wall clock of select + ids to host + host "
+                          "gather + one H2D + attention, median of 5",
+                "status": ice.ice_status_string(ice.ice_check(err))}
+            del idx, buf, dst, src, kbuf, vbuf, blen
+        finally:
+            hp.close()
         torch.cuda.empty_cache()
     # LongChat-7B shape: the assignment contraction at 100k tokens, then decode
     if "longchat_assign" in parts or "longchat_decode" in parts:
