@@ -71,7 +71,7 @@ __device__ __forceinline__ unsigned long long sort32_desc(unsigned long long v) 
 }
 
 template <typename T>
-__global__ void __launch_bounds__(128) k_select3(const T *__restrict__ Q, int g, int n_q_heads, int n_kv_heads,
+__global__ void __launch_bounds__(128, sizeof(T) == 2 ? 5 : 3) k_select3(const T *__restrict__ Q, int g, int n_q_heads, int n_kv_heads,
                                                  int np_cap, int page_cap, int k_pages, int n_pos,
                                                  const int32_t *__restrict__ n_pages,
                                                  const int32_t *__restrict__ n_nodes2, const int32_t *__restrict__ node2,
@@ -149,8 +149,13 @@ __global__ void __launch_bounds__(128) k_select3(const T *__restrict__ Q, int g,
             const int c = c0 + lane;
             unsigned long long key = 0ull;
             if (c < C) {
-                int grp = 0;  // the first group whose inclusive end exceeds c
-                while (grp < kc - 1 && s_gend[grp] <= c) ++grp;
+                int lo = 0, hi = kc - 1;  // the first group whose inclusive end exceeds c
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (s_gend[mid] <= c) lo = mid + 1;
+                    else hi = mid;
+                }
+                const int grp = lo;
                 const int m = children[up + s_g0[grp] + (c - (s_gend[grp] - s_gn[grp]))];
                 key = sort_key(row_dot<T>(Pu + (size_t)m * kHeadDim, s_q), m);
             }
