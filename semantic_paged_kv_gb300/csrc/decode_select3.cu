@@ -70,8 +70,10 @@ __device__ __forceinline__ unsigned long long sort32_desc(unsigned long long v) 
     return v;
 }
 
+// 128 threads; bf16 rows leave registers for 5 CTAs per SM, fp32 rows for 3.
 template <typename T>
-__global__ void __launch_bounds__(128, sizeof(T) == 2 ? 5 : 3) k_select3(const T *__restrict__ Q, int g, int n_q_heads, int n_kv_heads,
+__global__ void __launch_bounds__(128, sizeof(T) == 2 ? 5 : 3)
+    k_select3(const T *__restrict__ Q, int g, int n_q_heads, int n_kv_heads,
                                                  int np_cap, int page_cap, int k_pages, int n_pos,
                                                  const int32_t *__restrict__ n_pages,
                                                  const int32_t *__restrict__ n_nodes2, const int32_t *__restrict__ node2,
