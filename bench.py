@@ -385,9 +385,17 @@ def at_scale(pk, reps: int = 30, parts=("qwen_decode", "qwen_decode3", "mistral_
         if qwen_batch:
             w = w.scaled(batch=qwen_batch)
         cfg, p, K, V, Q, idx, ws, err = build(w)
+        a, b = E(), E()  # a second build of the same layer, timed
+        a.record()
+        ice.ice_build_index(p, K, V, idx, ws, err)
+        b.record()
+        torch.cuda.synchronize()
+        build_ms = a.elapsed_time(b)
         del K, V, ws
         key = f"decode_qwen3_32b_100k_b{w.batch}"
         out[key] = decode(cfg, p, Q, idx, err, max(w.budgets))
+        out[key]["build_ms"] = build_ms
+        out[key]["build_keys_per_s"] = w.batch * w.n_kv_heads * w.n_tokens / (build_ms * 1e-3)
         out[key]["status"] = ice.ice_status_string(ice.ice_check(err))
         del cfg, p, Q, idx, err
         torch.cuda.empty_cache()
@@ -398,6 +406,12 @@ def at_scale(pk, reps: int = 30, parts=("qwen_decode", "qwen_decode3", "mistral_
         if qwen_batch:
             w = w.scaled(batch=qwen_batch)
         cfg, p, K, V, Q, idx, ws, err = build(w, n_levels=3)
+        a, b = E(), E()  # a second build of the same layer, timed (two and three levels differ by level 2)
+        a.record()
+        ice.ice_build_index(p, K, V, idx, ws, err)
+        b.record()
+        torch.cuda.synchronize()
+        build3_ms = a.elapsed_time(b)
         del K, V, ws
         budget = max(w.budgets)
         buf = ice.DecodeBuffers(cfg, budget)
@@ -411,6 +425,7 @@ def at_scale(pk, reps: int = 30, parts=("qwen_decode", "qwen_decode3", "mistral_
         sel_tot = int(buf.sel_count.sum())
         out[f"decode3_qwen3_32b_100k_b{w.batch}"] = {
             "us": 1000 * ms, "no_buffer_us": 1000 * ms_nb, "select_only_us": 1000 * ms_sel, "budget_tokens": budget,
+            "build_ms": build3_ms,
             "level2_nodes": n2, "parents": int(idx.n_parents.sum()), "selected_pages": sel_tot,
             "what": "n_levels = 3: per head the best k level-2 nodes, then their children; the level-2 table "
                     f"({n2 * 256 / 1e6:.1f} MB) replaces the parent-table scan",

@@ -122,6 +122,10 @@ BuildWs build_ws_layout(const ice_params &p, void *base) {
     w.b_extra = reinterpret_cast<uint4 *>(take(32 * U * (size_t)p.np_cap));
     w.pack_cnt = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * U * tk * (size_t)p.np_cap));
     w.pack_total = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * U * (size_t)p.np_cap));
+    const size_t l2 = (p.n_levels == 3 && p.dtype == ICE_BF16) ? U * (size_t)p.np_cap : 0;
+    w.a_extra2 = reinterpret_cast<uint4 *>(take(32 * l2));
+    w.keys2 = take(sizeof(uint16_t) * kHeadDim * l2);
+    w.b_extra2 = reinterpret_cast<uint4 *>(take(32 * l2));
     w.bytes = off;
     return w;
 }
@@ -277,7 +281,7 @@ ice_status ice_build_assign(const ice_params *p, const void *K, const ice_index 
                                                : launch_assign_simt(*p, K, *idx, w, err_dev, s),
                           "ice_build_assign")))
         return st;
-    if (p->n_levels == 3) return cuda_status(launch_level2(*p, *idx, s), "ice_build_assign (level 2)");
+    if (p->n_levels == 3) return cuda_status(launch_level2(*p, *idx, w, err_dev, s), "ice_build_assign (level 2)");
     return ICE_OK;
 }
 

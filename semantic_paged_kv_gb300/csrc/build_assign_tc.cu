@@ -310,7 +310,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+int sm_count_assign() {
+    static int n_sm = 0;
+    if (!n_sm) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+        if (n_sm <= 0) n_sm = 1;
+    }
+    return n_sm;
+}
+
 }  // namespace
+
+cudaError_t launch_assign_level2_tc(const ice_params &p, const ice_index &idx, const BuildWs &ws, int32_t *err,
+                                    cudaStream_t s) {
+    // rows: the parents (their keys and row-form lifted coordinates); columns:
+    // the level-2 nodes gathered dense; the output and the keep-seeds: parent2
+    const int U = units_of(p);
+    CUtensorMap tmK, tmP, tmK2, tmP2;
+    const unsigned long long r = (unsigned long long)U * p.np_cap;
+    if (r > 0x7FFFFFFFull || !make_map_bf16(&tmK, idx.parent_keys, r, kHeadDim, 64, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_bf16(&tmP, ws.keys2, r, kHeadDim, 64, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_bf16(&tmK2, ws.a_extra2, r, kExtra, kExtra, BM, CU_TENSOR_MAP_SWIZZLE_32B) ||
+        !make_map_bf16(&tmP2, ws.b_extra2, r, kExtra, kExtra, BN, CU_TENSOR_MAP_SWIZZLE_32B))
+        return cudaErrorNotSupported;
+    cudaError_t e = cudaFuncSetAttribute(k_assign_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int mt = ceil_div(p.np_cap, BM);
+    const int items = mt * U;
+    const int n_sm = sm_count_assign();
+    const int grid = items < n_sm ? items : n_sm;
+    e = launch_dependent(k_assign_tc, dim3(grid), dim3(kThreads), kSmemBytes, s, tmK, tmP, tmK2, tmP2, p.np_cap,
+                         p.np_cap, p.np_cap, items, mt, idx.n_nodes2, idx.parent2, err);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
 
 cudaError_t launch_assign_tc(const ice_params &p, const void *K, const ice_index &idx, const BuildWs &ws,
                              int32_t *err, cudaStream_t s) {

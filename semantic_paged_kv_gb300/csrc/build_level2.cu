@@ -12,10 +12,15 @@
 //                  token at level 2 is below the threshold (the smallest draw
 //                  if none is); ordered compaction into node2 (level-2 node
 //                  i -> parent m), parent2 = i for those parents, -1 others
-//   k_l2_assign    32 parents per CTA: the nearest level-2 node in the lifted
-//                  space, argmax_i (p_m . p_i + e_m e_i) in fp32, exact ties
-//                  to the lowest i (parent keys staged as fp32 in shared
-//                  memory, the level-2 nodes streamed 32 at a time)
+//   k_l2_gather +  bf16: the nearest level-2 node in the lifted space on the
+//   k_assign_tc    tensor cores, the parent table against the level-2 nodes
+//                  gathered dense (the same contraction and argmax as the
+//                  token -> parent step, the split lifted coordinates as
+//                  extra K columns)
+//   k_l2_assign    fp32 (CUDA cores): 32 parents per CTA, argmax_i
+//                  (p_m . p_i + e_m e_i), exact ties to the lowest i (parent
+//                  keys staged as fp32 in shared memory, the level-2 nodes
+//                  streamed 32 at a time)
 //   k_l2_children  one CTA per unit: the parents grouped by parent2,
 //                  ascending m inside a group (counting sort: shared-memory
 //                  histogram, scan, one warp placing 32 parents at a time)
@@ -228,16 +233,54 @@ __global__ void __launch_bounds__(kPT) k_l2_children(int np_cap, const int32_t *
     }
 }
 
+// The tensor-core operands of the level-2 contraction (bf16), one warp per
+// row: per parent m its token's row-form split lifted coordinate, per
+// level-2 node i its key row and column-form split lifted coordinate.
+__global__ void __launch_bounds__(kAT) k_l2_gather(int N, int np_cap, const int32_t *__restrict__ n_parents,
+                                                   const int32_t *__restrict__ n_nodes2,
+                                                   const int32_t *__restrict__ parent_tok,
+                                                   const int32_t *__restrict__ node2, const uint4 *__restrict__ keys,
+                                                   const uint4 *__restrict__ a_extra, const uint4 *__restrict__ b_extra,
+                                                   uint4 *__restrict__ a_extra2, uint4 *__restrict__ keys2,
+                                                   uint4 *__restrict__ b_extra2) {
+    dep_wait();  // the level-2 nodes are complete
+    const int u = blockIdx.y;
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * (kAT / 32) + (threadIdx.x >> 5);
+    const size_t up = (size_t)u * np_cap;
+    if (r < min(n_parents[u], np_cap) && lane < 2)
+        a_extra2[(up + r) * 2 + lane] = a_extra[((size_t)u * N + parent_tok[up + r]) * 2 + lane];
+    if (r < min(n_nodes2[u], np_cap)) {
+        const int m = node2[up + r];
+        if (lane < 16) keys2[(up + r) * 16 + lane] = keys[(up + m) * 16 + lane];  // 16 x 16 B = 128 bf16
+        else if (lane < 18) b_extra2[(up + r) * 2 + lane - 16] = b_extra[(up + m) * 2 + lane - 16];
+    }
+}
+
 template <typename T>
-cudaError_t launch_t(const ice_params &p, const ice_index &idx, cudaStream_t s) {
+cudaError_t launch_t(const ice_params &p, const ice_index &idx, const BuildWs &ws, int32_t *err, cudaStream_t s) {
     const int U = units_of(p);
     cudaError_t e = launch_dependent(k_l2_promote, dim3(U), dim3(kPT), 0, s, p.n_kv_heads, p.np_cap, p.promote_thresh,
                                      promote_key(p.seed, p.layer), idx.n_parents, idx.parent_tok, idx.n_nodes2,
                                      idx.node2, idx.parent2);
     if (e != cudaSuccess) return e;
-    e = launch_dependent(k_l2_assign<T>, dim3(ceil_div(p.np_cap, kRows), U), dim3(kAT), 0, s, p.np_cap, idx.n_parents,
-                         idx.n_nodes2, idx.node2, static_cast<const T *>(idx.parent_keys), idx.parent_e, idx.parent2);
-    if (e != cudaSuccess) return e;
+    bool done = false;
+    if (sizeof(T) == 2 && ws.keys2) {  // bf16: the contraction on the tensor cores
+        e = launch_dependent(k_l2_gather, dim3(ceil_div(p.np_cap, kAT / 32), U), dim3(kAT), 0, s, p.n_tokens, p.np_cap,
+                             idx.n_parents, idx.n_nodes2, idx.parent_tok, idx.node2,
+                             static_cast<const uint4 *>(idx.parent_keys), ws.a_extra, ws.b_extra, ws.a_extra2,
+                             static_cast<uint4 *>(ws.keys2), ws.b_extra2);
+        if (e != cudaSuccess) return e;
+        e = launch_assign_level2_tc(p, idx, ws, err, s);
+        if (e != cudaSuccess && e != cudaErrorNotSupported) return e;
+        done = e == cudaSuccess;
+    }
+    if (!done) {
+        e = launch_dependent(k_l2_assign<T>, dim3(ceil_div(p.np_cap, kRows), U), dim3(kAT), 0, s, p.np_cap,
+                             idx.n_parents, idx.n_nodes2, idx.node2, static_cast<const T *>(idx.parent_keys),
+                             idx.parent_e, idx.parent2);
+        if (e != cudaSuccess) return e;
+    }
     const size_t smem = sizeof(int) * ((size_t)p.np_cap + 1);
     if (smem > 48 * 1024) {
         e = cudaFuncSetAttribute(k_l2_children, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -250,9 +293,10 @@ cudaError_t launch_t(const ice_params &p, const ice_index &idx, cudaStream_t s) 
 
 }  // namespace
 
-cudaError_t launch_level2(const ice_params &p, const ice_index &idx, cudaStream_t s) {
-    if (p.dtype == ICE_BF16) return launch_t<__nv_bfloat16>(p, idx, s);
-    return launch_t<float>(p, idx, s);
+cudaError_t launch_level2(const ice_params &p, const ice_index &idx, const BuildWs &ws, int32_t *err,
+                          cudaStream_t s) {
+    if (p.dtype == ICE_BF16) return launch_t<__nv_bfloat16>(p, idx, ws, err, s);
+    return launch_t<float>(p, idx, ws, err, s);
 }
 
 }  // namespace ice

@@ -46,6 +46,10 @@ struct BuildWs {
     uint4 *b_extra;       // [U, np_cap, 16] bf16: the same for each parent
     int32_t *pack_cnt;    // [U, Tk, np_cap] per-tile parent counts -> offsets
     int32_t *pack_total;  // [U, np_cap] tokens per parent
+    // three levels, bf16: the level-2 contraction's operands, gathered dense
+    uint4 *a_extra2;      // [U, np_cap, 16] bf16: each parent's split lifted coordinate, row form
+    void *keys2;          // [U, np_cap, d] the level-2 nodes' keys
+    uint4 *b_extra2;      // [U, np_cap, 16] bf16: each level-2 node's split lifted coordinate, column form
     size_t bytes;
 };
 BuildWs build_ws_layout(const ice_params &p, void *base);
@@ -97,7 +101,12 @@ cudaError_t launch_assign_tc(const ice_params &p, const void *K, const ice_index
 cudaError_t launch_pack(const ice_params &p, const void *K, const void *V, const ice_index &idx,
                         const BuildWs &ws, int32_t *err, cudaStream_t s);
 // Level 2 of a three-level index (promotion, nearest level-2 node, children).
-cudaError_t launch_level2(const ice_params &p, const ice_index &idx, cudaStream_t s);
+cudaError_t launch_level2(const ice_params &p, const ice_index &idx, const BuildWs &ws, int32_t *err,
+                          cudaStream_t s);
+// The parents' nearest level-2 node on the tensor cores (bf16): k_assign_tc
+// over the parent table against the gathered level-2 table.
+cudaError_t launch_assign_level2_tc(const ice_params &p, const ice_index &idx, const BuildWs &ws, int32_t *err,
+                                    cudaStream_t s);
 // Page selection by descent through level 2 (n_levels = 3).
 cudaError_t launch_select3(const ice_params &p, const ice_index &idx, const void *Q, const DecodeWs &ws,
                            int32_t *sel_pages, int32_t *sel_count, int max_sel, int32_t *err, cudaStream_t s);
