@@ -7,10 +7,11 @@
 // contiguous buffer; 关键设计 1: a_ij = s_ij exp(q_i.k_j/sqrt(d)) /
 // sum_j' s_ij' exp(q_i.k_j'/sqrt(d)) over the selected pages only.
 //
-// k_attn_mma<F, HR>: grid (S, units), 12 warps; CTA s takes its share of the
-// unit's union, warp w the share's pages w, w + 12, ... in order, double-
-// buffered in the warp's two shared-memory slots by 2-D TMA loads with a
-// 128-byte swizzle (so the 8-row fragment loads below are conflict-free).
+// k_attn_mma<F, HR>: grid (S, units), 8 warps; CTA s takes its share of the
+// unit's union, warp w the share's pages w, w + 8, ... in order, streamed
+// through the warp's three shared-memory slots (two pages in flight while
+// one is computed) by 2-D TMA loads with a 128-byte swizzle (so the 8-row
+// fragment loads below are conflict-free).
 // Per page, with the g <= 16 query rows of the group as the M = 16 rows:
 //   S = Q K^T     mma.sync m16n8k16 (bf16 in, fp32 accumulate): A = q in
 //                 registers (loaded once), B = K rows by ldmatrix; 2 key
@@ -41,18 +42,19 @@ namespace {
 
 using namespace tc;
 
-constexpr int kMW = 12;  // warps per CTA
+constexpr int kMW = 8;   // warps per CTA
+constexpr int kNS = 3;   // page slots per warp (pages in flight while one is computed)
 constexpr int kMT = kMW * 32;
 constexpr uint32_t kHalfBytes = kPage * 128;       // 16 rows x 64 bf16 columns (one swizzled box)
 constexpr uint32_t kTileBytes = 2 * kHalfBytes;    // K or V of one page: 4 KB
 constexpr uint32_t kSlotBytes = 2 * kTileBytes;    // K and V
 
 struct SmemM {
-    unsigned char kv[kMW][2][kSlotBytes];  // per warp two slots: 192 KB, reused by the merge
+    unsigned char kv[kMW][kNS][kSlotBytes];  // per warp kNS slots: 192 KB, reused by the merge
     float ml[kMW][16][2];                  // per warp and query row: running max, sum
     float wgt[kMW][16];
     float cml[16][2];
-    unsigned long long full[kMW][2];
+    unsigned long long full[kMW][kNS];
     int wsum[kMW];
     int last;
 };
@@ -105,7 +107,7 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
     const int b = u / n_kv_heads, h = u % n_kv_heads;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int qr = lane >> 2, qc = lane & 3;  // fragment row (query row) and column pair
-    if (tid < 2 * kMW) mbar_init(&S.full[tid >> 1][tid & 1], 1);
+    if (tid < kNS * kMW) mbar_init(&S.full[tid / kNS][tid % kNS], 1);
     if (tid == 0) mbar_init_fence();
     if (lane < 16) {
         S.ml[warp][lane][0] = -INFINITY;
@@ -151,8 +153,8 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
     auto issue = [&](int k, int pid) {
         const int x = xs + warp + k * kMW;
         const int row = kFused ? (u * page_cap + pid) * kPage : (int)((ubase + x) * kPage);
-        unsigned char *slot = S.kv[warp][k & 1];
-        unsigned long long *bar = &S.full[warp][k & 1];
+        unsigned char *slot = S.kv[warp][k % kNS];
+        unsigned long long *bar = &S.full[warp][k % kNS];
         mbar_expect_tx(bar, kSlotBytes);
         tma_load_2d(slot, &tm_k, bar, 0, row);
         tma_load_2d(slot + kHalfBytes, &tm_k, bar, 64, row);
@@ -161,11 +163,13 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
     };
     if (kSel) __syncthreads();  // every warp has its page ids before the slots fill
     {
-        const int p0 = __shfl_sync(0xffffffffu, my_pid, 0), p1 = __shfl_sync(0xffffffffu, my_pid, 1);
-        if (lane == 0) {
-            if (nk > 0) issue(0, p0);
-            if (nk > 1) issue(1, p1);
-        }
+        int pf[kNS];
+#pragma unroll
+        for (int k = 0; k < kNS; ++k) pf[k] = __shfl_sync(0xffffffffu, my_pid, k);
+        if (lane == 0)
+#pragma unroll
+            for (int k = 0; k < kNS; ++k)
+                if (nk > k) issue(k, pf[k]);
     }
 
     // A fragments of Q (rows = query rows of the group), 8 steps of 16 dims
@@ -190,12 +194,12 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
         const int x = xs + warp + k * kMW;
         const size_t slot = ubase + x;
         const int len = __shfl_sync(0xffffffffu, my_len, k);
-        const int pid_next = __shfl_sync(0xffffffffu, my_pid, (k + 2) & 31);
+        const int pid_next = __shfl_sync(0xffffffffu, my_pid, (k + kNS) & 31);
         if (store && lane == 0) buf_len[slot] = len;
-        if (ok) ok = mbar_wait(&S.full[warp][k & 1], (k >> 1) & 1);
+        if (ok) ok = mbar_wait(&S.full[warp][k % kNS], (k / kNS) & 1);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        unsigned char *sp = S.kv[warp][k & 1];
+        unsigned char *sp = S.kv[warp][k % kNS];
         if (store && lane == 0) {  // the contiguous buffer, straight from shared memory
             fence_proxy_async();
             const int row = (int)(slot * kPage);
@@ -284,9 +288,9 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
             mma16816(o[nt + 1], alo, b2, b3);
         }
         __syncwarp();
-        if (lane == 0 && k + 2 < nk) {  // refill this slot once its stores have read it
+        if (lane == 0 && k + kNS < nk) {  // refill this slot once its stores have read it
             if (store) bulk_wait_read_all();
-            issue(k + 2, pid_next);
+            issue(k + kNS, pid_next);
         }
         __syncwarp();
     }
