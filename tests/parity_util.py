@@ -35,7 +35,7 @@ def to_dev(x: np.ndarray, dtype) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(x)).to(device="cuda").to(dtype)
 
 
-class GpuRun:
+class DeviceRun:
     """One layer built and decoded on the GPU, with host copies of everything."""
 
     def __init__(self, w: workloads.Workload, layer: int = 0, assign: str = "auto", **cfg_kw):
@@ -94,7 +94,7 @@ def lifted_d2(K, e, j, t):
     return float(dk @ dk + (e[j] - e[t]) ** 2)
 
 
-def check_build_unit(run: GpuRun, u: int, sample_tokens: int | None = None):
+def check_build_unit(run: DeviceRun, u: int, sample_tokens: int | None = None):
     """Promotion, lift, parent assignment (tie-aware), pages and pool of unit u.
 
     With sample_tokens set, the assignment is checked on that many seeded
@@ -141,7 +141,7 @@ def check_build_unit(run: GpuRun, u: int, sample_tokens: int | None = None):
     check_pack_unit(run, u)
 
 
-def check_pack_unit(run: GpuRun, u: int):
+def check_pack_unit(run: DeviceRun, u: int):
     """Pages, page tables and pool of unit u: the oracle packs the GPU's own
     assignment, and every table must match bit-exactly."""
     b, h = run.unit(u)
@@ -172,7 +172,7 @@ def check_pack_unit(run: GpuRun, u: int):
     assert np.array_equal(gk, ok) and np.array_equal(gv, ov)
 
 
-def check_decode_unit(run: GpuRun, u: int, Q: np.ndarray, budget: int, buf):
+def check_decode_unit(run: DeviceRun, u: int, Q: np.ndarray, budget: int, buf):
     """Selection (tie-aware), gather (exact) and attention (tolerance) of unit u."""
     b, h = run.unit(u)
     cfg, H = run.cfg, run.h

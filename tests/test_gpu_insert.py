@@ -7,7 +7,7 @@ import torch
 import oracle
 import semantic_paged_kv_gb300 as ice
 import workloads
-from parity_util import GpuRun, TIE_REL, check_decode_unit, lifted_d2, to_dev
+from parity_util import DeviceRun, TIE_REL, check_decode_unit, lifted_d2, to_dev
 
 pytestmark = pytest.mark.gpu
 W = workloads.WORKLOADS
@@ -33,7 +33,7 @@ def _oracle_state(run, u):
 
 def _run_inserts(w, steps, budget=None, **cfg_kw):
     N = w.n_tokens
-    run = GpuRun(w, n_cap=N + steps, **cfg_kw)
+    run = DeviceRun(w, n_cap=N + steps, **cfg_kw)
     assert run.status == ice.ICE_OK
     cfg, U = run.cfg, run.cfg.units
     new = [workloads.unit_new_tokens(w, 0, *run.unit(u), steps) for u in range(U)]
@@ -121,7 +121,7 @@ def test_insert_every_token_promoted():
 
 def test_insert_capacity_error():
     w = W["tiny"].scaled(n_tokens=100)
-    run = GpuRun(w, n_cap=100)
+    run = DeviceRun(w, n_cap=100)
     ws = ice.workspace(ice.ice_insert_workspace_bytes(run.params))
     kn = torch.zeros((1, 1, 128), device="cuda")
     ice.ice_insert_tokens(run.params, run.idx, kn, kn, ws, run.err)

@@ -9,7 +9,7 @@ import torch
 import oracle
 import semantic_paged_kv_gb300 as ice
 import workloads
-from parity_util import GpuRun, check_build_unit, check_decode_unit, check_pack_unit, to_dev
+from parity_util import DeviceRun, check_build_unit, check_decode_unit, check_pack_unit, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -36,7 +36,7 @@ def _all_units_decode(run, budgets, fused=True):
 
 def test_tiny_fp32_full():
     """The tiny fp32 workload (1 KV head, 4 query heads, N = 2048) end to end."""
-    run = GpuRun(W["tiny"])
+    run = DeviceRun(W["tiny"])
     assert run.status == ice.ICE_OK
     _all_units(run, [64, 128], fused=True)
     _all_units(run, [64], fused=False)
@@ -47,7 +47,7 @@ def test_llama_shaped_bf16_ragged(assign):
     """Llama-3.1-8B head layout (g = 4), bf16, a ragged N spanning several
     2048-token tiles and 128-row tiles, two sequences, needle planted."""
     w = W["llama31_8b_16k"].scaled(n_tokens=5003, batch=2, n_q_heads=8, n_kv_heads=2)
-    run = GpuRun(w, assign=assign)
+    run = DeviceRun(w, assign=assign)
     assert run.status == ice.ICE_OK
     _all_units(run, [64, 128, 256])
 
@@ -57,7 +57,7 @@ def test_many_parent_tiles_ring_wrap():
     ring and the two TMEM accumulators are reused; assignment checked on a
     seeded sample of tokens, everything else on all tokens."""
     w = W["llama31_8b_16k"].scaled(n_tokens=12003, n_q_heads=4, n_kv_heads=1)
-    run = GpuRun(w)
+    run = DeviceRun(w)
     assert run.status == ice.ICE_OK
     _all_units(run, [256], sample=3000)
 
@@ -67,14 +67,14 @@ def test_llama_full_size_sampled():
     needle) in the launch configuration the benchmark times: promotion, pages,
     pool and decode checked in full, the assignment on 1500 sampled tokens per
     unit."""
-    run = GpuRun(W["llama31_8b_16k"])
+    run = DeviceRun(W["llama31_8b_16k"])
     assert run.status == ice.ICE_OK
     _all_units(run, [64, 128, 256], sample=1500)
 
 
 def test_fused_decode_equals_separate_calls():
     w = W["llama31_8b_16k"].scaled(n_tokens=3000, n_q_heads=8, n_kv_heads=2)
-    run = GpuRun(w)
+    run = DeviceRun(w)
     Q1, a, _ = run.decode(128, fused=True)
     Q2, b, _ = run.decode(128, fused=False)
     for x, y in [(a.sel_pages, b.sel_pages), (a.sel_count, b.sel_count), (a.kbuf, b.kbuf), (a.vbuf, b.vbuf),
@@ -95,7 +95,7 @@ def test_decode_without_contiguous_buffer(shape):
          "qwen_many_units": W["qwen3_32b_100k"].scaled(n_tokens=3000, batch=3, centres=256),
          "longchat_many_units": W["longchat_7b_100k"].scaled(n_tokens=2500, batch=1, n_q_heads=24, n_kv_heads=24,
                                                              centres=256)}[shape]
-    run = GpuRun(w)
+    run = DeviceRun(w)
     assert run.status == ice.ICE_OK
     for bgt in (64, 256):
         Q, a, st_a = run.decode(bgt, contiguous=True)
@@ -111,7 +111,7 @@ def test_decode_without_contiguous_buffer(shape):
 def test_qwen_shaped_g8_mha_longchat_shaped_g1():
     for w in (W["qwen3_32b_100k"].scaled(n_tokens=4100, batch=2, n_q_heads=16, n_kv_heads=2, centres=512),
               W["longchat_7b_100k"].scaled(n_tokens=4100, batch=1, n_q_heads=3, n_kv_heads=3, centres=512)):
-        run = GpuRun(w)
+        run = DeviceRun(w)
         assert run.status == ice.ICE_OK
         _all_units(run, [64, 256])
 
@@ -122,7 +122,7 @@ def test_many_units_take_select_and_attention_kernels():
     LongChat-shaped g = 1 groups), every unit checked."""
     for w in (W["qwen3_32b_100k"].scaled(n_tokens=3000, batch=3, centres=256),
               W["longchat_7b_100k"].scaled(n_tokens=2500, batch=1, n_q_heads=24, n_kv_heads=24, centres=256)):
-        run = GpuRun(w)
+        run = DeviceRun(w)
         assert run.status == ice.ICE_OK
         assert run.cfg.units * 8 > torch.cuda.get_device_properties(0).multi_processor_count
         for u in (0, run.cfg.units - 1):
@@ -135,7 +135,7 @@ def test_one_attention_cta_per_unit():
     """More units than SMs with a 128-page selection: the streaming attention
     runs one CTA per unit and writes O directly (fused and separate calls)."""
     w = W["qwen3_32b_100k"].scaled(n_tokens=2200, batch=20, centres=128)
-    run = GpuRun(w)
+    run = DeviceRun(w)
     assert run.status == ice.ICE_OK
     assert run.cfg.units >= torch.cuda.get_device_properties(0).multi_processor_count
     for fused in (True, False):
@@ -150,7 +150,7 @@ def test_longchat_100k_full_size_sampled():
     log-normal norms) in the launch configuration the benchmark times: the
     selection runs as several segments per unit.  Build checked on two units
     (assignment on 800 sampled tokens), decode on four."""
-    run = GpuRun(W["longchat_7b_100k"])
+    run = DeviceRun(W["longchat_7b_100k"])
     assert run.status == ice.ICE_OK
     for u in (3, 30):
         check_build_unit(run, u, sample_tokens=800)
@@ -164,7 +164,7 @@ def test_longchat_100k_full_size_sampled():
 def test_promote_all_is_exact_topk_mips():
     """p = 1: one-token pages, so selection is exact top-k inner product search."""
     w = W["tiny"].scaled(n_tokens=700, promote_p=1.0)
-    run = GpuRun(w)
+    run = DeviceRun(w)
     assert run.status == ice.ICE_OK
     assert int(run.h["n_pages"][0]) == 700
     _all_units(run, [16 * 5, 16 * 40])
@@ -182,7 +182,7 @@ def test_pack_with_many_parents_uses_tile_kernels():
     (count, scan, rank); checked bit-exactly against the oracle's packing of
     the GPU's assignment, then decoded."""
     w = W["llama31_8b_16k"].scaled(n_tokens=10000, n_q_heads=4, n_kv_heads=1, promote_p=0.95)
-    run = GpuRun(w)
+    run = DeviceRun(w)
     assert run.status == ice.ICE_OK
     assert run.cfg.np_cap * 24 > 225 * 1024
     check_pack_unit(run, 0)
@@ -194,7 +194,7 @@ def test_pack_with_many_parents_uses_tile_kernels():
 def test_promote_none_is_sequential_paging():
     """p = 0: one parent (the smallest draw), so pages are sequential 16-token pages."""
     w = W["tiny"].scaled(n_tokens=1000, promote_p=0.0)
-    run = GpuRun(w)
+    run = DeviceRun(w)
     assert int(run.h["n_parents"][0]) == 1
     assert np.array_equal(run.h["token_page"][0, :1000], np.arange(1000) // 16)
     _all_units(run, [64])
@@ -202,7 +202,7 @@ def test_promote_none_is_sequential_paging():
 
 def test_full_budget_is_dense_attention():
     w = W["llama31_8b_16k"].scaled(n_tokens=2500, n_q_heads=8, n_kv_heads=2)
-    run = GpuRun(w)
+    run = DeviceRun(w)
     P = int(run.h["n_pages"].max())
     Q, buf, _ = run.decode(16 * P)
     for u in range(run.cfg.units):
@@ -217,7 +217,7 @@ def test_full_budget_is_dense_attention():
 @pytest.mark.parametrize("n", [0, 1, 17, 2049])
 def test_small_and_empty_units(n):
     w = W["tiny"].scaled(n_tokens=n)
-    run = GpuRun(w, n_cap=max(n, 1))
+    run = DeviceRun(w, n_cap=max(n, 1))
     assert run.status == ice.ICE_OK
     _all_units(run, [64])
 
@@ -226,7 +226,7 @@ def test_needle_page_selected_at_every_budget():
     """Behavioural check from the passkey claim: the planted needle key's page
     is selected for its query head at budgets 64/128/256."""
     w = W["llama31_8b_16k"].scaled(n_tokens=6000, n_q_heads=8, n_kv_heads=2)
-    run = GpuRun(w)
+    run = DeviceRun(w)
     for bgt in (64, 128, 256):
         Q, buf, _ = run.decode(bgt)
         for u in range(run.cfg.units):
@@ -238,7 +238,7 @@ def test_needle_page_selected_at_every_budget():
 
 def test_capacity_error_is_reported_not_overrun():
     w = W["tiny"].scaled(n_tokens=3000)
-    run = GpuRun(w, np_cap=20, page_cap=200)
+    run = DeviceRun(w, np_cap=20, page_cap=200)
     assert run.status == ice.ICE_ERR_CAPACITY
     assert int(run.h["n_parents"][0]) == 20
 
@@ -267,9 +267,9 @@ def test_invalid_arguments_rejected():
     assert ei.value.status == ice.ICE_ERR_INVALID_ARG
 
 
-def _reused_run(run0: GpuRun, layer: int = 1, in_place: bool = False) -> GpuRun:
+def _reused_run(run0: DeviceRun, layer: int = 1, in_place: bool = False) -> DeviceRun:
     """Layer `layer` built by ice_build_index_reuse on run0's index."""
-    r = object.__new__(GpuRun)
+    r = object.__new__(DeviceRun)
     r.w, r.layer = run0.w, layer
     r.cfg = ice.Config(**{**run0.cfg.__dict__, "layer": layer})
     r.K, r.V = workloads.batch_kv(r.w, layer)
@@ -295,7 +295,7 @@ def test_reuse_build_matches_oracle(shape):
     the decode step over the reused index."""
     w = W["tiny"] if shape == "tiny_fp32" else W["llama31_8b_16k"].scaled(n_tokens=4003, batch=2, n_q_heads=8,
                                                                           n_kv_heads=2)
-    run0 = GpuRun(w)
+    run0 = DeviceRun(w)
     assert run0.status == ice.ICE_OK
     h0 = {k: v.copy() for k, v in run0.h.items()}
     run1 = _reused_run(run0, in_place=shape == "in_place")
@@ -343,7 +343,7 @@ def test_sink_and_window_pages(shape, n_sink, n_window):
          "tiny_fp32": W["tiny"],
          "many_units": W["qwen3_32b_100k"].scaled(n_tokens=3000, batch=3, centres=256),
          "no_middle": W["llama31_8b_16k"].scaled(n_tokens=3000, n_q_heads=8, n_kv_heads=2)}[shape]
-    run = GpuRun(w, n_sink=n_sink, n_window=n_window)
+    run = DeviceRun(w, n_sink=n_sink, n_window=n_window)
     assert run.status == ice.ICE_OK
     th = oracle.promote_threshold(w.promote_p)
     N, exact = w.n_tokens, 0
@@ -381,7 +381,7 @@ def test_sink_and_window_pages(shape, n_sink, n_window):
 
 def test_insert_rejected_with_positional_pages():
     w = W["llama31_8b_16k"].scaled(n_tokens=1000, n_q_heads=4, n_kv_heads=1)
-    run = GpuRun(w, n_sink=16, n_window=32)
+    run = DeviceRun(w, n_sink=16, n_window=32)
     ws = ice.workspace(ice.ice_insert_workspace_bytes(run.params))
     kn = torch.zeros((1, 1, 128), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(ice.IceError) as ei:
@@ -403,7 +403,7 @@ def test_three_levels_build_and_descent(shape, n_sink, n_window):
          "many_units": W["qwen3_32b_100k"].scaled(n_tokens=4000, batch=3, centres=256),
          # p = 1/2: ~1500 level-2 nodes per unit, more than the descent keeps in shared memory
          "dense_levels": W["llama31_8b_16k"].scaled(n_tokens=6000, n_q_heads=8, n_kv_heads=2, promote_p=0.5)}[shape]
-    run = GpuRun(w, n_levels=3, n_sink=n_sink, n_window=n_window)
+    run = DeviceRun(w, n_levels=3, n_sink=n_sink, n_window=n_window)
     assert run.status == ice.ICE_OK
     th = oracle.promote_threshold(w.promote_p)
     N, H = w.n_tokens, run.h
@@ -456,7 +456,7 @@ def test_reuse_with_sink_window_and_three_levels():
     level: tables, level 2, keys, M over the middle and pool against
     oracle.build_unit_reuse; then the descent decode over the result."""
     w = W["llama31_8b_16k"].scaled(n_tokens=4003, batch=2, n_q_heads=8, n_kv_heads=2, centres=512)
-    run0 = GpuRun(w, n_levels=3, n_sink=48, n_window=160)
+    run0 = DeviceRun(w, n_levels=3, n_sink=48, n_window=160)
     assert run0.status == ice.ICE_OK
     h0 = {k: v.copy() for k, v in run0.h.items()}
     run1 = _reused_run(run0)
