@@ -380,7 +380,7 @@ def at_scale(pk, reps: int = 30, parts=("qwen_decode", "qwen_decode3", "mistral_
                      f"and then a 2x L2 read of another buffer (no dirty flush lines left for the timed region)",
            "peak_source": pk["src"]}
     # Qwen3-32B shape: decode step
-    if "qwen_decode" in parts:
+    def part_qwen_decode():
         w = workloads.WORKLOADS["qwen3_32b_100k"]
         if qwen_batch:
             w = w.scaled(batch=qwen_batch)
@@ -401,7 +401,7 @@ def at_scale(pk, reps: int = 30, parts=("qwen_decode", "qwen_decode3", "mistral_
         torch.cuda.empty_cache()
     # Qwen3-32B shape with a third index level: the descent reads the level-2
     # table and the chosen nodes' children instead of the whole parent table
-    if "qwen_decode3" in parts:
+    def part_qwen_decode3():
         w = workloads.WORKLOADS["qwen3_32b_100k"]
         if qwen_batch:
             w = w.scaled(batch=qwen_batch)
@@ -434,7 +434,7 @@ def at_scale(pk, reps: int = 30, parts=("qwen_decode", "qwen_decode3", "mistral_
         torch.cuda.empty_cache()
     # Mistral-7B shape: 128 decode steps, each inserting one token per unit
     # first (step a11), the index growing from the 36,864-token build
-    if "mistral_insert" in parts:
+    def part_mistral_insert():
         w = workloads.WORKLOADS["mistral_7b_36k"]
         steps = 128
         cfg = ice.Config(batch=w.batch, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, n_tokens=w.n_tokens,
@@ -485,7 +485,7 @@ def at_scale(pk, reps: int = 30, parts=("qwen_decode", "qwen_decode3", "mistral_
         del cfg, p, Q, idx, err, buf, kn, vn, wsi
         torch.cuda.empty_cache()
     # Qwen3-32B shape with the page pool in pinned host memory (step a12)
-    if "qwen_host_pool" in parts:
+    def part_qwen_host_pool():
         w = workloads.WORKLOADS["qwen3_32b_100k"]
         if qwen_batch:
             w = w.scaled(batch=qwen_batch)
@@ -552,7 +552,7 @@ def at_scale(pk, reps: int = 30, parts=("qwen_decode", "qwen_decode3", "mistral_
             hp.close()
         torch.cuda.empty_cache()
     # LongChat-7B shape: the assignment contraction at 100k tokens, then decode
-    if "longchat_assign" in parts or "longchat_decode" in parts:
+    def part_longchat():
         w = workloads.WORKLOADS["longchat_7b_100k"]
         cfg, p, K, V, Q, idx, ws, err = build(w)
         if "longchat_assign" in parts:
@@ -569,6 +569,19 @@ def at_scale(pk, reps: int = 30, parts=("qwen_decode", "qwen_decode3", "mistral_
             out["decode_longchat_7b_100k_b1"] = decode(cfg, p, Q, idx, err, max(w.budgets))
         out["status"] = ice.ice_status_string(ice.ice_check(err))
         del cfg, p, Q, idx, err
+    # each part on its own: a failure is reported under the part's name and the others still run
+    for name, fn, wanted in (("qwen_decode", part_qwen_decode, "qwen_decode" in parts),
+                             ("qwen_decode3", part_qwen_decode3, "qwen_decode3" in parts),
+                             ("mistral_insert", part_mistral_insert, "mistral_insert" in parts),
+                             ("qwen_host_pool", part_qwen_host_pool, "qwen_host_pool" in parts),
+                             ("longchat", part_longchat, "longchat_assign" in parts or "longchat_decode" in parts)):
+        if not wanted:
+            continue
+        try:
+            fn()
+        except Exception as e:  # reported, the other parts stand
+            out[f"{name}_error"] = f"{type(e).__name__}: {e}"
+        torch.cuda.empty_cache()
     del flush, evict, sink
     torch.cuda.empty_cache()
     return out
