@@ -390,7 +390,8 @@ def test_insert_rejected_with_positional_pages():
 
 
 @pytest.mark.parametrize("shape,n_sink,n_window", [("llama_bf16", 0, 0), ("tiny_fp32", 0, 0), ("many_units", 0, 0),
-                                                   ("llama_bf16", 32, 96), ("dense_levels", 0, 0)])
+                                                   ("llama_bf16", 32, 96), ("dense_levels", 0, 0),
+                                                   ("sparse_levels", 0, 0)])
 def test_three_levels_build_and_descent(shape, n_sink, n_window):
     """n_levels = 3: level-2 promotion exact, level-2 parents tie-aware,
     children exact, against oracle.build_level2 on the oracle's own build;
@@ -402,7 +403,10 @@ def test_three_levels_build_and_descent(shape, n_sink, n_window):
          "tiny_fp32": W["tiny"],
          "many_units": W["qwen3_32b_100k"].scaled(n_tokens=4000, batch=3, centres=256),
          # p = 1/2: ~1500 level-2 nodes per unit, more than the descent keeps in shared memory
-         "dense_levels": W["llama31_8b_16k"].scaled(n_tokens=6000, n_q_heads=8, n_kv_heads=2, promote_p=0.5)}[shape]
+         "dense_levels": W["llama31_8b_16k"].scaled(n_tokens=6000, n_q_heads=8, n_kv_heads=2, promote_p=0.5),
+         # p = 1/64: ~25 parents per unit, most units promote none again (the smallest-draw fallback)
+         "sparse_levels": W["llama31_8b_16k"].scaled(n_tokens=1600, batch=2, n_q_heads=8, n_kv_heads=2,
+                                                     promote_p=1.0 / 64)}[shape]
     run = DeviceRun(w, n_levels=3, n_sink=n_sink, n_window=n_window)
     assert run.status == ice.ICE_OK
     th = oracle.promote_threshold(w.promote_p)

@@ -601,3 +601,20 @@ def test_reuse_of_own_positional_three_level_index_is_itself():
               "parent_keys", "parent_e", "pool_k", "pool_v"):
         assert np.array_equal(np.asarray(r[f]), np.asarray(idx[f])), f
     assert r["M2"] == idx["M2"] and r["n_pos"] == idx["n_pos"] and r["level2"] is idx["level2"]
+
+
+def test_level2_with_no_parent_promoted_takes_the_smallest_draw():
+    """p small enough that no parent passes the level-2 draw: the parent of
+    smallest level-2 draw (lowest m on ties) becomes the single level-2 node,
+    and every parent is its child."""
+    for seed_head in range(6):
+        w, th, K, V, idx, lv2 = _l3_unit(N=400, promote_p=1.0 / 64, seed_head=seed_head)
+        pt = idx["parent_tok"]
+        draws = [oracle.promote_draw(w.seed, 0, 0, seed_head, int(t), 2) for t in pt]
+        if any(d < th for d in draws):
+            continue
+        assert list(lv2["node2"]) == [int(np.argmin(draws))]
+        assert np.all(lv2["parent2"] == 0)
+        assert list(lv2["child_start"]) == [0, len(pt)] and np.array_equal(lv2["children"], np.arange(len(pt)))
+        return
+    pytest.skip("every seed promoted some parent to level 2")
