@@ -82,3 +82,19 @@ def test_product_never_touches_the_oracle():
             txt = open(os.path.join(ROOT, "oracle", f), encoding="utf-8").read()
             assert not re.search(r"\bimport\s+semantic_paged_kv_gb300|\bfrom\s+semantic_paged_kv_gb300|"
                                  r"#\s*include\s*[<\"].*(ice\.h|\.cuh)", txt), f
+
+
+def test_config_capacities_cover_positional_pages_and_descent_lists(lib):
+    """Host-side sizing: the default page capacity and the decode output width
+    include the sink / window pages; a three-level decode workspace holds the
+    per-head page lists of the descent."""
+    base = ice.Config(batch=1, n_q_heads=8, n_kv_heads=2, n_tokens=1000)
+    pos = ice.Config(batch=1, n_q_heads=8, n_kv_heads=2, n_tokens=1000, n_sink=40, n_window=70)
+    assert pos.n_pos == 3 + 5 and base.n_pos == 0
+    assert pos.page_cap == base.page_cap + pos.n_pos
+    assert ice.max_selected(pos, 64) == min(4 * 4 + 8, pos.page_cap)  # g = 4 heads x 4 pages + 8 positional
+    three = ice.Config(batch=2, n_q_heads=8, n_kv_heads=2, n_tokens=1000, n_levels=3)
+    assert ice.ice_decode_workspace_bytes(three.params(), 16, ice.max_selected(three, 16)) >= 4 * 4 * 4 * 32
+    # descent: at most 32 pages per head; more is refused before anything runs
+    assert ice.ice_build_workspace_bytes(three.params()) > ice.ice_build_workspace_bytes(
+        ice.Config(batch=2, n_q_heads=8, n_kv_heads=2, n_tokens=1000).params())
