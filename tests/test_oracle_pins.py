@@ -618,3 +618,28 @@ def test_level2_with_no_parent_promoted_takes_the_smallest_draw():
         assert list(lv2["child_start"]) == [0, len(pt)] and np.array_equal(lv2["children"], np.arange(len(pt)))
         return
     pytest.skip("every seed promoted some parent to level 2")
+
+
+def test_handworked_three_levels_and_descent():
+    g = _load("handworked_descent_d2.json")
+    K = np.array(g["keys"], float)
+    n, M2, e = oracle.lift(K)
+    assert M2 == 25 and np.all(e == 0)
+    tp = oracle.assign(K, e, g["parent_tok"])
+    assert tp.tolist() == g["token_parent"]
+    pk = oracle.pack(tp, len(g["parent_tok"]), g["page_size"])
+    for key in ("page_parent", "page_len", "page_tokens"):
+        assert np.asarray(pk[key]).tolist() == g["pages"][key], key
+    idx = dict(pk, S=g["page_size"], parent_tok=np.array(g["parent_tok"]), parent_keys=K[g["parent_tok"]],
+               parent_e=e[g["parent_tok"]], token_parent=tp)
+    # level 2 with the nodes of the example (the promotion draws are pinned separately)
+    p2 = oracle.assign(idx["parent_keys"], idx["parent_e"], g["node2"])
+    assert p2.tolist() == g["parent2"]
+    order = np.argsort(p2, kind="stable")
+    assert order.tolist() == g["children"]
+    lv2 = dict(node2=np.array(g["node2"]), parent2=p2, child_start=np.array(g["child_start"]),
+               children=np.array(g["children"]))
+    for case in g["descent"]:
+        heads, union = oracle.select_descent(np.array(case["q"], float), idx, lv2, case["k_pages"])
+        assert heads == case["head_pages"], case["why"]
+        assert union.tolist() == case["union"], case["why"]
