@@ -67,11 +67,15 @@ class DeviceRun:
     def unit(self, u):
         return u // self.cfg.n_kv_heads, u % self.cfg.n_kv_heads
 
+    def queries(self, step: int = 0):
+        """(host Q, device Q) of a decode step."""
+        Q = workloads.batch_queries(self.w, self.layer, step)
+        return Q, to_dev(Q, self.cfg.torch_dtype)
+
     def decode(self, budget: int, fused: bool = True, step: int = 0, contiguous: bool = True):
         """contiguous=False: ice_decode_step without kbuf/vbuf/buf_len (pages
         gathered on chip only)."""
-        Q = workloads.batch_queries(self.w, self.layer, step)
-        Qd = to_dev(Q, self.cfg.torch_dtype)
+        Q, Qd = self.queries(step)
         buf = ice.DecodeBuffers(self.cfg, budget)
         scale = 1.0 / np.sqrt(self.cfg.head_dim)
         if fused:
@@ -85,6 +89,62 @@ class DeviceRun:
                                        buf.ws)
         st = ice.ice_check(self.err)
         return Q, buf, st
+
+
+class _UnitArrays:
+    """K or V [B, H, N, d] on the device; [b, h] gives the host copy of one
+    unit (fp32), made on first use."""
+
+    def __init__(self, t: torch.Tensor):
+        self.t, self.cache = t, {}
+
+    def __getitem__(self, bh):
+        if bh not in self.cache:
+            self.cache[bh] = self.t[bh].float().cpu().numpy()
+        return self.cache[bh]
+
+
+class _UnitRows:
+    """An index array [U, ...] on the device; [u, ...] indexes the host copy
+    of row u, made on first use."""
+
+    def __init__(self, t: torch.Tensor):
+        self.t, self.cache = t, {}
+
+    def __getitem__(self, key):
+        u, rest = (key[0], key[1:]) if isinstance(key, tuple) else (key, ())
+        u = int(u)
+        if u not in self.cache:
+            r = self.t[u]
+            self.cache[u] = (r.float() if r.dtype == torch.bfloat16 else r).cpu().numpy()
+        return self.cache[u][rest] if rest else self.cache[u]
+
+
+class DeviceDrawnRun(DeviceRun):
+    """A full-size layer on inputs drawn on the device
+    (workloads.batch_kv_device / batch_queries_device, the benchmark's own
+    inputs), built with ice_build_index.  Only the units a test looks at are
+    copied to the host: their K, V rows and index rows, on first use; units
+    are independent problems, so the oracle needs nothing else."""
+
+    def __init__(self, w: workloads.Workload, layer: int = 0, **cfg_kw):
+        self.w = w
+        self.cfg = cfg_of(w, layer=layer, **cfg_kw)
+        self.layer = layer
+        self.Kd, self.Vd, self.C = workloads.batch_kv_device(w, layer)
+        self.K, self.V = _UnitArrays(self.Kd), _UnitArrays(self.Vd)
+        self.idx = ice.Index(self.cfg)
+        self.params = self.cfg.params()
+        self.ws = ice.workspace(ice.ice_build_workspace_bytes(self.params))
+        self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ice.ice_build_index(self.params, self.Kd, self.Vd, self.idx, self.ws, self.err)
+        self.status = ice.ice_check(self.err)
+        self.h = {f: _UnitRows(getattr(self.idx, f)) for f in ice.INDEX_FIELDS if f not in ("pool_k", "pool_v")}
+
+    def queries(self, step: int = 0):
+        assert step == 0
+        Qd = workloads.batch_queries_device(self.w, self.C, self.layer)
+        return Qd.float().cpu().numpy(), Qd
 
 
 # ------------------------------------------------------------ comparisons --

@@ -9,7 +9,8 @@ import torch
 import oracle
 import semantic_paged_kv_gb300 as ice
 import workloads
-from parity_util import DeviceRun, check_build_unit, check_decode_unit, check_pack_unit, to_dev
+from parity_util import (DeviceDrawnRun, DeviceRun, check_build_unit, check_decode_unit, check_pack_unit,
+                         lifted_d2, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -159,6 +160,80 @@ def test_longchat_100k_full_size_sampled():
         assert st == ice.ICE_OK
         for u in (0, 3, 17, 30):
             check_decode_unit(run, u, Q, bgt, buf)
+
+
+def test_qwen_100k_full_size_sampled():
+    """The Qwen3-32B-shaped decode batch at its full size (16 sequences x 8
+    KV heads, g = 8, N = 100000, budget 256) on the benchmark's own inputs
+    (drawn on the device) and in its launch configuration: the score table on
+    the tensor cores, the per-unit selection and the MMA attention.  Build
+    checked on two units (assignment on 800 sampled tokens), decode on four,
+    across both ends of the batch."""
+    run = DeviceDrawnRun(W["qwen3_32b_100k"])
+    assert run.status == ice.ICE_OK
+    assert run.cfg.units == 128
+    for u in (9, 118):
+        check_build_unit(run, u, sample_tokens=800)
+    Q, buf, st = run.decode(256)
+    assert st == ice.ICE_OK
+    for u in (0, 9, 77, 127):
+        check_decode_unit(run, u, Q, 256, buf)
+
+
+def test_qwen_100k_three_levels_full_size_sampled():
+    """The same batch with a third level, as the benchmark's descent decode
+    runs it.  On three units: level 1 as in the two-level build; level-2
+    promotion exact, level-2 parents tie-aware and children exact against
+    oracle.build_level2 over the device's (checked) level 1; the descent
+    selection against oracle.select_descent over the device's tables (fp32
+    near-ties aside); the attention over the selected pages."""
+    w = W["qwen3_32b_100k"]
+    run = DeviceDrawnRun(w, n_levels=3)
+    assert run.status == ice.ICE_OK
+    th = oracle.promote_threshold(w.promote_p)
+    H, g, units = run.h, run.cfg.group, (9, 64, 118)
+    lv2s = {}
+    for u in units:
+        check_build_unit(run, u, sample_tokens=600)
+        b, h = run.unit(u)
+        K = run.K[b, h].astype(np.float64)
+        _, M2, e = oracle.lift(K)
+        Np = int(H["n_parents"][u])
+        pt = H["parent_tok"][u, :Np]
+        lv2 = oracle.build_level2(dict(parent_tok=pt, parent_keys=K[pt], parent_e=e[pt]), seed=w.seed, layer=0, seq=b,
+                                  head=h, thresh=th)
+        n2 = len(lv2["node2"])
+        assert int(H["n_nodes2"][u]) == n2 and np.array_equal(H["node2"][u, :n2], lv2["node2"])
+        p2 = H["parent2"][u, :Np]
+        mism = np.nonzero(p2 != lv2["parent2"])[0]
+        assert len(mism) <= max(1, Np // 1000), (u, len(mism))
+        for m in mism:  # only fp32 near-ties may differ
+            da = lifted_d2(K, e, pt[m], pt[lv2["node2"][p2[m]]])
+            do = lifted_d2(K, e, pt[m], pt[lv2["node2"][lv2["parent2"][m]]])
+            assert da - do <= 2 * 1e-6 * M2, (u, m, da, do)
+        if len(mism) == 0:
+            assert np.array_equal(H["child_start"][u, :n2 + 1], lv2["child_start"])
+            assert np.array_equal(H["children"][u, :Np], lv2["children"])
+        lv2s[u] = lv2
+    Q, buf, st = run.decode(256)
+    assert st == ice.ICE_OK
+    agree = 0
+    for u in units:
+        b, h = run.unit(u)
+        q = Q[b, h * g:(h + 1) * g].astype(np.float64)
+        Np, P = int(H["n_parents"][u]), int(H["n_pages"][u])
+        pt = H["parent_tok"][u, :Np]
+        tables = dict(parent_keys=run.K[b, h][pt], n_pages=P, page_parent=H["page_parent"][u, :P])
+        _, union = oracle.select_descent(q, tables, lv2s[u], 256 // 16)
+        cnt = int(buf.sel_count[u])
+        got = buf.sel_pages[u, :cnt].cpu().numpy()
+        assert np.all(np.diff(got) > 0) and np.all(buf.sel_pages[u, cnt:].cpu().numpy() == -1)
+        agree += np.array_equal(got, union)
+        pk, pv = run.pool(u)
+        kb, vb, bl = oracle.gather(pk, pv, H["page_len"][u, :P], got)
+        out = oracle.attention(q, kb, vb, bl, 1.0 / np.sqrt(128))
+        assert np.max(np.abs(buf.O[b, h * g:(h + 1) * g].cpu().numpy() - out)) <= 2e-3
+    assert agree >= len(units) - 1, agree
 
 
 def test_promote_all_is_exact_topk_mips():

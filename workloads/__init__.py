@@ -166,8 +166,9 @@ def batch_queries(w: Workload, layer: int = 0, step: int = 0) -> np.ndarray:
 # contexts, batch 16), where drawing on the host takes tens of seconds.  Same
 # recipe as unit_kv / unit_queries (per-unit N(0, I) centres, spread noise,
 # log-normal norms when set, N(0, I) values), drawn from torch's generator on
-# the device instead of PCG64, so the values differ from the host draws; only
-# timing runs use them (parity runs use the host arrays above).
+# the device instead of PCG64, so the values differ from the host draws.  The
+# timing runs use them, and so do the full-size parity tests, which copy the
+# units they check back to the host for the oracle.
 def _torch_gen(w: Workload, layer: int, stream: int, device):
     import torch
     g = torch.Generator(device=device)
