@@ -102,6 +102,23 @@ def test_insert_stream_mistral_shaped():
         check_decode_unit(run, u, Q, 256, buf)
 
 
+def test_insert_stream_mistral_full_size():
+    """The Mistral-7B-shaped layer at its full size (32/8 heads, N = 36864)
+    with the 128 decode-step inserts the benchmark times, one
+    ice_insert_tokens call per step for all 8 units: every unit's tables,
+    pool and page chains against the oracle's insert started from the same
+    built index, then the decode over the grown index on every unit."""
+    w = W["mistral_7b_36k"]
+    run = _run_inserts(w, 128)
+    assert int(run.idx.n_indexed.sum()) == run.cfg.units * (w.n_tokens + 128)
+    run.h = {f: getattr(run.idx, f).float().cpu().numpy() if f == "parent_keys" else getattr(run.idx, f).cpu().numpy()
+             for f in ice.INDEX_FIELDS if f not in ("pool_k", "pool_v")}
+    Q, buf, st = run.decode(256)
+    assert st == ice.ICE_OK
+    for u in range(run.cfg.units):
+        check_decode_unit(run, u, Q, 256, buf)
+
+
 def test_insert_single_parent_splits_full_page_at_17():
     """p = 0: one parent, sequential pages; the last page (8 tokens) fills,
     and the 17th token of that page opens a new page linked after it."""
