@@ -321,6 +321,32 @@ def test_insert_p1_creates_one_token_pages():
     _unit_invariants(ui)
 
 
+def test_exact_ties_take_the_lowest_parent():
+    """Exact ties of the lifted distance go to the lowest parent index m, in
+    the build's assignment and in the insert; a promoted token is its own
+    parent even when an earlier parent has the same key (distance 0 too).
+    Integer coordinates keep every distance exact in double."""
+    # parents: tokens 0 (0, 5) and 1 (5, 0); M^2 = 25, e = 0 for both
+    K = np.array([[0, 5], [5, 0], [3, 3], [0, 5], [5, 0]], float)
+    n, M2, e = oracle.lift(K)
+    assert M2 == 25 and e[0] == 0 and e[1] == 0
+    # token 2: |(3,3) - (0,5)|^2 = 9 + 4 = 13 = |(3,3) - (5,0)|^2, same e gap -> m = 0
+    assert oracle.assign(K, e, [0, 1]).tolist() == [0, 1, 0, 0, 1]
+    # parents with equal keys (tokens 1 and 4): each its own parent; token 2 ties three ways -> m = 0
+    assert oracle.assign(K, e, [1, 3, 4]).tolist() == [1, 0, 0, 1, 2]
+    # insert: k = (0.5, 0.5, 0, 0) is at lifted distance 1 from both unit parents -> m = 0
+    d, S = 4, 16
+    P2 = np.array([[1.0, 0, 0, 0], [0, 1.0, 0, 0]])
+    idx = {"S": S, "M2": 1.0, "parent_tok": np.array([0, 1]), "parent_keys": P2, "parent_e": np.zeros(2),
+           "n_pages": 2, "page_parent": np.array([0, 1]), "page_len": np.array([1, 1]),
+           "page_tokens": np.array([[0] + [-1] * 15, [1] + [-1] * 15]), "pool_k": np.zeros((2, S, d)),
+           "pool_v": np.zeros((2, S, d)), "token_parent": np.array([0, 1]), "token_page": np.array([0, 1]),
+           "token_slot": np.array([0, 0])}
+    ui = oracle.UnitIndex(idx, d, np_cap=4, page_cap=8, n_cap=8)
+    ui.insert(np.array([0.5, 0.5, 0, 0]), np.ones(d), 2, seed=0, layer=0, seq=0, head=0, thresh=0)
+    assert ui.token_parent[2] == 0 and ui.page_len[:2].tolist() == [2, 1]
+
+
 def test_insert_attaches_to_nearest_parent_and_splits_at_17():
     """Keys equal to parent 0's key attach to parent 0 (distance 0); once its
     last page holds 16 tokens the 17th opens a new page."""
