@@ -440,7 +440,8 @@ size_t ice_host_pool_staging_bytes(const ice_params *p, int32_t max_sel);
  * a HOST copy of ice_index.page_len [U, page_cap].  Returns once the copy is
  * enqueued; the next call first waits for this transfer to have read the
  * staging buffer.  ICE_ERR_CAPACITY if the staging buffer or dst_bytes is
- * too small, ICE_ERR_INVALID_ARG on a page id outside [0, page_cap).
+ * too small, ICE_ERR_INVALID_ARG on a page id outside [0, page_cap) or a
+ * count outside [0, max_sel] (nothing is transferred then).
  */
 ice_status ice_host_pool_gather_h2d(ice_host_pool *hp, const ice_params *p, const int32_t *sel_pages_host,
                                     const int32_t *sel_count_host, const int32_t *page_len_host, int32_t max_sel,

@@ -177,6 +177,11 @@ ice_status ice_host_pool_gather_h2d(ice_host_pool *hp, const ice_params *p, cons
     run_all(hp, [&](int w) {
         for (size_t u = w; u < U; u += nt) {
             const int n = sel_count_host[u];
+            if (n < 0 || n > max_sel) {  // a count the selection cannot have produced
+                std::lock_guard<std::mutex> lk(bad_mu);
+                bad = true;
+                continue;
+            }
             for (int x = 0; x < max_sel; ++x) {
                 const size_t slot = u * max_sel + x;
                 if (x >= n) {

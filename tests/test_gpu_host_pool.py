@@ -79,6 +79,14 @@ def test_host_pool_direct_and_staged_match_hbm_pool():
         ice.ice_sparse_attn_decode(cfg.params(), Qd, kbuf, vbuf, blen, ref.sel_count, 1.0 / np.sqrt(128), O, ws)
         # a different split of the pages before the log-sum-exp merge than the fused step
         assert torch.max(torch.abs(O - ref.O)).item() <= 1e-5
+        # host-side checks: a page id outside the pool or a count outside [0, max_sel] is refused, nothing copied
+        bad_sel, bad_cnt = sel_h.clone(), cnt_h.clone()
+        bad_sel[0, 0] = cfg.page_cap
+        bad_cnt[1] = max_sel + 1
+        for s_h, c_h in ((bad_sel, cnt_h), (sel_h, bad_cnt)):
+            with pytest.raises(ice.IceError) as ex:
+                ice.ice_host_pool_gather_h2d(hp, cfg.params(), s_h, c_h, plen_h, max_sel, dst)
+            assert ex.value.status == ice.ICE_ERR_INVALID_ARG
     finally:
         hp.close()
 
