@@ -669,3 +669,21 @@ def test_handworked_three_levels_and_descent():
         heads, union = oracle.select_descent(np.array(case["q"], float), idx, lv2, case["k_pages"])
         assert heads == case["head_pages"], case["why"]
         assert union.tolist() == case["union"], case["why"]
+
+
+def test_handworked_sink_and_window():
+    g = _load("handworked_sink_window_d2.json")
+    K, V = np.array(g["keys"], float), np.array(g["values"], float)
+    assert oracle.positional_split(len(K), g["n_sink"], g["n_window"]) == tuple(g["split"])
+    assert oracle.positional_pages(len(K), g["n_sink"], g["n_window"], g["page_size"]) == g["n_pos"]
+    idx = oracle.build_unit_positional(K, V, seed=0, layer=0, seq=0, head=0, thresh=oracle.promote_threshold(1.0),
+                                       S=g["page_size"], n_sink=g["n_sink"], n_window=g["n_window"])
+    assert idx["M2"] == g["M2"] and np.asarray(idx["parent_e"]).tolist() == g["parent_e"]
+    for key in ("parent_tok", "token_parent", "page_parent", "page_len", "page_tokens", "token_page", "token_slot"):
+        assert np.asarray(idx[key]).tolist() == g[key], key
+    assert idx["n_pages"] == g["n_pages"] and idx["n_pos"] == g["n_pos"]
+    for case in g["decode"]:
+        dec = oracle.decode_unit(idx, np.array(case["q"], float), case["budget_tokens"])
+        assert dec["sel_pages"].tolist() == case["sel_pages"], case["why"]
+        if "out" in case:
+            assert np.allclose(dec["out"], case["out"], rtol=0, atol=1e-15), case["why"]
