@@ -71,6 +71,12 @@ MUTANTS = [
     # sink / window pages
     ("window_not_cut_at_the_sink", PY, [("return se, max(se, N - max(n_window, 0))",
                                          "return se, N - max(n_window, 0)")]),
+    ("sink_pages_run_past_the_sink", PY, [("[(a, min(a + S, se)) for a in range(0, se, S)]",
+                                           "[(a, a + S) for a in range(0, se, S)]")]),
+    ("window_pages_before_sink_pages", PY, [
+        ("ranges = [(a, min(a + S, se)) for a in range(0, se, S)] + [(a, min(a + S, N)) for a in range(ws, N, S)]",
+         "ranges = [(a, min(a + S, N)) for a in range(ws, N, S)] + [(a, min(a + S, se)) for a in range(0, se, S)]")]),
+    ("positional_pages_owned_by_parent_0", PY, [("np.full(len(ranges), -1, np.int32)", "np.full(len(ranges), 0, np.int32)")]),
     ("middle_promotion_ids_not_absolute", PY, [("return (out + lo).astype(np.int32)", "return out.astype(np.int32)")]),
     ("positional_pages_not_attended", PY, [("    if n_pos:\n        sel = np.concatenate",
                                             "    if n_pos < 0:\n        sel = np.concatenate")]),
