@@ -187,6 +187,32 @@ def gpu_id_for(dev) -> str | None:
 
 
 # ------------------------------------------------------- CPU oracle leg ---
+def host_cpu() -> str:
+    """The host's CPU model and logical CPU count, for the CPU-baseline record."""
+    name = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            k, _, v = line.partition(":")
+            if k.strip() == "Model name" and v.strip():
+                name = v.strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not name:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    k, _, v = line.partition(":")
+                    if k.strip().lower() == "model name" and v.strip():
+                        name = v.strip()
+                        break
+        except OSError:
+            pass
+    import platform
+    return f"{name or 'unknown model'} ({platform.machine()}, {os.cpu_count()} logical CPUs)"
+
+
 def oracle_sample(w: workloads.Workload, budget: int, units: int, n_tokens: int | None = None, passes: int = 1,
                   min_seconds: float = 0.0, max_seconds: float = float("inf")):
     """Time the oracle (as it stands) on `units` units of the workload: build
@@ -251,7 +277,8 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(w, budget, args.gpus, args.sets),
-        "cpu_baseline": {"value": value, "unit": "keys/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "keys/s", "cores": threads, "kind": "oracle", "sample": sample,
+                         "cpu": host_cpu()},
         "e2e": {"value": value, "unit": "keys/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 
@@ -821,6 +848,7 @@ def run_ours(args):
         units = args.cpu_units or min(U, os.cpu_count() or 1)
         cdt, passes, threads = oracle_sample(w, budget, units, min_seconds=10.0, max_seconds=30.0)
         cpu = {"value": passes * units * N / cdt, "unit": "keys/s", "cores": threads, "kind": "oracle",
+               "cpu": host_cpu(),
                "sample": f"{units} of {U} units (KV heads) of this workload, full N={N}: index build + one decode "
                          f"step at budget {budget}, one unit per host thread, {passes} passes ({cdt:.1f} s)"}
 
