@@ -49,16 +49,28 @@ def test_host_only_entry_points(lib):
     assert ice.ice_decode_workspace_bytes(cfg.params(), 256, 64) > 0
 
 
-@pytest.mark.parametrize("field,value,status", [("head_dim", 64, ice.ICE_ERR_UNSUPPORTED),
-                                                 ("page_size", 8, ice.ICE_ERR_UNSUPPORTED),
-                                                 ("n_levels", 4, ice.ICE_ERR_UNSUPPORTED),
-                                                 ("n_kv_heads", 3, ice.ICE_ERR_INVALID_ARG),
-                                                 ("dtype", 7, ice.ICE_ERR_INVALID_ARG),
-                                                 ("promote_thresh", 2 ** 32 + 1, ice.ICE_ERR_INVALID_ARG),
-                                                 ("n_cap", 10, ice.ICE_ERR_INVALID_ARG)])
-def test_invalid_params_rejected_on_host(lib, field, value, status):
+@pytest.mark.parametrize("fields,status", [({"head_dim": 64}, ice.ICE_ERR_UNSUPPORTED),
+                                           ({"page_size": 8}, ice.ICE_ERR_UNSUPPORTED),
+                                           ({"n_levels": 4}, ice.ICE_ERR_UNSUPPORTED),
+                                           ({"n_levels": 1}, ice.ICE_ERR_UNSUPPORTED),
+                                           ({"n_levels": 3, "np_cap": 50001}, ice.ICE_ERR_UNSUPPORTED),
+                                           ({"n_q_heads": 48}, ice.ICE_ERR_UNSUPPORTED),
+                                           ({"n_kv_heads": 3}, ice.ICE_ERR_INVALID_ARG),
+                                           ({"batch": 4096}, ice.ICE_ERR_INVALID_ARG),
+                                           ({"batch": 0}, ice.ICE_ERR_INVALID_ARG),
+                                           ({"dtype": 7}, ice.ICE_ERR_INVALID_ARG),
+                                           ({"promote_thresh": 2 ** 32 + 1}, ice.ICE_ERR_INVALID_ARG),
+                                           ({"n_cap": 10}, ice.ICE_ERR_INVALID_ARG),
+                                           ({"n_tokens": -1}, ice.ICE_ERR_INVALID_ARG),
+                                           ({"np_cap": 0}, ice.ICE_ERR_INVALID_ARG),
+                                           ({"page_cap": 0}, ice.ICE_ERR_INVALID_ARG),
+                                           ({"n_sink": -1}, ice.ICE_ERR_INVALID_ARG),
+                                           ({"n_window": -1}, ice.ICE_ERR_INVALID_ARG)],
+                         ids=lambda x: "-".join(f"{k}={v}" for k, v in x.items()) if isinstance(x, dict) else str(x))
+def test_invalid_params_rejected_on_host(lib, fields, status):
     p = ice.Config(batch=1, n_q_heads=8, n_kv_heads=2, n_tokens=100).params()
-    setattr(p, field, value)
+    for field, value in fields.items():
+        setattr(p, field, value)
     with pytest.raises(ice.IceError) as ei:
         ice.ice_build_workspace_bytes(p)
     assert ei.value.status == status
