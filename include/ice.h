@@ -177,7 +177,9 @@ ice_status ice_build_workspace_bytes(const ice_params *p, size_t *bytes);
  * ice_build_lift_promote, then ice_build_assign, then ice_build_pack, on one
  * stream.  The three stages are also exported so that they can be timed or
  * overlapped separately; they must run in this order with the same
- * arguments and workspace.
+ * arguments and workspace.  Every argument (params, index arrays, K, V,
+ * workspace) is checked before the first stage is launched:
+ * ICE_ERR_INVALID_ARG / ICE_ERR_UNSUPPORTED leave the index untouched.
  */
 ice_status ice_build_index(const ice_params *p, const void *K, const void *V, const ice_index *idx,
                            void *ws, size_t ws_bytes, int32_t *err_dev, void *stream);

@@ -307,7 +307,12 @@ ice_status ice_build_pack(const ice_params *p, const void *K, const void *V, con
 
 ice_status ice_build_index(const ice_params *p, const void *K, const void *V, const ice_index *idx, void *ws,
                            size_t ws_bytes, int32_t *err_dev, void *stream) {
-    ice_status st = ice_build_lift_promote(p, K, idx, ws, ws_bytes, err_dev, stream);
+    // every argument is checked before the first stage is launched
+    BuildWs w;
+    ice_status st = build_common(p, K, idx, ws, ws_bytes, &w);
+    if (st) return st;
+    if (p->n_tokens > 0 && (!V || !aligned16(V))) return fail(ICE_ERR_INVALID_ARG, "V must be a 16-byte aligned device pointer");
+    st = ice_build_lift_promote(p, K, idx, ws, ws_bytes, err_dev, stream);
     if (st) return st;
     if ((st = ice_build_assign(p, K, idx, ws, ws_bytes, err_dev, stream))) return st;
     return ice_build_pack(p, K, V, idx, ws, ws_bytes, err_dev, stream);
