@@ -16,6 +16,7 @@ import os
 import shutil
 import subprocess
 import sys
+from concurrent.futures import ThreadPoolExecutor
 
 import pytest
 
@@ -116,12 +117,24 @@ def _run_pins_against(tmp_path, fname=None, subs=()):
     return r.returncode, r.stdout[-3000:] + r.stderr[-1000:]
 
 
-def test_unchanged_copy_passes_the_pins(tmp_path):
-    rc, out = _run_pins_against(tmp_path)
+@pytest.fixture(scope="module")
+def outcomes(tmp_path_factory):
+    """(return code, output tail) of the pin suite against the unchanged copy
+    and against every mutant, the child processes run side by side."""
+    jobs = {"control": (None, ())}
+    jobs.update({name: (fname, subs) for name, fname, subs in MUTANTS})
+    with ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
+        futs = {name: ex.submit(_run_pins_against, tmp_path_factory.mktemp(name), fname, subs)
+                for name, (fname, subs) in jobs.items()}
+        return {name: f.result() for name, f in futs.items()}
+
+
+def test_unchanged_copy_passes_the_pins(outcomes):
+    rc, out = outcomes["control"]
     assert rc == 0, out
 
 
-@pytest.mark.parametrize("name,fname,subs", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_pins_catch_planted_mistake(name, fname, subs, tmp_path):
-    rc, out = _run_pins_against(tmp_path, fname, subs)
+@pytest.mark.parametrize("name", [m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(name, outcomes):
+    rc, out = outcomes[name]
     assert rc == 1, f"{name}: the pins let this mistake through (rc {rc})\n{out}"
