@@ -31,8 +31,11 @@ MUTANTS = [
     ("splitmix64_gamma_typo", C, [("0x9E3779B97F4A7C15ULL", "0x9E3779B97F4A7C17ULL")]),
     ("promotion_fallback_takes_largest_draw", C, [("if (u < bu) { bu = u; best = j; }",
                                                    "if (u > bu) { bu = u; best = j; }")]),
+    ("promotion_draws_at_level_2", C, [("        uint32_t u = orc_promote_draw(seed, layer, seq, head, j, 1);\n        if",
+                                        "        uint32_t u = orc_promote_draw(seed, layer, seq, head, j, 2);\n        if")]),
     # step a1, the lift
     ("lift_without_sqrt", C, [("e_out[j] = sqrt(r > 0.0 ? r : 0.0);", "e_out[j] = r > 0.0 ? r : 0.0;")]),
+    ("lift_adds_the_norm", C, [("double r = M2 - n_out[j];", "double r = M2 + n_out[j];")]),
     ("lift_takes_the_smallest_norm", C, [("if (s > M2) M2 = s;", "if (j == 0 || s < M2) M2 = s;")]),
     ("lifted_coordinate_dropped_from_the_distance", C, [("    return s + t * t;\n}", "    return s;\n}")]),
     # step a3, the assignment
@@ -47,6 +50,7 @@ MUTANTS = [
                                         "for (int64_t r = 0; r < count[m]; r += S - 1) {"),
                                        ("(count[m] - r) < S ? (count[m] - r) : S)",
                                         "(count[m] - r) < S - 1 ? (count[m] - r) : S - 1)")]),
+    ("pack_every_page_full_length", C, [("page_len[P] = len;", "page_len[P] = S;")]),
     # step a5, the pool
     ("pool_pad_slots_not_zero", C, [("dk[i] = j >= 0 ? K[(int64_t)j * d + i] : 0.0;",
                                      "dk[i] = K[(int64_t)(j >= 0 ? j : 0) * d + i];")]),
@@ -57,6 +61,8 @@ MUTANTS = [
                                              "return (x->id < y->id) - (x->id > y->id);")]),
     ("select_every_head_scores_with_head_0", C, [("s += q[(int64_t)h * d + i] * parent_keys[(int64_t)m * d + i];",
                                                   "s += q[i] * parent_keys[(int64_t)m * d + i];")]),
+    ("union_of_the_first_head_only", C, [("if (r < k) in_union[order[r].id] = 1;",
+                                          "if (r < k && h == 0) in_union[order[r].id] = 1;")]),
     # step a9, the gather
     ("gather_full_length_pages", C, [("buf_len[u] = page_len[p];", "buf_len[u] = S;")]),
     # step a10, the attention
@@ -81,6 +87,8 @@ MUTANTS = [
     ("middle_promotion_ids_not_absolute", PY, [("return (out + lo).astype(np.int32)", "return out.astype(np.int32)")]),
     ("positional_pages_not_attended", PY, [("    if n_pos:\n        sel = np.concatenate",
                                             "    if n_pos < 0:\n        sel = np.concatenate")]),
+    ("budget_counts_the_positional_pages", PY, [("    k_pages = -(-budget_tokens // S)\n",
+                                                 "    k_pages = max(0, -(-budget_tokens // S) - int(idx.get(\"n_pos\", 0)))\n")]),
     # inter-layer reuse
     ("reuse_keeps_the_previous_layers_keys", PY, [
         ("parent_keys=K[parent_tok] if N else K[:0],\n                parent_e=e[parent_tok] if N else e[:0], "
@@ -94,6 +102,7 @@ MUTANTS = [
                                                  "node2 = np.array([int(np.argmax(d2))])")]),
     ("descent_keeps_the_lowest_level2_scores", PY, [("key=lambda i: (-s2[i], i))[:k_pages]",
                                                      "key=lambda i: (s2[i], i))[:k_pages]")]),
+    ("descent_pages_not_limited_to_k", PY, [("                if len(pages) < k_pages:", "                if True:")]),
     ("descent_children_by_ascending_score", PY, [("sorted(cand, key=lambda m: (-s1[m], m))",
                                                   "sorted(cand, key=lambda m: (s1[m], m))")]),
 ]
