@@ -25,13 +25,18 @@ BUDGET = 64
 class _Run:
     """What the helpers read from a device run, filled from the oracle (one unit)."""
 
-    def __init__(self):
+    def __init__(self, n_sink: int = 0, n_window: int = 0):
         w = self.w = W
-        self.cfg = cfg_of(w, layer=0)
+        self.cfg = cfg_of(w, layer=0, n_sink=n_sink, n_window=n_window)
         self.layer = 0
         self.K, self.V = workloads.batch_kv(w, 0)
         th = oracle.promote_threshold(w.promote_p)
-        ref = self.ref = oracle.build_unit(self.K[0, 0], self.V[0, 0], seed=w.seed, layer=0, seq=0, head=0, thresh=th)
+        if n_sink or n_window:
+            ref = oracle.build_unit_positional(self.K[0, 0], self.V[0, 0], seed=w.seed, layer=0, seq=0, head=0,
+                                               thresh=th, n_sink=n_sink, n_window=n_window)
+        else:
+            ref = oracle.build_unit(self.K[0, 0], self.V[0, 0], seed=w.seed, layer=0, seq=0, head=0, thresh=th)
+        self.ref = ref
         cfg, N, S, d = self.cfg, w.n_tokens, self.cfg.page_size, self.cfg.head_dim
         Np, P = len(ref["parent_tok"]), int(ref["n_pages"])
         npc, pc = cfg.np_cap, cfg.page_cap
@@ -42,10 +47,11 @@ class _Run:
             return out
 
         pp = np.asarray(ref["page_parent"])
-        cnt = np.bincount(pp, minlength=Np)
+        cnt = np.bincount(pp[pp >= 0], minlength=Np)
         first = np.concatenate([[0], np.cumsum(cnt)[:-1]])
         nxt = np.arange(1, P + 1)
         nxt[np.cumsum(cnt) - 1] = -1
+        nxt[len(pp[pp >= 0]):] = -1
         self.h = {"n_parents": np.array([Np]), "n_pages": np.array([P]), "n_indexed": np.array([N]),
                   "m2": np.array([ref["M2"]]), "parent_tok": row(ref["parent_tok"], npc, -1),
                   "parent_e": row(np.asarray(ref["parent_e"], np.float32), npc, 0, np.float32),
@@ -74,7 +80,7 @@ class _Run:
         cfg, g = self.cfg, self.cfg.group
         Q = workloads.batch_queries(self.w, 0, 0)
         dec = oracle.decode_unit(self.ref, Q[0, :g], BUDGET)
-        max_sel, S, d = g * (BUDGET // cfg.page_size), cfg.page_size, cfg.head_dim
+        max_sel, S, d = g * (BUDGET // cfg.page_size) + cfg.n_pos, cfg.page_size, cfg.head_dim
         n = len(dec["sel_pages"])
         sel = torch.full((1, max_sel), -1, dtype=torch.int32)
         sel[0, :n] = torch.from_numpy(dec["sel_pages"])
@@ -172,5 +178,20 @@ def test_decode_check_rejects_a_planted_difference(plant):
     run = _Run()
     Q, buf = run.decode()
     DECODE_PLANTS[plant](run, buf)
+    with pytest.raises(AssertionError):
+        check_decode_unit(run, 0, Q, BUDGET, buf)
+
+
+def test_decode_check_with_sink_and_window_pages():
+    """The positional branch of check_decode_unit: the oracle's own decode
+    passes; a union without its last positional page fails."""
+    run = _Run(n_sink=16, n_window=40)
+    assert run.cfg.n_pos == 4
+    Q, buf = run.decode()
+    check_decode_unit(run, 0, Q, BUDGET, buf)
+    n = int(buf.sel_count[0])
+    buf.sel_pages[0, n - 1] = -1
+    buf.sel_count[0] = n - 1
+    buf.buf_len[0, n - 1] = 0
     with pytest.raises(AssertionError):
         check_decode_unit(run, 0, Q, BUDGET, buf)
