@@ -339,6 +339,8 @@ def at_scale(pk, reps: int = 30, parts=("qwen_decode", "qwen_decode3", "mistral_
     sink = torch.empty((), dtype=torch.float32, device="cuda")
     cap = torch.cuda.Stream()
 
+    spread = {}  # p10 and p90 (ms) of the replays of the last timed call
+
     def timed(fn):
         for _ in range(3):
             fn()
@@ -358,6 +360,7 @@ def at_scale(pk, reps: int = 30, parts=("qwen_decode", "qwen_decode3", "mistral_
             b.record()
             torch.cuda.synchronize()
             ts.append(a.elapsed_time(b))
+        spread["p10"], spread["p90"] = float(np.percentile(ts, 10)), float(np.percentile(ts, 90))
         return statistics.median(ts)  # ms
 
     def build(w, n_levels=2):
@@ -379,6 +382,7 @@ def at_scale(pk, reps: int = 30, parts=("qwen_decode", "qwen_decode3", "mistral_
         scale = 1.0 / math.sqrt(cfg.head_dim)
         ms = timed(lambda: ice.ice_decode_step(p, idx, Q, budget, buf.sel_pages, buf.sel_count, buf.kbuf, buf.vbuf,
                                                buf.buf_len, scale, buf.O, buf.ws, err))
+        us_p10, us_p90 = 1000 * spread["p10"], 1000 * spread["p90"]
         # the selection alone (score table + per-unit top-k and union), same flush
         ms_sel = timed(lambda: ice.ice_select_pages(p, idx, Q, budget, buf.sel_pages, buf.sel_count, buf.ws, err))
         # the same step without the contiguous buffer (pages gathered on chip only)
@@ -391,8 +395,8 @@ def at_scale(pk, reps: int = 30, parts=("qwen_decode", "qwen_decode3", "mistral_
         b_min = np_tot * d * 2 + sel_tot * S * d * 2 * 2 + qo
         b_pipe = b_min + sel_tot * S * d * 2 * 2
         gbs_min, gbs_pipe = b_min / (ms * 1e-3) / 1e9, b_pipe / (ms * 1e-3) / 1e9
-        return {"us": 1000 * ms, "select_only_us": 1000 * ms_sel, "budget_tokens": budget, "parents": np_tot,
-                "selected_pages": sel_tot,
+        return {"us": 1000 * ms, "us_p10": us_p10, "us_p90": us_p90, "select_only_us": 1000 * ms_sel,
+                "budget_tokens": budget, "parents": np_tot, "selected_pages": sel_tot,
                 "bytes_min": b_min, "hbm_gbs_min_bytes": gbs_min, "frac_min_bytes": gbs_min / pk["hbm"],
                 "bytes_pipeline": b_pipe, "hbm_gbs_pipeline_bytes": gbs_pipe, "frac_pipeline_bytes": gbs_pipe / pk["hbm"],
                 "no_buffer": {"us": 1000 * ms_nb, "bytes": b_min,
