@@ -69,7 +69,7 @@ def _load():
         lib.orc_select.argtypes = [P, i32, i32, P, i32, P, i32, i32, P, P, P]
         lib.orc_gather.argtypes = [P, P, P, i32, i32, i32, P, i32, P, P, P]
         lib.orc_attention.argtypes = [P, i32, i32, P, P, P, i32, i32, f64, P]
-        lib.orc_insert.argtypes = [u64, i32, i32, i32, u64, i32, i32, f64, P, P, i64,
+        lib.orc_insert.argtypes = [u64, i32, i32, i32, u64, i32, i32, f64, P, P, i64, i32,
                                    i32, P, P, P, P,
                                    i32, P, P, P, P, P, P,
                                    i64, P, P, P]
@@ -292,6 +292,22 @@ def build_unit_positional(K, V, *, seed: int, layer: int, seq: int, head: int, t
     parent_tok = promote_range(seed, layer, seq, head, se, ws, thresh)
     Np = len(parent_tok)
     tp_mid = assign(Km, e_m, parent_tok - se) if Np else np.zeros(0, np.int32)
+    pk = pack_positional(tp_mid, Np, N, se, ws, S)
+    pool_k, pool_v = scatter(K, V, pk["page_tokens"], S)
+    e = np.full(N, np.nan)
+    e[se:ws] = e_m
+    return dict(n=n_m, M2=M2, e=e, parent_tok=parent_tok, parent_keys=K[parent_tok] if Np else K[:0],
+                parent_e=e[parent_tok] if Np else e[:0], pool_k=pool_k, pool_v=pool_v, S=S, **pk)
+
+
+def pack_positional(tp_mid, Np: int, N: int, se: int, ws: int, S: int = 16) -> dict:
+    """The pages of a unit with sink / window tokens (article section 六):
+    the middle tokens [se, ws) with parents tp_mid (middle-relative token
+    order) packed as in pack(), then the sink tokens [0, se) in positional
+    pages of S in token order, then the window tokens [ws, N).  Returns the
+    page and token tables over all N tokens (token_parent -2 outside the
+    middle, page_parent -1 for positional pages)."""
+    tp_mid = np.asarray(tp_mid, np.int32)
     pk = pack(tp_mid, Np, S) if ws > se else dict(n_pages=0, page_parent=np.zeros(0, np.int32),
                                                    page_len=np.zeros(0, np.int32),
                                                    page_tokens=np.zeros((0, S), np.int32),
@@ -315,13 +331,8 @@ def build_unit_positional(K, V, *, seed: int, layer: int, seq: int, head: int, t
             t = page_tokens[p, sl]
             if t >= 0:
                 token_page[t], token_slot[t] = p, sl
-    pool_k, pool_v = scatter(K, V, page_tokens, S)
-    e = np.full(N, np.nan)
-    e[se:ws] = e_m
-    return dict(n=n_m, M2=M2, e=e, parent_tok=parent_tok, parent_keys=K[parent_tok] if Np else K[:0],
-                parent_e=e[parent_tok] if Np else e[:0], token_parent=token_parent, pool_k=pool_k, pool_v=pool_v,
-                S=S, n_pages=P, n_pos=len(ranges), split=(se, ws), page_parent=page_parent, page_len=page_len,
-                page_tokens=page_tokens, token_page=token_page, token_slot=token_slot)
+    return dict(token_parent=token_parent, n_pages=P, n_pos=len(ranges), split=(se, ws), page_parent=page_parent,
+                page_len=page_len, page_tokens=page_tokens, token_page=token_page, token_slot=token_slot)
 
 
 # ------------------------------------------------------------ level 2 ----
@@ -347,10 +358,18 @@ def build_level2(idx: dict, *, seed: int, layer: int, seq: int, head: int, thres
         node2 = np.array([int(np.argmin(d2))])
     node2 = node2.astype(np.int32)
     parent2 = assign(idx["parent_keys"], idx["parent_e"], node2)
+    return dict(node2=node2, parent2=parent2.astype(np.int32), **level2_groups(parent2, len(node2)))
+
+
+def level2_groups(parent2, n2: int) -> dict:
+    """The children of every level-2 node: the parents grouped by their
+    level-2 parent (ascending m inside a group), group i at
+    children[child_start[i] : child_start[i + 1])."""
+    parent2 = np.asarray(parent2, np.int64)
     order = np.argsort(parent2, kind="stable").astype(np.int32)
-    counts = np.bincount(parent2, minlength=len(node2))
+    counts = np.bincount(parent2, minlength=n2)
     child_start = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
-    return dict(node2=node2, parent2=parent2.astype(np.int32), child_start=child_start, children=order)
+    return dict(child_start=child_start, children=order)
 
 
 def select_descent(q, idx: dict, lv2: dict, k_pages: int) -> tuple[list, np.ndarray]:
@@ -461,10 +480,14 @@ class UnitIndex:
         self.token_slot = np.full(n_cap, -1, np.int32); self.token_slot[:N] = idx["token_slot"]
         self.np_cap, self.page_cap, self.n_cap = np_cap, page_cap, n_cap
 
-    def insert(self, k_new, v_new, pos: int, *, seed: int, layer: int, seq: int, head: int, thresh: int):
+    def insert(self, k_new, v_new, pos: int, *, seed: int, layer: int, seq: int, head: int, thresh: int,
+               parent: int = -1):
+        """One insert (step a11).  parent >= 0 replaces the nearest-parent
+        search by that parent (a test that follows a device's choice at a
+        checked fp32 near-tie); a promoted token ignores it."""
         k = _f64(k_new)
         v = _f64(v_new)
-        rc = _load().orc_insert(seed, layer, seq, head, thresh, self.d, self.S, self.M2, _p(k), _p(v), pos,
+        rc = _load().orc_insert(seed, layer, seq, head, thresh, self.d, self.S, self.M2, _p(k), _p(v), pos, parent,
                                 self.np_cap, ctypes.byref(self.n_parents), _p(self.parent_tok),
                                 _p(self.parent_keys), _p(self.parent_e),
                                 self.page_cap, ctypes.byref(self.n_pages), _p(self.page_parent),

@@ -398,7 +398,7 @@ int orc_attention(const double *q, int32_t g, int32_t d, const double *kbuf, con
 /* ------------------------------------------------------------------------ */
 int orc_insert(uint64_t seed, int32_t layer, int32_t seq, int32_t head, uint64_t thresh,
                int32_t d, int32_t S, double M2, const double *k_new, const double *v_new,
-               int64_t pos,
+               int64_t pos, int32_t forced_parent,
                /* parent level */
                int32_t np_cap, int32_t *n_parents, int32_t *parent_tok, double *parent_keys,
                double *parent_key_e,
@@ -425,11 +425,18 @@ int orc_insert(uint64_t seed, int32_t layer, int32_t seq, int32_t head, uint64_t
         parent_key_e[m] = e;
         *n_parents = Np + 1;
     } else {
-        m = -1;
-        double bd = 0.0;
-        for (int32_t c = 0; c < Np; ++c) {
-            double D = lifted_dist2(k_new, e, parent_keys + (int64_t)c * d, parent_key_e[c], d);
-            if (m < 0 || D < bd) { bd = D; m = c; }
+        if (forced_parent >= 0) {
+            /* the caller's parent: tests that follow a device's choice at a
+             * checked fp32 near-tie of the lifted distance */
+            if (forced_parent >= Np) return ORC_ERR_ARG;
+            m = forced_parent;
+        } else {
+            m = -1;
+            double bd = 0.0;
+            for (int32_t c = 0; c < Np; ++c) {
+                double D = lifted_dist2(k_new, e, parent_keys + (int64_t)c * d, parent_key_e[c], d);
+                if (m < 0 || D < bd) { bd = D; m = c; }
+            }
         }
         for (int32_t p = P - 1; p >= 0; --p)
             if (page_parent[p] == m) { page = p; break; }

@@ -6,8 +6,10 @@ as device outputs (CPU tensors in the layout the library writes): they must
 pass.  Then one output at a time is changed the way a kernel bug would
 change it (a token under a farther parent, two tokens swapped between pages,
 a pool value, a promoted token, M^2, a selected page, a gathered row, a page
-length, the attention output) and the same helper must fail.  Nothing here
-runs the CUDA library."""
+length, the attention output, the wrong page of a parent that straddles the
+budget, a tied page dropped, a parent under a far level-2 node) and the same
+helper must fail, while a reorder of parents that tie within the tolerance
+passes.  Nothing here runs the CUDA library."""
 import types
 
 import numpy as np
@@ -16,7 +18,8 @@ import torch
 
 import oracle
 import workloads
-from parity_util import cfg_of, check_build_unit, check_decode_unit
+from parity_util import (check_build_positional, check_build_unit, check_decode_unit, check_descent_selection,
+                         check_level2_unit, check_union, cfg_of, legal_selections, pages_by_parent)
 
 W = workloads.WORKLOADS["tiny"].scaled(n_tokens=700)
 BUDGET = 64
@@ -25,11 +28,13 @@ BUDGET = 64
 class _Run:
     """What the helpers read from a device run, filled from the oracle (one unit)."""
 
-    def __init__(self, n_sink: int = 0, n_window: int = 0):
+    def __init__(self, n_sink: int = 0, n_window: int = 0, K=None):
         w = self.w = W
         self.cfg = cfg_of(w, layer=0, n_sink=n_sink, n_window=n_window)
         self.layer = 0
         self.K, self.V = workloads.batch_kv(w, 0)
+        if K is not None:
+            self.K = K
         th = oracle.promote_threshold(w.promote_p)
         if n_sink or n_window:
             ref = oracle.build_unit_positional(self.K[0, 0], self.V[0, 0], seed=w.seed, layer=0, seq=0, head=0,
@@ -75,23 +80,31 @@ class _Run:
         P = int(self.h["n_pages"][u])
         return self.idx.pool_k[u, :P].numpy(), self.idx.pool_v[u, :P].numpy()
 
-    def decode(self):
+    def decode(self, budget: int = BUDGET):
         """(Q, buffers) as ice_decode_step leaves them, from the oracle's decode."""
-        cfg, g = self.cfg, self.cfg.group
+        g = self.cfg.group
         Q = workloads.batch_queries(self.w, 0, 0)
-        dec = oracle.decode_unit(self.ref, Q[0, :g], BUDGET)
-        max_sel, S, d = g * (BUDGET // cfg.page_size) + cfg.n_pos, cfg.page_size, cfg.head_dim
-        n = len(dec["sel_pages"])
+        dec = oracle.decode_unit(self.ref, Q[0, :g], budget)
+        return Q, self.buffers(Q, dec["sel_pages"], budget)
+
+    def buffers(self, Q, sel_pages, budget: int = BUDGET):
+        """Decode buffers that are consistent with the union sel_pages: the
+        pages gathered from the pool and the oracle's attention over them."""
+        cfg, g = self.cfg, self.cfg.group
+        max_sel, S, d = g * (budget // cfg.page_size) + cfg.n_pos, cfg.page_size, cfg.head_dim
+        sel_pages = np.asarray(sel_pages, np.int32)
+        kb, vb, bl = oracle.gather(self.ref["pool_k"], self.ref["pool_v"], self.ref["page_len"], sel_pages)
+        out = oracle.attention(Q[0, :g], kb, vb, bl)
+        n = len(sel_pages)
         sel = torch.full((1, max_sel), -1, dtype=torch.int32)
-        sel[0, :n] = torch.from_numpy(dec["sel_pages"])
+        sel[0, :n] = torch.from_numpy(sel_pages)
         kbuf, vbuf = torch.zeros((1, max_sel, S, d)), torch.zeros((1, max_sel, S, d))
-        kbuf[0, :n], vbuf[0, :n] = torch.from_numpy(dec["kbuf"]), torch.from_numpy(dec["vbuf"])
+        kbuf[0, :n], vbuf[0, :n] = torch.from_numpy(kb), torch.from_numpy(vb)
         blen = torch.zeros((1, max_sel), dtype=torch.int32)
-        blen[0, :n] = torch.from_numpy(np.asarray(dec["buf_len"]))
-        O = torch.from_numpy(dec["out"]).float().reshape(1, g, d)
-        buf = types.SimpleNamespace(sel_pages=sel, sel_count=torch.tensor([n], dtype=torch.int32), kbuf=kbuf,
-                                    vbuf=vbuf, buf_len=blen, O=O)
-        return Q, buf
+        blen[0, :n] = torch.from_numpy(np.asarray(bl))
+        O = torch.from_numpy(out).float().reshape(1, g, d)
+        return types.SimpleNamespace(sel_pages=sel, sel_count=torch.tensor([n], dtype=torch.int32), kbuf=kbuf,
+                                     vbuf=vbuf, buf_len=blen, O=O)
 
 
 def test_checks_accept_the_oracles_own_outputs():
@@ -195,3 +208,185 @@ def test_decode_check_with_sink_and_window_pages():
     buf.buf_len[0, n - 1] = 0
     with pytest.raises(AssertionError):
         check_decode_unit(run, 0, Q, BUDGET, buf)
+
+
+# ------------------------------------------------ selection near-tie rules --
+def test_legal_selections_enumerates_only_reorders_of_tied_parents():
+    """Groups 1 and 2 tie within the tolerance at the boundary (k = 3):
+    either may come first, and a group's pages go in id order."""
+    s = [5.0, 3.0, 3.0 + 1e-9, 1.0]
+    items = [[0], [1, 2], [3], [4, 5]]
+    got = legal_selections(s, items, 3, 1e-6)
+    assert got == {frozenset({0, 1, 2}), frozenset({0, 1, 3}), frozenset({0, 3, 1})}
+    assert frozenset({0, 2, 3}) not in got  # the tied parent's second page without its first
+    got = legal_selections(s, items, 2, 1e-6)
+    assert got == {frozenset({0, 1}), frozenset({0, 3})}
+    # outside the tolerance the order is fixed
+    assert legal_selections([5.0, 3.0, 2.9, 1.0], items, 2, 1e-6) == {frozenset({0, 1})}
+    # equal fp32 scores interleave pages by id in the flat order, not in the descent's
+    both = {frozenset({0, 5}), frozenset({3, 8})}
+    assert legal_selections([1.0, 1.0], [[0, 5], [3, 8]], 2, 0.0) == both | {frozenset({0, 3})}
+    assert legal_selections([1.0, 1.0], [[0, 5], [3, 8]], 2, 0.0, interleave=False) == both
+    # fewer items than k: all of them
+    assert legal_selections([1.0, 2.0], [[0], [1]], 5, 1e-6) == {frozenset({0, 1})}
+
+
+def test_check_union_needs_one_legal_selection_per_head():
+    h0 = {frozenset({1, 2}), frozenset({1, 3})}
+    h1 = {frozenset({7, 8})}
+    check_union([1, 2, 7, 8], [h0, h1])
+    check_union([1, 3, 7, 8], [h0, h1])
+    for bad in ([1, 7, 8], [1, 2, 3, 7, 8], [1, 2, 7], [1, 2, 7, 8, 9]):
+        with pytest.raises(AssertionError):
+            check_union(bad, [h0, h1])
+
+
+def _straddle(run, budget):
+    """(head list, union, k-th page a, next page b of the same parent) for a
+    head whose k-th page's parent has a page beyond the budget, or None."""
+    g = run.cfg.group
+    Q = workloads.batch_queries(run.w, 0, 0)
+    q = Q[0, :g].astype(np.float64)
+    head, union = oracle.select(q, run.ref["parent_keys"], run.ref["page_parent"], budget // 16)
+    pages_of = pages_by_parent(run.ref["page_parent"], len(run.ref["parent_tok"]))
+    for hh in range(g):
+        a = int(head[hh][-1])
+        own = pages_of[int(run.ref["page_parent"][a])]
+        later = [p for p in own if p > a and p not in set(union.tolist())]
+        others = set(head[np.arange(g) != hh].reshape(-1).tolist())
+        if later and a not in others:
+            return Q, head[hh], union, a, later[0]
+    return None
+
+
+def _straddle_case():
+    run = _Run()
+    for budget in range(32, 257, 16):
+        c = _straddle(run, budget)
+        if c:
+            return run, budget, c
+    raise AssertionError("no straddling parent in the tiny workload")
+
+
+def test_decode_check_rejects_the_wrong_page_of_a_straddling_parent():
+    """A head's k-th page is the first page of a parent whose next page is
+    not selected; the union with that next page instead (same parent, same
+    score, buffers and attention consistent with it) must fail."""
+    run, budget, (Q, _, union, a, b) = _straddle_case()
+    check_decode_unit(run, 0, Q, budget, run.buffers(Q, union, budget))
+    bad = sorted((set(union.tolist()) - {a}) | {b})
+    with pytest.raises(AssertionError):
+        check_decode_unit(run, 0, Q, budget, run.buffers(Q, bad, budget))
+
+
+def test_decode_check_rejects_one_tied_page_dropped():
+    """The same head's k-th page dropped from the union (its parent's score
+    is the boundary itself): the head would hold k - 1 pages."""
+    run, budget, (Q, _, union, a, _) = _straddle_case()
+    bad = sorted(set(union.tolist()) - {a})
+    with pytest.raises(AssertionError):
+        check_decode_unit(run, 0, Q, budget, run.buffers(Q, bad, budget))
+
+
+def test_decode_check_accepts_a_reorder_of_near_tied_parents():
+    """Parent tokens given equal keys: the k-th page's parent and the next
+    parent in the head's order tie exactly, so a device may take the other
+    parent's first page at the boundary; the helper accepts that union and
+    still rejects a page from an untied parent."""
+    base = _Run()
+    g = base.cfg.group
+    Q = workloads.batch_queries(base.w, 0, 0)
+    q = Q[0, :g].astype(np.float64)
+    for hh in range(g):
+        s = base.ref["parent_keys"] @ q[hh]
+        order = np.argsort(-s, kind="stable")
+        m1, m2 = int(order[0]), int(order[1])
+        K = base.K.copy()
+        K[0, 0, base.ref["parent_tok"][m2]] = K[0, 0, base.ref["parent_tok"][m1]]
+        run = _Run(K=K)
+        head, union = oracle.select(q, run.ref["parent_keys"], run.ref["page_parent"], 1)
+        pages_of = pages_by_parent(run.ref["page_parent"], len(run.ref["parent_tok"]))
+        lo, hi = min(m1, m2), max(m1, m2)
+        if int(head[hh][0]) != pages_of[lo][0] or pages_of[hi][0] in set(union.tolist()):
+            continue
+        others = set(np.delete(head, hh, axis=0).reshape(-1).tolist())
+        if pages_of[lo][0] in others:
+            continue
+        alt = sorted((set(union.tolist()) - {pages_of[lo][0]}) | {pages_of[hi][0]})
+        check_decode_unit(run, 0, Q, 16, run.buffers(Q, alt, 16))
+        far = max(range(int(run.ref["n_pages"])), key=lambda p: -s[run.ref["page_parent"][p]])
+        bad = sorted((set(union.tolist()) - {pages_of[lo][0]}) | {far})
+        with pytest.raises(AssertionError):
+            check_decode_unit(run, 0, Q, 16, run.buffers(Q, bad, 16))
+        return
+    raise AssertionError("no head with a usable tie")
+
+
+# ------------------------------------------------- three levels (descent) --
+def _run3():
+    run = _Run()
+    th = oracle.promote_threshold(run.w.promote_p)
+    lv2 = oracle.build_level2(run.ref, seed=run.w.seed, layer=0, seq=0, head=0, thresh=th)
+    run.ref["level2"] = lv2
+    Np, n2 = len(run.ref["parent_tok"]), len(lv2["node2"])
+    npc = run.cfg.np_cap
+
+    def row(a, cap):
+        out = np.full((1, cap), -1, np.int32)
+        out[0, :len(a)] = a
+        return out
+
+    run.h.update({"n_nodes2": np.array([n2]), "node2": row(lv2["node2"], npc), "parent2": row(lv2["parent2"], npc),
+                  "child_start": row(lv2["child_start"], npc + 1), "children": row(lv2["children"], npc)})
+    return run, lv2
+
+
+def test_descent_checks_accept_the_oracle_and_reject_planted_differences():
+    run, lv2_ref = _run3()
+    K = run.K[0, 0].astype(np.float64)
+    _, M2, e = oracle.lift(K)
+    lv2 = check_level2_unit(run, 0, K, e, M2, lv2_ref)
+    g = run.cfg.group
+    Q = workloads.batch_queries(run.w, 0, 0)
+    dec = oracle.decode_unit(run.ref, Q[0, :g], BUDGET)
+    check_descent_selection(run, 0, Q[0, :g], BUDGET // 16, dec["sel_pages"], lv2)
+    # another page in the union
+    sel = set(dec["sel_pages"].tolist())
+    out = next(p for p in range(int(run.ref["n_pages"])) if p not in sel)
+    with pytest.raises(AssertionError):
+        check_descent_selection(run, 0, Q[0, :g], BUDGET // 16, sorted(sel | {out}), lv2)
+    # a page dropped
+    with pytest.raises(AssertionError):
+        check_descent_selection(run, 0, Q[0, :g], BUDGET // 16, sorted(sel - {min(sel)}), lv2)
+    # a parent moved to the level-2 node farthest from it
+    Np = len(run.ref["parent_tok"])
+    m = next(m for m in range(Np) if m not in set(lv2_ref["node2"].tolist()))
+    pt = run.ref["parent_tok"]
+    d2 = [((K[pt[m]] - K[pt[i]]) ** 2).sum() + (e[pt[m]] - e[pt[i]]) ** 2 for i in lv2_ref["node2"]]
+    run.h["parent2"][0, m] = int(np.argmax(d2))
+    with pytest.raises(AssertionError):
+        check_level2_unit(run, 0, K, e, M2, lv2_ref)
+
+
+def test_positional_build_check_accepts_the_oracle_and_rejects_planted_differences():
+    """check_build_positional (sink and window pages): the oracle's own build
+    passes; a middle token under a far parent, a positional token given a
+    parent, and two tokens swapped between pages each fail."""
+    check_build_positional(_Run(n_sink=16, n_window=40), 0)
+    run = _Run(n_sink=16, n_window=40)
+    K = run.K[0, 0].astype(np.float64)
+    e = run.ref["e"]
+    pt = run.ref["parent_tok"]
+    j = next(t for t in range(16, 700 - 40) if t not in set(pt.tolist()))
+    d2 = ((K[pt] - K[j]) ** 2).sum(1) + (e[pt] - e[j]) ** 2
+    run.h["token_parent"][0, j] = int(np.argmax(d2))
+    with pytest.raises(AssertionError):
+        check_build_positional(run, 0)
+    run = _Run(n_sink=16, n_window=40)
+    run.h["token_parent"][0, 3] = 0
+    with pytest.raises(AssertionError):
+        check_build_positional(run, 0)
+    run = _Run(n_sink=16, n_window=40)
+    _swap_tokens(run)
+    with pytest.raises(AssertionError):
+        check_build_positional(run, 0)
