@@ -168,6 +168,41 @@ ice_status ice_check(int32_t *err_dev, void *stream);
  * integer). */
 int32_t ice_page_bound(int32_t n_tokens, int32_t n_parents, int32_t page_size);
 
+/*
+ * Capacities.  Fills p->np_cap and p->page_cap (and p->n_cap, raised to
+ * max(n_tokens, 1) when smaller) from n_cap, promote_thresh, n_sink and
+ * n_window; the other fields are left as they are.
+ *   np_cap   = min(n_cap, floor(mu + 8 sqrt(mu (1 - q) + 1) + 16)), at least
+ *              1, where q = promote_thresh / 2^32 and mu = n_cap q: the
+ *              promoted count is Binomial(n_cap, q), so the 8-sigma margin
+ *              is exceeded with negligible probability, and a build that
+ *              exceeds it reports ICE_ERR_CAPACITY without writing past it.
+ *              np_cap = n_cap is the bound that always holds.
+ *   page_cap = ice_page_bound(n_cap, np_cap, S) + the positional pages.
+ * ICE_ERR_INVALID_ARG / ICE_ERR_UNSUPPORTED on a bad n_tokens, page_size,
+ * promote_thresh, n_sink or n_window.
+ */
+ice_status ice_default_capacities(ice_params *p);
+
+/*
+ * Sizing of an index.  Every array of an ice_index for the shapes and
+ * capacities in *p (sizes as listed above ice_index) fits in one slab of
+ * *bytes bytes, each array starting on a 256-byte boundary, in ice_index
+ * field order.  with_pool = 0 leaves the pool out (a host page pool holds
+ * it; see ice_host_pool_create).  The level-2 arrays are counted only when
+ * n_levels = 3.
+ */
+ice_status ice_index_bytes(const ice_params *p, int32_t with_pool, size_t *bytes);
+/*
+ * Fills *out with pointers into the caller's slab `base` (device memory of
+ * ice_index_bytes bytes, 256-byte aligned) at the offsets ice_index_bytes
+ * counts.  Nothing is read or written at base: the caller zero-fills the
+ * slab if it wants defined contents before the first build.  Pool and
+ * level-2 pointers that are not counted are set to NULL.  The caller owns
+ * the slab; the library keeps no pointer.
+ */
+ice_status ice_index_layout(const ice_params *p, int32_t with_pool, void *base, ice_index *out);
+
 /* ------------------------------------------------------ index build ----- */
 /* Workspace bytes needed by ice_build_index and its three stages. */
 ice_status ice_build_workspace_bytes(const ice_params *p, size_t *bytes);
@@ -353,6 +388,9 @@ ice_status ice_gather_pages(const ice_params *p, const ice_index *idx, const int
  * a log-sum-exp merge; fp32 throughout.  O [B, Hq, d] float; a unit with no
  * selected page gives O = 0.
  */
+/* A bounded wait of the attention kernel that gives up (ICE_ERR_TIMEOUT in
+ * ice_decode_step's err_dev) leaves NaN in O of the query heads of that unit
+ * here, since this call has no error word. */
 ice_status ice_sparse_attn_decode(const ice_params *p, const void *Q, const void *kbuf, const void *vbuf,
                                   const int32_t *buf_len, const int32_t *sel_count, int32_t max_sel,
                                   float scale, float *O, void *ws, size_t ws_bytes, void *stream);
@@ -371,11 +409,19 @@ ice_status ice_sparse_attn_decode(const ice_params *p, const void *Q, const void
  *    ice_sparse_attn_decode.  The caller still owns Q, kbuf, vbuf, buf_len,
  *    sel_count and O.
  *  - A shape whose scratch exceeds ICE_NOALLOC_SCRATCH_BYTES is rejected
- *    with ICE_ERR_CAPACITY before anything is launched (about
- *    U * ceil(max_sel / 4) * g * 520 bytes are needed).
+ *    with ICE_ERR_CAPACITY before anything is launched.  The scratch is
+ *    r(4 U) + r(8 U n g) + r(512 U n g) bytes with U = B * Hkv units,
+ *    g = Hq / Hkv, n = ceil(max_sel / 4) splits and r(x) = x rounded up to
+ *    a multiple of 256: about U * n * g * 520 bytes (8 MiB holds, for
+ *    instance, 256 units with g = 1 and max_sel = 24, or 128 units with
+ *    g = 8 and max_sel = 32).
+ *  - A bounded wait that gives up leaves NaN in O for that unit's query
+ *    heads (there is no error word).
  *  - The first call on a device looks up the array's device address with
  *    that device current (cudaGetSymbolAddress) and caches it; make that
- *    first call before any stream capture.
+ *    first call before any stream capture.  The cached address belongs to
+ *    the device's primary context: after cudaDeviceReset (or any reset of
+ *    that context) the library must not be called again in the process.
  *  - It calls no cudaMalloc, cudaFree or allocating library routine.
  *  - Every call on a device shares the one array, which keeps the last
  *    call's contents; the ticket words are cleared on the stream at the start

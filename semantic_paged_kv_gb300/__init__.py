@@ -72,6 +72,9 @@ def load() -> ctypes.CDLL:
         "ice_version": ([], ctypes.c_char_p),
         "ice_check": ([P, P], i32),
         "ice_page_bound": ([i32, i32, i32], i32),
+        "ice_default_capacities": ([pp], i32),
+        "ice_index_bytes": ([pp, i32, ctypes.POINTER(sz)], i32),
+        "ice_index_layout": ([pp, i32, P, pi], i32),
         "ice_positional_pages": ([i32, i32, i32, i32], i32),
         "ice_build_workspace_bytes": ([pp, ctypes.POINTER(sz)], i32),
         "ice_build_index": ([pp, P, P, pi, P, sz, P, P], i32),
@@ -104,6 +107,7 @@ def load() -> ctypes.CDLL:
 
 def exported_symbols() -> list[str]:
     return ["ice_status_string", "ice_last_error", "ice_version", "ice_check", "ice_page_bound", "ice_positional_pages",
+            "ice_default_capacities", "ice_index_bytes", "ice_index_layout",
             "ice_build_workspace_bytes", "ice_build_index", "ice_build_lift_promote", "ice_build_assign",
             "ice_build_assign_simt", "ice_build_pack", "ice_build_index_reuse", "ice_decode_workspace_bytes",
             "ice_select_pages",
@@ -160,14 +164,15 @@ class Config:
     n_window: int = 0  # last tokens of the build kept as positional pages (not indexed)
 
     def __post_init__(self):
-        N, p = self.n_tokens, self.promote_p
         if self.n_cap is None:
-            self.n_cap = max(N, 1)
+            self.n_cap = max(self.n_tokens, 1)
         if self.np_cap is None:
-            # expected promoted count plus 8 standard deviations (a device-side
-            # capacity error reports the rare case that needs more)
-            mu = self.n_cap * p
-            self.np_cap = max(1, min(self.n_cap, int(mu + 8 * math.sqrt(mu * (1 - p) + 1) + 16)))
+            # the library's default capacities (ice_default_capacities)
+            d = self._params(np_cap=0, page_cap=0)
+            _check(load().ice_default_capacities(ctypes.byref(d)))
+            self.np_cap = d.np_cap
+            if self.page_cap is None:
+                self.page_cap = d.page_cap
         if self.page_cap is None:
             self.page_cap = max(1, ice_page_bound(self.n_cap, self.np_cap, self.page_size) + self.n_pos)
 
@@ -189,42 +194,57 @@ class Config:
         return torch.bfloat16 if self.dtype == ICE_BF16 else torch.float32
 
     def params(self) -> IceParams:
+        return self._params()
+
+    def _params(self, **over) -> IceParams:
+        f = {**dict(np_cap=self.np_cap, page_cap=self.page_cap, n_cap=self.n_cap), **over}
         return IceParams(self.batch, self.n_q_heads, self.n_kv_heads, self.head_dim, self.n_tokens, self.page_size,
                          self.dtype, self.n_levels, promote_threshold(self.promote_p), self.seed, self.layer,
-                         self.np_cap, self.page_cap, self.n_cap, self.n_sink, self.n_window)
+                         f["np_cap"], f["page_cap"], f["n_cap"], self.n_sink, self.n_window)
 
 
 class Index:
-    """Device arrays of one layer's index, allocated with torch (caller-owned
-    memory in the C ABI's terms)."""
+    """Device arrays of one layer's index in one slab of device memory
+    allocated with torch (caller-owned memory in the C ABI's terms), sized
+    by ice_index_bytes and carved by ice_index_layout; each array is a torch
+    view into the slab.  With a host pool the pool arrays are the pool's
+    device-mapped pointers instead."""
 
     def __init__(self, cfg: Config, device="cuda", host_pool=None):
         U, Np, Pc, Nc, S, d = cfg.units, cfg.np_cap, cfg.page_cap, cfg.n_cap, cfg.page_size, cfg.head_dim
         i32, dt = torch.int32, cfg.torch_dtype
-        z = lambda shape, t: torch.zeros(shape, dtype=t, device=device)
+        shapes = {"n_parents": (i32, (U,)), "n_pages": (i32, (U,)), "n_indexed": (i32, (U,)),
+                  "m2": (torch.float64, (U,)), "parent_tok": (i32, (U, Np)), "parent_keys": (dt, (U, Np, d)),
+                  "parent_e": (torch.float32, (U, Np)), "parent_corr": (torch.float32, (U, Np)),
+                  "parent_first_page": (i32, (U, Np)), "parent_last_page": (i32, (U, Np)),
+                  "parent_n_pages": (i32, (U, Np)), "page_parent": (i32, (U, Pc)), "page_len": (i32, (U, Pc)),
+                  "page_next": (i32, (U, Pc)), "page_tokens": (i32, (U, Pc, S)), "token_parent": (i32, (U, Nc)),
+                  "token_page": (i32, (U, Nc)), "token_slot": (i32, (U, Nc)), "pool_k": (dt, (U, Pc, S, d)),
+                  "pool_v": (dt, (U, Pc, S, d)), "n_nodes2": (i32, (U,)), "node2": (i32, (U, Np)),
+                  "parent2": (i32, (U, Np)), "child_start": (i32, (U, Np + 1)), "children": (i32, (U, Np))}
         self.cfg = cfg
-        self.n_parents, self.n_pages, self.n_indexed = z(U, i32), z(U, i32), z(U, i32)
-        self.m2 = z(U, torch.float64)
-        self.parent_tok = z((U, Np), i32)
-        self.parent_keys = z((U, Np, d), dt)
-        self.parent_e = z((U, Np), torch.float32)
-        self.parent_corr = z((U, Np), torch.float32)
-        self.parent_first_page, self.parent_last_page, self.parent_n_pages = z((U, Np), i32), z((U, Np), i32), z((U, Np), i32)
-        self.page_parent, self.page_len, self.page_next = z((U, Pc), i32), z((U, Pc), i32), z((U, Pc), i32)
-        self.page_tokens = z((U, Pc, S), i32)
-        self.token_parent, self.token_page, self.token_slot = z((U, Nc), i32), z((U, Nc), i32), z((U, Nc), i32)
-        # level 2 (used when cfg.n_levels == 3)
-        self.n_nodes2, self.node2, self.parent2 = z(U, i32), z((U, Np), i32), z((U, Np), i32)
-        self.child_start, self.children = z((U, Np + 1), i32), z((U, Np), i32)
+        params = cfg.params()
+        with_pool = host_pool is None
+        n = ctypes.c_size_t(0)
+        _check(load().ice_index_bytes(ctypes.byref(params), int(with_pool), ctypes.byref(n)))
+        self.slab = torch.zeros(n.value, dtype=torch.uint8, device=device)
+        st = IceIndex()
+        _check(load().ice_index_layout(ctypes.byref(params), int(with_pool), self.slab.data_ptr(), ctypes.byref(st)))
+        base = self.slab.data_ptr()
+        for f in INDEX_FIELDS:
+            ptr = getattr(st, f)
+            if ptr is None:
+                setattr(self, f, None)
+                continue
+            t, shape = shapes[f]
+            off = ptr - base
+            nb = math.prod(shape) * torch.empty((), dtype=t).element_size()
+            assert 0 <= off and off + nb <= n.value
+            setattr(self, f, self.slab[off:off + nb].view(t).view(shape))
         if host_pool is not None:  # pages live in the pinned host pool (device-mapped pointers)
             self.host_pool = host_pool
-            self.pool_k = self.pool_v = None
-            ptrs = {"pool_k": host_pool.k_dev, "pool_v": host_pool.v_dev}
-        else:
-            self.pool_k = torch.zeros((U, Pc, S, d), dtype=dt, device=device)
-            self.pool_v = torch.zeros((U, Pc, S, d), dtype=dt, device=device)
-            ptrs = {}
-        self._struct = IceIndex(*[ptrs[f] if f in ptrs else getattr(self, f).data_ptr() for f in INDEX_FIELDS])
+            st.pool_k, st.pool_v = host_pool.k_dev, host_pool.v_dev
+        self._struct = st
 
     @property
     def struct(self) -> IceIndex:

@@ -2,6 +2,7 @@
 // launch sequence of every entry point declared in ice.h.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <string>
@@ -145,12 +146,16 @@ DecodeWs decode_ws_layout(const ice_params &p, int budget_tokens, int max_sel, v
         off += align256(bytes);
         return r;
     };
-    w.sel_ticket = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * U));
+    // the attention alone (with_select false) needs only its ticket and partials
+    w.sel_ticket = with_select ? reinterpret_cast<int32_t *>(take(sizeof(int32_t) * U)) : nullptr;
     w.attn_ticket = reinterpret_cast<int32_t *>(take(sizeof(int32_t) * U));
-    // (also the per-head page lists [U, g, 32] int32 of the three-level descent)
-    const size_t ck = sizeof(unsigned long long) * U * w.n_chunks * g * (kc ? kc : 1);
-    w.cand_key = reinterpret_cast<unsigned long long *>(take(ck > sizeof(int32_t) * U * g * 32 ? ck : sizeof(int32_t) * U * g * 32));
-    w.cand_span = reinterpret_cast<int4 *>(take(sizeof(int4) * U * w.n_chunks * kSelChunk));
+    if (with_select) {
+        // (also the per-head page lists [U, g, 32] int32 of the three-level descent)
+        const size_t ck = sizeof(unsigned long long) * U * w.n_chunks * g * (kc ? kc : 1);
+        w.cand_key = reinterpret_cast<unsigned long long *>(
+            take(ck > sizeof(int32_t) * U * g * 32 ? ck : sizeof(int32_t) * U * g * 32));
+        w.cand_span = reinterpret_cast<int4 *>(take(sizeof(int4) * U * w.n_chunks * kSelChunk));
+    }
     w.part_ml = reinterpret_cast<float *>(take(sizeof(float) * U * w.n_splits * g * 2));
     w.part_o = reinterpret_cast<float *>(take(sizeof(float) * U * w.n_splits * g * kHeadDim));
     w.scores = with_select ? reinterpret_cast<float *>(take(sizeof(float) * U * select_tc_scores(p))) : nullptr;
@@ -213,6 +218,88 @@ int32_t ice_page_bound(int32_t n_tokens, int32_t n_parents, int32_t page_size) {
     // the page count is an integer, so the floor of the bound holds too
     const long long b = ((long long)n_tokens + (long long)(page_size - 1) * n_parents) / page_size;
     return b > 0x7fffffffll ? 0x7fffffff : (int32_t)b;
+}
+
+ice_status ice_default_capacities(ice_params *p) {
+    if (!p) return fail(ICE_ERR_INVALID_ARG, "params is NULL");
+    if (p->n_tokens < 0) return fail(ICE_ERR_INVALID_ARG, "n_tokens must be >= 0");
+    if (p->page_size != kPage) return fail(ICE_ERR_UNSUPPORTED, "page_size must be %d", kPage);
+    if (p->promote_thresh > (1ull << 32)) return fail(ICE_ERR_INVALID_ARG, "promote_thresh must be <= 2^32");
+    if (p->n_sink < 0 || p->n_window < 0) return fail(ICE_ERR_INVALID_ARG, "n_sink and n_window must be >= 0");
+    if (p->n_cap < p->n_tokens) p->n_cap = p->n_tokens > 1 ? p->n_tokens : 1;
+    if (p->n_cap < 1) p->n_cap = 1;
+    // promoted parents ~ Binomial(n_cap, q): the mean plus 8 standard deviations plus 16
+    const double q = (double)p->promote_thresh / 4294967296.0;
+    const double mu = (double)p->n_cap * q;
+    const double np = floor(mu + 8.0 * sqrt(mu * (1.0 - q) + 1.0) + 16.0);
+    p->np_cap = np >= (double)p->n_cap ? p->n_cap : (np < 1.0 ? 1 : (int32_t)np);
+    const int32_t bound = ice_page_bound(p->n_cap, p->np_cap, kPage);
+    const long long pc = (long long)bound + pos_split(*p).n_pos;
+    if (bound < 0 || pc > 0x7fffffffll) return fail(ICE_ERR_INVALID_ARG, "page capacity overflows int32");
+    p->page_cap = pc > 0 ? (int32_t)pc : 1;
+    return ICE_OK;
+}
+
+// One slab holding every array of an index: offsets from the slab's start
+// in ice_index field order, each array 256-byte aligned.
+static size_t index_layout(const ice_params &p, bool with_pool, char *base, ice_index *out) {
+    const size_t U = (size_t)units_of(p), Np = (size_t)p.np_cap, Pc = (size_t)p.page_cap, Nc = (size_t)p.n_cap;
+    const size_t S = kPage, d = kHeadDim, esz = p.dtype == ICE_BF16 ? 2 : 4;
+    size_t off = 0;
+    auto take = [&](size_t bytes) -> void * {
+        void *r = base ? base + off : nullptr;
+        off += align256(bytes);
+        return r;
+    };
+    ice_index x{};
+    x.n_parents = (int32_t *)take(4 * U);
+    x.n_pages = (int32_t *)take(4 * U);
+    x.n_indexed = (int32_t *)take(4 * U);
+    x.m2 = (double *)take(8 * U);
+    x.parent_tok = (int32_t *)take(4 * U * Np);
+    x.parent_keys = take(esz * U * Np * d);
+    x.parent_e = (float *)take(4 * U * Np);
+    x.parent_corr = (float *)take(4 * U * Np);
+    x.parent_first_page = (int32_t *)take(4 * U * Np);
+    x.parent_last_page = (int32_t *)take(4 * U * Np);
+    x.parent_n_pages = (int32_t *)take(4 * U * Np);
+    x.page_parent = (int32_t *)take(4 * U * Pc);
+    x.page_len = (int32_t *)take(4 * U * Pc);
+    x.page_next = (int32_t *)take(4 * U * Pc);
+    x.page_tokens = (int32_t *)take(4 * U * Pc * S);
+    x.token_parent = (int32_t *)take(4 * U * Nc);
+    x.token_page = (int32_t *)take(4 * U * Nc);
+    x.token_slot = (int32_t *)take(4 * U * Nc);
+    if (with_pool) {
+        x.pool_k = take(esz * U * Pc * S * d);
+        x.pool_v = take(esz * U * Pc * S * d);
+    }
+    if (p.n_levels == 3) {
+        x.n_nodes2 = (int32_t *)take(4 * U);
+        x.node2 = (int32_t *)take(4 * U * Np);
+        x.parent2 = (int32_t *)take(4 * U * Np);
+        x.child_start = (int32_t *)take(4 * U * (Np + 1));
+        x.children = (int32_t *)take(4 * U * Np);
+    }
+    if (out) *out = x;
+    return off;
+}
+
+ice_status ice_index_bytes(const ice_params *p, int32_t with_pool, size_t *bytes) {
+    ice_status st = check_params(p);
+    if (st) return st;
+    if (!bytes) return fail(ICE_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = index_layout(*p, with_pool != 0, nullptr, nullptr);
+    return ICE_OK;
+}
+
+ice_status ice_index_layout(const ice_params *p, int32_t with_pool, void *base, ice_index *out) {
+    ice_status st = check_params(p);
+    if (st) return st;
+    if (!base || !out) return fail(ICE_ERR_INVALID_ARG, "base and out must be non-NULL");
+    if (((uintptr_t)base & 255u) != 0) return fail(ICE_ERR_INVALID_ARG, "base must be 256-byte aligned");
+    index_layout(*p, with_pool != 0, static_cast<char *>(base), out);
+    return ICE_OK;
 }
 
 ice_status ice_check(int32_t *err_dev, void *stream) {

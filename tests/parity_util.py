@@ -39,6 +39,13 @@ def to_dev(x: np.ndarray, dtype) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(x)).to(device="cuda").to(dtype)
 
 
+def host_tables(idx) -> dict:
+    """Host copies of every index array but the pool (parent keys as fp32);
+    arrays the index does not have (level 2 with two levels) are left out."""
+    return {f: getattr(idx, f).float().cpu().numpy() if f == "parent_keys" else getattr(idx, f).cpu().numpy()
+            for f in ice.INDEX_FIELDS if f not in ("pool_k", "pool_v") and getattr(idx, f) is not None}
+
+
 class DeviceRun:
     """One layer built and decoded on the GPU, with host copies of everything."""
 
@@ -61,8 +68,7 @@ class DeviceRun:
                 self.params, self.Kd, self.idx, self.ws, self.err)
             ice.ice_build_pack(self.params, self.Kd, self.Vd, self.idx, self.ws, self.err)
         self.status = ice.ice_check(self.err)
-        self.h = {f: getattr(self.idx, f).float().cpu().numpy() if f == "parent_keys" else getattr(self.idx, f).cpu().numpy()
-                  for f in ice.INDEX_FIELDS if f not in ("pool_k", "pool_v")}
+        self.h = host_tables(self.idx)
 
     def pool(self, u):
         P = int(self.h["n_pages"][u])
@@ -143,7 +149,8 @@ class DeviceDrawnRun(DeviceRun):
         self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
         ice.ice_build_index(self.params, self.Kd, self.Vd, self.idx, self.ws, self.err)
         self.status = ice.ice_check(self.err)
-        self.h = {f: _UnitRows(getattr(self.idx, f)) for f in ice.INDEX_FIELDS if f not in ("pool_k", "pool_v")}
+        self.h = {f: _UnitRows(getattr(self.idx, f)) for f in ice.INDEX_FIELDS
+                  if f not in ("pool_k", "pool_v") and getattr(self.idx, f) is not None}
 
     def queries(self, step: int = 0):
         assert step == 0

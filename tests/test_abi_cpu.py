@@ -110,3 +110,68 @@ def test_config_capacities_cover_positional_pages_and_descent_lists(lib):
     # descent: at most 32 pages per head; more is refused before anything runs
     assert ice.ice_build_workspace_bytes(three.params()) > ice.ice_build_workspace_bytes(
         ice.Config(batch=2, n_q_heads=8, n_kv_heads=2, n_tokens=1000).params())
+
+
+@pytest.mark.parametrize("n,p,n_sink,n_window", [(16384, 1 / 16, 0, 0), (100000, 1 / 16, 0, 0), (5003, 0.95, 0, 0),
+                                                 (700, 1.0, 0, 0), (1000, 0.0, 40, 70), (0, 1 / 16, 0, 0)])
+def test_default_capacities(lib, n, p, n_sink, n_window):
+    """ice_default_capacities: np_cap = the binomial mean of promoted tokens
+    plus 8 standard deviations plus 16 (at most n_cap, at least 1); page_cap
+    = ice_page_bound(n_cap, np_cap) + the positional pages."""
+    import math
+    prm = ice.Config(batch=1, n_q_heads=4, n_kv_heads=1, n_tokens=n, promote_p=p, n_sink=n_sink,
+                     n_window=n_window, np_cap=1, page_cap=1).params()
+    prm.np_cap = prm.page_cap = 0
+    assert lib.ice_default_capacities(ctypes.byref(prm)) == 0
+    nc = max(n, 1)
+    q = ice.promote_threshold(p) / 2 ** 32
+    mu = nc * q
+    assert prm.n_cap == nc
+    assert prm.np_cap == max(1, min(nc, math.floor(mu + 8 * math.sqrt(mu * (1 - q) + 1) + 16)))
+    assert prm.page_cap == max(1, ice.ice_page_bound(nc, prm.np_cap) + lib.ice_positional_pages(n, n_sink, n_window, 16))
+    cfg = ice.Config(batch=1, n_q_heads=4, n_kv_heads=1, n_tokens=n, promote_p=p, n_sink=n_sink, n_window=n_window)
+    assert (cfg.np_cap, cfg.page_cap) == (prm.np_cap, prm.page_cap)
+    bad = ice.Config(batch=1, n_q_heads=4, n_kv_heads=1, n_tokens=100).params()
+    bad.page_size = 8
+    assert lib.ice_default_capacities(ctypes.byref(bad)) == ice.ICE_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("levels,with_pool,dtype", [(2, 1, ice.ICE_BF16), (3, 1, ice.ICE_FP32), (2, 0, ice.ICE_BF16)])
+def test_index_slab_layout(lib, levels, with_pool, dtype):
+    """ice_index_bytes / ice_index_layout: every array of the index at a
+    256-byte aligned offset of one slab, in field order, disjoint, each as
+    large as its documented shape; the pool and the level-2 arrays only when
+    counted.  Nothing is read or written at the (fake) base address."""
+    cfg = ice.Config(batch=3, n_q_heads=8, n_kv_heads=2, n_tokens=1000, n_levels=levels, dtype=dtype)
+    prm = cfg.params()
+    n = ctypes.c_size_t(0)
+    assert lib.ice_index_bytes(ctypes.byref(prm), with_pool, ctypes.byref(n)) == 0
+    base = 1 << 40
+    st = ice.IceIndex()
+    assert lib.ice_index_layout(ctypes.byref(prm), with_pool, base, ctypes.byref(st)) == 0
+    U, Np, Pc, Nc, S, d = cfg.units, cfg.np_cap, cfg.page_cap, cfg.n_cap, 16, 128
+    esz = 2 if dtype == ice.ICE_BF16 else 4
+    size = {"n_parents": 4 * U, "n_pages": 4 * U, "n_indexed": 4 * U, "m2": 8 * U, "parent_tok": 4 * U * Np,
+            "parent_keys": esz * U * Np * d, "parent_e": 4 * U * Np, "parent_corr": 4 * U * Np,
+            "parent_first_page": 4 * U * Np, "parent_last_page": 4 * U * Np, "parent_n_pages": 4 * U * Np,
+            "page_parent": 4 * U * Pc, "page_len": 4 * U * Pc, "page_next": 4 * U * Pc,
+            "page_tokens": 4 * U * Pc * S, "token_parent": 4 * U * Nc, "token_page": 4 * U * Nc,
+            "token_slot": 4 * U * Nc, "pool_k": esz * U * Pc * S * d, "pool_v": esz * U * Pc * S * d,
+            "n_nodes2": 4 * U, "node2": 4 * U * Np, "parent2": 4 * U * Np, "child_start": 4 * U * (Np + 1),
+            "children": 4 * U * Np}
+    end = 0
+    for f in ice.INDEX_FIELDS:
+        ptr = getattr(st, f)
+        counted = (with_pool or f not in ("pool_k", "pool_v")) and (levels == 3 or f not in
+                                                                      ("n_nodes2", "node2", "parent2",
+                                                                       "child_start", "children"))
+        if not counted:
+            assert ptr is None, f
+            continue
+        off = ptr - base
+        assert off % 256 == 0 and off >= end, f
+        end = off + size[f]
+    assert end <= n.value < end + 256
+    # refusals: unaligned or missing base
+    assert lib.ice_index_layout(ctypes.byref(prm), with_pool, base + 16, ctypes.byref(st)) == ice.ICE_ERR_INVALID_ARG
+    assert lib.ice_index_layout(ctypes.byref(prm), with_pool, None, ctypes.byref(st)) == ice.ICE_ERR_INVALID_ARG

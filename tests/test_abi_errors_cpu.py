@@ -138,3 +138,18 @@ def test_well_formed_host_checks_pass_up_to_the_device():
                  lambda: _gather()):
         st = call()
         assert st == ice.ICE_ERR_CUDA, (st, ice.load().ice_last_error().decode())
+
+
+@pytest.mark.parametrize("batch,n_q,n_kv,budget", [(8, 32, 32, 256), (8, 32, 32, 64), (16, 64, 8, 64)])
+def test_noalloc_accepts_documented_shapes(batch, n_q, n_kv, budget):
+    """The allocation-free attention's capacity check passes the LongChat-7B
+    shape at batch 8 (256 units, g = 1) and the Qwen3-32B shape at batch 16
+    with budget 64 (its scratch holds only the attention's ticket words and
+    partials); without a device the call then fails on its first CUDA call,
+    not on capacity."""
+    cfg = ice.Config(batch=batch, n_q_heads=n_q, n_kv_heads=n_kv, n_tokens=100000)
+    p = cfg.params()
+    max_sel = ice.max_selected(cfg, budget)
+    st = ice.load().ice_sparse_attn_decode_noalloc(ctypes.byref(p), Q, KB, VB, BL, CNT, max_sel, 0.088, O, None)
+    assert st != ice.ICE_ERR_CAPACITY, ice.load().ice_last_error().decode()
+    assert st == ice.ICE_ERR_CUDA

@@ -11,7 +11,7 @@ import torch
 import oracle
 import semantic_paged_kv_gb300 as ice
 import workloads
-from parity_util import DeviceRun, TIE_REL, check_build_unit, check_decode_unit, to_dev
+from parity_util import DeviceRun, TIE_REL, check_build_unit, check_decode_unit, host_tables, to_dev
 
 pytestmark = pytest.mark.gpu
 W = workloads.WORKLOADS
@@ -114,8 +114,7 @@ def test_insert_stream_mistral_shaped():
     w = W["mistral_7b_36k"].scaled(n_tokens=5000, n_q_heads=8, n_kv_heads=2, centres=256)
     run = _run_inserts(w, 48)
     # decode after the inserts sees the updated index
-    run.h = {f: getattr(run.idx, f).float().cpu().numpy() if f == "parent_keys" else getattr(run.idx, f).cpu().numpy()
-             for f in ice.INDEX_FIELDS if f not in ("pool_k", "pool_v")}
+    run.h = host_tables(run.idx)
     Q, buf, st = run.decode(256)
     assert st == ice.ICE_OK
     for u in range(run.cfg.units):
@@ -131,8 +130,7 @@ def test_insert_stream_mistral_full_size():
     w = W["mistral_7b_36k"]
     run = _run_inserts(w, 128, sample_tokens=1500)
     assert int(run.idx.n_indexed.sum()) == run.cfg.units * (w.n_tokens + 128)
-    run.h = {f: getattr(run.idx, f).float().cpu().numpy() if f == "parent_keys" else getattr(run.idx, f).cpu().numpy()
-             for f in ice.INDEX_FIELDS if f not in ("pool_k", "pool_v")}
+    run.h = host_tables(run.idx)
     Q, buf, st = run.decode(256)
     assert st == ice.ICE_OK
     for u in range(run.cfg.units):

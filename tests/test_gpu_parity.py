@@ -10,7 +10,8 @@ import oracle
 import semantic_paged_kv_gb300 as ice
 import workloads
 from parity_util import (DeviceDrawnRun, DeviceRun, check_build_level2, check_build_positional, check_build_unit,
-                         check_decode_descent, check_decode_unit, check_level2_unit, check_pack_unit, to_dev)
+                         check_decode_descent, check_decode_unit, check_level2_unit, check_pack_unit, host_tables,
+                         to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -332,8 +333,7 @@ def _reused_run(run0: DeviceRun, layer: int = 1, in_place: bool = False) -> Devi
     r.err = torch.zeros(1, dtype=torch.int32, device="cuda")
     ice.ice_build_index_reuse(r.params, r.Kd, r.Vd, run0.idx, r.idx, r.ws, r.err)
     r.status = ice.ice_check(r.err)
-    r.h = {f: getattr(r.idx, f).float().cpu().numpy() if f == "parent_keys" else getattr(r.idx, f).cpu().numpy()
-           for f in ice.INDEX_FIELDS if f not in ("pool_k", "pool_v")}
+    r.h = host_tables(r.idx)
     return r
 
 
