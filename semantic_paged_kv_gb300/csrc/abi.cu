@@ -5,6 +5,8 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
+#include <cstring>
 #include <string>
 
 #include "common.cuh"
@@ -34,6 +36,24 @@ ice_status cuda_status(cudaError_t e, const char *where) {
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+bool fault_armed(const char *what) {
+    const char *v = getenv("ICE_FAULT");
+    if (!v || !*v) return false;
+    const size_t n = strlen(what);
+    for (const char *c = v; *c;) {
+        const char *e = strchr(c, ',');
+        const size_t len = e ? (size_t)(e - c) : strlen(c);
+        if (len == n && strncmp(c, what, n) == 0) return true;
+        if (!e) break;
+        c = e + 1;
+    }
+    return false;
+}
+
+namespace {
 
 ice_status check_params(const ice_params *p) {
     if (!p) return fail(ICE_ERR_INVALID_ARG, "params is NULL");

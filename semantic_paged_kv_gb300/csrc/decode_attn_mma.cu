@@ -57,6 +57,7 @@ struct SmemM {
     unsigned long long full[kMW][kNS];
     int wsum[kMW];
     int last;
+    int bad;  // a bounded wait of some warp gave up: O is NaN for this unit
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
@@ -99,7 +100,7 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
     int page_cap, const int32_t *__restrict__ sel_pages, int32_t *__restrict__ buf_len,
     const int32_t *__restrict__ sel_count, int max_sel, float scale, int n_splits, float *__restrict__ part_ml,
     float *__restrict__ part_o, int32_t *__restrict__ ticket, float *__restrict__ O, int32_t *__restrict__ err,
-    const SelArgs SA) {
+    unsigned long long wait_ns, int fault_skip, const SelArgs SA) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     // the swizzled page tiles want 1024-byte alignment
     SmemM &S = *reinterpret_cast<SmemM *>(smem_raw + ((1024u - (su32(smem_raw) & 1023u)) & 1023u));
@@ -108,7 +109,10 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int qr = lane >> 2, qc = lane & 3;  // fragment row (query row) and column pair
     if (tid < kNS * kMW) mbar_init(&S.full[tid / kNS][tid % kNS], 1);
-    if (tid == 0) mbar_init_fence();
+    if (tid == 0) {
+        mbar_init_fence();
+        S.bad = 0;
+    }
     if (lane < 16) {
         S.ml[warp][lane][0] = -INFINITY;
         S.ml[warp][lane][1] = 0.f;
@@ -151,6 +155,7 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
         }
     }
     auto issue = [&](int k, int pid) {
+        if (fault_skip) return;  // fault injection: the wait below gives up
         const int x = xs + warp + k * kMW;
         const int row = kFused ? (u * page_cap + pid) * kPage : (int)((ubase + x) * kPage);
         unsigned char *slot = S.kv[warp][k % kNS];
@@ -196,7 +201,7 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
         const int len = __shfl_sync(0xffffffffu, my_len, k);
         const int pid_next = __shfl_sync(0xffffffffu, my_pid, (k + kNS) & 31);
         if (store && lane == 0) buf_len[slot] = len;
-        if (ok) ok = mbar_wait(&S.full[warp][k % kNS], (k / kNS) & 1);
+        if (ok) ok = mbar_wait(&S.full[warp][k % kNS], (k / kNS) & 1, wait_ns);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         unsigned char *sp = S.kv[warp][k % kNS];
@@ -294,7 +299,10 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
         }
         __syncwarp();
     }
-    if (!ok) set_err(err, ICE_ERR_TIMEOUT);
+    if (!ok) {
+        set_err(err, ICE_ERR_TIMEOUT);
+        if (lane == 0) S.bad = 1;
+    }
     if (store && lane == 0) bulk_wait_read_all();  // the slots are reused below
     if (qc == 0) {
         S.ml[warp][qr][0] = m_run[0];
@@ -325,6 +333,7 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
             S.wgt[w][tid] = wt;
             L = fmaf(S.ml[w][tid][1], wt, L);
         }
+        if (S.bad) L = __int_as_float(0x7fc00000);  // NaN: carried into O by the merges
         S.cml[tid][0] = M;
         S.cml[tid][1] = L;
         if (n_splits > 1) {
@@ -341,7 +350,7 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
         for (int w = 0; w < kMW; ++w) acc = fmaf(s_o[((size_t)w * 16 + hh) * kHeadDim + d], S.wgt[w][hh], acc);
         if (n_splits == 1) {
             const float L = S.cml[hh][1];
-            O[((size_t)b * n_q_heads + (size_t)h * g + hh) * kHeadDim + d] = L > 0.f ? acc / L : 0.f;
+            O[((size_t)b * n_q_heads + (size_t)h * g + hh) * kHeadDim + d] = L > 0.f ? acc / L : (L == L ? 0.f : L);
         } else {
             part_o[(((size_t)u * n_splits + split) * g + hh) * kHeadDim + d] = acc;
         }
@@ -376,7 +385,7 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
         for (int sp2 = 0; sp2 < n_splits; ++sp2)
             acc = fmaf(__ldcg(po + ((size_t)sp2 * g + hh) * kHeadDim + d), s_w[sp2 * g + hh], acc);
         const float L = s_w[nsg + hh];
-        O[((size_t)b * n_q_heads + (size_t)h * g + hh) * kHeadDim + d] = L > 0.f ? acc / L : 0.f;
+        O[((size_t)b * n_q_heads + (size_t)h * g + hh) * kHeadDim + d] = L > 0.f ? acc / L : (L == L ? 0.f : L);
     }
     if (tid == 0) ticket[u] = 0;
 }
@@ -423,9 +432,11 @@ cudaError_t launch_hr(const ice_params &p, const ice_index *pool, const int32_t 
     if (e != cudaSuccess) return e;
     const __nv_bfloat16 *Qb = static_cast<const __nv_bfloat16 *>(Q);
     const int32_t *plen = pool ? pool->page_len : nullptr;
+    const bool fault = fault_armed("timeout");
     e = launch_dependent(k_attn_mma<F, HR, kSel>, dim3(n_splits, U), dim3(kMT), need, s, tk, tv, tkb, tvb, Qb, g,
                          p.n_q_heads, p.n_kv_heads, plen, p.page_cap, sel_pages, buf_len, sel_count, max_sel, scale,
-                         n_splits, ws.part_ml, ws.part_o, ws.attn_ticket, O, err, SA);
+                         n_splits, ws.part_ml, ws.part_o, ws.attn_ticket, O, err, fault ? kFaultWaitNs : kWaitNs,
+                         fault ? 1 : 0, SA);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

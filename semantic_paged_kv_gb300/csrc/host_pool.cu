@@ -108,14 +108,14 @@ ice_status ice_host_pool_create(size_t pool_bytes, size_t staging_bytes, int32_t
     hp->pool_bytes = pool_bytes;
     hp->staging_bytes = staging_bytes;
     const unsigned flags = cudaHostAllocMapped | cudaHostAllocPortable;
-    if (cudaHostAlloc(&hp->k_host, pool_bytes, flags) != cudaSuccess ||
+    if (fault_armed("alloc") || cudaHostAlloc(&hp->k_host, pool_bytes, flags) != cudaSuccess ||
         cudaHostAlloc(&hp->v_host, pool_bytes, flags) != cudaSuccess ||
         (staging_bytes && cudaHostAlloc(&hp->staging, staging_bytes, cudaHostAllocPortable) != cudaSuccess)) {
         cudaGetLastError();
         release(hp);
         return ICE_ERR_OOM;
     }
-    if (cudaHostGetDevicePointer(&hp->k_dev, hp->k_host, 0) != cudaSuccess ||
+    if (fault_armed("hostpool") || cudaHostGetDevicePointer(&hp->k_dev, hp->k_host, 0) != cudaSuccess ||
         cudaHostGetDevicePointer(&hp->v_dev, hp->v_host, 0) != cudaSuccess ||
         cudaEventCreateWithFlags(&hp->copied, cudaEventDisableTiming) != cudaSuccess) {
         cudaGetLastError();
@@ -205,7 +205,7 @@ ice_status ice_host_pool_gather_h2d(ice_host_pool *hp, const ice_params *p, cons
     if (bad) return ICE_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // the one bulk transfer of this layer
-    if (cudaMemcpyAsync(dst_dev, hp->staging, need, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+    if (fault_armed("copy") || cudaMemcpyAsync(dst_dev, hp->staging, need, cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaEventRecord(hp->copied, s) != cudaSuccess) {
         cudaGetLastError();
         return ICE_ERR_CUDA;

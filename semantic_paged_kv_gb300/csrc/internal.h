@@ -20,6 +20,18 @@ constexpr int kAttnPagesPerSplit = 4;
 constexpr int kPackSmemBins = 12288;
 
 inline int units_of(const ice_params &p) { return p.batch * p.n_kv_heads; }
+
+// Fault injection for tests, on the host: the environment variable ICE_FAULT
+// holds a comma-separated list of
+//   alloc     ice_host_pool_create fails its first pinned allocation (ICE_ERR_OOM)
+//   hostpool  ice_host_pool_create fails after its allocations, at the device
+//             mapping (ICE_ERR_CUDA; everything allocated is freed)
+//   copy      ice_host_pool_gather_h2d fails its bulk copy (ICE_ERR_CUDA)
+//   timeout   the attention kernel's page producer issues no copy, and its
+//             bounded waits give up after kFaultWaitNs (ICE_ERR_TIMEOUT)
+// Read at every call; unset (the default) nothing changes.
+bool fault_armed(const char *what);
+constexpr unsigned long long kFaultWaitNs = 20000000ull;  // 20 ms
 inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
 // Sink / window split of a build over p.n_tokens tokens: the index covers the

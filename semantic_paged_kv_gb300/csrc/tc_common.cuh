@@ -47,12 +47,13 @@ __device__ __forceinline__ bool mbar_test(unsigned long long *b, uint32_t parity
         : "memory");
     return ok != 0;
 }
-// Bounded wait for the phase of the given parity; false after kWaitNs.
-__device__ __forceinline__ bool mbar_wait(unsigned long long *b, uint32_t parity) {
+// Bounded wait for the phase of the given parity; false after limit_ns.
+__device__ __forceinline__ bool mbar_wait(unsigned long long *b, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitNs) {
     if (mbar_test(b, parity)) return true;
     const unsigned long long t0 = now_ns();
     while (!mbar_test(b, parity))
-        if (now_ns() - t0 > kWaitNs) return false;
+        if (now_ns() - t0 > limit_ns) return false;
     return true;
 }
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, unsigned long long *bar, int x, int y) {

@@ -49,14 +49,18 @@ def host_tables(idx) -> dict:
 class DeviceRun:
     """One layer built and decoded on the GPU, with host copies of everything."""
 
-    def __init__(self, w: workloads.Workload, layer: int = 0, assign: str = "auto", **cfg_kw):
+    def __init__(self, w: workloads.Workload, layer: int = 0, assign: str = "auto", host_pool=None, **cfg_kw):
+        """host_pool: a callable cfg -> ice.HostPool; the pool then lives in
+        pinned host memory (step a12) and the kernels reach it over the
+        CPU-GPU link."""
         self.w = w
         self.cfg = cfg_of(w, layer=layer, **cfg_kw)
         self.layer = layer
         self.K, self.V = workloads.batch_kv(w, layer)
         dt = self.cfg.torch_dtype
         self.Kd, self.Vd = to_dev(self.K, dt), to_dev(self.V, dt)
-        self.idx = ice.Index(self.cfg)
+        self.hp = host_pool(self.cfg) if host_pool else None
+        self.idx = ice.Index(self.cfg, host_pool=self.hp)
         self.params = self.cfg.params()
         self.ws = ice.workspace(ice.ice_build_workspace_bytes(self.params))
         self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -71,7 +75,15 @@ class DeviceRun:
         self.h = host_tables(self.idx)
 
     def pool(self, u):
+        """Host copies (fp32) of unit u's pages, from HBM or the host pool."""
         P = int(self.h["n_pages"][u])
+        hp = getattr(self, "hp", None)
+        if hp is not None:
+            def bits(which):
+                x = hp.host_array(which)[u, :P]
+                return (x.astype(np.uint32) << 16).view(np.float32) if self.cfg.dtype == ice.ICE_BF16 else \
+                    x.view(np.float32).copy()
+            return bits("k"), bits("v")
         return (self.idx.pool_k[u, :P].float().cpu().numpy(), self.idx.pool_v[u, :P].float().cpu().numpy())
 
     def unit(self, u):
@@ -137,13 +149,14 @@ class DeviceDrawnRun(DeviceRun):
     copied to the host: their K, V rows and index rows, on first use; units
     are independent problems, so the oracle needs nothing else."""
 
-    def __init__(self, w: workloads.Workload, layer: int = 0, **cfg_kw):
+    def __init__(self, w: workloads.Workload, layer: int = 0, host_pool=None, **cfg_kw):
         self.w = w
         self.cfg = cfg_of(w, layer=layer, **cfg_kw)
         self.layer = layer
         self.Kd, self.Vd, self.C = workloads.batch_kv_device(w, layer)
         self.K, self.V = _UnitArrays(self.Kd), _UnitArrays(self.Vd)
-        self.idx = ice.Index(self.cfg)
+        self.hp = host_pool(self.cfg) if host_pool else None
+        self.idx = ice.Index(self.cfg, host_pool=self.hp)
         self.params = self.cfg.params()
         self.ws = ice.workspace(ice.ice_build_workspace_bytes(self.params))
         self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -517,9 +530,8 @@ def check_decode_unit(run: DeviceRun, u: int, Q: np.ndarray, budget: int, buf):
                                      what=("unit", u, "head", hh)) for hh in range(g)]
         check_union(got_sem, per_head, what=("unit", u))
     # gather: exact copies of the selected pages
-    gi = torch.as_tensor(got, dtype=torch.long, device=buf.kbuf.device)
-    pk_sel = run.idx.pool_k[u].index_select(0, gi).float().cpu().numpy()
-    pv_sel = run.idx.pool_v[u].index_select(0, gi).float().cpu().numpy()
+    pk_all, pv_all = run.pool(u)
+    pk_sel, pv_sel = pk_all[got], pv_all[got]
     kb = buf.kbuf[u, :cnt].float().cpu().numpy()
     vb = buf.vbuf[u, :cnt].float().cpu().numpy()
     bl = buf.buf_len[u].cpu().numpy()
