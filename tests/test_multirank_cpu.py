@@ -26,7 +26,7 @@ def _worker(rank, world, port, q):
 
     w = bench.rank_workload("llama31_8b_16k", rank)
     slowest = bench.max_over_ranks(10.0 + rank, world, "cpu")
-    rate = bench.whole_job_rate(w.units, w.n_tokens, 3, world, slowest)
+    rate = bench.whole_job_rate(w.units * w.n_tokens, 3, world, slowest)
     K, _ = workloads.unit_kv(w.scaled(n_tokens=64), 0, 0, 0)
     q.put((rank, w.seed, slowest, rate, float(K.astype("float64").sum())))
     dist.barrier()
