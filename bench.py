@@ -93,7 +93,7 @@ EXTRAS = ("build", "longchat", "longchat_b8", "qwen_levels3", "mistral_insert", 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen3_32b_100k")
@@ -281,6 +281,8 @@ def cpu_baseline_sample(w, budget, units=None, min_seconds=10.0, max_seconds=30.
     value = smp.bytes * passes / t / 1e9
     return {"value": value, "unit": "GB/s", "cores": smp.threads, "kind": "oracle", "cpu": host_cpu(),
             "sample": smp.describe(passes, t),
+            "short": f"{units}/{w.units} units, first {smp.n_tokens} tokens each, oracle-built index (untimed); "
+                     f"oracle decode, 1 unit/thread, {passes} passes in {t:.0f} s",
             "build_keys_per_s": units * smp.n_tokens / smp.build_s}
 
 
@@ -313,7 +315,7 @@ def config_of(w, budget, gpus, layers):
             "n_tokens": w.n_tokens, "head_dim": w.head_dim, "page_size": w.page_size, "promote_p": w.promote_p,
             "levels": 2, "budget_tokens": budget, "parallelism": f"dp{gpus}",
             "gather": "selected pages into shared memory (contiguous buffer: extra.buffer)",
-            "l2": f"{layers} layers rotated; each step reads > 2.5x L2"}
+            "l2": f"{layers} layers rotated, each step reads > 2.5x L2"}
 
 
 # ------------------------------------------------- multi-rank host logic ---
@@ -363,9 +365,14 @@ class Replay:
             fn()
         torch.cuda.synchronize()
         self.cap.wait_stream(torch.cuda.current_stream())
-        g = torch.cuda.CUDAGraph()
+        try:
+            g, kept = torch.cuda.CUDAGraph(keep_graph=True), True  # kept for counting its kernel nodes
+        except TypeError:
+            g, kept = torch.cuda.CUDAGraph(), False
         with torch.cuda.graph(g, stream=self.cap):
             fn()
+        if kept:
+            g.instantiate()
         torch.cuda.current_stream().wait_stream(self.cap)
         torch.cuda.synchronize()
         return g
@@ -796,9 +803,60 @@ def run_ours(args):
         if args.detail:
             with open(args.detail, "w") as f:
                 json.dump(line, f, indent=1)
-        print(json.dumps(line, separators=(",", ":")))
+        print(json.dumps(line, indent=1), file=sys.stderr)  # every number, readable
+        print(json.dumps(compact(line), separators=(",", ":")))
     if world > 1:
         dist.destroy_process_group()
+
+
+def compact(d: dict) -> dict:
+    """The contract line with every headline number and short keys (the
+    full record goes to stderr and --detail)."""
+    x = d["extra"]
+    c = d["config"]
+    g = lambda *ks: _get(x, ks)
+    out = {k: d[k] for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                             "higher_is_better", "scaling", "vs_baseline", "dtype")}
+    out["value"] = r3(d["value"])
+    out["data"] = "synthetic"
+    out["config"] = {"workload": c["workload"], "batch_per_gpu": c["batch_per_gpu"],
+                     "heads": f"{c['n_q_heads']}/{c['n_kv_heads']}", "n_tokens": c["n_tokens"],
+                     "budget_tokens": c["budget_tokens"], "levels": 2, "parallelism": c["parallelism"],
+                     "gather": "smem", "l2": c["l2"]}
+    out["decode_step_us"] = r3(d["decode_step_us"])
+    rf = d["roofline"]
+    out["roofline"] = {"kernel": rf["kernel"], "bound": "hbm", "achieved": r3(rf["achieved"]), "peak": rf["peak"],
+                       "unit": "GB/s", "frac": r3(rf["frac"]), "traffic": rf["traffic"]}
+    out["index_build_keys_per_s"] = r3(d["index_build_keys_per_s"])
+    e = d["e2e"] or {}
+    out["e2e"] = {"value": r3(e.get("value")), "unit": "GB/s", "h2d_bytes_per_step": e.get("h2d_bytes_per_step"),
+                  "d2h_bytes_per_step": e.get("d2h_bytes_per_step"), "ms": e.get("ms_per_step"),
+                  "direct": _get(e, ("direct", "value"))}
+    cb = d["cpu_baseline"] or {}
+    out["cpu_baseline"] = {"value": r3(cb.get("value")), "unit": cb.get("unit"), "cores": cb.get("cores"),
+                           "kind": "oracle", "sample": cb.get("short", cb.get("error"))}
+    out["gpu_launches"] = d["gpu_launches"]
+    ck = d["clocks"]
+    out["clocks"] = {"sm_mhz": ck["sm_mhz"], "sm_max_mhz": ck["sm_max_mhz"], "reasons": ck["reasons"]}
+    out["status"] = d["device_status"]
+    out["x"] = {"buf_us": g("buffer", "us"), "buf_frac": g("buffer", "frac_min"),
+                "p10_p90": [g("step", "p10_us"), g("step", "p90_us")], "sel_us": g("step", "select_us"),
+                "build_ms": g("build", "ms"),
+                "lc1": [g("longchat", "d256", "us"), g("longchat", "d256", "frac"), g("longchat", "d64", "us")],
+                "lc_assign_frac": g("longchat", "assign", "frac"),
+                "lc8": [g("longchat_b8", "d256", "us"), g("longchat_b8", "d256", "frac")],
+                "lv3_us": g("qwen_levels3", "us"), "ins_us": g("mistral_insert", "insert_us"),
+                "l16k": [g("llama16k", "build_us"), g("llama16k", "decode_us"), g("llama16k", "assign_frac")],
+                "link": [g("host_pool", "link_peak_gbs"), g("host_pool", "bulk_frac"), g("host_pool", "direct_frac")]}
+    return out
+
+
+def _get(d, keys):
+    for k in keys:
+        if not isinstance(d, dict) or k not in d:
+            return None
+        d = d[k]
+    return d
 
 
 def main():

@@ -34,6 +34,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "attn_page.cuh"
 #include "select_unit.cuh"
 #include "tc_common.cuh"
 
@@ -41,6 +42,7 @@ namespace ice {
 namespace {
 
 using namespace tc;
+using namespace mma;
 
 constexpr int kMW = 8;   // warps per CTA
 constexpr int kNS = 3;   // page slots per warp (pages in flight while one is computed)
@@ -59,38 +61,6 @@ struct SmemM {
     int last;
     int bad;  // a bounded wait of some warp gave up: O is NaN for this unit
 };
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-// D += A B, m16n8k16, bf16 in, fp32 accumulate.
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-// bf16 pair (round to nearest) and the pair of remainders, as packed words.
-__device__ __forceinline__ void split_pair(float x, float y, uint32_t &hi, uint32_t &lo) {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
-    const float2 hf = __bfloat1622float2(h);
-    const __nv_bfloat162 l = __floats2bfloat162_rn(x - hf.x, y - hf.y);
-    hi = *reinterpret_cast<const uint32_t *>(&h);
-    lo = *reinterpret_cast<const uint32_t *>(&l);
-}
-// Shared-memory address of 16-byte chunk `cc` (0..15 across the two 64-column
-// halves) of row `row` in a 128-byte-swizzled 16-row tile.
-__device__ __forceinline__ uint32_t sw_addr(uint32_t tile, int row, int cc) {
-    return tile + (uint32_t)((cc >> 3) * kHalfBytes + row * 128 + (((cc & 7) ^ (row & 7)) << 4));
-}
 
 template <bool kFused, int HR, bool kSel>
 __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
@@ -179,21 +149,9 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
 
     // A fragments of Q (rows = query rows of the group), 8 steps of 16 dims
     uint32_t qa[8][4];
-    {
-        const __nv_bfloat16 *Qu = Q + ((size_t)b * n_q_heads + (size_t)h * g) * kHeadDim;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            const int c0 = ks * 16 + 2 * qc;
-            qa[ks][0] = qr < g ? *reinterpret_cast<const uint32_t *>(Qu + (size_t)qr * kHeadDim + c0) : 0u;
-            qa[ks][1] = (HR > 1 && qr + 8 < g) ? *reinterpret_cast<const uint32_t *>(Qu + (size_t)(qr + 8) * kHeadDim + c0) : 0u;
-            qa[ks][2] = qr < g ? *reinterpret_cast<const uint32_t *>(Qu + (size_t)qr * kHeadDim + c0 + 8) : 0u;
-            qa[ks][3] = (HR > 1 && qr + 8 < g) ? *reinterpret_cast<const uint32_t *>(Qu + (size_t)(qr + 8) * kHeadDim + c0 + 8) : 0u;
-        }
-    }
-    float o[16][4];
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+    load_q_frag<HR>(Q + ((size_t)b * n_q_heads + (size_t)h * g) * kHeadDim, g, qa);
+    AttnState st;
+    st.init();
     bool ok = true;
     for (int k = 0; k < nk; ++k) {
         const int x = xs + warp + k * kMW;
@@ -214,84 +172,7 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
             tma_store_2d(&tm_vb, sp + kTileBytes + kHalfBytes, 64, row);
             bulk_commit();
         }
-        const uint32_t ks_base = su32(sp), vs_base = su32(sp + kTileBytes);
-        // ---- S = Q K^T: two 8-key tiles
-        float s[2][4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-#pragma unroll
-            for (int kk = 0; kk < 8; kk += 2) {
-                // matrices: keys 8nt..8nt+7 x 16-byte chunks 2kk .. 2kk + 3
-                const int mi = lane >> 3;
-                const uint32_t addr = sw_addr(ks_base, 8 * nt + (lane & 7), 2 * kk + mi);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(addr, b0, b1, b2, b3);
-                mma16816(s[nt], qa[kk], b0, b1);
-                mma16816(s[nt], qa[kk + 1], b2, b3);
-            }
-        }
-        // ---- online softmax of rows qr (and qr + 8): keys 8nt + 2qc + {0, 1}
-        float p[2][2][2];  // [row half][tile][pair]
-        float alpha[2];
-#pragma unroll
-        for (int rh = 0; rh < HR; ++rh) {
-            float v[2][2];
-            float mx = -INFINITY;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int key = 8 * nt + 2 * qc + e;
-                    v[nt][e] = key < len ? s[nt][2 * rh + e] * scale : -INFINITY;
-                    mx = fmaxf(mx, v[nt][e]);
-                }
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            const float m_new = fmaxf(m_run[rh], mx);
-            alpha[rh] = m_run[rh] == -INFINITY ? 0.f : expf(m_run[rh] - m_new);
-            float sm = 0.f;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    p[rh][nt][e] = v[nt][e] == -INFINITY ? 0.f : expf(v[nt][e] - m_new);
-                    sm += p[rh][nt][e];
-                }
-            sm += __shfl_xor_sync(0xffffffffu, sm, 1);
-            sm += __shfl_xor_sync(0xffffffffu, sm, 2);
-            l_run[rh] = l_run[rh] * alpha[rh] + sm;
-            m_run[rh] = m_new;
-        }
-        if (HR == 1) {
-            alpha[1] = 0.f;
-            p[1][0][0] = p[1][0][1] = p[1][1][0] = p[1][1][1] = 0.f;
-        }
-#pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-            o[nt][0] *= alpha[0];
-            o[nt][1] *= alpha[0];
-            o[nt][2] *= alpha[1];
-            o[nt][3] *= alpha[1];
-        }
-        // ---- O += P V: A = P (rows x 16 keys) as bf16 hi + lo
-        uint32_t ahi[4], alo[4];
-        split_pair(p[0][0][0], p[0][0][1], ahi[0], alo[0]);
-        split_pair(p[1][0][0], p[1][0][1], ahi[1], alo[1]);
-        split_pair(p[0][1][0], p[0][1][1], ahi[2], alo[2]);
-        split_pair(p[1][1][0], p[1][1][1], ahi[3], alo[3]);
-#pragma unroll
-        for (int nt = 0; nt < 16; nt += 2) {
-            // matrices: (keys 0-7, chunk nt), (keys 8-15, chunk nt), (keys 0-7, nt+1), (keys 8-15, nt+1)
-            const int mi = lane >> 3;
-            const uint32_t addr = sw_addr(vs_base, (mi & 1) * 8 + (lane & 7), nt + (mi >> 1));
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(addr, b0, b1, b2, b3);
-            mma16816(o[nt], ahi, b0, b1);
-            mma16816(o[nt], alo, b0, b1);
-            mma16816(o[nt + 1], ahi, b2, b3);
-            mma16816(o[nt + 1], alo, b2, b3);
-        }
+        attend_page<HR>(qa, su32(sp), su32(sp + kTileBytes), len, scale, st);
         __syncwarp();
         if (lane == 0 && k + kNS < nk) {  // refill this slot once its stores have read it
             if (store) bulk_wait_read_all();
@@ -305,11 +186,11 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
     }
     if (store && lane == 0) bulk_wait_read_all();  // the slots are reused below
     if (qc == 0) {
-        S.ml[warp][qr][0] = m_run[0];
-        S.ml[warp][qr][1] = l_run[0];
+        S.ml[warp][qr][0] = st.m[0];
+        S.ml[warp][qr][1] = st.l[0];
         if (HR > 1) {
-            S.ml[warp][qr + 8][0] = m_run[1];
-            S.ml[warp][qr + 8][1] = l_run[1];
+            S.ml[warp][qr + 8][0] = st.m[1];
+            S.ml[warp][qr + 8][1] = st.l[1];
         }
     }
     __syncthreads();
@@ -319,9 +200,11 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
 #pragma unroll
     for (int nt = 0; nt < 16; ++nt) {
         const int d = 8 * nt + 2 * qc;
-        *reinterpret_cast<float2 *>(s_o + ((size_t)warp * 16 + qr) * kHeadDim + d) = make_float2(o[nt][0], o[nt][1]);
+        *reinterpret_cast<float2 *>(s_o + ((size_t)warp * 16 + qr) * kHeadDim + d) =
+            make_float2(st.o[nt][0], st.o[nt][1]);
         if (HR > 1)
-            *reinterpret_cast<float2 *>(s_o + ((size_t)warp * 16 + qr + 8) * kHeadDim + d) = make_float2(o[nt][2], o[nt][3]);
+            *reinterpret_cast<float2 *>(s_o + ((size_t)warp * 16 + qr + 8) * kHeadDim + d) =
+                make_float2(st.o[nt][2], st.o[nt][3]);
     }
     if (tid < g) {
         float M = -INFINITY;

@@ -453,7 +453,7 @@ def check_build_positional(run: DeviceRun, u: int) -> dict:
     assert np.array_equal(H["token_slot"][u, :N], pk["token_slot"]), (u, "token_slot")
     Ps = P - n_pos
     cnt = np.bincount(pk["page_parent"][:Ps], minlength=Np)[:Np]
-    first = np.concatenate([[0], np.cumsum(cnt)[:-1]])
+    first = np.concatenate([[0], np.cumsum(cnt)[:-1]])[:Np]
     assert np.array_equal(H["parent_n_pages"][u, :Np], cnt)
     assert np.array_equal(H["parent_first_page"][u, :Np], first)
     assert np.array_equal(H["parent_last_page"][u, :Np], first + cnt - 1)
