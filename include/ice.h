@@ -24,6 +24,8 @@
  *    stream) and is asynchronous: no entry point synchronises unless it says
  *    so.  Scratch memory comes from the caller's workspace `ws` of `ws_bytes`
  *    bytes (256-byte aligned), sized by the matching *_workspace_bytes query.
+ *  - K, V, Q, k_new, v_new, kbuf, vbuf and the index's parent_keys, pool_k
+ *    and pool_v must be 16-byte aligned (ICE_ERR_INVALID_ARG otherwise).
  *  - A "unit" is one (sequence b, KV head h) pair of one layer; units are
  *    numbered u = b * n_kv_heads + h and are fully independent.
  *  - Conditions only the device can see (a capacity that turns out too
@@ -31,6 +33,13 @@
  *    0 by the caller before first use) as an ice_status; the kernels then
  *    clamp every write to the capacities, so memory outside the arrays is
  *    never touched.  ice_check() reads and clears that word.
+ *  - Overlap ([A] 关键设计 4, the three-stage pipeline): since every call is
+ *    stream-ordered, a caller overlaps layer i + 1's host-to-device copy of
+ *    K, V and Q (one stream) with layer i's ice_build_index and
+ *    ice_decode_step (another stream), ordering them with events: the copy
+ *    of layer i + 1 waits for the last use of the buffers it overwrites, the
+ *    build of layer i + 1 for its copy.  Calls that share a workspace stay on
+ *    one stream.
  *  - Floating point: keys/values/queries are bf16 or fp32 (ice_params.dtype);
  *    every score and every softmax is accumulated in fp32; outputs O are
  *    fp32.
@@ -434,11 +443,10 @@ ice_status ice_sparse_attn_decode_noalloc(const ice_params *p, const void *Q, co
                                           float scale, float *O, void *stream);
 
 /*
- * The whole decode step a6-a10 in two launches: ice_select_pages, then one
- * kernel that reads each selected page once from the pool, writes it to
- * kbuf/vbuf/buf_len (the contiguous buffer of step a9) and computes the
- * attention of step a10 from the same copy.  Same outputs as the three
- * separate calls.
+ * The whole decode step a6-a10 (the kernels of ice_decode_plan): every
+ * selected page is read once from the pool, written to kbuf/vbuf/buf_len
+ * (the contiguous buffer of step a9) and attended (step a10) from the same
+ * on-chip copy.  Same outputs as the three separate calls.
  * kbuf, vbuf and buf_len may all be NULL: the selected pages are then
  * gathered into on-chip shared memory only and attended from there, with no
  * contiguous copy in device memory (the pool is still read once); sel_pages,
@@ -449,6 +457,40 @@ ice_status ice_decode_step(const ice_params *p, const ice_index *idx, const void
                            int32_t *sel_pages, int32_t *sel_count, int32_t max_sel, void *kbuf, void *vbuf,
                            int32_t *buf_len, float scale, float *O, void *ws, size_t ws_bytes,
                            int32_t *err_dev, void *stream);
+
+/*
+ * The kernels ice_decode_step runs for a shape, chosen from the sizes in *p,
+ * the budget and max_sel (and the device's SM count):
+ *   ICE_PLAN_FUSED     bf16, g <= 8, k <= 32 (and the shared-memory and
+ *                      coordinate limits): one kernel, a cluster of CTAs per
+ *                      unit scans the parent table by TMA with tensor-core
+ *                      scores, keeps each head's best k on chip, forms the
+ *                      union and attends over its pages;
+ *   ICE_PLAN_CLUSTER   fp32 while every unit's 8-CTA cluster fits one wave:
+ *                      one kernel of 8-CTA clusters (CUDA-core scores);
+ *   ICE_PLAN_SCORE_TC  other bf16 shapes (g up to 16, k <= 32): the score
+ *                      table on the tensor cores, a per-unit top-k kernel,
+ *                      then the gather + attention kernel;
+ *   ICE_PLAN_SIMT      the rest: CUDA-core selection, then the gather +
+ *                      attention kernel;
+ *   ICE_PLAN_DESCENT   n_levels = 3: the descent kernel, then the gather +
+ *                      attention kernel.
+ * *attention_plan: the attention kernel of ice_sparse_attn_decode and of the
+ * last three plans: ICE_PLAN_ATTN_MMA (bf16, g <= 16, at most 32 pages per
+ * warp: warp-level tensor-core MMAs on TMA-staged pages) or
+ * ICE_PLAN_ATTN_SIMT.  A launch that the device refuses at run time (no
+ * cluster of that size schedulable) falls back to ICE_PLAN_SCORE_TC or
+ * ICE_PLAN_SIMT.  Either output may be NULL.
+ */
+#define ICE_PLAN_FUSED 1
+#define ICE_PLAN_CLUSTER 2
+#define ICE_PLAN_SCORE_TC 3
+#define ICE_PLAN_SIMT 4
+#define ICE_PLAN_DESCENT 5
+#define ICE_PLAN_ATTN_MMA 1
+#define ICE_PLAN_ATTN_SIMT 2
+ice_status ice_decode_plan(const ice_params *p, int32_t budget_tokens, int32_t max_sel, int32_t *step_plan,
+                           int32_t *attention_plan);
 
 /* ----------------------------------------------------- host page pool --- */
 /*

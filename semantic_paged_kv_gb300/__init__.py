@@ -88,6 +88,7 @@ def load() -> ctypes.CDLL:
         "ice_gather_pages": ([pp, pi, P, P, i32, P, P, P, P], i32),
         "ice_sparse_attn_decode": ([pp, P, P, P, P, P, i32, f32, P, P, sz, P], i32),
         "ice_decode_step": ([pp, pi, P, i32, P, P, i32, P, P, P, f32, P, P, sz, P, P], i32),
+        "ice_decode_plan": ([pp, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)], i32),
         "ice_sparse_attn_decode_noalloc": ([pp, P, P, P, P, P, i32, f32, P, P], i32),
         "ice_insert_workspace_bytes": ([pp, ctypes.POINTER(sz)], i32),
         "ice_insert_tokens": ([pp, pi, P, P, P, sz, P, P], i32),
@@ -112,6 +113,7 @@ def exported_symbols() -> list[str]:
             "ice_build_assign_simt", "ice_build_pack", "ice_build_index_reuse", "ice_decode_workspace_bytes",
             "ice_select_pages",
             "ice_gather_pages", "ice_sparse_attn_decode", "ice_sparse_attn_decode_noalloc", "ice_decode_step",
+            "ice_decode_plan",
             "ice_insert_workspace_bytes", "ice_insert_tokens", "ice_host_pool_create", "ice_host_pool_destroy",
             "ice_host_pool_pointers", "ice_host_pool_staging_bytes", "ice_host_pool_gather_h2d"]
 
@@ -420,6 +422,17 @@ def ice_decode_step(params, index, Q, budget_tokens, sel_pages, sel_count, kbuf,
     _check(load().ice_decode_step(ctypes.byref(params), ctypes.byref(ix), _ptr(Q), budget_tokens, _ptr(sel_pages),
                                   _ptr(sel_count), sel_pages.shape[-1], _ptr(kbuf), _ptr(vbuf), _ptr(buf_len),
                                   float(scale), _ptr(O), _ptr(ws), _nbytes(ws), _ptr(err), _stream(stream)))
+
+
+ICE_PLAN_FUSED, ICE_PLAN_CLUSTER, ICE_PLAN_SCORE_TC, ICE_PLAN_SIMT, ICE_PLAN_DESCENT = 1, 2, 3, 4, 5
+ICE_PLAN_ATTN_MMA, ICE_PLAN_ATTN_SIMT = 1, 2
+
+
+def ice_decode_plan(params, budget_tokens: int, max_sel: int) -> tuple[int, int]:
+    """(step plan, attention plan) of ice_decode_step for this shape."""
+    a, b = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(load().ice_decode_plan(ctypes.byref(params), budget_tokens, max_sel, ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
 
 
 # ----------------------------------------------------- buffer helpers -----

@@ -113,6 +113,18 @@ ice_status check_ws(void *ws, size_t ws_bytes, size_t need) {
 
 int k_pages_of(int budget_tokens) { return (budget_tokens + kPage - 1) / kPage; }
 
+int sm_count();
+
+// The kernels ice_decode_step runs for a shape (see ice_decode_plan).
+int decode_plan(const ice_params &p, int k_pages, int max_sel) {
+    if (p.n_levels == 3) return ICE_PLAN_DESCENT;
+    if (decode_fused_supported(p, k_pages, max_sel)) return ICE_PLAN_FUSED;
+    if (p.dtype == ICE_FP32 && units_of(p) * kDecodeCluster <= sm_count() &&
+        decode_cluster_supported(p, k_pages, max_sel))
+        return ICE_PLAN_CLUSTER;
+    return select_tc_supported(p, k_pages) ? ICE_PLAN_SCORE_TC : ICE_PLAN_SIMT;
+}
+
 int sm_count() {
     int dev = 0, n = 0;
     cudaGetDevice(&dev);
@@ -488,6 +500,7 @@ static ice_status select_checks(const ice_params *p, const ice_index *idx, const
     if (st) return st;
     if ((st = check_level2(p, idx))) return st;
     if (!Q || !sel_pages || !sel_count) return fail(ICE_ERR_INVALID_ARG, "Q, sel_pages and sel_count must be non-NULL");
+    if (!aligned16(Q)) return fail(ICE_ERR_INVALID_ARG, "Q must be 16-byte aligned");
     if (p->n_levels == 3 && k_pages_of(budget_tokens) > 32)
         return fail(ICE_ERR_UNSUPPORTED, "the three-level descent takes at most 32 pages per head");
     const long long g = p->n_q_heads / p->n_kv_heads;
@@ -542,7 +555,8 @@ ice_status ice_sparse_attn_decode(const ice_params *p, const void *Q, const void
     if (st) return st;
     if (!Q || !kbuf || !vbuf || !buf_len || !sel_count || !O)
         return fail(ICE_ERR_INVALID_ARG, "attention needs non-NULL Q, kbuf, vbuf, buf_len, sel_count and O");
-    if (!aligned16(kbuf) || !aligned16(vbuf)) return fail(ICE_ERR_INVALID_ARG, "kbuf and vbuf must be 16-byte aligned");
+    if (!aligned16(kbuf) || !aligned16(vbuf) || !aligned16(Q))
+        return fail(ICE_ERR_INVALID_ARG, "Q, kbuf and vbuf must be 16-byte aligned");
     return cuda_status(launch_attention(*p, nullptr, nullptr, Q, const_cast<void *>(kbuf), const_cast<void *>(vbuf),
                                         const_cast<int32_t *>(buf_len), sel_count, max_sel, scale, O, w,
                                         static_cast<cudaStream_t>(stream)),
@@ -581,42 +595,47 @@ ice_status ice_decode_step(const ice_params *p, const ice_index *idx, const void
         return fail(ICE_ERR_INVALID_ARG, "kbuf, vbuf and buf_len must be all non-NULL or all NULL");
     if (!aligned16(kbuf) || !aligned16(vbuf)) return fail(ICE_ERR_INVALID_ARG, "kbuf and vbuf must be 16-byte aligned");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (p->n_levels == 3) {  // descent through level 2, then the pages streamed from the pool
-        cudaError_t e = launch_select3(*p, *idx, Q, w, sel_pages, sel_count, max_sel, err_dev, s);
+    cudaError_t e = cudaErrorNotSupported;
+    switch (decode_plan(*p, w.k_pages, max_sel)) {
+    case ICE_PLAN_DESCENT:  // descent through level 2, then the pages streamed from the pool
+        e = launch_select3(*p, *idx, Q, w, sel_pages, sel_count, max_sel, err_dev, s);
         if (e == cudaSuccess)
             e = launch_attention(*p, idx, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, w, s,
                                  err_dev);
         return cuda_status(e, "ice_decode_step");
+    case ICE_PLAN_FUSED:  // the whole step in one kernel, a cluster of CTAs per unit
+        e = launch_decode_fused(*p, *idx, Q, w.k_pages, sel_pages, sel_count, max_sel, kbuf, vbuf, buf_len, scale, O,
+                                err_dev, s);
+        break;
+    case ICE_PLAN_CLUSTER:  // fp32, every unit's 8-CTA cluster in one wave
+        e = launch_decode_cluster(*p, *idx, Q, w.k_pages, sel_pages, sel_count, max_sel, kbuf, vbuf, buf_len, scale,
+                                  O, err_dev, s);
+        break;
+    default:
+        break;
     }
-    // one cluster per unit pays off while all clusters fit in one wave; with
-    // more units the select / attention kernels keep every SM streaming
-    if (units_of(*p) * kDecodeCluster <= sm_count() && aligned16(Q) &&
-        decode_cluster2_supported(*p, w.k_pages, max_sel))
-        return cuda_status(launch_decode_cluster2(*p, *idx, Q, w.k_pages, sel_pages, sel_count, max_sel, kbuf, vbuf,
-                                                  buf_len, scale, O, err_dev, s),
-                           "ice_decode_step");
-    if (units_of(*p) * kDecodeCluster <= sm_count() && decode_cluster_supported(*p, w.k_pages, max_sel))
-        return cuda_status(launch_decode_cluster(*p, *idx, Q, w.k_pages, sel_pages, sel_count, max_sel, kbuf, vbuf,
-                                                 buf_len, scale, O, err_dev, s),
-                           "ice_decode_step");
-    // more units: the score table on the tensor cores, then attention CTAs that
-    // select their unit's pages themselves
-    if (select_tc_supported(*p, w.k_pages) && attention_mma_select_supported(*p, max_sel)) {
-        cudaError_t e = launch_score_tc(*p, *idx, Q, w, err_dev, s);
-        if (e == cudaSuccess) {
-            const SelArgs A = select_args(*p, *idx, w, sel_pages, sel_count, max_sel, err_dev);
-            e = launch_attention_mma_select(*p, *idx, A, Q, kbuf, vbuf, buf_len, max_sel, scale, O, w, err_dev, s);
-            if (e == cudaErrorNotSupported && (e = launch_topk(*p, A, s)) == cudaSuccess)  // scores are there
-                e = launch_attention(*p, idx, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, w, s,
-                                     err_dev);
-        }
-        if (e != cudaErrorNotSupported) return cuda_status(e, "ice_decode_step");
+    if (e != cudaErrorNotSupported) return cuda_status(e, "ice_decode_step");
+    // the score table on the tensor cores and the per-unit top-k (bf16), or the SIMT selection;
+    // then the fused gather + attention
+    if (select_tc_supported(*p, w.k_pages)) {
+        e = launch_score_tc(*p, *idx, Q, w, err_dev, s);
+        if (e == cudaSuccess) e = launch_topk(*p, select_args(*p, *idx, w, sel_pages, sel_count, max_sel, err_dev), s);
+    } else {
+        e = launch_select(*p, *idx, Q, w, sel_pages, sel_count, max_sel, err_dev, s);
     }
-    if ((st = cuda_status(launch_select(*p, *idx, Q, w, sel_pages, sel_count, max_sel, err_dev, s), "ice_decode_step select")))
-        return st;
-    return cuda_status(
-        launch_attention(*p, idx, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, w, s, err_dev),
-        "ice_decode_step attention");
+    if (e == cudaSuccess)
+        e = launch_attention(*p, idx, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, w, s, err_dev);
+    return cuda_status(e, "ice_decode_step");
+}
+
+ice_status ice_decode_plan(const ice_params *p, int32_t budget_tokens, int32_t max_sel, int32_t *step_plan,
+                           int32_t *attention_plan) {
+    ice_status st = check_params(p);
+    if (st) return st;
+    if (budget_tokens < 0 || max_sel < 1) return fail(ICE_ERR_INVALID_ARG, "need budget_tokens >= 0 and max_sel >= 1");
+    if (step_plan) *step_plan = decode_plan(*p, k_pages_of(budget_tokens), max_sel);
+    if (attention_plan) *attention_plan = attention_mma_fits(*p, max_sel) ? ICE_PLAN_ATTN_MMA : ICE_PLAN_ATTN_SIMT;
+    return ICE_OK;
 }
 
 }  // extern "C"

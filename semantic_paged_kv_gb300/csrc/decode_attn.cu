@@ -339,14 +339,9 @@ cudaError_t launch_gather(const ice_params &p, const ice_index &idx, const int32
 cudaError_t launch_attention(const ice_params &p, const ice_index *pool, const int32_t *sel_pages, const void *Q,
                              void *kbuf, void *vbuf, int32_t *buf_len, const int32_t *sel_count, int max_sel,
                              float scale, float *O, const DecodeWs &ws, cudaStream_t s, int32_t *err) {
-    if (attention_mma_supported(p) && ((uintptr_t)Q & 3u) == 0) {
+    if (attention_mma_fits(p, max_sel)) {
         const cudaError_t e = launch_attention_mma(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel,
                                                    scale, O, ws, err, s);
-        if (e != cudaErrorNotSupported) return e;
-    }
-    if (attention_stream_supported(p) && ((uintptr_t)Q & 15u) == 0) {
-        const cudaError_t e = launch_attention_stream(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel,
-                                                      scale, O, ws, err, s);
         if (e != cudaErrorNotSupported) return e;
     }
     if (p.dtype == ICE_BF16)

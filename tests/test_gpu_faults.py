@@ -5,7 +5,7 @@ ICE_FAULT (read by the library at every call) injects:
   alloc     the host pool's first pinned allocation fails -> ICE_ERR_OOM
   hostpool  the host pool fails after its allocations     -> ICE_ERR_CUDA
   copy      the staged gather's bulk copy fails           -> ICE_ERR_CUDA
-  timeout   the attention kernel's page producer issues no copy and its
+  timeout   the decode kernels' TMA producers issue no copy and their
             bounded waits give up after 20 ms             -> ICE_ERR_TIMEOUT
 Each test checks the status, that nothing leaked or stayed broken, and that
 the next call without the fault gives the oracle's result."""
@@ -78,11 +78,11 @@ def test_staged_copy_fault_then_recovery(monkeypatch):
 
 
 def test_attention_wait_timeout_is_reported_and_the_context_stays_usable(monkeypatch):
-    """With the page producer silenced, every warp's bounded wait gives up:
-    ice_sparse_attn_decode (no error word) leaves NaN in O, and the fused
-    decode step of many units (the attention CTAs that select their own
-    pages) reports ICE_ERR_TIMEOUT through ice_check.  The kernels return;
-    the same calls without the fault then match the oracle."""
+    """With the TMA producers silenced, every warp's bounded wait gives up:
+    ice_sparse_attn_decode (no error word) leaves NaN in O, and the decode
+    step (the one-kernel decode: parent-table scan and page stream both
+    silenced) reports ICE_ERR_TIMEOUT through ice_check.  The kernels
+    return; the same calls without the fault then match the oracle."""
     w = workloads.WORKLOADS["qwen3_32b_100k"].scaled(n_tokens=3000, batch=3, centres=256)
     run = DeviceRun(w)
     assert run.status == ice.ICE_OK

@@ -476,3 +476,40 @@ def test_reuse_with_sink_window_and_three_levels():
     assert st == ice.ICE_OK
     for u, ref in refs.items():
         check_decode_descent(run1, u, Q, 128, buf, ref["level2"], ref)
+
+
+@pytest.mark.parametrize("shape,budget,plan,attn", [
+    ("fused_one_cta_per_unit", 256, ice.ICE_PLAN_FUSED, ice.ICE_PLAN_ATTN_MMA),
+    ("fused_cluster_per_unit", 256, ice.ICE_PLAN_FUSED, ice.ICE_PLAN_ATTN_MMA),
+    ("score_tc_g16", 256, ice.ICE_PLAN_SCORE_TC, ice.ICE_PLAN_ATTN_MMA),
+    ("simt_select_k64_bf16", 1024, ice.ICE_PLAN_SIMT, ice.ICE_PLAN_ATTN_MMA),
+    ("cluster_fp32", 64, ice.ICE_PLAN_CLUSTER, ice.ICE_PLAN_ATTN_SIMT),
+    ("simt_fp32_many_units", 64, ice.ICE_PLAN_SIMT, ice.ICE_PLAN_ATTN_SIMT),
+    ("simt_attention_bf16", 1024, ice.ICE_PLAN_SIMT, ice.ICE_PLAN_ATTN_SIMT)])
+def test_every_decode_plan_against_the_oracle(shape, budget, plan, attn):
+    """Each kernel path of ice_decode_step (ice_decode_plan names it) and
+    each attention kernel, on a shape that selects it: the fused decode with
+    one CTA and with a cluster per unit, the tensor-core score table with 16
+    query heads per group, the SIMT selection (more than 32 pages per head),
+    the fp32 cluster decode, the SIMT path for fp32 with many units, and the
+    SIMT attention when a warp would hold more than 32 pages.  The step
+    (fused call and separate calls) checked against the oracle."""
+    w = {"fused_one_cta_per_unit": W["qwen3_32b_100k"].scaled(n_tokens=2200, batch=20, centres=128),
+         "fused_cluster_per_unit": W["llama31_8b_16k"].scaled(n_tokens=3000, n_q_heads=8, n_kv_heads=2),
+         "score_tc_g16": W["llama31_8b_16k"].scaled(n_tokens=3000, n_q_heads=32, n_kv_heads=2),
+         "simt_select_k64_bf16": W["llama31_8b_16k"].scaled(n_tokens=3000, n_q_heads=8, n_kv_heads=2),
+         "cluster_fp32": W["tiny"],
+         "simt_fp32_many_units": W["tiny"].scaled(n_tokens=1500, batch=20),
+         "simt_attention_bf16": W["qwen3_32b_100k"].scaled(n_tokens=3000, batch=19, centres=128)}[shape]
+    run = DeviceRun(w)
+    assert run.status == ice.ICE_OK
+    max_sel = ice.max_selected(run.cfg, budget)
+    assert ice.ice_decode_plan(run.params, budget, max_sel) == (plan, attn)
+    units = range(run.cfg.units) if run.cfg.units <= 24 else (0, 7, 50, run.cfg.units - 1)
+    for u in (units if run.cfg.units <= 24 else units[:2]):
+        check_build_unit(run, u)
+    for fused in (True, False):
+        Q, buf, st = run.decode(budget, fused=fused)
+        assert st == ice.ICE_OK
+        for u in units:
+            check_decode_unit(run, u, Q, budget, buf)
