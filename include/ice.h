@@ -461,32 +461,36 @@ ice_status ice_decode_step(const ice_params *p, const ice_index *idx, const void
 /*
  * The kernels ice_decode_step runs for a shape, chosen from the sizes in *p,
  * the budget and max_sel (and the device's SM count):
- *   ICE_PLAN_FUSED     bf16, g <= 8, k <= 32 (and the shared-memory and
- *                      coordinate limits): one kernel, a cluster of CTAs per
- *                      unit scans the parent table by TMA with tensor-core
- *                      scores, keeps each head's best k on chip, forms the
- *                      union and attends over its pages;
- *   ICE_PLAN_CLUSTER   fp32 while every unit's 8-CTA cluster fits one wave:
- *                      one kernel of 8-CTA clusters (CUDA-core scores);
- *   ICE_PLAN_SCORE_TC  other bf16 shapes (g up to 16, k <= 32): the score
- *                      table on the tensor cores, a per-unit top-k kernel,
- *                      then the gather + attention kernel;
- *   ICE_PLAN_SIMT      the rest: CUDA-core selection, then the gather +
- *                      attention kernel;
- *   ICE_PLAN_DESCENT   n_levels = 3: the descent kernel, then the gather +
- *                      attention kernel.
+ *   ICE_PLAN_CLUSTER_BF16  bf16, g <= 8, k <= 32, while every unit's 8-CTA
+ *                          cluster fits one wave (U * 8 <= SMs): one kernel,
+ *                          the unit's parent slices scored on CUDA cores in
+ *                          its 8 CTAs, lists merged over distributed shared
+ *                          memory, pages bulk-copied and attended;
+ *   ICE_PLAN_CLUSTER       the same cluster kernel for fp32 (or k <= 64,
+ *                          g <= 16);
+ *   ICE_PLAN_SCORE_SELECT  bf16, g <= 8, k <= 32 with more units: the score
+ *                          table of every unit on the tensor cores (TMA +
+ *                          tcgen05 over all SMs), then attention CTAs that
+ *                          select their unit's pages and attend over them
+ *                          (warp-level MMAs on TMA-staged pages);
+ *   ICE_PLAN_SCORE_TOPK    other bf16 shapes with g <= 16, k <= 32: the score
+ *                          table, a per-unit top-k kernel, then the gather +
+ *                          attention kernel;
+ *   ICE_PLAN_SIMT          the rest: CUDA-core selection, then the gather +
+ *                          attention kernel;
+ *   ICE_PLAN_DESCENT       n_levels = 3: the descent kernel, then the gather +
+ *                          attention kernel.
  * *attention_plan: the attention kernel of ice_sparse_attn_decode and of the
  * last three plans: ICE_PLAN_ATTN_MMA (bf16, g <= 16, at most 32 pages per
  * warp: warp-level tensor-core MMAs on TMA-staged pages) or
- * ICE_PLAN_ATTN_SIMT.  A launch that the device refuses at run time (no
- * cluster of that size schedulable) falls back to ICE_PLAN_SCORE_TC or
- * ICE_PLAN_SIMT.  Either output may be NULL.
+ * ICE_PLAN_ATTN_SIMT.  Either output may be NULL.
  */
-#define ICE_PLAN_FUSED 1
+#define ICE_PLAN_CLUSTER_BF16 1
 #define ICE_PLAN_CLUSTER 2
-#define ICE_PLAN_SCORE_TC 3
-#define ICE_PLAN_SIMT 4
-#define ICE_PLAN_DESCENT 5
+#define ICE_PLAN_SCORE_SELECT 3
+#define ICE_PLAN_SCORE_TOPK 4
+#define ICE_PLAN_SIMT 5
+#define ICE_PLAN_DESCENT 6
 #define ICE_PLAN_ATTN_MMA 1
 #define ICE_PLAN_ATTN_SIMT 2
 ice_status ice_decode_plan(const ice_params *p, int32_t budget_tokens, int32_t max_sel, int32_t *step_plan,

@@ -424,7 +424,8 @@ def ice_decode_step(params, index, Q, budget_tokens, sel_pages, sel_count, kbuf,
                                   float(scale), _ptr(O), _ptr(ws), _nbytes(ws), _ptr(err), _stream(stream)))
 
 
-ICE_PLAN_FUSED, ICE_PLAN_CLUSTER, ICE_PLAN_SCORE_TC, ICE_PLAN_SIMT, ICE_PLAN_DESCENT = 1, 2, 3, 4, 5
+(ICE_PLAN_CLUSTER_BF16, ICE_PLAN_CLUSTER, ICE_PLAN_SCORE_SELECT, ICE_PLAN_SCORE_TOPK, ICE_PLAN_SIMT,
+ ICE_PLAN_DESCENT) = 1, 2, 3, 4, 5, 6
 ICE_PLAN_ATTN_MMA, ICE_PLAN_ATTN_SIMT = 1, 2
 
 

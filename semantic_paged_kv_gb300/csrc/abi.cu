@@ -118,11 +118,16 @@ int sm_count();
 // The kernels ice_decode_step runs for a shape (see ice_decode_plan).
 int decode_plan(const ice_params &p, int k_pages, int max_sel) {
     if (p.n_levels == 3) return ICE_PLAN_DESCENT;
-    if (decode_fused_supported(p, k_pages, max_sel)) return ICE_PLAN_FUSED;
-    if (p.dtype == ICE_FP32 && units_of(p) * kDecodeCluster <= sm_count() &&
-        decode_cluster_supported(p, k_pages, max_sel))
-        return ICE_PLAN_CLUSTER;
-    return select_tc_supported(p, k_pages) ? ICE_PLAN_SCORE_TC : ICE_PLAN_SIMT;
+    // one cluster per unit pays off while all clusters fit in one wave; with
+    // more units the score / attention kernels keep every SM streaming
+    if (units_of(p) * kDecodeCluster <= sm_count()) {
+        if (decode_cluster2_supported(p, k_pages, max_sel)) return ICE_PLAN_CLUSTER_BF16;
+        if (decode_cluster_supported(p, k_pages, max_sel)) return ICE_PLAN_CLUSTER;
+    }
+    if (select_tc_supported(p, k_pages))
+        return attention_mma_select_supported(p, max_sel) && attention_mma_fits(p, max_sel) ? ICE_PLAN_SCORE_SELECT
+                                                                                             : ICE_PLAN_SCORE_TOPK;
+    return ICE_PLAN_SIMT;
 }
 
 int sm_count() {
@@ -603,14 +608,20 @@ ice_status ice_decode_step(const ice_params *p, const ice_index *idx, const void
             e = launch_attention(*p, idx, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, w, s,
                                  err_dev);
         return cuda_status(e, "ice_decode_step");
-    case ICE_PLAN_FUSED:  // the whole step in one kernel, a cluster of CTAs per unit
-        e = launch_decode_fused(*p, *idx, Q, w.k_pages, sel_pages, sel_count, max_sel, kbuf, vbuf, buf_len, scale, O,
-                                err_dev, s);
+    case ICE_PLAN_CLUSTER_BF16:
+        e = launch_decode_cluster2(*p, *idx, Q, w.k_pages, sel_pages, sel_count, max_sel, kbuf, vbuf, buf_len, scale,
+                                   O, err_dev, s);
         break;
-    case ICE_PLAN_CLUSTER:  // fp32, every unit's 8-CTA cluster in one wave
+    case ICE_PLAN_CLUSTER:
         e = launch_decode_cluster(*p, *idx, Q, w.k_pages, sel_pages, sel_count, max_sel, kbuf, vbuf, buf_len, scale,
                                   O, err_dev, s);
         break;
+    case ICE_PLAN_SCORE_SELECT:  // the score table, then attention CTAs that select their unit's pages
+        e = launch_score_tc(*p, *idx, Q, w, err_dev, s);
+        if (e == cudaSuccess)
+            e = launch_attention_mma_select(*p, *idx, select_args(*p, *idx, w, sel_pages, sel_count, max_sel, err_dev),
+                                            Q, kbuf, vbuf, buf_len, max_sel, scale, O, w, err_dev, s);
+        return cuda_status(e, "ice_decode_step");
     default:
         break;
     }

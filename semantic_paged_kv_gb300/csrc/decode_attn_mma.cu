@@ -12,22 +12,30 @@
 // through the warp's three shared-memory slots (two pages in flight while
 // one is computed) by 2-D TMA loads with a 128-byte swizzle (so the 8-row
 // fragment loads below are conflict-free).
-// Per page, with the g <= 16 query rows of the group as the M = 16 rows, the
-// two contractions and the online softmax of attn_page.cuh (mma.sync
-// m16n8k16, bf16 in, fp32 accumulate).
+// Per page, with the g <= 16 query rows of the group as the M = 16 rows:
+//   S = Q K^T     mma.sync m16n8k16 (bf16 in, fp32 accumulate): A = q in
+//                 registers (loaded once), B = K rows by ldmatrix; 2 key
+//                 tiles x 8 dimension steps;
+//   online softmax on the accumulator fragments: a quad of lanes holds a
+//                 row's 16 keys (two shuffles per reduction), masked past
+//                 the page length;
+//   O += P V      P as the A fragment straight from S's accumulators, split
+//                 into bf16 hi + lo parts (two MMAs, ~2^-16 relative error
+//                 instead of bf16's 2^-9); B = V rows by ldmatrix.trans;
+//                 16 dimension tiles.
 // With F the page goes back to kbuf / vbuf by 2-D TMA stores from shared
 // memory (the slot is reloaded only after its stores have read it) and its
 // length to buf_len, unless buf_len is null: then the pages are gathered into
-// shared memory only and no contiguous copy is written.  The warps merge in
-// shared memory; with S = 1 the CTA writes O, otherwise its partial joins the
-// others through the unit's ticket
+// shared memory only and no contiguous copy is written.  The warps merge in shared memory; with S = 1 the CTA
+// writes O, otherwise its partial joins the others through the unit's ticket
 // (log-sum-exp, the last CTA writes O).  HR = 2 when g > 8 (rows 8..15 hold
 // query heads too).
 #include <cuda.h>
 
-#include "attn_page.cuh"
 #include "common.cuh"
 #include "internal.h"
+#include "attn_page.cuh"
+#include "select_unit.cuh"
 #include "tc_common.cuh"
 
 namespace ice {
@@ -54,7 +62,7 @@ struct SmemM {
     int bad;  // a bounded wait of some warp gave up: O is NaN for this unit
 };
 
-template <bool kFused, int HR>
+template <bool kFused, int HR, bool kSel>
 __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
     const __grid_constant__ CUtensorMap tm_kb, const __grid_constant__ CUtensorMap tm_vb,
@@ -62,7 +70,7 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
     int page_cap, const int32_t *__restrict__ sel_pages, int32_t *__restrict__ buf_len,
     const int32_t *__restrict__ sel_count, int max_sel, float scale, int n_splits, float *__restrict__ part_ml,
     float *__restrict__ part_o, int32_t *__restrict__ ticket, float *__restrict__ O, int32_t *__restrict__ err,
-    unsigned long long wait_ns, int fault_skip) {
+    unsigned long long wait_ns, int fault_skip, const SelArgs SA) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     // the swizzled page tiles want 1024-byte alignment
     SmemM &S = *reinterpret_cast<SmemM *>(smem_raw + ((1024u - (su32(smem_raw) & 1023u)) & 1023u));
@@ -79,8 +87,21 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
         S.ml[warp][lane][0] = -INFINITY;
         S.ml[warp][lane][1] = 0.f;
     }
-    dep_wait();  // the selected pages are complete
-    const int n = min(sel_count[u], max_sel);
+    dep_wait();  // the selected pages, or the score table (kSel), are complete
+
+    // kSel: the CTA selects its unit's pages itself, in the slot area; split 0
+    // also writes them out (sel_pages, sel_count)
+    int n;
+    const int *s_list = nullptr;
+    if (kSel) {
+        unsigned long long *s_cand = reinterpret_cast<unsigned long long *>(&S.kv[0][0][0]);
+        unsigned *s_mask = reinterpret_cast<unsigned *>(s_cand + kMW * sel::kCand);
+        int *lst = reinterpret_cast<int *>(s_mask + (page_cap + 31) / 32);
+        n = sel::select_unit<kMW>(SA, u, tid, s_mask, s_cand, S.wsum, lst, split == 0);
+        s_list = lst;
+    } else {
+        n = min(sel_count[u], max_sel);
+    }
     const int ps = (max_sel + n_splits - 1) / n_splits;
     const int xs = split * ps;
     const int xe = min(n, xs + ps);
@@ -97,7 +118,7 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
     if (lane < nk) {
         const size_t sl = ubase + xs + warp + lane * kMW;
         if (kFused) {
-            my_pid = sel_pages[sl];
+            my_pid = kSel ? s_list[xs + warp + lane * kMW] : sel_pages[sl];
             my_len = page_len[(size_t)u * page_cap + my_pid];
         } else {
             my_len = buf_len[sl];
@@ -115,6 +136,7 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
         tma_load_2d(slot + kTileBytes, &tm_v, bar, 0, row);
         tma_load_2d(slot + kTileBytes + kHalfBytes, &tm_v, bar, 64, row);
     };
+    if (kSel) __syncthreads();  // every warp has its page ids before the slots fill
     {
         int pf[kNS];
 #pragma unroll
@@ -262,10 +284,10 @@ int sm_count_cached() {
     return n_sm;
 }
 
-template <bool F, int HR>
+template <bool F, int HR, bool kSel>
 cudaError_t launch_hr(const ice_params &p, const ice_index *pool, const int32_t *sel_pages, const void *Q, void *kbuf,
                       void *vbuf, int32_t *buf_len, const int32_t *sel_count, int max_sel, float scale, float *O,
-                      const DecodeWs &ws, int32_t *err, cudaStream_t s, int n_splits) {
+                      const DecodeWs &ws, int32_t *err, cudaStream_t s, int n_splits, const SelArgs &SA) {
     const int U = units_of(p);
     const int g = p.n_q_heads / p.n_kv_heads;
     CUtensorMap tk, tv, tkb, tvb;
@@ -289,19 +311,44 @@ cudaError_t launch_hr(const ice_params &p, const ice_index *pool, const int32_t 
     const size_t merge = sizeof(float) * (size_t)(n_splits * g + g);
     const size_t need = (sizeof(SmemM) > merge ? sizeof(SmemM) : merge) + 1024;  // + alignment slack
     if (need > 227 * 1024) return cudaErrorNotSupported;
-    cudaError_t e = cudaFuncSetAttribute(k_attn_mma<F, HR>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)need);
+    cudaError_t e = cudaFuncSetAttribute(k_attn_mma<F, HR, kSel>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)need);
     if (e != cudaSuccess) return e;
     const __nv_bfloat16 *Qb = static_cast<const __nv_bfloat16 *>(Q);
     const int32_t *plen = pool ? pool->page_len : nullptr;
     const bool fault = fault_armed("timeout");
-    e = launch_dependent(k_attn_mma<F, HR>, dim3(n_splits, U), dim3(kMT), need, s, tk, tv, tkb, tvb, Qb, g,
+    e = launch_dependent(k_attn_mma<F, HR, kSel>, dim3(n_splits, U), dim3(kMT), need, s, tk, tv, tkb, tvb, Qb, g,
                          p.n_q_heads, p.n_kv_heads, plen, p.page_cap, sel_pages, buf_len, sel_count, max_sel, scale,
                          n_splits, ws.part_ml, ws.part_o, ws.attn_ticket, O, err, fault ? kFaultWaitNs : kWaitNs,
-                         fault ? 1 : 0);
+                         fault ? 1 : 0, SA);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
+
+// The selection runs in the attention CTAs: one warp per query head (g <= 12),
+// candidate keys, union bitmask and page list in the 192 KB slot area.
+bool attention_mma_select_supported(const ice_params &p, int max_sel) {
+    const int g = p.n_q_heads / p.n_kv_heads;
+    const size_t need = (size_t)kMW * sel::kCand * 8 + 4 * (size_t)((p.page_cap + 31) / 32) + 4 * (size_t)max_sel;
+    return attention_mma_supported(p) && g <= kMW && need <= sizeof(SmemM::kv);
+}
+
+cudaError_t launch_attention_mma_select(const ice_params &p, const ice_index &idx, const SelArgs &A, const void *Q,
+                                        void *kbuf, void *vbuf, int32_t *buf_len, int max_sel, float scale, float *O,
+                                        const DecodeWs &ws, int32_t *err, cudaStream_t s) {
+    const int U = units_of(p);
+    const int g = p.n_q_heads / p.n_kv_heads;
+    int splits = sm_count_cached() / U;
+    const int most = (max_sel + kMW - 1) / kMW;
+    splits = splits < 1 ? 1 : (splits > most ? most : splits);
+    const int per_warp = (ceil_div(max_sel, splits) + kMW - 1) / kMW;
+    if (splits > ws.n_splits || per_warp > 32 || ((uintptr_t)Q & 3u) != 0) return cudaErrorNotSupported;
+    if (g <= 8)
+        return launch_hr<true, 1, true>(p, &idx, A.sel_pages, Q, kbuf, vbuf, buf_len, A.sel_count, max_sel, scale, O,
+                                        ws, err, s, splits, A);
+    return launch_hr<true, 2, true>(p, &idx, A.sel_pages, Q, kbuf, vbuf, buf_len, A.sel_count, max_sel, scale, O, ws,
+                                    err, s, splits, A);
+}
 
 bool attention_mma_supported(const ice_params &p) {
     const int g = p.n_q_heads / p.n_kv_heads;
@@ -337,11 +384,11 @@ cudaError_t launch_attention_mma(const ice_params &p, const ice_index *pool, con
     const int splits = attention_splits(p, max_sel);
     if (!attention_mma_fits(p, max_sel) || splits > ws.n_splits) return cudaErrorNotSupported;
     if (pool) {
-        if (g <= 8) return launch_hr<true, 1>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s, splits);
-        return launch_hr<true, 2>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s, splits);
+        if (g <= 8) return launch_hr<true, 1, false>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s, splits, SelArgs{});
+        return launch_hr<true, 2, false>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s, splits, SelArgs{});
     }
-    if (g <= 8) return launch_hr<false, 1>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s, splits);
-    return launch_hr<false, 2>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s, splits);
+    if (g <= 8) return launch_hr<false, 1, false>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s, splits, SelArgs{});
+    return launch_hr<false, 2, false>(p, pool, sel_pages, Q, kbuf, vbuf, buf_len, sel_count, max_sel, scale, O, ws, err, s, splits, SelArgs{});
 }
 
 }  // namespace ice

@@ -158,6 +158,11 @@ cudaError_t launch_attention(const ice_params &p, const ice_index *pool, const i
 // The same with the page contractions on warp-level MMAs (bf16, g <= 16).
 bool attention_mma_supported(const ice_params &p);
 bool attention_mma_fits(const ice_params &p, int max_sel);
+// The attention CTAs select their unit's pages first (from the score table).
+bool attention_mma_select_supported(const ice_params &p, int max_sel);
+cudaError_t launch_attention_mma_select(const ice_params &p, const ice_index &idx, const SelArgs &A, const void *Q,
+                                        void *kbuf, void *vbuf, int32_t *buf_len, int max_sel, float scale, float *O,
+                                        const DecodeWs &ws, int32_t *err, cudaStream_t s);
 cudaError_t launch_attention_mma(const ice_params &p, const ice_index *pool, const int32_t *sel_pages, const void *Q,
                                  void *kbuf, void *vbuf, int32_t *buf_len, const int32_t *sel_count, int max_sel,
                                  float scale, float *O, const DecodeWs &ws, int32_t *err, cudaStream_t s);
@@ -171,13 +176,12 @@ cudaError_t launch_decode_cluster(const ice_params &p, const ice_index &idx, con
                                   int32_t *sel_pages, int32_t *sel_count, int max_sel, void *kbuf, void *vbuf,
                                   int32_t *buf_len, float scale, float *O, int32_t *err, cudaStream_t s);
 
-// The whole decode step of every unit in one kernel: a cluster of CTAs per
-// unit scans the parent table (TMA + mma.sync, top-k kept on chip), forms the
-// union and attends over its pages (bf16, g <= 8, k <= 32).
-bool decode_fused_supported(const ice_params &p, int k_pages, int max_sel);
-cudaError_t launch_decode_fused(const ice_params &p, const ice_index &idx, const void *Q, int k_pages,
-                                int32_t *sel_pages, int32_t *sel_count, int max_sel, void *kbuf, void *vbuf,
-                                int32_t *buf_len, float scale, float *O, int32_t *err, cudaStream_t s);
+// The same for bf16 tables with g <= 8 and k <= 32 pages per head: bulk-copied
+// pages, bisection top-k, packed fp32-pair arithmetic.
+bool decode_cluster2_supported(const ice_params &p, int k_pages, int max_sel);
+cudaError_t launch_decode_cluster2(const ice_params &p, const ice_index &idx, const void *Q, int k_pages,
+                                   int32_t *sel_pages, int32_t *sel_count, int max_sel, void *kbuf, void *vbuf,
+                                   int32_t *buf_len, float scale, float *O, int32_t *err, cudaStream_t s);
 
 // Allocation-free attention: scratch in the library's static device array.
 size_t attention_noalloc_bytes(const ice_params &p, int max_sel);

@@ -178,13 +178,14 @@ def test_index_slab_layout(lib, levels, with_pool, dtype):
 
 
 def test_decode_plan_host_query(lib):
-    """ice_decode_plan answers on the host: bf16 with g <= 8 and k <= 32 takes
-    the fused kernel, 16 heads per group the score-table path, more than 32
-    pages per head the SIMT selection, three levels the descent."""
+    """ice_decode_plan answers on the host (where the SM count reads as 1, so
+    no cluster plan fits): bf16 with g <= 8 and k <= 32 takes the score table
+    and selecting attention CTAs, 16 heads per group the top-k kernel, more
+    than 32 pages per head the SIMT selection, three levels the descent."""
     base = dict(batch=1, n_q_heads=8, n_kv_heads=2, n_tokens=3000)
     plan = lambda cfg, budget: ice.ice_decode_plan(cfg.params(), budget, ice.max_selected(cfg, budget))[0]
-    assert plan(ice.Config(**base), 256) == ice.ICE_PLAN_FUSED
-    assert plan(ice.Config(**{**base, "n_q_heads": 32}), 256) == ice.ICE_PLAN_SCORE_TC
+    assert plan(ice.Config(**base), 256) == ice.ICE_PLAN_SCORE_SELECT
+    assert plan(ice.Config(**{**base, "n_q_heads": 32}), 256) == ice.ICE_PLAN_SCORE_TOPK
     assert plan(ice.Config(**base), 1024) == ice.ICE_PLAN_SIMT
     assert plan(ice.Config(**base, n_levels=3), 256) == ice.ICE_PLAN_DESCENT
     with pytest.raises(ice.IceError):

@@ -90,8 +90,8 @@ def test_fused_decode_equals_separate_calls():
 def test_decode_without_contiguous_buffer(shape):
     """ice_decode_step with kbuf = vbuf = buf_len = NULL gathers the pages on
     chip only: same page lists and bit-identical O as with the buffer, on
-    each kernel path (fp32 and bf16 per-unit clusters, tensor-core selection
-    with the streaming attention for many units)."""
+    each kernel path (fp32 and bf16 per-unit clusters, the tensor-core score
+    table with the selecting MMA attention for many units)."""
     w = {"tiny_fp32": W["tiny"],
          "llama_cluster": W["llama31_8b_16k"].scaled(n_tokens=3000, n_q_heads=8, n_kv_heads=2),
          "qwen_many_units": W["qwen3_32b_100k"].scaled(n_tokens=3000, batch=3, centres=256),
@@ -134,8 +134,8 @@ def test_many_units_take_select_and_attention_kernels():
 
 
 def test_one_attention_cta_per_unit():
-    """More units than SMs with a 128-page selection: the streaming attention
-    runs one CTA per unit and writes O directly (fused and separate calls)."""
+    """More units than SMs with a 128-page selection: the MMA attention runs
+    one CTA per unit and writes O directly (fused and separate calls)."""
     w = W["qwen3_32b_100k"].scaled(n_tokens=2200, batch=20, centres=128)
     run = DeviceRun(w)
     assert run.status == ice.ICE_OK
@@ -479,34 +479,36 @@ def test_reuse_with_sink_window_and_three_levels():
 
 
 @pytest.mark.parametrize("shape,budget,plan,attn", [
-    ("fused_one_cta_per_unit", 256, ice.ICE_PLAN_FUSED, ice.ICE_PLAN_ATTN_MMA),
-    ("fused_cluster_per_unit", 256, ice.ICE_PLAN_FUSED, ice.ICE_PLAN_ATTN_MMA),
-    ("score_tc_g16", 256, ice.ICE_PLAN_SCORE_TC, ice.ICE_PLAN_ATTN_MMA),
-    ("simt_select_k64_bf16", 1024, ice.ICE_PLAN_SIMT, ice.ICE_PLAN_ATTN_MMA),
+    ("cluster_bf16", 256, ice.ICE_PLAN_CLUSTER_BF16, ice.ICE_PLAN_ATTN_MMA),
+    ("cluster_bf16_k64", 1024, ice.ICE_PLAN_CLUSTER, ice.ICE_PLAN_ATTN_MMA),
     ("cluster_fp32", 64, ice.ICE_PLAN_CLUSTER, ice.ICE_PLAN_ATTN_SIMT),
+    ("score_select_many_units", 256, ice.ICE_PLAN_SCORE_SELECT, ice.ICE_PLAN_ATTN_MMA),
+    ("score_topk_g16", 256, ice.ICE_PLAN_SCORE_TOPK, ice.ICE_PLAN_ATTN_MMA),
+    ("simt_select_k64_bf16", 1024, ice.ICE_PLAN_SIMT, ice.ICE_PLAN_ATTN_MMA),
     ("simt_fp32_many_units", 64, ice.ICE_PLAN_SIMT, ice.ICE_PLAN_ATTN_SIMT),
     ("simt_attention_bf16", 1024, ice.ICE_PLAN_SIMT, ice.ICE_PLAN_ATTN_SIMT)])
 def test_every_decode_plan_against_the_oracle(shape, budget, plan, attn):
     """Each kernel path of ice_decode_step (ice_decode_plan names it) and
-    each attention kernel, on a shape that selects it: the fused decode with
-    one CTA and with a cluster per unit, the tensor-core score table with 16
-    query heads per group, the SIMT selection (more than 32 pages per head),
-    the fp32 cluster decode, the SIMT path for fp32 with many units, and the
-    SIMT attention when a warp would hold more than 32 pages.  The step
-    (fused call and separate calls) checked against the oracle."""
-    w = {"fused_one_cta_per_unit": W["qwen3_32b_100k"].scaled(n_tokens=2200, batch=20, centres=128),
-         "fused_cluster_per_unit": W["llama31_8b_16k"].scaled(n_tokens=3000, n_q_heads=8, n_kv_heads=2),
-         "score_tc_g16": W["llama31_8b_16k"].scaled(n_tokens=3000, n_q_heads=32, n_kv_heads=2),
-         "simt_select_k64_bf16": W["llama31_8b_16k"].scaled(n_tokens=3000, n_q_heads=8, n_kv_heads=2),
+    each attention kernel, on a shape that selects it: the bf16 and generic
+    cluster decodes, the score table with selecting attention CTAs and with
+    the top-k kernel (16 query heads per group), the SIMT selection (more than
+    32 pages per head) with the MMA and with the SIMT attention (a warp would
+    hold more than 32 pages), and fp32 with many units.  The step (fused call
+    and separate calls) checked against the oracle."""
+    w = {"cluster_bf16": W["llama31_8b_16k"].scaled(n_tokens=3000, n_q_heads=8, n_kv_heads=2),
+         "cluster_bf16_k64": W["llama31_8b_16k"].scaled(n_tokens=3000, n_q_heads=8, n_kv_heads=2),
          "cluster_fp32": W["tiny"],
+         "score_select_many_units": W["qwen3_32b_100k"].scaled(n_tokens=2200, batch=20, centres=128),
+         "score_topk_g16": W["llama31_8b_16k"].scaled(n_tokens=3000, batch=12, n_q_heads=32, n_kv_heads=2),
+         "simt_select_k64_bf16": W["llama31_8b_16k"].scaled(n_tokens=3000, batch=3),
          "simt_fp32_many_units": W["tiny"].scaled(n_tokens=1500, batch=20),
          "simt_attention_bf16": W["qwen3_32b_100k"].scaled(n_tokens=3000, batch=19, centres=128)}[shape]
     run = DeviceRun(w)
     assert run.status == ice.ICE_OK
     max_sel = ice.max_selected(run.cfg, budget)
     assert ice.ice_decode_plan(run.params, budget, max_sel) == (plan, attn)
-    units = range(run.cfg.units) if run.cfg.units <= 24 else (0, 7, 50, run.cfg.units - 1)
-    for u in (units if run.cfg.units <= 24 else units[:2]):
+    units = list(range(run.cfg.units)) if run.cfg.units <= 24 else [0, 7, 50, run.cfg.units - 1]
+    for u in units[:4]:
         check_build_unit(run, u)
     for fused in (True, False):
         Q, buf, st = run.decode(budget, fused=fused)
