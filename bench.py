@@ -68,9 +68,15 @@ def graph_kernel_nodes(graph):
 # DRAM bytes per launch of a kernel from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum) on the named workload, with the SHA-256 of the kernel's
 # source file at capture time; reported only while the source is unchanged.
+# The decode step's entry: the two kernels of ICE_PLAN_SCORE_SELECT captured at batch 4 (32 units) and scaled by the
+# units to the 16-sequence batch (per-unit traffic does not depend on the batch).
 TRAFFIC = {
-    "assign": {"workload": "llama31_8b_16k", "source": "build_assign_tc.cu", "bytes": 40956672,
-               "sha256": "e01fe4ae62b7ec7e6b47084d7878e058fb8969145da1313ee833a5079d099c20"},
+    "decode": {"workload": "qwen3_32b_100k", "bytes": 355_920_000, "sha256": {
+        "decode_select_tc.cu": "5e1e4a0892f65d8aecbe3f5687461d1b9b308934cf73e8a212cff45a9c692840",
+        "decode_attn_mma.cu": "5890e9079dee592cbf38972c8050902e24106fbe44c4dee16b5cb154160f82d1",
+        "select_unit.cuh": "5b83540e3d042384f7e8a297312ce0b3e67e1d2958029440004df99602df4055",
+        "attn_page.cuh": "85d342159d9748393e05de4c7a6239fd0aff82ae1638b53295ee21aa72426620",
+    }},
 }
 
 
@@ -79,12 +85,15 @@ def measured_traffic(kernel: str, workload: str):
     t = TRAFFIC.get(kernel)
     if not t or t["workload"] != workload:
         return None
-    src = os.path.join(ROOT, "semantic_paged_kv_gb300", "csrc", t["source"])
-    try:
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    except OSError:
-        return None
-    return t["bytes"] if sha == t["sha256"] else None
+    for name, want in t["sha256"].items():
+        src = os.path.join(ROOT, "semantic_paged_kv_gb300", "csrc", name)
+        try:
+            sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        except OSError:
+            return None
+        if sha != want:
+            return None
+    return t["bytes"]
 
 
 EXTRAS = ("build", "longchat", "longchat_b8", "qwen_levels3", "mistral_insert", "host_pool", "llama16k")
@@ -101,6 +110,7 @@ def parse():
     ap.add_argument("--budget", type=int, default=None)
     ap.add_argument("--layers", type=int, default=2, help="distinct layers rotated between timed steps")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-e2e", action="store_true", help="skip the pinned-host pool end-to-end part (profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-units", type=int, default=None, help="units in the CPU-baseline sample")
     ap.add_argument("--extras", default=",".join(EXTRAS), help="comma list of " + ", ".join(EXTRAS) + " (or none)")
@@ -742,6 +752,8 @@ def run_ours(args):
     # ---- end to end through the public API with host buffers (pinned host page pool)
     e2e, hp_extra = None, None
     try:
+        if args.no_e2e:
+            raise RuntimeError("skipped (--no-e2e)")
         e2e, hp_extra = host_pool_part(ice, pk, rp, w, budget, args.e2e_steps)
         slowest = max_over_ranks(e2e["ms_per_step"], world, "cuda")
         e2e["value"] = whole_job_rate(e2e.pop("bytes_per_step"), 1, world, slowest) / 1e9
@@ -791,7 +803,7 @@ def run_ours(args):
             "roofline": {"kernel": "ice_decode_step" + (" (1 kernel)" if kernels == 1 else f" ({kernels} kernels)"),
                          "bound": "hbm", "achieved": ach, "peak": pk["hbm"], "unit": "GB/s", "frac": ach / pk["hbm"],
                          "peak_source": pk["src"], "bytes_per_launch": int(bmin),
-                         "traffic": measured_traffic("decode", w.name)},
+                         "traffic": measured_traffic("decode", w.name) if w.batch == 16 else None},
             "index_build_keys_per_s": w.units * w.n_tokens / (build_ms * 1e-3),
             "e2e": e2e,
             "cpu_baseline": cpu,

@@ -515,3 +515,23 @@ def test_every_decode_plan_against_the_oracle(shape, budget, plan, attn):
         assert st == ice.ICE_OK
         for u in units:
             check_decode_unit(run, u, Q, budget, buf)
+
+
+def test_three_levels_many_level2_nodes():
+    """p = 1/2 on one 20,000-token unit: about 10,000 parents and 5,000
+    level-2 nodes, more than the descent keeps in shared memory (4,096), so
+    each head's level-2 scores go through the decode workspace.  Level 1,
+    level 2 and the descent selection (near-ties enumerated) against the
+    oracle, and the attention over the selected pages."""
+    w = W["llama31_8b_16k"].scaled(n_tokens=20000, n_q_heads=4, n_kv_heads=1, promote_p=0.5)
+    run = DeviceRun(w, n_levels=3)
+    assert run.status == ice.ICE_OK
+    assert int(run.h["n_nodes2"][0]) > 4096
+    idx = check_build_positional(run, 0)
+    lv2 = check_build_level2(run, 0, idx)
+    assert ice.ice_decode_plan(run.params, 256, ice.max_selected(run.cfg, 256))[0] == ice.ICE_PLAN_DESCENT
+    for bgt in (64, 256):
+        for fused in (True, False):
+            Q, buf, st = run.decode(bgt, fused=fused)
+            assert st == ice.ICE_OK
+            check_decode_descent(run, 0, Q, bgt, buf, lv2, idx)
