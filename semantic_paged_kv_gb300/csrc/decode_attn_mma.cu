@@ -124,6 +124,7 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
             my_len = buf_len[sl];
         }
     }
+    const uint64_t pol = l2_evict_first();  // each selected page is read once per step
     auto issue = [&](int k, int pid) {
         if (fault_skip) return;  // fault injection: the wait below gives up
         const int x = xs + warp + k * kMW;
@@ -131,10 +132,10 @@ __global__ void __launch_bounds__(kMT, 1) k_attn_mma(
         unsigned char *slot = S.kv[warp][k % kNS];
         unsigned long long *bar = &S.full[warp][k % kNS];
         mbar_expect_tx(bar, kSlotBytes);
-        tma_load_2d(slot, &tm_k, bar, 0, row);
-        tma_load_2d(slot + kHalfBytes, &tm_k, bar, 64, row);
-        tma_load_2d(slot + kTileBytes, &tm_v, bar, 0, row);
-        tma_load_2d(slot + kTileBytes + kHalfBytes, &tm_v, bar, 64, row);
+        tma_load_2d_hint(slot, &tm_k, bar, 0, row, pol);
+        tma_load_2d_hint(slot + kHalfBytes, &tm_k, bar, 64, row, pol);
+        tma_load_2d_hint(slot + kTileBytes, &tm_v, bar, 0, row, pol);
+        tma_load_2d_hint(slot + kTileBytes + kHalfBytes, &tm_v, bar, 64, row, pol);
     };
     if (kSel) __syncthreads();  // every warp has its page ids before the slots fill
     {

@@ -27,14 +27,13 @@
 //              and the maximum of each 32-parent group to [unit][head][group].
 //   The kernel streams the parent table once; its extra traffic is the score
 //   table (g x 4 bytes per 256-byte parent row).
-// k_select_topk: one CTA per unit, one warp per query head.  The kc-th
-//   largest group maximum T0 is a lower bound of the kc-th best score (kc
-//   groups reach it), so the best kc keys (score, -m) all lie in the groups
-//   whose maximum is >= T0 (about kc of them): T0 by bisection on the group
-//   maxima, then only those groups' scores are read, the keys >= T0 sorted
-//   into the ordered best kc (their page spans load during the sort), whose
-//   pages (k per head) are ORed into the union bitmask; the block writes the
-//   ascending page list.  The kernel is a short chain of dependent loads; it
+// k_select_topk: one CTA per unit, one warp per query head (select_unit).  Any
+//   group maximum T0 that kc group maxima reach is a lower bound of the kc-th
+//   best score, so the best kc keys (score, -m) all lie in the groups whose
+//   maximum is >= T0: T0 by a radix search on the group maxima, then only
+//   those groups' scores are read, the keys >= T0 put in order (their page
+//   spans load meanwhile), whose pages (k per head) are ORed into the union
+//   bitmask; the block writes the ascending page list.  The kernel is a short chain of dependent loads; it
 //   runs after the streaming kernel so that the chain sees an idle memory
 //   system (inside the streaming kernel each load waited ~2.5 us).
 // Every mbarrier wait gives up after ~2 s and records ICE_ERR_TIMEOUT; the
@@ -155,6 +154,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer
         if (lane == 0) {
+            // the parent rows are read once: evicted first, so the score
+            // table stays in L2 for the selection that reads it back
+            const uint64_t pol = l2_evict_first();
             int gt = 0, sv = 0;
             for (long long it = it_begin; ok && it < it_end;) {
                 const Seg S = seg_at(it, it_end, T, np_cap, n_parents);
@@ -179,8 +181,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const int y = S.u * np_cap + t * BM;
                     mbar_expect_tx(&bars->full[s], A_BYTES);
-                    tma_load_2d(sA + s * A_BYTES, &tmP, &bars->full[s], 0, y);
-                    tma_load_2d(sA + s * A_BYTES + A_HALF, &tmP, &bars->full[s], 64, y);
+                    tma_load_2d_hint(sA + s * A_BYTES, &tmP, &bars->full[s], 0, y, pol);
+                    tma_load_2d_hint(sA + s * A_BYTES + A_HALF, &tmP, &bars->full[s], 64, y, pol);
                 }
             }
             // drain: every issued copy has landed before the CTA may exit

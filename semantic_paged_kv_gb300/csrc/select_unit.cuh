@@ -7,12 +7,14 @@
 // Order (-score, m) over parents, pages of a parent in page-id order, k pages
 // per head, union as a bitmask, then the ascending page list.
 //
-// The kc-th largest group maximum T0 is a lower bound of the kc-th best score
-// (kc groups reach it), so the best kc keys (score, -m) all lie in the groups
-// whose maximum is >= T0 (about kc of them): T0 by bisection on the group
-// maxima, then only those groups' scores are read, the keys >= T0 sorted into
-// the ordered best kc (their page spans load during the sort), whose pages
-// are ORed into the union bitmask.
+// Any group maximum T0 that at least kc group maxima reach is a lower bound
+// of the kc-th best score (each of those groups holds a score >= T0), so the
+// best kc keys (score, -m) all lie in the groups whose maximum is >= T0: T0
+// by a radix-4 search on the group maxima that stops once at most kc + 8
+// groups reach it, then only those groups' scores are read (32 groups' loads
+// in flight), the keys >= T0 are put in order (up to 32 of them by counting
+// each key's rank, more by a sorting network; their page spans load
+// meanwhile), and the pages of the best kc are ORed into the union bitmask.
 #pragma once
 
 #include "common.cuh"
@@ -27,6 +29,7 @@ using namespace topk;
 constexpr int kMaxKc = 32;  // best keys per query head: one per lane of a warp
 constexpr int kCand = 256;  // candidate keys a warp collects (more: exact slow path)
 constexpr int kGroup = 32;  // parents per group maximum
+constexpr int kSlack = 8;   // groups allowed above kc at the threshold T0
 
 __device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 
@@ -136,7 +139,7 @@ __device__ int select_unit(const SelArgs &A, int u, int tid, unsigned *s_mask, u
         float t0 = -INFINITY;
         if (ng >= kc) {
             if (ng <= 8 * 32) {
-                t0 = unord_f32(kth_largest_ord(v, kc));
+                t0 = unord_f32(kth_bound_ord(v, kc, kSlack));
             } else {  // more groups: stretches of 256 with a running bound
                 uint32_t res = 0u;
                 for (int x0 = 0; x0 < ng; x0 += 8 * 32) {
@@ -174,43 +177,82 @@ __device__ int select_unit(const SelArgs &A, int u, int tid, unsigned *s_mask, u
                 else
                     gm[i] = x < ng ? __ldcg(gh + x) : -INFINITY;
             }
-            // the qualifying groups of this stretch, in order
+            // the qualifying groups of this stretch, in order: the ballots
+            // first, then their slots
+            unsigned bl[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) bl[i] = __ballot_sync(0xffffffffu, gm[i] >= t0);
             int ngl = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const unsigned b = __ballot_sync(0xffffffffu, gm[i] >= t0);
-                if (((b >> lane) & 1u) && ngl + __popc(b & lanemask_lt()) < 128)
-                    glist[ngl + __popc(b & lanemask_lt())] = x0 + i * 32 + lane;
-                ngl += __popc(b);
+                const int at = ngl + __popc(bl[i] & lanemask_lt());
+                if (((bl[i] >> lane) & 1u) && at < 128) glist[at] = x0 + i * 32 + lane;
+                ngl += __popc(bl[i]);
             }
             __syncwarp();
             if (ngl > 128) {  // very many ties with T0: exact slow path below
                 cnt = kCand + 1;
                 break;
             }
-            for (int j0 = 0; j0 < ngl; j0 += 16) {  // 16 groups' loads in flight at once
-                float sv[16];
+            for (int j0 = 0; j0 < ngl; j0 += 32) {  // 32 groups' loads in flight at once
+                float sv[32];
+                unsigned pass = 0u;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
+                for (int i = 0; i < 32; ++i) {
                     const int m = j0 + i < ngl ? glist[j0 + i] * kGroup + lane : Np;
                     sv[i] = m < Np ? __ldcg(sh + m) : -INFINITY;
+                    pass |= (m < Np ? 1u : 0u) << i;
                 }
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int m = j0 + i < ngl ? glist[j0 + i] * kGroup + lane : Np;
-                    const bool pass = m < Np && sv[i] >= t0;
-                    const unsigned bal = __ballot_sync(0xffffffffu, pass);
-                    const int at = cnt + __popc(bal & lanemask_lt());
-                    if (pass && at < kCand - 64) cand[at] = sort_key(sv[i], m);
-                    cnt += __popc(bal);
+                for (int i = 0; i < 32; ++i) pass &= ~((sv[i] >= t0 ? 0u : 1u) << i);
+                // this lane's keys >= T0 go to consecutive slots after the
+                // lower lanes' (one warp scan of the counts)
+                const int c = __popc(pass);
+                int incl = c;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+                    if (lane >= off) incl += o;
                 }
+                int at = cnt + incl - c;
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if ((pass >> i) & 1u) {
+                        if (at < kCand - 64) cand[at] = sort_key(sv[i], glist[j0 + i] * kGroup + lane);
+                        ++at;
+                    }
+                cnt += __shfl_sync(0xffffffffu, incl, 31);
             }
             __syncwarp();
         }
         __syncwarp();
         // lane r < kc: the r-th best parent and its pages
         int pm = -1, fp = 0, pc = 0, contig = 1;
-        if (cnt <= 64) {
+        if (cnt <= 32) {
+            // lane i holds candidate i; its rank is the number of larger keys
+            // (keys are distinct); the candidates' page spans load meanwhile
+            const unsigned long long key = lane < cnt ? cand[lane] : 0ull;
+            int4 sp = make_int4(0, 0, 0, 0);
+            if (key != 0ull) {
+                const int m = key_id(key);
+                sp = make_int4(A.parent_first_page[up + m], A.parent_n_pages[up + m], A.parent_last_page[up + m], m);
+            }
+            int rank = 0;
+            for (int j = 0; j < cnt; ++j) rank += cand[j] > key ? 1 : 0;
+            int *s_src = glist;  // the group list is spent: lane of the r-th best key
+            __syncwarp();
+            if (key != 0ull) s_src[rank] = lane;
+            __syncwarp();
+            const int src = lane < cnt ? s_src[lane] : 0;
+            const int4 s = make_int4(__shfl_sync(0xffffffffu, sp.x, src), __shfl_sync(0xffffffffu, sp.y, src),
+                                     __shfl_sync(0xffffffffu, sp.z, src), __shfl_sync(0xffffffffu, sp.w, src));
+            if (lane < cnt && lane < kc) {
+                pm = s.w;
+                fp = s.x;
+                pc = s.y;
+                contig = s.z - s.x + 1 == s.y;
+            }
+        } else if (cnt <= 64) {
             // the candidates' page spans load while the keys sort; a key's low
             // byte holds its slot in the list
             unsigned long long w[2];

@@ -63,6 +63,22 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
         "l"(reinterpret_cast<uint64_t>(map)), "r"(su32(bar)), "r"(x), "r"(y)
         : "memory");
 }
+// An L2 policy for data read once (a stream): its lines are the first to be
+// evicted, so that the stream does not push out lines read again soon.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+// tma_load_2d with an L2 cache policy (l2_evict_first()).
+__device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *map, unsigned long long *bar, int x,
+                                                 int y, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, "
+        "%4}], [%2], %5;" ::"r"(su32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(su32(bar)), "r"(x), "r"(y), "l"(pol)
+        : "memory");
+}
 // 2-D TMA store of a shared-memory tile (the map's box and swizzle) to global.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int x, int y) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(

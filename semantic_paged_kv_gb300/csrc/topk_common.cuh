@@ -52,6 +52,65 @@ __device__ __forceinline__ uint32_t kth_largest_ord(const uint32_t (&v)[8], int 
     return r;
 }
 
+// A threshold T (order-preserving form) that at least kc of the warp's values
+// (8 per lane, 0 = none; kc <= 32 and at least kc values present) reach, and
+// at most kc + slack unless ties force more; T is itself one of the values.
+// The kc-th largest lies between lo, the smallest of the lanes' maxima (kc or
+// more values reach it), and the maximum hi, so the bits above their first
+// difference are those of hi; the remaining bits are fixed two at a time from
+// the top (three counts per step), and the search stops once at most
+// kc + slack values reach the prefix.  T is then the least value at or above
+// the prefix.
+__device__ __forceinline__ uint32_t kth_bound_ord(const uint32_t (&v)[8], int kc, int slack) {
+    uint32_t lm = 0u;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) lm = max(lm, v[e]);
+    const uint32_t hi = __reduce_max_sync(0xffffffffu, lm);
+    const uint32_t lo = __reduce_min_sync(0xffffffffu, lm != 0u ? lm : 0xFFFFFFFFu);
+    int nb = lo >= hi ? 0 : 32 - __clz(lo ^ hi);  // open low bits
+    uint32_t r = nb >= 32 ? 0u : (hi >> nb) << nb;
+    int nr = 0x7FFFFFFF;  // values >= r (unknown until a step raises r)
+    while (nb > 0 && nr > kc + slack) {
+        if (nb >= 2) {
+            const int b = nb - 2;
+            const uint32_t c1 = r | (1u << b), c2 = r | (2u << b), c3 = r | (3u << b);
+            unsigned a1 = 0, a2 = 0, a3 = 0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                a1 += v[e] >= c1;
+                a2 += v[e] >= c2;
+                a3 += v[e] >= c3;
+            }
+            const int n1 = (int)__reduce_add_sync(0xffffffffu, a1);
+            const int n2 = (int)__reduce_add_sync(0xffffffffu, a2);
+            const int n3 = (int)__reduce_add_sync(0xffffffffu, a3);
+            if (n3 >= kc) {
+                r = c3;
+                nr = n3;
+            } else if (n2 >= kc) {
+                r = c2;
+                nr = n2;
+            } else if (n1 >= kc) {
+                r = c1;
+                nr = n1;
+            }
+            nb = b;
+        } else {
+            const uint32_t c1 = r | 1u;
+            unsigned a1 = 0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) a1 += v[e] >= c1;
+            const int n1 = (int)__reduce_add_sync(0xffffffffu, a1);
+            if (n1 >= kc) r = c1;
+            nb = 0;
+        }
+    }
+    uint32_t mn = 0xFFFFFFFFu;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) mn = v[e] >= r && v[e] != 0u ? min(mn, v[e]) : mn;
+    return __reduce_min_sync(0xffffffffu, mn);
+}
+
 // Descending bitonic sort of the warp's 64 keys: key i in lane i % 32 of v[i / 32].
 __device__ __forceinline__ void sort64_desc(unsigned long long (&v)[2]) {
     const int lane = threadIdx.x & 31;
