@@ -66,16 +66,21 @@ def graph_kernel_nodes(graph):
 
 
 # DRAM bytes per launch of a kernel from one ncu capture (dram__bytes_read.sum +
-# dram__bytes_write.sum) on the named workload, with the SHA-256 of the kernel's
-# source file at capture time; reported only while the source is unchanged.
+# dram__bytes_write.sum) on the named workload, with the SHA-256 of the source files
+# the kernels and their launcher are built from; reported only while they are unchanged.
 # The decode step's entry: the two kernels of ICE_PLAN_SCORE_SELECT captured at batch 4 (32 units) and scaled by the
 # units to the 16-sequence batch (per-unit traffic does not depend on the batch).
 TRAFFIC = {
-    "decode": {"workload": "qwen3_32b_100k", "bytes": 355_920_000, "sha256": {
-        "decode_select_tc.cu": "5e1e4a0892f65d8aecbe3f5687461d1b9b308934cf73e8a212cff45a9c692840",
-        "decode_attn_mma.cu": "5890e9079dee592cbf38972c8050902e24106fbe44c4dee16b5cb154160f82d1",
-        "select_unit.cuh": "5b83540e3d042384f7e8a297312ce0b3e67e1d2958029440004df99602df4055",
+    "decode": {"workload": "qwen3_32b_100k", "bytes": 354_127_872, "sha256": {
+        "decode_select_tc.cu": "e1bb3c659f0a7ca618e4e526d2725e7008a7810019a25cc7f8f535f55bfebc75",
+        "decode_attn_mma.cu": "adaf3b86ba0647e99d7664b24e7e609cd3ab60f41722da3e7f3a5780c6ba3b4c",
+        "select_unit.cuh": "e9fb950a3869e70bb5b99941bbe3a5caa9f6d8414d43b7dc983ecc0ce5e5c767",
         "attn_page.cuh": "85d342159d9748393e05de4c7a6239fd0aff82ae1638b53295ee21aa72426620",
+        "tc_common.cuh": "bcc9600b9d3aaad4c363c2b9ce954eb63042c1c048f1de44ffffcd2b99354924",
+        "topk_common.cuh": "a0f2a6e40e018342dac4bb206612512047305897c042194378bd515af705f02c",
+        "common.cuh": "53dc15cf41d59e44bc74139d9b0186fadd82c77de4300f0bf51cdbad59c77fd7",
+        "internal.h": "d219025c74377dd8f9e11d923f0e86f66ce2550c253f84a76b8d32364939ab7f",
+        "abi.cu": "b59a4af786ba69638338aeab3e17defe18d08e634665209de73565912c09a6db",
     }},
 }
 
@@ -325,7 +330,9 @@ def config_of(w, budget, gpus, layers):
             "n_tokens": w.n_tokens, "head_dim": w.head_dim, "page_size": w.page_size, "promote_p": w.promote_p,
             "levels": 2, "budget_tokens": budget, "parallelism": f"dp{gpus}",
             "gather": "selected pages into shared memory (contiguous buffer: extra.buffer)",
-            "l2": f"{layers} layers rotated, each step reads > 2.5x L2"}
+            "l2": f"{layers} layers rotated (distinct K/V, index, queries), each step reads > 2.5x L2",
+            "graph": f"one CUDA graph per pass over the {layers} layers (one decode step each)",
+            "workspace": "one decode workspace and output set for all layers, as one stream reuses them"}
 
 
 # ------------------------------------------------- multi-rank host logic ---
@@ -690,26 +697,45 @@ def run_ours(args):
     w = rank_workload(args.workload, rank, args.batch)
     budget = args.budget or max(w.budgets)
     E = lambda: torch.cuda.Event(enable_timing=True)
-    # ---- the layers: distinct K/V (and index) per layer, rotated between steps
+    # ---- the layers: distinct K/V, index and queries per layer, one decode
+    # workspace and one set of outputs for all of them (one stream runs the
+    # layers one after another, as a serving engine does); one CUDA graph
+    # holds one decode step of every layer
     layers = []
     for layer in range(max(1, args.layers)):
-        L = build_layer(ice, w, layer=layer)
-        L["buf"] = ice.DecodeBuffers(L["cfg"], budget)
-        layers.append(L)
+        layers.append(build_layer(ice, w, layer=layer))
         torch.cuda.empty_cache()
+    buf = ice.DecodeBuffers(layers[0]["cfg"], budget)
+    nl = len(layers)
+    for L in layers:  # each layer's step once: its selection gives its bytes
+        decode_call(ice, L, budget, buf, False)()
+        torch.cuda.synchronize()
+        L["bytes"] = decode_bytes(L, buf, w)
+        L["n_sel"] = int(buf.sel_count.sum())
     rp = Replay(args.reps)
-    for L in layers:
-        L["g"] = rp.graph(decode_call(ice, L, budget, L["buf"], False))
-        L["g_buf"] = rp.graph(decode_call(ice, L, budget, L["buf"], True))
+    steps_of = lambda with_buffer: lambda: [decode_call(ice, L, budget, buf, with_buffer)() for L in layers]
+    g_all, g_all_buf = rp.graph(steps_of(False)), rp.graph(steps_of(True))
+    for L in layers:  # single-layer graphs for a step count that is not a multiple of the layers
+        L["g"] = rp.graph(decode_call(ice, L, budget, buf, False))
+        L["g_buf"] = rp.graph(decode_call(ice, L, budget, buf, True))
+    full, rest = divmod(args.steps, nl)
+
+    def run_steps(with_buffer: bool):
+        g = g_all_buf if with_buffer else g_all
+        for _ in range(full):
+            g.replay()
+        for i in range(rest):
+            layers[i]["g_buf" if with_buffer else "g"].replay()
+
     for i in range(max(args.warmup, 3)):
-        layers[i % len(layers)]["g"].replay()
+        g_all.replay()
     torch.cuda.synchronize()
     for L in layers:
         st = ice.ice_check(L["err"])
         if st != ice.ICE_OK:
             raise SystemExit(f"device reported status {st}: {ice.ice_status_string(st)}")
 
-    # ---- timed region: exactly `steps` decode steps, one graph replay each
+    # ---- timed region: exactly `steps` decode steps (full passes over the layers, then the rest)
     sampler = ClockSampler(gpu_id_for(local))
     barrier()
     torch.cuda.synchronize()
@@ -717,15 +743,13 @@ def run_ours(args):
     time.sleep(0.15)
     t0, t1 = E(), E()
     t0.record()
-    for i in range(args.steps):
-        layers[i % len(layers)]["g"].replay()
+    run_steps(False)
     t1.record()
     torch.cuda.synchronize()
     # the same steps writing the contiguous buffer (kbuf / vbuf / buf_len) as well
     t2, t3 = E(), E()
     t2.record()
-    for i in range(args.steps):
-        layers[i % len(layers)]["g_buf"].replay()
+    run_steps(True)
     t3.record()
     torch.cuda.synchronize()
     barrier()
@@ -733,20 +757,23 @@ def run_ours(args):
     elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world, "cuda")
     buf_ms = max_over_ranks(t2.elapsed_time(t3), world, "cuda")
     ms_step = elapsed_ms / args.steps
-    bmin = float(np.mean([decode_bytes(L, L["buf"], w)[0] for L in layers]))
-    bbuf = float(np.mean([decode_bytes(L, L["buf"], w)[1] for L in layers]))
+    # bytes of the timed steps: layer i % nl at step i
+    per_step = [layers[i % nl]["bytes"] for i in range(nl)]
+    bmin = float(np.mean([b[0] for b in per_step]))
+    bbuf = float(np.mean([b[1] for b in per_step]))
     value = whole_job_rate(bmin, args.steps, world, elapsed_ms) / 1e9  # GB/s
-    kernels = graph_kernel_nodes(layers[0]["g"])
+    kernels = graph_kernel_nodes(layers[0]["g"])  # kernels of one step
+    k_all = graph_kernel_nodes(g_all)
+    launches = (k_all * full + (kernels or 0) * rest) if k_all is not None else None
     # per-step spread (median, p10, p90) with an L2 flush before each replay
-    spread = rp(decode_call(ice, layers[0], budget, layers[0]["buf"], False)) if rank == 0 else None
+    spread = rp(decode_call(ice, layers[0], budget, buf, False)) if rank == 0 else None
     sel_only = rp(lambda: ice.ice_select_pages(layers[0]["p"], layers[0]["idx"], layers[0]["Q"], budget,
-                                               layers[0]["buf"].sel_pages, layers[0]["buf"].sel_count,
-                                               layers[0]["buf"].ws, layers[0]["err"])) if rank == 0 else None
+                                               buf.sel_pages, buf.sel_count, buf.ws, layers[0]["err"])) if rank == 0 else None
     build_ms = float(np.mean([L["build_ms"] for L in layers]))
     n_par = int(layers[0]["idx"].n_parents.sum())
-    n_sel = int(layers[0]["buf"].sel_count.sum())
+    n_sel = layers[0]["n_sel"]
     status = ice.ice_status_string(ice.ice_check(layers[0]["err"]))
-    del layers, L
+    del layers, L, buf, g_all, g_all_buf
     torch.cuda.empty_cache()
 
     # ---- end to end through the public API with host buffers (pinned host page pool)
@@ -807,7 +834,7 @@ def run_ours(args):
             "index_build_keys_per_s": w.units * w.n_tokens / (build_ms * 1e-3),
             "e2e": e2e,
             "cpu_baseline": cpu,
-            "gpu_launches": (kernels or 0) * args.steps,
+            "gpu_launches": launches,
             "clocks": clocks,
             "device_status": status,
             "extra": extra,
@@ -834,7 +861,8 @@ def compact(d: dict) -> dict:
     out["config"] = {"workload": c["workload"], "batch_per_gpu": c["batch_per_gpu"],
                      "heads": f"{c['n_q_heads']}/{c['n_kv_heads']}", "n_tokens": c["n_tokens"],
                      "budget_tokens": c["budget_tokens"], "levels": 2, "parallelism": c["parallelism"],
-                     "gather": "smem", "l2": c["l2"]}
+                     "gather": "smem", "l2": c["l2"].split(" (")[0] + ", > 2.5x L2 per step",
+                     "graph": "one per pass over the layers", "workspace": "shared by the layers"}
     out["decode_step_us"] = r3(d["decode_step_us"])
     rf = d["roofline"]
     out["roofline"] = {"kernel": rf["kernel"], "bound": "hbm", "achieved": r3(rf["achieved"]), "peak": rf["peak"],

@@ -37,6 +37,16 @@ ice_status cuda_status(cudaError_t e, const char *where) {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Whether p points to device memory (not pinned host memory mapped for the GPU).
+bool in_device_memory(const void *p) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeDevice;
+}
+
 }  // namespace
 
 bool fault_armed(const char *what) {
@@ -618,9 +628,15 @@ ice_status ice_decode_step(const ice_params *p, const ice_index *idx, const void
         break;
     case ICE_PLAN_SCORE_SELECT:  // the score table, then attention CTAs that select their unit's pages
         e = launch_score_tc(*p, *idx, Q, w, err_dev, s);
-        if (e == cudaSuccess)
-            e = launch_attention_mma_select(*p, *idx, select_args(*p, *idx, w, sel_pages, sel_count, max_sel, err_dev),
-                                            Q, kbuf, vbuf, buf_len, max_sel, scale, O, w, err_dev, s);
+        if (e == cudaSuccess) {
+            SelArgs A = select_args(*p, *idx, w, sel_pages, sel_count, max_sel, err_dev);
+            if (in_device_memory(idx->pool_k) && in_device_memory(idx->pool_v)) {  // not a host page pool
+                A.pf_k = static_cast<const unsigned char *>(idx->pool_k);
+                A.pf_v = static_cast<const unsigned char *>(idx->pool_v);
+                A.page_bytes = kPage * kHeadDim * 2;  // bf16
+            }
+            e = launch_attention_mma_select(*p, *idx, A, Q, kbuf, vbuf, buf_len, max_sel, scale, O, w, err_dev, s);
+        }
         return cuda_status(e, "ice_decode_step");
     default:
         break;

@@ -330,6 +330,8 @@ SelArgs select_args(const ice_params &p, const ice_index &idx, const DecodeWs &w
     A.sel_pages = sel_pages;
     A.sel_count = sel_count;
     A.err = err;
+    A.pf_k = A.pf_v = nullptr;
+    A.page_bytes = 0;
     return A;
 }
 

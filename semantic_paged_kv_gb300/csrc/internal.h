@@ -86,6 +86,11 @@ struct SelArgs {
     const float *scores, *gmax;
     const int32_t *parent_first_page, *parent_last_page, *parent_n_pages, *page_next;
     int32_t *sel_pages, *sel_count, *err;
+    // the decode step's page pools (device memory): each query head's first
+    // kPrefetchPages pages are prefetched into L2 as soon as they are known
+    // (NULL: no prefetch)
+    const unsigned char *pf_k, *pf_v;
+    int page_bytes;
 };
 
 // with_select = false: the attention part only (no selection scratch).

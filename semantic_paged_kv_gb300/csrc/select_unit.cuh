@@ -11,7 +11,7 @@
 // of the kc-th best score (each of those groups holds a score >= T0), so the
 // best kc keys (score, -m) all lie in the groups whose maximum is >= T0: T0
 // by a radix-4 search on the group maxima that stops once at most kc + 8
-// groups reach it, then only those groups' scores are read (32 groups' loads
+// groups reach it, then only those groups' scores are read (16 groups' loads
 // in flight), the keys >= T0 are put in order (up to 32 of them by counting
 // each key's rank, more by a sorting network; their page spans load
 // meanwhile), and the pages of the best kc are ORed into the union bitmask.
@@ -30,6 +30,7 @@ constexpr int kMaxKc = 32;  // best keys per query head: one per lane of a warp
 constexpr int kCand = 256;  // candidate keys a warp collects (more: exact slow path)
 constexpr int kGroup = 32;  // parents per group maximum
 constexpr int kSlack = 8;   // groups allowed above kc at the threshold T0
+constexpr int kPrefetchPages = 3;  // first pages of each head prefetched into L2 (decode step)
 
 __device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 
@@ -194,17 +195,17 @@ __device__ int select_unit(const SelArgs &A, int u, int tid, unsigned *s_mask, u
                 cnt = kCand + 1;
                 break;
             }
-            for (int j0 = 0; j0 < ngl; j0 += 32) {  // 32 groups' loads in flight at once
-                float sv[32];
+            for (int j0 = 0; j0 < ngl; j0 += 16) {  // 16 groups' loads in flight at once
+                float sv[16];
                 unsigned pass = 0u;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
+                for (int i = 0; i < 16; ++i) {
                     const int m = j0 + i < ngl ? glist[j0 + i] * kGroup + lane : Np;
                     sv[i] = m < Np ? __ldcg(sh + m) : -INFINITY;
                     pass |= (m < Np ? 1u : 0u) << i;
                 }
 #pragma unroll
-                for (int i = 0; i < 32; ++i) pass &= ~((sv[i] >= t0 ? 0u : 1u) << i);
+                for (int i = 0; i < 16; ++i) pass &= ~((sv[i] >= t0 ? 0u : 1u) << i);
                 // this lane's keys >= T0 go to consecutive slots after the
                 // lower lanes' (one warp scan of the counts)
                 const int c = __popc(pass);
@@ -216,7 +217,7 @@ __device__ int select_unit(const SelArgs &A, int u, int tid, unsigned *s_mask, u
                 }
                 int at = cnt + incl - c;
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
+                for (int i = 0; i < 16; ++i)
                     if ((pass >> i) & 1u) {
                         if (at < kCand - 64) cand[at] = sort_key(sv[i], glist[j0 + i] * kGroup + lane);
                         ++at;
@@ -309,6 +310,16 @@ __device__ int select_unit(const SelArgs &A, int u, int tid, unsigned *s_mask, u
             if (lane >= off) incl += o;
         }
         const int tk = max(0, min(pc, k_pages - (incl - pc)));
+        // the head's first pages into L2 while the union and the list are
+        // formed: the stream of the decode step starts from there
+        if (A.pf_k != nullptr && pm >= 0 && contig && incl - pc < kPrefetchPages && tk > 0 && fp >= 0 &&
+            fp + tk <= Ps) {
+            const int npf = min(tk, kPrefetchPages - (incl - pc));
+            const size_t off = ((size_t)u * A.page_cap + fp) * (size_t)A.page_bytes;
+            const unsigned sz = (unsigned)(npf * A.page_bytes);
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(A.pf_k + off), "r"(sz) : "memory");
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(A.pf_v + off), "r"(sz) : "memory");
+        }
         int pg = fp;
         for (int i = 0; i < tk; ++i) {
             const int qq = contig ? fp + i : pg;
