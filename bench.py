@@ -101,7 +101,7 @@ def measured_traffic(kernel: str, workload: str):
     return t["bytes"]
 
 
-EXTRAS = ("build", "longchat", "longchat_b8", "qwen_levels3", "mistral_insert", "host_pool", "llama16k")
+EXTRAS = ("build", "separate", "longchat", "longchat_b8", "qwen_levels3", "mistral_insert", "host_pool", "llama16k")
 
 
 def parse():
@@ -454,6 +454,29 @@ def decode_bytes(L, buf, w) -> tuple[int, int]:
     return decode_min_bytes(npar, nsel, w.batch, w.n_q_heads), nsel * S * D * 2 * 2
 
 
+def separate_calls(ice, pk, rp, L, buf, budget, w):
+    """Steps a6-a8, a9 and a10 as the three separate calls on one layer, each
+    timed as one replay after an L2 flush: the selection (parent rows read
+    once), the gather (the selected pages read from the pool and written to
+    the contiguous buffer) and the attention over the buffer (read once), with
+    HBM GB/s on each call's algorithmic bytes against the measured copy peak."""
+    scale = 1.0 / math.sqrt(D)
+    p, idx, Q = L["p"], L["idx"], L["Q"]
+    sel = rp(lambda: ice.ice_select_pages(p, idx, Q, budget, buf.sel_pages, buf.sel_count, buf.ws, L["err"]))
+    nsel, npar = int(buf.sel_count.sum()), int(idx.n_parents.sum())
+    gat = rp(lambda: ice.ice_gather_pages(p, idx, buf.sel_pages, buf.sel_count, buf.kbuf, buf.vbuf, buf.buf_len))
+    att = rp(lambda: ice.ice_sparse_attn_decode(p, Q, buf.kbuf, buf.vbuf, buf.buf_len, buf.sel_count, scale, buf.O,
+                                                buf.ws))
+    page = S * D * 2 * 2  # K and V of one page, bf16
+    qo = w.batch * w.n_q_heads * D * (2 + 4)
+    b_sel, b_gat, b_att = npar * D * 2 + w.batch * w.n_q_heads * D * 2, 2 * nsel * page, nsel * page + qo
+    rate = lambda b, t: b / (t["us"] * 1e-6) / 1e9
+    return {"select_us": r3(sel["us"]), "select_gbs": r3(rate(b_sel, sel)),
+            "gather_us": r3(gat["us"]), "gather_gbs": r3(rate(b_gat, gat)), "gather_frac": r3(rate(b_gat, gat) / pk["hbm"]),
+            "attn_us": r3(att["us"]), "attn_gbs": r3(rate(b_att, att)), "attn_frac": r3(rate(b_att, att) / pk["hbm"]),
+            "bytes": {"select": b_sel, "gather": b_gat, "attn": b_att}}
+
+
 def r3(x):
     """Three significant digits (compact JSON)."""
     if x is None or isinstance(x, (int, str)) or not math.isfinite(x):
@@ -769,6 +792,8 @@ def run_ours(args):
     spread = rp(decode_call(ice, layers[0], budget, buf, False)) if rank == 0 else None
     sel_only = rp(lambda: ice.ice_select_pages(layers[0]["p"], layers[0]["idx"], layers[0]["Q"], budget,
                                                buf.sel_pages, buf.sel_count, buf.ws, layers[0]["err"])) if rank == 0 else None
+    wanted = set(x for x in args.extras.split(",") if x) if args.extras != "none" else set()
+    separate = separate_calls(ice, pk, rp, layers[0], buf, budget, w) if rank == 0 and "separate" in wanted else None
     build_ms = float(np.mean([L["build_ms"] for L in layers]))
     n_par = int(layers[0]["idx"].n_parents.sum())
     n_sel = layers[0]["n_sel"]
@@ -796,7 +821,8 @@ def run_ours(args):
     if spread:
         extra["step"] = {"p10_us": r3(spread["p10"]), "med_us": r3(spread["us"]), "p90_us": r3(spread["p90"]),
                          "select_us": r3(sel_only["us"])}
-    wanted = set(x for x in args.extras.split(",") if x) if args.extras != "none" else set()
+    if separate:
+        extra["separate"] = separate
     if rank == 0:
         parts = [("longchat", lambda: extra_longchat(ice, pk, rp, 1)),
                  ("longchat_b8", lambda: extra_longchat(ice, pk, rp, 8)),
@@ -886,6 +912,8 @@ def compact(d: dict) -> dict:
                 "lc_assign_frac": g("longchat", "assign", "frac"),
                 "lc8": [g("longchat_b8", "d256", "us"), g("longchat_b8", "d256", "frac")],
                 "lv3_us": g("qwen_levels3", "us"), "ins_us": g("mistral_insert", "insert_us"),
+                "sep": [g("separate", "gather_us"), g("separate", "gather_frac"), g("separate", "attn_us"),
+                        g("separate", "attn_frac")],
                 "l16k": [g("llama16k", "build_us"), g("llama16k", "decode_us"), g("llama16k", "assign_frac")],
                 "link": [g("host_pool", "link_peak_gbs"), g("host_pool", "bulk_frac"), g("host_pool", "direct_frac")]}
     return out
