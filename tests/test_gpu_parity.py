@@ -435,7 +435,7 @@ def test_three_levels_build_and_descent(shape, n_sink, n_window):
     w = {"llama_bf16": W["llama31_8b_16k"].scaled(n_tokens=6003, batch=2, n_q_heads=8, n_kv_heads=2, centres=512),
          "tiny_fp32": W["tiny"],
          "many_units": W["qwen3_32b_100k"].scaled(n_tokens=4000, batch=3, centres=256),
-         # p = 1/2: ~1500 level-2 nodes per unit, more than the descent keeps in shared memory
+         # p = 1/2: ~1500 level-2 nodes per unit
          "dense_levels": W["llama31_8b_16k"].scaled(n_tokens=6000, n_q_heads=8, n_kv_heads=2, promote_p=0.5),
          # p = 1/64: ~25 parents per unit, most units promote none again (the smallest-draw fallback)
          "sparse_levels": W["llama31_8b_16k"].scaled(n_tokens=1600, batch=2, n_q_heads=8, n_kv_heads=2,
@@ -519,10 +519,11 @@ def test_every_decode_plan_against_the_oracle(shape, budget, plan, attn):
 
 def test_three_levels_many_level2_nodes():
     """p = 1/2 on one 20,000-token unit: about 10,000 parents and 5,000
-    level-2 nodes, more than the descent keeps in shared memory (4,096), so
-    each head's level-2 scores go through the decode workspace.  Level 1,
-    level 2 and the descent selection (near-ties enumerated) against the
-    oracle, and the attention over the selected pages."""
+    level-2 nodes, more than the descent keeps in shared memory (about 2,700
+    per head at g = 4), so the level-2 scores go through the decode
+    workspace.  Level 1, level 2 and the descent selection (near-ties
+    enumerated) against the oracle, and the attention over the selected
+    pages."""
     w = W["llama31_8b_16k"].scaled(n_tokens=20000, n_q_heads=4, n_kv_heads=1, promote_p=0.5)
     run = DeviceRun(w, n_levels=3)
     assert run.status == ice.ICE_OK
@@ -535,3 +536,26 @@ def test_three_levels_many_level2_nodes():
             Q, buf, st = run.decode(bgt, fused=fused)
             assert st == ice.ICE_OK
             check_decode_descent(run, 0, Q, bgt, buf, lv2, idx)
+
+
+def test_three_levels_many_candidates_per_head():
+    """p = 1/64 on one 65,536-token unit with 16 query heads per KV head:
+    about 1,000 parents under some 20 level-2 nodes.  At a budget of 512
+    tokens (k = 32) each head takes every level-2 node, so its candidates (all
+    parents) outgrow the keys the descent keeps in shared memory per head
+    (about 630 at g = 16) and go through the decode workspace; at 64 tokens
+    they fit.  Level 1, level 2, the descent selection (near-ties enumerated)
+    and the attention against the oracle."""
+    w = W["llama31_8b_16k"].scaled(n_tokens=65536, n_q_heads=16, n_kv_heads=1, promote_p=1.0 / 64)
+    run = DeviceRun(w, n_levels=3)
+    assert run.status == ice.ICE_OK
+    idx = check_build_positional(run, 0)
+    lv2 = check_build_level2(run, 0, idx)
+    starts = np.asarray(lv2["child_start"])
+    # at k = 32 pages every head takes all level-2 nodes: all parents are its candidates
+    assert len(starts) - 1 <= 32 and int(starts[-1]) > 640
+    assert ice.ice_decode_plan(run.params, 512, ice.max_selected(run.cfg, 512))[0] == ice.ICE_PLAN_DESCENT
+    for bgt in (64, 512):
+        Q, buf, st = run.decode(bgt, fused=True)
+        assert st == ice.ICE_OK
+        check_decode_descent(run, 0, Q, bgt, buf, lv2, idx)
