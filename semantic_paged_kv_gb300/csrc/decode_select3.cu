@@ -14,7 +14,7 @@
 //      over the block (R rows a slot, padded so that the rows read without
 //      bank conflicts; the row ids loaded beforehand) and scored against
 //      every head's query: mma.sync m16n8k16 with the queries as A and 8
-//      staged rows as B (bf16, g <= 16), else on the CUDA cores -> the
+//      staged rows as B (bf16), on the CUDA cores for fp32 -> the
 //      level-2 scores [g][n2] (shared memory, or the decode workspace);
 //   2. warp per head: its best kc = min(k, n2) level-2 nodes in (-q.p, i)
 //      order (the kc-th largest score by a radix search, the keys reaching
@@ -246,8 +246,8 @@ __device__ __forceinline__ void score_rows_mma(const uint32_t (&qa)[8][4], const
     }
 }
 
-// The same on the CUDA cores (fp32 rows, or more than 16 heads): TPR threads
-// share a row; heads(j) gives the row's heads [lo, hi).
+// The same on the CUDA cores (fp32 rows): TPR threads share a row; heads(j)
+// gives the row's heads [lo, hi).
 template <typename T, int NT, typename Heads, typename Out>
 __device__ __forceinline__ void score_rows_simt(const float *s_q, const unsigned char *base, int rows, Heads heads,
                                                 Out out) {
@@ -285,7 +285,7 @@ __device__ __forceinline__ void score_rows_simt(const float *s_q, const unsigned
 }
 
 // One CTA per unit, NW warps.  HR: query rows of the tensor-core scoring
-// (1: g <= 8, 2: g <= 16; bf16), 0: scoring on the CUDA cores.  cap2 / capc:
+// (1: g <= 8, 2: g <= 16; bf16), 0: scoring on the CUDA cores (fp32).  cap2 / capc:
 // level-2 scores and candidate keys kept in shared memory per head; larger
 // tables go through ws_scores.
 template <typename T, int NW, int HR>
@@ -582,11 +582,10 @@ cudaError_t launch_t(const ice_params &p, const ice_index &idx, const void *Q, c
 cudaError_t launch_select3(const ice_params &p, const ice_index &idx, const void *Q, const DecodeWs &ws,
                            int32_t *sel_pages, int32_t *sel_count, int max_sel, int32_t *err, cudaStream_t s) {
     const int g = p.n_q_heads / p.n_kv_heads;
-    if (p.dtype == ICE_BF16) {
-        if (g <= 8) return launch_t<__nv_bfloat16, 8, 1>(p, idx, Q, ws, sel_pages, sel_count, max_sel, err, s);
-        if (g <= 16) return launch_t<__nv_bfloat16, 8, 2>(p, idx, Q, ws, sel_pages, sel_count, max_sel, err, s);
-        return launch_t<__nv_bfloat16, 16, 0>(p, idx, Q, ws, sel_pages, sel_count, max_sel, err, s);
-    }
+    // g <= 16 (ice_params)
+    if (p.dtype == ICE_BF16)
+        return g <= 8 ? launch_t<__nv_bfloat16, 8, 1>(p, idx, Q, ws, sel_pages, sel_count, max_sel, err, s)
+                      : launch_t<__nv_bfloat16, 8, 2>(p, idx, Q, ws, sel_pages, sel_count, max_sel, err, s);
     return g <= 8 ? launch_t<float, 8, 0>(p, idx, Q, ws, sel_pages, sel_count, max_sel, err, s)
                   : launch_t<float, 16, 0>(p, idx, Q, ws, sel_pages, sel_count, max_sel, err, s);
 }

@@ -424,7 +424,7 @@ def test_insert_rejected_with_positional_pages():
 
 @pytest.mark.parametrize("shape,n_sink,n_window", [("llama_bf16", 0, 0), ("tiny_fp32", 0, 0), ("many_units", 0, 0),
                                                    ("llama_bf16", 32, 96), ("dense_levels", 0, 0),
-                                                   ("sparse_levels", 0, 0)])
+                                                   ("sparse_levels", 0, 0), ("wide_group_fp32", 0, 0)])
 def test_three_levels_build_and_descent(shape, n_sink, n_window):
     """n_levels = 3, every unit: level 1 as in the two-level build; level-2
     promotion exact, level-2 parents tie-aware and children exact against
@@ -439,7 +439,9 @@ def test_three_levels_build_and_descent(shape, n_sink, n_window):
          "dense_levels": W["llama31_8b_16k"].scaled(n_tokens=6000, n_q_heads=8, n_kv_heads=2, promote_p=0.5),
          # p = 1/64: ~25 parents per unit, most units promote none again (the smallest-draw fallback)
          "sparse_levels": W["llama31_8b_16k"].scaled(n_tokens=1600, batch=2, n_q_heads=8, n_kv_heads=2,
-                                                     promote_p=1.0 / 64)}[shape]
+                                                     promote_p=1.0 / 64),
+         # fp32 with 12 query heads a group: the descent's 16-warp CTA, CUDA-core scoring of fp32 rows
+         "wide_group_fp32": W["tiny"].scaled(n_tokens=3000, n_q_heads=12, n_kv_heads=1)}[shape]
     run = DeviceRun(w, n_levels=3, n_sink=n_sink, n_window=n_window)
     assert run.status == ice.ICE_OK
     idxs, lv2s = {}, {}
