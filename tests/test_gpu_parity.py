@@ -86,17 +86,20 @@ def test_fused_decode_equals_separate_calls():
     assert torch.max(torch.abs(a.O - b.O)).item() <= 1e-5
 
 
-@pytest.mark.parametrize("shape", ["tiny_fp32", "llama_cluster", "qwen_many_units", "longchat_many_units"])
+@pytest.mark.parametrize("shape", ["tiny_fp32", "llama_cluster", "qwen_many_units", "longchat_many_units",
+                                   "qwen_one_cta_per_unit"])
 def test_decode_without_contiguous_buffer(shape):
     """ice_decode_step with kbuf = vbuf = buf_len = NULL gathers the pages on
     chip only: same page lists and bit-identical O as with the buffer, on
     each kernel path (fp32 and bf16 per-unit clusters, the tensor-core score
-    table with the selecting MMA attention for many units)."""
+    table with the selecting MMA attention for many units, and for one CTA per
+    unit)."""
     w = {"tiny_fp32": W["tiny"],
          "llama_cluster": W["llama31_8b_16k"].scaled(n_tokens=3000, n_q_heads=8, n_kv_heads=2),
          "qwen_many_units": W["qwen3_32b_100k"].scaled(n_tokens=3000, batch=3, centres=256),
          "longchat_many_units": W["longchat_7b_100k"].scaled(n_tokens=2500, batch=1, n_q_heads=24, n_kv_heads=24,
-                                                             centres=256)}[shape]
+                                                             centres=256),
+         "qwen_one_cta_per_unit": W["qwen3_32b_100k"].scaled(n_tokens=2200, batch=20, centres=128)}[shape]
     run = DeviceRun(w)
     assert run.status == ice.ICE_OK
     for bgt in (64, 256):
@@ -105,8 +108,8 @@ def test_decode_without_contiguous_buffer(shape):
         assert st_a == ice.ICE_OK and st_b == ice.ICE_OK
         assert torch.equal(a.sel_count, b.sel_count)
         assert torch.equal(a.sel_pages, b.sel_pages)
-        assert torch.equal(a.O, b.O)
         assert torch.all(b.buf_len == 0)  # untouched
+        assert torch.equal(a.O, b.O)
         check_decode_unit(run, run.cfg.units - 1, Q, bgt, a)
 
 
