@@ -71,9 +71,9 @@ def graph_kernel_nodes(graph):
 # The decode step's entry: the two kernels of ICE_PLAN_SCORE_SELECT captured at batch 4 (32 units) and scaled by the
 # units to the 16-sequence batch (per-unit traffic does not depend on the batch).
 TRAFFIC = {
-    "decode": {"workload": "qwen3_32b_100k", "bytes": 354_127_872, "sha256": {
+    "decode": {"workload": "qwen3_32b_100k", "bytes": 354_381_824, "sha256": {
         "decode_select_tc.cu": "e1bb3c659f0a7ca618e4e526d2725e7008a7810019a25cc7f8f535f55bfebc75",
-        "decode_attn_mma.cu": "adaf3b86ba0647e99d7664b24e7e609cd3ab60f41722da3e7f3a5780c6ba3b4c",
+        "decode_attn_mma.cu": "116f2293b02f8bb342959191b40588d25efecaecdb78946e473417cbc5b66442",
         "select_unit.cuh": "e9fb950a3869e70bb5b99941bbe3a5caa9f6d8414d43b7dc983ecc0ce5e5c767",
         "attn_page.cuh": "85d342159d9748393e05de4c7a6239fd0aff82ae1638b53295ee21aa72426620",
         "tc_common.cuh": "bcc9600b9d3aaad4c363c2b9ce954eb63042c1c048f1de44ffffcd2b99354924",

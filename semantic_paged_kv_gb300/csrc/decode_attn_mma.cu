@@ -339,8 +339,10 @@ cudaError_t launch_attention_mma_select(const ice_params &p, const ice_index &id
                                         const DecodeWs &ws, int32_t *err, cudaStream_t s) {
     const int U = units_of(p);
     const int g = p.n_q_heads / p.n_kv_heads;
+    // a unit is split over CTAs only while each keeps its slots full: every
+    // split CTA repeats the selection and the last one merges
     int splits = sm_count_cached() / U;
-    const int most = (max_sel + kMW - 1) / kMW;
+    const int most = (max_sel + kMW * kNS - 1) / (kMW * kNS);
     splits = splits < 1 ? 1 : (splits > most ? most : splits);
     const int per_warp = (ceil_div(max_sel, splits) + kMW - 1) / kMW;
     if (splits > ws.n_splits || per_warp > 32 || ((uintptr_t)Q & 3u) != 0) return cudaErrorNotSupported;
