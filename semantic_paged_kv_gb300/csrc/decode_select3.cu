@@ -44,6 +44,7 @@ using namespace topk;
 template <typename T> constexpr int stage_rows() { return sizeof(T) == 2 ? 128 : 64; }  // rows per ring slot
 template <typename T> constexpr int stage_stride() { return row_bytes<T>() + 16; }       // padded row
 constexpr int kSlots = 3;  // ring slots: two batches in flight while one is scored
+constexpr int kTopkSlack = 16;  // keys past the k-th that the warp top-k may rank
 
 // The largest index j in [0, n) with a[j] <= x (a non-decreasing, a[0] <= x).
 __device__ __forceinline__ int last_le(const int *a, int n, int x) {
@@ -102,34 +103,12 @@ __device__ void stream_rows(int n, unsigned char *ring, int &slot, RowOf row_of,
     slot = slot_of(nb);
 }
 
-// The kc-th largest (kc <= 32) of the warp's V values a lane (order-preserving
-// form, 0 = none; at least kc values present): bit by bit from the top, three
-// candidate prefixes a step, the largest c with at least kc values >= c.
-template <int V>
-__device__ __forceinline__ uint32_t kth_largest_v(const uint32_t (&v)[V], int kc) {
-    uint32_t r = 0u;
-    for (int bit = 30; bit >= 0; bit -= 2) {
-        const uint32_t c1 = r | (1u << bit), c2 = r | (2u << bit), c3 = r | (3u << bit);
-        unsigned a1 = 0, a2 = 0, a3 = 0;
-#pragma unroll
-        for (int e = 0; e < V; ++e) {
-            a1 += v[e] >= c1;
-            a2 += v[e] >= c2;
-            a3 += v[e] >= c3;
-        }
-        const int n3 = (int)__reduce_add_sync(0xffffffffu, a3);
-        const int n2 = (int)__reduce_add_sync(0xffffffffu, a2);
-        const int n1 = (int)__reduce_add_sync(0xffffffffu, a1);
-        r = n3 >= kc ? c3 : n2 >= kc ? c2 : n1 >= kc ? c1 : r;
-    }
-    return r;
-}
-
 // Lane r < kc (kc <= 32) receives the r-th largest of the n keys key_of(i),
-// i < n (distinct; 0 = none); n <= 32 V.  The kc-th largest high word (the
-// score) bounds the best kc from below: the keys reaching it (kc of them plus
-// ties, at most 64 used, else k rounds of a warp maximum) are ranked by
-// counting.  s_tmp: 64 keys of this warp's scratch.
+// i < n (distinct; 0 = none); n <= 32 V.  A bound on the high words (the
+// scores) that the best kc reach and at most kc + kTopkSlack keys reach unless
+// ties force more (kth_bound_ord: a radix search that stops as soon as the
+// count is that small) selects the keys that are ranked by counting (at most
+// 64, else k rounds of a warp maximum).  s_tmp: 64 keys of this warp's scratch.
 template <int V, typename KeyOf>
 __device__ unsigned long long warp_topk(int n, int kc, KeyOf key_of, unsigned long long *s_tmp) {
     const int lane = threadIdx.x & 31;
@@ -141,7 +120,7 @@ __device__ unsigned long long warp_topk(int n, int kc, KeyOf key_of, unsigned lo
         k[e] = i < n ? key_of(i) : 0ull;
         v[e] = (uint32_t)(k[e] >> 32);
     }
-    const uint32_t t = kc < n ? kth_largest_v<V>(v, kc) : 1u;
+    const uint32_t t = kc < n ? kth_bound_ord<V>(v, kc, kTopkSlack) : 1u;
     unsigned pass = 0u;
 #pragma unroll
     for (int e = 0; e < V; ++e) pass |= (k[e] != 0ull && v[e] >= t ? 1u : 0u) << e;
@@ -582,12 +561,11 @@ cudaError_t launch_t(const ice_params &p, const ice_index &idx, const void *Q, c
 cudaError_t launch_select3(const ice_params &p, const ice_index &idx, const void *Q, const DecodeWs &ws,
                            int32_t *sel_pages, int32_t *sel_count, int max_sel, int32_t *err, cudaStream_t s) {
     const int g = p.n_q_heads / p.n_kv_heads;
-    // g <= 16 (ice_params)
+    // g <= 16 (ice_params); 16 warps: twice the row copies in flight of 8
     if (p.dtype == ICE_BF16)
-        return g <= 8 ? launch_t<__nv_bfloat16, 8, 1>(p, idx, Q, ws, sel_pages, sel_count, max_sel, err, s)
-                      : launch_t<__nv_bfloat16, 8, 2>(p, idx, Q, ws, sel_pages, sel_count, max_sel, err, s);
-    return g <= 8 ? launch_t<float, 8, 0>(p, idx, Q, ws, sel_pages, sel_count, max_sel, err, s)
-                  : launch_t<float, 16, 0>(p, idx, Q, ws, sel_pages, sel_count, max_sel, err, s);
+        return g <= 8 ? launch_t<__nv_bfloat16, 16, 1>(p, idx, Q, ws, sel_pages, sel_count, max_sel, err, s)
+                      : launch_t<__nv_bfloat16, 16, 2>(p, idx, Q, ws, sel_pages, sel_count, max_sel, err, s);
+    return launch_t<float, 16, 0>(p, idx, Q, ws, sel_pages, sel_count, max_sel, err, s);
 }
 
 }  // namespace ice

@@ -53,7 +53,7 @@ __device__ __forceinline__ uint32_t kth_largest_ord(const uint32_t (&v)[8], int 
 }
 
 // A threshold T (order-preserving form) that at least kc of the warp's values
-// (8 per lane, 0 = none; kc <= 32 and at least kc values present) reach, and
+// (V per lane, 0 = none; kc <= 32 and at least kc values present) reach, and
 // at most kc + slack unless ties force more; T is itself one of the values.
 // The kc-th largest lies between lo, the smallest of the lanes' maxima (kc or
 // more values reach it), and the maximum hi, so the bits above their first
@@ -61,10 +61,11 @@ __device__ __forceinline__ uint32_t kth_largest_ord(const uint32_t (&v)[8], int 
 // the top (three counts per step), and the search stops once at most
 // kc + slack values reach the prefix.  T is then the least value at or above
 // the prefix.
-__device__ __forceinline__ uint32_t kth_bound_ord(const uint32_t (&v)[8], int kc, int slack) {
+template <int V>
+__device__ __forceinline__ uint32_t kth_bound_ord(const uint32_t (&v)[V], int kc, int slack) {
     uint32_t lm = 0u;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) lm = max(lm, v[e]);
+    for (int e = 0; e < V; ++e) lm = max(lm, v[e]);
     const uint32_t hi = __reduce_max_sync(0xffffffffu, lm);
     const uint32_t lo = __reduce_min_sync(0xffffffffu, lm != 0u ? lm : 0xFFFFFFFFu);
     int nb = lo >= hi ? 0 : 32 - __clz(lo ^ hi);  // open low bits
@@ -76,7 +77,7 @@ __device__ __forceinline__ uint32_t kth_bound_ord(const uint32_t (&v)[8], int kc
             const uint32_t c1 = r | (1u << b), c2 = r | (2u << b), c3 = r | (3u << b);
             unsigned a1 = 0, a2 = 0, a3 = 0;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
+            for (int e = 0; e < V; ++e) {
                 a1 += v[e] >= c1;
                 a2 += v[e] >= c2;
                 a3 += v[e] >= c3;
@@ -99,7 +100,7 @@ __device__ __forceinline__ uint32_t kth_bound_ord(const uint32_t (&v)[8], int kc
             const uint32_t c1 = r | 1u;
             unsigned a1 = 0;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) a1 += v[e] >= c1;
+            for (int e = 0; e < V; ++e) a1 += v[e] >= c1;
             const int n1 = (int)__reduce_add_sync(0xffffffffu, a1);
             if (n1 >= kc) r = c1;
             nb = 0;
@@ -107,7 +108,7 @@ __device__ __forceinline__ uint32_t kth_bound_ord(const uint32_t (&v)[8], int kc
     }
     uint32_t mn = 0xFFFFFFFFu;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) mn = v[e] >= r && v[e] != 0u ? min(mn, v[e]) : mn;
+    for (int e = 0; e < V; ++e) mn = v[e] >= r && v[e] != 0u ? min(mn, v[e]) : mn;
     return __reduce_min_sync(0xffffffffu, mn);
 }
 
