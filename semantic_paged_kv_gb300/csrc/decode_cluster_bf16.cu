@@ -12,9 +12,11 @@
 //            row (one 16-byte load each), the lane's q slices of the GT heads
 //            in registers (packed fp32-pair FMAs), the 16 partial sums folded
 //            by recursive halving.  Per head (one warp each) the slice's best
-//            kc keys (score, -m): the kc-th largest score T by bisection on
-//            its order-preserving integer form (ballot counts), the keys with
-//            score >= T collected and sorted by a bitonic network; the page
+//            kc keys (score, -m): a bound T on the scores that the best kc
+//            reach and at most 64 keys reach (a radix search on their
+//            order-preserving integer form that stops as soon as the count is
+//            that small), the keys with score >= T collected and sorted by a
+//            bitonic network; the page
 //            spans of the slice's parents stay in shared memory.
 //                                                            -- cluster barrier
 //   phase 2  the leader merges the 8 sorted lists of each head pairwise
@@ -230,11 +232,18 @@ __global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(kT, 1) k_decode_clu
         uint32_t tbits = 0u;  // order-preserving form of T
         if (nvalid >= kc) {
             uint32_t res = 0u;
-            if (nvalid <= 8 * 32) {  // the lane's values in registers, counts summed by one reduction per bit
+            // the lane's values in registers; a bound that the best kc reach and
+            // at most kCand keys reach unless ties force more
+            if (nvalid <= 8 * 32) {
                 uint32_t vo[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) vo[e] = e * 32 + lane < nvalid ? ord_f32(sc[e * 32 + lane]) : 0u;
-                res = kth_largest_ord(vo, kc);
+                res = kth_bound_ord(vo, kc, kCand - kc);
+            } else if (nvalid <= 16 * 32) {
+                uint32_t vo[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) vo[e] = e * 32 + lane < nvalid ? ord_f32(sc[e * 32 + lane]) : 0u;
+                res = kth_bound_ord(vo, kc, kCand - kc);
             } else {
                 for (int bit = 31; bit >= 0; --bit) {
                     const uint32_t cnd = res | (1u << bit);

@@ -27,31 +27,6 @@ __device__ __forceinline__ int key_id(unsigned long long k) { return (int)(0xFFF
 __device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) { return a > b ? a : b; }
 __device__ __forceinline__ unsigned long long umin64(unsigned long long a, unsigned long long b) { return a < b ? a : b; }
 
-// The kc-th largest of the warp's values (8 per lane, order-preserving
-// integer form, 0 = none), found bit by bit from the top: the largest c with
-// at least kc values >= c.  Stops early once exactly kc values reach the
-// prefix: the answer is then their minimum.
-__device__ __forceinline__ uint32_t kth_largest_ord(const uint32_t (&v)[8], int kc) {
-    uint32_t r = 0u;
-    for (int bit = 31; bit >= 0; --bit) {
-        const uint32_t c = r | (1u << bit);
-        unsigned cnt = 0;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) cnt += v[e] >= c;
-        const int n = (int)__reduce_add_sync(0xffffffffu, cnt);
-        if (n >= kc) {
-            r = c;
-            if (n == kc) {
-                uint32_t mn = 0xFFFFFFFFu;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) mn = v[e] >= c ? min(mn, v[e]) : mn;
-                return __reduce_min_sync(0xffffffffu, mn);
-            }
-        }
-    }
-    return r;
-}
-
 // A threshold T (order-preserving form) that at least kc of the warp's values
 // (V per lane, 0 = none; kc <= 32 and at least kc values present) reach, and
 // at most kc + slack unless ties force more; T is itself one of the values.
