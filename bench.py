@@ -485,11 +485,53 @@ def r3(x):
 
 
 # ------------------------------------------------------------ extra parts --
+def steady_decode(ice, pk, w, budget: int, n_layers: int, steps: int = 2000) -> dict:
+    """Decode steps timed the way the contract line times them: n_layers
+    layers with distinct K/V, index and queries (together well above L2, so
+    that a layer's data has left L2 by its next step), one decode workspace
+    and one set of outputs, one CUDA graph per pass over the layers, the
+    passes back to back; HBM GB/s on the minimum bytes against the measured
+    copy peak."""
+    import torch
+    layers = []
+    for layer in range(n_layers):
+        layers.append(build_layer(ice, w, layer=layer))
+        torch.cuda.empty_cache()
+    buf = ice.DecodeBuffers(layers[0]["cfg"], budget)
+    for L in layers:
+        decode_call(ice, L, budget, buf, False)()
+        torch.cuda.synchronize()
+        L["bytes"] = decode_bytes(L, buf, w)[0]
+    g_all = Replay(1).graph(lambda: [decode_call(ice, L, budget, buf, False)() for L in layers])
+    passes = max(1, steps // n_layers)
+    for _ in range(3):
+        g_all.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(passes):
+        g_all.replay()
+    b.record()
+    torch.cuda.synchronize()
+    us = 1000.0 * a.elapsed_time(b) / (passes * n_layers)
+    bmin = float(np.mean([L["bytes"] for L in layers]))
+    st = [ice.ice_check(L["err"]) for L in layers]
+    out = {"us": r3(us), "frac": r3(bmin / (us * 1e-6) / 1e9 / pk["hbm"]), "MB": r3(bmin / 1e6), "layers": n_layers,
+           "steps": passes * n_layers}
+    if any(x != ice.ICE_OK for x in st):
+        out["status"] = ice.ice_status_string(max(st))
+    del layers, buf, g_all
+    torch.cuda.empty_cache()
+    return out
+
+
 def extra_longchat(ice, pk, rp, batch: int):
     """LongChat-7B shape (32/32 heads, MHA, 100k tokens, log-normal key
     norms): at batch 1 the parent-assignment contraction at 100k (tensor
     peak fraction) and the decode step at budgets 64 and 256; at batch 8 the
-    decode step at 256."""
+    decode step at 256.  Each decode step once after an L2 flush, and at 256
+    also steadily as the contract line runs (6 layers at batch 1, about 55 MB
+    of minimum bytes each; 2 at batch 8, about 443 MB each)."""
     import torch
     w = workloads.WORKLOADS["longchat_7b_100k"].scaled(batch=batch)
     L = build_layer(ice, w, keep_kv=batch == 1)
@@ -514,6 +556,7 @@ def extra_longchat(ice, pk, rp, batch: int):
     torch.cuda.empty_cache()
     if st != ice.ICE_OK:
         out["status"] = ice.ice_status_string(st)
+    out["steady256"] = steady_decode(ice, pk, w, 256, 6 if batch == 1 else 2)
     return out
 
 
@@ -944,6 +987,8 @@ def compact(d: dict) -> dict:
                 "lc1": [g("longchat", "d256", "us"), g("longchat", "d256", "frac"), g("longchat", "d64", "us")],
                 "lc_assign_frac": g("longchat", "assign", "frac"),
                 "lc8": [g("longchat_b8", "d256", "us"), g("longchat_b8", "d256", "frac")],
+                "lc_steady": [g("longchat", "steady256", "us"), g("longchat", "steady256", "frac"),
+                              g("longchat_b8", "steady256", "us"), g("longchat_b8", "steady256", "frac")],
                 "lv3_us": g("qwen_levels3", "us"), "ins_us": g("mistral_insert", "insert_us"),
                 "sep": [g("separate", "gather_us"), g("separate", "gather_frac"), g("separate", "attn_us"),
                         g("separate", "attn_frac")],
