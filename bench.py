@@ -485,7 +485,7 @@ def r3(x):
 
 
 # ------------------------------------------------------------ extra parts --
-def steady_decode(ice, pk, w, budget: int, n_layers: int, steps: int = 2000) -> dict:
+def steady_decode(ice, pk, rp, w, budget: int, n_layers: int, steps: int = 2000) -> dict:
     """Decode steps timed the way the contract line times them: n_layers
     layers with distinct K/V, index and queries (together well above L2, so
     that a layer's data has left L2 by its next step), one decode workspace
@@ -502,7 +502,7 @@ def steady_decode(ice, pk, w, budget: int, n_layers: int, steps: int = 2000) -> 
         decode_call(ice, L, budget, buf, False)()
         torch.cuda.synchronize()
         L["bytes"] = decode_bytes(L, buf, w)[0]
-    g_all = Replay(1).graph(lambda: [decode_call(ice, L, budget, buf, False)() for L in layers])
+    g_all = rp.graph(lambda: [decode_call(ice, L, budget, buf, False)() for L in layers])
     passes = max(1, steps // n_layers)
     for _ in range(3):
         g_all.replay()
@@ -556,7 +556,7 @@ def extra_longchat(ice, pk, rp, batch: int):
     torch.cuda.empty_cache()
     if st != ice.ICE_OK:
         out["status"] = ice.ice_status_string(st)
-    out["steady256"] = steady_decode(ice, pk, w, 256, 6 if batch == 1 else 2)
+    out["steady256"] = steady_decode(ice, pk, rp, w, 256, 6 if batch == 1 else 2)
     return out
 
 
