@@ -318,7 +318,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(w, budget, args.gpus, 1),
+        "config": compact_config(config_of(w, budget, args.gpus, args.layers)),  # the GPU arm's config
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": smp.threads, "kind": "oracle",
                          "sample": smp.describe(len(times), total), "cpu": host_cpu()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -950,6 +950,15 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def compact_config(c: dict) -> dict:
+    """The workload config of the contract line in short form (both arms print it)."""
+    return {"workload": c["workload"], "batch_per_gpu": c["batch_per_gpu"],
+            "heads": f"{c['n_q_heads']}/{c['n_kv_heads']}", "n_tokens": c["n_tokens"],
+            "budget_tokens": c["budget_tokens"], "levels": 2, "parallelism": c["parallelism"],
+            "gather": "smem", "l2": c["l2"].split(" (")[0] + ", > 2.5x L2 per step",
+            "graph": "one per pass over the layers", "workspace": "shared by the layers"}
+
+
 def compact(d: dict) -> dict:
     """The contract line with every headline number and short keys (the
     full record goes to stderr and --detail)."""
@@ -960,11 +969,7 @@ def compact(d: dict) -> dict:
                              "higher_is_better", "scaling", "vs_baseline", "dtype")}
     out["value"] = r3(d["value"])
     out["data"] = "synthetic"
-    out["config"] = {"workload": c["workload"], "batch_per_gpu": c["batch_per_gpu"],
-                     "heads": f"{c['n_q_heads']}/{c['n_kv_heads']}", "n_tokens": c["n_tokens"],
-                     "budget_tokens": c["budget_tokens"], "levels": 2, "parallelism": c["parallelism"],
-                     "gather": "smem", "l2": c["l2"].split(" (")[0] + ", > 2.5x L2 per step",
-                     "graph": "one per pass over the layers", "workspace": "shared by the layers"}
+    out["config"] = compact_config(c)
     out["decode_step_us"] = r3(d["decode_step_us"])
     rf = d["roofline"]
     out["roofline"] = {"kernel": rf["kernel"], "bound": "hbm", "achieved": r3(rf["achieved"]), "peak": rf["peak"],
