@@ -31,7 +31,11 @@
 //   warps 2..17 epilogue: warp w reads TMEM lane quarter w % 4 and the 64
 //               columns (w - 2) / 4 of each tile in one tcgen05 wait, frees
 //               the accumulator at once and then keeps a running argmax with
-//               the lowest index on exact ties; the four column quarters of a
+//               the lowest index on exact ties (the tile maximum by a tree of
+//               three-input maxima; a lane whose maximum moved finds its
+//               column inside the lowest nine-column group of the tree that
+//               holds it when at most 4 lanes of the warp moved, else over
+//               all 64); the four column quarters of a
 //               row combine through shared memory at the end of the item.
 //               The next item's promoted flags are prefetched.
 // Every mbarrier wait gives up after ~2 s (globaltimer) and records
@@ -73,6 +77,16 @@ struct Bars {
     uint32_t tmem_base;
 };
 static_assert(kEpiCols == 64, "the epilogue's maximum tree is written for 64 columns");
+
+// The lowest index i in [B, B + 9) with v[i] == x (B + 8 if none; the caller
+// knows one is there).  The indices are compile-time, so v stays in registers.
+template <int B>
+__device__ __forceinline__ int lowest9(const float (&v)[64], float x) {
+    int f = B + 8;
+#pragma unroll
+    for (int j = 7; j >= 0; --j) f = v[B + j] == x ? B + j : f;
+    return f;
+}
 
 // max(a, b, c) in one instruction (no NaN reaches it: scores are finite or -inf).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -251,6 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&bars->tempty[b]);
                 if (valid > 0) {
                     float cmax = -INFINITY;
+                    int gk = -1;  // full tiles: the lowest nine-column group holding cmax (7: column 63)
                     if (valid >= kEpiCols) {
                         // three-input maxima: 64 -> 22 -> 8 -> 3 -> 1
                         float m1[22], m2[8];
@@ -261,6 +276,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int i = 0; i < 7; ++i) m2[i] = fmax3(m1[3 * i], m1[3 * i + 1], m1[3 * i + 2]);
                         m2[7] = m1[21];
                         cmax = fmax3(fmax3(m2[0], m2[1], m2[2]), fmax3(m2[3], m2[4], m2[5]), fmaxf(m2[6], m2[7]));
+                        gk = 7;
+#pragma unroll
+                        for (int i = 6; i >= 0; --i) gk = m2[i] == cmax ? i : gk;
                     } else {
 #pragma unroll
                         for (int i = 0; i < kEpiCols; ++i) {
@@ -268,11 +286,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                             cmax = fmaxf(cmax, v[i]);
                         }
                     }
-                    if (cmax > best) {  // columns ascend, so only a strictly larger score moves the argmax
-                        int first = 0;
+                    // the lanes whose maximum moves search their columns: through the
+                    // group that holds cmax when few lanes do (each distinct group
+                    // is a branch of the warp), over every column otherwise
+                    const bool moved = cmax > best;
+                    if (__popc(__ballot_sync(0xffffffffu, moved)) > 4) gk = -1;
+                    if (moved) {  // columns ascend, so only a strictly larger score moves the argmax
+                        int first = 63;
+                        switch (gk) {
+                        case 0: first = lowest9<0>(v, cmax); break;
+                        case 1: first = lowest9<9>(v, cmax); break;
+                        case 2: first = lowest9<18>(v, cmax); break;
+                        case 3: first = lowest9<27>(v, cmax); break;
+                        case 4: first = lowest9<36>(v, cmax); break;
+                        case 5: first = lowest9<45>(v, cmax); break;
+                        case 6: first = lowest9<54>(v, cmax); break;
+                        case 7: first = 63; break;
+                        default:  // many lanes, or a partial tile: every column
 #pragma unroll
-                        for (int i = kEpiCols - 1; i >= 0; --i)
-                            if (v[i] == cmax) first = i;
+                            for (int i = kEpiCols - 1; i >= 0; --i)
+                                if (v[i] == cmax) first = i;
+                        }
                         best = cmax;
                         bidx = c_lo + first;
                     }
