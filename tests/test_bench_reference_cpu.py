@@ -23,3 +23,8 @@ def test_reference_arm_prints_one_contract_line():
     assert "logical CPUs" in d["cpu_baseline"]["cpu"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
     assert d["config"]["workload"] == "llama31_8b_16k" and d["unit"] == "GB/s"
+    # the GPU arm's compact config, key for key (the same workload, layers and timing method named)
+    assert set(d["config"]) == {"workload", "batch_per_gpu", "heads", "n_tokens", "budget_tokens", "levels",
+                                "parallelism", "gather", "l2", "graph", "workspace"}
+    assert d["config"]["heads"] == "32/8" and d["config"]["parallelism"] == "dp1"
+    assert d["config"]["l2"].startswith("2 layers rotated")
